@@ -1,0 +1,378 @@
+"""Benchmark of the KDA forward on GB300 (one JSON line on rank 0).
+
+Step = one chunked KDA forward (gate + cumsum, causal scores, triangular solve,
+WY terms, state scan, output) over the dense bf16 workload B=4, T=4096, H=64,
+K=V=128, C=64 (safe gate, lower_bound -5), inputs resident in HBM.  The
+workload's inputs (1.34 GB) are larger than L2, so consecutive steps re-read
+them from HBM.  A decode measurement (512 one-token sequences, H=32,
+K=V=128, FP32 states updated in place) is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own
+GPU (independent batches, no collective on the data path: weak scaling); the
+timed region is bracketed by barriers, the time is the max over ranks and the
+value counts the head-tokens of all ranks.  ``--impl reference`` times the
+float64 CPU oracle (the reference arm of this build) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd tokens/s (B*T*H) and TFLOP/s, % of GB300 roofline; decode steps/s"
+WORKLOAD = "dense_bf16_b4_t4096_h64_d128"
+UNIT = "head-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic_flops_per_head_token(K, V, C):
+    """6KV + 2K(C+16) + CK + CV + (C+1)V + C^2/3: state read-outs and updates, causal
+    scores on 16-row sub-blocks, WY terms, output (lower-triangular counts)."""
+    return 6 * K * V + 2 * K * (C + 16) + C * K + C * V + (C + 1) * V + C * C / 3.0
+
+
+def algorithmic_bytes_per_head_token(K, V, in_bytes=2, g_bytes=2):
+    """q, k, g (K each), v (V), beta in; o (V) out."""
+    return in_bytes * (2 * K + V) + g_bytes * K + in_bytes + in_bytes * V
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples in a background process."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        rows = self.samples
+        if self.window:
+            inside = [r for r in rows if self.window[0] - 0.05 <= r[0] <= self.window[1] + 0.05]
+            if inside:
+                rows = inside
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for _, f in rows:
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds, local_units, world, device=None):
+    """Max time and summed work over ranks (identity at world size 1)."""
+    if world == 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def oracle_sample(w, n_units, nthreads, seed=0):
+    """Time the float64 oracle on n_units (sequence, head) units of workload w.
+    Returns (head-tokens, wall seconds)."""
+    import numpy as np
+
+    import oracle
+
+    r = np.random.default_rng(seed)
+    units = [(int(r.integers(w.B)), int(r.integers(w.H))) for _ in range(n_units)]
+    # slice the sampled units out first so the conversion to float64 stays small
+    heads = sorted({h for _, h in units})
+    rows = sorted({b for b, _ in units})
+    pick = {name: getattr(w, name)[rows][:, :, heads].cpu() for name in ("q", "k", "v", "g", "beta")}
+    local = [(rows.index(b), heads.index(h)) for b, h in units]
+    al = w.A_log[heads].cpu() if w.A_log is not None else None
+    db = w.dt_bias[heads].cpu() if w.dt_bias is not None else None
+    t0 = time.perf_counter()
+    oracle.forward(pick["q"], pick["k"], pick["v"], pick["g"], pick["beta"], al, db, w.mode,
+                   w.lower_bound, None, None, units=local, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return n_units * w.T, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from chunked_kda_gb300 import workloads
+
+    oracle.build()
+    w = workloads.make(WORKLOAD, device="cuda" if torch.cuda.is_available() else "cpu")
+    cores = host_cores()
+    n_units = cores  # one (sequence, head) unit per core per step
+    for _ in range(args.warmup):
+        oracle_sample(w, max(1, cores // 4), cores, seed=99)
+    tot_tokens, tot_s = 0, 0.0
+    for s in range(args.steps):
+        tok, dt = oracle_sample(w, n_units, cores, seed=s)
+        tot_tokens += tok  # head-tokens: each unit is one head of one sequence
+        tot_s += dt
+    value = tot_tokens / tot_s
+    sample = f"{n_units} random (sequence, head) units of {WORKLOAD} per step ({w.T} tokens each)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "B": 4, "T": 4096, "H": 64, "K": 128,
+                                        "V": 128, "chunk_size": 64, "sampled": True},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import chunked_kda_gb300 as kda
+    from chunked_kda_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    kda.load_library()
+    peaks, peak_src = load_peaks()
+
+    w = workloads.make(WORKLOAD, device=dev)
+    B, T, H, K, V, C = w.B, w.T, w.H, w.K, w.V, w.chunk_size
+    stream = torch.cuda.current_stream()
+    o = torch.empty((B, T, H, V), device=dev, dtype=torch.bfloat16)
+    ws_bytes = kda.kda_chunk_workspace_bytes(torch.bfloat16, B, T, H, K, V, C, 0)
+    ws = torch.empty(max(ws_bytes, 1), device=dev, dtype=torch.uint8)
+
+    def step():
+        kda.kda_chunk_fwd(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, w.mode, w.lower_bound,
+                          None, False, None, C, o=o, workspace=ws)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    sampler.mark(wall0, wall1)
+    local_s = ev0.elapsed_time(ev1) / 1e3
+    head_tokens = B * T * H
+    t_max, units_all = aggregate(local_s, head_tokens * args.steps, world, dev)
+    ms_per_step = 1e3 * t_max / args.steps
+
+    # end to end through the public API: pinned host inputs -> device, forward, o -> host
+    names = ("q", "k", "v", "g", "beta")
+    host = {n: getattr(w, n).cpu().pin_memory() for n in names}
+    dbuf = {n: torch.empty_like(getattr(w, n)) for n in names}
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def e2e_step():
+        for n in names:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        kda.kda_chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], w.A_log,
+                          w.dt_bias, w.mode, w.lower_bound, None, False, None, C, o=o,
+                          workspace=ws)
+        o_host.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0, world, dev)
+    e2e_value = world * head_tokens * e2e_steps / e2e_s
+    del host, dbuf
+
+    # decode: 512 packed one-token sequences, H=32, K=V=128, FP32 states in place
+    n_dec, Hd = 512, 32
+    S = workloads.decode_state(n_dec, Hd, device=dev)
+    cu = workloads.decode_cu_seqlens(n_dec, device=dev)
+    pool = [workloads.decode_step(i, n_dec, Hd, device=dev) for i in range(4)]
+    od = torch.empty((1, n_dec, Hd, 128), device=dev, dtype=torch.bfloat16)
+
+    def dstep(i):
+        p = pool[i % len(pool)]
+        kda.kda_recurrent_fwd(p.q, p.k, p.v, p.gate, p.beta, S, True, cu, o=od, final_state=S)
+
+    for i in range(3):
+        dstep(i)
+    torch.cuda.synchronize()
+    d_steps = 64
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(d_steps):
+        dstep(i)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_s = d0.elapsed_time(d1) / 1e3 / d_steps
+    dec_bytes = 2 * S.numel() * 4 + n_dec * Hd * (3 * 128 * 2 + 128 * 4 + 2 + 128 * 2)
+    sampler.stop()
+
+    if rank != 0:
+        return
+    flops = algorithmic_flops_per_head_token(K, V, C) * head_tokens
+    nbytes = algorithmic_bytes_per_head_token(K, V) * head_tokens
+    t_step = ms_per_step / 1e3
+    achieved_gbs = nbytes / t_step / 1e9
+    value = units_all / t_max
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "K": K, "V": V, "chunk_size": C,
+                   "gate": "safe, lower_bound -5", "initial_state": None,
+                   "output_final_state": False, "l2": "inputs (1.34 GB) larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": flops / t_step / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peak_src,
+                     "kernel": "kda_chunk_fwd (all launches of one call)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * LAUNCHES_PER_CHUNK_CALL,
+        "decode": {"steps_per_s": 1.0 / dec_s, "ms_per_step": 1e3 * dec_s,
+                   "achieved_gbs": dec_bytes / dec_s / 1e9,
+                   "frac": dec_bytes / dec_s / 1e9 / peaks["hbm_gbs"],
+                   "workload": "512 one-token sequences, H=32, K=V=128, bf16, states in place"},
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        cores = host_cores()
+        tok, dt = oracle_sample(w, 2 * cores, cores, seed=1234)
+        line["cpu_baseline"] = {"value": tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{2 * cores} random (sequence, head) units of {WORKLOAD} "
+                                          f"({w.T} tokens each), float64, one OpenMP thread "
+                                          f"per unit"}
+    print(json.dumps(line), flush=True)
+
+
+# kernels one kda_chunk_fwd call launches: gate, scores, solve, w/u, scan, output
+LAUNCHES_PER_CHUNK_CALL = 6
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+// C ABI of libkda_gb300.so: host-side validation, workspace sizing and
+// dispatch to the kernels.  Declarations and the contract: include/kda.h.
+#include <stdio.h>
+
+#include <string>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kda_status fail(kda_status st, const char* msg) {
+    g_last_error = msg;
+    return st;
+}
+
+kda_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    g_last_error = std::string("CUDA: ") + cudaGetErrorString(e);
+    return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+// checks shared by every entry point; fills N (logical sequences)
+kda_status check_layout(const int32_t* cu, int n_seqs, int B, int T, int H, int* N) {
+    if (B < 0 || T < 0 || H <= 0) return fail(KDA_ERR_INVALID_ARG, "B, T must be >= 0 and H > 0");
+    if ((long long)B * T * H > (1ll << 40)) return fail(KDA_ERR_INVALID_ARG, "input too large");
+    if (cu) {
+        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "packed mode (cu_seqlens != NULL) needs B == 1");
+        if (n_seqs < 0 || n_seqs > 65535)
+            return fail(KDA_ERR_INVALID_ARG, "n_seqs must be in [0, 65535]");
+        if (((uintptr_t)cu & 3u) != 0) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens misaligned");
+        *N = n_seqs;
+    } else {
+        if (B > 65535) return fail(KDA_ERR_INVALID_ARG, "B must be <= 65535");
+        *N = B;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported configuration";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA error";
+    }
+    return "unknown kda_status";
+}
+
+const char* kda_last_error(void) { return g_last_error.c_str(); }
+
+kda_status kda_gate_fwd(const void* g, kda_dtype g_dtype, const float* A_log,
+                        const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                        const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                        int chunk_size, float* g_out, kda_stream_t stream) {
+    g_last_error.clear();
+    int N = 0;
+    kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
+    if (st != KDA_OK) return st;
+    if (K <= 0) return fail(KDA_ERR_INVALID_ARG, "K must be > 0");
+    if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) return fail(KDA_ERR_INVALID_ARG, "gate mode");
+    if (chunk_size != 1 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64)
+        return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 1, 16, 32 or 64");
+    if (mode == KDA_GATE_SAFE) {
+        if (!A_log) return fail(KDA_ERR_INVALID_ARG, "safe gate needs A_log");
+        if (!(lower_bound >= -5.0f && lower_bound < 0.0f))
+            return fail(KDA_ERR_INVALID_ARG, "safe gate needs -5 <= lower_bound < 0");
+    }
+    if ((long long)B * T == 0 || N == 0) return KDA_OK;
+    if (!g || !g_out) return fail(KDA_ERR_INVALID_ARG, "null g or g_out");
+    kda::GateArgs a{g, g_dtype == KDA_BF16, A_log, dt_bias, (int)mode, lower_bound, cu_seqlens,
+                    N, B, T, H, K, chunk_size, g_out, (cudaStream_t)stream};
+    return cuda_status(kda::launch_gate(a));
+}
+
+size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
+                                 int chunk_size, int n_seqs) {
+    if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(K) || !head_dim_ok(V)) return 0;
+    if (chunk_size != 32 && chunk_size != 64) return 0;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return 0;
+    bool packed = n_seqs > 0;
+    int N = packed ? n_seqs : B;
+    return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
+}
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                         const void* g, kda_dtype g_dtype, const float* A_log,
+                         const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                         const void* beta, const float* initial_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                         int V, int chunk_size, void* o, void* workspace,
+                         size_t workspace_bytes, kda_stream_t stream) {
+    g_last_error.clear();
+    int N = 0;
+    kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
+    if (st != KDA_OK) return st;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
+    if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
+    if (chunk_size != 32 && chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 32 or 64");
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) return fail(KDA_ERR_INVALID_ARG, "gate mode");
+    if (mode == KDA_GATE_SAFE) {
+        if (!A_log) return fail(KDA_ERR_INVALID_ARG, "safe gate needs A_log");
+        if (!(lower_bound >= -5.0f && lower_bound < 0.0f))
+            return fail(KDA_ERR_INVALID_ARG, "safe gate needs -5 <= lower_bound < 0");
+    }
+    const bool any_tokens = (long long)B * T > 0 && N > 0;
+    if (any_tokens && (!q || !k || !v || !g || !beta || !o))
+        return fail(KDA_ERR_INVALID_ARG, "null q, k, v, g, beta or o");
+    const void* ptrs[] = {q, k, v, g, o, initial_state, final_state, A_log, dt_bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (N == 0) return KDA_OK;
+    size_t need = kda_chunk_workspace_bytes(qkv_dtype, B, T, H, K, V, chunk_size,
+                                            cu_seqlens ? n_seqs : 0);
+    if (workspace_bytes < need || (need > 0 && !workspace))
+        return fail(KDA_ERR_INVALID_ARG, "workspace smaller than kda_chunk_workspace_bytes()");
+    if (workspace && ((uintptr_t)workspace & 255u) != 0)
+        return fail(KDA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,
+                   (int)mode, lower_bound, initial_state, final_state, cu_seqlens, N, B, T, H, K,
+                   V, chunk_size, o, workspace, workspace_bytes, (cudaStream_t)stream};
+    return cuda_status(kda::launch_chunk_precise(a));
+}
+
+kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                             const float* gate, const void* beta, const float* initial_state,
+                             float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
+                             int T, int H, int K, int V, void* o, kda_stream_t stream) {
+    g_last_error.clear();
+    int N = 0;
+    kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
+    if (st != KDA_OK) return st;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
+    const bool any_tokens = (long long)B * T > 0 && N > 0;
+    if (any_tokens && (!q || !k || !v || !gate || !beta || !o))
+        return fail(KDA_ERR_INVALID_ARG, "null q, k, v, gate, beta or o");
+    const void* ptrs[] = {q, k, v, gate, o, initial_state, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (N == 0) return KDA_OK;
+    kda::RecArgs a{q, k, v, gate, beta, qkv_dtype == KDA_BF16, initial_state, final_state,
+                   cu_seqlens, N, B, T, H, K, V, o, (cudaStream_t)stream};
+    return cuda_status(kda::launch_recurrent(a));
+}
+
+}  // extern "C"

@@ -1,0 +1,376 @@
+// Chunked KDA forward, float32 SIMT path, one kernel per step.
+//
+// This path computes every step in FP32 with FFMA, so it meets float32-input
+// accuracy (tensor-core bf16/tf32 operands would not), and it serves as the
+// stage-by-stage form of the chunked algorithm.  Steps and their sources:
+//   a1 gate + chunk-local log2 cumsum   FLA skill "fla-kda", "Gate modes" and
+//                                       "Safe gate numerical note" (RCP_LN2)
+//   a2 causal scores Akk, Aqk           Helion PR #3290 "Read only the causal
+//                                       columns in chunk_fwd_A_diag_anchored"
+//   a3 T = (I + Akk)^-1                 FLA skill "fla-kda", "Safe gate
+//                                       numerical note" (masked lower-triangular
+//                                       solve)
+//   a4 w = T (beta k 2^G), u = T (beta v)   FLA skill "fla-kda", "Public code
+//                                       map" (recompute_w_u_fwd)
+//   a5 v_new = u - w h; h <- 2^Glast h + (k 2^(Glast-G))^T v_new  (state scan)
+//   a6 o = s (q 2^G) h + Aqk v_new      attention-gym PR #345 (output kernel)
+// Every exp2 here has a non-positive argument (G is non-increasing inside a
+// chunk under the bounded-gate contract), so no offsets are needed: each
+// decay factor 2^(G_i - G_j), j <= i, is evaluated directly.
+//
+// Workspace (float32, token-indexed like the inputs; T_tot = B * T):
+//   G [T_tot,H,K] | Akk [T_tot,H,C] | Aqk [T_tot,H,C] | Tm [T_tot,H,C] |
+//   w [T_tot,H,K] | u [T_tot,H,V] | v_new [T_tot,H,V] | h [slots,H,K,V]
+#include "common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int DT = 32;  // channel tile
+
+struct PreciseWs {
+    float *G, *Akk, *Aqk, *Tm, *w, *u, *vn, *hc;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+PreciseWs carve(void* base, int B, int T, int H, int K, int V, int C, int slots, size_t* total) {
+    size_t tt = (size_t)B * T * H;
+    size_t sizes[8] = {tt * K, tt * C, tt * C, tt * C, tt * K, tt * V, tt * V,
+                       (size_t)slots * H * K * V};
+    float* ptrs[8];
+    size_t off = 0;
+    for (int i = 0; i < 8; ++i) {
+        ptrs[i] = base ? (float*)((char*)base + off) : nullptr;
+        off += align256(sizes[i] * sizeof(float));
+    }
+    if (total) *total = off;
+    return PreciseWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6], ptrs[7]};
+}
+
+// a2: Akk[i,j] = beta_i sum_d k_i k_j 2^(G_i-G_j) (j<i); Aqk[i,j] = s sum_d q_i k_j 2^(G_i-G_j) (j<=i)
+template <typename InT, int C>
+__global__ void __launch_bounds__(256) scores_kernel(const InT* __restrict__ q,
+                                                     const InT* __restrict__ k,
+                                                     const InT* __restrict__ beta,
+                                                     const float* __restrict__ G, ChunkMap cm,
+                                                     int H, int K, float* __restrict__ Akk,
+                                                     float* __restrict__ Aqk) {
+    constexpr int PM = C * C / 256;
+    __shared__ float qs[C][DT + 1], ks[C][DT + 1], gs[C][DT + 1];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x;
+    float akk[PM], aqk[PM];
+#pragma unroll
+    for (int m = 0; m < PM; ++m) akk[m] = aqk[m] = 0.f;
+    for (int d0 = 0; d0 < K; d0 += DT) {
+        __syncthreads();
+        for (int idx = tid; idx < C * DT; idx += 256) {
+            int i = idx / DT, dd = idx % DT;
+            float qv = 0.f, kv = 0.f, gv = 0.f;
+            if (i < len) {
+                size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
+                qv = to_f32(q[off]);
+                kv = to_f32(k[off]);
+                gv = G[off];
+            }
+            qs[i][dd] = qv;
+            ks[i][dd] = kv;
+            gs[i][dd] = gv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < PM; ++m) {
+            int p = tid + 256 * m, i = p / C, j = p % C;
+            if (j <= i && i < len) {
+                float a1 = 0.f, a2 = 0.f;
+#pragma unroll 8
+                for (int dd = 0; dd < DT; ++dd) {
+                    float e = exp2f(gs[i][dd] - gs[j][dd]);
+                    float kj = ks[j][dd] * e;
+                    a1 = fmaf(ks[i][dd], kj, a1);
+                    a2 = fmaf(qs[i][dd], kj, a2);
+                }
+                akk[m] += a1;
+                aqk[m] += a2;
+            }
+        }
+    }
+    const float scale = rsqrtf((float)K);
+#pragma unroll
+    for (int m = 0; m < PM; ++m) {
+        int p = tid + 256 * m, i = p / C, j = p % C;
+        if (i < len) {
+            size_t off = ((size_t)(t0 + i) * H + h) * C + j;
+            float bi = to_f32(beta[(size_t)(t0 + i) * H + h]);
+            Akk[off] = (j < i) ? bi * akk[m] : 0.f;
+            Aqk[off] = (j <= i) ? scale * aqk[m] : 0.f;
+        }
+    }
+}
+
+// a3: T = (I + Akk)^-1 by forward substitution, one thread per column of T
+template <int C>
+__global__ void __launch_bounds__(C) solve_kernel(const float* __restrict__ Akk, ChunkMap cm,
+                                                  int H, float* __restrict__ Tm) {
+    __shared__ float A[C][C + 1];
+    __shared__ float X[C][C + 1];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, col = threadIdx.x;
+    for (int i = 0; i < len; ++i) A[i][col] = Akk[((size_t)(t0 + i) * H + h) * C + col];
+    __syncthreads();
+    for (int i = 0; i < len; ++i) {
+        float val = (i == col) ? 1.f : 0.f;
+        for (int j = col; j < i; ++j) val = fmaf(-A[i][j], X[j][col], val);
+        X[i][col] = (i < col) ? 0.f : val;
+    }
+    for (int i = 0; i < len; ++i) Tm[((size_t)(t0 + i) * H + h) * C + col] = X[i][col];
+}
+
+// a4: w = T (beta k 2^G) [C,K], u = T (beta v) [C,V]; one thread per output column
+template <typename InT, int C>
+__global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
+                                                 const InT* __restrict__ v,
+                                                 const InT* __restrict__ beta,
+                                                 const float* __restrict__ G,
+                                                 const float* __restrict__ Tm, ChunkMap cm, int H,
+                                                 int K, int V, float* __restrict__ w,
+                                                 float* __restrict__ u) {
+    __shared__ float Ts[C][C];
+    __shared__ float bs[C];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x;
+    for (int idx = tid; idx < C * C; idx += 256) {
+        int i = idx / C, j = idx % C;
+        Ts[i][j] = (i < len) ? Tm[((size_t)(t0 + i) * H + h) * C + j] : 0.f;
+    }
+    for (int i = tid; i < C; i += 256) bs[i] = (i < len) ? to_f32(beta[(size_t)(t0 + i) * H + h]) : 0.f;
+    __syncthreads();
+    for (int col = tid; col < K + V; col += 256) {
+        float x[C];
+        const bool isk = col < K;
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            float val = 0.f;
+            if (j < len) {
+                if (isk) {
+                    size_t off = ((size_t)(t0 + j) * H + h) * K + col;
+                    val = bs[j] * to_f32(k[off]) * exp2f(G[off]);
+                } else {
+                    val = bs[j] * to_f32(v[((size_t)(t0 + j) * H + h) * V + (col - K)]);
+                }
+            }
+            x[j] = val;
+        }
+        // T is unit lower triangular and stored with zeros above the diagonal, so the
+        // full row product equals the causal one; x stays in registers (static indices)
+#pragma unroll 1
+        for (int i = 0; i < len; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < C; ++j) acc = fmaf(Ts[i][j], x[j], acc);
+            {
+                if (isk) w[((size_t)(t0 + i) * H + h) * K + col] = acc;
+                else u[((size_t)(t0 + i) * H + h) * V + (col - K)] = acc;
+            }
+        }
+    }
+}
+
+// a5: sequential state scan over the chunks of one sequence, 32 value columns per block
+template <typename InT, int C, int K>
+__global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
+                                                   const float* __restrict__ G,
+                                                   const float* __restrict__ w,
+                                                   const float* __restrict__ u, const float* h0,
+                                                   float* hT, ChunkMap cm, int H, int V,
+                                                   float* __restrict__ hc,
+                                                   float* __restrict__ vn) {
+    constexpr int BV = 32, DS = 16;  // value columns per block, channel tile of the update
+    __shared__ float hs[K][BV];
+    __shared__ float vns[C][BV];
+    __shared__ float kds[C][DS + 1];
+    __shared__ float gl[DS];
+    const int tid = threadIdx.x, lane = tid & 31, grp = tid >> 5;
+    const int v0 = blockIdx.x * BV, h = blockIdx.y, n = blockIdx.z;
+    long bos, eos;
+    if (cm.cu) { bos = __ldg(cm.cu + n); eos = __ldg(cm.cu + n + 1); }
+    else       { bos = (long)n * cm.T; eos = bos + cm.T; }
+    const size_t st = ((size_t)n * H + h) * (size_t)K * V;
+    for (int idx = tid; idx < K * BV; idx += 256) {
+        int d = idx / BV, vv = idx % BV;
+        hs[d][vv] = h0 ? h0[st + (size_t)d * V + v0 + vv] : 0.f;
+    }
+    const int slot0 = cm.first_slot(n, (int)bos);
+    const int nt = (int)((eos - bos + C - 1) / C);
+    for (int c = 0; c < nt; ++c) {
+        const long t0 = bos + (long)c * C;
+        const int len = (int)min((long)C, eos - t0);
+        __syncthreads();
+        const size_t hoff = ((size_t)(slot0 + c) * H + h) * (size_t)K * V;
+        for (int idx = tid; idx < K * BV; idx += 256) {
+            int d = idx / BV, vv = idx % BV;
+            hc[hoff + (size_t)d * V + v0 + vv] = hs[d][vv];
+        }
+        // v_new = u - w h
+        for (int i = grp; i < len; i += 8) {
+            size_t row = (size_t)(t0 + i) * H + h;
+            float acc = u[row * V + v0 + lane];
+            const float* wr = w + row * K;
+            for (int d = 0; d < K; ++d) acc = fmaf(-__ldg(wr + d), hs[d][lane], acc);
+            vns[i][lane] = acc;
+            vn[row * V + v0 + lane] = acc;
+        }
+        __syncthreads();
+        // h <- 2^Glast h + (k 2^(Glast - G))^T v_new, channel tiles of DS
+        const size_t last = ((size_t)(t0 + len - 1) * H + h) * K;
+        for (int d0 = 0; d0 < K; d0 += DS) {
+            if (tid < DS) gl[tid] = G[last + d0 + tid];
+            __syncthreads();
+            for (int idx = tid; idx < C * DS; idx += 256) {
+                int i = idx / DS, dd = idx % DS;
+                float val = 0.f;
+                if (i < len) {
+                    size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
+                    val = to_f32(k[off]) * exp2f(gl[dd] - G[off]);
+                }
+                kds[i][dd] = val;
+            }
+            __syncthreads();
+            for (int dd = grp; dd < DS; dd += 8) {
+                int d = d0 + dd;
+                float acc = exp2f(gl[dd]) * hs[d][lane];
+                for (int i = 0; i < len; ++i) acc = fmaf(kds[i][dd], vns[i][lane], acc);
+                hs[d][lane] = acc;
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    if (hT) {
+        for (int idx = tid; idx < K * BV; idx += 256) {
+            int d = idx / BV, vv = idx % BV;
+            hT[st + (size_t)d * V + v0 + vv] = hs[d][vv];
+        }
+    }
+}
+
+// a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows
+template <typename InT, int C>
+__global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
+                                                  const float* __restrict__ G,
+                                                  const float* __restrict__ Aqk,
+                                                  const float* __restrict__ hc,
+                                                  const float* __restrict__ vn, ChunkMap cm,
+                                                  int H, int K, int V, InT* __restrict__ o) {
+    __shared__ float qg[C][DT + 1];
+    __shared__ float As[C][C + 1];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
+    const float scale = rsqrtf((float)K);
+    for (int idx = tid; idx < C * C; idx += nthr) {
+        int i = idx / C, j = idx % C;
+        As[i][j] = (i < len) ? Aqk[((size_t)(t0 + i) * H + h) * C + j] : 0.f;
+    }
+    const int vcol = tid;  // blockDim.x == V
+    const size_t hoff = ((size_t)blockIdx.x * H + h) * (size_t)K * V;
+    float acc[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) acc[i] = 0.f;
+    for (int d0 = 0; d0 < K; d0 += DT) {
+        __syncthreads();
+        for (int idx = tid; idx < C * DT; idx += nthr) {
+            int i = idx / DT, dd = idx % DT;
+            float val = 0.f;
+            if (i < len) {
+                size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
+                val = scale * to_f32(q[off]) * exp2f(G[off]);
+            }
+            qg[i][dd] = val;
+        }
+        __syncthreads();
+        for (int dd = 0; dd < DT; ++dd) {
+            float hv = hc[hoff + (size_t)(d0 + dd) * V + vcol];
+#pragma unroll
+            for (int i = 0; i < C; ++i) acc[i] = fmaf(qg[i][dd], hv, acc[i]);
+        }
+    }
+    __syncthreads();
+    for (int j = 0; j < len; ++j) {
+        float vj = vn[((size_t)(t0 + j) * H + h) * V + vcol];
+#pragma unroll
+        for (int i = 0; i < C; ++i) acc[i] = fmaf(As[i][j], vj, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < C; ++i)
+        if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<InT>(acc[i]);
+}
+
+template <typename InT, int C>
+cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
+    ChunkMap cm{a.cu, a.N, a.T, C};
+    const int slots = cm.n_slots();
+    GateArgs ga{a.g, a.g_bf16, a.A_log, a.dt_bias, a.mode, a.lb, a.cu, a.N,
+                a.B, a.T, a.H, a.K, C, ws.G, a.stream};
+    cudaError_t e = launch_gate(ga);
+    if (e != cudaSuccess) return e;
+    const InT* q = (const InT*)a.q;
+    const InT* k = (const InT*)a.k;
+    const InT* v = (const InT*)a.v;
+    const InT* beta = (const InT*)a.beta;
+    if (slots > 0) {
+        dim3 g2(slots, a.H);
+        scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, a.K, ws.Akk,
+                                                        ws.Aqk);
+        solve_kernel<C><<<g2, C, 0, a.stream>>>(ws.Akk, cm, a.H, ws.Tm);
+        wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, a.K, a.V,
+                                                    ws.w, ws.u);
+    }
+    dim3 g5(a.V / 32, a.H, a.N);
+    switch (a.K) {
+        case 64:
+            scan_kernel<InT, C, 64><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
+                                                              a.H, a.V, ws.hc, ws.vn);
+            break;
+        case 128:
+            scan_kernel<InT, C, 128><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
+                                                               a.H, a.V, ws.hc, ws.vn);
+            break;
+        case 256:
+            scan_kernel<InT, C, 256><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
+                                                               a.H, a.V, ws.hc, ws.vn);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
+    if (slots > 0)
+        out_kernel<InT, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn,
+                                                                   cm, a.H, a.K, a.V, (InT*)a.o);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t precise_workspace_bytes(int B, int T, int H, int K, int V, int C, int N, bool packed) {
+    ChunkMap cm{packed ? (const int32_t*)1 : nullptr, N, T, C};
+    size_t total = 0;
+    carve(nullptr, B, T, H, K, V, C, cm.n_slots(), &total);
+    return total;
+}
+
+cudaError_t launch_chunk_precise(const FwdArgs& a) {
+    ChunkMap cm{a.cu, a.N, a.T, a.C};
+    size_t total = 0;
+    PreciseWs ws = carve(a.ws, a.B, a.T, a.H, a.K, a.V, a.C, cm.n_slots(), &total);
+    if (a.ws_bytes < total) return cudaErrorInvalidValue;
+    if (a.C == 64)
+        return a.qkv_bf16 ? run<__nv_bfloat16, 64>(a, ws) : run<float, 64>(a, ws);
+    return a.qkv_bf16 ? run<__nv_bfloat16, 32>(a, ws) : run<float, 32>(a, ws);
+}
+
+}  // namespace kda

@@ -1,0 +1,70 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+struct GateArgs {
+    const void* g;
+    bool g_bf16;
+    const float* A_log;
+    const float* dt_bias;
+    int mode;
+    float lb;
+    const int32_t* cu;
+    int N;  // logical sequences (B when dense)
+    int B, T, H, K, C;
+    float* out;
+    cudaStream_t stream;
+};
+
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    bool qkv_bf16;
+    bool g_bf16;
+    const float* A_log;
+    const float* dt_bias;
+    int mode;  // 0 pre-gated, 1 safe
+    float lb;
+    const float* h0;
+    float* hT;
+    const int32_t* cu;
+    int N;  // logical sequences (B when dense)
+    int B, T, H, K, V, C;
+    void* o;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+struct RecArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* gate;
+    const void* beta;
+    bool qkv_bf16;
+    const float* h0;
+    float* hT;
+    const int32_t* cu;
+    int N;
+    int B, T, H, K, V;
+    void* o;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_gate(const GateArgs& a);
+cudaError_t launch_recurrent(const RecArgs& a);
+
+// float32 SIMT chunked path: stage-by-stage kernels with a device workspace
+size_t precise_workspace_bytes(int B, int T, int H, int K, int V, int C, int N, bool packed);
+cudaError_t launch_chunk_precise(const FwdArgs& a);
+
+}  // namespace kda

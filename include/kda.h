@@ -1,0 +1,169 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library
+ *          (libkda_gb300.so).
+ *
+ * The library computes the KDA forward: per head, a K x V FP32 state S that
+ * decays per key channel and is updated by the delta rule,
+ *
+ *     S_t = Diag(exp(a_t)) S_{t-1};  S_t += beta_t k_t (v_t - S_t^T k_t)^T;
+ *     o_t = S_t^T q_t / sqrt(K),
+ *
+ * in chunked (WY) form for prefill and token by token for decode.  Sources:
+ *   - attention-gym PR #317 "Add fused recurrent_kda for decode and inference
+ *     prefill", Agent note: call contract (q, k, v, gate, beta, initial_state,
+ *     cu_seqlens, output_final_state), device-resident int32 offsets, repeated
+ *     offsets as empty slots whose state passes through bitwise, a terminal
+ *     offset below the physical capacity leaving the tail outside the
+ *     contract, FP32 states with one leading entry per logical sequence, the
+ *     recurrent gate as a per-token log2 decay, the 1/sqrt(K) query scale.
+ *   - FLA skill page "fla-kda", sections "Gate modes" (pre-gated and safe
+ *     in-kernel activations, -5 <= lower_bound < 0) and "Safe gate numerical
+ *     note" (RCP_LN2 conversion to base 2, sub-chunk offsets before exp2).
+ *   - Helion PR #3290 "Read only the causal columns in
+ *     chunk_fwd_A_diag_anchored": chunk sizes 32 and 64, 16-row diagonal
+ *     sub-blocks, causal columns only.
+ *
+ * Conventions for every entry point
+ *   - All pointers are DEVICE pointers (cudaMalloc'd or equivalent), owned by
+ *     the caller, contiguous in the stated layout, 16-byte aligned.  The
+ *     library never allocates, never synchronises the stream and never reads
+ *     cu_seqlens on the host; all work is enqueued on `stream`, so calls can be
+ *     captured in a CUDA graph.
+ *   - Layout is token-major: q, k, g [B, T, H, K]; v, o [B, T, H, V];
+ *     beta [B, T, H]; A_log, dt_bias [H, K] float32; states [N, H, K, V]
+ *     float32 with N = n_seqs (packed) or B (dense).
+ *   - Packed (varlen) mode: cu_seqlens != NULL, B must be 1, T is the physical
+ *     capacity, cu_seqlens holds n_seqs + 1 non-decreasing int32 offsets with
+ *     cu_seqlens[0] = 0 and cu_seqlens[n_seqs] <= T.  A repeated offset is an
+ *     empty slot: its final state equals its initial state bit for bit (zeros
+ *     when initial_state is NULL).  Rows of o at or beyond cu_seqlens[n_seqs]
+ *     are neither read into any result nor written.  Offsets that break these
+ *     rules are undefined behaviour (they live on the device and are not
+ *     checked on the host).
+ *   - Dense mode: cu_seqlens == NULL, n_seqs is ignored, B sequences of T.
+ *   - initial_state == NULL means a zero initial state; final_state == NULL
+ *     means the final state is not produced (output_final_state = False).
+ *   - Every argument that the host can check is checked before any launch;
+ *     a failed check returns KDA_ERR_INVALID_ARG or KDA_ERR_UNSUPPORTED and
+ *     enqueues nothing.  A launch error returns KDA_ERR_CUDA.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* a cudaStream_t (NULL = the legacy default stream) */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad bound */
+    KDA_ERR_UNSUPPORTED = 2, /* valid but not implemented (dtype, head dim, chunk size) */
+    KDA_ERR_CUDA = 3         /* a CUDA launch or runtime call failed */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef enum {
+    /* g already is the natural-log decay (FLA skill "fla-kda", "Gate modes",
+       pre-gated mode); A_log, dt_bias and lower_bound are ignored.  The chunked
+       path assumes the bounded-gate contract -5 <= g <= 0 (attention-gym PR #345
+       text: the flag assumes the bounded-gate contract). */
+    KDA_GATE_PRE = 0,
+    /* safe in-kernel mode: a = lower_bound * sigmoid(exp(A_log) * (g + dt_bias)),
+       A_log required, dt_bias optional, -5 <= lower_bound < 0 (FLA skill
+       "fla-kda", "Gate modes") */
+    KDA_GATE_SAFE = 1
+} kda_gate_mode;
+
+/*
+ * Gate activation followed by the chunk-local inclusive cumulative sum in
+ * log2 units (FLA skill "fla-kda", "Safe gate numerical note": RCP_LN2
+ * conversion; attention-gym PR #317: bounded_gate_cumsum, chunk_size = 1 gives
+ * the recurrent entry point's per-token log2 gate).
+ *
+ *   g          [B, T, H, K], dtype g_dtype (KDA_F32 or KDA_BF16)
+ *   A_log      [H, K] float32, required in KDA_GATE_SAFE mode
+ *   dt_bias    [H, K] float32 or NULL (= 0)
+ *   chunk_size 1, 16, 32 or 64; chunks restart at every sequence start
+ *   g_out      [B, T, H, K] float32: g_out[t] = (1/ln 2) * sum of the
+ *              activation over the tokens of t's chunk up to and including t.
+ *              Packed mode: rows at or beyond cu_seqlens[n_seqs] are not written.
+ */
+kda_status kda_gate_fwd(const void* g, kda_dtype g_dtype, const float* A_log,
+                        const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                        const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                        int chunk_size, float* g_out, kda_stream_t stream);
+
+/*
+ * Bytes of device scratch memory kda_chunk_fwd needs for these sizes (0 when
+ * the selected kernels need none).  n_seqs is the number of logical sequences
+ * in packed mode and 0 in dense mode.  The caller allocates the scratch and
+ * passes it to kda_chunk_fwd; its contents on entry do not matter.  Returns 0
+ * as well for sizes kda_chunk_fwd would reject.
+ */
+size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
+                                 int chunk_size, int n_seqs);
+
+/*
+ * Chunked KDA forward (prefill).  Steps: gate activation + chunk-local log2
+ * cumsum; causal intra-chunk scores Akk (strictly lower, beta-scaled) and Aqk
+ * (lower incl. diagonal, 1/sqrt(K)-scaled) on 16-token sub-blocks; the unit
+ * lower-triangular solve T = (I + Akk)^-1; WY terms w = T (beta k 2^G),
+ * u = T (beta v); the sequential inter-chunk state scan; the output
+ * o = (1/sqrt(K)) (q 2^G) h + Aqk v_new.
+ *
+ *   q, k       [B, T, H, K], dtype qkv_dtype; rows are used as given
+ *   v          [B, T, H, V], dtype qkv_dtype
+ *   g          [B, T, H, K], dtype g_dtype (raw gate in SAFE mode, the
+ *              natural-log decay in PRE mode)
+ *   beta       [B, T, H], dtype qkv_dtype, post-sigmoid
+ *   o          [B, T, H, V], dtype qkv_dtype (output)
+ *   chunk_size 32 or 64 (Helion PR #3290: the two chunk sizes FLA's KDA accepts)
+ *   K, V       64, 128 or 256 (K == V on the bf16 tensor-core path; any pair
+ *              of these on the float32 path)
+ *   workspace  device scratch of at least kda_chunk_workspace_bytes(...) bytes,
+ *              256-byte aligned; may be NULL when that size is 0.
+ * initial_state and final_state may be the same buffer.
+ */
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                         const void* g, kda_dtype g_dtype, const float* A_log,
+                         const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                         const void* beta, const float* initial_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                         int V, int chunk_size, void* o, void* workspace,
+                         size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Token-sequential KDA forward (decode and short prefill), attention-gym PR
+ * #317: one program per (sequence, head, value block) scans the tokens with
+ * its FP32 state block in registers and computes in FP32 for any input dtype.
+ *
+ *   gate       [B, T, H, K] float32: per-token LOG2 decay (S rows scale by
+ *              2^gate), e.g. kda_gate_fwd(..., chunk_size = 1, ...)
+ *   q, k, v, beta, o, states, cu_seqlens: as for kda_chunk_fwd.
+ *   K, V       64, 128 or 256 (any pair).
+ * final_state may alias initial_state (in-place decode): each program reads
+ * its whole state block before it writes any of it.
+ */
+kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                             const float* gate, const void* beta, const float* initial_state,
+                             float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
+                             int T, int H, int K, int V, void* o, kda_stream_t stream);
+
+/* static, NUL-terminated description of a status code */
+const char* kda_status_string(kda_status status);
+
+/* the last error detail recorded by a failed call on this host thread ("" if none) */
+const char* kda_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

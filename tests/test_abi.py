@@ -1,0 +1,136 @@
+"""The C-ABI library: it loads, exports exactly what include/kda.h declares, and rejects
+bad arguments on the host before any launch (no GPU needed: every call below fails
+validation, or needs no device work, so no CUDA call is made)."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+F32, BF16 = 0, 1
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names |= set(re.findall(r"^\s*(?:kda_status|size_t|const char\s*\*)\s*(kda_\w+)\s*\(",
+                                text, flags=re.M))
+    return names
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from chunked_kda_gb300 import _build
+
+    path = _build.build()
+    L = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
+                                i32, i32, i32, i32, i32, i32, vp, vp, ctypes.c_size_t, vp]
+    L.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                    i32, vp, vp]
+    L.kda_gate_fwd.argtypes = [vp, i32, vp, vp, i32, f32, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    L.kda_chunk_workspace_bytes.argtypes = [i32] * 8
+    L.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
+    L.kda_status_string.restype = ctypes.c_char_p
+    L.kda_last_error.restype = ctypes.c_char_p
+    return L
+
+
+def test_header_declares_the_entry_points():
+    assert {"kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_recurrent_fwd",
+            "kda_status_string", "kda_last_error"} <= declared_functions()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+@pytest.mark.skipif(shutil.which("nm") is None, reason="nm not available")
+def test_no_undeclared_kda_exports():
+    from chunked_kda_gb300 import _build
+
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.build()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.split() and
+                ln.split()[-1].startswith("kda_")}
+    assert exported == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        assert lib.kda_status_string(code).startswith(b"KDA_")
+
+
+P = ctypes.c_void_p(4096)  # aligned stand-in: never dereferenced, validation fails first
+
+
+def _chunk(lib, **kw):
+    a = dict(q=P, k=P, v=P, dt=BF16, g=P, gdt=BF16, A_log=P, dt_bias=None, mode=1, lb=-5.0,
+             beta=P, h0=None, hT=None, cu=None, n=0, B=1, T=64, H=2, K=128, V=128, C=64, o=P,
+             ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["dt"], a["g"], a["gdt"], a["A_log"],
+                             a["dt_bias"], a["mode"], a["lb"], a["beta"], a["h0"], a["hT"],
+                             a["cu"], a["n"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
+                             a["o"], a["ws"], a["ws_bytes"], None)
+
+
+def test_chunk_host_validation(lib):
+    assert _chunk(lib, C=48) == UNSUPPORTED
+    assert _chunk(lib, K=96) == UNSUPPORTED
+    assert _chunk(lib, dt=7) == UNSUPPORTED
+    assert _chunk(lib, lb=-5.5) == INVALID
+    assert _chunk(lib, lb=0.0) == INVALID
+    assert _chunk(lib, A_log=None) == INVALID
+    assert _chunk(lib, q=None) == INVALID
+    assert _chunk(lib, o=ctypes.c_void_p(4098)) == INVALID  # misaligned
+    assert _chunk(lib, B=2, cu=P, n=1) == INVALID  # packed needs B == 1
+    assert _chunk(lib, ws=None, ws_bytes=0) == INVALID  # workspace too small
+    assert b"workspace" in lib.kda_last_error()
+    assert _chunk(lib, H=0) == INVALID
+    # nothing to do: zero logical sequences is OK and launches nothing
+    assert _chunk(lib, B=0) == OK
+    assert _chunk(lib, cu=P, n=0, B=1) == OK
+
+
+def test_recurrent_and_gate_host_validation(lib):
+    r = lib.kda_recurrent_fwd(P, P, P, BF16, None, P, None, None, None, 0, 1, 4, 2, 128, 128, P,
+                              None)
+    assert r == INVALID  # null gate
+    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 100, 128, P, None)
+    assert r == UNSUPPORTED
+    g = lib.kda_gate_fwd(P, BF16, None, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, P, None)
+    assert g == INVALID  # safe gate without A_log
+    g = lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 48, P, None)
+    assert g == UNSUPPORTED
+
+
+def test_workspace_bytes(lib):
+    def al(x):
+        return (x + 255) // 256 * 256
+
+    # float32 stage-by-stage path: G, Akk, Aqk, T, w, u, v_new token-indexed + h per chunk slot
+    B, T, H, K, V, C = 2, 100, 3, 64, 128, 32
+    tt = B * T * H
+    slots = B * ((T + C - 1) // C)
+    want = sum(al(4 * x) for x in (tt * K, tt * C, tt * C, tt * C, tt * K, tt * V, tt * V,
+                                   slots * H * K * V))
+    assert lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0) == want
+    # packed: floor(T_cap / C) + N + 1 chunk slots
+    n = 5
+    slots = T // C + n + 1
+    tt = T * H
+    want = sum(al(4 * x) for x in (tt * K, tt * C, tt * C, tt * C, tt * K, tt * V, tt * V,
+                                   slots * H * K * V))
+    assert lib.kda_chunk_workspace_bytes(F32, 1, T, H, K, V, C, n) == want
+    assert lib.kda_chunk_workspace_bytes(F32, 1, T, H, K, V, 48, 0) == 0

@@ -1,0 +1,215 @@
+"""kda_chunk_fwd (C ABI, through the binding) against the float64 oracle, element by
+element on small inputs spanning several chunks and ragged tails, and on sampled
+(sequence, head) units of the full-size workloads."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_kda_gb300 import workloads
+from parity import check_o, check_state, check_units, to_device, valid_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def kda():
+    import chunked_kda_gb300
+
+    return chunked_kda_gb300
+
+
+def run_gpu(w, **kw):
+    t = to_device(w)
+    args = dict(A_log=t["A_log"], dt_bias=t["dt_bias"], mode=w.mode, lower_bound=w.lower_bound,
+                initial_state=t["initial_state"], output_final_state=True,
+                cu_seqlens=t["cu_seqlens"], chunk_size=w.chunk_size)
+    args.update(kw)
+    o, st = kda().kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], **args)
+    torch.cuda.synchronize()
+    return o, st
+
+
+def run_oracle(w):
+    return oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, w.mode, w.lower_bound,
+                          w.initial_state, w.cu_seqlens)
+
+
+def compare(w, o, st):
+    o_ref, s_ref = run_oracle(w)
+    check_o(o, o_ref, w.q.dtype, valid_mask(w))
+    if st is not None:
+        check_state(st, s_ref, w.q.dtype)
+
+
+def test_tiny_fp32_workload():
+    w = workloads.make("tiny_fp32_b1_t128_h2_d64")
+    o, st = run_gpu(w)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("T", [1, 17, 64, 65, 130, 200])
+@pytest.mark.parametrize("D", [64, 128])
+def test_dense_small(dtype, C, T, D):
+    w = workloads.make_dense("t", 2, T, 2, D, D, C, dtype, 11 + T + D, state_std=0.05)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("K,V", [(256, 256), (64, 128), (256, 64)])
+def test_dense_head_dims(dtype, K, V):
+    w = workloads.make_dense("t", 1, 97, 2, K, V, 64, dtype, 5 + K + V, state_std=0.05)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("C", [32, 64])
+def test_pre_gated(dtype, C):
+    w = workloads.make_dense("t", 2, 150, 2, 128, 128, C, dtype, 21, state_std=0.05,
+                             mode=workloads.GATE_PRE)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("lb,g_std", [(-5.0, 10.0), (-0.01, 1.0), (-1e-4, 3.0), (-5.0, 0.01)])
+def test_gate_extremes(lb, g_std):
+    """lb = -5 with large +-(g + dt_bias), lb close to 0, long cumulative decay
+    (FLA skill "fla-kda", correctness checklist: gate numerical extremes)."""
+    w = workloads.make_dense("t", 1, 300, 2, 128, 128, 64, torch.bfloat16, 31, g_std=g_std,
+                             state_std=0.05, lower_bound=lb)
+    w.A_log = w.A_log * 3.0  # exp(A_log) up to 4096: saturates the sigmoid
+    o, st = run_gpu(w)
+    compare(w, o, st)
+
+
+VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+def test_varlen_contract(dtype, C, mode):
+    """Packed sequences with empty slots (first, interior, consecutive, last) and a
+    NaN-poisoned capacity tail (attention-gym PR #317, Agent note)."""
+    cap = sum(VARLEN_LENGTHS) + 23
+    w = workloads.make_varlen("t", VARLEN_LENGTHS, cap, 2, 128, 128, C, dtype, 41, mode=mode)
+    t = to_device(w)
+    sentinel = torch.full((1, cap, 2, 128), 12345.0, device="cuda", dtype=dtype)
+    o, st = run_gpu(w, o=sentinel)
+    compare(w, o, st)
+    end = int(w.cu_seqlens[-1])
+    # the tail beyond the last offset is not written (bitwise)
+    assert torch.equal(o[:, end:], torch.full_like(o[:, end:], 12345.0))
+    # empty slots pass their state through bit for bit
+    for n, L in enumerate(VARLEN_LENGTHS):
+        if L == 0:
+            assert torch.equal(st[n], t["initial_state"][n])
+    # each packed sequence equals the same sequence run alone (same chunk alignment)
+    cu = w.cu_seqlens.tolist()
+    for n, L in enumerate(VARLEN_LENGTHS):
+        if L == 0:
+            continue
+        sl = slice(cu[n], cu[n + 1])
+        wd = workloads.Workload("d", 1, L, 2, 128, 128, C, mode, w.lower_bound,
+                                w.q[:, sl].contiguous(), w.k[:, sl].contiguous(),
+                                w.v[:, sl].contiguous(), w.g[:, sl].contiguous(),
+                                w.beta[:, sl].contiguous(), w.A_log, w.dt_bias,
+                                w.initial_state[n:n + 1].contiguous())
+        od, sd = run_gpu(wd)
+        assert torch.equal(od[0], o[0, sl]), f"sequence {n}: packed != alone"
+        assert torch.equal(sd[0], st[n])
+
+
+def test_no_initial_state_equals_zeros_and_no_final_state():
+    w = workloads.make_dense("t", 2, 100, 2, 128, 128, 64, torch.bfloat16, 51)
+    o1, s1 = run_gpu(w)
+    t = to_device(w)
+    zeros = torch.zeros((2, 2, 128, 128), device="cuda")
+    o2, s2 = run_gpu(w, initial_state=zeros)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    o3, s3 = run_gpu(w, output_final_state=False)
+    assert s3 is None and torch.equal(o1, o3)
+
+
+def test_final_state_in_place():
+    w = workloads.make_dense("t", 2, 100, 2, 128, 128, 64, torch.bfloat16, 52, state_std=0.05)
+    o1, s1 = run_gpu(w)
+    t = to_device(w)
+    S = t["initial_state"].clone()
+    o2, _ = kda().kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["A_log"],
+                                t["dt_bias"], w.mode, w.lower_bound, S, True, None, 64,
+                                final_state=S)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, S)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_linear_in_v_and_state_exactly(dtype):
+    """(v, S0) -> (o, S_T) is linear, and scaling by 2 is exact in floating point."""
+    w = workloads.make_dense("t", 1, 130, 2, 128, 128, 64, dtype, 53, state_std=0.05)
+    o1, s1 = run_gpu(w)
+    w.v = (w.v.float() * 2).to(dtype)
+    w.initial_state = w.initial_state * 2
+    o2, s2 = run_gpu(w)
+    assert torch.equal(o2.float(), 2 * o1.float()) and torch.equal(s2, 2 * s1)
+
+
+def test_state_carry():
+    """Two calls chained through the state equal one call (within tolerance: the chunk
+    boundaries differ)."""
+    w = workloads.make_dense("t", 1, 200, 2, 128, 128, 64, torch.bfloat16, 54, state_std=0.05)
+    o, st = run_gpu(w)
+    t1 = 77
+    parts = []
+    S = w.initial_state
+    for sl in (slice(0, t1), slice(t1, 200)):
+        wp = workloads.Workload("p", 1, sl.stop - sl.start, 2, 128, 128, 64, w.mode,
+                                w.lower_bound, w.q[:, sl].contiguous(), w.k[:, sl].contiguous(),
+                                w.v[:, sl].contiguous(), w.g[:, sl].contiguous(),
+                                w.beta[:, sl].contiguous(), w.A_log, w.dt_bias, S)
+        op, sp = run_gpu(wp)
+        parts.append(op)
+        S = sp.cpu()
+    oc = torch.cat(parts, dim=1)
+    o_ref, s_ref = run_oracle(w)
+    check_o(oc, o_ref, torch.bfloat16)
+    check_state(S, s_ref, torch.bfloat16)
+
+
+def _sample_units(w, k=4, seed=0):
+    r = np.random.default_rng(seed)
+    N = w.n_seqs
+    units = {(0, 0), (N - 1, w.H - 1)}
+    while len(units) < k:
+        units.add((int(r.integers(N)), int(r.integers(w.H))))
+    if w.cu_seqlens is not None:
+        cu = w.cu_seqlens.tolist()
+        units = {(n, h) for n, h in units if cu[n + 1] > cu[n]} | {
+            (n, 0) for n in range(N) if cu[n + 1] == cu[n]}
+    return sorted(units)
+
+
+@pytest.mark.parametrize("name", ["dense_bf16_b4_t2048_h16_d128",
+                                  "varlen_bf16_n16_cap20480_h32_d128_c32",
+                                  "dense_bf16_b1_t8192_h96_d128",
+                                  "dense_bf16_b4_t4096_h64_d128",
+                                  "dense_bf16_b8_t2048_h32_d256"])
+def test_full_size_sampled(name):
+    """The full workloads, in the configuration bench.py times, checked on sampled
+    (sequence, head) units the oracle computes one by one."""
+    w = workloads.make(name, device="cpu")
+    o, st = run_gpu(w)
+    assert torch.isfinite(o[torch.from_numpy(valid_mask(w)).cuda()]).all()
+    check_units(w, o, st, _sample_units(w))
