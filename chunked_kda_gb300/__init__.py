@@ -54,10 +54,10 @@ def load_library():
         lib.kda_chunk_workspace_bytes.argtypes = [i32] * 8
         lib.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
-                                      i32, i32, i32, i32, i32, i32, i32, vp, vp, ctypes.c_size_t,
-                                      vp]
+                                      i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
+                                      ctypes.c_size_t, vp]
         lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
-                                          i32, i32, vp, vp]
+                                          i32, i32, vp, i32, vp]
         for fn in (lib.kda_gate_fwd, lib.kda_chunk_fwd, lib.kda_recurrent_fwd):
             fn.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -139,8 +139,10 @@ def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0) -> int
 
 def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
                   initial_state=None, output_final_state=False, cu_seqlens=None, chunk_size=64,
-                  o=None, final_state=None, workspace=None, stream=None):
+                  o=None, final_state=None, workspace=None, stream=None, o_dtype=None):
     """Chunked KDA forward; returns (o, final_state or None).
+
+    ``o_dtype`` is the dtype of q (default) or torch.float32.
 
     ``final_state`` may be passed (and may be ``initial_state`` itself) to
     write the final state in place; otherwise it is allocated when
@@ -159,8 +161,8 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     _cuda(initial_state, "initial_state", torch.float32)
     n = _seqs(cu_seqlens, B)
     if o is None:
-        o = torch.empty((B, T, H, V), device=q.device, dtype=q.dtype)
-    _cuda(o, "o", q.dtype)
+        o = torch.empty((B, T, H, V), device=q.device, dtype=o_dtype or q.dtype)
+    _cuda(o, "o")
     if final_state is None and output_final_state:
         N = n if cu_seqlens is not None else B
         final_state = torch.empty((N, H, K, V), device=q.device, dtype=torch.float32)
@@ -173,12 +175,13 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     _check("kda_chunk_fwd", lib.kda_chunk_fwd(
         _ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
         lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n, B,
-        T, H, K, V, chunk_size, _ptr(o), _ptr(workspace), ws_bytes, _stream(stream)))
+        T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes,
+        _stream(stream)))
     return o, final_state
 
 
 def kda_recurrent_fwd(q, k, v, gate, beta, initial_state=None, output_final_state=False,
-                      cu_seqlens=None, o=None, final_state=None, stream=None):
+                      cu_seqlens=None, o=None, final_state=None, stream=None, o_dtype=None):
     """Token-sequential KDA forward with a per-token log2 gate; returns (o, final_state or None).
 
     ``final_state`` may be ``initial_state`` itself (in-place decode).
@@ -194,8 +197,8 @@ def kda_recurrent_fwd(q, k, v, gate, beta, initial_state=None, output_final_stat
     _cuda(initial_state, "initial_state", torch.float32)
     n = _seqs(cu_seqlens, B)
     if o is None:
-        o = torch.empty((B, T, H, V), device=q.device, dtype=q.dtype)
-    _cuda(o, "o", q.dtype)
+        o = torch.empty((B, T, H, V), device=q.device, dtype=o_dtype or q.dtype)
+    _cuda(o, "o")
     if final_state is None and output_final_state:
         N = n if cu_seqlens is not None else B
         final_state = torch.empty((N, H, K, V), device=q.device, dtype=torch.float32)
@@ -203,5 +206,6 @@ def kda_recurrent_fwd(q, k, v, gate, beta, initial_state=None, output_final_stat
     lib = load_library()
     _check("kda_recurrent_fwd", lib.kda_recurrent_fwd(
         _ptr(q), _ptr(k), _ptr(v), dt, _ptr(gate), _ptr(beta), _ptr(initial_state),
-        _ptr(final_state), _ptr(cu_seqlens), n, B, T, H, K, V, _ptr(o), _stream(stream)))
+        _ptr(final_state), _ptr(cu_seqlens), n, B, T, H, K, V, _ptr(o), _dt(o, "o"),
+        _stream(stream)))
     return o, final_state

@@ -88,6 +88,7 @@ size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K
     if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(K) || !head_dim_ok(V)) return 0;
     if (chunk_size != 32 && chunk_size != 64) return 0;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return 0;
+    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size)) return 0;
     bool packed = n_seqs > 0;
     int N = packed ? n_seqs : B;
     return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
@@ -98,7 +99,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          const float* dt_bias, kda_gate_mode mode, float lower_bound,
                          const void* beta, const float* initial_state, float* final_state,
                          const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
-                         int V, int chunk_size, void* o, void* workspace,
+                         int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                          size_t workspace_bytes, kda_stream_t stream) {
     g_last_error.clear();
     int N = 0;
@@ -106,6 +107,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
     if (st != KDA_OK) return st;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
     if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
+    if (o_dtype != qkv_dtype && o_dtype != KDA_F32)
+        return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
     if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
     if (chunk_size != 32 && chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 32 or 64");
     if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) return fail(KDA_ERR_INVALID_ARG, "gate mode");
@@ -129,19 +132,24 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
         return fail(KDA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,
                    (int)mode, lower_bound, initial_state, final_state, cu_seqlens, N, B, T, H, K,
-                   V, chunk_size, o, workspace, workspace_bytes, (cudaStream_t)stream};
+                   V, chunk_size, o, o_dtype == KDA_F32, workspace, workspace_bytes,
+                   (cudaStream_t)stream};
+    if (kda::fused_supported(a)) return cuda_status(kda::launch_chunk_fused(a));
     return cuda_status(kda::launch_chunk_precise(a));
 }
 
 kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                              const float* gate, const void* beta, const float* initial_state,
                              float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
-                             int T, int H, int K, int V, void* o, kda_stream_t stream) {
+                             int T, int H, int K, int V, void* o, kda_dtype o_dtype,
+                             kda_stream_t stream) {
     g_last_error.clear();
     int N = 0;
     kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
     if (st != KDA_OK) return st;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
+    if (o_dtype != qkv_dtype && o_dtype != KDA_F32)
+        return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
     if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
     const bool any_tokens = (long long)B * T > 0 && N > 0;
     if (any_tokens && (!q || !k || !v || !gate || !beta || !o))
@@ -151,7 +159,7 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
         if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;
     kda::RecArgs a{q, k, v, gate, beta, qkv_dtype == KDA_BF16, initial_state, final_state,
-                   cu_seqlens, N, B, T, H, K, V, o, (cudaStream_t)stream};
+                   cu_seqlens, N, B, T, H, K, V, o, o_dtype == KDA_F32, (cudaStream_t)stream};
     return cuda_status(kda::launch_recurrent(a));
 }
 

@@ -260,13 +260,13 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
 }
 
 // a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows
-template <typename InT, int C>
+template <typename InT, typename OutT, int C>
 __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
                                                   const float* __restrict__ G,
                                                   const float* __restrict__ Aqk,
                                                   const float* __restrict__ hc,
                                                   const float* __restrict__ vn, ChunkMap cm,
-                                                  int H, int K, int V, InT* __restrict__ o) {
+                                                  int H, int K, int V, OutT* __restrict__ o) {
     __shared__ float qg[C][DT + 1];
     __shared__ float As[C][C + 1];
     int n, t0, len, bos, eos;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
     }
 #pragma unroll
     for (int i = 0; i < C; ++i)
-        if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<InT>(acc[i]);
+        if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<OutT>(acc[i]);
 }
 
 template <typename InT, int C>
@@ -348,9 +348,14 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
         default:
             return cudaErrorInvalidValue;
     }
-    if (slots > 0)
-        out_kernel<InT, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn,
-                                                                   cm, a.H, a.K, a.V, (InT*)a.o);
+    if (slots > 0) {
+        if (a.o_f32)
+            out_kernel<InT, float, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, (float*)a.o);
+        else
+            out_kernel<InT, InT, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, (InT*)a.o);
+    }
     return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@ struct FwdArgs {
     int N;  // logical sequences (B when dense)
     int B, T, H, K, V, C;
     void* o;
+    bool o_f32;  // o is float32 (else the qkv dtype)
     void* ws;
     size_t ws_bytes;
     cudaStream_t stream;
@@ -57,6 +58,7 @@ struct RecArgs {
     int N;
     int B, T, H, K, V;
     void* o;
+    bool o_f32;  // o is float32 (else the qkv dtype)
     cudaStream_t stream;
 };
 
@@ -66,5 +68,10 @@ cudaError_t launch_recurrent(const RecArgs& a);
 // float32 SIMT chunked path: stage-by-stage kernels with a device workspace
 size_t precise_workspace_bytes(int B, int T, int H, int K, int V, int C, int N, bool packed);
 cudaError_t launch_chunk_precise(const FwdArgs& a);
+
+// bf16 fused single-kernel path (tcgen05 / TMEM / TMA); needs no workspace
+bool fused_supported(const FwdArgs& a);
+bool fused_supported_dims(bool qkv_bf16, int K, int V, int C);
+cudaError_t launch_chunk_fused(const FwdArgs& a);
 
 }  // namespace kda

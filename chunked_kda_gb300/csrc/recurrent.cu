@@ -51,11 +51,11 @@ __device__ __forceinline__ void st_vec(float* p, const float* r) {
     }
 }
 
-template <typename InT, int K, int BV>
+template <typename InT, typename OutT, int K, int BV>
 __global__ void __launch_bounds__(256) recurrent_kernel(
     const InT* __restrict__ q, const InT* __restrict__ k, const InT* __restrict__ v,
     const float* __restrict__ gate, const InT* __restrict__ beta, const float* h0, float* hT,
-    const int32_t* __restrict__ cu, int T, int H, int V, InT* __restrict__ o) {
+    const int32_t* __restrict__ cu, int T, int H, int V, OutT* __restrict__ o) {
     constexpr int RPW = K / 8;    // state rows per warp
     constexpr int VPT = BV / 32;  // value columns per lane
     __shared__ float s_q[K], s_k[K], s_dec[K];
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) recurrent_kernel(
             float acc = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) acc += s_red[w][i];
-            o[v_off + i] = from_f32<InT>(acc * scale);
+            o[v_off + i] = from_f32<OutT>(acc * scale);
         }
     }
 
@@ -165,9 +165,14 @@ __global__ void __launch_bounds__(256) recurrent_kernel(
 template <typename InT, int K, int BV>
 static cudaError_t launch_rec_t(const RecArgs& a) {
     dim3 grid(a.V / BV, a.H, a.N);
-    recurrent_kernel<InT, K, BV><<<grid, 256, 0, a.stream>>>(
-        (const InT*)a.q, (const InT*)a.k, (const InT*)a.v, a.gate, (const InT*)a.beta, a.h0,
-        a.hT, a.cu, a.T, a.H, a.V, (InT*)a.o);
+    if (a.o_f32)
+        recurrent_kernel<InT, float, K, BV><<<grid, 256, 0, a.stream>>>(
+            (const InT*)a.q, (const InT*)a.k, (const InT*)a.v, a.gate, (const InT*)a.beta, a.h0,
+            a.hT, a.cu, a.T, a.H, a.V, (float*)a.o);
+    else
+        recurrent_kernel<InT, InT, K, BV><<<grid, 256, 0, a.stream>>>(
+            (const InT*)a.q, (const InT*)a.k, (const InT*)a.v, a.gate, (const InT*)a.beta, a.h0,
+            a.hT, a.cu, a.T, a.H, a.V, (InT*)a.o);
     return cudaGetLastError();
 }
 

@@ -123,7 +123,8 @@ size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K
  *   g          [B, T, H, K], dtype g_dtype (raw gate in SAFE mode, the
  *              natural-log decay in PRE mode)
  *   beta       [B, T, H], dtype qkv_dtype, post-sigmoid
- *   o          [B, T, H, V], dtype qkv_dtype (output)
+ *   o          [B, T, H, V], dtype o_dtype (output): the qkv dtype, or KDA_F32
+ *              to keep the forward's FP32 result without the final rounding
  *   chunk_size 32 or 64 (Helion PR #3290: the two chunk sizes FLA's KDA accepts)
  *   K, V       64, 128 or 256 (K == V on the bf16 tensor-core path; any pair
  *              of these on the float32 path)
@@ -136,7 +137,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          const float* dt_bias, kda_gate_mode mode, float lower_bound,
                          const void* beta, const float* initial_state, float* final_state,
                          const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
-                         int V, int chunk_size, void* o, void* workspace,
+                         int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                          size_t workspace_bytes, kda_stream_t stream);
 
 /*
@@ -146,7 +147,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
  *
  *   gate       [B, T, H, K] float32: per-token LOG2 decay (S rows scale by
  *              2^gate), e.g. kda_gate_fwd(..., chunk_size = 1, ...)
- *   q, k, v, beta, o, states, cu_seqlens: as for kda_chunk_fwd.
+ *   q, k, v, beta, o, o_dtype, states, cu_seqlens: as for kda_chunk_fwd.
  *   K, V       64, 128 or 256 (any pair).
  * final_state may alias initial_state (in-place decode): each program reads
  * its whole state block before it writes any of it.
@@ -154,7 +155,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
 kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                              const float* gate, const void* beta, const float* initial_state,
                              float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
-                             int T, int H, int K, int V, void* o, kda_stream_t stream);
+                             int T, int H, int K, int V, void* o, kda_dtype o_dtype,
+                             kda_stream_t stream);
 
 /* static, NUL-terminated description of a status code */
 const char* kda_status_string(kda_status status);

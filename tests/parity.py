@@ -3,7 +3,12 @@
 Tolerances (always against the float64 oracle on the exact quantised inputs):
   float32 inputs: rel-L2 <= 1e-4 on o and on the final state;
   bf16 inputs:    rel-L2 <= 2e-2 on o and on the final state, and
-                  max |o - o_ref| <= 5e-2 * RMS(o_ref).
+                  max |o - o_ref| <= 5e-2 * RMS(o_ref) for the forward's value.
+When o is stored in bf16, the storage rounding adds up to half a bf16 ulp,
+2^-8 |o|, to each element on top of the forward's own error (it is at most
+2^-8 max|o|, which alone exceeds 5e-2 RMS wherever max|o| > 12.8 RMS), so a
+bf16 o is held to |o - o_ref| <= 5e-2 RMS (1 + 2^-8) + 2^-8 |o_ref| element by
+element; a float32 o from bf16 inputs is held to the plain bound.
 """
 from __future__ import annotations
 
@@ -25,8 +30,13 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_o(o_gpu, o_ref, dtype, mask=None, what="o"):
-    """Compare an output tensor (valid rows only when ``mask`` is given)."""
+def check_o(o_gpu, o_ref, dtype, mask=None, what="o", out_bf16=None):
+    """Compare an output tensor (valid rows only when ``mask`` is given).
+
+    ``dtype`` is the input dtype; ``out_bf16`` says whether o was stored in bf16
+    (taken from o_gpu's dtype when o_gpu is a tensor)."""
+    if out_bf16 is None:
+        out_bf16 = isinstance(o_gpu, torch.Tensor) and o_gpu.dtype == torch.bfloat16
     a = to_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu)
     b = np.asarray(o_ref)
     if mask is not None:
@@ -39,8 +49,15 @@ def check_o(o_gpu, o_ref, dtype, mask=None, what="o"):
         assert e <= BF16_REL, f"{what}: rel-L2 {e:.3e} > {BF16_REL}"
         if what.startswith("o") and b.size:
             rms = float(np.sqrt(np.mean(b * b)))
-            mx = float(np.abs(a - b).max())
-            assert mx <= BF16_MAXABS_RMS * rms, f"{what}: max-abs {mx:.3e} > 5e-2*RMS {rms:.3e}"
+            d = np.abs(a - b)
+            if out_bf16:
+                excess = float((d - 2.0 ** -8 * np.abs(b)).max())
+                bound = BF16_MAXABS_RMS * rms * (1 + 2.0 ** -8)
+                assert excess <= bound, (f"{what}: max(|o-o_ref| - 2^-8|o_ref|) {excess:.3e} > "
+                                         f"5e-2*RMS {rms:.3e}")
+            else:
+                mx = float(d.max())
+                assert mx <= BF16_MAXABS_RMS * rms, f"{what}: max-abs {mx:.3e} > 5e-2*RMS {rms:.3e}"
     return e
 
 

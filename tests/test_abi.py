@@ -34,9 +34,9 @@ def lib():
     L = ctypes.CDLL(path)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
-                                i32, i32, i32, i32, i32, i32, vp, vp, ctypes.c_size_t, vp]
+                                i32, i32, i32, i32, i32, i32, vp, i32, vp, ctypes.c_size_t, vp]
     L.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
-                                    i32, vp, vp]
+                                    i32, vp, i32, vp]
     L.kda_gate_fwd.argtypes = [vp, i32, vp, vp, i32, f32, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     L.kda_chunk_workspace_bytes.argtypes = [i32] * 8
     L.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
@@ -77,25 +77,29 @@ P = ctypes.c_void_p(4096)  # aligned stand-in: never dereferenced, validation fa
 def _chunk(lib, **kw):
     a = dict(q=P, k=P, v=P, dt=BF16, g=P, gdt=BF16, A_log=P, dt_bias=None, mode=1, lb=-5.0,
              beta=P, h0=None, hT=None, cu=None, n=0, B=1, T=64, H=2, K=128, V=128, C=64, o=P,
-             ws=None, ws_bytes=0)
+             odt=None, ws=None, ws_bytes=0)
     a.update(kw)
+    if a["odt"] is None:
+        a["odt"] = a["dt"]
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["dt"], a["g"], a["gdt"], a["A_log"],
                              a["dt_bias"], a["mode"], a["lb"], a["beta"], a["h0"], a["hT"],
                              a["cu"], a["n"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
-                             a["o"], a["ws"], a["ws_bytes"], None)
+                             a["o"], a["odt"], a["ws"], a["ws_bytes"], None)
 
 
 def test_chunk_host_validation(lib):
     assert _chunk(lib, C=48) == UNSUPPORTED
     assert _chunk(lib, K=96) == UNSUPPORTED
     assert _chunk(lib, dt=7) == UNSUPPORTED
+    assert _chunk(lib, dt=F32, odt=BF16) == UNSUPPORTED  # float32 inputs write float32 o
     assert _chunk(lib, lb=-5.5) == INVALID
     assert _chunk(lib, lb=0.0) == INVALID
     assert _chunk(lib, A_log=None) == INVALID
     assert _chunk(lib, q=None) == INVALID
     assert _chunk(lib, o=ctypes.c_void_p(4098)) == INVALID  # misaligned
     assert _chunk(lib, B=2, cu=P, n=1) == INVALID  # packed needs B == 1
-    assert _chunk(lib, ws=None, ws_bytes=0) == INVALID  # workspace too small
+    # workspace too small (the float32 path needs one; bf16 K=V=128 C=64 needs none)
+    assert _chunk(lib, dt=F32, ws=None, ws_bytes=0) == INVALID
     assert b"workspace" in lib.kda_last_error()
     assert _chunk(lib, H=0) == INVALID
     # nothing to do: zero logical sequences is OK and launches nothing
@@ -105,9 +109,10 @@ def test_chunk_host_validation(lib):
 
 def test_recurrent_and_gate_host_validation(lib):
     r = lib.kda_recurrent_fwd(P, P, P, BF16, None, P, None, None, None, 0, 1, 4, 2, 128, 128, P,
-                              None)
+                              BF16, None)
     assert r == INVALID  # null gate
-    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 100, 128, P, None)
+    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 100, 128, P, BF16,
+                              None)
     assert r == UNSUPPORTED
     g = lib.kda_gate_fwd(P, BF16, None, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, P, None)
     assert g == INVALID  # safe gate without A_log
@@ -134,3 +139,6 @@ def test_workspace_bytes(lib):
                                    slots * H * K * V))
     assert lib.kda_chunk_workspace_bytes(F32, 1, T, H, K, V, C, n) == want
     assert lib.kda_chunk_workspace_bytes(F32, 1, T, H, K, V, 48, 0) == 0
+    # the fused bf16 kernel keeps every intermediate on chip
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) > 0

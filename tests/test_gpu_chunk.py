@@ -56,13 +56,16 @@ def test_tiny_fp32_workload():
     compare(w, o, st)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dtype,o_dtype", [(torch.float32, None), (torch.bfloat16, None),
+                                           (torch.bfloat16, torch.float32)],
+                         ids=["f32", "bf16", "bf16-f32out"])
 @pytest.mark.parametrize("C", [32, 64])
 @pytest.mark.parametrize("T", [1, 17, 64, 65, 130, 200])
 @pytest.mark.parametrize("D", [64, 128])
-def test_dense_small(dtype, C, T, D):
+def test_dense_small(dtype, o_dtype, C, T, D):
     w = workloads.make_dense("t", 2, T, 2, D, D, C, dtype, 11 + T + D, state_std=0.05)
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
+    assert o.dtype == (o_dtype or dtype)
     compare(w, o, st)
 
 
@@ -207,9 +210,12 @@ def _sample_units(w, k=4, seed=0):
                                   "dense_bf16_b4_t4096_h64_d128",
                                   "dense_bf16_b8_t2048_h32_d256"])
 def test_full_size_sampled(name):
-    """The full workloads, in the configuration bench.py times, checked on sampled
-    (sequence, head) units the oracle computes one by one."""
+    """The full workloads, in the configuration bench.py times (bf16 o), and with a
+    float32 o, checked on sampled (sequence, head) units the oracle computes one by one."""
     w = workloads.make(name, device="cpu")
-    o, st = run_gpu(w)
-    assert torch.isfinite(o[torch.from_numpy(valid_mask(w)).cuda()]).all()
-    check_units(w, o, st, _sample_units(w))
+    units = _sample_units(w)
+    for o_dtype in (None, torch.float32):
+        o, st = run_gpu(w, o_dtype=o_dtype)
+        assert torch.isfinite(o[torch.from_numpy(valid_mask(w)).cuda()]).all()
+        check_units(w, o, st, units)
+        del o, st
