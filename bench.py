@@ -228,7 +228,7 @@ def run_ours(args, world, rank, local):
     kda.load_library()
     peaks, peak_src = load_peaks()
 
-    w = workloads.make(WORKLOAD, device=dev)
+    w = workloads.make(args.workload, device=dev)
     B, T, H, K, V, C = w.B, w.T, w.H, w.K, w.V, w.chunk_size
     stream = torch.cuda.current_stream()
     o = torch.empty((B, T, H, V), device=dev, dtype=torch.bfloat16)
@@ -260,6 +260,13 @@ def run_ours(args, world, rank, local):
     head_tokens = B * T * H
     t_max, units_all = aggregate(local_s, head_tokens * args.steps, world, dev)
     ms_per_step = 1e3 * t_max / args.steps
+
+    if args.chunk_only:
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "ms_per_step": ms_per_step,
+                              "head_tokens_per_s": units_all / t_max}), flush=True)
+        return
 
     # end to end through the public API: pinned host inputs -> device, forward, o -> host
     names = ("q", "k", "v", "g", "beta")
@@ -327,7 +334,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "K": K, "V": V, "chunk_size": C,
+        "config": {"workload": args.workload, "B": B, "T": T, "H": H, "K": K, "V": V, "chunk_size": C,
                    "gate": "safe, lower_bound -5", "initial_state": None,
                    "output_final_state": False, "l2": "inputs (1.34 GB) larger than L2",
                    "parallelism": f"replicas x{world}"},
@@ -349,7 +356,7 @@ def run_ours(args, world, rank, local):
         cores = host_cores()
         tok, dt = oracle_sample(w, 2 * cores, cores, seed=1234)
         line["cpu_baseline"] = {"value": tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{2 * cores} random (sequence, head) units of {WORKLOAD} "
+                                "sample": f"{2 * cores} random (sequence, head) units of {args.workload} "
                                           f"({w.T} tokens each), float64, one OpenMP thread "
                                           f"per unit"}
     print(json.dumps(line), flush=True)
@@ -370,6 +377,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="dense workload name (chunked_kda_gb300.workloads); default is the one "
+                         "the metric is quoted on")
+    ap.add_argument("--chunk-only", action="store_true",
+                    help="time the chunked forward only (no e2e, decode or CPU leg); for profiling")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
