@@ -14,11 +14,13 @@ import threading
 
 import torch
 
-__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_recurrent_fwd",
-           "KdaError", "GATE_PRE", "GATE_SAFE", "library_path", "load_library"]
+__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_chunk_fwd_noalloc",
+           "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE", "NOALLOC_SCRATCH_BYTES",
+           "library_path", "load_library"]
 
 GATE_PRE = 0
 GATE_SAFE = 1
+NOALLOC_SCRATCH_BYTES = 16 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 _F32, _BF16 = 0, 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -58,6 +60,10 @@ def load_library():
                                       ctypes.c_size_t, vp]
         lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, vp, i32, vp]
+        lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
+                                              vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32,
+                                              vp]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         for fn in (lib.kda_gate_fwd, lib.kda_chunk_fwd, lib.kda_recurrent_fwd):
             fn.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -177,6 +183,34 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
         lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n, B,
         T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes,
         _stream(stream)))
+    return o, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE,
+                          lower_bound=-5.0, initial_state=None, cu_seqlens=None, chunk_size=64,
+                          o=None, final_state=None, stream=None):
+    """The chunked forward without a workspace, for callers that cannot allocate device
+    memory: the library's fixed scratch array (NOALLOC_SCRATCH_BYTES per device) stands in
+    for it.  ``o`` and ``final_state`` must be passed preallocated (so this call allocates
+    nothing); ``final_state`` may be None.  Returns (o, final_state)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("o", o)):
+        if t is None:
+            raise ValueError(f"{name} is required")
+        _cuda(t, name)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError("q, k, v and beta must share one dtype")
+    _cuda(A_log, "A_log", torch.float32)
+    _cuda(dt_bias, "dt_bias", torch.float32)
+    _cuda(initial_state, "initial_state", torch.float32)
+    _cuda(final_state, "final_state", torch.float32)
+    n = _seqs(cu_seqlens, B)
+    lib = load_library()
+    _check("kda_chunk_fwd_noalloc", lib.kda_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _dt(q, "q"), _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias),
+        mode, lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens),
+        n, B, T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _stream(stream)))
     return o, final_state
 
 

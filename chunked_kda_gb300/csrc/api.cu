@@ -44,6 +44,10 @@ kda_status check_layout(const int32_t* cu, int n_seqs, int B, int T, int H, int*
 
 }  // namespace
 
+namespace kda {
+void record_error(const char* msg) { g_last_error = msg; }
+}  // namespace kda
+
 extern "C" {
 
 const char* kda_status_string(kda_status s) {

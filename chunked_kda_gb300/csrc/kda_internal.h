@@ -74,4 +74,7 @@ bool fused_supported(const FwdArgs& a);
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
 
+// sets the message kda_last_error() returns on this host thread
+void record_error(const char* msg);
+
 }  // namespace kda

@@ -141,6 +141,43 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * Chunked forward for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  Some callers only
+ * receive input and output pointers and may not call cudaMalloc: a plugin or
+ * callback inside a host framework that owns all device memory, code running
+ * under an allocator or capture mode that forbids new allocations, or an
+ * embedded caller with a fixed memory budget.  kda_chunk_fwd needs a
+ * caller-allocated workspace; this entry point instead runs the float32
+ * stage-by-stage chunked path (for any input dtype) on a fixed scratch array
+ * of KDA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  It allocates
+ * nothing and calls no allocating routine.
+ *
+ *   Arguments, layouts and results: as for kda_chunk_fwd, without the
+ *   workspace.  Sizes whose scratch would exceed KDA_NOALLOC_SCRATCH_BYTES
+ *   (kda_chunk_workspace_bytes(KDA_F32, ...) of the same sizes, roughly 3.8 KB
+ *   per token and head at K = V = 128, C = 64) are rejected with
+ *   KDA_ERR_INVALID_ARG before anything is enqueued.
+ *   Set-up: the first call on each device looks up the scratch array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Sharing: every call on a device uses the same scratch array and it keeps
+ *   the last call's contents (each call writes every byte it reads, so nothing
+ *   needs clearing); calls whose kernels overlap on the GPU, e.g. from two
+ *   streams or two host threads, race on it and must be serialised.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                 const void* g, kda_dtype g_dtype, const float* A_log,
+                                 const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                                 const void* beta, const float* initial_state, float* final_state,
+                                 const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                                 int V, int chunk_size, void* o, kda_dtype o_dtype,
+                                 kda_stream_t stream);
+
+/*
  * Token-sequential KDA forward (decode and short prefill), attention-gym PR
  * #317: one program per (sequence, head, value block) scans the tokens with
  * its FP32 state block in registers and computes in FP32 for any input dtype.
