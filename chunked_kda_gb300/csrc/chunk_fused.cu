@@ -1,9 +1,9 @@
 // Fused chunked KDA forward for bf16 inputs, K = V = 128, C = 64 (sm_103a).
 //
-// One CTA per (sequence, head) walks the sequence chunk by chunk; the FP32
-// state stays on chip for the whole sequence, so HBM sees only q, k, v, g,
-// beta, o and the states.  Per chunk of 64 tokens (all steps of the chunked
-// form, FLA skill "fla-kda", "Public code map"):
+// One CTA of 512 threads per (sequence, head) walks the sequence chunk by
+// chunk; the FP32 state never leaves the SM, so HBM sees only q, k, v, g,
+// beta, o and the states.  Steps per chunk of 64 tokens (FLA skill "fla-kda",
+// "Public code map": gate, intra, inter/solve, WY, state, output):
 //   a1 gate activation + chunk-local cumsum in log2 units (FLA skill "fla-kda",
 //      "Gate modes", "Safe gate numerical note": RCP_LN2 before exp2)
 //   a2 causal scores on 16-token sub-blocks, one tcgen05 MMA of N = 160: the
@@ -16,22 +16,35 @@
 //      the column factor is the paired product 2^(G_m(row) - G_m(col)) *
 //      2^(G_m(col) - G_j), whose first term is <= 1 (FLA skill "fla-kda",
 //      "Safe gate numerical note").
-//   a3 T = (I + Akk)^-1 in FP32: 16 x 16 diagonal blocks by forward
-//      substitution, then the off-diagonal blocks level by level
+//   a3 T = (I + Akk)^-1: 16 x 16 diagonal blocks by forward substitution in
+//      FP32, the off-diagonal blocks level by level with warp-level tf32 MMAs
 //   a4/a5 the WY terms and the state step as tcgen05 MMAs, with the state
 //      transposed (TMEM lane = value channel v):
-//        Y^T   = h^T (k 2^G)^T                      [V x C]
-//        vn^T  = v^T (T diag beta)^T - Y^T (T diag beta)^T      (v_new)
-//        dH^T  = vn^T (k 2^(Glast - G))             [V x K]
-//        h^T  <- h^T Diag(2^Glast) + dH^T           (FP32, registers)
-//   a6 o^T = h^T (s q 2^G)^T + vn^T Aqk^T           [V x C]
+//        Y^T   = h^T (k 2^G)^T                               [V x C]
+//        vn^T  = v^T (T diag beta)^T - Y^T (T diag beta)^T   (v_new)
+//        dH^T  = vn^T (k 2^(Glast - G))                      [V x K]
+//        h^T  <- h^T Diag(2^Glast) + dH^T                    (FP32, registers)
+//   a6 o^T = h^T (s q 2^G)^T + vn^T Aqk^T                    [V x C]
 // Rows beyond the end of a sequence are masked to zero before any product.
 //
-// Precision: every product runs on bf16 operands with FP32 accumulation; the
-// operands whose rounding dominates the output error are carried as a bf16
-// pair x = hi + lo (hi = bf16(x), lo = bf16(x - hi), about 16 significant
-// bits) and multiplied as hi*B + lo*B (+ A*lo): the score rows, v_new and Aqk.
+// Warp roles.  Warps 0-7 ("prep") build everything chunk c needs that does
+// not depend on the state: gate, cumsum, exponent anchors, score operands,
+// the score MMA, Akk / Aqk, the solve, and the hand-off operands (k 2^G,
+// s q 2^G, k 2^(Gl-G), T diag(beta), Aqk, 2^Glast).  Warps 8-15 ("chain")
+// run the state step of the previous chunk at the same time: their operands
+// h^T, Y^T and v_new^T live in TMEM as MMA A operands, the state in
+// registers.  The groups hand buffers to each other through mbarriers; a
+// buffer the chain has finished with is released by the commit of the MMA
+// that read it.  Every mbarrier wait is bounded: a wait that gives up counts
+// a timeout, after which the CTA skips all further waits, MMAs and copies,
+// runs out its loop, drains the MMAs in flight and frees TMEM.
+//
+// Precision: bf16 operands, FP32 accumulation; the score rows, v_new and Aqk
+// are carried as bf16 pairs x = hi + lo (hi = bf16(x), lo = bf16(x - hi))
+// and multiplied as hi*B + lo*B (+ A*lo), about 16 significant bits.
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kda_internal.h"
@@ -45,37 +58,53 @@ namespace fused {
 
 using namespace sm100;
 
-constexpr int C = 64, KD = 128, VD = 128, NTHR = 256;
+constexpr int C = 64, KD = 128, VD = 128;
+constexpr int NTHR = 512, NGRP = 256;            // two groups of 8 warps
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;  // named barriers of the groups
+
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_V = 0;         // v tile (TMA) = MN-major A of v^T            16 KB
-constexpr uint32_t OFF_SAH = 16384;   // score rows hi [128 ch][128 rows] MN-major    32 KB
-constexpr uint32_t OFF_SAL = 49152;   // score rows lo                                32 KB
-constexpr uint32_t OFF_SB = 81920;    // score cols [160][128 ch] K-major             40 KB
-constexpr uint32_t OFF_AQKH = 16384;  //   after the scores: Aqk hi [64][64]  (alias)  8 KB
-constexpr uint32_t OFF_AQKL = 24576;  //   Aqk lo                            (alias)  8 KB
-constexpr uint32_t OFF_TP = 32768;    //   T diag(beta) bf16 [64][64]        (alias)  8 KB
-constexpr uint32_t OFF_YA = 40960;    //   Y^T, then v_new^T hi [128][64]    (alias) 16 KB
-constexpr uint32_t OFF_VNL = 57344;   //   v_new^T lo                        (alias) 16 KB
-constexpr uint32_t OFF_AS = 73728;    //   Akk fp32 [64][65]                 (alias)
-constexpr uint32_t OFF_TF = 90368;    //   T fp32 [64][65]                   (alias)
-constexpr uint32_t OFF_XS = 107008;   //   block products fp32 [3][16][17]   (alias)
-constexpr uint32_t OFF_KG = 122880;   // k 2^G        [128 ch][64 tok]                 16 KB
-constexpr uint32_t OFF_QG = 139264;   // s q 2^G      [128 ch][64 tok]                 16 KB
-constexpr uint32_t OFF_KD = 155648;   // k 2^(Gl-G)   [128 ch][64 tok]                 16 KB
-constexpr uint32_t OFF_HA = 172032;   // h^T bf16 [128 v][128 ch] K-major              32 KB
-constexpr uint32_t OFF_XCH = 204800;  // fp32 [4][128] per-sub-block sums of the gate
-constexpr uint32_t OFF_GM = 206848;   // fp32 [4][128] G at the sub-block midpoints
-constexpr uint32_t OFF_GL = 208896;   // fp32 [128] G at the last row
-constexpr uint32_t OFF_GAM = 209408;  // fp32 [128] 2^G at the last row
-constexpr uint32_t OFF_BETA = 209920; // fp32 [64]
-constexpr uint32_t OFF_BAR = 210176;  // 2 mbarriers
-constexpr uint32_t OFF_MISC = 210192; // tmem base, abort flag
-constexpr uint32_t SMEM_BYTES = 210208 + 1024;  // + alignment slack
-constexpr int LD = 65;                // fp32 row stride of the solve matrices
+constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T          [chain]
+constexpr uint32_t OFF_GT = 16384;     // g tile (TMA, bf16 gate only), 16 KB               [prep]
+constexpr uint32_t OFF_SAH = 32768;    // score rows hi [128 ch][128 rows] MN-major      [prep]
+constexpr uint32_t OFF_SAL = 65536;    // score rows lo
+constexpr uint32_t OFF_SB = 98304;     // score cols [160][128 ch] K-major, 40 KB
+constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
+constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
+constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [3][16][24]
+constexpr uint32_t OFF_KG = 139264;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
+                                       //   before that, the next chunk's k tile (TMA)
+constexpr uint32_t OFF_QG = 155648;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
+                                       //   before that, the next chunk's q tile (TMA)
+constexpr uint32_t OFF_KD = 172032;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
+constexpr uint32_t OFF_TP = 188416;    // hand-off: T diag(beta) bf16 [64][64] K-major B
+constexpr uint32_t OFF_AQKH = 196608;  // hand-off: Aqk hi [64][64]
+constexpr uint32_t OFF_AQKL = 204800;  // hand-off: Aqk lo [64][64]
+constexpr uint32_t OFF_GAM = 212992;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
+constexpr uint32_t OFF_BETA = 214016;  // prep: beta fp32 [64]
+constexpr uint32_t OFF_XCH = 214272;   // prep: fp32 [4][128] per-sub-block gate sums
+constexpr uint32_t OFF_GM = 216320;    // prep: fp32 [4][128] G at the sub-block midpoints
+constexpr uint32_t OFF_GL = 218368;    // prep: fp32 [128] G at the last row
+constexpr uint32_t OFF_BAR = 218880;   // mbarriers (8 bytes each)
+constexpr uint32_t OFF_MISC = 218976;  // tmem base, abort flag
+constexpr uint32_t SMEM_BYTES = 218992 + 1024;  // + alignment slack
+constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
+                                       // of 8 rows x 4 columns then touch 32 distinct banks)
+
+// mbarriers (each completes once per chunk, the v tiles once per two chunks)
+enum {
+    B_VFULL = 0, B_QKIN, B_GIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
+    B_DRAIN0, B_DRAIN1, NBAR
+};
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_Y = 160, TM_O = 224, TM_VN = 288, TM_DH = 352, TM_COLS = 512;
-constexpr int SB_ROWS = 160;                     // score columns (causal only)
+constexpr uint32_t TM_S = 0;     // scores [128 lanes][160]                          (prep)
+constexpr uint32_t TM_Y = 160;   // Y^T [128][64]; then v_new^T hi (160..191), lo (192..223)
+constexpr uint32_t TM_O = 224;   // o^T [128][64]
+constexpr uint32_t TM_VN = 288;  // v_new^T accumulator [128][64]; holds h^T (bf16) between chunks
+constexpr uint32_t TM_DH = 352;  // dH^T [128][128]
+constexpr uint32_t TM_YA = 480;  // Y^T bf16 [128][64] packed in 32 columns
+constexpr uint32_t TM_COLS = 512;
+constexpr int SB_ROWS = 160;                                                   // causal columns
 __host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -83,7 +112,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&p);
 }
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 // x = hi + lo: hi = bf16(x), lo = bf16(x - hi), for the pair (a, b)
 __device__ __forceinline__ void pack_split(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -98,6 +126,7 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 template <>
 __device__ __forceinline__ float to_out<float>(float x) { return x; }
+
 __device__ __forceinline__ void st_s32(uint32_t a, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
@@ -105,6 +134,7 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
                  : "memory");
 }
+
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
@@ -130,11 +160,12 @@ struct GatePair<float> {
     }
 };
 
-// per-token decay in log2 units
-__device__ __forceinline__ float gate_log2(float g, float expA, float dtb, int mode, float lb) {
+// per-token decay in log2 units: mode 0 pre-gated (a = g), mode 1 safe
+// (a = lb * sigmoid(expA * (g + dtb)), with sigmoid(z) = 1 / (1 + 2^(-z log2 e)))
+__device__ __forceinline__ float gate_log2(float g, float expA, float dtb, int mode, float lbl2) {
     if (mode == 0) return g * kLog2e;
-    float z = expA * (g + dtb);
-    return (lb * kLog2e) * __frcp_rn(1.0f + __expf(-z));
+    const float z = expA * (g + dtb);
+    return lbl2 * rcp_fast(1.0f + ex2_fast(-z * kLog2e));
 }
 
 struct Params {
@@ -153,13 +184,29 @@ struct Params {
     int T, H;
 };
 
-template <typename GT, typename OT>
-__global__ void __launch_bounds__(NTHR, 1)
-chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    const uint32_t sb = smem_u32(smem);
+struct Sync {
+    uint32_t bars;
+    volatile uint32_t* abort_flag;
+    __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * i; }
+    // bounded wait; after any timeout the CTA stops waiting
+    __device__ __forceinline__ void wait(int i, uint32_t parity) const {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar(i), parity)) {
+            atomicAdd(&g_fused_timeouts, 1u);
+            *abort_flag = 1u;
+        }
+    }
+    __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
+};
+
+// ------------------------------------------------------------------ prep group
+template <typename GT>
+__device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
+                                          const Sync& sy, const CUtensorMap* tm_g, int h, long bos,
+                                          long eos, int nt) {
+    constexpr bool kGateTile = std::is_same<GT, __nv_bfloat16>::value;  // g arrives by TMA
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int H = p.H;
     float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
     float* gmid = reinterpret_cast<float*>(smem + OFF_GM);
     float* glast = reinterpret_cast<float*>(smem + OFF_GL);
@@ -168,36 +215,8 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
     float* Tf = reinterpret_cast<float*>(smem + OFF_TF);
     float* Xs = reinterpret_cast<float*>(smem + OFF_XS);
-    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
-    const uint32_t bar_tma = sb + OFF_BAR, bar_mma = sb + OFF_BAR + 8;
 
-    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    const int h = blockIdx.y, n = blockIdx.x;
-    const int H = p.H;
-    long bos, eos;
-    if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
-    else      { bos = (long)n * p.T; eos = bos + p.T; }
-    const int nt = (int)((eos - bos + C - 1) / C);
-
-    if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
-        fence_mbar_init();
-        misc[1] = 0;
-        prefetch_tmap(&tm_v);
-    }
-    if (w == 0) tmem_alloc(sb + OFF_MISC, TM_COLS);
-
-    // ---- state: thread owns value channel v (TMEM lane) and key channels [64 ch, 64 ch + 64)
-    const int vlane = 32 * (w & 3) + l;
-    const int hch = w >> 2;
-    const size_t st_off = ((size_t)n * H + h) * (size_t)KD * VD;
-    float hs[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j)
-        hs[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + j) * VD + vlane) : 0.f;
-
-    // ---- prep mapping: channel pair (d0, d0 + 1), sub-block rq (rows 16 rq .. 16 rq + 15)
+    // channel pair (d0, d0 + 1), sub-block rq (rows 16 rq .. 16 rq + 15)
     const int cbp = w & 1;
     const int d0 = 2 * (32 * cbp + l);
     const int rq = w >> 1;
@@ -210,65 +229,72 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             dtb1 = __ldg(p.dt_bias + h * KD + d0 + 1);
         }
     }
+    const float lbl2 = p.lb * kLog2e;
     const float scale = rsqrtf((float)KD);
     const GT* gptr = reinterpret_cast<const GT*>(p.g);
+    const uint32_t sw_d0 = (uint32_t)((d0 & 63) >> 3), sw_b0 = (uint32_t)(d0 & 7) * 2;
+    // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
+    auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
 
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = misc[0];
-    uint32_t mma_phase = 0;
-    bool abort_ = false;
-
-    // write h^T (bf16) into the K-major A operand
-    auto write_hA = [&]() {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t a = sb + OFF_HA + hch * 16384 + sw128(vlane, c8);
-            st_s128(a, pack_bf16(hs[8 * c8 + 0], hs[8 * c8 + 1]), pack_bf16(hs[8 * c8 + 2], hs[8 * c8 + 3]),
-                    pack_bf16(hs[8 * c8 + 4], hs[8 * c8 + 5]), pack_bf16(hs[8 * c8 + 6], hs[8 * c8 + 7]));
-        }
+    // beta of the next chunk is loaded one chunk ahead (threads 0-63, one row each)
+    auto load_beta = [&](long t, int len_) {
+        return (tid < len_) ? __bfloat162float(p.beta[(size_t)(t + tid) * H + h]) : 0.f;
     };
-    write_hA();
+    float beta_next = (tid < C && nt > 0) ? load_beta(bos, (int)min((long)C, eos - bos)) : 0.f;
 
-    for (int c = 0; c < nt && !abort_; ++c) {
+    if (kGateTile && tid == 0 && nt > 0) {
+        mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
+        for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)bos, sy.bar(B_GIN));
+    }
+
+    for (int c = 0; c < nt; ++c) {
         const long t0 = bos + (long)c * C;
         const int len = (int)min((long)C, eos - t0);
 
-        // ---------------- phase 0: TMA v tile; gate of own rows meanwhile
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            mbar_arrive_expect_tx(bar_tma, 16384);
-            for (int cb = 0; cb < 2; ++cb)
-                tma_load_3d(sb + OFF_V + cb * 8192, &tm_v, 64 * cb, h, (int)t0, bar_tma);
+        // ---- gate of the own rows: from the g tile (bf16) or from global memory (float32)
+        float g0[16], g1[16];
+        if constexpr (kGateTile) {
+            sy.wait(B_GIN, c & 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t x = ld_s32(sb + OFF_GT + tile_off(16 * rq + i));
+                g0[i] = bf_lo(x);
+                g1[i] = bf_hi(x);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = min(16 * rq + i, len - 1);
+                GatePair<GT>::load(gptr + ((size_t)(t0 + r) * H + h) * KD + d0, g0[i], g1[i]);
+            }
         }
-        // gate of own rows while the tiles land (global loads)
+        if (tid < C) {
+            bsm[tid] = beta_next;
+            if (c + 1 < nt) beta_next = load_beta(t0 + C, (int)min((long)C, eos - t0 - C));
+        }
+
+        // ---- a1: gate, chunk-local cumsum (log2 units), sub-block carries
         float G0[16], G1[16];
         {
             float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int r = 16 * rq + i;
-                float a0 = 0.f, a1 = 0.f;
-                if (r < len) {
-                    float g0, g1;
-                    GatePair<GT>::load(gptr + ((size_t)(t0 + r) * H + h) * KD + d0, g0, g1);
-                    a0 = gate_log2(g0, expA0, dtb0, p.mode, p.lb);
-                    a1 = gate_log2(g1, expA1, dtb1, p.mode, p.lb);
-                }
-                acc0 += a0;
-                acc1 += a1;
+                const bool valid = 16 * rq + i < len;
+                acc0 += valid ? gate_log2(g0[i], expA0, dtb0, p.mode, lbl2) : 0.f;
+                acc1 += valid ? gate_log2(g1[i], expA1, dtb1, p.mode, lbl2) : 0.f;
                 G0[i] = acc0;
                 G1[i] = acc1;
             }
             xch[rq * 128 + d0] = acc0;
             xch[rq * 128 + d0 + 1] = acc1;
         }
-        if (tid < C) bsm[tid] = (tid < len) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-        if (!mbar_wait(bar_tma, c & 1)) { atomicAdd(&g_fused_timeouts, 1u); misc[1] = 1; }
-        __syncthreads();
-        if (misc[1]) { abort_ = true; break; }
+        bar_sync(BAR_PREP, NGRP);
+        if (kGateTile && tid == 0 && c + 1 < nt && !sy.aborted()) {  // g tile read: prefetch chunk c + 1
+            mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
+            for (int cb = 0; cb < 2; ++cb)
+                tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)(t0 + C), sy.bar(B_GIN));
+        }
         {
             float c0 = 0.f, c1 = 0.f;
             for (int q2 = 0; q2 < rq; ++q2) {
@@ -281,58 +307,60 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             gmid[rq * 128 + d0 + 1] = G1[8];
             if (rq == 3) { glast[d0] = G0[15]; glast[d0 + 1] = G1[15]; }
         }
-        // zero the v rows beyond the end of the sequence (they may hold the next
-        // sequence's data or NaN padding; T's zero columns would not cancel NaN)
-        if (len < C) {
-            for (int idx = tid; idx < (C - len) * 16; idx += NTHR) {
-                int r = len + idx / 16, cbk = (idx / 8) & 1, ch = idx & 7;
-                st_s128(sb + OFF_V + cbk * 8192 + sw128(r, ch), 0, 0, 0, 0);
-            }
-        }
-        __syncthreads();
+        bar_sync(BAR_PREP, NGRP);
 
-        // ---------------- phase 1: operands
+        // ---- k and q of the own rows from the tiles the chain prefetched into the k 2^G /
+        // s q 2^G hand-off buffers; every thread reads before any thread overwrites them
+        uint32_t kr[16], qr[16];
+        sy.wait(B_QKIN, c & 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const bool valid = 16 * rq + i < len;
+            const uint32_t off = tile_off(16 * rq + i);
+            kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
+            qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
+        }
+        bar_sync(BAR_PREP, NGRP);
+
+        // ---- operands
+        uint32_t kd0[8], kd1[8];
         {
             const float gm0 = G0[8], gm1 = G1[8];
             const float gl0 = glast[d0], gl1 = glast[d0 + 1];
-            const float P0 = exp2f(gm0), P1 = exp2f(gm1);              // 2^G at the midpoint
-            const float L0 = exp2f(gl0 - gm0), L1 = exp2f(gl1 - gm1);  // 2^(Glast - Gmid) <= 1
-            if (rq == 3) { gam[d0] = exp2f(gl0); gam[d0 + 1] = exp2f(gl1); }
-            // paired offsets for the later sub-blocks bi > rq: 2^(G_m(bi) - G_m(rq)) <= 1
-            float R0[4], R1[4];
+            const float P0 = ex2_fast(gm0), P1 = ex2_fast(gm1);              // 2^G at the midpoint
+            const float L0 = ex2_fast(gl0 - gm0), L1 = ex2_fast(gl1 - gm1);  // 2^(Glast - Gmid) <= 1
+            float R0[4], R1[4];  // paired offsets 2^(G_m(bi) - G_m(rq)) <= 1 for bi > rq
 #pragma unroll
             for (int bi = 0; bi < 4; ++bi) {
-                R0[bi] = (bi > rq) ? exp2f(gmid[bi * 128 + d0] - gm0) : 1.f;
-                R1[bi] = (bi > rq) ? exp2f(gmid[bi * 128 + d0 + 1] - gm1) : 1.f;
+                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + d0] - gm0) : 1.f;
+                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + d0 + 1] - gm1) : 1.f;
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const uint32_t ch = 2 * rq + half;
-                uint32_t ak0[4], ak1[4], aq0[4], aq1[4], g_k0[4], g_k1[4], g_q0[4], g_q1[4], dk0[4], dk1[4];
-                uint32_t lk0[4], lk1[4], lq0[4], lq1[4];
+                uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lk0[4], lk1[4], lq0[4], lq1[4];
+                uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4];
 #pragma unroll
                 for (int pr = 0; pr < 4; ++pr) {
                     float kv0[2], kv1[2], qv0[2], qv1[2], e0[2], e1[2], f0[2], f1[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int i = 8 * half + 2 * pr + u, r = 16 * rq + i;
-                        uint32_t kr = 0u, qr = 0u;
-                        if (r < len) {
-                            const size_t off = ((size_t)(t0 + r) * H + h) * KD + d0;
-                            kr = __ldg(reinterpret_cast<const unsigned int*>(p.k + off));
-                            qr = __ldg(reinterpret_cast<const unsigned int*>(p.q + off));
-                        }
-                        kv0[u] = bf_lo(kr); kv1[u] = bf_hi(kr);
-                        qv0[u] = scale * bf_lo(qr); qv1[u] = scale * bf_hi(qr);
-                        e0[u] = exp2f(G0[i] - gm0); e1[u] = exp2f(G1[i] - gm1);
-                        f0[u] = exp2f(gm0 - G0[i]); f1[u] = exp2f(gm1 - G1[i]);
+                        kv0[u] = bf_lo(kr[i]);
+                        kv1[u] = bf_hi(kr[i]);
+                        qv0[u] = scale * bf_lo(qr[i]);
+                        qv1[u] = scale * bf_hi(qr[i]);
+                        e0[u] = ex2_fast(G0[i] - gm0);
+                        e1[u] = ex2_fast(G1[i] - gm1);
+                        f0[u] = ex2_fast(gm0 - G0[i]);
+                        f1[u] = ex2_fast(gm1 - G1[i]);
                         // score columns, K-major [n][channel]: sub-block bi >= rq sees row r as
                         // column j = r with anchor m_bi: k_j 2^(G_m(bi) - G_j) = k_j F_j R(bi)
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
                             if (bi < rq) continue;
                             const int nrow = sb_off(bi) + r;
-                            st_s32(sb + OFF_SB + cbp * (SB_ROWS * 128) + sw128(nrow, (d0 & 63) >> 3) + (d0 & 7) * 2,
+                            st_s32(sb + OFF_SB + cbp * (SB_ROWS * 128) + sw128(nrow, sw_d0) + sw_b0,
                                    pack_bf16(kv0[u] * f0[u] * R0[bi], kv1[u] * f1[u] * R1[bi]));
                         }
                     }
@@ -344,10 +372,10 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                     g_k1[pr] = pack_bf16(kv1[0] * e1[0] * P1, kv1[1] * e1[1] * P1);
                     g_q0[pr] = pack_bf16(qv0[0] * e0[0] * P0, qv0[1] * e0[1] * P0);
                     g_q1[pr] = pack_bf16(qv1[0] * e1[0] * P1, qv1[1] * e1[1] * P1);
-                    dk0[pr] = pack_bf16(kv0[0] * f0[0] * L0, kv0[1] * f0[1] * L0);
-                    dk1[pr] = pack_bf16(kv1[0] * f1[0] * L1, kv1[1] * f1[1] * L1);
+                    kd0[4 * half + pr] = pack_bf16(kv0[0] * f0[0] * L0, kv0[1] * f0[1] * L0);
+                    kd1[4 * half + pr] = pack_bf16(kv1[0] * f1[0] * L1, kv1[1] * f1[1] * L1);
                 }
-                // MN-major [channel][row] operands: one 16-byte chunk of 8 rows per channel
+                // MN-major [channel][row] tiles: one 16-byte chunk of 8 rows per channel
                 const uint32_t r0 = sw128(d0, ch), r1 = sw128(d0 + 1, ch);
                 st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
                 st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
@@ -361,19 +389,16 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
                 st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
                 st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
-                st_s128(sb + OFF_KD + r0, dk0[0], dk0[1], dk0[2], dk0[3]);
-                st_s128(sb + OFF_KD + r1, dk1[0], dk1[1], dk1[2], dk1[3]);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        bar_sync(BAR_PREP, NGRP);
 
-        // ---------------- phase 2: scores, Y^T = h^T kg^T, o^T = h^T qg^T
-        if (tid == 0) {
+        // ---- a2: score MMA (rows hi and lo against the causal columns); k 2^G, s q 2^G handed off
+        if (tid == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 0);
-            const uint32_t id_y = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint64_t b = umma_desc(sb + OFF_SB + (kk >> 2) * (SB_ROWS * 128) + (kk & 3) * 32, 16, 1024);
@@ -382,24 +407,32 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 umma_bf16(tmem + TM_S, ah, b, id_s, kk > 0);
                 umma_bf16(tmem + TM_S, al, b, id_s, 1);
             }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                uint64_t a = umma_desc(sb + OFF_HA + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                uint64_t bk = umma_desc(sb + OFF_KG + kk * 2048, 16384, 1024);
-                uint64_t bq = umma_desc(sb + OFF_QG + kk * 2048, 16384, 1024);
-                umma_bf16(tmem + TM_Y, a, bk, id_y, kk > 0);
-                umma_bf16(tmem + TM_O, a, bq, id_y, kk > 0);
-            }
-            umma_commit(bar_mma);
+            umma_commit(sy.bar(B_SCORE));
+            mbar_arrive(sy.bar(B_KQFULL));
         }
-        if (!mbar_wait(bar_mma, mma_phase)) { atomicAdd(&g_fused_timeouts, 1u); misc[1] = 1; }
-        mma_phase ^= 1;
+        // ---- while the score MMA runs: hand off k 2^(Gl - G) and 2^Glast once the chain's
+        // o / dH MMAs of the previous chunk (the readers of the buffers) are done
+        if (c > 0) sy.wait(B_OHDONE, (uint32_t)((c - 1) & 1));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t ch = 2 * rq + half;
+            st_s128(sb + OFF_KD + sw128(d0, ch), kd0[4 * half], kd0[4 * half + 1], kd0[4 * half + 2],
+                    kd0[4 * half + 3]);
+            st_s128(sb + OFF_KD + sw128(d0 + 1, ch), kd1[4 * half], kd1[4 * half + 1],
+                    kd1[4 * half + 2], kd1[4 * half + 3]);
+        }
+        if (rq == 3) {
+            gam[(c & 1) * 128 + d0] = ex2_fast(G0[15]);
+            gam[(c & 1) * 128 + d0 + 1] = ex2_fast(G1[15]);
+        }
+        sy.wait(B_SCORE, c & 1);
         tc_fence_after();
 
-        // ---------------- phase 3: read scores (warps 0-3) and Y^T (warps 4-7)
+        // ---- read the scores: warps 0-1 Akk rows (beta-scaled, strictly lower) into the solve
+        // matrix, warps 2-3 Aqk rows (hi, lo) straight into the hand-off buffers
         if (w < 4) {
-            const int row = 32 * w + l;       // TMEM lane
-            const int i = row & 63;           // chunk row
+            const int row = 32 * w + l;  // TMEM lane
+            const int i = row & 63;
             const bool is_q = row >= 64;
             const int bi = i >> 4;
             // the 32 lanes of this warp hold two sub-blocks (bmin, bmin + 1); every lane
@@ -424,196 +457,369 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 }
             }
             if (!is_q) {
-                const float bi_beta = bsm[i];
+                const float b_i = bsm[i];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) As[i * LD + j] = (j < i && j < 16 * (bi + 1)) ? bi_beta * sv[j] : 0.f;
+                for (int j = 0; j < 64; ++j) As[j * LD + i] = (j < i) ? b_i * sv[j] : 0.f;  // Akk^T
             } else {
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t pk[4], pl[4];
+                    uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        int j0 = 8 * c8 + 2 * e, j1 = j0 + 1;
-                        float x0 = (j0 <= i && j0 < 16 * (bi + 1)) ? sv[j0] : 0.f;
-                        float x1 = (j1 <= i && j1 < 16 * (bi + 1)) ? sv[j1] : 0.f;
-                        pack_split(x0, x1, pk[e], pl[e]);
+                        const int j0 = 8 * c8 + 2 * e;
+                        pack_split(j0 <= i ? sv[j0] : 0.f, j0 + 1 <= i ? sv[j0 + 1] : 0.f, hi[e], lo[e]);
                     }
-                    st_s128(sb + OFF_AQKH + sw128(i, c8), pk[0], pk[1], pk[2], pk[3]);
-                    st_s128(sb + OFF_AQKL + sw128(i, c8), pl[0], pl[1], pl[2], pl[3]);
+                    st_s128(sb + OFF_AQKH + sw128(i, c8), hi[0], hi[1], hi[2], hi[3]);
+                    st_s128(sb + OFF_AQKL + sw128(i, c8), lo[0], lo[1], lo[2], lo[3]);
                 }
             }
-        } else {
-            float yv[64];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) tmem_ld16(tmem + ((uint32_t)(32 * (w & 3)) << 16) + TM_Y + 16 * t, yv + 16 * t);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                st_s128(sb + OFF_YA + sw128(vlane, c8), pack_bf16(yv[8 * c8], yv[8 * c8 + 1]),
-                        pack_bf16(yv[8 * c8 + 2], yv[8 * c8 + 3]), pack_bf16(yv[8 * c8 + 4], yv[8 * c8 + 5]),
-                        pack_bf16(yv[8 * c8 + 6], yv[8 * c8 + 7]));
         }
-        __syncthreads();
+        tc_fence_before();
+        bar_sync(BAR_PREP, NGRP);
 
-        // ---------------- phase 4: T = (I + Akk)^-1 (FP32), then T diag(beta) in bf16
-        if (tid < 64) {
-            const int b = tid >> 4, cc = tid & 15;
+        // ---- a3: T = (I + Akk)^-1.  Diagonal 16 x 16 blocks by forward substitution, one
+        // thread per column (warps 0-1); the strictly upper blocks are zero.
+        if (w < 2) {
+            const int b = 2 * w + (l >> 4), cc = l & 15;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float val = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j < i; ++j) val = fmaf(-As[(16 * b + i) * LD + 16 * b + j], x[j], val);
+                for (int j = 0; j < i; ++j) val = fmaf(-As[(16 * b + j) * LD + 16 * b + i], x[j], val);
                 x[i] = (i < cc) ? 0.f : val;
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
         }
-        for (int idx = tid; idx < 64 * 64; idx += NTHR) {
-            int i = idx >> 6, j = idx & 63;
+        for (int idx = tid; idx < 64 * 64; idx += NGRP) {
+            const int i = idx >> 6, j = idx & 63;
             if ((j >> 4) > (i >> 4)) Tf[i * LD + j] = 0.f;
         }
-        __syncthreads();
+        bar_sync(BAR_PREP, NGRP);
+        // Off-diagonal blocks, level by level: T[b+L][b] = -T[b+L][b+L] (sum_t A[b+L][t] T[t][b])
+        // over blocks t = b .. b+L-1; warp b computes one block with m16n8k8 tf32 MMAs
+        // (fragments: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
+        //  c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]; g = lane / 4, t = lane % 4).
+        {
+            const int gq = l >> 2, tq = l & 3;
 #pragma unroll 1
-        for (int lev = 1; lev < 4; ++lev) {
-            const int nb = 4 - lev;  // blocks (b + lev, b), b < nb
-            const int i = tid >> 4, j = tid & 15;
-            for (int b = 0; b < nb; ++b) {
-                float acc = 0.f;
-                for (int t = 0; t < 16 * lev; ++t)
-                    acc = fmaf(As[(16 * (b + lev) + i) * LD + 16 * b + t], Tf[(16 * b + t) * LD + 16 * b + j], acc);
-                Xs[(b * 16 + i) * 17 + j] = acc;
-            }
-            __syncthreads();
-            for (int b = 0; b < nb; ++b) {
-                float acc = 0.f;
+            for (int lev = 1; lev < 4; ++lev) {
+                if (w < 4 - lev) {
+                    const int b = w, r0 = 16 * (b + lev), c0 = 16 * b;
+                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int ks = 0; ks < 2 * lev; ++ks) {
+                        const int kc = c0 + 8 * ks;
+                        uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
+                                         to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
+                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
+                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    acc = fmaf(Tf[(16 * (b + lev) + i) * LD + 16 * (b + lev) + t], Xs[(b * 16 + t) * 17 + j], acc);
-                Tf[(16 * (b + lev) + i) * LD + 16 * b + j] = -acc;
+                        for (int n8 = 0; n8 < 2; ++n8) {
+                            uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + c0 + 8 * n8 + gq]),
+                                              to_tf32(Tf[(kc + tq + 4) * LD + c0 + 8 * n8 + gq])};
+                            mma_tf32_16x8x8(xa[n8], a, bb);
+                        }
+                    }
+                    float* X = Xs + w * (16 * 24);
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        X[gq * 24 + 8 * n8 + 2 * tq] = xa[n8][0];
+                        X[gq * 24 + 8 * n8 + 2 * tq + 1] = xa[n8][1];
+                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = xa[n8][2];
+                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = xa[n8][3];
+                    }
+                    __syncwarp();
+                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int kc = r0 + 8 * ks;
+                        uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]),
+                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
+                                         to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
+                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
+#pragma unroll
+                        for (int n8 = 0; n8 < 2; ++n8) {
+                            uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
+                                              to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
+                            mma_tf32_16x8x8(ta[n8], a, bb);
+                        }
+                    }
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        Tf[(r0 + gq) * LD + c0 + 8 * n8 + 2 * tq] = -ta[n8][0];
+                        Tf[(r0 + gq) * LD + c0 + 8 * n8 + 2 * tq + 1] = -ta[n8][1];
+                        Tf[(r0 + gq + 8) * LD + c0 + 8 * n8 + 2 * tq] = -ta[n8][2];
+                        Tf[(r0 + gq + 8) * LD + c0 + 8 * n8 + 2 * tq + 1] = -ta[n8][3];
+                    }
+                }
+                bar_sync(BAR_PREP, NGRP);
             }
-            __syncthreads();
         }
-        for (int idx = tid; idx < 64 * 8; idx += NTHR) {
+
+        // ---- hand off T diag(beta) once the chain's v_new MMAs of the previous chunk are done
+        if (c > 0) sy.wait(B_VNDONE, (uint32_t)((c - 1) & 1));
+        for (int idx = tid; idx < 64 * 8; idx += NGRP) {
             const int i = idx >> 3, c8 = idx & 7;
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                int j0 = 8 * c8 + 2 * e;
+                const int j0 = 8 * c8 + 2 * e;
                 pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
             }
             st_s128(sb + OFF_TP + sw128(i, c8), pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        bar_sync(BAR_PREP, NGRP);
+        if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
+    }
+}
 
-        // ---------------- phase 5: vn^T = v^T T'^T - Y^T T'^T
-        if (tid == 0) {
+// ------------------------------------------------------------------ chain group
+template <typename OT>
+__device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
+                                           const Sync& sy, const CUtensorMap* tm_v,
+                                           const CUtensorMap* tm_q, const CUtensorMap* tm_k, int n,
+                                           int h, long bos, long eos, int nt) {
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int ct = tid - NGRP;          // 0 .. 255
+    const int lg = w & 3;               // TMEM lane group
+    const int vlane = 32 * lg + l;      // value channel
+    const int hch = (w - 8) >> 2;       // key-channel half of the state / column half
+    const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
+    const int H = p.H;
+    const float* gam = reinterpret_cast<const float*>(smem + OFF_GAM);
+    const size_t st_off = ((size_t)n * H + h) * (size_t)KD * VD;
+
+    float hs[64];  // h^T[v][64 hch + j]
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+        hs[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + j) * VD + vlane) : 0.f;
+
+    auto store_hA = [&]() {  // bf16 h^T into the TMEM A operand (columns TM_VN + 32 hch ..)
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hs[32 * s + 2 * e], hs[32 * s + 2 * e + 1]);
+            tmem_st16(tmem + lane_base + TM_VN + 32 * hch + 16 * s, r);
+        }
+    };
+
+    // q and k tiles of chunk c land in the k 2^G / s q 2^G buffers for the prep group
+    auto load_qk = [&](long t) {
+        mbar_arrive_expect_tx(sy.bar(B_QKIN), 32768);
+        for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(sb + OFF_KG + cb * 8192, tm_k, 64 * cb, h, (int)t, sy.bar(B_QKIN));
+            tma_load_3d(sb + OFF_QG + cb * 8192, tm_q, 64 * cb, h, (int)t, sy.bar(B_QKIN));
+        }
+    };
+    auto load_v = [&](long t) {
+        mbar_arrive_expect_tx(sy.bar(B_VFULL), 16384);
+        for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sb + OFF_V + cb * 8192, tm_v, 64 * cb, h, (int)t, sy.bar(B_VFULL));
+    };
+    if (nt > 0) {
+        store_hA();
+        tmem_wait_st();
+        if (ct == 0) {
+            load_qk(bos);
+            load_v(bos);
+        }
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NGRP);
+    }
+
+    for (int c = 0; c < nt; ++c) {
+        const long t0 = bos + (long)c * C;
+        const int len = (int)min((long)C, eos - t0);
+        const uint32_t vbuf = sb + OFF_V;
+
+        // ---- Y^T = h^T kg^T, o^T = h^T qg^T
+        sy.wait(B_KQFULL, c & 1);
+        if (ct == 0 && !sy.aborted()) {
             tc_fence_after();
-            const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
-            const uint32_t id_y = idesc_bf16(128, 64, 0, 0, 1, 0);
+            const uint32_t id_y = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                uint64_t a = umma_desc(sb + OFF_V + kk * 2048, 8192, 1024);
-                uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
-                umma_bf16(tmem + TM_VN, a, b, id_v, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+                uint64_t bk = umma_desc(sb + OFF_KG + kk * 2048, 16384, 1024);
+                uint64_t bq = umma_desc(sb + OFF_QG + kk * 2048, 16384, 1024);
+                umma_bf16_ta(tmem + TM_Y, tmem + TM_VN + 8 * kk, bk, id_y, kk > 0);
+                umma_bf16_ta(tmem + TM_O, tmem + TM_VN + 8 * kk, bq, id_y, kk > 0);
             }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                uint64_t a = umma_desc(sb + OFF_YA + kk * 32, 16, 1024);
-                uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
-                umma_bf16(tmem + TM_VN, a, b, id_y, 1);
-            }
-            umma_commit(bar_mma);
+            umma_commit(sy.bar(B_YDONE));
         }
-        if (!mbar_wait(bar_mma, mma_phase)) { atomicAdd(&g_fused_timeouts, 1u); misc[1] = 1; }
-        mma_phase ^= 1;
+        sy.wait(B_YDONE, c & 1);
         tc_fence_after();
-
-        // ---------------- phase 6: v_new^T -> bf16 A operand (overwrites Y^T)
+        // the k 2^G / s q 2^G buffers are free: prefetch the next chunk's k and q tiles
+        if (ct == 0 && c + 1 < nt && !sy.aborted()) load_qk(t0 + C);
+        // ---- Y^T -> bf16 A operand
         {
-            float vv[32];
-            const int half = w >> 2;
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                tmem_ld16(tmem + ((uint32_t)(32 * (w & 3)) << 16) + TM_VN + 32 * half + 16 * t, vv + 16 * t);
+            float y[32];
+            tmem_ld16(tmem + lane_base + TM_Y + 32 * hch, y);
+            tmem_ld16(tmem + lane_base + TM_Y + 32 * hch + 16, y + 16);
             tmem_wait_ld();
+            uint32_t r[16];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t hi[4], lo[4];
+            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
+            tmem_st16(tmem + lane_base + TM_YA + 16 * hch, r);
+            tmem_wait_st();
+        }
+        sy.wait(B_RESTFULL, c & 1);
+        if (len < C) {
+            // rows past the end of the sequence may hold the next sequence's tokens or NaN
+            // padding; T diag(beta) has zero columns there, which would not cancel a NaN
+            sy.wait(B_VFULL, c & 1);
+            for (int idx = ct; idx < (C - len) * 16; idx += NGRP) {
+                const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
+                st_s128(vbuf + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NGRP);
+        // ---- v_new^T = v^T T'^T - Y^T T'^T (h^T's TMEM columns are free once Y / o are done)
+        if (ct == 0) {
+            sy.wait(B_VFULL, c & 1);
+            if (!sy.aborted()) {
+                tc_fence_after();
+                const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
+                const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pack_split(vv[8 * c4 + 2 * e], vv[8 * c4 + 2 * e + 1], hi[e], lo[e]);
-                st_s128(sb + OFF_YA + sw128(vlane, 4 * half + c4), hi[0], hi[1], hi[2], hi[3]);
-                st_s128(sb + OFF_VNL + sw128(vlane, 4 * half + c4), lo[0], lo[1], lo[2], lo[3]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint64_t a = umma_desc(vbuf + kk * 2048, 8192, 1024);
+                    uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
+                    umma_bf16(tmem + TM_VN, a, b, id_v, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
+                    umma_bf16_ta(tmem + TM_VN, tmem + TM_YA + 8 * kk, b, id_n, 1);
+                }
+                umma_commit(sy.bar(B_VNDONE));
             }
         }
-        fence_proxy_async_smem();
+        sy.wait(B_VNDONE, c & 1);
+        tc_fence_after();
+        if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);  // the v tile is free again
+        // ---- v_new^T -> (hi, lo) bf16 A operands in the Y^T columns
+        {
+            float x[32];
+            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch, x);
+            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch + 16, x + 16);
+            tmem_wait_ld();
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pack_split(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+            tmem_st16(tmem + lane_base + TM_Y + 16 * hch, hi);
+            tmem_st16(tmem + lane_base + TM_Y + 32 + 16 * hch, lo);
+            tmem_wait_st();
+        }
         tc_fence_before();
-        __syncthreads();
-
-        // ---------------- phase 7: o^T += vn^T Aqk^T; dH^T = vn^T kd
-        if (tid == 0) {
+        bar_sync(BAR_CHAIN, NGRP);
+        // ---- o^T += v_new^T Aqk^T (hi*hi + lo*hi + hi*lo); dH^T = v_new^T kd (hi + lo)
+        if (ct == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_o = idesc_bf16(128, 64, 0, 0);
             const uint32_t id_h = idesc_bf16(128, 128, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                uint64_t ah = umma_desc(sb + OFF_YA + kk * 32, 16, 1024);
-                uint64_t al = umma_desc(sb + OFF_VNL + kk * 32, 16, 1024);
+                const uint32_t ah = tmem + TM_Y + 8 * kk, al = tmem + TM_Y + 32 + 8 * kk;
                 uint64_t boh = umma_desc(sb + OFF_AQKH + kk * 32, 16, 1024);
                 uint64_t bol = umma_desc(sb + OFF_AQKL + kk * 32, 16, 1024);
-                uint64_t bh = umma_desc(sb + OFF_KD + kk * 32, 16, 1024);
-                umma_bf16(tmem + TM_O, ah, boh, id_o, 1);
-                umma_bf16(tmem + TM_O, al, boh, id_o, 1);
-                umma_bf16(tmem + TM_O, ah, bol, id_o, 1);
-                umma_bf16(tmem + TM_DH, ah, bh, id_h, kk > 0);
-                umma_bf16(tmem + TM_DH, al, bh, id_h, 1);
+                uint64_t bk = umma_desc(sb + OFF_KD + kk * 32, 16, 1024);
+                umma_bf16_ta(tmem + TM_O, ah, boh, id_o, 1);
+                umma_bf16_ta(tmem + TM_O, al, boh, id_o, 1);
+                umma_bf16_ta(tmem + TM_O, ah, bol, id_o, 1);
+                umma_bf16_ta(tmem + TM_DH, ah, bk, id_h, kk > 0);
+                umma_bf16_ta(tmem + TM_DH, al, bk, id_h, 1);
             }
-            umma_commit(bar_mma);
+            umma_commit(sy.bar(B_OHDONE));
         }
-        if (!mbar_wait(bar_mma, mma_phase)) { atomicAdd(&g_fused_timeouts, 1u); misc[1] = 1; }
-        mma_phase ^= 1;
+        sy.wait(B_OHDONE, c & 1);
         tc_fence_after();
-
-        // ---------------- phase 8: state update, o out
+        // ---- h^T <- h^T Diag(2^Glast) + dH^T; bf16 h^T for the next chunk; o out
         {
-            float dh[64];
+            const float* gm = gam + (c & 1) * 128 + 64 * hch;
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                tmem_ld16(tmem + ((uint32_t)(32 * (w & 3)) << 16) + TM_DH + 64 * hch + 16 * t, dh + 16 * t);
+            for (int s = 0; s < 2; ++s) {
+                float dh[32];
+                tmem_ld16(tmem + lane_base + TM_DH + 64 * hch + 32 * s, dh);
+                tmem_ld16(tmem + lane_base + TM_DH + 64 * hch + 32 * s + 16, dh + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hs[32 * s + j] = fmaf(gm[32 * s + j], hs[32 * s + j], dh[j]);
+            }
+            store_hA();
             float ov[32];
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                tmem_ld16(tmem + ((uint32_t)(32 * (w & 3)) << 16) + TM_O + 32 * hch + 16 * t, ov + 16 * t);
+            tmem_ld16(tmem + lane_base + TM_O + 32 * hch, ov);
+            tmem_ld16(tmem + lane_base + TM_O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 64; ++j) hs[j] = fmaf(gam[64 * hch + j], hs[j], dh[j]);
-            write_hA();
+            OT* o = reinterpret_cast<OT*>(p.o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int i = 32 * hch + j;
-                if (i < len) reinterpret_cast<OT*>(p.o)[((size_t)(t0 + i) * H + h) * VD + vlane] = to_out<OT>(ov[j]);
+                if (i < len) o[((size_t)(t0 + i) * H + h) * VD + vlane] = to_out<OT>(ov[j]);
             }
+            tmem_wait_st();
         }
         tc_fence_before();
-        __syncthreads();
-        if (misc[1]) abort_ = true;
+        bar_sync(BAR_CHAIN, NGRP);
     }
 
-    if (p.hT && !abort_) {
+    if (p.hT && !sy.aborted()) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) p.hT[st_off + (size_t)(64 * hch + j) * VD + vlane] = hs[j];
+    }
+}
+
+template <typename GT, typename OT>
+__global__ void __launch_bounds__(NTHR, 1)
+chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                   Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
+    Sync sy{sb + OFF_BAR, misc + 1};
+
+    const int tid = threadIdx.x, w = tid >> 5;
+    const int h = blockIdx.y, n = blockIdx.x;
+    long bos, eos;
+    if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
+    else      { bos = (long)n * p.T; eos = bos + p.T; }
+    const int nt = (int)((eos - bos + C - 1) / C);
+
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
+        fence_mbar_init();
+        misc[1] = 0;
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_g);
+    }
+    if (w == 0) tmem_alloc(sb + OFF_MISC, TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (w < 8) prep_loop<GT>(p, sb, smem, tmem, sy, &tm_g, h, bos, eos, nt);
+    else       chain_loop<OT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, n, h, bos, eos, nt);
+
+    // Every MMA was waited for, unless a wait gave up: then let the ones in flight finish.
+    if (sy.aborted() && (tid == 0 || tid == NGRP)) {
+        const uint32_t bar = sy.bar(tid == 0 ? B_DRAIN0 : B_DRAIN1);
+        umma_commit(bar);
+        mbar_wait(bar, 0);
     }
     tc_fence_before();
     __syncthreads();
     if (w == 0) {
-        if (abort_ && l == 0) {
-            // let any MMA still in flight finish before the columns are released
-            umma_commit(bar_mma);
-            mbar_wait(bar_mma, mma_phase);
-        }
-        __syncwarp();
+        tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
     }
 }
@@ -655,25 +861,32 @@ bool fused_supported_dims(bool qkv_bf16, int K, int V, int C) {
 bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C); }
 
 template <typename GT, typename OT>
-static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mv, const fused::Params& p) {
+static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mg, const fused::Params& p) {
     using namespace fused;
     auto kern = chunk_fused_kernel<GT, OT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(a.N, a.H), NTHR, SMEM_BYTES, a.stream>>>(mv, p);
+    kern<<<dim3(a.N, a.H), NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_fused(const FwdArgs& a) {
     using namespace fused;
-    CUtensorMap mv;
+    CUtensorMap mq, mk, mv, mg;
     const long tokens = (long)a.B * a.T;
-    if (!make_map(&mv, a.v, tokens, a.H, VD)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, a.q, tokens, a.H, KD) || !make_map(&mk, a.k, tokens, a.H, KD) ||
+        !make_map(&mv, a.v, tokens, a.H, VD))
+        return cudaErrorInvalidValue;
+    // the float32 gate is read with plain loads; its map is a placeholder the kernel never uses
+    if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
              a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H};
     if (a.g_bf16)
-        return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mv, p) : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mv, p);
-    return a.o_f32 ? launch_t<float, float>(a, mv, p) : launch_t<float, __nv_bfloat16>(a, mv, p);
+        return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
+                       : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);
+    return a.o_f32 ? launch_t<float, float>(a, mq, mk, mv, mg, p)
+                   : launch_t<float, __nv_bfloat16>(a, mq, mk, mv, mg, p);
 }
 
 }  // namespace kda
