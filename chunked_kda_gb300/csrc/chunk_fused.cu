@@ -197,6 +197,11 @@ struct Sync {
         }
     }
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
+    // wait of a whole warp group: one warp polls, the others sleep on the group's barrier
+    __device__ __forceinline__ void group_wait(int i, uint32_t parity, bool leader, uint32_t barid) const {
+        if (leader) wait(i, parity);
+        bar_sync(barid, NGRP);
+    }
 };
 
 // ------------------------------------------------------------------ prep group
@@ -236,11 +241,15 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
 
-    // beta of the next chunk is loaded one chunk ahead (threads 0-63, one row each)
-    auto load_beta = [&](long t, int len_) {
-        return (tid < len_) ? __bfloat162float(p.beta[(size_t)(t + tid) * H + h]) : 0.f;
+    // beta of the next chunk is loaded one chunk ahead (threads 0-63, one row each); the raw
+    // bits stay in flight until the store, so no thread waits on the load
+    // (a clamped, always valid row; the mask is applied when the value is stored)
+    const unsigned short* beta_bits = reinterpret_cast<const unsigned short*>(p.beta);
+    auto load_beta = [&](long t, int len_) -> unsigned short {
+        return __ldg(beta_bits + (size_t)(t + min(tid, len_ - 1)) * H + h);
     };
-    float beta_next = (tid < C && nt > 0) ? load_beta(bos, (int)min((long)C, eos - bos)) : 0.f;
+    unsigned short beta_next = 0;
+    if (tid < C && nt > 0) beta_next = load_beta(bos, (int)min((long)C, eos - bos));
 
     if (kGateTile && tid == 0 && nt > 0) {
         mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
@@ -255,7 +264,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // ---- gate of the own rows: from the g tile (bf16) or from global memory (float32)
         float g0[16], g1[16];
         if constexpr (kGateTile) {
-            sy.wait(B_GIN, c & 1);
+            sy.group_wait(B_GIN, c & 1, w == 0, BAR_PREP);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t x = ld_s32(sb + OFF_GT + tile_off(16 * rq + i));
@@ -270,19 +279,33 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
         }
         if (tid < C) {
-            bsm[tid] = beta_next;
+            bsm[tid] = (tid < len) ? __uint_as_float((uint32_t)beta_next << 16) : 0.f;
             if (c + 1 < nt) beta_next = load_beta(t0 + C, (int)min((long)C, eos - t0 - C));
         }
 
         // ---- a1: gate, chunk-local cumsum (log2 units), sub-block carries
         float G0[16], G1[16];
         {
+            // per-token decay in log2 units (mode decided once, so the 32 evaluations interleave)
+            if (p.mode == 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    g0[i] = lbl2 * rcp_fast(1.0f + ex2_fast(-(expA0 * (g0[i] + dtb0)) * kLog2e));
+                    g1[i] = lbl2 * rcp_fast(1.0f + ex2_fast(-(expA1 * (g1[i] + dtb1)) * kLog2e));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    g0[i] *= kLog2e;
+                    g1[i] *= kLog2e;
+                }
+            }
             float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const bool valid = 16 * rq + i < len;
-                acc0 += valid ? gate_log2(g0[i], expA0, dtb0, p.mode, lbl2) : 0.f;
-                acc1 += valid ? gate_log2(g1[i], expA1, dtb1, p.mode, lbl2) : 0.f;
+                acc0 += valid ? g0[i] : 0.f;
+                acc1 += valid ? g1[i] : 0.f;
                 G0[i] = acc0;
                 G1[i] = acc1;
             }
@@ -312,7 +335,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // ---- k and q of the own rows from the tiles the chain prefetched into the k 2^G /
         // s q 2^G hand-off buffers; every thread reads before any thread overwrites them
         uint32_t kr[16], qr[16];
-        sy.wait(B_QKIN, c & 1);
+        sy.group_wait(B_QKIN, c & 1, w == 0, BAR_PREP);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const bool valid = 16 * rq + i < len;
@@ -412,7 +435,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         }
         // ---- while the score MMA runs: hand off k 2^(Gl - G) and 2^Glast once the chain's
         // o / dH MMAs of the previous chunk (the readers of the buffers) are done
-        if (c > 0) sy.wait(B_OHDONE, (uint32_t)((c - 1) & 1));
+        if (c > 0) sy.group_wait(B_OHDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint32_t ch = 2 * rq + half;
@@ -425,7 +448,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             gam[(c & 1) * 128 + d0] = ex2_fast(G0[15]);
             gam[(c & 1) * 128 + d0 + 1] = ex2_fast(G1[15]);
         }
-        sy.wait(B_SCORE, c & 1);
+        sy.group_wait(B_SCORE, c & 1, w == 0, BAR_PREP);
         tc_fence_after();
 
         // ---- read the scores: warps 0-1 Akk rows (beta-scaled, strictly lower) into the solve
@@ -558,7 +581,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         }
 
         // ---- hand off T diag(beta) once the chain's v_new MMAs of the previous chunk are done
-        if (c > 0) sy.wait(B_VNDONE, (uint32_t)((c - 1) & 1));
+        if (c > 0) sy.group_wait(B_VNDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
         for (int idx = tid; idx < 64 * 8; idx += NGRP) {
             const int i = idx >> 3, c8 = idx & 7;
             uint32_t pk[4];
@@ -636,7 +659,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         const uint32_t vbuf = sb + OFF_V;
 
         // ---- Y^T = h^T kg^T, o^T = h^T qg^T
-        sy.wait(B_KQFULL, c & 1);
+        if (ct == 0) sy.wait(B_KQFULL, c & 1);
         if (ct == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_y = idesc_bf16(128, 64, 0, 1);
@@ -649,7 +672,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             }
             umma_commit(sy.bar(B_YDONE));
         }
-        sy.wait(B_YDONE, c & 1);
+        sy.group_wait(B_YDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
         // the k 2^G / s q 2^G buffers are free: prefetch the next chunk's k and q tiles
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_qk(t0 + C);
@@ -665,11 +688,14 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             tmem_st16(tmem + lane_base + TM_YA + 16 * hch, r);
             tmem_wait_st();
         }
-        sy.wait(B_RESTFULL, c & 1);
+        if (w == 8) {
+            sy.wait(B_RESTFULL, c & 1);
+            if (len < C) sy.wait(B_VFULL, c & 1);
+        }
+        bar_sync(BAR_CHAIN, NGRP);
         if (len < C) {
             // rows past the end of the sequence may hold the next sequence's tokens or NaN
             // padding; T diag(beta) has zero columns there, which would not cancel a NaN
-            sy.wait(B_VFULL, c & 1);
             for (int idx = ct; idx < (C - len) * 16; idx += NGRP) {
                 const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
                 st_s128(vbuf + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
@@ -699,7 +725,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
                 umma_commit(sy.bar(B_VNDONE));
             }
         }
-        sy.wait(B_VNDONE, c & 1);
+        sy.group_wait(B_VNDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);  // the v tile is free again
         // ---- v_new^T -> (hi, lo) bf16 A operands in the Y^T columns
@@ -736,7 +762,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             }
             umma_commit(sy.bar(B_OHDONE));
         }
-        sy.wait(B_OHDONE, c & 1);
+        sy.group_wait(B_OHDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
         // ---- h^T <- h^T Diag(2^Glast) + dH^T; bf16 h^T for the next chunk; o out
         {
@@ -755,12 +781,11 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
-            OT* o = reinterpret_cast<OT*>(p.o);
+            OT* orow = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * VD + vlane;
+            const int ostride = H * VD, nvalid = len - 32 * hch;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = 32 * hch + j;
-                if (i < len) o[((size_t)(t0 + i) * H + h) * VD + vlane] = to_out<OT>(ov[j]);
-            }
+            for (int j = 0; j < 32; ++j)
+                if (j < nvalid) orow[j * ostride] = to_out<OT>(ov[j]);
             tmem_wait_st();
         }
         tc_fence_before();
