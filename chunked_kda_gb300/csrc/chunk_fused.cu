@@ -67,26 +67,29 @@ constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T
 constexpr uint32_t OFF_GT = 16384;     // g tile (TMA, bf16 gate only), 16 KB               [prep]
 constexpr uint32_t OFF_SAH = 32768;    // score rows hi [128 ch][128 rows] MN-major      [prep]
 constexpr uint32_t OFF_SAL = 65536;    // score rows lo
-constexpr uint32_t OFF_SB = 98304;     // score cols [160][128 ch] K-major, 40 KB
+constexpr uint32_t OFF_SB = 98304;     // score cols [128 ch][160] MN-major, 3 groups of 64 columns
+                                       //   (16 KB each), 48 KB
 constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
 constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
 constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [3][16][24]
-constexpr uint32_t OFF_KG = 139264;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_KG = 147456;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
-constexpr uint32_t OFF_QG = 155648;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_QG = 163840;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's q tile (TMA)
-constexpr uint32_t OFF_KD = 172032;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
-constexpr uint32_t OFF_TP = 188416;    // hand-off: T diag(beta) bf16 [64][64] K-major B
-constexpr uint32_t OFF_AQKH = 196608;  // hand-off: Aqk hi [64][64]
-constexpr uint32_t OFF_AQKL = 204800;  // hand-off: Aqk lo [64][64]
-constexpr uint32_t OFF_GAM = 212992;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
-constexpr uint32_t OFF_BETA = 214016;  // prep: beta fp32 [64]
-constexpr uint32_t OFF_XCH = 214272;   // prep: fp32 [4][128] per-sub-block gate sums
-constexpr uint32_t OFF_GM = 216320;    // prep: fp32 [4][128] G at the sub-block midpoints
-constexpr uint32_t OFF_GL = 218368;    // prep: fp32 [128] G at the last row
-constexpr uint32_t OFF_BAR = 218880;   // mbarriers (8 bytes each)
-constexpr uint32_t OFF_MISC = 218976;  // tmem base, abort flag
-constexpr uint32_t SMEM_BYTES = 218992 + 1024;  // + alignment slack
+constexpr uint32_t OFF_KD = 180224;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
+constexpr uint32_t OFF_TP = 196608;    // hand-off: T diag(beta) bf16 [64][64] K-major B
+constexpr uint32_t OFF_AQKH = 204800;  // hand-off: Aqk hi [64][64]
+constexpr uint32_t OFF_AQKL = 212992;  // hand-off: Aqk lo [64][64]
+constexpr uint32_t OFF_GAM = 221184;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
+constexpr uint32_t OFF_BETA = 222208;  // prep: beta fp32 [64]
+constexpr uint32_t OFF_XCH = 222464;   // prep: fp32 [4][128] per-sub-block gate sums
+constexpr uint32_t OFF_GM = 224512;    // prep: fp32 [4][128] G at the sub-block midpoints
+constexpr uint32_t OFF_GL = 226560;    // prep: fp32 [128] G at the last row
+constexpr uint32_t OFF_BAR = 227072;   // mbarriers (8 bytes each)
+constexpr uint32_t OFF_MISC = 227168;  // tmem base, abort flag
+constexpr uint32_t SMEM_BYTES = 227184 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
+static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 3 * 16 * 24 * 4 <= OFF_SB + 3 * 16384, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
 
@@ -135,6 +138,13 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
                  : "memory");
 }
 
+// a 16-bit global load the compiler keeps where it is written (issued one chunk ahead of its
+// use, it must not be re-issued next to the use)
+__device__ __forceinline__ unsigned short ld_g16_pinned(const unsigned short* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
@@ -145,28 +155,21 @@ template <typename GT>
 struct GatePair;
 template <>
 struct GatePair<__nv_bfloat16> {
-    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float& a, float& b) {
+    // channels (d0, d0 + 1) at p, returned in the order (ch0, ch1) of the owning thread
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, int swap, float& a, float& b) {
         uint32_t x = __ldg(reinterpret_cast<const unsigned int*>(p));
-        a = bf_lo(x);
-        b = bf_hi(x);
+        a = swap ? bf_hi(x) : bf_lo(x);
+        b = swap ? bf_lo(x) : bf_hi(x);
     }
 };
 template <>
 struct GatePair<float> {
-    static __device__ __forceinline__ void load(const float* p, float& a, float& b) {
+    static __device__ __forceinline__ void load(const float* p, int swap, float& a, float& b) {
         float2 x = __ldg(reinterpret_cast<const float2*>(p));
-        a = x.x;
-        b = x.y;
+        a = swap ? x.y : x.x;
+        b = swap ? x.x : x.y;
     }
 };
-
-// per-token decay in log2 units: mode 0 pre-gated (a = g), mode 1 safe
-// (a = lb * sigmoid(expA * (g + dtb)), with sigmoid(z) = 1 / (1 + 2^(-z log2 e)))
-__device__ __forceinline__ float gate_log2(float g, float expA, float dtb, int mode, float lbl2) {
-    if (mode == 0) return g * kLog2e;
-    const float z = expA * (g + dtb);
-    return lbl2 * rcp_fast(1.0f + ex2_fast(-z * kLog2e));
-}
 
 struct Params {
     const __nv_bfloat16* q;
@@ -221,17 +224,25 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     float* Tf = reinterpret_cast<float*>(smem + OFF_TF);
     float* Xs = reinterpret_cast<float*>(smem + OFF_XS);
 
-    // channel pair (d0, d0 + 1), sub-block rq (rows 16 rq .. 16 rq + 15)
+    // channel pair (d0, d0 + 1), sub-block rq (rows 16 rq .. 16 rq + 15).  The thread's
+    // "first" channel ch0 is d0 for lanes with bit 2 clear and d0 + 1 for the others, so a
+    // warp's 16-byte stores to a channel-major tile cover all eight 16-byte bank groups
     const int cbp = w & 1;
     const int d0 = 2 * (32 * cbp + l);
     const int rq = w >> 1;
+    const int swap = (l >> 2) & 1;
+    const int ch0 = d0 + swap, ch1 = d0 + 1 - swap;
+    // byte selectors taking the bf16 of ch0 / ch1 out of the (d0, d0 + 1) word as a float
+    const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
+    auto bf_0 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel0)); };
+    auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel1)); };
     float expA0 = 0.f, expA1 = 0.f, dtb0 = 0.f, dtb1 = 0.f;
     if (p.mode == 1) {
-        expA0 = expf(__ldg(p.A_log + h * KD + d0));
-        expA1 = expf(__ldg(p.A_log + h * KD + d0 + 1));
+        expA0 = expf(__ldg(p.A_log + h * KD + ch0));
+        expA1 = expf(__ldg(p.A_log + h * KD + ch1));
         if (p.dt_bias) {
-            dtb0 = __ldg(p.dt_bias + h * KD + d0);
-            dtb1 = __ldg(p.dt_bias + h * KD + d0 + 1);
+            dtb0 = __ldg(p.dt_bias + h * KD + ch0);
+            dtb1 = __ldg(p.dt_bias + h * KD + ch1);
         }
     }
     const float lbl2 = p.lb * kLog2e;
@@ -246,7 +257,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     // (a clamped, always valid row; the mask is applied when the value is stored)
     const unsigned short* beta_bits = reinterpret_cast<const unsigned short*>(p.beta);
     auto load_beta = [&](long t, int len_) -> unsigned short {
-        return __ldg(beta_bits + (size_t)(t + min(tid, len_ - 1)) * H + h);
+        return ld_g16_pinned(beta_bits + (size_t)(t + min(tid, len_ - 1)) * H + h);
     };
     unsigned short beta_next = 0;
     if (tid < C && nt > 0) beta_next = load_beta(bos, (int)min((long)C, eos - bos));
@@ -255,6 +266,12 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
         for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)bos, sy.bar(B_GIN));
+    }
+
+    // the strictly upper 16 x 16 blocks of T diag(beta) are zero in every chunk
+    for (int idx = tid; idx < 64 * 8; idx += NGRP) {
+        const int i = idx >> 3, c8 = idx & 7;
+        if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
     }
 
     for (int c = 0; c < nt; ++c) {
@@ -268,14 +285,14 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t x = ld_s32(sb + OFF_GT + tile_off(16 * rq + i));
-                g0[i] = bf_lo(x);
-                g1[i] = bf_hi(x);
+                g0[i] = bf_0(x);
+                g1[i] = bf_1(x);
             }
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = min(16 * rq + i, len - 1);
-                GatePair<GT>::load(gptr + ((size_t)(t0 + r) * H + h) * KD + d0, g0[i], g1[i]);
+                GatePair<GT>::load(gptr + ((size_t)(t0 + r) * H + h) * KD + d0, swap, g0[i], g1[i]);
             }
         }
         if (tid < C) {
@@ -309,8 +326,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 G0[i] = acc0;
                 G1[i] = acc1;
             }
-            xch[rq * 128 + d0] = acc0;
-            xch[rq * 128 + d0 + 1] = acc1;
+            xch[rq * 128 + ch0] = acc0;
+            xch[rq * 128 + ch1] = acc1;
         }
         bar_sync(BAR_PREP, NGRP);
         if (kGateTile && tid == 0 && c + 1 < nt && !sy.aborted()) {  // g tile read: prefetch chunk c + 1
@@ -321,19 +338,21 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         {
             float c0 = 0.f, c1 = 0.f;
             for (int q2 = 0; q2 < rq; ++q2) {
-                c0 += xch[q2 * 128 + d0];
-                c1 += xch[q2 * 128 + d0 + 1];
+                c0 += xch[q2 * 128 + ch0];
+                c1 += xch[q2 * 128 + ch1];
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) { G0[i] += c0; G1[i] += c1; }
-            gmid[rq * 128 + d0] = G0[8];
-            gmid[rq * 128 + d0 + 1] = G1[8];
-            if (rq == 3) { glast[d0] = G0[15]; glast[d0 + 1] = G1[15]; }
+            gmid[rq * 128 + ch0] = G0[8];
+            gmid[rq * 128 + ch1] = G1[8];
+            if (rq == 3) { glast[ch0] = G0[15]; glast[ch1] = G1[15]; }
         }
         bar_sync(BAR_PREP, NGRP);
 
         // ---- k and q of the own rows from the tiles the chain prefetched into the k 2^G /
-        // s q 2^G hand-off buffers; every thread reads before any thread overwrites them
+        // s q 2^G hand-off buffers; every thread reads before any thread overwrites them.
+        // k 2^(Gl - G) and 2^Glast are overwritten below, so the chain's o / dH MMAs of the
+        // previous chunk (their readers) must be done as well.
         uint32_t kr[16], qr[16];
         sy.group_wait(B_QKIN, c & 1, w == 0, BAR_PREP);
 #pragma unroll
@@ -343,88 +362,108 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
             qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
         }
-        bar_sync(BAR_PREP, NGRP);
+        if (c > 0) sy.group_wait(B_OHDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
+        else       bar_sync(BAR_PREP, NGRP);
 
-        // ---- operands
-        uint32_t kd0[8], kd1[8];
+        // ---- operands: channel-major [128 ch][rows] tiles, one 16-byte chunk (8 rows) of
+        // each of the two own channels per store
         {
             const float gm0 = G0[8], gm1 = G1[8];
-            const float gl0 = glast[d0], gl1 = glast[d0 + 1];
+            const float gl0 = glast[ch0], gl1 = glast[ch1];
             const float P0 = ex2_fast(gm0), P1 = ex2_fast(gm1);              // 2^G at the midpoint
             const float L0 = ex2_fast(gl0 - gm0), L1 = ex2_fast(gl1 - gm1);  // 2^(Glast - Gmid) <= 1
             float R0[4], R1[4];  // paired offsets 2^(G_m(bi) - G_m(rq)) <= 1 for bi > rq
 #pragma unroll
             for (int bi = 0; bi < 4; ++bi) {
-                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + d0] - gm0) : 1.f;
-                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + d0 + 1] - gm1) : 1.f;
+                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
+                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+            }
+            if (rq == 3) {
+                gam[(c & 1) * 128 + ch0] = ex2_fast(G0[15]);
+                gam[(c & 1) * 128 + ch1] = ex2_fast(G1[15]);
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const uint32_t ch = 2 * rq + half;
-                uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lk0[4], lk1[4], lq0[4], lq1[4];
-                uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4];
+                const uint32_t r0 = sw128(ch0, ch), r1 = sw128(ch1, ch);
+                float kf0[8], kf1[8];  // k 2^(G_m(rq) - G) of the 8 rows
+                {
+                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lk0[4], lk1[4], lq0[4], lq1[4];
+                    uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4], kd0[4], kd1[4];
 #pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    float kv0[2], kv1[2], qv0[2], qv1[2], e0[2], e1[2], f0[2], f1[2];
+                    for (int pr = 0; pr < 4; ++pr) {
+                        float ke0[2], ke1[2], qe0[2], qe1[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 8 * half + 2 * pr + u, r = 16 * rq + i;
-                        kv0[u] = bf_lo(kr[i]);
-                        kv1[u] = bf_hi(kr[i]);
-                        qv0[u] = scale * bf_lo(qr[i]);
-                        qv1[u] = scale * bf_hi(qr[i]);
-                        e0[u] = ex2_fast(G0[i] - gm0);
-                        e1[u] = ex2_fast(G1[i] - gm1);
-                        f0[u] = ex2_fast(gm0 - G0[i]);
-                        f1[u] = ex2_fast(gm1 - G1[i]);
-                        // score columns, K-major [n][channel]: sub-block bi >= rq sees row r as
-                        // column j = r with anchor m_bi: k_j 2^(G_m(bi) - G_j) = k_j F_j R(bi)
-#pragma unroll
-                        for (int bi = 0; bi < 4; ++bi) {
-                            if (bi < rq) continue;
-                            const int nrow = sb_off(bi) + r;
-                            st_s32(sb + OFF_SB + cbp * (SB_ROWS * 128) + sw128(nrow, sw_d0) + sw_b0,
-                                   pack_bf16(kv0[u] * f0[u] * R0[bi], kv1[u] * f1[u] * R1[bi]));
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = 8 * half + 2 * pr + u;
+                            const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
+                            const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
+                            const float kv0 = bf_0(kr[i]), kv1 = bf_1(kr[i]);
+                            ke0[u] = kv0 * e0;
+                            ke1[u] = kv1 * e1;
+                            qe0[u] = scale * bf_0(qr[i]) * e0;
+                            qe1[u] = scale * bf_1(qr[i]) * e1;
+                            kf0[2 * pr + u] = kv0 * f0;
+                            kf1[2 * pr + u] = kv1 * f1;
                         }
+                        pack_split(ke0[0], ke0[1], ak0[pr], lk0[pr]);
+                        pack_split(ke1[0], ke1[1], ak1[pr], lk1[pr]);
+                        pack_split(qe0[0], qe0[1], aq0[pr], lq0[pr]);
+                        pack_split(qe1[0], qe1[1], aq1[pr], lq1[pr]);
+                        g_k0[pr] = pack_bf16(ke0[0] * P0, ke0[1] * P0);
+                        g_k1[pr] = pack_bf16(ke1[0] * P1, ke1[1] * P1);
+                        g_q0[pr] = pack_bf16(qe0[0] * P0, qe0[1] * P0);
+                        g_q1[pr] = pack_bf16(qe1[0] * P1, qe1[1] * P1);
+                        kd0[pr] = pack_bf16(kf0[2 * pr] * L0, kf0[2 * pr + 1] * L0);
+                        kd1[pr] = pack_bf16(kf1[2 * pr] * L1, kf1[2 * pr + 1] * L1);
                     }
-                    pack_split(kv0[0] * e0[0], kv0[1] * e0[1], ak0[pr], lk0[pr]);
-                    pack_split(kv1[0] * e1[0], kv1[1] * e1[1], ak1[pr], lk1[pr]);
-                    pack_split(qv0[0] * e0[0], qv0[1] * e0[1], aq0[pr], lq0[pr]);
-                    pack_split(qv1[0] * e1[0], qv1[1] * e1[1], aq1[pr], lq1[pr]);
-                    g_k0[pr] = pack_bf16(kv0[0] * e0[0] * P0, kv0[1] * e0[1] * P0);
-                    g_k1[pr] = pack_bf16(kv1[0] * e1[0] * P1, kv1[1] * e1[1] * P1);
-                    g_q0[pr] = pack_bf16(qv0[0] * e0[0] * P0, qv0[1] * e0[1] * P0);
-                    g_q1[pr] = pack_bf16(qv1[0] * e1[0] * P1, qv1[1] * e1[1] * P1);
-                    kd0[4 * half + pr] = pack_bf16(kv0[0] * f0[0] * L0, kv0[1] * f0[1] * L0);
-                    kd1[4 * half + pr] = pack_bf16(kv1[0] * f1[0] * L1, kv1[1] * f1[1] * L1);
+                    st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
+                    st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
+                    st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
+                    st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
+                    st_s128(sb + OFF_SAL + r0, lk0[0], lk0[1], lk0[2], lk0[3]);
+                    st_s128(sb + OFF_SAL + r1, lk1[0], lk1[1], lk1[2], lk1[3]);
+                    st_s128(sb + OFF_SAL + 16384 + r0, lq0[0], lq0[1], lq0[2], lq0[3]);
+                    st_s128(sb + OFF_SAL + 16384 + r1, lq1[0], lq1[1], lq1[2], lq1[3]);
+                    st_s128(sb + OFF_KG + r0, g_k0[0], g_k0[1], g_k0[2], g_k0[3]);
+                    st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
+                    st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
+                    st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
+                    st_s128(sb + OFF_KD + r0, kd0[0], kd0[1], kd0[2], kd0[3]);
+                    st_s128(sb + OFF_KD + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
                 }
-                // MN-major [channel][row] tiles: one 16-byte chunk of 8 rows per channel
-                const uint32_t r0 = sw128(d0, ch), r1 = sw128(d0 + 1, ch);
-                st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
-                st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
-                st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
-                st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
-                st_s128(sb + OFF_SAL + r0, lk0[0], lk0[1], lk0[2], lk0[3]);
-                st_s128(sb + OFF_SAL + r1, lk1[0], lk1[1], lk1[2], lk1[3]);
-                st_s128(sb + OFF_SAL + 16384 + r0, lq0[0], lq0[1], lq0[2], lq0[3]);
-                st_s128(sb + OFF_SAL + 16384 + r1, lq1[0], lq1[1], lq1[2], lq1[3]);
-                st_s128(sb + OFF_KG + r0, g_k0[0], g_k0[1], g_k0[2], g_k0[3]);
-                st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
-                st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
-                st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
+                // score columns, channel-major [128 ch][n] in groups of 64 columns: sub-block
+                // bi >= rq sees row r as column n = sb_off(bi) + r with anchor m_bi:
+                // k_r 2^(G_m(bi) - G_r) = kf_r R(bi)
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+                    if (bi < rq) continue;
+                    const uint32_t n0 = (uint32_t)(sb_off(bi) + 16 * rq + 8 * half);
+                    const uint32_t base = sb + OFF_SB + (n0 >> 6) * 16384u;
+                    const uint32_t cn = (n0 & 63u) >> 3;
+                    uint32_t s0[4], s1[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        s0[pr] = pack_bf16(kf0[2 * pr] * R0[bi], kf0[2 * pr + 1] * R0[bi]);
+                        s1[pr] = pack_bf16(kf1[2 * pr] * R1[bi], kf1[2 * pr + 1] * R1[bi]);
+                    }
+                    st_s128(base + sw128(ch0, cn), s0[0], s0[1], s0[2], s0[3]);
+                    st_s128(base + sw128(ch1, cn), s1[0], s1[1], s1[2], s1[3]);
+                }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         bar_sync(BAR_PREP, NGRP);
 
-        // ---- a2: score MMA (rows hi and lo against the causal columns); k 2^G, s q 2^G handed off
+        // ---- a2: score MMA (rows hi and lo against the causal columns); k 2^G, s q 2^G,
+        // k 2^(Gl - G) and 2^Glast handed off
         if (tid == 0 && !sy.aborted()) {
             tc_fence_after();
-            const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 0);
+            const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint64_t b = umma_desc(sb + OFF_SB + (kk >> 2) * (SB_ROWS * 128) + (kk & 3) * 32, 16, 1024);
+                uint64_t b = umma_desc(sb + OFF_SB + kk * 2048, 16384, 1024);
                 uint64_t ah = umma_desc(sb + OFF_SAH + kk * 2048, 16384, 1024);
                 uint64_t al = umma_desc(sb + OFF_SAL + kk * 2048, 16384, 1024);
                 umma_bf16(tmem + TM_S, ah, b, id_s, kk > 0);
@@ -432,21 +471,6 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
             umma_commit(sy.bar(B_SCORE));
             mbar_arrive(sy.bar(B_KQFULL));
-        }
-        // ---- while the score MMA runs: hand off k 2^(Gl - G) and 2^Glast once the chain's
-        // o / dH MMAs of the previous chunk (the readers of the buffers) are done
-        if (c > 0) sy.group_wait(B_OHDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t ch = 2 * rq + half;
-            st_s128(sb + OFF_KD + sw128(d0, ch), kd0[4 * half], kd0[4 * half + 1], kd0[4 * half + 2],
-                    kd0[4 * half + 3]);
-            st_s128(sb + OFF_KD + sw128(d0 + 1, ch), kd1[4 * half], kd1[4 * half + 1],
-                    kd1[4 * half + 2], kd1[4 * half + 3]);
-        }
-        if (rq == 3) {
-            gam[(c & 1) * 128 + d0] = ex2_fast(G0[15]);
-            gam[(c & 1) * 128 + d0 + 1] = ex2_fast(G1[15]);
         }
         sy.group_wait(B_SCORE, c & 1, w == 0, BAR_PREP);
         tc_fence_after();
@@ -498,10 +522,15 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
         }
         tc_fence_before();
-        bar_sync(BAR_PREP, NGRP);
+        // T diag(beta) is written below: the chain's v_new MMAs of the previous chunk (its
+        // readers) must be done
+        if (c > 0) sy.group_wait(B_VNDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
+        else       bar_sync(BAR_PREP, NGRP);
 
-        // ---- a3: T = (I + Akk)^-1.  Diagonal 16 x 16 blocks by forward substitution, one
-        // thread per column (warps 0-1); the strictly upper blocks are zero.
+        // ---- a3: T = (I + Akk)^-1, each block written as fp32 (for the later blocks) and
+        // straight into the bf16 T diag(beta) hand-off (K-major [64][64]; its strictly upper
+        // blocks were zeroed once).  Diagonal 16 x 16 blocks by forward substitution, one
+        // thread per column (warps 0-1).
         if (w < 2) {
             const int b = 2 * w + (l >> 4), cc = l & 15;
             float x[16];
@@ -514,10 +543,17 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
-        }
-        for (int idx = tid; idx < 64 * 64; idx += NGRP) {
-            const int i = idx >> 6, j = idx & 63;
-            if ((j >> 4) > (i >> 4)) Tf[i * LD + j] = 0.f;
+            __syncwarp();
+            // row 16 b + cc of the block, its columns scaled by beta
+            const int i = 16 * b + cc;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j0 = 16 * b + 2 * e;
+                pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
+            }
+            st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
+            st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
         }
         bar_sync(BAR_PREP, NGRP);
         // Off-diagonal blocks, level by level: T[b+L][b] = -T[b+L][b+L] (sum_t A[b+L][t] T[t][b])
@@ -570,30 +606,23 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     }
 #pragma unroll
                     for (int n8 = 0; n8 < 2; ++n8) {
-                        Tf[(r0 + gq) * LD + c0 + 8 * n8 + 2 * tq] = -ta[n8][0];
-                        Tf[(r0 + gq) * LD + c0 + 8 * n8 + 2 * tq + 1] = -ta[n8][1];
-                        Tf[(r0 + gq + 8) * LD + c0 + 8 * n8 + 2 * tq] = -ta[n8][2];
-                        Tf[(r0 + gq + 8) * LD + c0 + 8 * n8 + 2 * tq + 1] = -ta[n8][3];
+                        const int j = c0 + 8 * n8 + 2 * tq;
+                        if (lev < 3) {
+                            Tf[(r0 + gq) * LD + j] = -ta[n8][0];
+                            Tf[(r0 + gq) * LD + j + 1] = -ta[n8][1];
+                            Tf[(r0 + gq + 8) * LD + j] = -ta[n8][2];
+                            Tf[(r0 + gq + 8) * LD + j + 1] = -ta[n8][3];
+                        }
+                        const float b0 = -bsm[j], b1 = -bsm[j + 1];
+                        const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
+                        st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(ta[n8][0] * b0, ta[n8][1] * b1));
+                        st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(ta[n8][2] * b0, ta[n8][3] * b1));
                     }
                 }
+                if (lev == 3) fence_proxy_async_smem();  // the hand-off is complete
                 bar_sync(BAR_PREP, NGRP);
             }
         }
-
-        // ---- hand off T diag(beta) once the chain's v_new MMAs of the previous chunk are done
-        if (c > 0) sy.group_wait(B_VNDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
-        for (int idx = tid; idx < 64 * 8; idx += NGRP) {
-            const int i = idx >> 3, c8 = idx & 7;
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j0 = 8 * c8 + 2 * e;
-                pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
-            }
-            st_s128(sb + OFF_TP + sw128(i, c8), pk[0], pk[1], pk[2], pk[3]);
-        }
-        fence_proxy_async_smem();
-        bar_sync(BAR_PREP, NGRP);
         if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
     }
 }
