@@ -65,31 +65,32 @@ constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;  // named barriers of the groups
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T          [chain]
 constexpr uint32_t OFF_GT = 16384;     // g tile (TMA, bf16 gate only), 16 KB               [prep]
-constexpr uint32_t OFF_SAH = 32768;    // score rows hi [128 ch][128 rows] MN-major      [prep]
-constexpr uint32_t OFF_SAL = 65536;    // score rows lo
-constexpr uint32_t OFF_SB = 98304;     // score cols [128 ch][160] MN-major, 3 groups of 64 columns
+constexpr uint32_t OFF_SAH = 32768;    // score rows hi [128 ch][128 rows] MN-major (k rows 0-63,
+                                       //   q rows 64-127; 16 KB each)                      [prep]
+constexpr uint32_t OFF_SALQ = 65536;   // score rows lo of the q rows [128 ch][64 rows], 16 KB
+constexpr uint32_t OFF_SB = 81920;     // score cols [128 ch][160] MN-major, 3 groups of 64 columns
                                        //   (16 KB each), 48 KB
 constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
 constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
 constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [3][16][24]
-constexpr uint32_t OFF_KG = 147456;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_KG = 131072;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
-constexpr uint32_t OFF_QG = 163840;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_QG = 147456;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's q tile (TMA)
-constexpr uint32_t OFF_KD = 180224;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
-constexpr uint32_t OFF_TP = 196608;    // hand-off: T diag(beta) bf16 [64][64] K-major B
-constexpr uint32_t OFF_AQKH = 204800;  // hand-off: Aqk hi [64][64]
-constexpr uint32_t OFF_AQKL = 212992;  // hand-off: Aqk lo [64][64]
-constexpr uint32_t OFF_GAM = 221184;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
-constexpr uint32_t OFF_BETA = 222208;  // prep: beta fp32 [64]
-constexpr uint32_t OFF_XCH = 222464;   // prep: fp32 [4][128] per-sub-block gate sums
-constexpr uint32_t OFF_GM = 224512;    // prep: fp32 [4][128] G at the sub-block midpoints
-constexpr uint32_t OFF_GL = 226560;    // prep: fp32 [128] G at the last row
-constexpr uint32_t OFF_BAR = 227072;   // mbarriers (8 bytes each)
-constexpr uint32_t OFF_MISC = 227168;  // tmem base, abort flag
-constexpr uint32_t SMEM_BYTES = 227184 + 1024;  // + alignment slack
+constexpr uint32_t OFF_KD = 163840;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
+constexpr uint32_t OFF_TP = 180224;    // hand-off: T diag(beta) bf16 [64][64] K-major B
+constexpr uint32_t OFF_AQKH = 188416;  // hand-off: Aqk hi [64][64]
+constexpr uint32_t OFF_AQKL = 196608;  // hand-off: Aqk lo [64][64]
+constexpr uint32_t OFF_GAM = 204800;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
+constexpr uint32_t OFF_BETA = 205824;  // prep: beta fp32 [64]
+constexpr uint32_t OFF_XCH = 206080;   // prep: fp32 [4][128] per-sub-block gate sums
+constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block midpoints
+constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
+constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
+constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
+constexpr uint32_t SMEM_BYTES = 210800 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
-static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 3 * 16 * 24 * 4 <= OFF_SB + 3 * 16384, "layout");
+static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 3 * 16 * 24 * 4 <= OFF_SB, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
 
@@ -388,7 +389,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 const uint32_t r0 = sw128(ch0, ch), r1 = sw128(ch1, ch);
                 float kf0[8], kf1[8];  // k 2^(G_m(rq) - G) of the 8 rows
                 {
-                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lk0[4], lk1[4], lq0[4], lq1[4];
+                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lq0[4], lq1[4];
                     uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4], kd0[4], kd1[4];
 #pragma unroll
                     for (int pr = 0; pr < 4; ++pr) {
@@ -406,8 +407,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                             kf0[2 * pr + u] = kv0 * f0;
                             kf1[2 * pr + u] = kv1 * f1;
                         }
-                        pack_split(ke0[0], ke0[1], ak0[pr], lk0[pr]);
-                        pack_split(ke1[0], ke1[1], ak1[pr], lk1[pr]);
+                        ak0[pr] = pack_bf16(ke0[0], ke0[1]);
+                        ak1[pr] = pack_bf16(ke1[0], ke1[1]);
                         pack_split(qe0[0], qe0[1], aq0[pr], lq0[pr]);
                         pack_split(qe1[0], qe1[1], aq1[pr], lq1[pr]);
                         g_k0[pr] = pack_bf16(ke0[0] * P0, ke0[1] * P0);
@@ -421,10 +422,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
                     st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
                     st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
-                    st_s128(sb + OFF_SAL + r0, lk0[0], lk0[1], lk0[2], lk0[3]);
-                    st_s128(sb + OFF_SAL + r1, lk1[0], lk1[1], lk1[2], lk1[3]);
-                    st_s128(sb + OFF_SAL + 16384 + r0, lq0[0], lq0[1], lq0[2], lq0[3]);
-                    st_s128(sb + OFF_SAL + 16384 + r1, lq1[0], lq1[1], lq1[2], lq1[3]);
+                    st_s128(sb + OFF_SALQ + r0, lq0[0], lq0[1], lq0[2], lq0[3]);
+                    st_s128(sb + OFF_SALQ + r1, lq1[0], lq1[1], lq1[2], lq1[3]);
                     st_s128(sb + OFF_KG + r0, g_k0[0], g_k0[1], g_k0[2], g_k0[3]);
                     st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
                     st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
@@ -456,8 +455,10 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         tc_fence_before();
         bar_sync(BAR_PREP, NGRP);
 
-        // ---- a2: score MMA (rows hi and lo against the causal columns); k 2^G, s q 2^G,
-        // k 2^(Gl - G) and 2^Glast handed off
+        // ---- a2: score MMA against the causal columns: rows hi, then the q rows' lo with the
+        // k rows' hi a second time (the k-row scores come out doubled, exactly; the lo part of
+        // the k rows is below the accuracy the path needs).  k 2^G, s q 2^G, k 2^(Gl - G) and
+        // 2^Glast handed off
         if (tid == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
@@ -465,7 +466,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             for (int kk = 0; kk < 8; ++kk) {
                 uint64_t b = umma_desc(sb + OFF_SB + kk * 2048, 16384, 1024);
                 uint64_t ah = umma_desc(sb + OFF_SAH + kk * 2048, 16384, 1024);
-                uint64_t al = umma_desc(sb + OFF_SAL + kk * 2048, 16384, 1024);
+                uint64_t al = umma_desc(sb + OFF_SAH + kk * 2048, OFF_SALQ - OFF_SAH, 1024);
                 umma_bf16(tmem + TM_S, ah, b, id_s, kk > 0);
                 umma_bf16(tmem + TM_S, al, b, id_s, 1);
             }
@@ -504,7 +505,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 }
             }
             if (!is_q) {
-                const float b_i = bsm[i];
+                const float b_i = 0.5f * bsm[i];  // the k-row scores are doubled
 #pragma unroll
                 for (int j = 0; j < 64; ++j) As[j * LD + i] = (j < i) ? b_i * sv[j] : 0.f;  // Akk^T
             } else {
