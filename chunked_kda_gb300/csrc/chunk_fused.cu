@@ -72,7 +72,7 @@ constexpr uint32_t OFF_SB = 81920;     // score cols [128 ch][160] MN-major, 3 g
                                        //   (16 KB each), 48 KB
 constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
 constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
-constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [3][16][24]
+constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [4][16][24]
 constexpr uint32_t OFF_KG = 131072;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
 constexpr uint32_t OFF_QG = 147456;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
@@ -90,7 +90,7 @@ constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
 constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
 constexpr uint32_t SMEM_BYTES = 210800 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
-static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 3 * 16 * 24 * 4 <= OFF_SB, "layout");
+static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
 
@@ -476,49 +476,56 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         sy.group_wait(B_SCORE, c & 1, w == 0, BAR_PREP);
         tc_fence_after();
 
-        // ---- read the scores: warps 0-1 Akk rows (beta-scaled, strictly lower) into the solve
-        // matrix, warps 2-3 Aqk rows (hi, lo) straight into the hand-off buffers
-        if (w < 4) {
-            const int row = 32 * w + l;  // TMEM lane
+        // ---- read the scores, all eight warps: warps w and w + 4 share the TMEM lanes of
+        // quadrant w & 3 and take alternate 16-column pieces of each row.  Akk rows (lanes
+        // 0-63: beta-scaled, strictly lower) go into the solve matrix, Aqk rows (lanes 64-127:
+        // hi, lo) straight into the hand-off buffers.
+        {
+            const int lq = w & 3, part = w >> 2;
+            const int row = 32 * lq + l;  // TMEM lane
             const int i = row & 63;
             const bool is_q = row >= 64;
             const int bi = i >> 4;
-            // the 32 lanes of this warp hold two sub-blocks (bmin, bmin + 1); every lane
-            // loads the columns of both (warp-collective loads), then keeps its own
-            const int bmin = 2 * (w & 1);
-            float sv[64];
+            // the 32 lanes of the quadrant hold two sub-blocks (bmin, bmin + 1); the warp loads
+            // the piece of both (warp-collective loads), every lane keeps its own
+            const int bmin = 2 * (lq & 1);
+            const bool own_a = bi == bmin;
+            const float b_i = 0.5f * bsm[i];  // the k-row scores are doubled
+            const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16) + TM_S;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) sv[j] = 0.f;
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = part + 2 * tt;  // columns 16 t .. 16 t + 15 of the row
+                float va[16], vb[16];
 #pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                const int bb = bmin + sub;
+                for (int e = 0; e < 16; ++e) { va[e] = 0.f; vb[e] = 0.f; }
+                if (t <= bmin) tmem_ld16(tl + sb_off(bmin) + 16 * t, va);
+                if (t <= bmin + 1) tmem_ld16(tl + sb_off(bmin + 1) + 16 * t, vb);
+                if (t <= bmin + 1) tmem_wait_ld();
+                float sv[16];
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    if (t <= bb) {
-                        float tmp[16];
-                        tmem_ld16(tmem + ((uint32_t)(32 * w) << 16) + TM_S + sb_off(bb) + 16 * t, tmp);
-                        tmem_wait_ld();
+                for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
+                if (!is_q) {
+                    if (t <= bi) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (bi == bb) sv[16 * t + e] = tmp[e];
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = 16 * t + e;
+                            As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;  // Akk^T
+                        }
                     }
-                }
-            }
-            if (!is_q) {
-                const float b_i = 0.5f * bsm[i];  // the k-row scores are doubled
+                } else {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) As[j * LD + i] = (j < i) ? b_i * sv[j] : 0.f;  // Akk^T
-            } else {
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j0 = 8 * c8 + 2 * e;
-                        pack_split(j0 <= i ? sv[j0] : 0.f, j0 + 1 <= i ? sv[j0 + 1] : 0.f, hi[e], lo[e]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int j0 = 16 * t + 8 * c2 + 2 * e;
+                            const float x0 = (j0 <= i) ? sv[8 * c2 + 2 * e] : 0.f;
+                            const float x1 = (j0 + 1 <= i) ? sv[8 * c2 + 2 * e + 1] : 0.f;
+                            pack_split(x0, x1, hi[e], lo[e]);
+                        }
+                        st_s128(sb + OFF_AQKH + sw128(i, 2 * t + c2), hi[0], hi[1], hi[2], hi[3]);
+                        st_s128(sb + OFF_AQKL + sw128(i, 2 * t + c2), lo[0], lo[1], lo[2], lo[3]);
                     }
-                    st_s128(sb + OFF_AQKH + sw128(i, c8), hi[0], hi[1], hi[2], hi[3]);
-                    st_s128(sb + OFF_AQKL + sw128(i, c8), lo[0], lo[1], lo[2], lo[3]);
                 }
             }
         }
@@ -557,72 +564,101 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
         }
         bar_sync(BAR_PREP, NGRP);
-        // Off-diagonal blocks, level by level: T[b+L][b] = -T[b+L][b+L] (sum_t A[b+L][t] T[t][b])
-        // over blocks t = b .. b+L-1; warp b computes one block with m16n8k8 tf32 MMAs
+        // Off-diagonal blocks as a 2 x 2 recursion on 32 x 32 blocks, with m16n8k8 tf32 MMAs
         // (fragments: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
-        //  c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]; g = lane / 4, t = lane % 4).
+        //  c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]; g = lane / 4, t = lane % 4):
+        //  1. T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)                      (warps 0, 1)
+        //  2. X[r][c] = sum_{t=c..1} A[r][t] T[t][c]                  r = 2, 3; c = 0, 1 (warps 0-3)
+        //  3. T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]                                  (warps 0-3)
+        // Every finished block goes into the bf16 T diag(beta) hand-off; T10 and T32 also
+        // into the fp32 T for step 2 and 3.
         {
             const int gq = l >> 2, tq = l & 3;
-#pragma unroll 1
-            for (int lev = 1; lev < 4; ++lev) {
-                if (w < 4 - lev) {
-                    const int b = w, r0 = 16 * (b + lev), c0 = 16 * b;
-                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int ks = 0; ks < 2 * lev; ++ks) {
-                        const int kc = c0 + 8 * ks;
-                        uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
-                                         to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
-                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
-                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
-#pragma unroll
-                        for (int n8 = 0; n8 < 2; ++n8) {
-                            uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + c0 + 8 * n8 + gq]),
-                                              to_tf32(Tf[(kc + tq + 4) * LD + c0 + 8 * n8 + gq])};
-                            mma_tf32_16x8x8(xa[n8], a, bb);
-                        }
-                    }
-                    float* X = Xs + w * (16 * 24);
+            // acc += A[r0.., kc0 .. kc0 + 8 nk) T[.., n0 .. n0 + 16), A read from its transpose
+            auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
+                for (int ks = 0; ks < nk; ++ks) {
+                    const int kc = kc0 + 8 * ks;
+                    uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
+                                     to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
+                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
+                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
 #pragma unroll
                     for (int n8 = 0; n8 < 2; ++n8) {
-                        X[gq * 24 + 8 * n8 + 2 * tq] = xa[n8][0];
-                        X[gq * 24 + 8 * n8 + 2 * tq + 1] = xa[n8][1];
-                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = xa[n8][2];
-                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = xa[n8][3];
-                    }
-                    __syncwarp();
-                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const int kc = r0 + 8 * ks;
-                        uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]),
-                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
-                                         to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
-                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
-#pragma unroll
-                        for (int n8 = 0; n8 < 2; ++n8) {
-                            uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
-                                              to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
-                            mma_tf32_16x8x8(ta[n8], a, bb);
-                        }
-                    }
-#pragma unroll
-                    for (int n8 = 0; n8 < 2; ++n8) {
-                        const int j = c0 + 8 * n8 + 2 * tq;
-                        if (lev < 3) {
-                            Tf[(r0 + gq) * LD + j] = -ta[n8][0];
-                            Tf[(r0 + gq) * LD + j + 1] = -ta[n8][1];
-                            Tf[(r0 + gq + 8) * LD + j] = -ta[n8][2];
-                            Tf[(r0 + gq + 8) * LD + j + 1] = -ta[n8][3];
-                        }
-                        const float b0 = -bsm[j], b1 = -bsm[j + 1];
-                        const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
-                        st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(ta[n8][0] * b0, ta[n8][1] * b1));
-                        st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(ta[n8][2] * b0, ta[n8][3] * b1));
+                        uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
+                                          to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
+                        mma_tf32_16x8x8(acc[n8], a, bb);
                     }
                 }
-                if (lev == 3) fence_proxy_async_smem();  // the hand-off is complete
-                bar_sync(BAR_PREP, NGRP);
+            };
+            // acc += T[r0.., k0 .. k0 + 16) X, X a 16 x 16 block stored with row stride 24
+            auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int kc = k0 + 8 * ks;
+                    uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]),
+                                     to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
+                                     to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
+                                     to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
+                                          to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
+                        mma_tf32_16x8x8(acc[n8], a, bb);
+                    }
+                }
+            };
+            auto store_X = [&](float* X, const float (&acc)[2][4]) {
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8) {
+                    X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
+                    X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
+                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
+                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
+                }
+            };
+            // T[r0.., c0..] = -acc: the hand-off (times beta of the columns), optionally fp32 T
+            auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8) {
+                    const int j = c0 + 8 * n8 + 2 * tq;
+                    if (keep) {
+                        Tf[(r0 + gq) * LD + j] = -acc[n8][0];
+                        Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
+                        Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
+                        Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
+                    }
+                    const float b0 = -bsm[j], b1 = -bsm[j + 1];
+                    const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
+                    st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
+                    st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
+                }
+            };
+            if (w < 2) {  // step 1
+                const int r0 = 32 * w + 16, c0 = 32 * w;
+                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_A_T(xa, r0, c0, 2, c0);
+                float* X = Xs + w * (16 * 24);
+                store_X(X, xa);
+                __syncwarp();
+                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_T_X(ta, r0, r0, X);
+                store_T(r0, c0, ta, true);
             }
+            bar_sync(BAR_PREP, NGRP);
+            const int rb = 2 + (w >> 1), cb = w & 1;  // block (rb, cb) of warp w < 4
+            if (w < 4) {  // step 2
+                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_A_T(xa, 16 * rb, 16 * cb, 4 - 2 * cb, 16 * cb);
+                store_X(Xs + w * (16 * 24), xa);
+            }
+            bar_sync(BAR_PREP, NGRP);
+            if (w < 4) {  // step 3
+                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int s = 2; s <= rb; ++s) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
+                store_T(16 * rb, 16 * cb, ta, false);
+            }
+            fence_proxy_async_smem();  // the hand-off is complete
+            bar_sync(BAR_PREP, NGRP);
         }
         if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
     }
