@@ -124,7 +124,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
     const bool any_tokens = (long long)B * T > 0 && N > 0;
     if (any_tokens && (!q || !k || !v || !g || !beta || !o))
         return fail(KDA_ERR_INVALID_ARG, "null q, k, v, g, beta or o");
-    const void* ptrs[] = {q, k, v, g, o, initial_state, final_state, A_log, dt_bias};
+    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;
@@ -158,7 +158,7 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
     const bool any_tokens = (long long)B * T > 0 && N > 0;
     if (any_tokens && (!q || !k || !v || !gate || !beta || !o))
         return fail(KDA_ERR_INVALID_ARG, "null q, k, v, gate, beta or o");
-    const void* ptrs[] = {q, k, v, gate, o, initial_state, final_state};
+    const void* ptrs[] = {q, k, v, gate, beta, o, initial_state, final_state};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;

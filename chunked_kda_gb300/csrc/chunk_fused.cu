@@ -88,7 +88,8 @@ constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block
 constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
 constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
-constexpr uint32_t SMEM_BYTES = 210800 + 1024;  // + alignment slack
+constexpr uint32_t OFF_BRAW = 210816;  // prep: raw beta words of the next chunk [64]
+constexpr uint32_t SMEM_BYTES = 211072 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
@@ -139,13 +140,14 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
                  : "memory");
 }
 
-// a 16-bit global load the compiler keeps where it is written (issued one chunk ahead of its
-// use, it must not be re-issued next to the use)
-__device__ __forceinline__ unsigned short ld_g16_pinned(const unsigned short* p) {
-    unsigned short v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
+// asynchronous 4-byte global -> shared copy that reads only the first `src_bytes` bytes
+// (the rest is zero-filled); both addresses 4-byte aligned
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
@@ -253,15 +255,21 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
 
-    // beta of the next chunk is loaded one chunk ahead (threads 0-63, one row each); the raw
-    // bits stay in flight until the store, so no thread waits on the load
-    // (a clamped, always valid row; the mask is applied when the value is stored)
+    // beta of the next chunk is copied one chunk ahead (threads 0-63, one row each, from a
+    // clamped, always valid row; the mask is applied when the value is used) by an
+    // asynchronous copy into shared memory, so no register waits on it.  The copy takes the
+    // aligned 4-byte word holding the element: the element and the one before it for an odd
+    // element index, the element alone (zero-filled to 4 bytes) for an even one.
     const unsigned short* beta_bits = reinterpret_cast<const unsigned short*>(p.beta);
-    auto load_beta = [&](long t, int len_) -> unsigned short {
-        return ld_g16_pinned(beta_bits + (size_t)(t + min(tid, len_ - 1)) * H + h);
+    uint32_t* braw = reinterpret_cast<uint32_t*>(smem + OFF_BRAW);
+    bool beta_odd = false;
+    auto load_beta = [&](long t, int len_) {
+        const size_t idx = (size_t)(t + min(tid, len_ - 1)) * H + h;
+        beta_odd = idx & 1;
+        cp_async4(sb + OFF_BRAW + 4 * tid, beta_bits + (idx & ~(size_t)1), beta_odd ? 4u : 2u);
+        cp_async_commit();
     };
-    unsigned short beta_next = 0;
-    if (tid < C && nt > 0) beta_next = load_beta(bos, (int)min((long)C, eos - bos));
+    if (tid < C && nt > 0) load_beta(bos, (int)min((long)C, eos - bos));
 
     if (kGateTile && tid == 0 && nt > 0) {
         mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
@@ -297,8 +305,10 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
         }
         if (tid < C) {
-            bsm[tid] = (tid < len) ? __uint_as_float((uint32_t)beta_next << 16) : 0.f;
-            if (c + 1 < nt) beta_next = load_beta(t0 + C, (int)min((long)C, eos - t0 - C));
+            cp_async_wait_all();
+            const uint32_t x = braw[tid];
+            bsm[tid] = (tid < len) ? __uint_as_float(beta_odd ? (x & 0xFFFF0000u) : (x << 16)) : 0.f;
+            if (c + 1 < nt) load_beta(t0 + C, (int)min((long)C, eos - t0 - C));
         }
 
         // ---- a1: gate, chunk-local cumsum (log2 units), sub-block carries
@@ -464,9 +474,9 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint64_t b = umma_desc(sb + OFF_SB + kk * 2048, 16384, 1024);
-                uint64_t ah = umma_desc(sb + OFF_SAH + kk * 2048, 16384, 1024);
-                uint64_t al = umma_desc(sb + OFF_SAH + kk * 2048, OFF_SALQ - OFF_SAH, 1024);
+                uint64_t b = desc_at(umma_desc(sb + OFF_SB, 16384, 1024), kk * 2048);
+                uint64_t ah = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
+                uint64_t al = desc_at(umma_desc(sb + OFF_SAH, OFF_SALQ - OFF_SAH, 1024), kk * 2048);
                 umma_bf16(tmem + TM_S, ah, b, id_s, kk > 0);
                 umma_bf16(tmem + TM_S, al, b, id_s, 1);
             }
@@ -731,8 +741,8 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             const uint32_t id_y = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint64_t bk = umma_desc(sb + OFF_KG + kk * 2048, 16384, 1024);
-                uint64_t bq = umma_desc(sb + OFF_QG + kk * 2048, 16384, 1024);
+                uint64_t bk = desc_at(umma_desc(sb + OFF_KG, 16384, 1024), kk * 2048);
+                uint64_t bq = desc_at(umma_desc(sb + OFF_QG, 16384, 1024), kk * 2048);
                 umma_bf16_ta(tmem + TM_Y, tmem + TM_VN + 8 * kk, bk, id_y, kk > 0);
                 umma_bf16_ta(tmem + TM_O, tmem + TM_VN + 8 * kk, bq, id_y, kk > 0);
             }
@@ -779,13 +789,13 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
                 const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    uint64_t a = umma_desc(vbuf + kk * 2048, 8192, 1024);
-                    uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
+                    uint64_t a = desc_at(umma_desc(vbuf, 8192, 1024), kk * 2048);
+                    uint64_t b = desc_at(umma_desc(sb + OFF_TP, 16, 1024), kk * 32);
                     umma_bf16(tmem + TM_VN, a, b, id_v, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    uint64_t b = umma_desc(sb + OFF_TP + kk * 32, 16, 1024);
+                    uint64_t b = desc_at(umma_desc(sb + OFF_TP, 16, 1024), kk * 32);
                     umma_bf16_ta(tmem + TM_VN, tmem + TM_YA + 8 * kk, b, id_n, 1);
                 }
                 umma_commit(sy.bar(B_VNDONE));
@@ -817,9 +827,9 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t ah = tmem + TM_Y + 8 * kk, al = tmem + TM_Y + 32 + 8 * kk;
-                uint64_t boh = umma_desc(sb + OFF_AQKH + kk * 32, 16, 1024);
-                uint64_t bol = umma_desc(sb + OFF_AQKL + kk * 32, 16, 1024);
-                uint64_t bk = umma_desc(sb + OFF_KD + kk * 32, 16, 1024);
+                uint64_t boh = desc_at(umma_desc(sb + OFF_AQKH, 16, 1024), kk * 32);
+                uint64_t bol = desc_at(umma_desc(sb + OFF_AQKL, 16, 1024), kk * 32);
+                uint64_t bk = desc_at(umma_desc(sb + OFF_KD, 16, 1024), kk * 32);
                 umma_bf16_ta(tmem + TM_O, ah, boh, id_o, 1);
                 umma_bf16_ta(tmem + TM_O, al, boh, id_o, 1);
                 umma_bf16_ta(tmem + TM_O, ah, bol, id_o, 1);

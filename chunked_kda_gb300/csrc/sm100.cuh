@@ -122,6 +122,9 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)(layout & 7) << 61;
     return d;
 }
+// The descriptor of the same matrix `bytes` further on (a multiple of 16): only the start
+// address field changes, and it cannot overflow for shared-memory addresses below 256 KB.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 // Instruction descriptor of kind::f16 with bf16 A/B and f32 accumulation.
 // a_mn / b_mn: operand stored MN-major (M or N index contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn, int neg_a = 0,
