@@ -57,8 +57,8 @@ def load(path: str | None = None):
             ip = ctypes.POINTER(ctypes.c_int32)
             lib.kda_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_double,
                                            dp, dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, ip,
-                                           ctypes.c_int, ctypes.c_int]
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
+                                           ctypes.c_double, ip, ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_fwd.restype = ctypes.c_int
             lib.kda_oracle_gate.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_double, ip,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -129,10 +129,16 @@ def gate(g, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0, cu_seqle
     return out
 
 
+Q_L2NORM_EPS = 1e-6  # eps floor of the optional query l2 normalisation
+
+
 def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
-            initial_state=None, cu_seqlens=None, units=None, nthreads=0, lib=None):
+            initial_state=None, cu_seqlens=None, units=None, nthreads=0, lib=None,
+            q_l2norm=False):
     """Token-by-token float64 KDA forward.
 
+    ``q_l2norm``: each query row is first replaced by q / sqrt(sum q^2 + Q_L2NORM_EPS)
+    (attention-gym PR #345 "Fuse q l2norm into the chunk_kda output kernel").
     Returns (o [B,T,H,V] float64, final_state [N,H,K,V] float64).  Rows of o
     outside every sequence (and rows of units not listed in ``units``) are NaN.
     """
@@ -151,6 +157,7 @@ def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bo
     rc = _load(lib).kda_oracle_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(al), _dptr(db),
                                 int(mode), float(lower_bound), _dptr(beta), _dptr(S0), _dptr(ST),
                                 _iptr(cu), 0 if cu is None else N, B, T, H, K, V, _dptr(o),
+                                float(Q_L2NORM_EPS if q_l2norm else -1.0),
                                 _iptr(un), 0 if un is None else un.shape[0], int(nthreads))
     if rc != 0:
         raise ValueError(f"kda_oracle_fwd failed ({rc})")

@@ -31,6 +31,10 @@
  *     dt_bias optional.
  *   - FLA skill page "fla-kda", section "Safe gate numerical note": the gate is
  *     in natural-log units before the RCP_LN2 (1/ln 2) conversion to base 2.
+ *   - attention-gym PR #345 "Fuse q l2norm into the chunk_kda output kernel"
+ *     (optional, q_eps >= 0): every query row is first normalised,
+ *     q_t <- q_t / sqrt(sum_d q_t[d]^2 + q_eps), the l2norm of the inference
+ *     callers (its eps floor); keys are not touched.
  *
  * Layouts (all contiguous, row-major):
  *   q, k, g : [B, T, H, K]      v, o : [B, T, H, V]      beta : [B, T, H]
@@ -122,8 +126,8 @@ int kda_oracle_gate(const double* g, const double* A_log, const double* dt_bias,
 static void run_unit(const double* q, const double* k, const double* v, const double* g,
                      const double* A_log, const double* dt_bias, int mode, double lb,
                      const double* beta, const double* S0, double* ST, double* o,
-                     long bos, long eos, int n, int h, int H, int K, int V, double* S,
-                     double* r)
+                     long bos, long eos, int n, int h, int H, int K, int V, double q_eps,
+                     double* S, double* r)
 {
     size_t st_off = ((size_t)n * H + h) * (size_t)K * V;
     if (S0) memcpy(S, S0 + st_off, sizeof(double) * (size_t)K * V);
@@ -152,10 +156,16 @@ static void run_unit(const double* q, const double* k, const double* v, const do
         /* S += beta_t k_t (v_t - r)^T */
         for (int d = 0; d < K; ++d)
             for (int j = 0; j < V; ++j) S[(size_t)d * V + j] += bt * kt[d] * (vt[j] - r[j]);
-        /* o_t = S^T q_t / sqrt(K) */
+        /* o_t = S^T q_t / sqrt(K), q_t optionally l2-normalised first */
+        double qs = 1.0;
+        if (q_eps >= 0.0) {
+            double ss = 0.0;
+            for (int d = 0; d < K; ++d) ss += qt[d] * qt[d];
+            qs = 1.0 / sqrt(ss + q_eps);
+        }
         for (int j = 0; j < V; ++j) {
             double acc = 0.0;
-            for (int d = 0; d < K; ++d) acc += S[(size_t)d * V + j] * qt[d];
+            for (int d = 0; d < K; ++d) acc += S[(size_t)d * V + j] * (qt[d] * qs);
             ot[j] = acc * scale;
         }
     }
@@ -166,6 +176,7 @@ static void run_unit(const double* q, const double* k, const double* v, const do
 /*
  * Full forward over every unit, or over the listed units only.
  *   units / n_units : optional list of (n, h) pairs (2 * n_units ints); NULL = all.
+ *   q_eps           : < 0: q as given; >= 0: each q row l2-normalised with this eps floor.
  *   nthreads        : OpenMP threads over independent units (<= 0: library default).
  * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
  * Outputs of units not computed, and o rows outside every sequence, are not written.
@@ -174,7 +185,7 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                    const double* A_log, const double* dt_bias, int mode, double lb,
                    const double* beta, const double* S0, double* ST,
                    const int32_t* cu, int n_seqs, int B, int T, int H, int K, int V,
-                   double* o, const int32_t* units, int n_units, int nthreads)
+                   double* o, double q_eps, const int32_t* units, int n_units, int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !o || H <= 0 || K <= 0 || V <= 0) return 1;
     if (mode == ORC_GATE_SAFE && !A_log) return 1;
@@ -201,7 +212,7 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                 long bos, eos;
                 seq_bounds(cu, n, T, &bos, &eos);
                 run_unit(q, k, v, g, A_log, dt_bias, mode, lb, beta, S0, ST, o, bos, eos, n,
-                         h, H, K, V, S, r);
+                         h, H, K, V, q_eps, S, r);
             }
         }
         free(S);

@@ -280,7 +280,47 @@ def pin_varlen_contract(lib=None):
         assert np.array_equal(on[0], o[0, sl]) and np.array_equal(Sn[0], ST[n])
 
 
+def pin_q_l2norm_single_token(lib=None):
+    """Query l2 normalisation (attention-gym PR #345, eps floor of the callers' l2norm): one
+    token, S_1 = S' + beta k (v - S'^T k)^T with S' = Diag(e^a) S0, o = S_1^T q^ / sqrt(K),
+    q^ = q / sqrt(|q|^2 + eps); the state does not see q."""
+    r = _rng(10)
+    K, V = 5, 4
+    k = _unit(r.normal(size=(1, 1, 1, K)))
+    q = 3.7 * r.normal(size=(1, 1, 1, K))
+    v = r.normal(size=(1, 1, 1, V))
+    g = -r.uniform(0.01, 2.0, size=(1, 1, 1, K))
+    beta = np.array([[[0.6]]])
+    S0 = r.normal(size=(1, 1, K, V))
+    o, ST = oracle.forward(q, k, v, g, beta, mode=oracle.GATE_PRE, initial_state=S0, lib=lib,
+                           q_l2norm=True)
+    Sd = np.exp(g[0, 0, 0])[:, None] * S0[0, 0]
+    kk, qq = k[0, 0, 0], q[0, 0, 0]
+    S1 = Sd + 0.6 * np.outer(kk, v[0, 0, 0] - Sd.T @ kk)
+    qh = qq / math.sqrt(qq @ qq + oracle.Q_L2NORM_EPS)
+    assert np.allclose(ST[0, 0], S1, atol=1e-12)
+    assert np.allclose(o[0, 0, 0], S1.T @ qh / math.sqrt(K), atol=1e-12)
+
+
+def pin_q_l2norm_rows(lib=None):
+    """The read-out is linear in the query row, so normalising row t scales o_t by
+    1 / sqrt(|q_t|^2 + eps): rows scaled by 1e-3 .. 1e3 and all-zero rows; the final
+    state is the same bit for bit."""
+    c = _random_case(11, T=24)
+    r = _rng(12)
+    scales = 10.0 ** r.uniform(-3, 3, size=(1, 24, 2, 1))
+    scales[0, 5] = 0.0  # zero query rows (both heads)
+    scales[0, 17, 1] = 0.0
+    c["q"] = c["q"] * scales
+    o1, s1 = oracle.forward(**c, lib=lib)
+    o2, s2 = oracle.forward(**c, lib=lib, q_l2norm=True)
+    assert np.array_equal(s1, s2)
+    ss = (c["q"] ** 2).sum(-1, keepdims=True)
+    assert np.allclose(o2, o1 / np.sqrt(ss + oracle.Q_L2NORM_EPS), rtol=1e-12, atol=1e-14)
+    assert (o2[0, 5] == 0).all() and (o2[0, 17, 1] == 0).all()
+
+
 ALL_PINS = [pin_gate_points, pin_gate_cumsum_closed_form, pin_gate_chunk1_is_per_token,
             pin_hand_worked, pin_beta_zero, pin_linear_attention, pin_one_hot_gated,
             pin_repeated_key_ema, pin_single_token_delta, pin_scale_exact, pin_state_carry,
-            pin_varlen_contract]
+            pin_varlen_contract, pin_q_l2norm_single_token, pin_q_l2norm_rows]

@@ -16,8 +16,11 @@ MUTANTS = [
     ("no_decay", "S[(size_t)d * V + j] *= decay;", "(void)decay;"),
     ("delta_sign", "(vt[j] - r[j])", "(r[j] - vt[j])"),
     ("no_beta", "bt * kt[d] * (vt[j] - r[j])", "kt[d] * (vt[j] - r[j])"),
-    ("readout_transposed", "acc += S[(size_t)d * V + j] * qt[d];",
-     "acc += S[(size_t)j * V + d] * qt[d];"),
+    ("readout_transposed", "acc += S[(size_t)d * V + j] * (qt[d] * qs);",
+     "acc += S[(size_t)j * V + d] * (qt[d] * qs);"),
+    ("qnorm_no_sqrt", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / (ss + q_eps);"),
+    ("qnorm_no_eps", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / sqrt(ss);"),
+    ("qnorm_abs_sum", "ss += qt[d] * qt[d];", "ss += fabs(qt[d]);"),
     ("no_scale", "ot[j] = acc * scale;", "ot[j] = acc;"),
     ("r_uses_q", "r[j] += S[(size_t)d * V + j] * kt[d];", "r[j] += S[(size_t)d * V + j] * qt[d];"),
     ("sigmoid_sign", "exp(-z)", "exp(z)"),
