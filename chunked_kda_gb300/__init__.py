@@ -14,13 +14,14 @@ import threading
 
 import torch
 
-__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_chunk_fwd_noalloc",
-           "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE", "NOALLOC_SCRATCH_BYTES",
-           "library_path", "load_library"]
+__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_chunk_fwd_ex",
+           "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
+           "FLAG_Q_L2NORM", "NOALLOC_SCRATCH_BYTES", "library_path", "load_library"]
 
 GATE_PRE = 0
 GATE_SAFE = 1
 NOALLOC_SCRATCH_BYTES = 16 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
+FLAG_Q_L2NORM = 1  # KDA_FLAG_Q_L2NORM
 _F32, _BF16 = 0, 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -58,6 +59,10 @@ def load_library():
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
                                       i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
                                       ctypes.c_size_t, vp]
+        lib.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
+                                         vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
+                                         ctypes.c_size_t, ctypes.c_uint, vp]
+        lib.kda_chunk_fwd_ex.restype = ctypes.c_int
         lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, vp, i32, vp]
         lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
@@ -145,10 +150,14 @@ def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0) -> int
 
 def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
                   initial_state=None, output_final_state=False, cu_seqlens=None, chunk_size=64,
-                  o=None, final_state=None, workspace=None, stream=None, o_dtype=None):
+                  o=None, final_state=None, workspace=None, stream=None, o_dtype=None,
+                  q_l2norm=False):
     """Chunked KDA forward; returns (o, final_state or None).
 
     ``o_dtype`` is the dtype of q (default) or torch.float32.
+
+    ``q_l2norm``: use every query row as q / sqrt(|q|^2 + 1e-6) without a separate pass
+    over q (kda_chunk_fwd_ex with KDA_FLAG_Q_L2NORM); forward only.
 
     ``final_state`` may be passed (and may be ``initial_state`` itself) to
     write the final state in place; otherwise it is allocated when
@@ -178,12 +187,21 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = load_library()
-    _check("kda_chunk_fwd", lib.kda_chunk_fwd(
-        _ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
-        lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n, B,
-        T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes,
-        _stream(stream)))
+    args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
+            lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n,
+            B, T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes)
+    if q_l2norm:
+        _check("kda_chunk_fwd_ex", lib.kda_chunk_fwd_ex(*args, FLAG_Q_L2NORM, _stream(stream)))
+    else:
+        _check("kda_chunk_fwd", lib.kda_chunk_fwd(*args, _stream(stream)))
     return o, final_state
+
+
+def kda_chunk_fwd_ex(*args, flags=0, **kwargs):
+    """kda_chunk_fwd with option bits (``FLAG_Q_L2NORM``); other arguments as kda_chunk_fwd."""
+    if flags & ~FLAG_Q_L2NORM:
+        raise ValueError(f"unknown flag bits {flags:#x}")
+    return kda_chunk_fwd(*args, q_l2norm=bool(flags & FLAG_Q_L2NORM), **kwargs)
 
 
 def kda_chunk_fwd_noalloc(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE,

@@ -105,7 +105,20 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
                          int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                          size_t workspace_bytes, kda_stream_t stream) {
+    return kda_chunk_fwd_ex(q, k, v, qkv_dtype, g, g_dtype, A_log, dt_bias, mode, lower_bound, beta,
+                            initial_state, final_state, cu_seqlens, n_seqs, B, T, H, K, V,
+                            chunk_size, o, o_dtype, workspace, workspace_bytes, 0u, stream);
+}
+
+kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const void* g, kda_dtype g_dtype, const float* A_log,
+                            const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                            const void* beta, const float* initial_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                            int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
+                            size_t workspace_bytes, unsigned flags, kda_stream_t stream) {
     g_last_error.clear();
+    if (flags & ~KDA_FLAG_Q_L2NORM) return fail(KDA_ERR_INVALID_ARG, "unknown flag bits");
     int N = 0;
     kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
     if (st != KDA_OK) return st;
@@ -137,7 +150,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
     kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,
                    (int)mode, lower_bound, initial_state, final_state, cu_seqlens, N, B, T, H, K,
                    V, chunk_size, o, o_dtype == KDA_F32, workspace, workspace_bytes,
-                   (cudaStream_t)stream};
+                   (cudaStream_t)stream, (flags & KDA_FLAG_Q_L2NORM) != 0};
     if (kda::fused_supported(a)) return cuda_status(kda::launch_chunk_fused(a));
     return cuda_status(kda::launch_chunk_precise(a));
 }

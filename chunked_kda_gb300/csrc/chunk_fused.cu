@@ -89,7 +89,8 @@ constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
 constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
 constexpr uint32_t OFF_BRAW = 210816;  // prep: raw beta words of the next chunk [64]
-constexpr uint32_t SMEM_BYTES = 211072 + 1024;  // + alignment slack
+constexpr uint32_t OFF_QSS = 211072;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
+constexpr uint32_t SMEM_BYTES = 212096 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
@@ -188,6 +189,7 @@ struct Params {
     int mode;
     float lb;
     int T, H;
+    int qnorm;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
 };
 
 struct Sync {
@@ -375,6 +377,34 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         }
         if (c > 0) sy.group_wait(B_OHDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
         else       bar_sync(BAR_PREP, NGRP);
+
+        // ---- deferred q l2norm (attention-gym PR #345): the sums of q^2 of the own rows over
+        // this warp's 64 channels; the chain scales each output row once the row is complete
+        if (p.qnorm) {
+            float v16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = bf_lo(qr[i]), b = bf_hi(qr[i]);
+                v16[i] = fmaf(a, a, b * b);
+            }
+            // butterfly over lane bits 4, 3, 2, 1: lane l ends with row (l >> 1) & 15, then the
+            // pair (l, l ^ 1) completes it
+            float v8[8], v4[4], v2[2];
+            const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v8[i] = (b4 ? v16[8 + i] : v16[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v16[i] : v16[8 + i], 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
+            float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            float* qss = reinterpret_cast<float*>(smem + OFF_QSS);
+            if ((l & 1) == 0) qss[(c & 1) * 128 + cbp * 64 + 16 * rq + ((l >> 1) & 15)] = v1;
+        }
 
         // ---- operands: channel-major [128 ch][rows] tiles, one 16-byte chunk (8 rows) of
         // each of the two own channels per store
@@ -857,6 +887,11 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
+            if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps)
+                const float* qss = reinterpret_cast<const float*>(smem + OFF_QSS) + (c & 1) * 128 + 32 * hch;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ov[j] *= rsqrtf(qss[j] + qss[64 + j] + kQNormEps);
+            }
             OT* orow = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * VD + vlane;
             const int ostride = H * VD, nvalid = len - 32 * hch;
 #pragma unroll
@@ -982,7 +1017,7 @@ cudaError_t launch_chunk_fused(const FwdArgs& a) {
     // the float32 gate is read with plain loads; its map is a placeholder the kernel never uses
     if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
-             a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H};
+             a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0};
     if (a.g_bf16)
         return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
                        : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);

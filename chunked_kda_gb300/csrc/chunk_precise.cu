@@ -259,20 +259,34 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
     }
 }
 
-// a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows
+// a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows.  With
+// qnorm, row i is finally scaled by 1 / sqrt(|q_i|^2 + eps): every q-dependent term of the
+// row is linear in q_i (attention-gym PR #345, deferred q l2norm).
 template <typename InT, typename OutT, int C>
 __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
                                                   const float* __restrict__ G,
                                                   const float* __restrict__ Aqk,
                                                   const float* __restrict__ hc,
                                                   const float* __restrict__ vn, ChunkMap cm,
-                                                  int H, int K, int V, OutT* __restrict__ o) {
+                                                  int H, int K, int V, int qnorm,
+                                                  OutT* __restrict__ o) {
     __shared__ float qg[C][DT + 1];
     __shared__ float As[C][C + 1];
+    __shared__ float rs[C];
     int n, t0, len, bos, eos;
     if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
     const int h = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
     const float scale = rsqrtf((float)K);
+    for (int i = tid; i < C; i += nthr) {
+        float r = 1.f;
+        if (qnorm && i < len) {
+            float ss = 0.f;
+            const InT* qi = q + ((size_t)(t0 + i) * H + h) * K;
+            for (int d = 0; d < K; ++d) ss = fmaf(to_f32(qi[d]), to_f32(qi[d]), ss);
+            r = rsqrtf(ss + kQNormEps);
+        }
+        rs[i] = r;
+    }
     for (int idx = tid; idx < C * C; idx += nthr) {
         int i = idx / C, j = idx % C;
         As[i][j] = (i < len) ? Aqk[((size_t)(t0 + i) * H + h) * C + j] : 0.f;
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
     }
 #pragma unroll
     for (int i = 0; i < C; ++i)
-        if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<OutT>(acc[i]);
+        if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<OutT>(acc[i] * rs[i]);
 }
 
 template <typename InT, int C>
@@ -351,10 +365,10 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     if (slots > 0) {
         if (a.o_f32)
             out_kernel<InT, float, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
-                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, (float*)a.o);
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, a.q_l2norm, (float*)a.o);
         else
             out_kernel<InT, InT, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
-                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, (InT*)a.o);
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, a.q_l2norm, (InT*)a.o);
     }
     return cudaGetLastError();
 }

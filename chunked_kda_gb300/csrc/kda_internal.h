@@ -43,7 +43,9 @@ struct FwdArgs {
     void* ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    bool q_l2norm = false;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
 };
+constexpr float kQNormEps = 1e-6f;
 
 struct RecArgs {
     const void* q;

@@ -140,6 +140,32 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                          size_t workspace_bytes, kda_stream_t stream);
 
+/* Option bits of kda_chunk_fwd_ex. */
+#define KDA_FLAG_Q_L2NORM 1u /* normalise every query row inside the forward */
+
+/*
+ * kda_chunk_fwd with options (attention-gym PR #345 "Fuse q l2norm into the
+ * chunk_kda output kernel").  flags = 0 is kda_chunk_fwd.
+ *
+ *   KDA_FLAG_Q_L2NORM  each query row is used as q / sqrt(sum_d q[d]^2 + 1e-6)
+ *                      (the eps floor of the callers' l2norm), without a
+ *                      separate pass over q: every q-dependent term of the
+ *                      output row is linear in that row, so the scores stay in
+ *                      the raw-q basis and the finished output row is scaled
+ *                      by the row's 1/||q||.  Keys are used as given.  The
+ *                      final state does not depend on q.  Forward only.
+ *
+ * Every other argument, the layouts and the errors are those of
+ * kda_chunk_fwd; unknown flag bits return KDA_ERR_INVALID_ARG.
+ */
+kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const void* g, kda_dtype g_dtype, const float* A_log,
+                            const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                            const void* beta, const float* initial_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                            int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
+                            size_t workspace_bytes, unsigned flags, kda_stream_t stream);
+
 /*
  * Chunked forward for callers that cannot allocate device memory.
  *

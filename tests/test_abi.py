@@ -107,6 +107,23 @@ def test_chunk_host_validation(lib):
     assert _chunk(lib, cu=P, n=0, B=1) == OK
 
 
+def test_chunk_ex_flags_host_validation(lib):
+    """kda_chunk_fwd_ex: unknown option bits are rejected before any launch; with valid bits
+    the usual validation still applies first."""
+    def ex(flags, **kw):
+        a = dict(q=P, o=P, lb=-5.0, C=64)
+        a.update(kw)
+        return lib.kda_chunk_fwd_ex(a["q"], P, P, BF16, P, BF16, P, None, 1, ctypes.c_float(a["lb"]),
+                                    P, None, None, None, 0, 1, 64, 2, 128, 128, a["C"], a["o"],
+                                    BF16, None, ctypes.c_size_t(0), ctypes.c_uint(flags), None)
+    assert ex(2) == INVALID
+    assert b"flag" in lib.kda_last_error()
+    assert ex(0x80000000) == INVALID
+    assert ex(1, C=48) == UNSUPPORTED
+    assert ex(1, q=None) == INVALID
+    assert ex(1, lb=0.0) == INVALID
+
+
 def test_recurrent_and_gate_host_validation(lib):
     r = lib.kda_recurrent_fwd(P, P, P, BF16, None, P, None, None, None, 0, 1, 4, 2, 128, 128, P,
                               BF16, None)
