@@ -149,11 +149,11 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
  *
  *   KDA_FLAG_Q_L2NORM  each query row is used as q / sqrt(sum_d q[d]^2 + 1e-6)
  *                      (the eps floor of the callers' l2norm), without a
- *                      separate pass over q: every q-dependent term of the
- *                      output row is linear in that row, so the scores stay in
- *                      the raw-q basis and the finished output row is scaled
- *                      by the row's 1/||q||.  Keys are used as given.  The
- *                      final state does not depend on q.  Forward only.
+ *                      separate pass over q: an output row is linear in its
+ *                      query row, so the scores are formed from q as given
+ *                      and each finished output row is scaled once by that
+ *                      row's 1/||q||.  Keys are used as given.  The final
+ *                      state does not depend on q.  Forward only.
  *
  * Every other argument, the layouts and the errors are those of
  * kda_chunk_fwd; unknown flag bits return KDA_ERR_INVALID_ARG.
