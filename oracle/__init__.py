@@ -32,7 +32,8 @@ _libs = {}
 
 GATE_PRE = 0
 GATE_SAFE = 1
-GATE_LOG2 = 2
+GATE_NONSAFE = 2  # -exp(A_log) * softplus(g + dt_bias)
+GATE_LOG2 = 3     # the recurrent entry point's per-token log2 decay
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:

@@ -37,15 +37,19 @@ LN2 = math.log(2.0)
 
 
 def gate_act(g, A_log=None, dt_bias=None, mode=1, lower_bound=-5.0):
-    """Natural-log per-token decay a (FLA skill "fla-kda", "Gate modes")."""
+    """Natural-log per-token decay a (FLA skill "fla-kda", "Gate modes"): 0 pre-gated,
+    1 safe lb * sigmoid(exp(A_log) (g + dt_bias)), 2 non-safe -exp(A_log) softplus(g + dt_bias),
+    3 a per-token log2 decay."""
     g = np.asarray(g, dtype=np.float64)
     if mode == 0:
         return g.copy()
-    if mode == 2:
+    if mode == 3:
         return g * LN2
-    z = np.exp(np.asarray(A_log, dtype=np.float64)) * (
-        g + (0.0 if dt_bias is None else np.asarray(dt_bias, dtype=np.float64)))
-    return lower_bound / (1.0 + np.exp(-z))
+    x = g + (0.0 if dt_bias is None else np.asarray(dt_bias, dtype=np.float64))
+    expA = np.exp(np.asarray(A_log, dtype=np.float64))
+    if mode == 2:
+        return -expA * np.logaddexp(0.0, x)  # softplus(x) = ln(1 + e^x)
+    return lower_bound / (1.0 + np.exp(-expA * x))
 
 
 def chunk_unit(q, k, v, a, beta, h0, C):

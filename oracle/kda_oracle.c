@@ -52,16 +52,25 @@
 #endif
 
 /* gate modes of the oracle (the last one is the recurrent entry point's input) */
-#define ORC_GATE_PRE 0  /* g is the natural-log decay itself                 */
-#define ORC_GATE_SAFE 1 /* a = lb * sigmoid(exp(A_log) * (g + dt_bias))      */
-#define ORC_GATE_LOG2 2 /* g is the per-token log2 decay: decay = 2^g          */
+#define ORC_GATE_PRE 0     /* g is the natural-log decay itself                   */
+#define ORC_GATE_SAFE 1    /* a = lb * sigmoid(exp(A_log) * (g + dt_bias))        */
+#define ORC_GATE_NONSAFE 2 /* a = -exp(A_log) * softplus(g + dt_bias)             */
+#define ORC_GATE_LOG2 3    /* g is the per-token log2 decay: decay = 2^g            */
 
 static const double ORC_LN2 = 0.693147180559945309417232121458176568;
+
+/* softplus(x) = ln(1 + e^x), without overflow for large x */
+static double softplus(double x)
+{
+    return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+}
 
 /*
  * Per-element gate activation, natural-log units.
  * FLA skill "fla-kda", "Gate modes": pre-gated mode passes g through; the safe
- * in-kernel mode is lower_bound * sigmoid(exp(A_log) * (g + dt_bias)).
+ * in-kernel mode is lower_bound * sigmoid(exp(A_log) * (g + dt_bias)); without
+ * the safe gate the in-kernel activation is -exp(A_log) * softplus(g + dt_bias),
+ * unbounded below.
  * attention-gym PR #317, Agent note: the recurrent gate is a log2 decay, so it
  * is converted back to natural-log units with a factor ln 2.
  */
@@ -69,6 +78,7 @@ double kda_oracle_gate_act(double g, double A_log, double dt_bias, int mode, dou
 {
     if (mode == ORC_GATE_PRE) return g;
     if (mode == ORC_GATE_LOG2) return g * ORC_LN2;
+    if (mode == ORC_GATE_NONSAFE) return -exp(A_log) * softplus(g + dt_bias);
     /* ORC_GATE_SAFE */
     double z = exp(A_log) * (g + dt_bias);
     double sig = 1.0 / (1.0 + exp(-z));
@@ -188,7 +198,7 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                    double* o, double q_eps, const int32_t* units, int n_units, int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !o || H <= 0 || K <= 0 || V <= 0) return 1;
-    if (mode == ORC_GATE_SAFE && !A_log) return 1;
+    if ((mode == ORC_GATE_SAFE || mode == ORC_GATE_NONSAFE) && !A_log) return 1;
     if (cu && B != 1) return 1;
     int N = cu ? n_seqs : B;
     long total = units ? n_units : (long)N * H;

@@ -20,7 +20,23 @@ def test_chunked_equals_recurrence(C, T):
     assert np.allclose(s, s_ref, rtol=0, atol=1e-11)
 
 
-@pytest.mark.parametrize("mode", [oracle.GATE_PRE, oracle.GATE_SAFE])
+@pytest.mark.parametrize("gscale", [1.0, 40.0])
+def test_chunked_equals_recurrence_nonsafe(gscale):
+    """The non-safe gate -exp(A_log) softplus(g + dt_bias) is unbounded below; with raw g up to
+    about +-120 single tokens decay by e^-1000 and more, and the chunked form (decay ratios
+    2^(G_i - G_j), j <= i) still equals the token recurrence."""
+    c = _random_case(55, T=130, H=2, K=8, V=6)
+    c["g"] = c["g"] * gscale
+    c["mode"] = oracle.GATE_NONSAFE
+    o_ref, s_ref = oracle.forward(**c)
+    assert np.isfinite(o_ref).all()
+    for C in (16, 64):
+        o, s = chunked.forward(**c, chunk_size=C)
+        assert np.allclose(o, o_ref, rtol=0, atol=1e-11)
+        assert np.allclose(s, s_ref, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("mode", [oracle.GATE_PRE, oracle.GATE_SAFE, oracle.GATE_NONSAFE])
 def test_chunked_equals_recurrence_varlen(mode):
     c = _random_case(7, T=200, H=2, K=8, V=8, mode=mode)
     lens = [0, 70, 1, 0, 64, 33, 0]

@@ -18,6 +18,12 @@ MUTANTS = [
     ("no_beta", "bt * kt[d] * (vt[j] - r[j])", "kt[d] * (vt[j] - r[j])"),
     ("readout_transposed", "acc += S[(size_t)d * V + j] * (qt[d] * qs);",
      "acc += S[(size_t)j * V + d] * (qt[d] * qs);"),
+    ("nonsafe_sign", "return -exp(A_log) * softplus(g + dt_bias);",
+     "return exp(A_log) * softplus(g + dt_bias);"),
+    ("nonsafe_no_exp_A", "return -exp(A_log) * softplus(g + dt_bias);",
+     "return -A_log * softplus(g + dt_bias);"),
+    ("softplus_relu", "return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));",
+     "return x > 0.0 ? x : log1p(exp(x));"),
     ("qnorm_no_sqrt", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / (ss + q_eps);"),
     ("qnorm_no_eps", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / sqrt(ss);"),
     ("qnorm_abs_sum", "ss += qt[d] * qt[d];", "ss += fabs(qt[d]);"),
