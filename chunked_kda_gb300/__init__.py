@@ -14,12 +14,15 @@ import threading
 
 import torch
 
-__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_chunk_fwd_ex",
+__all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_bytes_ex",
+           "kda_chunk_fwd", "kda_chunk_fwd_ex",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
+           "GATE_NONSAFE",
            "FLAG_Q_L2NORM", "NOALLOC_SCRATCH_BYTES", "library_path", "load_library"]
 
 GATE_PRE = 0
 GATE_SAFE = 1
+GATE_NONSAFE = 2  # -exp(A_log) * softplus(g + dt_bias); runs on the float32 stage-by-stage path
 NOALLOC_SCRATCH_BYTES = 16 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 FLAG_Q_L2NORM = 1  # KDA_FLAG_Q_L2NORM
 _F32, _BF16 = 0, 1
@@ -56,6 +59,8 @@ def load_library():
                                      vp, vp]
         lib.kda_chunk_workspace_bytes.argtypes = [i32] * 8
         lib.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_chunk_workspace_bytes_ex.argtypes = [i32] * 9
+        lib.kda_chunk_workspace_bytes_ex.restype = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
                                       i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
                                       ctypes.c_size_t, vp]
@@ -143,9 +148,17 @@ def kda_gate_fwd(g, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
     return out
 
 
-def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0) -> int:
+def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=None) -> int:
+    """Scratch bytes of kda_chunk_fwd; ``mode`` (a gate mode) selects kda_chunk_workspace_bytes_ex."""
     code = _F32 if dtype == torch.float32 else _BF16
-    return int(load_library().kda_chunk_workspace_bytes(code, B, T, H, K, V, chunk_size, n_seqs))
+    lib = load_library()
+    if mode is None:
+        return int(lib.kda_chunk_workspace_bytes(code, B, T, H, K, V, chunk_size, n_seqs))
+    return int(lib.kda_chunk_workspace_bytes_ex(code, B, T, H, K, V, chunk_size, n_seqs, mode))
+
+
+def kda_chunk_workspace_bytes_ex(dtype, B, T, H, K, V, chunk_size, n_seqs, mode) -> int:
+    return kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs, mode)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
@@ -182,7 +195,7 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
         N = n if cu_seqlens is not None else B
         final_state = torch.empty((N, H, K, V), device=q.device, dtype=torch.float32)
     _cuda(final_state, "final_state", torch.float32)
-    need = kda_chunk_workspace_bytes(q.dtype, B, T, H, K, V, chunk_size, n)
+    need = kda_chunk_workspace_bytes(q.dtype, B, T, H, K, V, chunk_size, n, mode)
     if workspace is None and need > 0:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

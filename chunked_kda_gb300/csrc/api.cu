@@ -42,6 +42,16 @@ kda_status check_layout(const int32_t* cu, int n_seqs, int B, int T, int H, int*
     return KDA_OK;
 }
 
+// gate mode and its parameters (FLA skill "fla-kda", "Gate modes")
+kda_status check_gate(kda_gate_mode mode, const float* A_log, float lower_bound) {
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE)
+        return fail(KDA_ERR_INVALID_ARG, "gate mode");
+    if (mode != KDA_GATE_PRE && !A_log) return fail(KDA_ERR_INVALID_ARG, "in-kernel gate needs A_log");
+    if (mode == KDA_GATE_SAFE && !(lower_bound >= -5.0f && lower_bound < 0.0f))
+        return fail(KDA_ERR_INVALID_ARG, "safe gate needs -5 <= lower_bound < 0");
+    return KDA_OK;
+}
+
 }  // namespace
 
 namespace kda {
@@ -72,14 +82,10 @@ kda_status kda_gate_fwd(const void* g, kda_dtype g_dtype, const float* A_log,
     if (st != KDA_OK) return st;
     if (K <= 0) return fail(KDA_ERR_INVALID_ARG, "K must be > 0");
     if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
-    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) return fail(KDA_ERR_INVALID_ARG, "gate mode");
     if (chunk_size != 1 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64)
         return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 1, 16, 32 or 64");
-    if (mode == KDA_GATE_SAFE) {
-        if (!A_log) return fail(KDA_ERR_INVALID_ARG, "safe gate needs A_log");
-        if (!(lower_bound >= -5.0f && lower_bound < 0.0f))
-            return fail(KDA_ERR_INVALID_ARG, "safe gate needs -5 <= lower_bound < 0");
-    }
+    st = check_gate(mode, A_log, lower_bound);
+    if (st != KDA_OK) return st;
     if ((long long)B * T == 0 || N == 0) return KDA_OK;
     if (!g || !g_out) return fail(KDA_ERR_INVALID_ARG, "null g or g_out");
     kda::GateArgs a{g, g_dtype == KDA_BF16, A_log, dt_bias, (int)mode, lower_bound, cu_seqlens,
@@ -89,10 +95,16 @@ kda_status kda_gate_fwd(const void* g, kda_dtype g_dtype, const float* A_log,
 
 size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
                                  int chunk_size, int n_seqs) {
+    return kda_chunk_workspace_bytes_ex(qkv_dtype, B, T, H, K, V, chunk_size, n_seqs, KDA_GATE_SAFE);
+}
+
+size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
+                                    int chunk_size, int n_seqs, kda_gate_mode mode) {
     if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(K) || !head_dim_ok(V)) return 0;
     if (chunk_size != 32 && chunk_size != 64) return 0;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return 0;
-    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size)) return 0;
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE) return 0;
+    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode)) return 0;
     bool packed = n_seqs > 0;
     int N = packed ? n_seqs : B;
     return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
@@ -128,12 +140,8 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
         return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
     if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
     if (chunk_size != 32 && chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 32 or 64");
-    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) return fail(KDA_ERR_INVALID_ARG, "gate mode");
-    if (mode == KDA_GATE_SAFE) {
-        if (!A_log) return fail(KDA_ERR_INVALID_ARG, "safe gate needs A_log");
-        if (!(lower_bound >= -5.0f && lower_bound < 0.0f))
-            return fail(KDA_ERR_INVALID_ARG, "safe gate needs -5 <= lower_bound < 0");
-    }
+    st = check_gate(mode, A_log, lower_bound);
+    if (st != KDA_OK) return st;
     const bool any_tokens = (long long)B * T > 0 && N > 0;
     if (any_tokens && (!q || !k || !v || !g || !beta || !o))
         return fail(KDA_ERR_INVALID_ARG, "null q, k, v, g, beta or o");
@@ -141,10 +149,10 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;
-    size_t need = kda_chunk_workspace_bytes(qkv_dtype, B, T, H, K, V, chunk_size,
-                                            cu_seqlens ? n_seqs : 0);
+    size_t need = kda_chunk_workspace_bytes_ex(qkv_dtype, B, T, H, K, V, chunk_size,
+                                               cu_seqlens ? n_seqs : 0, mode);
     if (workspace_bytes < need || (need > 0 && !workspace))
-        return fail(KDA_ERR_INVALID_ARG, "workspace smaller than kda_chunk_workspace_bytes()");
+        return fail(KDA_ERR_INVALID_ARG, "workspace smaller than kda_chunk_workspace_bytes_ex()");
     if (workspace && ((uintptr_t)workspace & 255u) != 0)
         return fail(KDA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,

@@ -990,11 +990,13 @@ bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D) {
 
 }  // namespace fused
 
-bool fused_supported_dims(bool qkv_bf16, int K, int V, int C) {
-    return qkv_bf16 && K == 128 && V == 128 && C == 64;
+// bf16, K = V = 128, C = 64, and a gate whose per-token decay is bounded (pre-gated under the
+// bounded-gate contract, or safe): the sub-block anchors of the score operands rely on it
+bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode) {
+    return qkv_bf16 && K == 128 && V == 128 && C == 64 && (mode == 0 || mode == 1);
 }
 
-bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C); }
+bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C, a.mode); }
 
 template <typename GT, typename OT>
 static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,

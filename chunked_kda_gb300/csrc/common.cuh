@@ -27,9 +27,15 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { retu
 
 // Natural-log per-token decay from the gate input (FLA skill "fla-kda",
 // "Gate modes").  mode 0: pre-gated, a = g.  mode 1: safe in-kernel,
-// a = lb * sigmoid(expA * (g + dt_bias)) with expA = exp(A_log) precomputed.
+// a = lb * sigmoid(expA * (g + dt_bias)).  mode 2: in-kernel without the safe
+// gate, a = -expA * softplus(g + dt_bias), unbounded below.  expA = exp(A_log)
+// precomputed.
+__device__ __forceinline__ float softplus_f(float x) {  // ln(1 + e^x) without overflow
+    return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+}
 __device__ __forceinline__ float gate_act(float g, float expA, float dtb, int mode, float lb) {
     if (mode == 0) return g;
+    if (mode == 2) return -expA * softplus_f(g + dtb);
     float z = expA * (g + dtb);
     return lb / (1.0f + expf(-z));
 }

@@ -1,6 +1,6 @@
 // K1 standalone: gate activation + chunk-local inclusive cumsum in log2 units.
 //
-// FLA skill "fla-kda", "Gate modes" (pre-gated and safe in-kernel
+// FLA skill "fla-kda", "Gate modes" (pre-gated, safe and non-safe in-kernel
 // activations) and "Safe gate numerical note" (RCP_LN2 conversion before
 // exp2); attention-gym PR #317, Agent note (bounded_gate_cumsum with
 // chunk_size = 1 is the per-token log2 gate of the recurrent entry point).
@@ -23,8 +23,8 @@ __global__ void __launch_bounds__(128) gate_cumsum_kernel(
     if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
     int hk = blockIdx.y * 128 + threadIdx.x;
     if (hk >= HK) return;
-    float expA = (mode == 1) ? expf(__ldg(A_log + hk)) : 0.f;
-    float dtb = (mode == 1 && dt_bias) ? __ldg(dt_bias + hk) : 0.f;
+    float expA = (mode != 0) ? expf(__ldg(A_log + hk)) : 0.f;
+    float dtb = (mode != 0 && dt_bias) ? __ldg(dt_bias + hk) : 0.f;
     float acc = 0.f;
     size_t idx = (size_t)t0 * HK + hk;
     for (int i = 0; i < len; ++i, idx += HK) {

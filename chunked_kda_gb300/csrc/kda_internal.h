@@ -31,7 +31,7 @@ struct FwdArgs {
     bool g_bf16;
     const float* A_log;
     const float* dt_bias;
-    int mode;  // 0 pre-gated, 1 safe
+    int mode;  // 0 pre-gated, 1 safe, 2 non-safe
     float lb;
     const float* h0;
     float* hT;
@@ -73,7 +73,7 @@ cudaError_t launch_chunk_precise(const FwdArgs& a);
 
 // bf16 fused single-kernel path (tcgen05 / TMEM / TMA); needs no workspace
 bool fused_supported(const FwdArgs& a);
-bool fused_supported_dims(bool qkv_bf16, int K, int V, int C);
+bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
 
 // sets the message kda_last_error() returns on this host thread

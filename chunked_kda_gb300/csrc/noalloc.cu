@@ -74,12 +74,16 @@ extern "C" kda_status kda_chunk_fwd_noalloc(
         kda::record_error("kda_chunk_fwd_noalloc: unsupported dtype, head dim or chunk size");
         return KDA_ERR_UNSUPPORTED;
     }
-    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE) {
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE) {
         kda::record_error("kda_chunk_fwd_noalloc: bad gate mode");
         return KDA_ERR_INVALID_ARG;
     }
-    if (mode == KDA_GATE_SAFE && (!A_log || !(lower_bound >= -5.0f && lower_bound < 0.0f))) {
-        kda::record_error("kda_chunk_fwd_noalloc: safe gate needs A_log and -5 <= lower_bound < 0");
+    if (mode != KDA_GATE_PRE && !A_log) {
+        kda::record_error("kda_chunk_fwd_noalloc: in-kernel gate needs A_log");
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (mode == KDA_GATE_SAFE && !(lower_bound >= -5.0f && lower_bound < 0.0f)) {
+        kda::record_error("kda_chunk_fwd_noalloc: safe gate needs -5 <= lower_bound < 0");
         return KDA_ERR_INVALID_ARG;
     }
     const int N = cu_seqlens ? n_seqs : B;
@@ -87,7 +91,7 @@ extern "C" kda_status kda_chunk_fwd_noalloc(
         kda::record_error("kda_chunk_fwd_noalloc: null q, k, v, g, beta or o");
         return KDA_ERR_INVALID_ARG;
     }
-    const void* ptrs[] = {q, k, v, g, o, initial_state, final_state, A_log, dt_bias};
+    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
     for (const void* p : ptrs)
         if (p && !al16(p)) {
             kda::record_error("kda_chunk_fwd_noalloc: pointers must be 16-byte aligned");

@@ -12,6 +12,7 @@ with ``1000 + workload id`` on the requested device, then cast):
 * safe in-kernel gate: raw g ~ N(0, sigma_g) in the dtype of q,
   A_log ~ U(0, ln 16) and dt_bias ~ N(0, 0.5) as float32 [H, K], lower_bound -5.
 * pre-gated: g = -U(0.01, 5) per token and channel (natural-log decay).
+* non-safe in-kernel gate: g, A_log, dt_bias drawn as for the safe gate.
 * recurrent decode: per-token log2 gate = log2(e) * (-U(0.01, 5)) in float32.
 * initial states (where drawn): N(0, 0.05) float32 [N, H, K, V].
 """
@@ -25,6 +26,7 @@ import torch
 
 GATE_PRE = 0
 GATE_SAFE = 1
+GATE_NONSAFE = 2
 
 
 @dataclass
@@ -110,7 +112,7 @@ def make_dense(name, B, T, H, K, V, chunk_size, dtype, seed, device="cpu", g_std
     gen = _gen(device, seed)
     q, k, v, beta = _qkvb(B, T, H, K, V, gen, device, dtype)
     A_log = dt_bias = None
-    if mode == GATE_SAFE:
+    if mode in (GATE_SAFE, GATE_NONSAFE):
         g = _randn((B, T, H, K), gen, device, g_std).to(dtype)
         A_log = _rand((H, K), gen, device, 0.0, math.log(16.0))
         dt_bias = _randn((H, K), gen, device, 0.5)
@@ -142,7 +144,7 @@ def make_varlen(name, lengths, capacity, H, K, V, chunk_size, dtype, seed, devic
     assert cu[-1] <= capacity
     q, k, v, beta = _qkvb(1, capacity, H, K, V, gen, device, dtype)
     A_log = dt_bias = None
-    if mode == GATE_SAFE:
+    if mode in (GATE_SAFE, GATE_NONSAFE):
         g = _randn((1, capacity, H, K), gen, device).to(dtype)
         A_log = _rand((H, K), gen, device, 0.0, math.log(16.0))
         dt_bias = _randn((H, K), gen, device, 0.5)

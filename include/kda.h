@@ -72,13 +72,20 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 typedef enum {
     /* g already is the natural-log decay (FLA skill "fla-kda", "Gate modes",
        pre-gated mode); A_log, dt_bias and lower_bound are ignored.  The chunked
-       path assumes the bounded-gate contract -5 <= g <= 0 (attention-gym PR #345
-       text: the flag assumes the bounded-gate contract). */
+       bf16 kernel needs the bounded range -5 <= g <= 0 that attention-gym
+       PR #345 calls the bounded-gate contract. */
     KDA_GATE_PRE = 0,
     /* safe in-kernel mode: a = lower_bound * sigmoid(exp(A_log) * (g + dt_bias)),
        A_log required, dt_bias optional, -5 <= lower_bound < 0 (FLA skill
        "fla-kda", "Gate modes") */
-    KDA_GATE_SAFE = 1
+    KDA_GATE_SAFE = 1,
+    /* in-kernel mode without the safe gate: a = -exp(A_log) * softplus(g + dt_bias),
+       A_log required, dt_bias optional, lower_bound ignored; the decay is
+       unbounded (same section).  The chunked forward runs it on the float32
+       stage-by-stage path, whose intra-chunk decay ratios 2^(G_i - G_j), j <= i,
+       never exceed 1; that path needs a workspace even for bf16 inputs
+       (kda_chunk_workspace_bytes_ex). */
+    KDA_GATE_NONSAFE = 2
 } kda_gate_mode;
 
 /*
@@ -88,7 +95,7 @@ typedef enum {
  * the recurrent entry point's per-token log2 gate).
  *
  *   g          [B, T, H, K], dtype g_dtype (KDA_F32 or KDA_BF16)
- *   A_log      [H, K] float32, required in KDA_GATE_SAFE mode
+ *   A_log      [H, K] float32, required in the in-kernel modes (SAFE, NONSAFE)
  *   dt_bias    [H, K] float32 or NULL (= 0)
  *   chunk_size 1, 16, 32 or 64; chunks restart at every sequence start
  *   g_out      [B, T, H, K] float32: g_out[t] = (1/ln 2) * sum of the
@@ -109,6 +116,12 @@ kda_status kda_gate_fwd(const void* g, kda_dtype g_dtype, const float* A_log,
  */
 size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
                                  int chunk_size, int n_seqs);
+
+/* The scratch size for a given gate mode: kda_chunk_workspace_bytes is this with
+   KDA_GATE_SAFE (the pre-gated mode needs the same); KDA_GATE_NONSAFE selects
+   the stage-by-stage path, which needs scratch for bf16 inputs as well. */
+size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
+                                    int chunk_size, int n_seqs, kda_gate_mode mode);
 
 /*
  * Chunked KDA forward (prefill).  Steps: gate activation + chunk-local log2

@@ -102,6 +102,11 @@ def test_chunk_host_validation(lib):
     assert _chunk(lib, dt=F32, ws=None, ws_bytes=0) == INVALID
     assert b"workspace" in lib.kda_last_error()
     assert _chunk(lib, H=0) == INVALID
+    # non-safe gate: A_log required, lower_bound ignored, scratch needed even for bf16
+    assert _chunk(lib, mode=2, A_log=None) == INVALID
+    assert _chunk(lib, mode=2, lb=0.0) == INVALID
+    assert b"workspace" in lib.kda_last_error()
+    assert _chunk(lib, mode=3) == INVALID
     # nothing to do: zero logical sequences is OK and launches nothing
     assert _chunk(lib, B=0) == OK
     assert _chunk(lib, cu=P, n=0, B=1) == OK
@@ -135,6 +140,10 @@ def test_recurrent_and_gate_host_validation(lib):
     assert g == INVALID  # safe gate without A_log
     g = lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 48, P, None)
     assert g == UNSUPPORTED
+    g = lib.kda_gate_fwd(P, BF16, None, None, 2, 0.0, None, 0, 1, 4, 2, 128, 64, P, None)
+    assert g == INVALID  # non-safe gate without A_log
+    g = lib.kda_gate_fwd(P, BF16, P, None, 3, 0.0, None, 0, 1, 4, 2, 128, 64, P, None)
+    assert g == INVALID  # no such mode
 
 
 def test_workspace_bytes(lib):
@@ -159,3 +168,12 @@ def test_workspace_bytes(lib):
     # the fused bf16 kernel keeps every intermediate on chip
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) > 0
+    # by gate mode: the non-safe gate runs on the stage-by-stage path (scratch for bf16 too)
+    ex = lib.kda_chunk_workspace_bytes_ex
+    ex.restype = ctypes.c_size_t
+    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 0) == 0
+    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 0
+    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
+        F32, 4, 4096, 64, 128, 128, 64, 0) > 0
+    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 3) == 0  # no such mode
+    assert ex(F32, B, T, H, K, V, C, 0, 2) == lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0)

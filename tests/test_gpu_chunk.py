@@ -219,3 +219,25 @@ def test_full_size_sampled(name):
         assert torch.isfinite(o[torch.from_numpy(valid_mask(w)).cuda()]).all()
         check_units(w, o, st, units)
         del o, st
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("g_std", [1.0, 30.0], ids=["g1", "g30"])
+def test_nonsafe_gate(dtype, C, g_std):
+    """The non-safe in-kernel gate -exp(A_log) softplus(g + dt_bias) (FLA skill "fla-kda",
+    "Gate modes"): with raw g ~ N(0, 30) single tokens decay by e^-1000 and more; the result
+    stays finite and matches the oracle."""
+    w = workloads.make_dense("t", 2, 150, 2, 128, 128, C, dtype, 300 + C, state_std=0.05,
+                             g_std=g_std, mode=workloads.GATE_NONSAFE)
+    o, st = run_gpu(w)
+    assert torch.isfinite(o).all() and torch.isfinite(st).all()
+    compare(w, o, st)
+
+
+def test_nonsafe_gate_varlen():
+    lens = workloads.varlen_lengths(6, 200, 1000, empty_slots=(1,), seed=31)
+    w = workloads.make_varlen("t", lens, 1100, 2, 128, 128, 64, torch.bfloat16, 31,
+                              mode=workloads.GATE_NONSAFE)
+    o, st = run_gpu(w)
+    compare(w, o, st)

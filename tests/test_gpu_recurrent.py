@@ -111,7 +111,8 @@ def test_decode_in_place_256_steps():
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("C", [1, 16, 32, 64])
-@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE, workloads.GATE_NONSAFE],
+                         ids=["pre", "safe", "nonsafe"])
 def test_gate_fwd(dtype, C, mode):
     lens = [0, 70, 1, 0, 64, 33]
     cap = sum(lens) + 11
