@@ -59,7 +59,8 @@ def load(path: str | None = None):
             lib.kda_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_double,
                                            dp, dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
-                                           ctypes.c_double, ip, ctypes.c_int, ctypes.c_int]
+                                           ctypes.c_double, ctypes.c_double, ctypes.c_int, ip,
+                                           ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_fwd.restype = ctypes.c_int
             lib.kda_oracle_gate.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_double, ip,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -135,11 +136,13 @@ Q_L2NORM_EPS = 1e-6  # eps floor of the optional query l2 normalisation
 
 def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
             initial_state=None, cu_seqlens=None, units=None, nthreads=0, lib=None,
-            q_l2norm=False):
+            q_l2norm=False, k_l2norm=False, beta_logits=False):
     """Token-by-token float64 KDA forward.
 
     ``q_l2norm``: each query row is first replaced by q / sqrt(sum q^2 + Q_L2NORM_EPS)
-    (attention-gym PR #345 "Fuse q l2norm into the chunk_kda output kernel").
+    (attention-gym PR #345 "Fuse q l2norm into the chunk_kda output kernel"); ``k_l2norm``
+    the same for the key rows; ``beta_logits``: beta holds logits, sigmoid(beta) is used
+    (the decode-side preprocessing of the recurrent path).
     Returns (o [B,T,H,V] float64, final_state [N,H,K,V] float64).  Rows of o
     outside every sequence (and rows of units not listed in ``units``) are NaN.
     """
@@ -159,6 +162,7 @@ def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bo
                                 int(mode), float(lower_bound), _dptr(beta), _dptr(S0), _dptr(ST),
                                 _iptr(cu), 0 if cu is None else N, B, T, H, K, V, _dptr(o),
                                 float(Q_L2NORM_EPS if q_l2norm else -1.0),
+                                float(Q_L2NORM_EPS if k_l2norm else -1.0), int(bool(beta_logits)),
                                 _iptr(un), 0 if un is None else un.shape[0], int(nthreads))
     if rc != 0:
         raise ValueError(f"kda_oracle_fwd failed ({rc})")

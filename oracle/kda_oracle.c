@@ -34,7 +34,11 @@
  *   - attention-gym PR #345 "Fuse q l2norm into the chunk_kda output kernel"
  *     (optional, q_eps >= 0): every query row is first normalised,
  *     q_t <- q_t / sqrt(sum_d q_t[d]^2 + q_eps), the l2norm of the inference
- *     callers (its eps floor); keys are not touched.
+ *     callers (its eps floor).  The same normalisation of the key rows
+ *     (k_eps >= 0) and beta given as logits (beta_t <- sigmoid(beta_t)) are the
+ *     decode-side preprocessing of the recurrent path (attention-gym PR #317,
+ *     "Test Plan"; FLA skill "fla-kda", "Correctness checklist": raw beta logits,
+ *     qk l2norm in kernel).
  *
  * Layouts (all contiguous, row-major):
  *   q, k, g : [B, T, H, K]      v, o : [B, T, H, V]      beta : [B, T, H]
@@ -137,7 +141,7 @@ static void run_unit(const double* q, const double* k, const double* v, const do
                      const double* A_log, const double* dt_bias, int mode, double lb,
                      const double* beta, const double* S0, double* ST, double* o,
                      long bos, long eos, int n, int h, int H, int K, int V, double q_eps,
-                     double* S, double* r)
+                     double k_eps, int beta_logits, double* S, double* r, double* kn)
 {
     size_t st_off = ((size_t)n * H + h) * (size_t)K * V;
     if (S0) memcpy(S, S0 + st_off, sizeof(double) * (size_t)K * V);
@@ -147,9 +151,17 @@ static void run_unit(const double* q, const double* k, const double* v, const do
     for (long t = bos; t < eos; ++t) {
         const double* qt = q + ((size_t)t * H + h) * K;
         const double* kt = k + ((size_t)t * H + h) * K;
+        if (k_eps >= 0.0) {  /* k_t <- k_t / sqrt(|k_t|^2 + k_eps) */
+            double ss = 0.0;
+            for (int d = 0; d < K; ++d) ss += kt[d] * kt[d];
+            const double ks = 1.0 / sqrt(ss + k_eps);
+            for (int d = 0; d < K; ++d) kn[d] = kt[d] * ks;
+            kt = kn;
+        }
         const double* gt = g + ((size_t)t * H + h) * K;
         const double* vt = v + ((size_t)t * H + h) * V;
-        const double bt = beta[(size_t)t * H + h];
+        const double braw = beta[(size_t)t * H + h];
+        const double bt = beta_logits ? 1.0 / (1.0 + exp(-braw)) : braw;
         double* ot = o + ((size_t)t * H + h) * V;
 
         /* S = Diag(exp(a_t)) S */
@@ -186,7 +198,9 @@ static void run_unit(const double* q, const double* k, const double* v, const do
 /*
  * Full forward over every unit, or over the listed units only.
  *   units / n_units : optional list of (n, h) pairs (2 * n_units ints); NULL = all.
- *   q_eps           : < 0: q as given; >= 0: each q row l2-normalised with this eps floor.
+ *   q_eps, k_eps    : < 0: q (k) as given; >= 0: each q (k) row l2-normalised with this
+ *                     eps floor.
+ *   beta_logits     : nonzero: beta holds logits, the forward uses sigmoid(beta).
  *   nthreads        : OpenMP threads over independent units (<= 0: library default).
  * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
  * Outputs of units not computed, and o rows outside every sequence, are not written.
@@ -195,7 +209,8 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                    const double* A_log, const double* dt_bias, int mode, double lb,
                    const double* beta, const double* S0, double* ST,
                    const int32_t* cu, int n_seqs, int B, int T, int H, int K, int V,
-                   double* o, double q_eps, const int32_t* units, int n_units, int nthreads)
+                   double* o, double q_eps, double k_eps, int beta_logits,
+                   const int32_t* units, int n_units, int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !o || H <= 0 || K <= 0 || V <= 0) return 1;
     if ((mode == ORC_GATE_SAFE || mode == ORC_GATE_NONSAFE) && !A_log) return 1;
@@ -210,7 +225,8 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
     {
         double* S = (double*)malloc(sizeof(double) * (size_t)K * V);
         double* r = (double*)malloc(sizeof(double) * (size_t)V);
-        if (!S || !r) {
+        double* kn = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!S || !r || !kn) {
             failed = 1;
         } else {
 #ifdef _OPENMP
@@ -222,11 +238,12 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                 long bos, eos;
                 seq_bounds(cu, n, T, &bos, &eos);
                 run_unit(q, k, v, g, A_log, dt_bias, mode, lb, beta, S0, ST, o, bos, eos, n,
-                         h, H, K, V, q_eps, S, r);
+                         h, H, K, V, q_eps, k_eps, beta_logits, S, r, kn);
             }
         }
         free(S);
         free(r);
+        free(kn);
     }
     return failed ? 2 : 0;
 }

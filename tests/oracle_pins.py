@@ -320,7 +320,45 @@ def pin_q_l2norm_rows(lib=None):
     assert (o2[0, 5] == 0).all() and (o2[0, 17, 1] == 0).all()
 
 
+def pin_decode_preprocessing_single_token(lib=None):
+    """Decode-side preprocessing (attention-gym PR #317; FLA skill "fla-kda", "Correctness
+    checklist": raw beta logits, qk l2norm in kernel): one token with k^ = k / sqrt(|k|^2 + eps),
+    q^ likewise and beta = sigmoid(x): S_1 = S' + beta k^ (v - S'^T k^)^T, o = S_1^T q^ / sqrt(K)."""
+    r = _rng(13)
+    K, V = 6, 3
+    k = 5.0 * r.normal(size=(1, 1, 1, K))
+    q = 0.2 * r.normal(size=(1, 1, 1, K))
+    v = r.normal(size=(1, 1, 1, V))
+    g = -r.uniform(0.01, 2.0, size=(1, 1, 1, K))
+    x = np.array([[[-0.4]]])
+    S0 = r.normal(size=(1, 1, K, V))
+    o, ST = oracle.forward(q, k, v, g, x, mode=oracle.GATE_PRE, initial_state=S0, lib=lib,
+                           q_l2norm=True, k_l2norm=True, beta_logits=True)
+    eps = oracle.Q_L2NORM_EPS
+    kk, qq = k[0, 0, 0], q[0, 0, 0]
+    kh, qh = kk / math.sqrt(kk @ kk + eps), qq / math.sqrt(qq @ qq + eps)
+    b = 1.0 / (1.0 + math.exp(0.4))
+    Sd = np.exp(g[0, 0, 0])[:, None] * S0[0, 0]
+    S1 = Sd + b * np.outer(kh, v[0, 0, 0] - Sd.T @ kh)
+    assert np.allclose(ST[0, 0], S1, atol=1e-12)
+    assert np.allclose(o[0, 0, 0], S1.T @ qh / math.sqrt(K), atol=1e-12)
+
+
+def pin_k_l2norm_scale_free(lib=None):
+    """With the key rows normalised, scaling every key row by any c > 0 leaves the result
+    unchanged up to the eps floor: keys of norm 1e3 (eps negligible) give the same o and S_T
+    as keys of norm 1e3 scaled again by 7."""
+    c = _random_case(14, T=21)
+    c["k"] = c["k"] * 1e3
+    o1, s1 = oracle.forward(**c, lib=lib, k_l2norm=True)
+    o2, s2 = oracle.forward(**dict(c, k=7.0 * c["k"]), lib=lib, k_l2norm=True)
+    assert np.allclose(o1, o2, rtol=1e-9, atol=1e-12) and np.allclose(s1, s2, rtol=1e-9, atol=1e-12)
+    o3, _ = oracle.forward(**c, lib=lib)  # without the option the keys of norm 1e3 blow up
+    assert not np.allclose(o3, o1, atol=1e-3)
+
+
 ALL_PINS = [pin_gate_points, pin_gate_cumsum_closed_form, pin_gate_chunk1_is_per_token,
             pin_hand_worked, pin_beta_zero, pin_linear_attention, pin_one_hot_gated,
             pin_repeated_key_ema, pin_single_token_delta, pin_scale_exact, pin_state_carry,
-            pin_varlen_contract, pin_q_l2norm_single_token, pin_q_l2norm_rows]
+            pin_varlen_contract, pin_q_l2norm_single_token, pin_q_l2norm_rows,
+            pin_decode_preprocessing_single_token, pin_k_l2norm_scale_free]
