@@ -17,14 +17,17 @@ import torch
 __all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_bytes_ex",
            "kda_chunk_fwd", "kda_chunk_fwd_ex",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
-           "GATE_NONSAFE",
+           "GATE_NONSAFE", "GATE_LOG2", "FLAG_K_L2NORM", "FLAG_BETA_LOGITS", "kda_recurrent_fwd_ex",
            "FLAG_Q_L2NORM", "NOALLOC_SCRATCH_BYTES", "library_path", "load_library"]
 
 GATE_PRE = 0
 GATE_SAFE = 1
 GATE_NONSAFE = 2  # -exp(A_log) * softplus(g + dt_bias); runs on the float32 stage-by-stage path
+GATE_LOG2 = 3     # the per-token log2 decay (the recurrent entry points' gate)
 NOALLOC_SCRATCH_BYTES = 16 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 FLAG_Q_L2NORM = 1  # KDA_FLAG_Q_L2NORM
+FLAG_K_L2NORM = 2  # KDA_FLAG_K_L2NORM
+FLAG_BETA_LOGITS = 4  # KDA_FLAG_BETA_LOGITS
 _F32, _BF16 = 0, 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -68,6 +71,10 @@ def load_library():
                                          vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
                                          ctypes.c_size_t, ctypes.c_uint, vp]
         lib.kda_chunk_fwd_ex.restype = ctypes.c_int
+        lib.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
+                                             vp, i32, i32, i32, i32, i32, i32, vp, i32,
+                                             ctypes.c_uint, vp]
+        lib.kda_recurrent_fwd_ex.restype = ctypes.c_int
         lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, vp, i32, vp]
         lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
@@ -273,4 +280,38 @@ def kda_recurrent_fwd(q, k, v, gate, beta, initial_state=None, output_final_stat
         _ptr(q), _ptr(k), _ptr(v), dt, _ptr(gate), _ptr(beta), _ptr(initial_state),
         _ptr(final_state), _ptr(cu_seqlens), n, B, T, H, K, V, _ptr(o), _dt(o, "o"),
         _stream(stream)))
+    return o, final_state
+
+
+def kda_recurrent_fwd_ex(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_LOG2,
+                         lower_bound=-5.0, initial_state=None, output_final_state=False,
+                         cu_seqlens=None, o=None, final_state=None, stream=None, o_dtype=None,
+                         flags=0):
+    """Token-sequential KDA forward with the decode-side preprocessing in the kernel: ``g`` is
+    read according to ``mode`` (GATE_LOG2 per-token log2 decay, GATE_PRE natural-log decay,
+    GATE_SAFE / GATE_NONSAFE raw gate with A_log, dt_bias); ``flags`` combines FLAG_Q_L2NORM,
+    FLAG_K_L2NORM and FLAG_BETA_LOGITS.  Returns (o, final_state or None)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        _cuda(t, name)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dt = _dt(q, "q")
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError("q, k, v and beta must share one dtype")
+    _cuda(A_log, "A_log", torch.float32)
+    _cuda(dt_bias, "dt_bias", torch.float32)
+    _cuda(initial_state, "initial_state", torch.float32)
+    n = _seqs(cu_seqlens, B)
+    if o is None:
+        o = torch.empty((B, T, H, V), device=q.device, dtype=o_dtype or q.dtype)
+    _cuda(o, "o")
+    if final_state is None and output_final_state:
+        N = n if cu_seqlens is not None else B
+        final_state = torch.empty((N, H, K, V), device=q.device, dtype=torch.float32)
+    _cuda(final_state, "final_state", torch.float32)
+    lib = load_library()
+    _check("kda_recurrent_fwd_ex", lib.kda_recurrent_fwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
+        lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n, B,
+        T, H, K, V, _ptr(o), _dt(o, "o"), flags, _stream(stream)))
     return o, final_state

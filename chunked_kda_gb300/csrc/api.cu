@@ -168,23 +168,44 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
                              float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
                              int T, int H, int K, int V, void* o, kda_dtype o_dtype,
                              kda_stream_t stream) {
+    return kda_recurrent_fwd_ex(q, k, v, qkv_dtype, gate, KDA_F32, nullptr, nullptr, KDA_GATE_LOG2,
+                                0.0f, beta, initial_state, final_state, cu_seqlens, n_seqs, B, T,
+                                H, K, V, o, o_dtype, 0u, stream);
+}
+
+kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                const void* g, kda_dtype g_dtype, const float* A_log,
+                                const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                                const void* beta, const float* initial_state, float* final_state,
+                                const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                                int V, void* o, kda_dtype o_dtype, unsigned flags,
+                                kda_stream_t stream) {
     g_last_error.clear();
     int N = 0;
     kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
     if (st != KDA_OK) return st;
+    if (flags & ~(KDA_FLAG_Q_L2NORM | KDA_FLAG_K_L2NORM | KDA_FLAG_BETA_LOGITS))
+        return fail(KDA_ERR_INVALID_ARG, "unknown flag bits");
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
+    if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
     if (o_dtype != qkv_dtype && o_dtype != KDA_F32)
         return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
-    if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
+    if (K < 1 || K > 256 || V < 1 || V > 256)
+        return fail(KDA_ERR_UNSUPPORTED, "K and V must be in [1, 256]");
+    if (mode != KDA_GATE_LOG2) {
+        st = check_gate(mode, A_log, lower_bound);
+        if (st != KDA_OK) return st;
+    }
     const bool any_tokens = (long long)B * T > 0 && N > 0;
-    if (any_tokens && (!q || !k || !v || !gate || !beta || !o))
+    if (any_tokens && (!q || !k || !v || !g || !beta || !o))
         return fail(KDA_ERR_INVALID_ARG, "null q, k, v, gate, beta or o");
-    const void* ptrs[] = {q, k, v, gate, beta, o, initial_state, final_state};
+    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;
-    kda::RecArgs a{q, k, v, gate, beta, qkv_dtype == KDA_BF16, initial_state, final_state,
-                   cu_seqlens, N, B, T, H, K, V, o, o_dtype == KDA_F32, (cudaStream_t)stream};
+    kda::RecArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, initial_state, final_state,
+                   cu_seqlens, N, B, T, H, K, V, o, o_dtype == KDA_F32, (cudaStream_t)stream,
+                   g_dtype == KDA_BF16, (int)mode, lower_bound, A_log, dt_bias, flags};
     return cuda_status(kda::launch_recurrent(a));
 }
 

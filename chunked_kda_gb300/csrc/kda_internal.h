@@ -51,7 +51,7 @@ struct RecArgs {
     const void* q;
     const void* k;
     const void* v;
-    const float* gate;
+    const void* gate;  // the per-token log2 decay (mode 3) or the raw gate of modes 0-2
     const void* beta;
     bool qkv_bf16;
     const float* h0;
@@ -62,6 +62,12 @@ struct RecArgs {
     void* o;
     bool o_f32;  // o is float32 (else the qkv dtype)
     cudaStream_t stream;
+    bool gate_bf16 = false;
+    int mode = 3;  // 0 pre-gated (natural log), 1 safe, 2 non-safe, 3 log2 decay
+    float lb = 0.f;
+    const float* A_log = nullptr;
+    const float* dt_bias = nullptr;
+    unsigned flags = 0;  // KDA_FLAG_Q_L2NORM, KDA_FLAG_K_L2NORM, KDA_FLAG_BETA_LOGITS
 };
 
 cudaError_t launch_gate(const GateArgs& a);

@@ -85,7 +85,11 @@ typedef enum {
        stage-by-stage path, whose intra-chunk decay ratios 2^(G_i - G_j), j <= i,
        never exceed 1; that path needs a workspace even for bf16 inputs
        (kda_chunk_workspace_bytes_ex). */
-    KDA_GATE_NONSAFE = 2
+    KDA_GATE_NONSAFE = 2,
+    /* the per-token log2 decay itself (S rows scale by 2^g): the gate of the
+       recurrent entry points (attention-gym PR #317, Agent note); rejected by
+       kda_gate_fwd and the chunked forward */
+    KDA_GATE_LOG2 = 3
 } kda_gate_mode;
 
 /*
@@ -153,8 +157,10 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                          size_t workspace_bytes, kda_stream_t stream);
 
-/* Option bits of kda_chunk_fwd_ex. */
-#define KDA_FLAG_Q_L2NORM 1u /* normalise every query row inside the forward */
+/* Option bits of kda_chunk_fwd_ex (Q_L2NORM) and kda_recurrent_fwd_ex (all three). */
+#define KDA_FLAG_Q_L2NORM 1u    /* normalise every query row inside the forward */
+#define KDA_FLAG_K_L2NORM 2u    /* normalise every key row inside the forward */
+#define KDA_FLAG_BETA_LOGITS 4u /* beta holds logits; sigmoid(beta) is used */
 
 /*
  * kda_chunk_fwd with options (attention-gym PR #345 "Fuse q l2norm into the
@@ -224,7 +230,9 @@ kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, kd
  *   gate       [B, T, H, K] float32: per-token LOG2 decay (S rows scale by
  *              2^gate), e.g. kda_gate_fwd(..., chunk_size = 1, ...)
  *   q, k, v, beta, o, o_dtype, states, cu_seqlens: as for kda_chunk_fwd.
- *   K, V       64, 128 or 256 (any pair).
+ *   K, V       any value from 1 to 256 (rows and columns beyond them are masked
+ *              inside the kernel; attention-gym PR #317 tests non-power-of-two
+ *              K and V).
  * final_state may alias initial_state (in-place decode): each program reads
  * its whole state block before it writes any of it.
  */
@@ -233,6 +241,31 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
                              float* final_state, const int32_t* cu_seqlens, int n_seqs, int B,
                              int T, int H, int K, int V, void* o, kda_dtype o_dtype,
                              kda_stream_t stream);
+
+/*
+ * kda_recurrent_fwd with the decode-side preprocessing inside the kernel (attention-gym
+ * PR #317 test plan; FLA skill "fla-kda", "Correctness checklist": gate modes, raw beta
+ * logits, qk l2norm in kernel), so a decode step needs no separate activation or
+ * normalisation pass:
+ *
+ *   g, g_dtype  [B, T, H, K], KDA_F32 or KDA_BF16, read according to mode:
+ *               KDA_GATE_LOG2 the per-token log2 decay (kda_recurrent_fwd's gate);
+ *               KDA_GATE_PRE the natural-log decay; KDA_GATE_SAFE / KDA_GATE_NONSAFE
+ *               the raw gate, activated per token as kda_gate_fwd does (A_log
+ *               required, dt_bias optional, lower_bound as for kda_chunk_fwd)
+ *   flags       KDA_FLAG_Q_L2NORM / KDA_FLAG_K_L2NORM: each q / k row is used as
+ *               x / sqrt(sum x^2 + 1e-6); KDA_FLAG_BETA_LOGITS: beta holds logits
+ *               and sigmoid(beta) is used.  Unknown bits return KDA_ERR_INVALID_ARG.
+ * Every other argument is that of kda_recurrent_fwd; flags = 0 with KDA_GATE_LOG2 and a
+ * float32 g is kda_recurrent_fwd.
+ */
+kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                const void* g, kda_dtype g_dtype, const float* A_log,
+                                const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                                const void* beta, const float* initial_state, float* final_state,
+                                const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                                int V, void* o, kda_dtype o_dtype, unsigned flags,
+                                kda_stream_t stream);
 
 /* static, NUL-terminated description of a status code */
 const char* kda_status_string(kda_status status);

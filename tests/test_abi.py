@@ -133,9 +133,22 @@ def test_recurrent_and_gate_host_validation(lib):
     r = lib.kda_recurrent_fwd(P, P, P, BF16, None, P, None, None, None, 0, 1, 4, 2, 128, 128, P,
                               BF16, None)
     assert r == INVALID  # null gate
-    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 100, 128, P, BF16,
+    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 300, 128, P, BF16,
+                              None)
+    assert r == UNSUPPORTED  # K above 256 (any K, V in [1, 256] is accepted)
+    r = lib.kda_recurrent_fwd(P, P, P, BF16, P, P, None, None, None, 0, 1, 4, 2, 128, 0, P, BF16,
                               None)
     assert r == UNSUPPORTED
+
+    def rex(mode=3, flags=0, A_log=None, gdt=F32):
+        return lib.kda_recurrent_fwd_ex(P, P, P, BF16, P, gdt, A_log, None, mode, ctypes.c_float(-5.0),
+                                        P, None, None, None, 0, 1, 4, 2, 128, 128, P, BF16,
+                                        ctypes.c_uint(flags), None)
+    assert rex(flags=8) == INVALID and b"flag" in lib.kda_last_error()
+    assert rex(mode=1) == INVALID  # in-kernel gate without A_log
+    assert rex(mode=2) == INVALID
+    assert rex(mode=4) == INVALID
+    assert rex(gdt=7) == UNSUPPORTED
     g = lib.kda_gate_fwd(P, BF16, None, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, P, None)
     assert g == INVALID  # safe gate without A_log
     g = lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 48, P, None)

@@ -160,3 +160,88 @@ def test_chunk_vs_recurrent(C):
     torch.cuda.synchronize()
     assert rel_l2(to_np(o_c), to_np(o_r)) <= 2e-2
     assert rel_l2(to_np(s_c), to_np(s_r)) <= 2e-2
+
+
+# ---- non-power-of-two head sizes and the decode-side preprocessing (kda_recurrent_fwd_ex)
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("K,V", [(40, 24), (96, 80), (100, 130), (200, 256), (256, 7), (1, 1)])
+def test_recurrent_masked_head_dims(dtype, K, V):
+    """K and V that are not 64, 128 or 256 (attention-gym PR #317 test plan: non-power-of-two
+    K/V masking): dense and packed, against the oracle."""
+    w = workloads.make_dense("r", 2, 9, 3, K, V, 64, dtype, 500 + K + V, state_std=0.05)
+    gate = log2_gate((2, 9, 3, K), 501 + K)
+    o, st = run_rec(w.q, w.k, w.v, gate, w.beta, w.initial_state)
+    o_ref, s_ref = oracle.forward(w.q, w.k, w.v, gate, w.beta, None, None, oracle.GATE_LOG2, 0.0,
+                                  w.initial_state)
+    check_o(o, o_ref, dtype)
+    check_state(st, s_ref, dtype)
+    lens = [3, 0, 11]
+    wp = workloads.make_varlen("r", lens, 16, 2, K, V, 64, dtype, 502 + K)
+    gp = log2_gate((1, 16, 2, K), 503 + K)
+    o, st = run_rec(wp.q, wp.k, wp.v, gp, wp.beta, wp.initial_state, wp.cu_seqlens)
+    o_ref, s_ref = oracle.forward(wp.q, wp.k, wp.v, gp, wp.beta, None, None, oracle.GATE_LOG2,
+                                  0.0, wp.initial_state, wp.cu_seqlens)
+    check_o(o, o_ref, dtype, valid_mask(wp))
+    check_state(st, s_ref, dtype)
+
+
+def run_rec_ex(w, g, mode, flags, beta=None):
+    t = to_device(w)
+    o, st = kda().kda_recurrent_fwd_ex(t["q"], t["k"], t["v"], g.cuda(), t["beta"] if beta is None
+                                       else beta.cuda(), t["A_log"], t["dt_bias"], mode,
+                                       w.lower_bound, t["initial_state"], True, t["cu_seqlens"],
+                                       flags=flags)
+    torch.cuda.synchronize()
+    return o, st
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE, workloads.GATE_NONSAFE],
+                         ids=["pre", "safe", "nonsafe"])
+def test_recurrent_in_kernel_gate(dtype, mode):
+    """The raw gate activated inside the recurrent kernel equals the oracle with the same gate
+    mode, and the explicit path (kda_gate_fwd with chunk_size 1, then kda_recurrent_fwd)."""
+    lens = [0, 40, 1, 0, 23]
+    w = workloads.make_varlen("r", lens, 70, 2, 128, 128, 64, dtype, 520 + mode, mode=mode)
+    o, st = run_rec_ex(w, w.g, mode, 0)
+    o_ref, s_ref = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, mode,
+                                  w.lower_bound, w.initial_state, w.cu_seqlens)
+    check_o(o, o_ref, dtype, valid_mask(w))
+    check_state(st, s_ref, dtype)
+    t = to_device(w)
+    gate = kda().kda_gate_fwd(t["g"], t["A_log"], t["dt_bias"], mode, w.lower_bound,
+                              t["cu_seqlens"], 1)
+    o2, st2 = run_rec(w.q, w.k, w.v, gate, w.beta, w.initial_state, w.cu_seqlens)
+    end = sum(lens)
+    assert rel_l2(to_np(o)[:, :end], to_np(o2)[:, :end]) < 1e-5
+    assert rel_l2(to_np(st), to_np(st2)) < 1e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("flags", [1, 2, 4, 7], ids=["q", "k", "beta", "all"])
+def test_recurrent_preprocessing_flags(dtype, flags):
+    """q / k l2norm and beta logits inside the kernel: rows scaled by 1e-3 .. 1e3 and a zero
+    row, against the oracle with the same options."""
+    w = workloads.make_dense("r", 2, 21, 3, 128, 128, 64, dtype, 540 + flags, state_std=0.05)
+    gen = torch.Generator().manual_seed(541 + flags)
+    sq = torch.pow(10.0, torch.rand((2, 21, 3, 1), generator=gen) * 6 - 3)
+    sk = torch.pow(10.0, torch.rand((2, 21, 3, 1), generator=gen) * 6 - 3)
+    sq[:, 4] = 0.0
+    if flags & 1:
+        w.q = (w.q.float() * sq).to(dtype)
+    if flags & 2:
+        w.k = (w.k.float() * sk).to(dtype)
+    beta = w.beta
+    if flags & 4:
+        beta = (torch.randn((2, 21, 3), generator=gen) * 2).to(dtype)  # logits
+    gate = log2_gate((2, 21, 3, 128), 542 + flags)
+    w2 = w
+    o, st = run_rec_ex(w2, gate, kda().GATE_LOG2, flags, beta=beta)
+    o_ref, s_ref = oracle.forward(w.q, w.k, w.v, gate, beta, None, None, oracle.GATE_LOG2, 0.0,
+                                  w.initial_state, q_l2norm=bool(flags & 1),
+                                  k_l2norm=bool(flags & 2), beta_logits=bool(flags & 4))
+    check_o(o, o_ref, dtype)
+    check_state(st, s_ref, dtype)
+    if flags & 1:
+        assert (to_np(o)[:, 4] == 0).all()
