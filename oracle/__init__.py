@@ -58,7 +58,7 @@ def load(path: str | None = None):
             ip = ctypes.POINTER(ctypes.c_int32)
             lib.kda_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_double,
                                            dp, dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
                                            ctypes.c_double, ctypes.c_double, ctypes.c_int, ip,
                                            ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_fwd.restype = ctypes.c_int
@@ -147,7 +147,8 @@ def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bo
     outside every sequence (and rows of units not listed in ``units``) are NaN.
     """
     q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
-    B, T, H, K = q.shape
+    B, T, Hk, K = q.shape
+    H = v.shape[2]  # value heads; the query / key heads Hk divide them
     V = v.shape[-1]
     cu = _i32(cu_seqlens)
     N = B if cu is None else len(cu) - 1
@@ -160,7 +161,7 @@ def forward(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bo
         un = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
     rc = _load(lib).kda_oracle_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(al), _dptr(db),
                                 int(mode), float(lower_bound), _dptr(beta), _dptr(S0), _dptr(ST),
-                                _iptr(cu), 0 if cu is None else N, B, T, H, K, V, _dptr(o),
+                                _iptr(cu), 0 if cu is None else N, B, T, H, Hk, K, V, _dptr(o),
                                 float(Q_L2NORM_EPS if q_l2norm else -1.0),
                                 float(Q_L2NORM_EPS if k_l2norm else -1.0), int(bool(beta_logits)),
                                 _iptr(un), 0 if un is None else un.shape[0], int(nthreads))

@@ -41,7 +41,10 @@
  *     qk l2norm in kernel).
  *
  * Layouts (all contiguous, row-major):
- *   q, k, g : [B, T, H, K]      v, o : [B, T, H, V]      beta : [B, T, H]
+ *   q, k : [B, T, Hk, K]        g : [B, T, H, K]      v, o : [B, T, H, V]      beta : [B, T, H]
+ *   Hk = H (multi-head) or a divisor of H: value head h reads query/key head h / (H / Hk)
+ *   (grouped value heads, HV > H in FLA skill "fla-kda", "Correctness checklist"); gate,
+ *   beta, values and states follow the value heads.
  *   A_log, dt_bias : [H, K]     S0, ST : [Nst, H, K, V]  (Nst = n_seqs or B)
  *   cu_seqlens : [n_seqs + 1] int32 (NULL = dense: B rows of length T each;
  *                otherwise B must be 1 and T is the physical capacity).
@@ -140,7 +143,7 @@ int kda_oracle_gate(const double* g, const double* A_log, const double* dt_bias,
 static void run_unit(const double* q, const double* k, const double* v, const double* g,
                      const double* A_log, const double* dt_bias, int mode, double lb,
                      const double* beta, const double* S0, double* ST, double* o,
-                     long bos, long eos, int n, int h, int H, int K, int V, double q_eps,
+                     long bos, long eos, int n, int h, int H, int Hk, int K, int V, double q_eps,
                      double k_eps, int beta_logits, double* S, double* r, double* kn)
 {
     size_t st_off = ((size_t)n * H + h) * (size_t)K * V;
@@ -149,8 +152,9 @@ static void run_unit(const double* q, const double* k, const double* v, const do
     const double scale = 1.0 / sqrt((double)K);
 
     for (long t = bos; t < eos; ++t) {
-        const double* qt = q + ((size_t)t * H + h) * K;
-        const double* kt = k + ((size_t)t * H + h) * K;
+        const int hk = h / (H / Hk); /* the query / key head of value head h */
+        const double* qt = q + ((size_t)t * Hk + hk) * K;
+        const double* kt = k + ((size_t)t * Hk + hk) * K;
         if (k_eps >= 0.0) {  /* k_t <- k_t / sqrt(|k_t|^2 + k_eps) */
             double ss = 0.0;
             for (int d = 0; d < K; ++d) ss += kt[d] * kt[d];
@@ -208,11 +212,13 @@ static void run_unit(const double* q, const double* k, const double* v, const do
 int kda_oracle_fwd(const double* q, const double* k, const double* v, const double* g,
                    const double* A_log, const double* dt_bias, int mode, double lb,
                    const double* beta, const double* S0, double* ST,
-                   const int32_t* cu, int n_seqs, int B, int T, int H, int K, int V,
+                   const int32_t* cu, int n_seqs, int B, int T, int H, int Hk, int K, int V,
                    double* o, double q_eps, double k_eps, int beta_logits,
                    const int32_t* units, int n_units, int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !o || H <= 0 || K <= 0 || V <= 0) return 1;
+    if (Hk <= 0) Hk = H;
+    if (H % Hk != 0) return 1;
     if ((mode == ORC_GATE_SAFE || mode == ORC_GATE_NONSAFE) && !A_log) return 1;
     if (cu && B != 1) return 1;
     int N = cu ? n_seqs : B;
@@ -238,7 +244,7 @@ int kda_oracle_fwd(const double* q, const double* k, const double* v, const doub
                 long bos, eos;
                 seq_bounds(cu, n, T, &bos, &eos);
                 run_unit(q, k, v, g, A_log, dt_bias, mode, lb, beta, S0, ST, o, bos, eos, n,
-                         h, H, K, V, q_eps, k_eps, beta_logits, S, r, kn);
+                         h, H, Hk, K, V, q_eps, k_eps, beta_logits, S, r, kn);
             }
         }
         free(S);

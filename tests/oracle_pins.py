@@ -357,8 +357,27 @@ def pin_k_l2norm_scale_free(lib=None):
     assert not np.allclose(o3, o1, atol=1e-3)
 
 
+def pin_gva_is_repeated_heads(lib=None):
+    """Grouped value heads (HV > H, FLA skill "fla-kda", "Correctness checklist"): with Hk
+    query / key heads shared by H = 3 Hk value heads, value head h reads head h / 3, which is
+    the multi-head forward on q and k with every head repeated 3 times in a row."""
+    r = _rng(15)
+    B, T, Hk, H, K, V = 2, 19, 2, 6, 5, 4
+    q = _unit(r.normal(size=(B, T, Hk, K)))
+    k = _unit(r.normal(size=(B, T, Hk, K)))
+    v = r.normal(size=(B, T, H, V))
+    g = r.normal(size=(B, T, H, K))
+    beta = r.uniform(size=(B, T, H))
+    al = r.uniform(0, 2, size=(H, K))
+    S0 = r.normal(size=(B, H, K, V))
+    o1, s1 = oracle.forward(q, k, v, g, beta, al, None, oracle.GATE_SAFE, -4.0, S0, lib=lib)
+    q3, k3 = np.repeat(q, 3, axis=2), np.repeat(k, 3, axis=2)
+    o2, s2 = oracle.forward(q3, k3, v, g, beta, al, None, oracle.GATE_SAFE, -4.0, S0, lib=lib)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
 ALL_PINS = [pin_gate_points, pin_gate_cumsum_closed_form, pin_gate_chunk1_is_per_token,
             pin_hand_worked, pin_beta_zero, pin_linear_attention, pin_one_hot_gated,
             pin_repeated_key_ema, pin_single_token_delta, pin_scale_exact, pin_state_carry,
             pin_varlen_contract, pin_q_l2norm_single_token, pin_q_l2norm_rows,
-            pin_decode_preprocessing_single_token, pin_k_l2norm_scale_free]
+            pin_decode_preprocessing_single_token, pin_k_l2norm_scale_free, pin_gva_is_repeated_heads]

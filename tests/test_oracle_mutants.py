@@ -26,6 +26,7 @@ MUTANTS = [
      "return x > 0.0 ? x : log1p(exp(x));"),
     ("knorm_no_sqrt", "const double ks = 1.0 / sqrt(ss + k_eps);", "const double ks = 1.0 / (ss + k_eps);"),
     ("beta_logit_sign", "1.0 / (1.0 + exp(-braw))", "1.0 / (1.0 + exp(braw))"),
+    ("gva_heads_interleaved", "const int hk = h / (H / Hk);", "const int hk = h % Hk;"),
     ("qnorm_no_sqrt", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / (ss + q_eps);"),
     ("qnorm_no_eps", "qs = 1.0 / sqrt(ss + q_eps);", "qs = 1.0 / sqrt(ss);"),
     ("qnorm_abs_sum", "ss += qt[d] * qt[d];", "ss += fabs(qt[d]);"),
