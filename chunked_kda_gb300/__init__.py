@@ -69,10 +69,10 @@ def load_library():
                                       ctypes.c_size_t, vp]
         lib.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
                                          vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
-                                         ctypes.c_size_t, ctypes.c_uint, vp]
+                                         ctypes.c_size_t, i32, ctypes.c_uint, vp]
         lib.kda_chunk_fwd_ex.restype = ctypes.c_int
         lib.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
-                                             vp, i32, i32, i32, i32, i32, i32, vp, i32,
+                                             vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
                                              ctypes.c_uint, vp]
         lib.kda_recurrent_fwd_ex.restype = ctypes.c_int
         lib.kda_recurrent_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -179,6 +179,9 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     ``q_l2norm``: use every query row as q / sqrt(|q|^2 + 1e-6) without a separate pass
     over q (kda_chunk_fwd_ex with KDA_FLAG_Q_L2NORM); forward only.
 
+    Grouped value heads: q and k may have fewer heads than v (a divisor of them); value
+    head h then reads query / key head h / (H / Hk).
+
     ``final_state`` may be passed (and may be ``initial_state`` itself) to
     write the final state in place; otherwise it is allocated when
     ``output_final_state`` is true.  ``workspace`` is a uint8 CUDA tensor of at
@@ -186,8 +189,10 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         _cuda(t, name)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[3]  # value heads; q, k may have fewer (grouped value heads)
+    if k.shape != q.shape or H % Hk != 0:
+        raise ValueError("k must have q's shape and the q/k heads must divide v's heads")
     dt = _dt(q, "q")
     if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
         raise TypeError("q, k, v and beta must share one dtype")
@@ -210,8 +215,9 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
             lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n,
             B, T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes)
-    if q_l2norm:
-        _check("kda_chunk_fwd_ex", lib.kda_chunk_fwd_ex(*args, FLAG_Q_L2NORM, _stream(stream)))
+    if q_l2norm or Hk != H:
+        _check("kda_chunk_fwd_ex", lib.kda_chunk_fwd_ex(
+            *args, Hk, FLAG_Q_L2NORM if q_l2norm else 0, _stream(stream)))
     else:
         _check("kda_chunk_fwd", lib.kda_chunk_fwd(*args, _stream(stream)))
     return o, final_state
@@ -293,8 +299,10 @@ def kda_recurrent_fwd_ex(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_L
     FLAG_K_L2NORM and FLAG_BETA_LOGITS.  Returns (o, final_state or None)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
         _cuda(t, name)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[3]  # value heads; q, k may have fewer (grouped value heads)
+    if k.shape != q.shape or H % Hk != 0:
+        raise ValueError("k must have q's shape and the q/k heads must divide v's heads")
     dt = _dt(q, "q")
     if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
         raise TypeError("q, k, v and beta must share one dtype")
@@ -313,5 +321,5 @@ def kda_recurrent_fwd_ex(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_L
     _check("kda_recurrent_fwd_ex", lib.kda_recurrent_fwd_ex(
         _ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
         lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n, B,
-        T, H, K, V, _ptr(o), _dt(o, "o"), flags, _stream(stream)))
+        T, H, K, V, _ptr(o), _dt(o, "o"), Hk, flags, _stream(stream)))
     return o, final_state

@@ -119,7 +119,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          size_t workspace_bytes, kda_stream_t stream) {
     return kda_chunk_fwd_ex(q, k, v, qkv_dtype, g, g_dtype, A_log, dt_bias, mode, lower_bound, beta,
                             initial_state, final_state, cu_seqlens, n_seqs, B, T, H, K, V,
-                            chunk_size, o, o_dtype, workspace, workspace_bytes, 0u, stream);
+                            chunk_size, o, o_dtype, workspace, workspace_bytes, 0, 0u, stream);
 }
 
 kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -128,9 +128,12 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
                             const void* beta, const float* initial_state, float* final_state,
                             const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
                             int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
-                            size_t workspace_bytes, unsigned flags, kda_stream_t stream) {
+                            size_t workspace_bytes, int n_qk_heads, unsigned flags,
+                            kda_stream_t stream) {
     g_last_error.clear();
     if (flags & ~KDA_FLAG_Q_L2NORM) return fail(KDA_ERR_INVALID_ARG, "unknown flag bits");
+    if (n_qk_heads < 0 || (n_qk_heads > 0 && (H <= 0 || H % n_qk_heads != 0)))
+        return fail(KDA_ERR_INVALID_ARG, "n_qk_heads must divide H");
     int N = 0;
     kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
     if (st != KDA_OK) return st;
@@ -158,7 +161,8 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
     kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,
                    (int)mode, lower_bound, initial_state, final_state, cu_seqlens, N, B, T, H, K,
                    V, chunk_size, o, o_dtype == KDA_F32, workspace, workspace_bytes,
-                   (cudaStream_t)stream, (flags & KDA_FLAG_Q_L2NORM) != 0};
+                   (cudaStream_t)stream, (flags & KDA_FLAG_Q_L2NORM) != 0,
+                   n_qk_heads > 0 ? n_qk_heads : H};
     if (kda::fused_supported(a)) return cuda_status(kda::launch_chunk_fused(a));
     return cuda_status(kda::launch_chunk_precise(a));
 }
@@ -170,7 +174,7 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
                              kda_stream_t stream) {
     return kda_recurrent_fwd_ex(q, k, v, qkv_dtype, gate, KDA_F32, nullptr, nullptr, KDA_GATE_LOG2,
                                 0.0f, beta, initial_state, final_state, cu_seqlens, n_seqs, B, T,
-                                H, K, V, o, o_dtype, 0u, stream);
+                                H, K, V, o, o_dtype, 0, 0u, stream);
 }
 
 kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -178,9 +182,11 @@ kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda
                                 const float* dt_bias, kda_gate_mode mode, float lower_bound,
                                 const void* beta, const float* initial_state, float* final_state,
                                 const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
-                                int V, void* o, kda_dtype o_dtype, unsigned flags,
-                                kda_stream_t stream) {
+                                int V, void* o, kda_dtype o_dtype, int n_qk_heads,
+                                unsigned flags, kda_stream_t stream) {
     g_last_error.clear();
+    if (n_qk_heads < 0 || (n_qk_heads > 0 && (H <= 0 || H % n_qk_heads != 0)))
+        return fail(KDA_ERR_INVALID_ARG, "n_qk_heads must divide H");
     int N = 0;
     kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
     if (st != KDA_OK) return st;
@@ -205,7 +211,8 @@ kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda
     if (N == 0) return KDA_OK;
     kda::RecArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, initial_state, final_state,
                    cu_seqlens, N, B, T, H, K, V, o, o_dtype == KDA_F32, (cudaStream_t)stream,
-                   g_dtype == KDA_BF16, (int)mode, lower_bound, A_log, dt_bias, flags};
+                   g_dtype == KDA_BF16, (int)mode, lower_bound, A_log, dt_bias, flags,
+                   n_qk_heads > 0 ? n_qk_heads : H};
     return cuda_status(kda::launch_recurrent(a));
 }
 

@@ -190,6 +190,7 @@ struct Params {
     float lb;
     int T, H;
     int qnorm;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
+    int hr;     // value heads per query / key head: value head h reads q, k head h / hr
 };
 
 struct Sync {
@@ -739,8 +740,8 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     auto load_qk = [&](long t) {
         mbar_arrive_expect_tx(sy.bar(B_QKIN), 32768);
         for (int cb = 0; cb < 2; ++cb) {
-            tma_load_3d(sb + OFF_KG + cb * 8192, tm_k, 64 * cb, h, (int)t, sy.bar(B_QKIN));
-            tma_load_3d(sb + OFF_QG + cb * 8192, tm_q, 64 * cb, h, (int)t, sy.bar(B_QKIN));
+            tma_load_3d(sb + OFF_KG + cb * 8192, tm_k, 64 * cb, h / p.hr, (int)t, sy.bar(B_QKIN));
+            tma_load_3d(sb + OFF_QG + cb * 8192, tm_q, 64 * cb, h / p.hr, (int)t, sy.bar(B_QKIN));
         }
     };
     auto load_v = [&](long t) {
@@ -1013,13 +1014,15 @@ cudaError_t launch_chunk_fused(const FwdArgs& a) {
     using namespace fused;
     CUtensorMap mq, mk, mv, mg;
     const long tokens = (long)a.B * a.T;
-    if (!make_map(&mq, a.q, tokens, a.H, KD) || !make_map(&mk, a.k, tokens, a.H, KD) ||
+    const int Hk = a.Hk > 0 ? a.Hk : a.H;
+    if (!make_map(&mq, a.q, tokens, Hk, KD) || !make_map(&mk, a.k, tokens, Hk, KD) ||
         !make_map(&mv, a.v, tokens, a.H, VD))
         return cudaErrorInvalidValue;
     // the float32 gate is read with plain loads; its map is a placeholder the kernel never uses
     if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
-             a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0};
+             a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0,
+             a.Hk > 0 ? a.H / a.Hk : 1};
     if (a.g_bf16)
         return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
                        : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);

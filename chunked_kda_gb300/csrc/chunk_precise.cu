@@ -25,6 +25,12 @@
 #include "kda_internal.h"
 
 namespace kda {
+
+// row of query / key head for value head h at token t: Hk = H / hr query / key heads, value
+// head h reads head h / hr (grouped value heads; hr = 1 is multi-head)
+__device__ __forceinline__ size_t qk_row(long t, int h, int H, int hr) {
+    return (size_t)t * (size_t)(H / hr) + (size_t)(h / hr);
+}
 namespace {
 
 constexpr int DT = 32;  // channel tile
@@ -55,7 +61,7 @@ __global__ void __launch_bounds__(256) scores_kernel(const InT* __restrict__ q,
                                                      const InT* __restrict__ k,
                                                      const InT* __restrict__ beta,
                                                      const float* __restrict__ G, ChunkMap cm,
-                                                     int H, int K, float* __restrict__ Akk,
+                                                     int H, int hr, int K, float* __restrict__ Akk,
                                                      float* __restrict__ Aqk) {
     constexpr int PM = C * C / 256;
     __shared__ float qs[C][DT + 1], ks[C][DT + 1], gs[C][DT + 1];
@@ -72,8 +78,9 @@ __global__ void __launch_bounds__(256) scores_kernel(const InT* __restrict__ q,
             float qv = 0.f, kv = 0.f, gv = 0.f;
             if (i < len) {
                 size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
-                qv = to_f32(q[off]);
-                kv = to_f32(k[off]);
+                size_t qo = qk_row(t0 + i, h, H, hr) * K + d0 + dd;
+                qv = to_f32(q[qo]);
+                kv = to_f32(k[qo]);
                 gv = G[off];
             }
             qs[i][dd] = qv;
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
                                                  const InT* __restrict__ beta,
                                                  const float* __restrict__ G,
                                                  const float* __restrict__ Tm, ChunkMap cm, int H,
-                                                 int K, int V, float* __restrict__ w,
+                                                 int hr, int K, int V, float* __restrict__ w,
                                                  float* __restrict__ u) {
     __shared__ float Ts[C][C];
     __shared__ float bs[C];
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
             if (j < len) {
                 if (isk) {
                     size_t off = ((size_t)(t0 + j) * H + h) * K + col;
-                    val = bs[j] * to_f32(k[off]) * exp2f(G[off]);
+                    val = bs[j] * to_f32(k[qk_row(t0 + j, h, H, hr) * K + col]) * exp2f(G[off]);
                 } else {
                     val = bs[j] * to_f32(v[((size_t)(t0 + j) * H + h) * V + (col - K)]);
                 }
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
                                                    const float* __restrict__ G,
                                                    const float* __restrict__ w,
                                                    const float* __restrict__ u, const float* h0,
-                                                   float* hT, ChunkMap cm, int H, int V,
+                                                   float* hT, ChunkMap cm, int H, int hr, int V,
                                                    float* __restrict__ hc,
                                                    float* __restrict__ vn) {
     constexpr int BV = 32, DS = 16;  // value columns per block, channel tile of the update
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
                 float val = 0.f;
                 if (i < len) {
                     size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
-                    val = to_f32(k[off]) * exp2f(gl[dd] - G[off]);
+                    val = to_f32(k[qk_row(t0 + i, h, H, hr) * K + d0 + dd]) * exp2f(gl[dd] - G[off]);
                 }
                 kds[i][dd] = val;
             }
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
                                                   const float* __restrict__ Aqk,
                                                   const float* __restrict__ hc,
                                                   const float* __restrict__ vn, ChunkMap cm,
-                                                  int H, int K, int V, int qnorm,
+                                                  int H, int hr, int K, int V, int qnorm,
                                                   OutT* __restrict__ o) {
     __shared__ float qg[C][DT + 1];
     __shared__ float As[C][C + 1];
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
         float r = 1.f;
         if (qnorm && i < len) {
             float ss = 0.f;
-            const InT* qi = q + ((size_t)(t0 + i) * H + h) * K;
+            const InT* qi = q + qk_row(t0 + i, h, H, hr) * K;
             for (int d = 0; d < K; ++d) ss = fmaf(to_f32(qi[d]), to_f32(qi[d]), ss);
             r = rsqrtf(ss + kQNormEps);
         }
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
             float val = 0.f;
             if (i < len) {
                 size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
-                val = scale * to_f32(q[off]) * exp2f(G[off]);
+                val = scale * to_f32(q[qk_row(t0 + i, h, H, hr) * K + d0 + dd]) * exp2f(G[off]);
             }
             qg[i][dd] = val;
         }
@@ -329,6 +336,7 @@ template <typename InT, int C>
 cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     ChunkMap cm{a.cu, a.N, a.T, C};
     const int slots = cm.n_slots();
+    const int hr = a.Hk > 0 ? a.H / a.Hk : 1;  // value heads per query / key head
     GateArgs ga{a.g, a.g_bf16, a.A_log, a.dt_bias, a.mode, a.lb, a.cu, a.N,
                 a.B, a.T, a.H, a.K, C, ws.G, a.stream};
     cudaError_t e = launch_gate(ga);
@@ -339,25 +347,25 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     const InT* beta = (const InT*)a.beta;
     if (slots > 0) {
         dim3 g2(slots, a.H);
-        scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, a.K, ws.Akk,
+        scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K, ws.Akk,
                                                         ws.Aqk);
         solve_kernel<C><<<g2, C, 0, a.stream>>>(ws.Akk, cm, a.H, ws.Tm);
-        wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, a.K, a.V,
+        wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, hr, a.K, a.V,
                                                     ws.w, ws.u);
     }
     dim3 g5(a.V / 32, a.H, a.N);
     switch (a.K) {
         case 64:
             scan_kernel<InT, C, 64><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
-                                                              a.H, a.V, ws.hc, ws.vn);
+                                                              a.H, hr, a.V, ws.hc, ws.vn);
             break;
         case 128:
             scan_kernel<InT, C, 128><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
-                                                               a.H, a.V, ws.hc, ws.vn);
+                                                               a.H, hr, a.V, ws.hc, ws.vn);
             break;
         case 256:
             scan_kernel<InT, C, 256><<<g5, 256, 0, a.stream>>>(k, ws.G, ws.w, ws.u, a.h0, a.hT, cm,
-                                                               a.H, a.V, ws.hc, ws.vn);
+                                                               a.H, hr, a.V, ws.hc, ws.vn);
             break;
         default:
             return cudaErrorInvalidValue;
@@ -365,10 +373,10 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     if (slots > 0) {
         if (a.o_f32)
             out_kernel<InT, float, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
-                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, a.q_l2norm, (float*)a.o);
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr, a.K, a.V, a.q_l2norm, (float*)a.o);
         else
             out_kernel<InT, InT, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
-                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, a.K, a.V, a.q_l2norm, (InT*)a.o);
+                q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr, a.K, a.V, a.q_l2norm, (InT*)a.o);
     }
     return cudaGetLastError();
 }

@@ -44,6 +44,7 @@ struct FwdArgs {
     size_t ws_bytes;
     cudaStream_t stream;
     bool q_l2norm = false;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
+    int Hk = 0;             // query / key heads (a divisor of H; value head h reads h / (H / Hk))
 };
 constexpr float kQNormEps = 1e-6f;
 
@@ -68,6 +69,7 @@ struct RecArgs {
     const float* A_log = nullptr;
     const float* dt_bias = nullptr;
     unsigned flags = 0;  // KDA_FLAG_Q_L2NORM, KDA_FLAG_K_L2NORM, KDA_FLAG_BETA_LOGITS
+    int Hk = 0;          // query / key heads (a divisor of H; value head h reads h / (H / Hk))
 };
 
 cudaError_t launch_gate(const GateArgs& a);

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256, 2) recurrent_kernel(  // two programs per
     const InT* __restrict__ q, const InT* __restrict__ k, const InT* __restrict__ v,
     const GT* __restrict__ gate, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
     int mode, float lb, const InT* __restrict__ beta, const float* h0, float* hT,
-    const int32_t* __restrict__ cu, int T, int H, int K, int V, unsigned flags,
+    const int32_t* __restrict__ cu, int T, int H, int hr, int K, int V, unsigned flags,
     OutT* __restrict__ o) {
     constexpr int RPW = KP / 8;   // state rows per warp
     constexpr int VPT = BV / 32;  // value columns per lane
@@ -126,14 +126,15 @@ __global__ void __launch_bounds__(256, 2) recurrent_kernel(  // two programs per
 
     for (long t = bos; t < eos; ++t) {
         __syncthreads();  // previous token's readers of s_* are done
-        const size_t qk_off = ((size_t)t * H + h) * K;
+        const size_t qk_off = ((size_t)t * (H / hr) + h / hr) * K;  // query / key head h / hr
+        const size_t g_off = ((size_t)t * H + h) * K;
         float qv = 0.f, kv = 0.f;
         if (tid < KP) {
             float dec = 1.f;
             if (tid < K) {
                 qv = to_f32(q[qk_off + tid]);
                 kv = to_f32(k[qk_off + tid]);
-                const float gv = to_f32(gate[qk_off + tid]);
+                const float gv = to_f32(gate[g_off + tid]);
                 if constexpr (PREP)
                     dec = (mode == 3) ? exp2f(gv) : expf(gate_act(gv, s_expA[tid], s_dtb[tid], mode, lb));
                 else
@@ -241,7 +242,8 @@ static cudaError_t launch_rec_p(const RecArgs& a) {
     dim3 grid((a.V + BV - 1) / BV, a.H, a.N);
     recurrent_kernel<InT, GT, OutT, KP, BV, MASKED, PREP><<<grid, 256, 0, a.stream>>>(
         (const InT*)a.q, (const InT*)a.k, (const InT*)a.v, (const GT*)a.gate, a.A_log, a.dt_bias,
-        a.mode, a.lb, (const InT*)a.beta, a.h0, a.hT, a.cu, a.T, a.H, a.K, a.V, a.flags, (OutT*)a.o);
+        a.mode, a.lb, (const InT*)a.beta, a.h0, a.hT, a.cu, a.T, a.H, a.Hk > 0 ? a.H / a.Hk : 1, a.K,
+        a.V, a.flags, (OutT*)a.o);
     return cudaGetLastError();
 }
 

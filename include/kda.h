@@ -174,6 +174,13 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
  *                      row's 1/||q||.  Keys are used as given.  The final
  *                      state does not depend on q.  Forward only.
  *
+ *   n_qk_heads         grouped value heads (FLA skill "fla-kda", "Correctness
+ *                      checklist": HV > H): q and k are [B, T, n_qk_heads, K]
+ *                      and value head h (of H) reads query / key head
+ *                      h / (H / n_qk_heads); g, beta, v, o, A_log, dt_bias and
+ *                      the states have H heads.  0 means H (multi-head); it
+ *                      must divide H.
+ *
  * Every other argument, the layouts and the errors are those of
  * kda_chunk_fwd; unknown flag bits return KDA_ERR_INVALID_ARG.
  */
@@ -183,7 +190,8 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
                             const void* beta, const float* initial_state, float* final_state,
                             const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
                             int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
-                            size_t workspace_bytes, unsigned flags, kda_stream_t stream);
+                            size_t workspace_bytes, int n_qk_heads, unsigned flags,
+                            kda_stream_t stream);
 
 /*
  * Chunked forward for callers that cannot allocate device memory.
@@ -256,16 +264,17 @@ kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dt
  *   flags       KDA_FLAG_Q_L2NORM / KDA_FLAG_K_L2NORM: each q / k row is used as
  *               x / sqrt(sum x^2 + 1e-6); KDA_FLAG_BETA_LOGITS: beta holds logits
  *               and sigmoid(beta) is used.  Unknown bits return KDA_ERR_INVALID_ARG.
- * Every other argument is that of kda_recurrent_fwd; flags = 0 with KDA_GATE_LOG2 and a
- * float32 g is kda_recurrent_fwd.
+ *   n_qk_heads  grouped value heads, as for kda_chunk_fwd_ex (0 = H).
+ * Every other argument is that of kda_recurrent_fwd; flags = 0 with KDA_GATE_LOG2, a
+ * float32 g and n_qk_heads = 0 is kda_recurrent_fwd.
  */
 kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                                 const void* g, kda_dtype g_dtype, const float* A_log,
                                 const float* dt_bias, kda_gate_mode mode, float lower_bound,
                                 const void* beta, const float* initial_state, float* final_state,
                                 const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
-                                int V, void* o, kda_dtype o_dtype, unsigned flags,
-                                kda_stream_t stream);
+                                int V, void* o, kda_dtype o_dtype, int n_qk_heads,
+                                unsigned flags, kda_stream_t stream);
 
 /* static, NUL-terminated description of a status code */
 const char* kda_status_string(kda_status status);

@@ -40,6 +40,17 @@ def lib():
     L.kda_gate_fwd.argtypes = [vp, i32, vp, vp, i32, f32, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     L.kda_chunk_workspace_bytes.argtypes = [i32] * 8
     L.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
+    L.kda_chunk_workspace_bytes_ex.argtypes = [i32] * 9
+    L.kda_chunk_workspace_bytes_ex.restype = ctypes.c_size_t
+    # full prototypes: a call with the wrong arity raises instead of passing stray values
+    L.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
+                                   i32, i32, i32, i32, i32, i32, vp, i32, vp, ctypes.c_size_t, i32,
+                                   ctypes.c_uint, vp]
+    L.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
+                                       i32, i32, i32, i32, i32, i32, vp, i32, i32, ctypes.c_uint,
+                                       vp]
+    L.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
+                                        i32, i32, i32, i32, i32, i32, i32, vp, i32, vp]
     L.kda_status_string.restype = ctypes.c_char_p
     L.kda_last_error.restype = ctypes.c_char_p
     return L
@@ -116,13 +127,17 @@ def test_chunk_ex_flags_host_validation(lib):
     """kda_chunk_fwd_ex: unknown option bits are rejected before any launch; with valid bits
     the usual validation still applies first."""
     def ex(flags, **kw):
-        a = dict(q=P, o=P, lb=-5.0, C=64)
+        a = dict(q=P, o=P, lb=-5.0, C=64, H=2, hk=0)
         a.update(kw)
         return lib.kda_chunk_fwd_ex(a["q"], P, P, BF16, P, BF16, P, None, 1, ctypes.c_float(a["lb"]),
-                                    P, None, None, None, 0, 1, 64, 2, 128, 128, a["C"], a["o"],
-                                    BF16, None, ctypes.c_size_t(0), ctypes.c_uint(flags), None)
+                                    P, None, None, None, 0, 1, 64, a["H"], 128, 128, a["C"], a["o"],
+                                    BF16, None, ctypes.c_size_t(0), ctypes.c_int(a["hk"]),
+                                    ctypes.c_uint(flags), None)
     assert ex(2) == INVALID
     assert b"flag" in lib.kda_last_error()
+    assert ex(0, H=3, hk=2) == INVALID  # query / key heads must divide the value heads
+    assert b"n_qk_heads" in lib.kda_last_error()
+    assert ex(0, hk=-1) == INVALID
     assert ex(0x80000000) == INVALID
     assert ex(1, C=48) == UNSUPPORTED
     assert ex(1, q=None) == INVALID
@@ -143,12 +158,16 @@ def test_recurrent_and_gate_host_validation(lib):
     def rex(mode=3, flags=0, A_log=None, gdt=F32):
         return lib.kda_recurrent_fwd_ex(P, P, P, BF16, P, gdt, A_log, None, mode, ctypes.c_float(-5.0),
                                         P, None, None, None, 0, 1, 4, 2, 128, 128, P, BF16,
-                                        ctypes.c_uint(flags), None)
+                                        ctypes.c_int(0), ctypes.c_uint(flags), None)
     assert rex(flags=8) == INVALID and b"flag" in lib.kda_last_error()
     assert rex(mode=1) == INVALID  # in-kernel gate without A_log
     assert rex(mode=2) == INVALID
     assert rex(mode=4) == INVALID
     assert rex(gdt=7) == UNSUPPORTED
+    r = lib.kda_recurrent_fwd_ex(P, P, P, BF16, P, F32, None, None, 3, ctypes.c_float(0.0), P, None,
+                                 None, None, 0, 1, 4, 4, 128, 128, P, BF16, ctypes.c_int(3),
+                                 ctypes.c_uint(0), None)
+    assert r == INVALID  # 3 query / key heads do not divide 4 value heads
     g = lib.kda_gate_fwd(P, BF16, None, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, P, None)
     assert g == INVALID  # safe gate without A_log
     g = lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 48, P, None)

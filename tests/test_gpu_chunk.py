@@ -241,3 +241,31 @@ def test_nonsafe_gate_varlen():
                               mode=workloads.GATE_NONSAFE)
     o, st = run_gpu(w)
     compare(w, o, st)
+
+
+def grouped(w, hk):
+    """Keep the first hk query / key heads: value head h then reads head h / (H / hk)."""
+    w.q = w.q[:, :, :hk].contiguous()
+    w.k = w.k[:, :, :hk].contiguous()
+    return w
+
+
+@pytest.mark.parametrize("dtype,C", [(torch.bfloat16, 64), (torch.bfloat16, 32), (torch.float32, 64)],
+                         ids=["fused", "stagewise-c32", "stagewise-f32"])
+@pytest.mark.parametrize("hk", [1, 2])
+def test_grouped_value_heads(dtype, C, hk):
+    """GVA (FLA skill "fla-kda", "Correctness checklist": HV > H): 4 value heads over 1 or 2
+    query / key heads, against the oracle, and equal to the multi-head call on q and k with
+    their heads repeated."""
+    w = grouped(workloads.make_dense("t", 2, 130, 4, 128, 128, C, dtype, 600 + C + hk,
+                                     state_std=0.05), hk)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+    t = to_device(w)
+    r = 4 // hk
+    q4 = t["q"].repeat_interleave(r, dim=2)
+    k4 = t["k"].repeat_interleave(r, dim=2)
+    o2, st2 = kda().kda_chunk_fwd(q4, k4, t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
+                                  w.mode, w.lower_bound, t["initial_state"], True, None, C)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(st, st2)

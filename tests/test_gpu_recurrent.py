@@ -245,3 +245,20 @@ def test_recurrent_preprocessing_flags(dtype, flags):
     check_state(st, s_ref, dtype)
     if flags & 1:
         assert (to_np(o)[:, 4] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_recurrent_grouped_value_heads(dtype):
+    """GVA in the recurrent form: 6 value heads over 2 query / key heads."""
+    w = workloads.make_dense("r", 2, 17, 6, 128, 128, 64, dtype, 640, state_std=0.05)
+    w.q = w.q[:, :, :2].contiguous()
+    w.k = w.k[:, :, :2].contiguous()
+    gate = log2_gate((2, 17, 6, 128), 641)
+    t = to_device(w)
+    o, st = kda().kda_recurrent_fwd_ex(t["q"], t["k"], t["v"], gate.cuda(), t["beta"],
+                                       initial_state=t["initial_state"], output_final_state=True)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle.forward(w.q, w.k, w.v, gate, w.beta, None, None, oracle.GATE_LOG2, 0.0,
+                                  w.initial_state)
+    check_o(o, o_ref, dtype)
+    check_state(st, s_ref, dtype)
