@@ -255,12 +255,17 @@ def run_ours(args, world, rank, local):
     B, T, H, K, V, C = w.B, w.T, w.H, w.K, w.V, w.chunk_size
     stream = torch.cuda.current_stream()
     o = torch.empty((B, T, H, V), device=dev, dtype=torch.bfloat16)
-    ws_bytes = kda.kda_chunk_workspace_bytes(torch.bfloat16, B, T, H, K, V, C, 0)
+    n_ws = 0 if w.cu_seqlens is None else w.n_seqs
+    ws_bytes = kda.kda_chunk_workspace_bytes(w.q.dtype, B, T, H, K, V, C, n_ws, w.mode)
     ws = torch.empty(max(ws_bytes, 1), device=dev, dtype=torch.uint8)
+    # the workload's own initial state and packing; a final state is written when an initial
+    # state is given (the dense B4 T4096 H64 case is the output-only forward)
+    S_fin = None if w.initial_state is None else torch.empty_like(w.initial_state)
 
     def step():
         kda.kda_chunk_fwd(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, w.mode, w.lower_bound,
-                          None, False, None, C, o=o, workspace=ws)
+                          w.initial_state, False, w.cu_seqlens, C, o=o, workspace=ws,
+                          final_state=S_fin)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -280,15 +285,22 @@ def run_ours(args, world, rank, local):
     barrier()
     sampler.mark(wall0, wall1)
     local_s = ev0.elapsed_time(ev1) / 1e3
-    head_tokens = B * T * H
+    head_tokens = w.head_tokens()  # valid tokens x heads (packed: the sum of the lengths)
     t_max, units_all = aggregate(local_s, head_tokens * args.steps, world, dev)
     ms_per_step = 1e3 * t_max / args.steps
 
     if args.chunk_only:
         sampler.stop()
         if rank == 0:
+            state_bytes = 0 if w.initial_state is None else 2 * w.initial_state.numel() * 4
+            nb = algorithmic_bytes_per_head_token(K, V) * head_tokens + state_bytes
             print(json.dumps({"workload": args.workload, "ms_per_step": ms_per_step,
-                              "head_tokens_per_s": units_all / t_max}), flush=True)
+                              "head_tokens_per_s": units_all / t_max,
+                              "path": "fused" if launches_per_chunk_call(w.q.dtype, K, V, C) == 1
+                              and w.mode in (0, 1) else "stage-by-stage",
+                              "algorithmic_gbs": nb / (ms_per_step / 1e3) / 1e9,
+                              "frac_of_hbm": nb / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"]}),
+                  flush=True)
         return
 
     # end to end through the public API: pinned host inputs -> device, forward, o -> host
@@ -303,8 +315,8 @@ def run_ours(args, world, rank, local):
         for n in names:
             dbuf[n].copy_(host[n], non_blocking=True)
         kda.kda_chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], w.A_log,
-                          w.dt_bias, w.mode, w.lower_bound, None, False, None, C, o=o,
-                          workspace=ws)
+                          w.dt_bias, w.mode, w.lower_bound, w.initial_state, False, w.cu_seqlens,
+                          C, o=o, workspace=ws, final_state=S_fin)
         o_host.copy_(o, non_blocking=True)
 
     e2e_step()
@@ -387,11 +399,11 @@ def run_ours(args, world, rank, local):
 
 
 def launches_per_chunk_call(dtype, K, V, C):
-    """Kernels one kda_chunk_fwd call launches: the fused bf16 kernel (K = V = 128, C = 64),
+    """Kernels one kda_chunk_fwd call launches: the fused bf16 kernel (K = V = 128),
     else the six stage kernels (gate, scores, solve, w/u, scan, output)."""
     import torch
 
-    return 1 if (dtype == torch.bfloat16 and K == 128 and V == 128 and C == 64) else 6
+    return 1 if (dtype == torch.bfloat16 and K == 128 and V == 128 and C in (32, 64)) else 6
 
 
 def main():
@@ -402,8 +414,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="dense workload name (chunked_kda_gb300.workloads); default is the one "
-                         "the metric is quoted on")
+                    help="workload name (chunked_kda_gb300.workloads, dense or packed); default is "
+                         "the one the metric is quoted on")
     ap.add_argument("--chunk-only", action="store_true",
                     help="time the chunked forward only (no e2e, decode or CPU leg); for profiling")
     args = ap.parse_args()

@@ -991,10 +991,12 @@ bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D) {
 
 }  // namespace fused
 
-// bf16, K = V = 128, C = 64, and a gate whose per-token decay is bounded (pre-gated under the
-// bounded-gate contract, or safe): the sub-block anchors of the score operands rely on it
+// bf16, K = V = 128 and a gate whose per-token decay is bounded (pre-gated under the
+// bounded-gate contract, or safe): the sub-block anchors of the score operands rely on it.
+// Both chunk sizes run as 64-token chunks: the chunked form computes the same function for
+// any chunk size (only the rounding differs), and chunks restart at every sequence start.
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode) {
-    return qkv_bf16 && K == 128 && V == 128 && C == 64 && (mode == 0 || mode == 1);
+    return qkv_bf16 && K == 128 && V == 128 && (C == 32 || C == 64) && (mode == 0 || mode == 1);
 }
 
 bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C, a.mode); }

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(256, 2) recurrent_kernel(  // two programs per
         s_dtb[tid] = (in && dt_bias) ? __ldg(dt_bias + (size_t)h * K + tid) : 0.f;
     }
     const size_t st_base = ((size_t)n * H + h) * (size_t)K * V;
+    const int Hq = H / hr, hq = h / hr;  // query / key heads, and the one of this value head
     const int col = v0 + lane * VPT;
     // whole vectors of VPT columns when the rows allow it, else one column at a time
     const bool vec = !MASKED || ((V % VPT) == 0 && col + VPT <= V);
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(256, 2) recurrent_kernel(  // two programs per
 
     for (long t = bos; t < eos; ++t) {
         __syncthreads();  // previous token's readers of s_* are done
-        const size_t qk_off = ((size_t)t * (H / hr) + h / hr) * K;  // query / key head h / hr
+        const size_t qk_off = ((size_t)t * Hq + hq) * K;  // query / key head h / hr
         const size_t g_off = ((size_t)t * H + h) * K;
         float qv = 0.f, kv = 0.f;
         if (tid < KP) {

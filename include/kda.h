@@ -142,7 +142,11 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
  *   beta       [B, T, H], dtype qkv_dtype, post-sigmoid
  *   o          [B, T, H, V], dtype o_dtype (output): the qkv dtype, or KDA_F32
  *              to keep the forward's FP32 result without the final rounding
- *   chunk_size 32 or 64 (Helion PR #3290: the two chunk sizes FLA's KDA accepts)
+ *   chunk_size 32 or 64 (Helion PR #3290: the two chunk sizes FLA's KDA accepts).
+ *              The bf16 tensor-core path (K = V = 128, pre-gated or safe gate)
+ *              runs both as 64-token chunks: the chunked form is exact for any
+ *              chunk size, so only the rounding differs; the float32 path uses
+ *              the size given.
  *   K, V       64, 128 or 256 (K == V on the bf16 tensor-core path; any pair
  *              of these on the float32 path)
  *   workspace  device scratch of at least kda_chunk_workspace_bytes(...) bytes,

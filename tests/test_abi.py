@@ -199,7 +199,8 @@ def test_workspace_bytes(lib):
     assert lib.kda_chunk_workspace_bytes(F32, 1, T, H, K, V, 48, 0) == 0
     # the fused bf16 kernel keeps every intermediate on chip
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) > 0
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) == 0  # fused too
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) > 0
     # by gate mode: the non-safe gate runs on the stage-by-stage path (scratch for bf16 too)
     ex = lib.kda_chunk_workspace_bytes_ex
     ex.restype = ctypes.c_size_t
