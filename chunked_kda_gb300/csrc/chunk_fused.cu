@@ -579,16 +579,25 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // ---- a3: T = (I + Akk)^-1, each block written as fp32 (for the later blocks) and
         // straight into the bf16 T diag(beta) hand-off (K-major [64][64]; its strictly upper
         // blocks were zeroed once).  Diagonal 16 x 16 blocks by forward substitution, one
-        // thread per column (warps 0-1).
+        // thread per column (warps 0-1), right-looking: once x[j] is final, column j of the
+        // block (contiguous in the stored transpose, read 4 entries at a time) updates the
+        // later rows; entries above the thread's column stay exactly zero.
         if (w < 2) {
             const int b = 2 * w + (l >> 4), cc = l & 15;
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float val = (i == cc) ? 1.f : 0.f;
+            for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j < i; ++j) val = fmaf(-As[(16 * b + j) * LD + 16 * b + i], x[j], val);
-                x[i] = (i < cc) ? 0.f : val;
+            for (int j = 0; j < 15; ++j) {
+                const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
+#pragma unroll
+                for (int m = (j + 1) / 4; m < 4; ++m) {
+                    const float4 a4 = col[m];
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * m + e > j) x[4 * m + e] = fmaf(-av[e], x[j], x[4 * m + e]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
@@ -616,8 +625,11 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         {
             const int gq = l >> 2, tq = l & 3;
             // acc += A[r0.., kc0 .. kc0 + 8 nk) T[.., n0 .. n0 + 16), A read from its transpose
+            // (nk is 2 or 4; the loop is unrolled to the larger count so loads can run ahead)
             auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
-                for (int ks = 0; ks < nk; ++ks) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks >= nk) break;
                     const int kc = kc0 + 8 * ks;
                     uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
                                      to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
@@ -695,7 +707,9 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             bar_sync(BAR_PREP, NGRP);
             if (w < 4) {  // step 3
                 float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                for (int s = 2; s <= rb; ++s) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
+#pragma unroll
+                for (int s = 2; s <= 3; ++s)
+                    if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
                 store_T(16 * rb, 16 * cb, ta, false);
             }
             fence_proxy_async_smem();  // the hand-off is complete
