@@ -47,8 +47,8 @@ def algorithmic_flops_per_head_token(K, V, C):
 # capture of the kernel source whose sha256 starts with `source_sha256`: the 152-head case
 # (311,296 head-tokens) scaled by head-tokens to 1,048,576.  Reported only while the source is
 # unchanged; a changed kernel reports null until it is captured again.
-FUSED_TRAFFIC = {"source_sha256": "b75f2b5df4b01dda", "workload": "dense_bf16_b4_t4096_h64_d128",
-                 "bytes": (319.83e6 + 62.98e6) * 1048576 / 311296}
+FUSED_TRAFFIC = {"source_sha256": "7a65cc6588d26f3f", "workload": "dense_bf16_b4_t4096_h64_d128",
+                 "bytes": (319.79e6 + 63.37e6) * 1048576 / 311296}
 
 
 def fused_traffic_bytes(workload):
