@@ -29,6 +29,8 @@ bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 kda_status check_layout(const int32_t* cu, int n_seqs, int B, int T, int H, int* N) {
     if (B < 0 || T < 0 || H <= 0) return fail(KDA_ERR_INVALID_ARG, "B, T must be >= 0 and H > 0");
     if ((long long)B * T * H > (1ll << 40)) return fail(KDA_ERR_INVALID_ARG, "input too large");
+    // token coordinates (TMA) and chunk-slot numbers are 32-bit
+    if ((long long)B * T >= (1ll << 31)) return fail(KDA_ERR_INVALID_ARG, "B * T must be below 2^31");
     if (cu) {
         if (B != 1) return fail(KDA_ERR_INVALID_ARG, "packed mode (cu_seqlens != NULL) needs B == 1");
         if (n_seqs < 0 || n_seqs > 65535)

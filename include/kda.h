@@ -29,6 +29,8 @@
  *     library never allocates, never synchronises the stream and never reads
  *     cu_seqlens on the host; all work is enqueued on `stream`, so calls can be
  *     captured in a CUDA graph.
+ *   - Sizes: B * T (tokens, or the packed capacity) below 2^31; B and n_seqs
+ *     at most 65535.
  *   - Layout is token-major: q, k, g [B, T, H, K]; v, o [B, T, H, V];
  *     beta [B, T, H]; A_log, dt_bias [H, K] float32; states [N, H, K, V]
  *     float32 with N = n_seqs (packed) or B (dense).

@@ -113,6 +113,8 @@ def test_chunk_host_validation(lib):
     assert _chunk(lib, dt=F32, ws=None, ws_bytes=0) == INVALID
     assert b"workspace" in lib.kda_last_error()
     assert _chunk(lib, H=0) == INVALID
+    assert _chunk(lib, B=2, T=1 << 30) == INVALID  # B * T reaches 2^31
+    assert b"2^31" in lib.kda_last_error()
     # non-safe gate: A_log required, lower_bound ignored, scratch needed even for bf16
     assert _chunk(lib, mode=2, A_log=None) == INVALID
     assert _chunk(lib, mode=2, lb=0.0) == INVALID
