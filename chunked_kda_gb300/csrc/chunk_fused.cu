@@ -1,4 +1,4 @@
-// Fused chunked KDA forward for bf16 inputs, K = V = 128, C = 64 (sm_103a).
+// Fused chunked KDA forward for bf16 inputs, K = V = 128, 64-token chunks (sm_103a).
 //
 // One CTA of 512 threads per (sequence, head) walks the sequence chunk by
 // chunk; the FP32 state never leaves the SM, so HBM sees only q, k, v, g,
@@ -17,7 +17,8 @@
 //      2^(G_m(col) - G_j), whose first term is <= 1 (FLA skill "fla-kda",
 //      "Safe gate numerical note").
 //   a3 T = (I + Akk)^-1: 16 x 16 diagonal blocks by forward substitution in
-//      FP32, the off-diagonal blocks level by level with warp-level tf32 MMAs
+//      FP32, the off-diagonal blocks by a 2 x 2 recursion on 32 x 32 blocks with
+//      warp-level tf32 MMAs
 //   a4/a5 the WY terms and the state step as tcgen05 MMAs, with the state
 //      transposed (TMEM lane = value channel v):
 //        Y^T   = h^T (k 2^G)^T                               [V x C]
@@ -39,9 +40,14 @@
 // a timeout, after which the CTA skips all further waits, MMAs and copies,
 // runs out its loop, drains the MMAs in flight and frees TMEM.
 //
-// Precision: bf16 operands, FP32 accumulation; the score rows, v_new and Aqk
+// Precision: bf16 operands, FP32 accumulation; the q score rows, v_new and Aqk
 // are carried as bf16 pairs x = hi + lo (hi = bf16(x), lo = bf16(x - hi))
-// and multiplied as hi*B + lo*B (+ A*lo), about 16 significant bits.
+// and multiplied as hi*B + lo*B (+ A*lo), about 16 significant bits; the k
+// score rows are hi only.
+//
+// Options: the deferred q l2norm (each output row scaled by 1/||q row||, the
+// sums of squares from the prep warps) and grouped value heads (value head h
+// reads query / key head h / (H / Hk) through the TMA head coordinate).
 #include <cudaTypedefs.h>
 
 #include <type_traits>
