@@ -269,3 +269,63 @@ def test_grouped_value_heads(dtype, C, hk):
                                   w.mode, w.lower_bound, t["initial_state"], True, None, C)
     torch.cuda.synchronize()
     assert torch.equal(o, o2) and torch.equal(st, st2)
+
+
+# ---- degenerate inputs and a long sequence
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_beta_zero_reads_the_decayed_state(dtype):
+    """beta = 0: the state is only decayed, o_t = S_t^T q_t / sqrt(K) with S_t the initial state
+    decayed through token t (a closed form; the oracle pins the same case)."""
+    w = workloads.make_dense("t", 1, 70, 2, 128, 128, 64, dtype, 801, state_std=0.05,
+                             mode=workloads.GATE_PRE)
+    w.beta = torch.zeros_like(w.beta)
+    w.g = (w.g.float() * 0.02).to(dtype)  # decay mild enough that S_0 is still visible at the end
+    o, st = run_gpu(w)
+    a = w.g.double()[0].cumsum(0)                       # [T, H, K] natural-log decay so far
+    S0 = w.initial_state.double()[0]                    # [H, K, V]
+    q = w.q.double()[0]                                 # [T, H, K]
+    ref = torch.einsum("thk,hkv->thv", q * torch.exp(a), S0) / math.sqrt(128)
+    check_o(o, ref.unsqueeze(0).numpy(), dtype)
+    check_state(st, (torch.exp(a[-1])[..., None] * S0).unsqueeze(0).numpy(), dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_zero_queries_and_single_tokens(dtype):
+    """All-zero query rows give zero output rows exactly; sequences of one token match the
+    oracle (the chunk is one valid row and 63 masked ones)."""
+    w = workloads.make_dense("t", 3, 1, 2, 128, 128, 64, dtype, 802, state_std=0.05)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+    w2 = workloads.make_dense("t", 1, 90, 2, 128, 128, 64, dtype, 803, state_std=0.05)
+    w2.q[:, 10:30] = 0
+    o2, _ = run_gpu(w2)
+    assert (o2[:, 10:30] == 0).all()
+
+
+@pytest.mark.slow
+def test_long_sequence_carry_is_bitwise():
+    """2^17 tokens through the fused kernel: the first 4096 outputs against the oracle, and
+    two calls split at a chunk boundary and chained through the state equal one call bit
+    for bit (the chunks, hence the arithmetic, are the same)."""
+    T, H = 1 << 17, 2
+    w = workloads.make_dense("t", 1, T, H, 128, 128, 64, torch.bfloat16, 804, state_std=0.05)
+    o, st = run_gpu(w)
+    n = 4096
+    wp = workloads.Workload("p", 1, n, H, 128, 128, 64, w.mode, w.lower_bound, w.q[:, :n],
+                            w.k[:, :n], w.v[:, :n], w.g[:, :n], w.beta[:, :n], w.A_log,
+                            w.dt_bias, w.initial_state)
+    o_ref, _ = run_oracle(wp)
+    check_o(o[:, :n], o_ref, torch.bfloat16)
+    t1 = 64 * 1000
+    S = w.initial_state
+    outs = []
+    for sl in (slice(0, t1), slice(t1, T)):
+        ws = workloads.Workload("p", 1, sl.stop - sl.start, H, 128, 128, 64, w.mode,
+                                w.lower_bound, w.q[:, sl].contiguous(), w.k[:, sl].contiguous(),
+                                w.v[:, sl].contiguous(), w.g[:, sl].contiguous(),
+                                w.beta[:, sl].contiguous(), w.A_log, w.dt_bias, S)
+        op, sp = run_gpu(ws)
+        outs.append(op)
+        S = sp.cpu()
+    assert torch.equal(torch.cat(outs, dim=1), o) and torch.equal(S.cuda(), st)
