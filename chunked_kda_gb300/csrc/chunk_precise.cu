@@ -188,7 +188,11 @@ __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
     }
 }
 
-// a5: sequential state scan over the chunks of one sequence, 32 value columns per block
+// a5: sequential state scan over the chunks of one sequence, 32 value columns per block.
+// v_new = u - w h: the w rows of the chunk are staged 32 channels at a time and every
+// thread accumulates a register tile of C / 16 rows x 2 columns.  h <- 2^Glast h + kd^T v_new:
+// every thread owns CPT consecutive columns of one state row d in registers and adds
+// kd[i][d] v_new[i][.] over the chunk's rows, kd = k 2^(Glast - G) read coalesced over d.
 template <typename InT, int C, int K>
 __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
                                                    const float* __restrict__ G,
@@ -197,12 +201,15 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
                                                    float* hT, ChunkMap cm, int H, int hr, int V,
                                                    float* __restrict__ hc,
                                                    float* __restrict__ vn) {
-    constexpr int BV = 32, DS = 16;  // value columns per block, channel tile of the update
-    __shared__ float hs[K][BV];
-    __shared__ float vns[C][BV];
-    __shared__ float kds[C][DS + 1];
-    __shared__ float gl[DS];
-    const int tid = threadIdx.x, lane = tid & 31, grp = tid >> 5;
+    constexpr int BV = 32, DW = 32;       // value columns per block, channels per w tile
+    constexpr int RPT = C / 16;           // v_new rows per thread (16 row groups x 16 column pairs)
+    constexpr int TPR = 256 / K;          // threads per state row in the update
+    constexpr int CPT = BV / TPR;         // state columns per thread in the update
+    static_assert(K * TPR == 256 && CPT % 4 == 0, "state tiling");
+    __shared__ __align__(16) float hs[K][BV];
+    __shared__ __align__(16) float vns[C][BV];
+    __shared__ float wt[C][DW + 1];
+    const int tid = threadIdx.x;
     const int v0 = blockIdx.x * BV, h = blockIdx.y, n = blockIdx.z;
     long bos, eos;
     if (cm.cu) { bos = __ldg(cm.cu + n); eos = __ldg(cm.cu + n + 1); }
@@ -212,6 +219,8 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
         int d = idx / BV, vv = idx % BV;
         hs[d][vv] = h0 ? h0[st + (size_t)d * V + v0 + vv] : 0.f;
     }
+    const int rg = tid >> 4, cp = tid & 15;          // v_new: rows rg*RPT.., columns 2cp, 2cp+1
+    const int dr = tid / TPR, c0 = (tid % TPR) * CPT;  // update: row dr, columns c0..c0+CPT
     const int slot0 = cm.first_slot(n, (int)bos);
     const int nt = (int)((eos - bos + C - 1) / C);
     for (int c = 0; c < nt; ++c) {
@@ -224,38 +233,72 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
             hc[hoff + (size_t)d * V + v0 + vv] = hs[d][vv];
         }
         // v_new = u - w h
-        for (int i = grp; i < len; i += 8) {
-            size_t row = (size_t)(t0 + i) * H + h;
-            float acc = u[row * V + v0 + lane];
-            const float* wr = w + row * K;
-            for (int d = 0; d < K; ++d) acc = fmaf(-__ldg(wr + d), hs[d][lane], acc);
-            vns[i][lane] = acc;
-            vn[row * V + v0 + lane] = acc;
+        float acc[RPT][2];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = rg * RPT + r;
+            const size_t row = (size_t)(t0 + i) * H + h;
+            acc[r][0] = (i < len) ? u[row * V + v0 + 2 * cp] : 0.f;
+            acc[r][1] = (i < len) ? u[row * V + v0 + 2 * cp + 1] : 0.f;
+        }
+        for (int d0 = 0; d0 < K; d0 += DW) {
+            __syncthreads();  // the previous w tile is consumed
+            for (int idx = tid; idx < C * DW; idx += 256) {
+                const int i = idx / DW, dd = idx % DW;
+                wt[i][dd] = (i < len) ? w[((size_t)(t0 + i) * H + h) * K + d0 + dd] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int dd = 0; dd < DW; ++dd) {
+                const float2 hv = *reinterpret_cast<const float2*>(&hs[d0 + dd][2 * cp]);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const float wv = wt[rg * RPT + r][dd];
+                    acc[r][0] = fmaf(-wv, hv.x, acc[r][0]);
+                    acc[r][1] = fmaf(-wv, hv.y, acc[r][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = rg * RPT + r;
+            vns[i][2 * cp] = acc[r][0];
+            vns[i][2 * cp + 1] = acc[r][1];
+            if (i < len) {
+                const size_t row = (size_t)(t0 + i) * H + h;
+                vn[row * V + v0 + 2 * cp] = acc[r][0];
+                vn[row * V + v0 + 2 * cp + 1] = acc[r][1];
+            }
         }
         __syncthreads();
-        // h <- 2^Glast h + (k 2^(Glast - G))^T v_new, channel tiles of DS
-        const size_t last = ((size_t)(t0 + len - 1) * H + h) * K;
-        for (int d0 = 0; d0 < K; d0 += DS) {
-            if (tid < DS) gl[tid] = G[last + d0 + tid];
-            __syncthreads();
-            for (int idx = tid; idx < C * DS; idx += 256) {
-                int i = idx / DS, dd = idx % DS;
-                float val = 0.f;
-                if (i < len) {
-                    size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
-                    val = to_f32(k[qk_row(t0 + i, h, H, hr) * K + d0 + dd]) * exp2f(gl[dd] - G[off]);
-                }
-                kds[i][dd] = val;
+        // h <- 2^Glast h + (k 2^(Glast - G))^T v_new
+        const float gl = G[((size_t)(t0 + len - 1) * H + h) * K + dr];
+        float hrow[CPT];
+        {
+            const float gam = exp2f(gl);
+#pragma unroll
+            for (int j = 0; j < CPT; j += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(&hs[dr][c0 + j]);
+                hrow[j] = gam * x.x; hrow[j + 1] = gam * x.y; hrow[j + 2] = gam * x.z; hrow[j + 3] = gam * x.w;
             }
-            __syncthreads();
-            for (int dd = grp; dd < DS; dd += 8) {
-                int d = d0 + dd;
-                float acc = exp2f(gl[dd]) * hs[d][lane];
-                for (int i = 0; i < len; ++i) acc = fmaf(kds[i][dd], vns[i][lane], acc);
-                hs[d][lane] = acc;
-            }
-            __syncthreads();
         }
+#pragma unroll 4
+        for (int i = 0; i < len; ++i) {
+            const size_t off = ((size_t)(t0 + i) * H + h) * K + dr;
+            const float kd = to_f32(k[qk_row(t0 + i, h, H, hr) * K + dr]) * exp2f(gl - G[off]);
+#pragma unroll
+            for (int j = 0; j < CPT; j += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(&vns[i][c0 + j]);
+                hrow[j] = fmaf(kd, x.x, hrow[j]);
+                hrow[j + 1] = fmaf(kd, x.y, hrow[j + 1]);
+                hrow[j + 2] = fmaf(kd, x.z, hrow[j + 2]);
+                hrow[j + 3] = fmaf(kd, x.w, hrow[j + 3]);
+            }
+        }
+        __syncthreads();  // every thread has read hs and vns
+#pragma unroll
+        for (int j = 0; j < CPT; j += 4)
+            *reinterpret_cast<float4*>(&hs[dr][c0 + j]) = make_float4(hrow[j], hrow[j + 1], hrow[j + 2], hrow[j + 3]);
     }
     __syncthreads();
     if (hT) {
