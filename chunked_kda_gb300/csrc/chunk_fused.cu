@@ -23,18 +23,19 @@
 //      transposed (TMEM lane = value channel v):
 //        Y^T   = h^T (k 2^G)^T                               [V x C]
 //        vn^T  = v^T (T diag beta)^T - Y^T (T diag beta)^T   (v_new)
-//        dH^T  = vn^T (k 2^(Glast - G))                      [V x K]
-//        h^T  <- h^T Diag(2^Glast) + dH^T                    (FP32, registers)
+//        h^T  <- h^T Diag(2^Glast) + vn^T (k 2^(Glast - G))  [V x K], FP32 in TMEM:
+//                the scaling by the chain warps, the product accumulated by the MMA
 //   a6 o^T = h^T (s q 2^G)^T + vn^T Aqk^T                    [V x C]
 // Rows beyond the end of a sequence are masked to zero before any product.
 //
 // Warp roles.  Warps 0-7 ("prep") build everything chunk c needs that does
 // not depend on the state: gate, cumsum, exponent anchors, score operands,
 // the score MMA, Akk / Aqk, the solve, and the hand-off operands (k 2^G,
-// s q 2^G, k 2^(Gl-G), T diag(beta), Aqk, 2^Glast).  Warps 8-15 ("chain")
-// run the state step of the previous chunk at the same time: their operands
-// h^T, Y^T and v_new^T live in TMEM as MMA A operands, the state in
-// registers.  The groups hand buffers to each other through mbarriers; a
+// s q 2^G, k 2^(Gl-G), T diag(beta), Aqk, 2^Glast); warps 4-7 compute the
+// next chunk's gate while warps 0-3 invert.  Warps 8-15 ("chain") run the
+// state step of the previous chunk at the same time: their operands h^T,
+// Y^T and v_new^T live in TMEM as MMA A operands, the FP32 state in TMEM as
+// well.  The groups hand buffers to each other through mbarriers; a
 // buffer the chain has finished with is released by the commit of the MMA
 // that read it.  Every mbarrier wait is bounded: a wait that gives up counts
 // a timeout, after which the CTA skips all further waits, MMAs and copies,
@@ -67,6 +68,7 @@ using namespace sm100;
 constexpr int C = 64, KD = 128, VD = 128;
 constexpr int NTHR = 512, NGRP = 256;            // two groups of 8 warps
 constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;  // named barriers of the groups
+constexpr uint32_t BAR_INV = 3, BAR_GATE = 4;    // prep warps 0-3 (inverse) / 4-7 (next gate)
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T          [chain]
@@ -79,6 +81,7 @@ constexpr uint32_t OFF_SB = 81920;     // score cols [128 ch][160] MN-major, 3 g
 constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
 constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
 constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [4][16][24]
+constexpr uint32_t OFF_GS = 73728;     //   the next chunk's G fp32 [64 rows][128 ch]
 constexpr uint32_t OFF_KG = 131072;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
 constexpr uint32_t OFF_QG = 147456;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
@@ -88,17 +91,20 @@ constexpr uint32_t OFF_TP = 180224;    // hand-off: T diag(beta) bf16 [64][64] K
 constexpr uint32_t OFF_AQKH = 188416;  // hand-off: Aqk hi [64][64]
 constexpr uint32_t OFF_AQKL = 196608;  // hand-off: Aqk lo [64][64]
 constexpr uint32_t OFF_GAM = 204800;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
-constexpr uint32_t OFF_BETA = 205824;  // prep: beta fp32 [64]
-constexpr uint32_t OFF_XCH = 206080;   // prep: fp32 [4][128] per-sub-block gate sums
+constexpr uint32_t OFF_BETA = 205824;  // prep: beta fp32 [2 chunks][64]
+constexpr uint32_t OFF_GCARRY = 206336;  // prep: fp32 [128] gate sums of rows 0-31
 constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block midpoints
 constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
 constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
-constexpr uint32_t OFF_BRAW = 210816;  // prep: raw beta words of the next chunk [64]
 constexpr uint32_t OFF_QSS = 211072;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
-constexpr uint32_t SMEM_BYTES = 212096 + 1024;  // + alignment slack
+constexpr uint32_t OFF_KD1 = 212992;   // hand-off: k 2^(Gl-G) of the odd chunks (OFF_KD: the even)
+constexpr uint32_t SMEM_BYTES = 229376 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
-static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB, "layout");
+static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_GS, "layout");
+static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG, "layout");
+static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 128 * 4 <= OFF_GM, "layout");
+static_assert(OFF_QSS + 1024 <= OFF_KD1 && OFF_KD1 % 1024 == 0, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
 
@@ -107,15 +113,18 @@ enum {
     B_VFULL = 0, B_QKIN, B_GIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
     B_DRAIN0, B_DRAIN1, NBAR
 };
+static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC, "mbarriers");
 
 // TMEM columns
-constexpr uint32_t TM_S = 0;     // scores [128 lanes][160]                          (prep)
-constexpr uint32_t TM_Y = 160;   // Y^T [128][64]; then v_new^T hi (160..191), lo (192..223)
-constexpr uint32_t TM_O = 224;   // o^T [128][64]
-constexpr uint32_t TM_VN = 288;  // v_new^T accumulator [128][64]; holds h^T (bf16) between chunks
-constexpr uint32_t TM_DH = 352;  // dH^T [128][128]
-constexpr uint32_t TM_YA = 480;  // Y^T bf16 [128][64] packed in 32 columns
+constexpr uint32_t TM_H = 0;     // the state h^T fp32 [128 lanes = v][128 = k]; the dH MMA
+                                 // accumulates into it once it is scaled by 2^Glast  (chain)
+constexpr uint32_t TM_Y = 128;   // Y^T [128][64]; then v_new^T hi (128..159), lo (160..191)
+constexpr uint32_t TM_O = 192;   // o^T [128][64]
+constexpr uint32_t TM_VN = 256;  // v_new^T accumulator [128][64]; holds h^T (bf16) between chunks
+constexpr uint32_t TM_YA = 320;  // Y^T bf16 [128][64] packed in 32 columns
+constexpr uint32_t TM_S = 352;   // scores [128][160]                                  (prep)
 constexpr uint32_t TM_COLS = 512;
+static_assert(TM_S + 160 <= TM_COLS && TM_YA + 32 <= TM_S, "TMEM map");
 constexpr int SB_ROWS = 160;                                                   // causal columns
 __host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
 
@@ -149,12 +158,6 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
 
 // asynchronous 4-byte global -> shared copy that reads only the first `src_bytes` bytes
 // (the rest is zero-filled); both addresses 4-byte aligned
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
@@ -227,7 +230,6 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     constexpr bool kGateTile = std::is_same<GT, __nv_bfloat16>::value;  // g arrives by TMA
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int H = p.H;
-    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
     float* gmid = reinterpret_cast<float*>(smem + OFF_GM);
     float* glast = reinterpret_cast<float*>(smem + OFF_GL);
     float* gam = reinterpret_cast<float*>(smem + OFF_GAM);
@@ -248,132 +250,140 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
     auto bf_0 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel0)); };
     auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel1)); };
-    float expA0 = 0.f, expA1 = 0.f, dtb0 = 0.f, dtb1 = 0.f;
-    if (p.mode == 1) {
-        expA0 = expf(__ldg(p.A_log + h * KD + ch0));
-        expA1 = expf(__ldg(p.A_log + h * KD + ch1));
-        if (p.dt_bias) {
-            dtb0 = __ldg(p.dt_bias + h * KD + ch0);
-            dtb1 = __ldg(p.dt_bias + h * KD + ch1);
-        }
-    }
     const float lbl2 = p.lb * kLog2e;
     const float scale = rsqrtf((float)KD);
     const GT* gptr = reinterpret_cast<const GT*>(p.g);
     const uint32_t sw_d0 = (uint32_t)((d0 & 63) >> 3), sw_b0 = (uint32_t)(d0 & 7) * 2;
+    const float* Gs = reinterpret_cast<const float*>(smem + OFF_GS);
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
 
-    // beta of the next chunk is copied one chunk ahead (threads 0-63, one row each, from a
-    // clamped, always valid row; the mask is applied when the value is used) by an
-    // asynchronous copy into shared memory, so no register waits on it.  The copy takes the
-    // aligned 4-byte word holding the element: the element and the one before it for an odd
-    // element index, the element alone (zero-filled to 4 bytes) for an even one.
-    const unsigned short* beta_bits = reinterpret_cast<const unsigned short*>(p.beta);
-    uint32_t* braw = reinterpret_cast<uint32_t*>(smem + OFF_BRAW);
-    bool beta_odd = false;
-    auto load_beta = [&](long t, int len_) {
-        const size_t idx = (size_t)(t + min(tid, len_ - 1)) * H + h;
-        beta_odd = idx & 1;
-        cp_async4(sb + OFF_BRAW + 4 * tid, beta_bits + (idx & ~(size_t)1), beta_odd ? 4u : 2u);
-        cp_async_commit();
+    // ---- a1 of chunk cn, on warps 4-7: the per-token decay in log2 units and its
+    // chunk-local cumsum (rows past the end add zero), G into the shared [64][128] buffer,
+    // the sub-block midpoints and the last row into their arrays.  Gate thread t takes the
+    // key channels 2 (t % 64) and 2 (t % 64) + 1 over the rows 32 (t / 64) .. + 31: all its
+    // loads are issued at once, and the row half 1 adds the totals of row half 0 (one
+    // exchange).  Threads t < 64 also stage beta of row t (zero past the end) into the
+    // chunk's half of a double buffer.  Chunk 0 runs before the loop, chunk c + 1 while
+    // warps 0-3 invert chunk c's Akk, in a part of the score operand area that the inverse
+    // leaves free.
+    const int gt = tid - 128;                    // gate thread 0 .. 127
+    const int gcp = gt & 63, grh = gt >> 6;      // channel pair, row half
+    const int gc0 = 2 * gcp;                     // first channel of the pair
+    // safe gate: lb log2(e) sigmoid(z), z = exp(A_log) (g + dt_bias), as
+    // lbl2 / (1 + 2^(nA g + nAd)) with nA = -exp(A_log) log2(e), nAd = nA dt_bias
+    float nA0 = 0.f, nA1 = 0.f, nAd0 = 0.f, nAd1 = 0.f;
+    if (p.mode == 1 && w >= 4) {
+        nA0 = -expf(__ldg(p.A_log + h * KD + gc0)) * kLog2e;
+        nA1 = -expf(__ldg(p.A_log + h * KD + gc0 + 1)) * kLog2e;
+        if (p.dt_bias) {
+            nAd0 = nA0 * __ldg(p.dt_bias + h * KD + gc0);
+            nAd1 = nA1 * __ldg(p.dt_bias + h * KD + gc0 + 1);
+        }
+    }
+    float* gcarry = reinterpret_cast<float*>(smem + OFF_GCARRY);
+    // beta of row gt of a chunk, loaded one chunk ahead into a register (its global load
+    // then has a whole chunk to land)
+    auto beta_of = [&](int cn) -> float {
+        const long tc0 = bos + (long)cn * C;
+        return (gt < eos - tc0) ? __bfloat162float(p.beta[(size_t)(tc0 + gt) * H + h]) : 0.f;
     };
-    if (tid < C && nt > 0) load_beta(bos, (int)min((long)C, eos - bos));
-
-    if (kGateTile && tid == 0 && nt > 0) {
+    float bet_next = (w >= 4 && gt < C && nt > 0) ? beta_of(0) : 0.f;
+    auto load_gtile = [&](long t) {
         mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
         for (int cb = 0; cb < 2; ++cb)
-            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)bos, sy.bar(B_GIN));
-    }
+            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)t, sy.bar(B_GIN));
+    };
+    auto gate_chunk = [&](int cn) {
+        const long tc0 = bos + (long)cn * C;
+        const int lenc = (int)min((long)C, eos - tc0);
+        float* gs = reinterpret_cast<float*>(smem + OFF_GS);
+        if (gt < C) {
+            bsm[(cn & 1) * C + gt] = bet_next;
+            bet_next = (cn + 1 < nt) ? beta_of(cn + 1) : 0.f;
+        }
+        if constexpr (kGateTile) {
+            if (w == 4) sy.wait(B_GIN, (uint32_t)(cn & 1));
+            bar_sync(BAR_GATE, 128);
+        }
+        const int r0 = 32 * grh;
+        float a0[32], a1[32];
+        if constexpr (kGateTile) {
+            // the pair's word in row r of the token-major [64][128] tile (two 64-channel blocks)
+            const uint32_t base = sb + OFF_GT + (uint32_t)(gc0 >> 6) * 8192u + (uint32_t)(gc0 & 6) * 2u;
+            const uint32_t chunk = (uint32_t)((gc0 & 63) >> 3);
+            uint32_t x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = ld_s32(base + sw128((uint32_t)(r0 + i), chunk));
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { a0[i] = bf_lo(x[i]); a1[i] = bf_hi(x[i]); }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float2 v2 = __ldg(reinterpret_cast<const float2*>(
+                    gptr + ((size_t)(tc0 + min(r0 + i, lenc - 1)) * H + h) * KD + gc0));
+                a0[i] = v2.x;
+                a1[i] = v2.y;
+            }
+        }
+        float m = kLog2e;  // per-token factor into log2 units
+        if (p.mode == 1) {
+            m = lbl2;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                a0[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0[i], nAd0)));
+                a1[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1[i], nAd1)));
+            }
+        }
+        // rows past the end add zero (selected, so that NaN padding there does not spread)
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const bool valid = r0 + i < lenc;
+            acc0 = fmaf(m, valid ? a0[i] : 0.f, acc0);
+            acc1 = fmaf(m, valid ? a1[i] : 0.f, acc1);
+            a0[i] = acc0;
+            a1[i] = acc1;
+        }
+        if (grh == 0) { gcarry[gc0] = acc0; gcarry[gc0 + 1] = acc1; }
+        bar_sync(BAR_GATE, 128);  // the row half 0 totals are out; every thread read the tile
+        if (kGateTile && tid == 128 && cn + 1 < nt && !sy.aborted()) load_gtile(tc0 + C);
+        float cy0 = 0.f, cy1 = 0.f;
+        if (grh == 1) { cy0 = gcarry[gc0]; cy1 = gcarry[gc0 + 1]; }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<float2*>(gs + (r0 + i) * KD + gc0) = make_float2(a0[i] + cy0, a1[i] + cy1);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            *reinterpret_cast<float2*>(gmid + (2 * grh + j) * KD + gc0) =
+                make_float2(a0[16 * j + 8] + cy0, a1[16 * j + 8] + cy1);
+        }
+        if (grh == 1) *reinterpret_cast<float2*>(glast + gc0) = make_float2(acc0 + cy0, acc1 + cy1);
+    };
+    if (kGateTile && tid == 128 && nt > 0) load_gtile(bos);
 
     // the strictly upper 16 x 16 blocks of T diag(beta) are zero in every chunk
     for (int idx = tid; idx < 64 * 8; idx += NGRP) {
         const int i = idx >> 3, c8 = idx & 7;
         if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
     }
+    if (w >= 4 && nt > 0) gate_chunk(0);
+    bar_sync(BAR_PREP, NGRP);
 
     for (int c = 0; c < nt; ++c) {
         const long t0 = bos + (long)c * C;
         const int len = (int)min((long)C, eos - t0);
 
-        // ---- gate of the own rows: from the g tile (bf16) or from global memory (float32)
-        float g0[16], g1[16];
-        if constexpr (kGateTile) {
-            sy.group_wait(B_GIN, c & 1, w == 0, BAR_PREP);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t x = ld_s32(sb + OFF_GT + tile_off(16 * rq + i));
-                g0[i] = bf_0(x);
-                g1[i] = bf_1(x);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = min(16 * rq + i, len - 1);
-                GatePair<GT>::load(gptr + ((size_t)(t0 + r) * H + h) * KD + d0, swap, g0[i], g1[i]);
-            }
-        }
-        if (tid < C) {
-            cp_async_wait_all();
-            const uint32_t x = braw[tid];
-            bsm[tid] = (tid < len) ? __uint_as_float(beta_odd ? (x & 0xFFFF0000u) : (x << 16)) : 0.f;
-            if (c + 1 < nt) load_beta(t0 + C, (int)min((long)C, eos - t0 - C));
-        }
-
-        // ---- a1: gate, chunk-local cumsum (log2 units), sub-block carries
-        float G0[16], G1[16];
-        {
-            // per-token decay in log2 units (mode decided once, so the 32 evaluations interleave)
-            if (p.mode == 1) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    g0[i] = lbl2 * rcp_fast(1.0f + ex2_fast(-(expA0 * (g0[i] + dtb0)) * kLog2e));
-                    g1[i] = lbl2 * rcp_fast(1.0f + ex2_fast(-(expA1 * (g1[i] + dtb1)) * kLog2e));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    g0[i] *= kLog2e;
-                    g1[i] *= kLog2e;
-                }
-            }
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const bool valid = 16 * rq + i < len;
-                acc0 += valid ? g0[i] : 0.f;
-                acc1 += valid ? g1[i] : 0.f;
-                G0[i] = acc0;
-                G1[i] = acc1;
-            }
-            xch[rq * 128 + ch0] = acc0;
-            xch[rq * 128 + ch1] = acc1;
-        }
-        bar_sync(BAR_PREP, NGRP);
-        if (kGateTile && tid == 0 && c + 1 < nt && !sy.aborted()) {  // g tile read: prefetch chunk c + 1
-            mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
-            for (int cb = 0; cb < 2; ++cb)
-                tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)(t0 + C), sy.bar(B_GIN));
-        }
-        {
-            float c0 = 0.f, c1 = 0.f;
-            for (int q2 = 0; q2 < rq; ++q2) {
-                c0 += xch[q2 * 128 + ch0];
-                c1 += xch[q2 * 128 + ch1];
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) { G0[i] += c0; G1[i] += c1; }
-            gmid[rq * 128 + ch0] = G0[8];
-            gmid[rq * 128 + ch1] = G1[8];
-            if (rq == 3) { glast[ch0] = G0[15]; glast[ch1] = G1[15]; }
-        }
-        bar_sync(BAR_PREP, NGRP);
+        const float* bcur = bsm + (c & 1) * C;  // beta of the chunk (zero past the end)
 
         // ---- k and q of the own rows from the tiles the chain prefetched into the k 2^G /
         // s q 2^G hand-off buffers; every thread reads before any thread overwrites them.
-        // k 2^(Gl - G) and 2^Glast are overwritten below, so the chain's o / dH MMAs of the
-        // previous chunk (their readers) must be done as well.
+        // (The tiles arrive after the chain's Y / o MMAs of the previous chunk, the readers
+        // of k 2^G and s q 2^G; k 2^(Gl - G), 2^Glast and the q^2 sums are double buffers.)
+        // G of the own rows and channels, from the buffer the gate warps filled (the operand
+        // stores below overwrite it as well)
         uint32_t kr[16], qr[16];
+        float G0[16], G1[16];
         sy.group_wait(B_QKIN, c & 1, w == 0, BAR_PREP);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -381,9 +391,11 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             const uint32_t off = tile_off(16 * rq + i);
             kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
             qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
+            const float2 gv = *reinterpret_cast<const float2*>(Gs + (16 * rq + i) * KD + d0);
+            G0[i] = swap ? gv.y : gv.x;
+            G1[i] = swap ? gv.x : gv.y;
         }
-        if (c > 0) sy.group_wait(B_OHDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
-        else       bar_sync(BAR_PREP, NGRP);
+        bar_sync(BAR_PREP, NGRP);
 
         // ---- deferred q l2norm (attention-gym PR #345): the sums of q^2 of the own rows over
         // this warp's 64 channels; the chain scales each output row once the row is complete
@@ -416,6 +428,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // ---- operands: channel-major [128 ch][rows] tiles, one 16-byte chunk (8 rows) of
         // each of the two own channels per store
         {
+            const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
             const float gm0 = G0[8], gm1 = G1[8];
             const float gl0 = glast[ch0], gl1 = glast[ch1];
             const float P0 = ex2_fast(gm0), P1 = ex2_fast(gm1);              // 2^G at the midpoint
@@ -475,8 +488,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
                     st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
                     st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
-                    st_s128(sb + OFF_KD + r0, kd0[0], kd0[1], kd0[2], kd0[3]);
-                    st_s128(sb + OFF_KD + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
+                    st_s128(kd_buf + r0, kd0[0], kd0[1], kd0[2], kd0[3]);
+                    st_s128(kd_buf + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
                 }
                 // score columns, channel-major [128 ch][n] in groups of 64 columns: sub-block
                 // bi >= rq sees row r as column n = sb_off(bi) + r with anchor m_bi:
@@ -520,7 +533,13 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             umma_commit(sy.bar(B_SCORE));
             mbar_arrive(sy.bar(B_KQFULL));
         }
-        sy.group_wait(B_SCORE, c & 1, w == 0, BAR_PREP);
+        // Aqk is overwritten below: the chain's o MMAs of the previous chunk (its readers)
+        // must be done as well
+        if (w == 0) {
+            sy.wait(B_SCORE, c & 1);
+            if (c > 0) sy.wait(B_OHDONE, (uint32_t)((c - 1) & 1));
+        }
+        bar_sync(BAR_PREP, NGRP);
         tc_fence_after();
 
         // ---- read the scores, all eight warps: warps w and w + 4 share the TMEM lanes of
@@ -537,7 +556,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             // the piece of both (warp-collective loads), every lane keeps its own
             const int bmin = 2 * (lq & 1);
             const bool own_a = bi == bmin;
-            const float b_i = 0.5f * bsm[i];  // the k-row scores are doubled
+            const float b_i = 0.5f * bcur[i];  // the k-row scores are doubled
             const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16) + TM_S;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
@@ -582,145 +601,150 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         if (c > 0) sy.group_wait(B_VNDONE, (uint32_t)((c - 1) & 1), w == 0, BAR_PREP);
         else       bar_sync(BAR_PREP, NGRP);
 
-        // ---- a3: T = (I + Akk)^-1, each block written as fp32 (for the later blocks) and
-        // straight into the bf16 T diag(beta) hand-off (K-major [64][64]; its strictly upper
-        // blocks were zeroed once).  Diagonal 16 x 16 blocks by forward substitution, one
-        // thread per column (warps 0-1), right-looking: once x[j] is final, column j of the
-        // block (contiguous in the stored transpose, read 4 entries at a time) updates the
-        // later rows; entries above the thread's column stay exactly zero.
-        if (w < 2) {
-            const int b = 2 * w + (l >> 4), cc = l & 15;
-            float x[16];
+        // ---- a3 on warps 0-3 (warps 4-7 run a1 of the next chunk meanwhile): T = (I + Akk)^-1,
+        // each block written as fp32 (for the later blocks) and straight into the bf16
+        // T diag(beta) hand-off (K-major [64][64]; its strictly upper blocks were zeroed once).
+        // Diagonal 16 x 16 blocks by forward substitution, one thread per column (warps 0-1),
+        // right-looking: once x[j] is final, column j of the block (contiguous in the stored
+        // transpose, read 4 entries at a time) updates the later rows; entries above the
+        // thread's column stay exactly zero.
+        if (w < 4) {
+            if (w < 2) {
+                const int b = 2 * w + (l >> 4), cc = l & 15;
+                float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+                for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < 15; ++j) {
-                const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
+                for (int j = 0; j < 15; ++j) {
+                    const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
 #pragma unroll
-                for (int m = (j + 1) / 4; m < 4; ++m) {
-                    const float4 a4 = col[m];
-                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int m = (j + 1) / 4; m < 4; ++m) {
+                        const float4 a4 = col[m];
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (4 * m + e > j) x[4 * m + e] = fmaf(-av[e], x[j], x[4 * m + e]);
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * m + e > j) x[4 * m + e] = fmaf(-av[e], x[j], x[4 * m + e]);
+                    }
                 }
-            }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
-            __syncwarp();
-            // row 16 b + cc of the block, its columns scaled by beta
-            const int i = 16 * b + cc;
-            uint32_t pk[8];
+                for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
+                __syncwarp();
+                // row 16 b + cc of the block, its columns scaled by beta
+                const int i = 16 * b + cc;
+                uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j0 = 16 * b + 2 * e;
-                pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
+                for (int e = 0; e < 8; ++e) {
+                    const int j0 = 16 * b + 2 * e;
+                    pk[e] = pack_bf16(Tf[i * LD + j0] * bcur[j0], Tf[i * LD + j0 + 1] * bcur[j0 + 1]);
+                }
+                st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
+                st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
             }
-            st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
-            st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
+            bar_sync(BAR_INV, 128);
+            // Off-diagonal blocks as a 2 x 2 recursion on 32 x 32 blocks, with m16n8k8 tf32 MMAs
+            // (fragments: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
+            //  c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]; g = lane / 4, t = lane % 4):
+            //  1. T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)                      (warps 0, 1)
+            //  2. X[r][c] = sum_{t=c..1} A[r][t] T[t][c]                  r = 2, 3; c = 0, 1 (warps 0-3)
+            //  3. T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]                                  (warps 0-3)
+            // Every finished block goes into the bf16 T diag(beta) hand-off; T10 and T32 also
+            // into the fp32 T for step 2 and 3.
+            {
+                const int gq = l >> 2, tq = l & 3;
+                // acc += A[r0.., kc0 .. kc0 + 8 nk) T[.., n0 .. n0 + 16), A read from its transpose
+                // (nk is 2 or 4; the loop is unrolled to the larger count so loads can run ahead)
+                auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        if (ks >= nk) break;
+                        const int kc = kc0 + 8 * ks;
+                        uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
+                                         to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
+                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
+                                         to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
+#pragma unroll
+                        for (int n8 = 0; n8 < 2; ++n8) {
+                            uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
+                                              to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
+                            mma_tf32_16x8x8(acc[n8], a, bb);
+                        }
+                    }
+                };
+                // acc += T[r0.., k0 .. k0 + 16) X, X a 16 x 16 block stored with row stride 24
+                auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int kc = k0 + 8 * ks;
+                        uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]),
+                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
+                                         to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
+                                         to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
+#pragma unroll
+                        for (int n8 = 0; n8 < 2; ++n8) {
+                            uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
+                                              to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
+                            mma_tf32_16x8x8(acc[n8], a, bb);
+                        }
+                    }
+                };
+                auto store_X = [&](float* X, const float (&acc)[2][4]) {
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
+                        X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
+                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
+                        X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
+                    }
+                };
+                // T[r0.., c0..] = -acc: the hand-off (times beta of the columns), optionally fp32 T
+                auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        const int j = c0 + 8 * n8 + 2 * tq;
+                        if (keep) {
+                            Tf[(r0 + gq) * LD + j] = -acc[n8][0];
+                            Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
+                            Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
+                            Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
+                        }
+                        const float b0 = -bcur[j], b1 = -bcur[j + 1];
+                        const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
+                        st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
+                        st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
+                    }
+                };
+                if (w < 2) {  // step 1
+                    const int r0 = 32 * w + 16, c0 = 32 * w;
+                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    prod_A_T(xa, r0, c0, 2, c0);
+                    float* X = Xs + w * (16 * 24);
+                    store_X(X, xa);
+                    __syncwarp();
+                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    prod_T_X(ta, r0, r0, X);
+                    store_T(r0, c0, ta, true);
+                }
+                bar_sync(BAR_INV, 128);
+                const int rb = 2 + (w >> 1), cb = w & 1;  // block (rb, cb) of warp w < 4
+                {  // step 2
+                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    prod_A_T(xa, 16 * rb, 16 * cb, 4 - 2 * cb, 16 * cb);
+                    store_X(Xs + w * (16 * 24), xa);
+                }
+                bar_sync(BAR_INV, 128);
+                {  // step 3
+                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int s = 2; s <= 3; ++s)
+                        if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
+                    store_T(16 * rb, 16 * cb, ta, false);
+                }
+                fence_proxy_async_smem();  // the hand-off is complete
+            }
+        } else if (c + 1 < nt) {
+            gate_chunk(c + 1);
         }
         bar_sync(BAR_PREP, NGRP);
-        // Off-diagonal blocks as a 2 x 2 recursion on 32 x 32 blocks, with m16n8k8 tf32 MMAs
-        // (fragments: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
-        //  c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]; g = lane / 4, t = lane % 4):
-        //  1. T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)                      (warps 0, 1)
-        //  2. X[r][c] = sum_{t=c..1} A[r][t] T[t][c]                  r = 2, 3; c = 0, 1 (warps 0-3)
-        //  3. T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]                                  (warps 0-3)
-        // Every finished block goes into the bf16 T diag(beta) hand-off; T10 and T32 also
-        // into the fp32 T for step 2 and 3.
-        {
-            const int gq = l >> 2, tq = l & 3;
-            // acc += A[r0.., kc0 .. kc0 + 8 nk) T[.., n0 .. n0 + 16), A read from its transpose
-            // (nk is 2 or 4; the loop is unrolled to the larger count so loads can run ahead)
-            auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    if (ks >= nk) break;
-                    const int kc = kc0 + 8 * ks;
-                    uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]),
-                                     to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
-                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
-                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
-#pragma unroll
-                    for (int n8 = 0; n8 < 2; ++n8) {
-                        uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
-                                          to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
-                        mma_tf32_16x8x8(acc[n8], a, bb);
-                    }
-                }
-            };
-            // acc += T[r0.., k0 .. k0 + 16) X, X a 16 x 16 block stored with row stride 24
-            auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int kc = k0 + 8 * ks;
-                    uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]),
-                                     to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
-                                     to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
-                                     to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
-#pragma unroll
-                    for (int n8 = 0; n8 < 2; ++n8) {
-                        uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
-                                          to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
-                        mma_tf32_16x8x8(acc[n8], a, bb);
-                    }
-                }
-            };
-            auto store_X = [&](float* X, const float (&acc)[2][4]) {
-#pragma unroll
-                for (int n8 = 0; n8 < 2; ++n8) {
-                    X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
-                    X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
-                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
-                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
-                }
-            };
-            // T[r0.., c0..] = -acc: the hand-off (times beta of the columns), optionally fp32 T
-            auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
-#pragma unroll
-                for (int n8 = 0; n8 < 2; ++n8) {
-                    const int j = c0 + 8 * n8 + 2 * tq;
-                    if (keep) {
-                        Tf[(r0 + gq) * LD + j] = -acc[n8][0];
-                        Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
-                        Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
-                        Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
-                    }
-                    const float b0 = -bsm[j], b1 = -bsm[j + 1];
-                    const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
-                    st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
-                    st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
-                }
-            };
-            if (w < 2) {  // step 1
-                const int r0 = 32 * w + 16, c0 = 32 * w;
-                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                prod_A_T(xa, r0, c0, 2, c0);
-                float* X = Xs + w * (16 * 24);
-                store_X(X, xa);
-                __syncwarp();
-                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                prod_T_X(ta, r0, r0, X);
-                store_T(r0, c0, ta, true);
-            }
-            bar_sync(BAR_PREP, NGRP);
-            const int rb = 2 + (w >> 1), cb = w & 1;  // block (rb, cb) of warp w < 4
-            if (w < 4) {  // step 2
-                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                prod_A_T(xa, 16 * rb, 16 * cb, 4 - 2 * cb, 16 * cb);
-                store_X(Xs + w * (16 * 24), xa);
-            }
-            bar_sync(BAR_PREP, NGRP);
-            if (w < 4) {  // step 3
-                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int s = 2; s <= 3; ++s)
-                    if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
-                store_T(16 * rb, 16 * cb, ta, false);
-            }
-            fence_proxy_async_smem();  // the hand-off is complete
-            bar_sync(BAR_PREP, NGRP);
-        }
         if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
     }
 }
@@ -741,19 +765,23 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     const float* gam = reinterpret_cast<const float*>(smem + OFF_GAM);
     const size_t st_off = ((size_t)n * H + h) * (size_t)KD * VD;
 
-    float hs[64];  // h^T[v][64 hch + j]
+    // The state h^T stays in TMEM (fp32, columns TM_H; the thread's lane is value channel
+    // vlane, its columns the key channels 64 hch .. + 63).  Its bf16 copy in the columns
+    // TM_VN + 32 hch .. is the A operand of the next chunk's Y / o MMAs.
+    // key channels 64 hch + 32 s .. + 31 of the thread's row: load / store fp32, store bf16
+    auto ld_h = [&](int s, float (&hv)[32]) {
+        tmem_ld16(tmem + lane_base + TM_H + 64 * hch + 32 * s, hv);
+        tmem_ld16(tmem + lane_base + TM_H + 64 * hch + 32 * s + 16, hv + 16);
+    };
+    auto st_h = [&](int s, const float (&hv)[32]) {
+        tmem_st16(tmem + lane_base + TM_H + 64 * hch + 32 * s, reinterpret_cast<const uint32_t*>(hv));
+        tmem_st16(tmem + lane_base + TM_H + 64 * hch + 32 * s + 16, reinterpret_cast<const uint32_t*>(hv) + 16);
+    };
+    auto st_hA = [&](int s, const float (&hv)[32]) {
+        uint32_t r[16];
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-        hs[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + j) * VD + vlane) : 0.f;
-
-    auto store_hA = [&]() {  // bf16 h^T into the TMEM A operand (columns TM_VN + 32 hch ..)
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            uint32_t r[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hs[32 * s + 2 * e], hs[32 * s + 2 * e + 1]);
-            tmem_st16(tmem + lane_base + TM_VN + 32 * hch + 16 * s, r);
-        }
+        for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hv[2 * e], hv[2 * e + 1]);
+        tmem_st16(tmem + lane_base + TM_VN + 32 * hch + 16 * s, r);
     };
 
     // q and k tiles of chunk c land in the k 2^G / s q 2^G buffers for the prep group
@@ -770,7 +798,15 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             tma_load_3d(sb + OFF_V + cb * 8192, tm_v, 64 * cb, h, (int)t, sy.bar(B_VFULL));
     };
     if (nt > 0) {
-        store_hA();
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            float hv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + 32 * s + j) * VD + vlane) : 0.f;
+            st_h(s, hv);
+            st_hA(s, hv);
+        }
         tmem_wait_st();
         if (ct == 0) {
             load_qk(bos);
@@ -813,6 +849,20 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 #pragma unroll
             for (int e = 0; e < 16; ++e) r[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
             tmem_st16(tmem + lane_base + TM_YA + 16 * hch, r);
+        }
+        // ---- h^T <- h^T Diag(2^Glast) while the prep group finishes the chunk (2^Glast came
+        // with the chunk's operands); the dH MMA below accumulates into it
+        {
+            const float* gm = gam + (c & 1) * 128 + 64 * hch;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                float hv[32];
+                ld_h(s, hv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hv[j] *= gm[32 * s + j];
+                st_h(s, hv);
+            }
             tmem_wait_st();
         }
         if (w == 8) {
@@ -870,40 +920,37 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         }
         tc_fence_before();
         bar_sync(BAR_CHAIN, NGRP);
-        // ---- o^T += v_new^T Aqk^T (hi*hi + lo*hi + hi*lo); dH^T = v_new^T kd (hi + lo)
+        // ---- o^T += v_new^T Aqk^T (hi*hi + lo*hi + hi*lo); h^T += v_new^T kd (hi + lo)
         if (ct == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_o = idesc_bf16(128, 64, 0, 0);
             const uint32_t id_h = idesc_bf16(128, 128, 0, 0);
+            const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t ah = tmem + TM_Y + 8 * kk, al = tmem + TM_Y + 32 + 8 * kk;
                 uint64_t boh = desc_at(umma_desc(sb + OFF_AQKH, 16, 1024), kk * 32);
                 uint64_t bol = desc_at(umma_desc(sb + OFF_AQKL, 16, 1024), kk * 32);
-                uint64_t bk = desc_at(umma_desc(sb + OFF_KD, 16, 1024), kk * 32);
+                uint64_t bk = desc_at(umma_desc(kd_buf, 16, 1024), kk * 32);
                 umma_bf16_ta(tmem + TM_O, ah, boh, id_o, 1);
                 umma_bf16_ta(tmem + TM_O, al, boh, id_o, 1);
                 umma_bf16_ta(tmem + TM_O, ah, bol, id_o, 1);
-                umma_bf16_ta(tmem + TM_DH, ah, bk, id_h, kk > 0);
-                umma_bf16_ta(tmem + TM_DH, al, bk, id_h, 1);
+                umma_bf16_ta(tmem + TM_H, ah, bk, id_h, 1);
+                umma_bf16_ta(tmem + TM_H, al, bk, id_h, 1);
             }
             umma_commit(sy.bar(B_OHDONE));
         }
         sy.group_wait(B_OHDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
-        // ---- h^T <- h^T Diag(2^Glast) + dH^T; bf16 h^T for the next chunk; o out
+        // ---- bf16 h^T for the next chunk; o out
         {
-            const float* gm = gam + (c & 1) * 128 + 64 * hch;
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-                float dh[32];
-                tmem_ld16(tmem + lane_base + TM_DH + 64 * hch + 32 * s, dh);
-                tmem_ld16(tmem + lane_base + TM_DH + 64 * hch + 32 * s + 16, dh + 16);
+                float hv[32];
+                ld_h(s, hv);
                 tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) hs[32 * s + j] = fmaf(gm[32 * s + j], hs[32 * s + j], dh[j]);
+                st_hA(s, hv);
             }
-            store_hA();
             float ov[32];
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM_O + 32 * hch + 16, ov + 16);
@@ -926,7 +973,19 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 
     if (p.hT && !sy.aborted()) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) p.hT[st_off + (size_t)(64 * hch + j) * VD + vlane] = hs[j];
+        for (int s = 0; s < 2; ++s) {
+            float hv[32];
+            if (nt > 0) {
+                ld_h(s, hv);
+                tmem_wait_ld();
+            } else {  // an empty sequence passes its state through
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + 32 * s + j) * VD + vlane) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p.hT[st_off + (size_t)(64 * hch + 32 * s + j) * VD + vlane] = hv[j];
+        }
     }
 }
 
