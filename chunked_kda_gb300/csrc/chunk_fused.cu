@@ -68,7 +68,7 @@ using namespace sm100;
 constexpr int C = 64, KD = 128, VD = 128;
 constexpr int NTHR = 512, NGRP = 256;            // two groups of 8 warps
 constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;  // named barriers of the groups
-constexpr uint32_t BAR_INV = 3, BAR_GATE = 4;    // prep warps 0-3 (inverse) / 4-7 (next gate)
+constexpr uint32_t BAR_INV = 3;                  // prep warps 0-3 (inverse)
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T          [chain]
@@ -92,7 +92,7 @@ constexpr uint32_t OFF_AQKH = 188416;  // hand-off: Aqk hi [64][64]
 constexpr uint32_t OFF_AQKL = 196608;  // hand-off: Aqk lo [64][64]
 constexpr uint32_t OFF_GAM = 204800;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
 constexpr uint32_t OFF_BETA = 205824;  // prep: beta fp32 [2 chunks][64]
-constexpr uint32_t OFF_GCARRY = 206336;  // prep: fp32 [128] gate sums of rows 0-31
+constexpr uint32_t OFF_GCARRY = 206336;  // chain: fp32 [3][128] gate sums of row quarters 0-2
 constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block midpoints
 constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
@@ -103,7 +103,7 @@ constexpr uint32_t SMEM_BYTES = 229376 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_GS, "layout");
 static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG, "layout");
-static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 128 * 4 <= OFF_GM, "layout");
+static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 3 * 128 * 4 <= OFF_GM, "layout");
 static_assert(OFF_QSS + 1024 <= OFF_KD1 && OFF_KD1 % 1024 == 0, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
@@ -111,7 +111,7 @@ constexpr int LD = 68;                 // fp32 row stride of the solve matrices 
 // mbarriers (each completes once per chunk, the v tiles once per two chunks)
 enum {
     B_VFULL = 0, B_QKIN, B_GIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
-    B_DRAIN0, B_DRAIN1, NBAR
+    B_DRAIN0, B_DRAIN1, B_GATE, NBAR
 };
 static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC, "mbarriers");
 
@@ -156,33 +156,12 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
                  : "memory");
 }
 
-// asynchronous 4-byte global -> shared copy that reads only the first `src_bytes` bytes
-// (the rest is zero-filled); both addresses 4-byte aligned
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
     return v;
 }
 
-template <typename GT>
-struct GatePair;
-template <>
-struct GatePair<__nv_bfloat16> {
-    // channels (d0, d0 + 1) at p, returned in the order (ch0, ch1) of the owning thread
-    static __device__ __forceinline__ void load(const __nv_bfloat16* p, int swap, float& a, float& b) {
-        uint32_t x = __ldg(reinterpret_cast<const unsigned int*>(p));
-        a = swap ? bf_hi(x) : bf_lo(x);
-        b = swap ? bf_lo(x) : bf_hi(x);
-    }
-};
-template <>
-struct GatePair<float> {
-    static __device__ __forceinline__ void load(const float* p, int swap, float& a, float& b) {
-        float2 x = __ldg(reinterpret_cast<const float2*>(p));
-        a = swap ? x.y : x.x;
-        b = swap ? x.x : x.y;
-    }
-};
 
 struct Params {
     const __nv_bfloat16* q;
@@ -223,13 +202,9 @@ struct Sync {
 };
 
 // ------------------------------------------------------------------ prep group
-template <typename GT>
 __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
-                                          const Sync& sy, const CUtensorMap* tm_g, int h, long bos,
-                                          long eos, int nt) {
-    constexpr bool kGateTile = std::is_same<GT, __nv_bfloat16>::value;  // g arrives by TMA
+                                          const Sync& sy, int h, long bos, long eos, int nt) {
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    const int H = p.H;
     float* gmid = reinterpret_cast<float*>(smem + OFF_GM);
     float* glast = reinterpret_cast<float*>(smem + OFF_GL);
     float* gam = reinterpret_cast<float*>(smem + OFF_GAM);
@@ -250,125 +225,17 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
     auto bf_0 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel0)); };
     auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel1)); };
-    const float lbl2 = p.lb * kLog2e;
     const float scale = rsqrtf((float)KD);
-    const GT* gptr = reinterpret_cast<const GT*>(p.g);
     const uint32_t sw_d0 = (uint32_t)((d0 & 63) >> 3), sw_b0 = (uint32_t)(d0 & 7) * 2;
     const float* Gs = reinterpret_cast<const float*>(smem + OFF_GS);
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
-
-    // ---- a1 of chunk cn, on warps 4-7: the per-token decay in log2 units and its
-    // chunk-local cumsum (rows past the end add zero), G into the shared [64][128] buffer,
-    // the sub-block midpoints and the last row into their arrays.  Gate thread t takes the
-    // key channels 2 (t % 64) and 2 (t % 64) + 1 over the rows 32 (t / 64) .. + 31: all its
-    // loads are issued at once, and the row half 1 adds the totals of row half 0 (one
-    // exchange).  Threads t < 64 also stage beta of row t (zero past the end) into the
-    // chunk's half of a double buffer.  Chunk 0 runs before the loop, chunk c + 1 while
-    // warps 0-3 invert chunk c's Akk, in a part of the score operand area that the inverse
-    // leaves free.
-    const int gt = tid - 128;                    // gate thread 0 .. 127
-    const int gcp = gt & 63, grh = gt >> 6;      // channel pair, row half
-    const int gc0 = 2 * gcp;                     // first channel of the pair
-    // safe gate: lb log2(e) sigmoid(z), z = exp(A_log) (g + dt_bias), as
-    // lbl2 / (1 + 2^(nA g + nAd)) with nA = -exp(A_log) log2(e), nAd = nA dt_bias
-    float nA0 = 0.f, nA1 = 0.f, nAd0 = 0.f, nAd1 = 0.f;
-    if (p.mode == 1 && w >= 4) {
-        nA0 = -expf(__ldg(p.A_log + h * KD + gc0)) * kLog2e;
-        nA1 = -expf(__ldg(p.A_log + h * KD + gc0 + 1)) * kLog2e;
-        if (p.dt_bias) {
-            nAd0 = nA0 * __ldg(p.dt_bias + h * KD + gc0);
-            nAd1 = nA1 * __ldg(p.dt_bias + h * KD + gc0 + 1);
-        }
-    }
-    float* gcarry = reinterpret_cast<float*>(smem + OFF_GCARRY);
-    // beta of row gt of a chunk, loaded one chunk ahead into a register (its global load
-    // then has a whole chunk to land)
-    auto beta_of = [&](int cn) -> float {
-        const long tc0 = bos + (long)cn * C;
-        return (gt < eos - tc0) ? __bfloat162float(p.beta[(size_t)(tc0 + gt) * H + h]) : 0.f;
-    };
-    float bet_next = (w >= 4 && gt < C && nt > 0) ? beta_of(0) : 0.f;
-    auto load_gtile = [&](long t) {
-        mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
-        for (int cb = 0; cb < 2; ++cb)
-            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)t, sy.bar(B_GIN));
-    };
-    auto gate_chunk = [&](int cn) {
-        const long tc0 = bos + (long)cn * C;
-        const int lenc = (int)min((long)C, eos - tc0);
-        float* gs = reinterpret_cast<float*>(smem + OFF_GS);
-        if (gt < C) {
-            bsm[(cn & 1) * C + gt] = bet_next;
-            bet_next = (cn + 1 < nt) ? beta_of(cn + 1) : 0.f;
-        }
-        if constexpr (kGateTile) {
-            if (w == 4) sy.wait(B_GIN, (uint32_t)(cn & 1));
-            bar_sync(BAR_GATE, 128);
-        }
-        const int r0 = 32 * grh;
-        float a0[32], a1[32];
-        if constexpr (kGateTile) {
-            // the pair's word in row r of the token-major [64][128] tile (two 64-channel blocks)
-            const uint32_t base = sb + OFF_GT + (uint32_t)(gc0 >> 6) * 8192u + (uint32_t)(gc0 & 6) * 2u;
-            const uint32_t chunk = (uint32_t)((gc0 & 63) >> 3);
-            uint32_t x[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = ld_s32(base + sw128((uint32_t)(r0 + i), chunk));
-#pragma unroll
-            for (int i = 0; i < 32; ++i) { a0[i] = bf_lo(x[i]); a1[i] = bf_hi(x[i]); }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float2 v2 = __ldg(reinterpret_cast<const float2*>(
-                    gptr + ((size_t)(tc0 + min(r0 + i, lenc - 1)) * H + h) * KD + gc0));
-                a0[i] = v2.x;
-                a1[i] = v2.y;
-            }
-        }
-        float m = kLog2e;  // per-token factor into log2 units
-        if (p.mode == 1) {
-            m = lbl2;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                a0[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0[i], nAd0)));
-                a1[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1[i], nAd1)));
-            }
-        }
-        // rows past the end add zero (selected, so that NaN padding there does not spread)
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const bool valid = r0 + i < lenc;
-            acc0 = fmaf(m, valid ? a0[i] : 0.f, acc0);
-            acc1 = fmaf(m, valid ? a1[i] : 0.f, acc1);
-            a0[i] = acc0;
-            a1[i] = acc1;
-        }
-        if (grh == 0) { gcarry[gc0] = acc0; gcarry[gc0 + 1] = acc1; }
-        bar_sync(BAR_GATE, 128);  // the row half 0 totals are out; every thread read the tile
-        if (kGateTile && tid == 128 && cn + 1 < nt && !sy.aborted()) load_gtile(tc0 + C);
-        float cy0 = 0.f, cy1 = 0.f;
-        if (grh == 1) { cy0 = gcarry[gc0]; cy1 = gcarry[gc0 + 1]; }
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<float2*>(gs + (r0 + i) * KD + gc0) = make_float2(a0[i] + cy0, a1[i] + cy1);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            *reinterpret_cast<float2*>(gmid + (2 * grh + j) * KD + gc0) =
-                make_float2(a0[16 * j + 8] + cy0, a1[16 * j + 8] + cy1);
-        }
-        if (grh == 1) *reinterpret_cast<float2*>(glast + gc0) = make_float2(acc0 + cy0, acc1 + cy1);
-    };
-    if (kGateTile && tid == 128 && nt > 0) load_gtile(bos);
 
     // the strictly upper 16 x 16 blocks of T diag(beta) are zero in every chunk
     for (int idx = tid; idx < 64 * 8; idx += NGRP) {
         const int i = idx >> 3, c8 = idx & 7;
         if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
     }
-    if (w >= 4 && nt > 0) gate_chunk(0);
-    bar_sync(BAR_PREP, NGRP);
 
     for (int c = 0; c < nt; ++c) {
         const long t0 = bos + (long)c * C;
@@ -384,7 +251,11 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // stores below overwrite it as well)
         uint32_t kr[16], qr[16];
         float G0[16], G1[16];
-        sy.group_wait(B_QKIN, c & 1, w == 0, BAR_PREP);
+        if (w == 0) {
+            sy.wait(B_QKIN, c & 1);
+            sy.wait(B_GATE, c & 1);
+        }
+        bar_sync(BAR_PREP, NGRP);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const bool valid = 16 * rq + i < len;
@@ -447,6 +318,15 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             for (int half = 0; half < 2; ++half) {
                 const uint32_t ch = 2 * rq + half;
                 const uint32_t r0 = sw128(ch0, ch), r1 = sw128(ch1, ch);
+                float Gh0[8], Gh1[8];
+                uint32_t krh[8], qrh[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    Gh0[i] = half ? G0[8 + i] : G0[i];
+                    Gh1[i] = half ? G1[8 + i] : G1[i];
+                    krh[i] = half ? kr[8 + i] : kr[i];
+                    qrh[i] = half ? qr[8 + i] : qr[i];
+                }
                 float kf0[8], kf1[8];  // k 2^(G_m(rq) - G) of the 8 rows
                 {
                     uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lq0[4], lq1[4];
@@ -456,14 +336,14 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         float ke0[2], ke1[2], qe0[2], qe1[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int i = 8 * half + 2 * pr + u;
-                            const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
-                            const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
-                            const float kv0 = bf_0(kr[i]), kv1 = bf_1(kr[i]);
+                            const int i = 2 * pr + u;
+                            const float e0 = ex2_fast(Gh0[i] - gm0), e1 = ex2_fast(Gh1[i] - gm1);
+                            const float f0 = ex2_fast(gm0 - Gh0[i]), f1 = ex2_fast(gm1 - Gh1[i]);
+                            const float kv0 = bf_0(krh[i]), kv1 = bf_1(krh[i]);
                             ke0[u] = kv0 * e0;
                             ke1[u] = kv1 * e1;
-                            qe0[u] = scale * bf_0(qr[i]) * e0;
-                            qe1[u] = scale * bf_1(qr[i]) * e1;
+                            qe0[u] = scale * bf_0(qrh[i]) * e0;
+                            qe1[u] = scale * bf_1(qrh[i]) * e1;
                             kf0[2 * pr + u] = kv0 * f0;
                             kf1[2 * pr + u] = kv1 * f1;
                         }
@@ -558,7 +438,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             const bool own_a = bi == bmin;
             const float b_i = 0.5f * bcur[i];  // the k-row scores are doubled
             const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16) + TM_S;
-#pragma unroll
+#pragma unroll 1
             for (int tt = 0; tt < 2; ++tt) {
                 const int t = part + 2 * tt;  // columns 16 t .. 16 t + 15 of the row
                 float va[16], vb[16];
@@ -741,8 +621,6 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 }
                 fence_proxy_async_smem();  // the hand-off is complete
             }
-        } else if (c + 1 < nt) {
-            gate_chunk(c + 1);
         }
         bar_sync(BAR_PREP, NGRP);
         if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
@@ -750,11 +628,12 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 }
 
 // ------------------------------------------------------------------ chain group
-template <typename OT>
+template <typename GT, typename OT>
 __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
                                            const Sync& sy, const CUtensorMap* tm_v,
-                                           const CUtensorMap* tm_q, const CUtensorMap* tm_k, int n,
-                                           int h, long bos, long eos, int nt) {
+                                           const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                           const CUtensorMap* tm_g, int n, int h, long bos, long eos,
+                                           int nt) {
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int ct = tid - NGRP;          // 0 .. 255
     const int lg = w & 3;               // TMEM lane group
@@ -784,6 +663,123 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         tmem_st16(tmem + lane_base + TM_VN + 32 * hch + 16 * s, r);
     };
 
+
+    // ---- a1 of chunk cn: the per-token decay in log2 units and its chunk-local cumsum
+    // (rows past the end add zero) into the shared G [64][128] that the prep group reads,
+    // the sub-block midpoints and the last row into their arrays, beta into the chunk's
+    // half of a double buffer.  Thread ct takes the key channels 2 (ct % 64), 2 (ct % 64)
+    // + 1 over the row quarter ct / 64 (all its loads issued at once); the quarters add
+    // the totals of the ones before them (one exchange).  Chunk 0 runs before the loop,
+    // chunk c + 1 while the chain waits for the prep group to finish chunk c, in a part of
+    // the score operand area that the prep group's inverse leaves free.
+    constexpr bool kGateTile = std::is_same<GT, __nv_bfloat16>::value;  // g arrives by TMA
+    const GT* gptr = reinterpret_cast<const GT*>(p.g);
+    const int gq = ct >> 6, gc0 = 2 * (ct & 63);  // row quarter, first channel of the pair
+    const float lbl2 = p.lb * kLog2e;
+    // safe gate: lb log2(e) sigmoid(z), z = exp(A_log) (g + dt_bias), as
+    // lbl2 / (1 + 2^(nA g + nAd)) with nA = -exp(A_log) log2(e), nAd = nA dt_bias
+    float nA0 = 0.f, nA1 = 0.f, nAd0 = 0.f, nAd1 = 0.f;
+    if (p.mode == 1) {
+        nA0 = -expf(__ldg(p.A_log + h * KD + gc0)) * kLog2e;
+        nA1 = -expf(__ldg(p.A_log + h * KD + gc0 + 1)) * kLog2e;
+        if (p.dt_bias) {
+            nAd0 = nA0 * __ldg(p.dt_bias + h * KD + gc0);
+            nAd1 = nA1 * __ldg(p.dt_bias + h * KD + gc0 + 1);
+        }
+    }
+    float* gs = reinterpret_cast<float*>(smem + OFF_GS);
+    float* gcarry = reinterpret_cast<float*>(smem + OFF_GCARRY);
+    float* gmid = reinterpret_cast<float*>(smem + OFF_GM);
+    float* glast = reinterpret_cast<float*>(smem + OFF_GL);
+    float* bsm = reinterpret_cast<float*>(smem + OFF_BETA);
+    // beta of row ct of a chunk, loaded one chunk ahead into a register
+    auto beta_of = [&](int cn) -> float {
+        const long tc0 = bos + (long)cn * C;
+        return (ct < eos - tc0) ? __bfloat162float(p.beta[(size_t)(tc0 + ct) * H + h]) : 0.f;
+    };
+    float bet_next = (ct < C && nt > 0) ? beta_of(0) : 0.f;
+    auto load_gtile = [&](long t) {
+        mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
+        for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)t, sy.bar(B_GIN));
+    };
+    // score_chunk >= 0: the score MMA of that chunk must have read its operands first
+    auto gate_chunk = [&](int cn, int score_chunk) {
+        const long tc0 = bos + (long)cn * C;
+        const int lenc = (int)min((long)C, eos - tc0);
+        if (w == 8) {
+            if (score_chunk >= 0) sy.wait(B_SCORE, (uint32_t)(score_chunk & 1));
+            if (kGateTile) sy.wait(B_GIN, (uint32_t)(cn & 1));
+        }
+        bar_sync(BAR_CHAIN, NGRP);
+        // compact (rolled) loops: this runs once per chunk next to the prep group's code, and
+        // instruction fetch is a shared limit of the SM
+        const int r0 = 16 * gq;
+        const uint32_t base = sb + OFF_GT + (uint32_t)(gc0 >> 6) * 8192u + (uint32_t)(gc0 & 6) * 2u;
+        const uint32_t chunk = (uint32_t)((gc0 & 63) >> 3);
+        const float m = (p.mode == 1) ? lbl2 : kLog2e;  // per-token factor into log2 units
+        float acc0 = 0.f, acc1 = 0.f;
+        float2* grow = reinterpret_cast<float2*>(gs + r0 * KD + gc0);
+#pragma unroll 1
+        for (int i0 = 0; i0 < 16; i0 += 4) {
+            float a0[4], a1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if constexpr (kGateTile) {
+                    // the pair's word in row r of the token-major [64][128] tile
+                    const uint32_t x = ld_s32(base + sw128((uint32_t)(r0 + i0 + i), chunk));
+                    a0[i] = bf_lo(x);
+                    a1[i] = bf_hi(x);
+                } else {
+                    const float2 v2 = __ldg(reinterpret_cast<const float2*>(
+                        gptr + ((size_t)(tc0 + min(r0 + i0 + i, lenc - 1)) * H + h) * KD + gc0));
+                    a0[i] = v2.x;
+                    a1[i] = v2.y;
+                }
+            }
+            if (p.mode == 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a0[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0[i], nAd0)));
+                    a1[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1[i], nAd1)));
+                }
+            }
+            // rows past the end add zero (selected, so that NaN padding there does not spread);
+            // the partial sums of the quarter are stored now and carried below
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool valid = r0 + i0 + i < lenc;
+                acc0 = fmaf(m, valid ? a0[i] : 0.f, acc0);
+                acc1 = fmaf(m, valid ? a1[i] : 0.f, acc1);
+                grow[(i0 + i) * (KD / 2)] = make_float2(acc0, acc1);
+            }
+        }
+        if (gq < 3) *reinterpret_cast<float2*>(gcarry + gq * KD + gc0) = make_float2(acc0, acc1);
+        bar_sync(BAR_CHAIN, NGRP);  // quarter totals out; every thread has read the tile
+        if (kGateTile && ct == 0 && cn + 1 < nt && !sy.aborted()) load_gtile(tc0 + C);
+        float cy0 = 0.f, cy1 = 0.f;
+        for (int q = 0; q < gq; ++q) {
+            const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * KD + gc0);
+            cy0 += t2.x;
+            cy1 += t2.y;
+        }
+        // add the carry to the stored partial sums (the thread's own values)
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const float2 v = grow[i * (KD / 2)];
+            const float2 g2 = make_float2(v.x + cy0, v.y + cy1);
+            grow[i * (KD / 2)] = g2;
+            if (i == 8) *reinterpret_cast<float2*>(gmid + gq * KD + gc0) = g2;
+        }
+        if (gq == 3) *reinterpret_cast<float2*>(glast + gc0) = make_float2(acc0 + cy0, acc1 + cy1);
+        if (ct < C) {
+            bsm[(cn & 1) * C + ct] = bet_next;
+            bet_next = (cn + 1 < nt) ? beta_of(cn + 1) : 0.f;
+        }
+        bar_sync(BAR_CHAIN, NGRP);  // G, its midpoints, last row and beta are out
+        if (ct == 0) mbar_arrive(sy.bar(B_GATE));
+    };
+
     // q and k tiles of chunk c land in the k 2^G / s q 2^G buffers for the prep group
     auto load_qk = [&](long t) {
         mbar_arrive_expect_tx(sy.bar(B_QKIN), 32768);
@@ -809,11 +805,12 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         }
         tmem_wait_st();
         if (ct == 0) {
+            if (kGateTile) load_gtile(bos);
             load_qk(bos);
             load_v(bos);
         }
         tc_fence_before();
-        bar_sync(BAR_CHAIN, NGRP);
+        gate_chunk(0, -1);
     }
 
     for (int c = 0; c < nt; ++c) {
@@ -865,6 +862,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             }
             tmem_wait_st();
         }
+        if (c + 1 < nt) gate_chunk(c + 1, c);
         if (w == 8) {
             sy.wait(B_RESTFULL, c & 1);
             if (len < C) sy.wait(B_VFULL, c & 1);
@@ -960,11 +958,12 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ov[j] *= rsqrtf(qss[j] + qss[64 + j] + kQNormEps);
             }
-            OT* orow = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * VD + vlane;
-            const int ostride = H * VD, nvalid = len - 32 * hch;
+            OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * VD + vlane;
+            const size_t ostride = (size_t)H * VD;
+            const int nvalid = len - 32 * hch;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j < nvalid) orow[j * ostride] = to_out<OT>(ov[j]);
+            for (int j = 0; j < 32; ++j, op += ostride)
+                if (j < nvalid) *op = to_out<OT>(ov[j]);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -1023,8 +1022,8 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (w < 8) prep_loop<GT>(p, sb, smem, tmem, sy, &tm_g, h, bos, eos, nt);
-    else       chain_loop<OT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, n, h, bos, eos, nt);
+    if (w < 8) prep_loop(p, sb, smem, tmem, sy, h, bos, eos, nt);
+    else       chain_loop<GT, OT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, &tm_g, n, h, bos, eos, nt);
 
     // Every MMA was waited for, unless a wait gave up: then let the ones in flight finish.
     if (sy.aborted() && (tid == 0 || tid == NGRP)) {
