@@ -494,17 +494,27 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 float x[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < 15; ++j) {
+                // the columns are loaded kPre steps ahead, so a step waits only for x[j]
+                constexpr int kPre = 3;
+                float4 cbuf[kPre][4];
+                auto load_col = [&](int j, float4 (&dst)[4]) {
                     const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
 #pragma unroll
+                    for (int m = (j + 1) / 4; m < 4; ++m) dst[m] = col[m];
+                };
+#pragma unroll
+                for (int j = 0; j < kPre; ++j) load_col(j, cbuf[j]);
+#pragma unroll
+                for (int j = 0; j < 15; ++j) {
+                    float4 (&cj)[4] = cbuf[j % kPre];
+#pragma unroll
                     for (int m = (j + 1) / 4; m < 4; ++m) {
-                        const float4 a4 = col[m];
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const float av[4] = {cj[m].x, cj[m].y, cj[m].z, cj[m].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (4 * m + e > j) x[4 * m + e] = fmaf(-av[e], x[j], x[4 * m + e]);
                     }
+                    if (j + kPre < 15) load_col(j + kPre, cbuf[j % kPre]);
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
@@ -614,7 +624,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 bar_sync(BAR_INV, 128);
                 {  // step 3
                     float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
+#pragma unroll 1
                     for (int s = 2; s <= 3; ++s)
                         if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
                     store_T(16 * rb, 16 * cb, ta, false);
