@@ -629,9 +629,11 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cb) * (16 * 24));
                     store_T(16 * rb, 16 * cb, ta, false);
                 }
-                fence_proxy_async_smem();  // the hand-off is complete
             }
         }
+        // every writer of the hand-off (T diag(beta) by warps 0-3, Aqk by the readback warps)
+        // orders its stores before the chain's MMAs read them
+        fence_proxy_async_smem();
         bar_sync(BAR_PREP, NGRP);
         if (tid == 0) mbar_arrive(sy.bar(B_RESTFULL));
     }
