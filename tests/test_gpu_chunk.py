@@ -97,6 +97,34 @@ def test_gate_extremes(lb, g_std):
     compare(w, o, st)
 
 
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+@pytest.mark.parametrize("T", [64, 150])
+def test_float32_gate_with_bf16_inputs(mode, T):
+    """bf16 q, k, v, beta with a float32 gate: the fused kernel reads g from global memory
+    instead of a bf16 TMA tile.  A float32 gate holding the bf16 gate's values gives the
+    same activations, so the results are bitwise those of the bf16-gate call (and match
+    the oracle)."""
+    w = workloads.make_dense("t", 2, T, 2, 128, 128, 64, torch.bfloat16, 23, state_std=0.05,
+                             mode=mode)
+    o16, st16 = run_gpu(w)
+    w.g = w.g.float()
+    o32, st32 = run_gpu(w)
+    assert torch.equal(o32, o16) and torch.equal(st32, st16)
+    compare(w, o32, st32)
+
+
+def test_float32_gate_varlen():
+    cap = sum([0, 37, 64, 1, 0, 130]) + 23
+    w = workloads.make_varlen("t", [0, 37, 64, 1, 0, 130], cap, 2, 128, 128, 64, torch.bfloat16,
+                              43, mode=workloads.GATE_SAFE)
+    o16, st16 = run_gpu(w)
+    w.g = w.g.float()
+    o32, st32 = run_gpu(w)
+    end = int(w.cu_seqlens[-1])
+    assert torch.equal(o32[:, :end], o16[:, :end]) and torch.equal(st32, st16)
+    compare(w, o32, st32)
+
+
 VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
 
 
