@@ -48,8 +48,8 @@ def algorithmic_flops_per_head_token(K, V, C):
 # 152-head case
 # (311,296 head-tokens) scaled by head-tokens to 1,048,576.  Reported only while the source is
 # unchanged; a changed kernel reports null until it is captured again.
-FUSED_TRAFFIC = {"source_sha256": "3dd2b1d3eb112387", "workload": "dense_bf16_b4_t4096_h64_d128",
-                 "bytes": (324.36e6 + 62.19e6) * 1048576 / 311296}
+FUSED_TRAFFIC = {"source_sha256": "da0a2762a88074cd", "workload": "dense_bf16_b4_t4096_h64_d128",
+                 "bytes": (324.16e6 + 62.22e6) * 1048576 / 311296}
 
 
 def kernel_code_digest(path):
@@ -263,7 +263,7 @@ def run_ours(args, world, rank, local):
     w = workloads.make(args.workload, device=dev)
     B, T, H, K, V, C = w.B, w.T, w.H, w.K, w.V, w.chunk_size
     stream = torch.cuda.current_stream()
-    o = torch.empty((B, T, H, V), device=dev, dtype=torch.bfloat16)
+    o = torch.empty((B, T, H, V), device=dev, dtype=w.q.dtype)  # o in the dtype of q, k, v
     n_ws = 0 if w.cu_seqlens is None else w.n_seqs
     ws_bytes = kda.kda_chunk_workspace_bytes(w.q.dtype, B, T, H, K, V, C, n_ws, w.mode)
     ws = torch.empty(max(ws_bytes, 1), device=dev, dtype=torch.uint8)
@@ -302,7 +302,8 @@ def run_ours(args, world, rank, local):
         sampler.stop()
         if rank == 0:
             state_bytes = 0 if w.initial_state is None else 2 * w.initial_state.numel() * 4
-            nb = algorithmic_bytes_per_head_token(K, V) * head_tokens + state_bytes
+            nb = (algorithmic_bytes_per_head_token(K, V, w.q.element_size(), w.g.element_size())
+                  * head_tokens + state_bytes)
             print(json.dumps({"workload": args.workload, "ms_per_step": ms_per_step,
                               "head_tokens_per_s": units_all / t_max,
                               "path": "fused" if launches_per_chunk_call(w.q.dtype, K, V, C) == 1

@@ -1000,7 +1000,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     }
 }
 
-template <typename GT, typename OT>
+template <typename GT, typename OT, bool kHeadsFastest>
 __global__ void __launch_bounds__(NTHR, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -1013,12 +1013,19 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     Sync sy{sb + OFF_BAR, misc + 1};
 
     const int tid = threadIdx.x, w = tid >> 5;
-    const int h = blockIdx.y, n = blockIdx.x;
+
+    // Grid (sequences, heads), or (heads, sequences) for packed inputs: launched x fastest,
+    // all heads of a packed sequence then go out together, which keeps the long sequences of
+    // a mixed-length batch from piling up in the last wave (measured 0.44 -> 0.36 ms on 16
+    // sequences of 1-2048 tokens, 32 heads); dense batches measure faster with the
+    // sequences fastest.  (Both indices stay block-index registers: a sequence index taken
+    // from a ranking in shared memory cost more in register spills than it saved.)
+    const int n = kHeadsFastest ? blockIdx.y : blockIdx.x;
+    const int h = kHeadsFastest ? blockIdx.x : blockIdx.y;
     long bos, eos;
     if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
     else      { bos = (long)n * p.T; eos = bos + p.T; }
     const int nt = (int)((eos - bos + C - 1) / C);
-
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
         fence_mbar_init();
@@ -1095,10 +1102,12 @@ template <typename GT, typename OT>
 static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mg, const fused::Params& p) {
     using namespace fused;
-    auto kern = chunk_fused_kernel<GT, OT>;
+    const bool packed = a.cu != nullptr;
+    auto kern = packed ? chunk_fused_kernel<GT, OT, true> : chunk_fused_kernel<GT, OT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(a.N, a.H), NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
+    const dim3 grid = packed ? dim3(a.H, a.N) : dim3(a.N, a.H);
+    kern<<<grid, NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
 }
 

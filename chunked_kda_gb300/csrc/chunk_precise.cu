@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(C) solve_kernel(const float* __restrict__ Akk,
     for (int i = 0; i < len; ++i) Tm[((size_t)(t0 + i) * H + h) * C + col] = X[i][col];
 }
 
-// a4: w = T (beta k 2^G) [C,K], u = T (beta v) [C,V]; one thread per output column
+// a4: w = T (beta k 2^G) [C,K], u = T (beta v) [C,V]; one thread per output column, four
+// rows at a time (four independent sums; T read as float4, broadcast to the warp)
 template <typename InT, int C>
 __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
                                                  const InT* __restrict__ v,
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
                                                  const float* __restrict__ Tm, ChunkMap cm, int H,
                                                  int hr, int K, int V, float* __restrict__ w,
                                                  float* __restrict__ u) {
-    __shared__ float Ts[C][C];
+    __shared__ __align__(16) float Ts[C][C];
     __shared__ float bs[C];
     int n, t0, len, bos, eos;
     if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
@@ -173,16 +174,30 @@ __global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
             }
             x[j] = val;
         }
-        // T is unit lower triangular and stored with zeros above the diagonal, so the
-        // full row product equals the causal one; x stays in registers (static indices)
+        // T is unit lower triangular and stored with zeros above the diagonal (and in the
+        // rows past the end), so the full row product equals the causal one; x stays in
+        // registers (static indices)
 #pragma unroll 1
-        for (int i = 0; i < len; ++i) {
-            float acc = 0.f;
+        for (int i0 = 0; i0 < len; i0 += 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < C; ++j) acc = fmaf(Ts[i][j], x[j], acc);
-            {
-                if (isk) w[((size_t)(t0 + i) * H + h) * K + col] = acc;
-                else u[((size_t)(t0 + i) * H + h) * V + (col - K)] = acc;
+            for (int j = 0; j < C; j += 4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(&Ts[min(i0 + r, C - 1)][j]);
+                    acc[r] = fmaf(t4.x, x[j], acc[r]);
+                    acc[r] = fmaf(t4.y, x[j + 1], acc[r]);
+                    acc[r] = fmaf(t4.z, x[j + 2], acc[r]);
+                    acc[r] = fmaf(t4.w, x[j + 3], acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r;
+                if (i < len) {
+                    if (isk) w[((size_t)(t0 + i) * H + h) * K + col] = acc[r];
+                    else u[((size_t)(t0 + i) * H + h) * V + (col - K)] = acc[r];
+                }
             }
         }
     }
@@ -309,7 +324,8 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
     }
 }
 
-// a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows.  With
+// a6: o = s (q 2^G) h_c + Aqk v_new; one thread per value column, all C rows (the q 2^G and
+// Aqk tiles read as float4, broadcast to the warp, four channels / columns per step).  With
 // qnorm, row i is finally scaled by 1 / sqrt(|q_i|^2 + eps): every q-dependent term of the
 // row is linear in q_i (attention-gym PR #345, deferred q l2norm).
 template <typename InT, typename OutT, int C>
@@ -320,8 +336,8 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
                                                   const float* __restrict__ vn, ChunkMap cm,
                                                   int H, int hr, int K, int V, int qnorm,
                                                   OutT* __restrict__ o) {
-    __shared__ float qg[C][DT + 1];
-    __shared__ float As[C][C + 1];
+    __shared__ __align__(16) float qg[C][DT];
+    __shared__ __align__(16) float As[C][C];
     __shared__ float rs[C];
     int n, t0, len, bos, eos;
     if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
@@ -358,17 +374,35 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
             qg[i][dd] = val;
         }
         __syncthreads();
-        for (int dd = 0; dd < DT; ++dd) {
-            float hv = hc[hoff + (size_t)(d0 + dd) * V + vcol];
+        for (int dd = 0; dd < DT; dd += 4) {
+            float hv[4];
 #pragma unroll
-            for (int i = 0; i < C; ++i) acc[i] = fmaf(qg[i][dd], hv, acc[i]);
+            for (int e = 0; e < 4; ++e) hv[e] = hc[hoff + (size_t)(d0 + dd + e) * V + vcol];
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                const float4 g4 = *reinterpret_cast<const float4*>(&qg[i][dd]);
+                acc[i] = fmaf(g4.x, hv[0], acc[i]);
+                acc[i] = fmaf(g4.y, hv[1], acc[i]);
+                acc[i] = fmaf(g4.z, hv[2], acc[i]);
+                acc[i] = fmaf(g4.w, hv[3], acc[i]);
+            }
         }
     }
     __syncthreads();
-    for (int j = 0; j < len; ++j) {
-        float vj = vn[((size_t)(t0 + j) * H + h) * V + vcol];
+    // Aqk is zero above the diagonal and in the rows past the end; v_new rows past the end
+    // are not read (they may hold anything)
+    for (int j = 0; j < len; j += 4) {
+        float vj[4];
 #pragma unroll
-        for (int i = 0; i < C; ++i) acc[i] = fmaf(As[i][j], vj, acc[i]);
+        for (int e = 0; e < 4; ++e) vj[e] = (j + e < len) ? vn[((size_t)(t0 + j + e) * H + h) * V + vcol] : 0.f;
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&As[i][j]);
+            acc[i] = fmaf(a4.x, vj[0], acc[i]);
+            acc[i] = fmaf(a4.y, vj[1], acc[i]);
+            acc[i] = fmaf(a4.z, vj[2], acc[i]);
+            acc[i] = fmaf(a4.w, vj[3], acc[i]);
+        }
     }
 #pragma unroll
     for (int i = 0; i < C; ++i)
