@@ -118,6 +118,104 @@ __global__ void __launch_bounds__(256) scores_kernel(const InT* __restrict__ q,
     }
 }
 
+// a2 for the safe gate, whose per-token decay is bounded (lb >= -5: at most 5 / ln 2 in log2
+// units per token): the pairwise factor 2^(G_i - G_j) split at the midpoint m of row i's
+// 16-row sub-block, as in the fused kernel (Helion PR #3290, "chunk_fwd_A_diag_anchored"):
+// rows k_i 2^(G_i - G_m), q_i 2^(G_i - G_m) (|exponent| <= 16 * 5 / ln 2), columns
+// k_j 2^(G_m - G_j) per sub-block anchor; then plain products.  Thread: column j, rows
+// r0 + RS m (their sub-block is known at compile time); the scaled row tiles are read as
+// float4, broadcast to the warp.
+template <typename InT, int C>
+__global__ void __launch_bounds__(256) scores_anchored_kernel(const InT* __restrict__ q,
+                                                              const InT* __restrict__ k,
+                                                              const InT* __restrict__ beta,
+                                                              const float* __restrict__ G,
+                                                              ChunkMap cm, int H, int hr, int K,
+                                                              float* __restrict__ Akk,
+                                                              float* __restrict__ Aqk) {
+    constexpr int NB = C / 16, DA = 16, PM = C * C / 256, RS = 256 / C;
+    static_assert(RS * PM == C && 16 % RS == 0, "pair layout");
+    __shared__ __align__(16) float krs[C][DA];
+    __shared__ __align__(16) float qrs[C][DA];
+    __shared__ float ksm[C][DA + 1], gsm[C][DA + 1];
+    __shared__ float kcs[NB][C][DA + 1];
+    __shared__ float gm[NB][DA];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x;
+    const int j = tid % C, r0 = tid / C;
+    float a1[PM], a2[PM];
+#pragma unroll
+    for (int m = 0; m < PM; ++m) a1[m] = a2[m] = 0.f;
+    for (int d0 = 0; d0 < K; d0 += DA) {
+        __syncthreads();
+        for (int idx = tid; idx < C * DA; idx += 256) {
+            const int i = idx / DA, dd = idx % DA;
+            float kv = 0.f, qv = 0.f, gv = 0.f;
+            if (i < len) {
+                const size_t qo = qk_row(t0 + i, h, H, hr) * K + d0 + dd;
+                kv = to_f32(k[qo]);
+                qv = to_f32(q[qo]);
+                gv = G[((size_t)(t0 + i) * H + h) * K + d0 + dd];
+            }
+            ksm[i][dd] = kv;
+            gsm[i][dd] = gv;
+            qrs[i][dd] = qv;
+        }
+        __syncthreads();
+        if (tid < NB * DA) {  // anchors: the sub-block's midpoint row, or its last valid row
+            const int b = tid / DA, dd = tid % DA;
+            gm[b][dd] = (16 * b < len) ? gsm[min(16 * b + 8, len - 1)][dd] : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < C * DA; idx += 256) {
+            const int i = idx / DA, dd = idx % DA;
+            const float e = (i < len) ? exp2f(gsm[i][dd] - gm[i / 16][dd]) : 0.f;
+            krs[i][dd] = ksm[i][dd] * e;
+            qrs[i][dd] *= e;
+        }
+        for (int idx = tid; idx < NB * C * DA; idx += 256) {
+            const int b = idx / (C * DA), jj = (idx / DA) % C, dd = idx % DA;
+            kcs[b][jj][dd] = (jj < 16 * (b + 1) && jj < len)
+                                 ? ksm[jj][dd] * exp2f(gm[b][dd] - gsm[jj][dd]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int dd = 0; dd < DA; dd += 4) {
+            float kc[NB][4];
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kc[b][e] = kcs[b][j][dd + e];
+#pragma unroll
+            for (int m = 0; m < PM; ++m) {
+                const int i = r0 + RS * m, b = (RS * m) / 16;
+                const float4 kr = *reinterpret_cast<const float4*>(&krs[i][dd]);
+                const float4 qr = *reinterpret_cast<const float4*>(&qrs[i][dd]);
+                a1[m] = fmaf(kr.x, kc[b][0], a1[m]);
+                a1[m] = fmaf(kr.y, kc[b][1], a1[m]);
+                a1[m] = fmaf(kr.z, kc[b][2], a1[m]);
+                a1[m] = fmaf(kr.w, kc[b][3], a1[m]);
+                a2[m] = fmaf(qr.x, kc[b][0], a2[m]);
+                a2[m] = fmaf(qr.y, kc[b][1], a2[m]);
+                a2[m] = fmaf(qr.z, kc[b][2], a2[m]);
+                a2[m] = fmaf(qr.w, kc[b][3], a2[m]);
+            }
+        }
+    }
+    const float scale = rsqrtf((float)K);
+#pragma unroll
+    for (int m = 0; m < PM; ++m) {
+        const int i = r0 + RS * m;
+        if (i < len) {
+            const size_t off = ((size_t)(t0 + i) * H + h) * C + j;
+            const float bi = to_f32(beta[(size_t)(t0 + i) * H + h]);
+            Akk[off] = (j < i) ? bi * a1[m] : 0.f;
+            Aqk[off] = (j <= i) ? scale * a2[m] : 0.f;
+        }
+    }
+}
+
 // a3: T = (I + Akk)^-1 by forward substitution, one thread per column of T
 template <int C>
 __global__ void __launch_bounds__(C) solve_kernel(const float* __restrict__ Akk, ChunkMap cm,
@@ -424,8 +522,12 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     const InT* beta = (const InT*)a.beta;
     if (slots > 0) {
         dim3 g2(slots, a.H);
-        scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K, ws.Akk,
-                                                        ws.Aqk);
+        if (a.mode == 1)  // safe gate: bounded decay, anchored products
+            scores_anchored_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K,
+                                                                     ws.Akk, ws.Aqk);
+        else
+            scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K, ws.Akk,
+                                                            ws.Aqk);
         solve_kernel<C><<<g2, C, 0, a.stream>>>(ws.Akk, cm, a.H, ws.Tm);
         wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, hr, a.K, a.V,
                                                     ws.w, ws.u);
