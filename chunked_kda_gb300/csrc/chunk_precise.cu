@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(C) solve_kernel(const float* __restrict__ Akk,
 // a4: w = T (beta k 2^G) [C,K], u = T (beta v) [C,V]; one thread per output column, four
 // rows at a time (four independent sums; T read as float4, broadcast to the warp)
 template <typename InT, int C>
-__global__ void __launch_bounds__(256) wu_kernel(const InT* __restrict__ k,
+__global__ void __launch_bounds__(256, 2) wu_kernel(const InT* __restrict__ k,
                                                  const InT* __restrict__ v,
                                                  const InT* __restrict__ beta,
                                                  const float* __restrict__ G,
