@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(256, 2) wu_kernel(const InT* __restrict__ k,
 // every thread owns CPT consecutive columns of one state row d in registers and adds
 // kd[i][d] v_new[i][.] over the chunk's rows, kd = k 2^(Glast - G) read coalesced over d.
 template <typename InT, int C, int K>
-__global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
+__global__ void __launch_bounds__(256, 3) scan_kernel(const InT* __restrict__ k,
                                                    const float* __restrict__ G,
                                                    const float* __restrict__ w,
                                                    const float* __restrict__ u, const float* h0,
@@ -354,13 +354,27 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
             acc[r][0] = (i < len) ? u[row * V + v0 + 2 * cp] : 0.f;
             acc[r][1] = (i < len) ? u[row * V + v0 + 2 * cp + 1] : 0.f;
         }
+        // the w tiles are software-pipelined: tile d0 + DW is loaded into registers while the
+        // products of tile d0 run
+        constexpr int WPT = C * DW / 256;  // w elements per thread and tile
+        float wreg[WPT];
+        auto load_w = [&](int d0) {
+#pragma unroll
+            for (int e = 0; e < WPT; ++e) {
+                const int idx = tid + 256 * e, i = idx / DW, dd = idx % DW;
+                wreg[e] = (i < len) ? w[((size_t)(t0 + i) * H + h) * K + d0 + dd] : 0.f;
+            }
+        };
+        load_w(0);
         for (int d0 = 0; d0 < K; d0 += DW) {
             __syncthreads();  // the previous w tile is consumed
-            for (int idx = tid; idx < C * DW; idx += 256) {
-                const int i = idx / DW, dd = idx % DW;
-                wt[i][dd] = (i < len) ? w[((size_t)(t0 + i) * H + h) * K + d0 + dd] : 0.f;
+#pragma unroll
+            for (int e = 0; e < WPT; ++e) {
+                const int idx = tid + 256 * e;
+                wt[idx / DW][idx % DW] = wreg[e];
             }
             __syncthreads();
+            if (d0 + DW < K) load_w(d0 + DW);
 #pragma unroll 8
             for (int dd = 0; dd < DW; ++dd) {
                 const float2 hv = *reinterpret_cast<const float2*>(&hs[d0 + dd][2 * cp]);
@@ -395,7 +409,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const InT* __restrict__ k,
                 hrow[j] = gam * x.x; hrow[j + 1] = gam * x.y; hrow[j + 2] = gam * x.z; hrow[j + 3] = gam * x.w;
             }
         }
-#pragma unroll 4
+#pragma unroll 8
         for (int i = 0; i < len; ++i) {
             const size_t off = ((size_t)(t0 + i) * H + h) * K + dr;
             const float kd = to_f32(k[qk_row(t0 + i, h, H, hr) * K + dr]) * exp2f(gl - G[off]);
