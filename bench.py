@@ -365,29 +365,7 @@ def run_ours(args, world, rank, local):
     e2e_value = world * head_tokens * e2e_steps / e2e_s
     del host, dbufs, obufs
 
-    # decode: 512 packed one-token sequences, H=32, K=V=128, FP32 states in place
-    n_dec, Hd = 512, 32
-    S = workloads.decode_state(n_dec, Hd, device=dev)
-    cu = workloads.decode_cu_seqlens(n_dec, device=dev)
-    pool = [workloads.decode_step(i, n_dec, Hd, device=dev) for i in range(4)]
-    od = torch.empty((1, n_dec, Hd, 128), device=dev, dtype=torch.bfloat16)
-
-    def dstep(i):
-        p = pool[i % len(pool)]
-        kda.kda_recurrent_fwd(p.q, p.k, p.v, p.gate, p.beta, S, True, cu, o=od, final_state=S)
-
-    for i in range(3):
-        dstep(i)
-    torch.cuda.synchronize()
-    d_steps = 64
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for i in range(d_steps):
-        dstep(i)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    dec_s = d0.elapsed_time(d1) / 1e3 / d_steps
-    dec_bytes = 2 * S.numel() * 4 + n_dec * Hd * (3 * 128 * 2 + 128 * 4 + 2 + 128 * 2)
+    dec_s, dec_bytes = time_decode(kda, workloads, dev, stream, 512, 64)
     sampler.stop()
 
     if rank != 0:
@@ -439,6 +417,53 @@ def launches_per_chunk_call(dtype, K, V, C):
     return 1 if (dtype == torch.bfloat16 and K == 128 and V == 128 and C in (32, 64)) else 6
 
 
+def time_decode(kda, workloads, dev, stream, n_dec, d_steps):
+    """Decode: n_dec packed one-token sequences, H=32, K=V=128, FP32 states in place; returns
+    (seconds per step, algorithmic bytes per step)."""
+    import torch
+
+    Hd = 32
+    S = workloads.decode_state(n_dec, Hd, device=dev)
+    cu = workloads.decode_cu_seqlens(n_dec, device=dev)
+    pool = [workloads.decode_step(i, n_dec, Hd, device=dev) for i in range(4)]
+    od = torch.empty((1, n_dec, Hd, 128), device=dev, dtype=torch.bfloat16)
+
+    def dstep(i):
+        p = pool[i % len(pool)]
+        kda.kda_recurrent_fwd(p.q, p.k, p.v, p.gate, p.beta, S, True, cu, o=od, final_state=S)
+
+    for i in range(3):
+        dstep(i)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(d_steps):
+        dstep(i)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_s = d0.elapsed_time(d1) / 1e3 / d_steps
+    dec_bytes = 2 * S.numel() * 4 + n_dec * Hd * (3 * 128 * 2 + 128 * 4 + 2 + 128 * 2)
+    return dec_s, dec_bytes
+
+
+def run_decode_only(args, local):
+    """The decode step alone (kda_recurrent_fwd), for profiling: one JSON line."""
+    import torch
+
+    import chunked_kda_gb300 as kda
+    from chunked_kda_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kda.load_library()
+    peaks, _ = load_peaks()
+    dec_s, dec_bytes = time_decode(kda, workloads, dev, torch.cuda.current_stream(),
+                                   args.decode_seqs, args.steps)
+    print(json.dumps({"decode_seqs": args.decode_seqs, "heads": 32, "ms_per_step": 1e3 * dec_s,
+                      "achieved_gbs": dec_bytes / dec_s / 1e9,
+                      "frac_of_hbm": dec_bytes / dec_s / 1e9 / peaks["hbm_gbs"]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -451,10 +476,17 @@ def main():
                          "the one the metric is quoted on")
     ap.add_argument("--chunk-only", action="store_true",
                     help="time the chunked forward only (no e2e, decode or CPU leg); for profiling")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time the decode step only (kda_recurrent_fwd); for profiling")
+    ap.add_argument("--decode-seqs", type=int, default=512,
+                    help="one-token sequences of the decode step (32 heads each)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.decode_only:
+        run_decode_only(args, local)
         return
     run_ours(args, world, rank, local)
 
