@@ -15,6 +15,7 @@ import threading
 import torch
 
 __all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_bytes_ex",
+           "kda_fused_wait_timeouts",
            "kda_chunk_fwd", "kda_chunk_fwd_ex",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
            "GATE_NONSAFE", "GATE_LOG2", "FLAG_K_L2NORM", "FLAG_BETA_LOGITS", "kda_recurrent_fwd_ex",
@@ -64,6 +65,8 @@ def load_library():
         lib.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_chunk_workspace_bytes_ex.argtypes = [i32] * 9
         lib.kda_chunk_workspace_bytes_ex.restype = ctypes.c_size_t
+        lib.kda_fused_wait_timeouts.argtypes = [vp, i32]
+        lib.kda_fused_wait_timeouts.restype = i32
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
                                       i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
                                       ctypes.c_size_t, vp]
@@ -166,6 +169,15 @@ def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=N
 
 def kda_chunk_workspace_bytes_ex(dtype, B, T, H, K, V, chunk_size, n_seqs, mode) -> int:
     return kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs, mode)
+
+
+def kda_fused_wait_timeouts(reset=False) -> int:
+    """Fused-kernel mbarrier waits that gave up on the current device (0 after normal runs);
+    synchronises with the device."""
+    lib = load_library()
+    n = ctypes.c_uint(0)
+    _check("kda_fused_wait_timeouts", lib.kda_fused_wait_timeouts(ctypes.byref(n), 1 if reset else 0))
+    return int(n.value)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,

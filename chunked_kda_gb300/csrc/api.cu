@@ -112,6 +112,12 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
     return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
 }
 
+kda_status kda_fused_wait_timeouts(unsigned int* count, int reset) {
+    g_last_error.clear();
+    if (!count) return fail(KDA_ERR_INVALID_ARG, "null count");
+    return cuda_status(kda::read_fused_timeouts(count, reset != 0));
+}
+
 kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                          const void* g, kda_dtype g_dtype, const float* A_log,
                          const float* dt_bias, kda_gate_mode mode, float lower_bound,

@@ -51,6 +51,7 @@
 // reads query / key head h / (H / Hk) through the TMA head coordinate).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <type_traits>
 
 #include "common.cuh"
@@ -96,7 +97,7 @@ constexpr uint32_t OFF_GCARRY = 206336;  // chain: fp32 [3][128] gate sums of ro
 constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block midpoints
 constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
-constexpr uint32_t OFF_MISC = 210784;  // tmem base, abort flag
+constexpr uint32_t OFF_MISC = 210800;  // tmem base, abort flag, TMA loads issued (qk, v, g)
 constexpr uint32_t OFF_QSS = 211072;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
 constexpr uint32_t OFF_KD1 = 212992;   // hand-off: k 2^(Gl-G) of the odd chunks (OFF_KD: the even)
 constexpr uint32_t SMEM_BYTES = 229376 + 1024;  // + alignment slack
@@ -111,9 +112,9 @@ constexpr int LD = 68;                 // fp32 row stride of the solve matrices 
 // mbarriers (each completes once per chunk, the v tiles once per two chunks)
 enum {
     B_VFULL = 0, B_QKIN, B_GIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
-    B_DRAIN0, B_DRAIN1, B_GATE, NBAR
+    B_DRAIN0, B_DRAIN1, B_GATE, B_STALL, NBAR
 };
-static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC, "mbarriers");
+static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC && OFF_MISC + 32 <= OFF_QSS, "mbarriers");
 
 // TMEM columns
 constexpr uint32_t TM_H = 0;     // the state h^T fp32 [128 lanes = v][128 = k]; the dH MMA
@@ -179,6 +180,8 @@ struct Params {
     int T, H;
     int qnorm;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
     int hr;     // value heads per query / key head: value head h reads q, k head h / hr
+    int stall_chunk;  // test hook (>= 0): at this chunk the preparation group waits, with a short
+                      // limit, on an mbarrier nothing completes, so the CTA takes its abort path
 };
 
 struct Sync {
@@ -241,6 +244,13 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         const long t0 = bos + (long)c * C;
         const int len = (int)min((long)C, eos - t0);
 
+        if (c == p.stall_chunk) {  // test hook: a bounded wait that gives up
+            if (w == 0 && !sy.aborted() && !mbar_wait(sy.bar(B_STALL), 0, 1u << 10)) {
+                if (l == 0) atomicAdd(&g_fused_timeouts, 1u);
+                *sy.abort_flag = 1u;
+            }
+            bar_sync(BAR_PREP, NGRP);
+        }
         const float* bcur = bsm + (c & 1) * C;  // beta of the chunk (zero past the end)
 
         // ---- k and q of the own rows from the tiles the chain prefetched into the k 2^G /
@@ -710,7 +720,12 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         return (ct < eos - tc0) ? __bfloat162float(p.beta[(size_t)(tc0 + ct) * H + h]) : 0.f;
     };
     float bet_next = (ct < C && nt > 0) ? beta_of(0) : 0.f;
+    // TMA loads issued per barrier, counted by their one issuing thread (ct == 0) in shared
+    // memory (a register count would stay live across the whole loop)
+    volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC) + 2;
+    if (ct == 0) issued[0] = issued[1] = issued[2] = 0u;
     auto load_gtile = [&](long t) {
+        issued[2] = issued[2] + 1u;
         mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
         for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)t, sy.bar(B_GIN));
@@ -794,6 +809,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 
     // q and k tiles of chunk c land in the k 2^G / s q 2^G buffers for the prep group
     auto load_qk = [&](long t) {
+        issued[0] = issued[0] + 1u;
         mbar_arrive_expect_tx(sy.bar(B_QKIN), 32768);
         for (int cb = 0; cb < 2; ++cb) {
             tma_load_3d(sb + OFF_KG + cb * 8192, tm_k, 64 * cb, h / p.hr, (int)t, sy.bar(B_QKIN));
@@ -801,6 +817,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         }
     };
     auto load_v = [&](long t) {
+        issued[1] = issued[1] + 1u;
         mbar_arrive_expect_tx(sy.bar(B_VFULL), 16384);
         for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(sb + OFF_V + cb * 8192, tm_v, 64 * cb, h, (int)t, sy.bar(B_VFULL));
@@ -998,6 +1015,15 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             for (int j = 0; j < 32; ++j) p.hT[st_off + (size_t)(64 * hch + 32 * s + j) * VD + vlane] = hv[j];
         }
     }
+    // A CTA that gave up a wait leaves no copy in flight behind it: the issuing thread waits
+    // (bounded) for the last load of each kind (before an abort every load is consumed before
+    // the next is issued, after it none is issued, so at most the last one can be in flight).
+    if (ct == 0 && sy.aborted()) {
+        for (int b = 0; b < 3; ++b) {
+            const uint32_t n = issued[b];
+            if (n > 0) mbar_wait(sy.bar(b == 0 ? B_QKIN : b == 1 ? B_VFULL : B_GIN), (n - 1u) & 1u);
+        }
+    }
 }
 
 template <typename GT, typename OT, bool kHeadsFastest>
@@ -1111,6 +1137,21 @@ static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUten
     return cudaGetLastError();
 }
 
+// test hook: KDA_TEST_WAIT_TIMEOUT_CHUNK=<c> makes every CTA give up a wait at chunk c
+static int stall_chunk_from_env() {
+    const char* v = getenv("KDA_TEST_WAIT_TIMEOUT_CHUNK");
+    return (v && *v) ? atoi(v) : -1;
+}
+
+cudaError_t read_fused_timeouts(unsigned* count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_fused_timeouts, sizeof(unsigned));
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_fused_timeouts, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
 cudaError_t launch_chunk_fused(const FwdArgs& a) {
     using namespace fused;
     CUtensorMap mq, mk, mv, mg;
@@ -1123,7 +1164,7 @@ cudaError_t launch_chunk_fused(const FwdArgs& a) {
     if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
              a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0,
-             a.Hk > 0 ? a.H / a.Hk : 1};
+             a.Hk > 0 ? a.H / a.Hk : 1, stall_chunk_from_env()};
     if (a.g_bf16)
         return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
                        : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);

@@ -83,6 +83,8 @@ cudaError_t launch_chunk_precise(const FwdArgs& a);
 bool fused_supported(const FwdArgs& a);
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
+// fused-kernel mbarrier waits that gave up on the current device (synchronises), optional reset
+cudaError_t read_fused_timeouts(unsigned* count, bool reset);
 
 // sets the message kda_last_error() returns on this host thread
 void record_error(const char* msg);

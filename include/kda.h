@@ -283,6 +283,21 @@ kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda
                                 unsigned flags, kda_stream_t stream);
 
 /* static, NUL-terminated description of a status code */
+/*
+ * Diagnostics of the fused path's bounded waits.  Every mbarrier wait of the fused
+ * chunked kernel gives up after a fixed number of polls; a CTA whose wait gave up adds to a
+ * per-device counter, stops waiting, issuing MMAs and copies, lets the ones in flight finish
+ * (bounded), frees its TMEM and returns, so the context stays usable but that launch's
+ * outputs are not valid.  kda_fused_wait_timeouts writes the counter of the current device
+ * to *count (0 after normal runs) and zeroes it when reset != 0.  It copies from the device
+ * and therefore synchronises with it: a diagnostic call, not for the hot path.  Null count:
+ * KDA_ERR_INVALID_ARG; a failing copy: KDA_ERR_CUDA.
+ * Test hook: with the environment variable KDA_TEST_WAIT_TIMEOUT_CHUNK=<c> set when
+ * kda_chunk_fwd launches the fused kernel, every CTA waits at its chunk c on an mbarrier
+ * that nothing completes (with a short limit) and takes that path.
+ */
+kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
+
 const char* kda_status_string(kda_status status);
 
 /* the last error detail recorded by a failed call on this host thread ("" if none) */

@@ -82,6 +82,12 @@ def test_status_strings(lib):
         assert lib.kda_status_string(code).startswith(b"KDA_")
 
 
+def test_wait_timeouts_null_count(lib):
+    """The diagnostics query rejects a null count on the host (no device access)."""
+    lib.kda_fused_wait_timeouts.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    assert lib.kda_fused_wait_timeouts(None, 0) == 1  # KDA_ERR_INVALID_ARG
+
+
 P = ctypes.c_void_p(4096)  # aligned stand-in: never dereferenced, validation fails first
 
 

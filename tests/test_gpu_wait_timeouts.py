@@ -1,0 +1,39 @@
+"""The fused kernel's bounded waits: a wait that nothing completes gives up after its limit,
+the launch takes its abort path (no MMAs or copies left in flight, TMEM freed), the host reads
+the count, and the CUDA context stays usable.  The failure is made by the kernel's test hook
+(an mbarrier that nothing arrives on), never by a fault, trap or hang."""
+import pytest
+import torch
+
+from chunked_kda_gb300 import workloads
+from test_gpu_chunk import compare, kda, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def test_normal_runs_count_no_timeouts():
+    w = workloads.make_dense("t", 1, 200, 2, 128, 128, 64, torch.bfloat16, 61, state_std=0.05)
+    kda().kda_fused_wait_timeouts(reset=True)
+    o, st = run_gpu(w)
+    assert kda().kda_fused_wait_timeouts() == 0
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("chunk", [0, 2])
+def test_wait_gives_up_and_the_context_stays_usable(monkeypatch, chunk):
+    w = workloads.make_dense("t", 1, 260, 2, 128, 128, 64, torch.bfloat16, 62, state_std=0.05)
+    kda().kda_fused_wait_timeouts(reset=True)
+    monkeypatch.setenv("KDA_TEST_WAIT_TIMEOUT_CHUNK", str(chunk))
+    run_gpu(w)  # the launch itself succeeds; its outputs are not valid
+    assert kda().kda_fused_wait_timeouts(reset=True) >= 2  # both CTAs gave up a wait
+    monkeypatch.delenv("KDA_TEST_WAIT_TIMEOUT_CHUNK")
+    o, st = run_gpu(w)  # the same context: a normal call matches the oracle again
+    assert kda().kda_fused_wait_timeouts() == 0
+    compare(w, o, st)
