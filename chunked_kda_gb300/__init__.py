@@ -15,7 +15,7 @@ import threading
 import torch
 
 __all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_bytes_ex",
-           "kda_fused_wait_timeouts",
+           "kda_fused_wait_timeouts", "kda_chunk_fwd_launches",
            "kda_chunk_fwd", "kda_chunk_fwd_ex",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
            "GATE_NONSAFE", "GATE_LOG2", "FLAG_K_L2NORM", "FLAG_BETA_LOGITS", "kda_recurrent_fwd_ex",
@@ -65,6 +65,8 @@ def load_library():
         lib.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_chunk_workspace_bytes_ex.argtypes = [i32] * 9
         lib.kda_chunk_workspace_bytes_ex.restype = ctypes.c_size_t
+        lib.kda_chunk_fwd_launches.argtypes = [i32] * 10
+        lib.kda_chunk_fwd_launches.restype = i32
         lib.kda_fused_wait_timeouts.argtypes = [vp, i32]
         lib.kda_fused_wait_timeouts.restype = i32
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
@@ -169,6 +171,16 @@ def kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=N
 
 def kda_chunk_workspace_bytes_ex(dtype, B, T, H, K, V, chunk_size, n_seqs, mode) -> int:
     return kda_chunk_workspace_bytes(dtype, B, T, H, K, V, chunk_size, n_seqs, mode)
+
+
+def kda_chunk_fwd_launches(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=GATE_SAFE,
+                           o_dtype=None) -> int:
+    """Kernel launches of one kda_chunk_fwd call with these sizes on the current device (-1 for
+    invalid sizes)."""
+    code = _F32 if dtype == torch.float32 else _BF16
+    ocode = code if o_dtype is None else (_F32 if o_dtype == torch.float32 else _BF16)
+    lib = load_library()
+    return int(lib.kda_chunk_fwd_launches(code, ocode, B, T, H, K, V, chunk_size, n_seqs, mode))
 
 
 def kda_fused_wait_timeouts(reset=False) -> int:

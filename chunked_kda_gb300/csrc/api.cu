@@ -112,6 +112,22 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
     return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
 }
 
+int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T, int H, int K, int V,
+                           int chunk_size, int n_seqs, kda_gate_mode mode) {
+    if (B < 0 || T < 0 || H <= 0 || n_seqs < 0 || !head_dim_ok(K) || !head_dim_ok(V)) return -1;
+    if (chunk_size != 32 && chunk_size != 64) return -1;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return -1;
+    if (o_dtype != qkv_dtype && o_dtype != KDA_F32) return -1;
+    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE) return -1;
+    const bool packed = n_seqs > 0;
+    if (packed && B != 1) return -1;
+    const int N = packed ? n_seqs : B;
+    if (N == 0) return 0;
+    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode))
+        return kda::fused_launch_count(N, H, T, packed, o_dtype == KDA_F32);
+    return 6;
+}
+
 kda_status kda_fused_wait_timeouts(unsigned int* count, int reset) {
     g_last_error.clear();
     if (!count) return fail(KDA_ERR_INVALID_ARG, "null count");

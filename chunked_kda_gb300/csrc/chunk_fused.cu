@@ -52,6 +52,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
+#include <cstring>
 #include <type_traits>
 
 #include "common.cuh"
@@ -182,6 +183,15 @@ struct Params {
     int hr;     // value heads per query / key head: value head h reads q, k head h / hr
     int stall_chunk;  // test hook (>= 0): at this chunk the preparation group waits, with a short
                       // limit, on an mbarrier nothing completes, so the CTA takes its abort path
+    // Dense inputs, split schedule (sp_mode 1, 2; 0 = one CTA per unit on an (N, H) grid).  The
+    // units u = n + N h, the order of the plain grid, are laid out on two 1-D launches:
+    //   sp_mode 1: CTA i runs tokens [0, sp_cut) of unit i, i < sp_split;
+    //   sp_mode 2: CTA i < sp_rest runs unit sp_split + i whole, CTA sp_rest + i runs tokens
+    //              [sp_cut, T) of unit i.
+    // The state crosses from the first piece to the second through the unit's own output rows
+    // from token sp_cut on, which the second piece reads before it writes any output.
+    int N;
+    int sp_mode, sp_split, sp_rest, sp_cut;
 };
 
 struct Sync {
@@ -650,7 +660,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 }
 
 // ------------------------------------------------------------------ chain group
-template <typename GT, typename OT>
+template <typename GT, typename OT, bool kSplit>
 __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
                                            const Sync& sy, const CUtensorMap* tm_v,
                                            const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -683,6 +693,14 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 #pragma unroll
         for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hv[2 * e], hv[2 * e + 1]);
         tmem_st16(tmem + lane_base + TM_VN + 32 * hch + 16 * s, r);
+    };
+    // split schedule: state word (key channel kch, value channel vlane) in the unit's output
+    // rows from token ts on, row-major words (each row of o holds WPR of them)
+    auto stash = [&](long ts, int kch) -> uint32_t* {
+        constexpr int WPR = VD * (int)sizeof(OT) / 4;
+        const int j = kch * VD + vlane;
+        return reinterpret_cast<uint32_t*>(reinterpret_cast<OT*>(p.o) + ((size_t)(ts + j / WPR) * H + h) * VD) +
+               (j % WPR);
     };
 
 
@@ -823,12 +841,16 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             tma_load_3d(sb + OFF_V + cb * 8192, tm_v, 64 * cb, h, (int)t, sy.bar(B_VFULL));
     };
     if (nt > 0) {
+        const bool second = kSplit && p.sp_mode == 2 && bos != (long)n * p.T;  // second piece of a split unit
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             float hv[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)(64 * hch + 32 * s + j) * VD + vlane) : 0.f;
+            for (int j = 0; j < 32; ++j) {
+                const int kch = 64 * hch + 32 * s + j;
+                hv[j] = second ? __uint_as_float(*stash(bos, kch))
+                               : p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * VD + vlane) : 0.f;
+            }
             st_h(s, hv);
             st_hA(s, hv);
         }
@@ -999,7 +1021,18 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         bar_sync(BAR_CHAIN, NGRP);
     }
 
-    if (p.hT && !sy.aborted()) {
+    if (kSplit && p.sp_mode == 1) {  // first piece of a split unit: the state goes to the stash
+        if (!sy.aborted()) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                float hv[32];
+                ld_h(s, hv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) *stash(eos, 64 * hch + 32 * s + j) = __float_as_uint(hv[j]);
+            }
+        }
+    } else if (p.hT && !sy.aborted()) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             float hv[32];
@@ -1026,7 +1059,10 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     }
 }
 
-template <typename GT, typename OT, bool kHeadsFastest>
+// kGrid: GRID_DENSE (sequences, heads), GRID_PACKED (heads, sequences), GRID_SPLIT (the
+// split schedule of dense inputs, 1-D)
+enum { GRID_DENSE = 0, GRID_PACKED = 1, GRID_SPLIT = 2 };
+template <typename GT, typename OT, int kGrid>
 __global__ void __launch_bounds__(NTHR, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -1046,11 +1082,24 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // sequences of 1-2048 tokens, 32 heads); dense batches measure faster with the
     // sequences fastest.  (Both indices stay block-index registers: a sequence index taken
     // from a ranking in shared memory cost more in register spills than it saved.)
-    const int n = kHeadsFastest ? blockIdx.y : blockIdx.x;
-    const int h = kHeadsFastest ? blockIdx.x : blockIdx.y;
+    int n, h;
     long bos, eos;
-    if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
-    else      { bos = (long)n * p.T; eos = bos + p.T; }
+    if (kGrid != GRID_SPLIT) {
+        constexpr bool kHeadsFastest = kGrid == GRID_PACKED;
+        n = kHeadsFastest ? blockIdx.y : blockIdx.x;
+        h = kHeadsFastest ? blockIdx.x : blockIdx.y;
+        if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
+        else      { bos = (long)n * p.T; eos = bos + p.T; }
+    } else {
+        int u = blockIdx.x;
+        const bool first = p.sp_mode == 1, whole = !first && u < p.sp_rest;
+        u = first ? u : whole ? u + p.sp_split : u - p.sp_rest;
+        n = u % p.N;
+        h = u / p.N;
+        const long base = (long)n * p.T;
+        bos = (first || whole) ? base : base + p.sp_cut;
+        eos = first ? base + p.sp_cut : base + p.T;
+    }
     const int nt = (int)((eos - bos + C - 1) / C);
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
@@ -1068,7 +1117,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t tmem = misc[0];
 
     if (w < 8) prep_loop(p, sb, smem, tmem, sy, h, bos, eos, nt);
-    else       chain_loop<GT, OT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, &tm_g, n, h, bos, eos, nt);
+    else       chain_loop<GT, OT, kGrid == GRID_SPLIT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, &tm_g, n, h, bos, eos, nt);
 
     // Every MMA was waited for, unless a wait gave up: then let the ones in flight finish.
     if (sy.aborted() && (tid == 0 || tid == NGRP)) {
@@ -1124,14 +1173,89 @@ bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode) {
 
 bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C, a.mode); }
 
+// test hook: KDA_FUSED_SCHEDULE=plain keeps every dense launch at one CTA per unit
+static bool split_allowed_from_env() {
+    const char* v = getenv("KDA_FUSED_SCHEDULE");
+    return !(v && strcmp(v, "plain") == 0);
+}
+
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();  // no device: plan one launch, leave no error behind
+        return 0;
+    }
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Split schedule for dense inputs (one CTA per SM, units of nt chunks).  U = f S + r units on
+// S SMs take f + 1 unit-lengths one CTA per unit, the last wave r / S full.  Instead the
+// first S units run their first `a` chunks in one launch; a second launch runs the other
+// U - S units whole and, on the S - r SMs the last of them leave free, the S remaining pieces
+// of nt - a chunks, `rounds` after another: a + f nt chunk-times when rounds (nt - a + 1) <= nt
+// (one chunk-time for a CTA's start and end).  The second pieces must hold at least
+// `min_tail` tokens.  Returns a (chunks), or 0 for one launch.
+static int split_cut_chunks(int U, int S, int T, int min_tail) {
+    if (S <= 0 || U <= S || U % S == 0) return 0;
+    const int nt = (T + fused::C - 1) / fused::C;
+    const int f = U / S, r = U % S, free_sms = S - r;
+    const int rounds = (S + free_sms - 1) / free_sms;
+    const int tail = nt / rounds - 1;
+    if (tail < 1) return 0;
+    const int a = nt - tail;
+    if ((long)T - (long)a * fused::C < min_tail) return 0;
+    // keep it only for a clear gain over (f + 1) nt
+    if (20L * (a + (long)f * nt) > 19L * (f + 1) * nt) return 0;
+    return a;
+}
+
+// chunks of the first piece of the split schedule for these sizes (0: one launch)
+static int split_cut_for(int N, int H, int T, bool packed, bool o_f32) {
+    if (packed || !split_allowed_from_env()) return 0;
+    // the state (K V words) spans this many of the unit's output rows
+    const int stash_rows = fused::KD * fused::VD * 4 / (fused::VD * (o_f32 ? 4 : 2));
+    return split_cut_chunks(N * H, sm_count(), T, stash_rows);
+}
+
+int fused_launch_count(int N, int H, int T, bool packed, bool o_f32) {
+    return split_cut_for(N, H, T, packed, o_f32) > 0 ? 2 : 1;
+}
+
 template <typename GT, typename OT>
 static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mg, const fused::Params& p) {
+                            const CUtensorMap& mv, const CUtensorMap& mg, fused::Params p) {
     using namespace fused;
     const bool packed = a.cu != nullptr;
-    auto kern = packed ? chunk_fused_kernel<GT, OT, true> : chunk_fused_kernel<GT, OT, false>;
+    auto kern = packed ? chunk_fused_kernel<GT, OT, GRID_PACKED> : chunk_fused_kernel<GT, OT, GRID_DENSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    {
+        const int cut = split_cut_for(a.N, a.H, a.T, packed, sizeof(OT) == 4);
+        const int U = a.N * a.H, S = sm_count();
+        if (cut > 0) {
+            auto ks = chunk_fused_kernel<GT, OT, GRID_SPLIT>;
+            e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            p.sp_split = S;
+            p.sp_rest = U - S;
+            p.sp_cut = cut * C;
+            p.sp_mode = 1;
+            ks<<<dim3(S), NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            p.sp_mode = 2;
+            ks<<<dim3(U), NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
+            return cudaGetLastError();
+        }
+    }
     const dim3 grid = packed ? dim3(a.H, a.N) : dim3(a.N, a.H);
     kern<<<grid, NTHR, SMEM_BYTES, a.stream>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
@@ -1164,7 +1288,7 @@ cudaError_t launch_chunk_fused(const FwdArgs& a) {
     if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
              a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0,
-             a.Hk > 0 ? a.H / a.Hk : 1, stall_chunk_from_env()};
+             a.Hk > 0 ? a.H / a.Hk : 1, stall_chunk_from_env(), a.N, 0, 0, 0, 0};
     if (a.g_bf16)
         return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
                        : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);

@@ -83,6 +83,9 @@ cudaError_t launch_chunk_precise(const FwdArgs& a);
 bool fused_supported(const FwdArgs& a);
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
+// kernel launches of the fused path for these sizes on the current device (1, or 2 for the
+// split schedule of dense inputs)
+int fused_launch_count(int N, int H, int T, bool packed, bool o_f32);
 // fused-kernel mbarrier waits that gave up on the current device (synchronises), optional reset
 cudaError_t read_fused_timeouts(unsigned* count, bool reset);
 

@@ -130,6 +130,25 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
                                     int chunk_size, int n_seqs, kda_gate_mode mode);
 
 /*
+ * Kernel launches one kda_chunk_fwd call with these sizes makes on the current device, for
+ * profiling and launch accounting: 0 when there are no sequences, 6 on the stage-by-stage
+ * path, 1 on the fused path, 2 when the fused path uses its split schedule.  n_seqs as for
+ * kda_chunk_workspace_bytes (0 = dense).  Invalid sizes or enums: -1.  No device work.
+ *
+ * Split schedule (dense bf16 inputs, K = V = 128): one CTA per SM runs one (sequence, head)
+ * unit, so U = f S + r units on S SMs take f + 1 unit-lengths with the last wave r / S full.
+ * When that wave is partial enough to matter, the call launches the fused kernel twice on
+ * the stream: the first S units' leading chunks, then the other units whole together with
+ * the first S units' remaining chunks, which fill the SMs the last whole units leave free.
+ * The FP32 state crosses between the two launches through the unit's own rows of o (before
+ * the second launch overwrites them), so the split needs no workspace and the results are
+ * bitwise those of one launch.  The environment variable KDA_FUSED_SCHEDULE=plain, read per
+ * call, keeps one launch.
+ */
+int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T, int H, int K, int V,
+                           int chunk_size, int n_seqs, kda_gate_mode mode);
+
+/*
  * Chunked KDA forward (prefill).  Steps: gate activation + chunk-local log2
  * cumsum; causal intra-chunk scores Akk (strictly lower, beta-scaled) and Aqk
  * (lower incl. diagonal, 1/sqrt(K)-scaled) on 16-token sub-blocks; the unit

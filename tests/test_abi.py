@@ -21,7 +21,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = open(h).read()
-        names |= set(re.findall(r"^\s*(?:kda_status|size_t|const char\s*\*)\s*(kda_\w+)\s*\(",
+        names |= set(re.findall(r"^\s*(?:kda_status|size_t|int|const char\s*\*)\s*(kda_\w+)\s*\(",
                                 text, flags=re.M))
     return names
 
@@ -42,6 +42,8 @@ def lib():
     L.kda_chunk_workspace_bytes.restype = ctypes.c_size_t
     L.kda_chunk_workspace_bytes_ex.argtypes = [i32] * 9
     L.kda_chunk_workspace_bytes_ex.restype = ctypes.c_size_t
+    L.kda_chunk_fwd_launches.argtypes = [i32] * 10
+    L.kda_chunk_fwd_launches.restype = i32
     # full prototypes: a call with the wrong arity raises instead of passing stray values
     L.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
                                    i32, i32, i32, i32, i32, i32, vp, i32, vp, ctypes.c_size_t, i32,
@@ -184,6 +186,21 @@ def test_recurrent_and_gate_host_validation(lib):
     assert g == INVALID  # non-safe gate without A_log
     g = lib.kda_gate_fwd(P, BF16, P, None, 3, 0.0, None, 0, 1, 4, 2, 128, 64, P, None)
     assert g == INVALID  # no such mode
+
+
+def test_launch_counts(lib):
+    f = lib.kda_chunk_fwd_launches
+    SAFE, NONSAFE = 1, 2
+    assert f(F32, F32, 1, 128, 2, 64, 64, 64, 0, SAFE) == 6           # stage-by-stage
+    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 6
+    assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 6
+    assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, SAFE) == 1   # fused, packed
+    assert f(BF16, F32, 4, 4096, 64, 128, 128, 64, 0, SAFE) in (1, 2)  # split: by the SM count
+    assert f(BF16, BF16, 0, 4096, 64, 128, 128, 64, 0, SAFE) == 0     # no sequences
+    assert f(BF16, BF16, 4, 4096, 64, 128, 128, 48, 0, SAFE) == -1    # chunk size
+    assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, 7) == -1       # gate mode
+    assert f(BF16, BF16, 2, 4096, 64, 128, 128, 64, 3, SAFE) == -1    # packed needs B == 1
+    assert f(F32, BF16, 1, 128, 2, 64, 64, 64, 0, SAFE) == -1         # o dtype
 
 
 def test_workspace_bytes(lib):
