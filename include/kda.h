@@ -137,7 +137,7 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
  *
  * Split schedule (dense bf16 inputs, K = V = 128): one CTA per SM runs one (sequence, head)
  * unit, so U = f S + r units on S SMs take f + 1 unit-lengths with the last wave r / S full.
- * When that wave is partial enough to matter, the call launches the fused kernel twice on
+ * When that wave is at most half full, the call launches the fused kernel twice on
  * the stream: the first S units' leading chunks, then the other units whole together with
  * the first S units' remaining chunks, which fill the SMs the last whole units leave free.
  * The FP32 state crosses between the two launches through the unit's own rows of o (before

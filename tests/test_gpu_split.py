@@ -92,7 +92,8 @@ def test_no_split_when_the_second_pieces_are_too_short():
     B, H, S = split_shape()
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, B, 320, H, 128, 128, 64, 0) == 1
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, B, T_SPLIT, H, 128, 128, 64, 0) == 2
-    # whole waves, or fewer units than SMs: one launch
+    # whole waves, fewer units than SMs, or a last wave more than half full: one launch
+    assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, 4096, S + S // 2 + 2, 128, 128, 64, 0) == 1
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, 4096, S, 128, 128, 64, 0) == 1
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, 4096, S - 1, 128, 128, 64, 0) == 1
     # packed inputs keep their heads-fastest grid
