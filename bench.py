@@ -391,8 +391,9 @@ def run_ours(args, world, rank, local):
                      "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                      "traffic": fused_traffic_bytes(args.workload),
                      "peak_source": peak_src,
-                     "kernel": f"chunk_fused_kernel ({n_launch} launch{'es' if n_launch > 1 else ''} "
-                               f"per kda_chunk_fwd call, timed together)"},
+                     "kernel": "chunk_fused_kernel (one launch per kda_chunk_fwd call)" if n_launch == 1
+                               else f"chunk_fused_kernel ({n_launch} launches per kda_chunk_fwd call, "
+                                    f"timed together)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "pipelined": "two device buffer sets, copy-in / forward / copy-out streams"},
