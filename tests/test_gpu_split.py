@@ -98,3 +98,39 @@ def test_no_split_when_the_second_pieces_are_too_short():
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, 4096, S - 1, 128, 128, 64, 0) == 1
     # packed inputs keep their heads-fastest grid
     assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, 8192, H, 128, 128, 64, B) == 1
+
+
+def test_split_schedule_in_a_cuda_graph():
+    """Both launches of the split schedule are captured; replays with new inputs written in
+    place match eager calls bitwise."""
+    B, H, S = split_shape()
+    ws = [workloads.make_dense("t", B, T_SPLIT, H, 128, 128, 64, torch.bfloat16, 80 + i,
+                               state_std=0.05) for i in range(2)]
+    t = to_device(ws[0])
+    S0, S_fin = t["initial_state"].clone(), torch.empty_like(t["initial_state"])
+    o = torch.empty((B, T_SPLIT, H, 128), device="cuda", dtype=torch.bfloat16)
+
+    def call():
+        kda().kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
+                            ws[0].mode, ws[0].lower_bound, S0, True, None, 64, o=o,
+                            final_state=S_fin)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        call()  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    for w in ws[::-1]:
+        src = to_device(w)
+        for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias"):
+            t[name].copy_(src[name])
+        S0.copy_(src["initial_state"])
+        graph.replay()
+        torch.cuda.synchronize()
+        o_g, s_g = o.clone(), S_fin.clone()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o) and torch.equal(s_g, S_fin)
