@@ -1,8 +1,11 @@
-// Chunked KDA forward, float32 SIMT path, one kernel per step.
+// Chunked KDA forward, float32 stage-by-stage path, one kernel per step.
 //
 // This path computes every step in FP32 with FFMA, so it meets float32-input
 // accuracy (tensor-core bf16/tf32 operands would not), and it serves as the
-// stage-by-stage form of the chunked algorithm.  Steps and their sources:
+// stage-by-stage form of the chunked algorithm.  The one exception: with bf16
+// inputs the output step runs its two products on the tensor cores with tf32
+// operands (10-bit mantissa, FP32 accumulation), far inside the bf16-input
+// tolerance.  Steps and their sources:
 //   a1 gate + chunk-local log2 cumsum   FLA skill "fla-kda", "Gate modes" and
 //                                       "Safe gate numerical note" (RCP_LN2)
 //   a2 causal scores Akk, Aqk           Helion PR #3290 "Read only the causal
@@ -21,8 +24,11 @@
 // Workspace (float32, token-indexed like the inputs; T_tot = B * T):
 //   G [T_tot,H,K] | Akk [T_tot,H,C] | Aqk [T_tot,H,C] | Tm [T_tot,H,C] |
 //   w [T_tot,H,K] | u [T_tot,H,V] | v_new [T_tot,H,V] | h [slots,H,K,V]
+#include <type_traits>
+
 #include "common.cuh"
 #include "kda_internal.h"
+#include "sm100.cuh"
 
 namespace kda {
 
@@ -521,6 +527,137 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
         if (i < len) o[((size_t)(t0 + i) * H + h) * V + vcol] = from_f32<OutT>(acc[i] * rs[i]);
 }
 
+// a6 for bf16 inputs: the same o = s (q 2^G) h_c + Aqk v_new with m16n8k8 tf32 MMAs (FP32
+// accumulation).  One block of 256 threads per (chunk slot, head); warp w owns the 16 rows
+// 16 (w % WM) .. and the V / WN columns from (w / WM) V / WN on, as NT tiles of 8 columns.
+// The K (then C) dimension goes through shared memory in slabs of KS: rows of s q 2^G (then
+// of Aqk) and rows of h_c (then of v_new, zero past the end of the chunk, where it may hold
+// anything).  Fragments (g = lane / 4, t = lane % 4): a = A[g][t], A[g+8][t], A[g][t+4],
+// A[g+8][t+4]; b = B[t][g], B[t+4][g]; c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1].
+// The padded row lengths make both fragment loads hit 32 different banks.
+template <int C, int V, typename OutT>
+__global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __restrict__ q,
+                                                     const float* __restrict__ G,
+                                                     const float* __restrict__ Aqk,
+                                                     const float* __restrict__ hc,
+                                                     const float* __restrict__ vn, ChunkMap cm,
+                                                     int H, int hr, int K, int qnorm,
+                                                     OutT* __restrict__ o) {
+    using namespace sm100;
+    constexpr int WM = C / 16, WN = 8 / WM, NT = V / (8 * WN), KS = 32;
+    constexpr int LA = KS + 4, LB = V + 8;
+    __shared__ __align__(16) float As[C][LA];
+    __shared__ __align__(16) float Bs[KS][LB];
+    __shared__ float rs[C];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int g = l >> 2, t = l & 3;
+    const int r0 = 16 * (w % WM), c0 = (w / WM) * (V / WN);
+    const float scale = rsqrtf((float)K);
+    for (int i = tid; i < C; i += 256) {
+        float r = 1.f;
+        if (qnorm && i < len) {
+            float ss = 0.f;
+            const __nv_bfloat16* qi = q + qk_row(t0 + i, h, H, hr) * K;
+            for (int d = 0; d < K; ++d) ss = fmaf(__bfloat162float(qi[d]), __bfloat162float(qi[d]), ss);
+            r = rsqrtf(ss + kQNormEps);
+        }
+        rs[i] = r;
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    auto mma_slab = [&]() {
+#pragma unroll
+        for (int k0 = 0; k0 < KS; k0 += 8) {
+            const uint32_t a[4] = {to_tf32(As[r0 + g][k0 + t]), to_tf32(As[r0 + g + 8][k0 + t]),
+                                   to_tf32(As[r0 + g][k0 + t + 4]), to_tf32(As[r0 + g + 8][k0 + t + 4])};
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int cb = c0 + 8 * j + g;
+                const uint32_t b[2] = {to_tf32(Bs[k0 + t][cb]), to_tf32(Bs[k0 + t + 4][cb])};
+                mma_tf32_16x8x8(acc[j], a, b);
+            }
+        }
+    };
+    // s (q 2^G) h_c
+    const size_t hoff = ((size_t)blockIdx.x * H + h) * (size_t)K * V;
+    for (int d0 = 0; d0 < K; d0 += KS) {
+        __syncthreads();  // the previous slab is consumed
+        for (int idx = tid; idx < C * KS; idx += 256) {
+            const int i = idx / KS, dd = idx % KS;
+            float val = 0.f;
+            if (i < len) {
+                const size_t off = ((size_t)(t0 + i) * H + h) * K + d0 + dd;
+                val = scale * __bfloat162float(q[qk_row(t0 + i, h, H, hr) * K + d0 + dd]) * exp2f(G[off]);
+            }
+            As[i][dd] = val;
+        }
+        for (int idx = tid; idx < KS * (V / 4); idx += 256) {
+            const int dd = idx / (V / 4), c4 = idx % (V / 4);
+            *reinterpret_cast<float4*>(&Bs[dd][4 * c4]) =
+                *reinterpret_cast<const float4*>(hc + hoff + (size_t)(d0 + dd) * V + 4 * c4);
+        }
+        __syncthreads();
+        mma_slab();
+    }
+    // + Aqk v_new (Aqk is zero above the diagonal; both operands are zero past the end)
+    for (int j0 = 0; j0 < C; j0 += KS) {
+        __syncthreads();
+        for (int idx = tid; idx < C * KS; idx += 256) {
+            const int i = idx / KS, jj = idx % KS;
+            As[i][jj] = (i < len) ? Aqk[((size_t)(t0 + i) * H + h) * C + j0 + jj] : 0.f;
+        }
+        for (int idx = tid; idx < KS * (V / 4); idx += 256) {
+            const int jj = idx / (V / 4), c4 = idx % (V / 4);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j0 + jj < len)
+                x = *reinterpret_cast<const float4*>(vn + ((size_t)(t0 + j0 + jj) * H + h) * V + 4 * c4);
+            *reinterpret_cast<float4*>(&Bs[jj][4 * c4]) = x;
+        }
+        __syncthreads();
+        mma_slab();
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int col = c0 + 8 * j + 2 * t;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int i = r0 + g + 8 * half;
+            if (i < len) {
+                OutT* orow = o + ((size_t)(t0 + i) * H + h) * V + col;
+                orow[0] = from_f32<OutT>(acc[j][2 * half] * rs[i]);
+                orow[1] = from_f32<OutT>(acc[j][2 * half + 1] * rs[i]);
+            }
+        }
+    }
+}
+
+template <int C, typename OutT>
+cudaError_t launch_out_tc(const FwdArgs& a, const PreciseWs& ws, const ChunkMap& cm, int slots, int hr) {
+    const dim3 grid(slots, a.H);
+    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
+    OutT* o = (OutT*)a.o;
+    switch (a.V) {
+        case 64:
+            out_tc_kernel<C, 64, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
+                                                                   a.K, a.q_l2norm, o);
+            break;
+        case 128:
+            out_tc_kernel<C, 128, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
+                                                                    a.K, a.q_l2norm, o);
+            break;
+        case 256:
+            out_tc_kernel<C, 256, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
+                                                                    a.K, a.q_l2norm, o);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 template <typename InT, int C>
 cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     ChunkMap cm{a.cu, a.N, a.T, C};
@@ -563,7 +700,11 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
         default:
             return cudaErrorInvalidValue;
     }
-    if (slots > 0) {
+    if (slots > 0 && std::is_same<InT, __nv_bfloat16>::value) {
+        e = a.o_f32 ? launch_out_tc<C, float>(a, ws, cm, slots, hr)
+                    : launch_out_tc<C, __nv_bfloat16>(a, ws, cm, slots, hr);
+        if (e != cudaSuccess) return e;
+    } else if (slots > 0) {
         if (a.o_f32)
             out_kernel<InT, float, C><<<dim3(slots, a.H), a.V, 0, a.stream>>>(
                 q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr, a.K, a.V, a.q_l2norm, (float*)a.o);
