@@ -532,7 +532,8 @@ __global__ void __launch_bounds__(256) out_kernel(const InT* __restrict__ q,
 // 16 (w % WM) .. and the V / WN columns from (w / WM) V / WN on, as NT tiles of 8 columns.
 // The K (then C) dimension goes through shared memory in slabs of KS: rows of s q 2^G (then
 // of Aqk) and rows of h_c (then of v_new, zero past the end of the chunk, where it may hold
-// anything).  Fragments (g = lane / 4, t = lane % 4): a = A[g][t], A[g+8][t], A[g][t+4],
+// anything).  The h_c slabs are double-buffered: slab s + 1 is copied asynchronously while
+// the MMAs of slab s run.  Fragments (g = lane / 4, t = lane % 4): a = A[g][t], A[g+8][t], A[g][t+4],
 // A[g+8][t+4]; b = B[t][g], B[t+4][g]; c = C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1].
 // The padded row lengths make both fragment loads hit 32 different banks.
 template <int C, int V, typename OutT>
@@ -546,9 +547,10 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
     using namespace sm100;
     constexpr int WM = C / 16, WN = 8 / WM, NT = V / (8 * WN), KS = 32;
     constexpr int LA = KS + 4, LB = V + 8;
-    __shared__ __align__(16) float As[C][LA];
-    __shared__ __align__(16) float Bs[KS][LB];
-    __shared__ float rs[C];
+    extern __shared__ __align__(16) float out_tc_smem[];
+    float (*As)[LA] = reinterpret_cast<float (*)[LA]>(out_tc_smem);                  // [C][LA]
+    float (*Bb)[KS][LB] = reinterpret_cast<float (*)[KS][LB]>(out_tc_smem + C * LA);  // [2][KS][LB]
+    float* rs = out_tc_smem + C * LA + 2 * KS * LB;                                   // [C]
     int n, t0, len, bos, eos;
     if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
     const int h = blockIdx.y, tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    auto mma_slab = [&]() {
+    auto mma_slab = [&](const float (*Bs)[LB]) {
 #pragma unroll
         for (int k0 = 0; k0 < KS; k0 += 8) {
             const uint32_t a[4] = {to_tf32(As[r0 + g][k0 + t]), to_tf32(As[r0 + g + 8][k0 + t]),
@@ -583,8 +585,18 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
     };
     // s (q 2^G) h_c
     const size_t hoff = ((size_t)blockIdx.x * H + h) * (size_t)K * V;
-    for (int d0 = 0; d0 < K; d0 += KS) {
+    auto load_h = [&](int d0, int buf) {
+        for (int idx = tid; idx < KS * (V / 4); idx += 256) {
+            const int dd = idx / (V / 4), c4 = idx % (V / 4);
+            cp_async16(smem_u32(&Bb[buf][dd][4 * c4]), hc + hoff + (size_t)(d0 + dd) * V + 4 * c4);
+        }
+        cp_async_commit();
+    };
+    load_h(0, 0);
+    for (int d0 = 0, buf = 0; d0 < K; d0 += KS, buf ^= 1) {
         __syncthreads();  // the previous slab is consumed
+        if (d0 + KS < K) load_h(d0 + KS, buf ^ 1);
+        else cp_async_commit();  // an empty group keeps the count below uniform
         for (int idx = tid; idx < C * KS; idx += 256) {
             const int i = idx / KS, dd = idx % KS;
             float val = 0.f;
@@ -594,14 +606,11 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
             }
             As[i][dd] = val;
         }
-        for (int idx = tid; idx < KS * (V / 4); idx += 256) {
-            const int dd = idx / (V / 4), c4 = idx % (V / 4);
-            *reinterpret_cast<float4*>(&Bs[dd][4 * c4]) =
-                *reinterpret_cast<const float4*>(hc + hoff + (size_t)(d0 + dd) * V + 4 * c4);
-        }
+        cp_async_wait_groups<1>();  // this slab's copy (the next one may still be in flight)
         __syncthreads();
-        mma_slab();
+        mma_slab(Bb[buf]);
     }
+    cp_async_wait_groups<0>();
     // + Aqk v_new (Aqk is zero above the diagonal; both operands are zero past the end)
     for (int j0 = 0; j0 < C; j0 += KS) {
         __syncthreads();
@@ -614,10 +623,10 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j0 + jj < len)
                 x = *reinterpret_cast<const float4*>(vn + ((size_t)(t0 + j0 + jj) * H + h) * V + 4 * c4);
-            *reinterpret_cast<float4*>(&Bs[jj][4 * c4]) = x;
+            *reinterpret_cast<float4*>(&Bb[0][jj][4 * c4]) = x;
         }
         __syncthreads();
-        mma_slab();
+        mma_slab(Bb[0]);
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -634,28 +643,25 @@ __global__ void __launch_bounds__(256) out_tc_kernel(const __nv_bfloat16* __rest
     }
 }
 
+template <int C, int V, typename OutT>
+cudaError_t launch_out_tc_v(const FwdArgs& a, const PreciseWs& ws, const ChunkMap& cm, int slots, int hr) {
+    constexpr size_t smem = sizeof(float) * (C * (32 + 4) + 2 * 32 * (V + 8) + C);
+    auto kern = out_tc_kernel<C, V, OutT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(slots, a.H), 256, smem, a.stream>>>((const __nv_bfloat16*)a.q, ws.G, ws.Aqk, ws.hc, ws.vn,
+                                                     cm, a.H, hr, a.K, a.q_l2norm, (OutT*)a.o);
+    return cudaSuccess;
+}
+
 template <int C, typename OutT>
 cudaError_t launch_out_tc(const FwdArgs& a, const PreciseWs& ws, const ChunkMap& cm, int slots, int hr) {
-    const dim3 grid(slots, a.H);
-    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
-    OutT* o = (OutT*)a.o;
     switch (a.V) {
-        case 64:
-            out_tc_kernel<C, 64, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
-                                                                   a.K, a.q_l2norm, o);
-            break;
-        case 128:
-            out_tc_kernel<C, 128, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
-                                                                    a.K, a.q_l2norm, o);
-            break;
-        case 256:
-            out_tc_kernel<C, 256, OutT><<<grid, 256, 0, a.stream>>>(q, ws.G, ws.Aqk, ws.hc, ws.vn, cm, a.H, hr,
-                                                                    a.K, a.q_l2norm, o);
-            break;
-        default:
-            return cudaErrorInvalidValue;
+        case 64: return launch_out_tc_v<C, 64, OutT>(a, ws, cm, slots, hr);
+        case 128: return launch_out_tc_v<C, 128, OutT>(a, ws, cm, slots, hr);
+        case 256: return launch_out_tc_v<C, 256, OutT>(a, ws, cm, slots, hr);
+        default: return cudaErrorInvalidValue;
     }
-    return cudaSuccess;
 }
 
 template <typename InT, int C>
