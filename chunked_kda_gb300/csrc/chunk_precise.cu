@@ -2,9 +2,9 @@
 //
 // This path computes every step in FP32 with FFMA, so it meets float32-input
 // accuracy (tensor-core bf16/tf32 operands would not), and it serves as the
-// stage-by-stage form of the chunked algorithm.  The one exception: with bf16
-// inputs the output step runs its two products on the tensor cores with tf32
-// operands (10-bit mantissa, FP32 accumulation), far inside the bf16-input
+// stage-by-stage form of the chunked algorithm.  The exceptions: with bf16 inputs
+// the WY step and the output step run their products on the tensor cores with
+// tf32 operands (10-bit mantissa, FP32 accumulation), far inside the bf16-input
 // tolerance.  Steps and their sources:
 //   a1 gate + chunk-local log2 cumsum   FLA skill "fla-kda", "Gate modes" and
 //                                       "Safe gate numerical note" (RCP_LN2)
@@ -218,6 +218,92 @@ __global__ void __launch_bounds__(256) scores_anchored_kernel(const InT* __restr
             const float bi = to_f32(beta[(size_t)(t0 + i) * H + h]);
             Akk[off] = (j < i) ? bi * a1[m] : 0.f;
             Aqk[off] = (j <= i) ? scale * a2[m] : 0.f;
+        }
+    }
+}
+
+// a4 for bf16 inputs: [w | u] = T [beta k 2^G | beta v] with m16n8k8 tf32 MMAs (FP32
+// accumulation).  One block of 256 threads per (chunk slot, head); T (rows past the end zero)
+// stays in shared memory and in the A fragments of each warp; the K + V columns go in passes of
+// NB, each staged as rows of beta k 2^G or beta v (zero past the end).  Warp w owns rows
+// 16 (w % WM) .. + 15 and NB / WN columns of each pass.  Fragment layout as in out_tc_kernel.
+template <int C>
+__global__ void __launch_bounds__(256) wu_tc_kernel(const __nv_bfloat16* __restrict__ k,
+                                                    const __nv_bfloat16* __restrict__ v,
+                                                    const __nv_bfloat16* __restrict__ beta,
+                                                    const float* __restrict__ G,
+                                                    const float* __restrict__ Tm, ChunkMap cm, int H,
+                                                    int hr, int K, int V, float* __restrict__ w,
+                                                    float* __restrict__ u) {
+    using namespace sm100;
+    constexpr int WM = C / 16, WN = 8 / WM, NB = 64, NT = NB / (8 * WN);
+    constexpr int LA = C + 4, LB = NB + 8;
+    __shared__ __align__(16) float Ts[C][LA];
+    __shared__ __align__(16) float Xs[C][LB];
+    __shared__ float bs[C];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x, wp = tid >> 5, l = tid & 31;
+    const int g = l >> 2, t = l & 3;
+    const int r0 = 16 * (wp % WM), c0 = (wp / WM) * (NB / WN);
+    for (int idx = tid; idx < C * C; idx += 256) {
+        const int i = idx / C, j = idx % C;
+        Ts[i][j] = (i < len) ? Tm[((size_t)(t0 + i) * H + h) * C + j] : 0.f;
+    }
+    for (int i = tid; i < C; i += 256) bs[i] = (i < len) ? __bfloat162float(beta[(size_t)(t0 + i) * H + h]) : 0.f;
+    __syncthreads();
+    uint32_t a[C / 8][4];
+#pragma unroll
+    for (int ks = 0; ks < C / 8; ++ks) {
+        const int k0 = 8 * ks;
+        a[ks][0] = to_tf32(Ts[r0 + g][k0 + t]);
+        a[ks][1] = to_tf32(Ts[r0 + g + 8][k0 + t]);
+        a[ks][2] = to_tf32(Ts[r0 + g][k0 + t + 4]);
+        a[ks][3] = to_tf32(Ts[r0 + g + 8][k0 + t + 4]);
+    }
+#pragma unroll 1
+    for (int col0 = 0; col0 < K + V; col0 += NB) {  // K is a multiple of NB: no pass straddles it
+        const bool isk = col0 < K;
+        __syncthreads();  // the previous pass is consumed
+        for (int idx = tid; idx < C * NB; idx += 256) {
+            const int j = idx / NB, c = idx % NB;
+            float val = 0.f;
+            if (j < len) {
+                if (isk) {
+                    const size_t off = ((size_t)(t0 + j) * H + h) * K + col0 + c;
+                    val = bs[j] * __bfloat162float(k[qk_row(t0 + j, h, H, hr) * K + col0 + c]) * exp2f(G[off]);
+                } else {
+                    val = bs[j] * __bfloat162float(v[((size_t)(t0 + j) * H + h) * V + (col0 - K) + c]);
+                }
+            }
+            Xs[j][c] = val;
+        }
+        __syncthreads();
+        float acc[NT][4];
+#pragma unroll
+        for (int jt = 0; jt < NT; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks) {
+#pragma unroll
+            for (int jt = 0; jt < NT; ++jt) {
+                const int cb = c0 + 8 * jt + g;
+                const uint32_t b[2] = {to_tf32(Xs[8 * ks + t][cb]), to_tf32(Xs[8 * ks + t + 4][cb])};
+                mma_tf32_16x8x8(acc[jt], a[ks], b);
+            }
+        }
+#pragma unroll
+        for (int jt = 0; jt < NT; ++jt) {
+            const int col = col0 + c0 + 8 * jt + 2 * t;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int i = r0 + g + 8 * half;
+                if (i < len) {
+                    float* dst = isk ? w + ((size_t)(t0 + i) * H + h) * K + col
+                                     : u + ((size_t)(t0 + i) * H + h) * V + (col - K);
+                    dst[0] = acc[jt][2 * half];
+                    dst[1] = acc[jt][2 * half + 1];
+                }
+            }
         }
     }
 }
@@ -686,8 +772,13 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
             scores_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K, ws.Akk,
                                                             ws.Aqk);
         solve_kernel<C><<<g2, C, 0, a.stream>>>(ws.Akk, cm, a.H, ws.Tm);
-        wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, hr, a.K, a.V,
-                                                    ws.w, ws.u);
+        if (std::is_same<InT, __nv_bfloat16>::value)
+            wu_tc_kernel<C><<<g2, 256, 0, a.stream>>>((const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
+                                                      (const __nv_bfloat16*)beta, ws.G, ws.Tm, cm, a.H, hr,
+                                                      a.K, a.V, ws.w, ws.u);
+        else
+            wu_kernel<InT, C><<<g2, 256, 0, a.stream>>>(k, v, beta, ws.G, ws.Tm, cm, a.H, hr, a.K, a.V,
+                                                        ws.w, ws.u);
     }
     dim3 g5(a.V / 32, a.H, a.N);
     switch (a.K) {
