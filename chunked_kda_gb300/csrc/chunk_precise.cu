@@ -3,9 +3,9 @@
 // This path computes every step in FP32 with FFMA, so it meets float32-input
 // accuracy (tensor-core bf16/tf32 operands would not), and it serves as the
 // stage-by-stage form of the chunked algorithm.  The exceptions: with bf16 inputs
-// the WY step and the output step run their products on the tensor cores with
-// tf32 operands (10-bit mantissa, FP32 accumulation), far inside the bf16-input
-// tolerance.  Steps and their sources:
+// the safe gate's scores, the WY step and the output step run their products on
+// the tensor cores with tf32 operands (10-bit mantissa, FP32 accumulation), far
+// inside the bf16-input tolerance.  Steps and their sources:
 //   a1 gate + chunk-local log2 cumsum   FLA skill "fla-kda", "Gate modes" and
 //                                       "Safe gate numerical note" (RCP_LN2)
 //   a2 causal scores Akk, Aqk           Helion PR #3290 "Read only the causal
@@ -304,6 +304,132 @@ __global__ void __launch_bounds__(256) wu_tc_kernel(const __nv_bfloat16* __restr
                     dst[1] = acc[jt][2 * half + 1];
                 }
             }
+        }
+    }
+}
+
+// a2 for the safe gate with bf16 inputs: the anchored products of scores_anchored_kernel as
+// m16n8k8 tf32 MMAs (FP32 accumulation).  Per channel slab of DA: rows k_i 2^(G_i - G_m) and
+// q_i 2^(G_i - G_m) (A operands, anchor m of row i's sub-block), and for each sub-block b the
+// causal columns k_j 2^(G_m(b) - G_j), j < 16 (b + 1) (B operands).  The output tiles of
+// 16 rows x 8 columns are (sub-block b, k or q rows, column tile nt < 2 (b + 1)): 40 for
+// C = 64, dealt round-robin to the eight warps; entries above the diagonal are dropped by
+// selection (never multiplied), the columns right of the causal ones written as zeros.
+// Fragment layout as in out_tc_kernel; the row length DA + 4 keeps both fragment loads on
+// 32 different banks.
+template <int C>
+__global__ void __launch_bounds__(256) scores_tc_kernel(const __nv_bfloat16* __restrict__ q,
+                                                        const __nv_bfloat16* __restrict__ k,
+                                                        const __nv_bfloat16* __restrict__ beta,
+                                                        const float* __restrict__ G, ChunkMap cm,
+                                                        int H, int hr, int K, float* __restrict__ Akk,
+                                                        float* __restrict__ Aqk) {
+    using namespace sm100;
+    constexpr int NB = C / 16, DA = 16, LD = DA + 4;
+    constexpr int NTILE = 2 * NB * (NB + 1), TPW = (NTILE + 7) / 8;
+    __shared__ __align__(16) float krs[C][LD];
+    __shared__ __align__(16) float qrs[C][LD];
+    __shared__ float gsm[C][DA + 1];
+    __shared__ __align__(16) float kcs[NB][C][LD];
+    __shared__ float gm[NB][DA];
+    int n, t0, len, bos, eos;
+    if (!cm.map(blockIdx.x, n, t0, len, bos, eos)) return;
+    const int h = blockIdx.y, tid = threadIdx.x, wp = tid >> 5, l = tid & 31;
+    const int g = l >> 2, t = l & 3;
+    // the warp's tiles T = wp + 8 s: sub-block tb, rows tk (0: k, 1: q), column tile tn
+    int tb[TPW], tk[TPW], tn[TPW];
+#pragma unroll
+    for (int s = 0; s < TPW; ++s) {
+        int rem = wp + 8 * s, b = 0;
+        tb[s] = -1;
+        tk[s] = tn[s] = 0;
+        for (; b < NB; ++b) {
+            const int per = 2 * (b + 1);  // column tiles of sub-block b
+            if (rem < 2 * per) {
+                tb[s] = b;
+                tk[s] = rem / per;
+                tn[s] = rem % per;
+                break;
+            }
+            rem -= 2 * per;
+        }
+    }
+    float acc[TPW][4];
+#pragma unroll
+    for (int s = 0; s < TPW; ++s) acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+    for (int d0 = 0; d0 < K; d0 += DA) {
+        __syncthreads();  // the previous slab is consumed
+        for (int idx = tid; idx < C * DA; idx += 256) {
+            const int i = idx / DA, dd = idx % DA;
+            float kv = 0.f, qv = 0.f, gv = 0.f;
+            if (i < len) {
+                const size_t qo = qk_row(t0 + i, h, H, hr) * K + d0 + dd;
+                kv = __bfloat162float(k[qo]);
+                qv = __bfloat162float(q[qo]);
+                gv = G[((size_t)(t0 + i) * H + h) * K + d0 + dd];
+            }
+            krs[i][dd] = kv;  // raw k until the columns below are built
+            qrs[i][dd] = qv;
+            gsm[i][dd] = gv;
+        }
+        __syncthreads();
+        if (tid < NB * DA) {  // anchors: the sub-block's midpoint row, or its last valid row
+            const int b = tid / DA, dd = tid % DA;
+            gm[b][dd] = (16 * b < len) ? gsm[min(16 * b + 8, len - 1)][dd] : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < NB * C * DA; idx += 256) {
+            const int b = idx / (C * DA), jj = (idx / DA) % C, dd = idx % DA;
+            kcs[b][jj][dd] = (jj < 16 * (b + 1) && jj < len)
+                                 ? krs[jj][dd] * exp2f(gm[b][dd] - gsm[jj][dd]) : 0.f;
+        }
+        __syncthreads();  // the columns have read the raw k rows
+        for (int idx = tid; idx < C * DA; idx += 256) {
+            const int i = idx / DA, dd = idx % DA;
+            const float e = (i < len) ? exp2f(gsm[i][dd] - gm[i / 16][dd]) : 0.f;
+            krs[i][dd] *= e;
+            qrs[i][dd] *= e;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k0 = 0; k0 < DA; k0 += 8) {
+#pragma unroll
+            for (int s = 0; s < TPW; ++s) {
+                if (tb[s] < 0) continue;
+                const float (*A)[LD] = tk[s] ? qrs : krs;
+                const int r = 16 * tb[s], cb = 8 * tn[s] + g;
+                const uint32_t a[4] = {to_tf32(A[r + g][k0 + t]), to_tf32(A[r + g + 8][k0 + t]),
+                                       to_tf32(A[r + g][k0 + t + 4]), to_tf32(A[r + g + 8][k0 + t + 4])};
+                const uint32_t bb[2] = {to_tf32(kcs[tb[s]][cb][k0 + t]), to_tf32(kcs[tb[s]][cb][k0 + t + 4])};
+                mma_tf32_16x8x8(acc[s], a, bb);
+            }
+        }
+    }
+    const float scale = rsqrtf((float)K);
+#pragma unroll
+    for (int s = 0; s < TPW; ++s) {
+        if (tb[s] < 0) continue;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int i = 16 * tb[s] + g + 8 * half;
+            if (i >= len) continue;
+            const float bi = __bfloat162float(beta[(size_t)(t0 + i) * H + h]);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = 8 * tn[s] + 2 * t + e;
+                const float val = acc[s][2 * half + e];
+                const size_t off = ((size_t)(t0 + i) * H + h) * C + j;
+                if (tk[s] == 0) Akk[off] = (j < i) ? bi * val : 0.f;
+                else            Aqk[off] = (j <= i) ? scale * val : 0.f;
+            }
+        }
+    }
+    for (int idx = tid; idx < C * C; idx += 256) {  // right of the causal columns
+        const int i = idx / C, j = idx % C;
+        if (i < len && j >= 16 * (i / 16 + 1)) {
+            const size_t off = ((size_t)(t0 + i) * H + h) * C + j;
+            Akk[off] = 0.f;
+            Aqk[off] = 0.f;
         }
     }
 }
@@ -765,7 +891,11 @@ cudaError_t run(const FwdArgs& a, const PreciseWs& ws) {
     const InT* beta = (const InT*)a.beta;
     if (slots > 0) {
         dim3 g2(slots, a.H);
-        if (a.mode == 1)  // safe gate: bounded decay, anchored products
+        if (a.mode == 1 && std::is_same<InT, __nv_bfloat16>::value)  // safe gate, tensor cores
+            scores_tc_kernel<C><<<g2, 256, 0, a.stream>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
+                                                          (const __nv_bfloat16*)beta, ws.G, cm, a.H, hr, a.K,
+                                                          ws.Akk, ws.Aqk);
+        else if (a.mode == 1)  // safe gate: bounded decay, anchored products
             scores_anchored_kernel<InT, C><<<g2, 256, 0, a.stream>>>(q, k, beta, ws.G, cm, a.H, hr, a.K,
                                                                      ws.Akk, ws.Aqk);
         else
