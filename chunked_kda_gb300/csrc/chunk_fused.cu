@@ -1179,7 +1179,14 @@ static bool split_allowed_from_env() {
     return !(v && strcmp(v, "plain") == 0);
 }
 
+// SMs of the current device; test hook: KDA_TEST_SM_COUNT=<n> plans for n SMs instead (the
+// split schedule is correct for any n, only its balance depends on it), which lets the plan be
+// checked without a device
 static int sm_count() {
+    if (const char* v = getenv("KDA_TEST_SM_COUNT")) {
+        const int n = atoi(v);
+        if (n > 0) return n;
+    }
     static int cached[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {

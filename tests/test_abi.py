@@ -235,3 +235,31 @@ def test_workspace_bytes(lib):
         F32, 4, 4096, 64, 128, 128, 64, 0) > 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 3) == 0  # no such mode
     assert ex(F32, B, T, H, K, V, C, 0, 2) == lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0)
+
+
+def test_split_schedule_plan(lib, monkeypatch):
+    """The two-launch plan for dense fused calls, on a stated SM count (no device needed): it
+    splits only when the last wave of (sequence, head) units is at most half full and the second
+    pieces hold the FP32 state in their output rows (256 bf16 rows, 128 float32 rows)."""
+    f = lib.kda_chunk_fwd_launches
+    SAFE = 1
+
+    def launches(B, T, H, o=BF16, S=152):
+        monkeypatch.setenv("KDA_TEST_SM_COUNT", str(S))
+        return f(BF16, o, B, T, H, 128, 128, 64, 0, SAFE)
+
+    assert launches(2, 720, 114) == 2        # 228 units: the last wave half full
+    assert launches(1, 4096, 160) == 2       # 160 units: 8 in the last wave
+    assert launches(1, 8192, 200) == 2
+    assert launches(4, 4096, 64) == 1        # 256 units: 68 % full, four rounds of pieces
+    assert launches(1, 4096, 152) == 1       # whole waves
+    assert launches(1, 4096, 304) == 1
+    assert launches(1, 4096, 100) == 1       # fewer units than SMs
+    assert launches(2, 320, 114) == 1        # 5 chunks: the second pieces too short
+    assert launches(2, 512, 114) == 1        # 192-token second pieces: too short for bf16 o ...
+    assert launches(2, 512, 114, o=F32) == 2  # ... long enough for a float32 o
+    assert launches(1, 4096, 12, S=8) == 2   # any SM count
+    assert launches(1, 20480, 32, S=8) == 1  # a whole number of waves
+    assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 3, SAFE) == 1  # packed: never split
+    monkeypatch.setenv("KDA_FUSED_SCHEDULE", "plain")
+    assert launches(2, 720, 114) == 1
