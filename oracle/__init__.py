@@ -7,7 +7,7 @@ CPU-baseline leg of ``bench.py`` may import this package.  The product package
 Two independent restatements live here:
 
 * ``kda_oracle.c`` (loaded through ctypes): the token-by-token float64
-  recurrence, the definition every result is judged against.
+  recurrence, the definition every result is checked against.
 * ``chunked.py``: a float64 numpy restatement of the chunked (WY) form that
   exposes the per-chunk intermediates (G, Akk, Aqk, (I+Akk)^-1, w, u, v_new,
   h).  It is pinned to the recurrence by brute force on small inputs.
