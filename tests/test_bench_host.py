@@ -1,0 +1,36 @@
+"""Host arithmetic of bench.py (CPU): the per-head-token algorithmic bytes and flops behind the
+roofline fraction, and the comment-blind code digest that keeps a DRAM-traffic figure tied to
+the kernel source it was captured from."""
+import math
+
+import bench
+
+
+def test_algorithmic_bytes_per_head_token():
+    # bf16 q, k, g (K each) and v (V) in, beta in, o (V) out
+    assert bench.algorithmic_bytes_per_head_token(128, 128) == 3 * 256 + 256 + 2 + 256 == 1282
+    assert bench.algorithmic_bytes_per_head_token(256, 256) == 2562
+    # float32 inputs and gate
+    assert bench.algorithmic_bytes_per_head_token(64, 64, 4, 4) == 4 * (2 * 64 + 64) + 4 * 64 + 4 + 4 * 64
+
+
+def test_algorithmic_flops_per_head_token():
+    # 6KV + 2K(C+16) + CK + CV + (C+1)V + C^2/3: 144,853 / 123,349 / 484,949 as tabulated for
+    # K = V = 128 at C = 64 and 32, and K = V = 256 at C = 64
+    assert math.floor(bench.algorithmic_flops_per_head_token(128, 128, 64)) == 144853
+    assert math.floor(bench.algorithmic_flops_per_head_token(128, 128, 32)) == 123349
+    assert math.floor(bench.algorithmic_flops_per_head_token(256, 256, 64)) == 484949
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void f(float* x) {\n    x[0] = 1.f;  // one\n}\n")
+    d0 = bench.kernel_code_digest(str(src))
+    src.write_text("// a new header line\n__global__ void f(float* x) {\n\n    x[0] = 1.f;  // changed\n}\n")
+    assert bench.kernel_code_digest(str(src)) == d0
+    src.write_text("__global__ void f(float* x) {\n    x[0] = 2.f;\n}\n")
+    assert bench.kernel_code_digest(str(src)) != d0
+
+
+def test_traffic_only_for_its_workload():
+    assert bench.fused_traffic_bytes("dense_bf16_b4_t2048_h16_d128") is None
