@@ -155,6 +155,11 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  * lower-triangular solve T = (I + Akk)^-1; WY terms w = T (beta k 2^G),
  * u = T (beta v); the sequential inter-chunk state scan; the output
  * o = (1/sqrt(K)) (q 2^G) h + Aqk v_new.
+ * Paths: bf16 inputs with K = V = 128 and a pre-gated or safe gate run the
+ * fused tensor-core kernel (one launch, or two for the split schedule below);
+ * everything else runs the stage-by-stage path (six launches, a workspace),
+ * which computes in FP32 except that with bf16 inputs the safe-gate scores, the
+ * WY terms and the output are tf32 tensor-core products with FP32 accumulation.
  *
  *   q, k       [B, T, H, K], dtype qkv_dtype; rows are used as given
  *   v          [B, T, H, V], dtype qkv_dtype
