@@ -156,7 +156,8 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  * u = T (beta v); the sequential inter-chunk state scan; the output
  * o = (1/sqrt(K)) (q 2^G) h + Aqk v_new.
  * Paths: bf16 inputs with K = V = 128 and a pre-gated or safe gate run the
- * fused tensor-core kernel (one launch, or two for the split schedule below);
+ * fused tensor-core kernel (one launch, or two for the split schedule described
+ * with kda_chunk_fwd_launches);
  * everything else runs the stage-by-stage path (six launches, a workspace),
  * which computes in FP32 except that with bf16 inputs the safe-gate scores, the
  * WY terms and the output are tf32 tensor-core products with FP32 accumulation.
