@@ -263,3 +263,23 @@ def test_split_schedule_plan(lib, monkeypatch):
     assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 3, SAFE) == 1  # packed: never split
     monkeypatch.setenv("KDA_FUSED_SCHEDULE", "plain")
     assert launches(2, 720, 114) == 1
+
+
+def test_layout_and_alignment_validation(lib):
+    """The remaining host checks of the layout, the packed offsets, the workspace and the gate
+    entry point: each is reported before any launch."""
+    assert _chunk(lib, B=1, T=1 << 30, H=1 << 11) == INVALID  # more than 2^40 elements
+    assert b"too large" in lib.kda_last_error()
+    assert _chunk(lib, B=65536, T=1) == INVALID
+    assert b"65535" in lib.kda_last_error()
+    assert _chunk(lib, cu=P, n=65536, B=1) == INVALID
+    assert _chunk(lib, cu=ctypes.c_void_p(4098), n=2, B=1) == INVALID
+    assert b"misaligned" in lib.kda_last_error()
+    need = lib.kda_chunk_workspace_bytes(F32, 1, 64, 2, 128, 128, 64, 0)
+    assert need > 0
+    assert _chunk(lib, dt=F32, gdt=F32, ws=ctypes.c_void_p(4096 + 16), ws_bytes=need) == INVALID
+    assert b"256-byte" in lib.kda_last_error()
+    assert lib.kda_gate_fwd(None, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, P, None) == INVALID
+    assert lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, None, None) == INVALID
+    assert b"null g" in lib.kda_last_error()
+    assert lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 0, 64, P, None) == INVALID
