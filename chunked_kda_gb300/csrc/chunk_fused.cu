@@ -74,45 +74,48 @@ constexpr uint32_t BAR_INV = 3;                  // prep warps 0-3 (inverse)
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_V = 0;          // v tile (TMA), 16 KB; MN-major A of v^T          [chain]
-constexpr uint32_t OFF_GT = 16384;     // g tile (TMA, bf16 gate only), 16 KB               [prep]
-constexpr uint32_t OFF_SAH = 32768;    // score rows hi [128 ch][128 rows] MN-major (k rows 0-63,
+constexpr uint32_t OFF_SAH = 16384;    // score rows [128 ch][128 rows] MN-major bf16 (k rows 0-63,
                                        //   q rows 64-127; 16 KB each)                      [prep]
-constexpr uint32_t OFF_SALQ = 65536;   // score rows lo of the q rows [128 ch][64 rows], 16 KB
-constexpr uint32_t OFF_SB = 81920;     // score cols [128 ch][160] MN-major, 3 groups of 64 columns
+constexpr uint32_t OFF_SB = 49152;     // score cols [128 ch][160] MN-major, 3 groups of 64 columns
                                        //   (16 KB each), 48 KB
-constexpr uint32_t OFF_AS = 32768;     //   after the score MMA: Akk^T fp32 [64][68]
-constexpr uint32_t OFF_TF = 50176;     //   T fp32 [64][68]
-constexpr uint32_t OFF_XS = 67584;     //   block products fp32 [4][16][24]
-constexpr uint32_t OFF_GS = 73728;     //   the next chunk's G fp32 [64 rows][128 ch]
-constexpr uint32_t OFF_KG = 131072;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_AS = 16384;     //   after the score MMA: Akk^T fp32 [64][68]
+constexpr uint32_t OFF_TF = 33792;     //   T fp32 [64][68]
+constexpr uint32_t OFF_XS = 51200;     //   block products fp32 [4][16][24]
+constexpr uint32_t OFF_GS = 57344;     //   the next chunk's G fp32 [64 rows][128 ch]
+constexpr uint32_t OFF_KG = 98304;     // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
-constexpr uint32_t OFF_QG = 147456;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_QG = 114688;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's q tile (TMA)
-constexpr uint32_t OFF_KD = 163840;    // hand-off: k 2^(Gl-G)  [128 ch][64 tok] K-major B
-constexpr uint32_t OFF_TP = 180224;    // hand-off: T diag(beta) bf16 [64][64] K-major B
-constexpr uint32_t OFF_AQKH = 188416;  // hand-off: Aqk hi [64][64]
-constexpr uint32_t OFF_AQKL = 196608;  // hand-off: Aqk lo [64][64]
-constexpr uint32_t OFF_GAM = 204800;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
-constexpr uint32_t OFF_BETA = 205824;  // prep: beta fp32 [2 chunks][64]
-constexpr uint32_t OFF_GCARRY = 206336;  // chain: fp32 [3][128] gate sums of row quarters 0-2
-constexpr uint32_t OFF_GM = 208128;    // prep: fp32 [4][128] G at the sub-block midpoints
-constexpr uint32_t OFF_GL = 210176;    // prep: fp32 [128] G at the last row
-constexpr uint32_t OFF_BAR = 210688;   // mbarriers (8 bytes each)
-constexpr uint32_t OFF_MISC = 210800;  // tmem base, abort flag, TMA loads issued (qk, v, g)
-constexpr uint32_t OFF_QSS = 211072;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
-constexpr uint32_t OFF_KD1 = 212992;   // hand-off: k 2^(Gl-G) of the odd chunks (OFF_KD: the even)
-constexpr uint32_t SMEM_BYTES = 229376 + 1024;  // + alignment slack
+constexpr uint32_t OFF_KD = 131072;    // hand-off: k 2^(Gl-G) fp32 [128 ch][64 tok] K-major B in two
+                                       //   32-token halves of 16 KB; even chunks here, odd chunks
+constexpr uint32_t OFF_KD1 = 163840;   //   here
+constexpr uint32_t OFF_TP = 196608;    // hand-off: T diag(beta) bf16 [64][64] K-major B
+constexpr uint32_t OFF_AQK = 204800;   // hand-off: Aqk fp32 [64 i][64 j] K-major B in two
+                                       //   32-column halves of 8 KB
+constexpr uint32_t OFF_GAM = 221184;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
+constexpr uint32_t OFF_BETA = 222208;  // prep: beta fp32 [2 chunks][64]
+constexpr uint32_t OFF_GCARRY = 222720;  // chain: fp32 [3][128] gate sums of row quarters 0-2
+constexpr uint32_t OFF_GM = 224256;    // prep: fp32 [4][128] G at the sub-block midpoints
+constexpr uint32_t OFF_GL = 226304;    // prep: fp32 [128] G at the last row
+constexpr uint32_t OFF_BAR = 226816;   // mbarriers (8 bytes each)
+constexpr uint32_t OFF_MISC = 226928;  // tmem base, abort flag, TMA loads issued (qk, v)
+constexpr uint32_t OFF_QSS = 226976;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
+constexpr uint32_t SMEM_BYTES = 228000 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_GS, "layout");
-static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG, "layout");
+static_assert(OFF_AS + 64 * 68 * 4 <= OFF_TF && OFF_TF + 64 * 68 * 4 <= OFF_XS, "layout");
+static_assert(OFF_GS + 64 * 128 * 4 <= OFF_SB + 3 * 16384, "layout");
+static_assert(OFF_KD + 32768 <= OFF_KD1 && OFF_KD1 + 32768 <= OFF_TP && OFF_TP + 8192 <= OFF_AQK, "layout");
+static_assert(OFF_AQK + 16384 <= OFF_GAM && OFF_GAM + 1024 <= OFF_BETA, "layout");
 static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 3 * 128 * 4 <= OFF_GM, "layout");
-static_assert(OFF_QSS + 1024 <= OFF_KD1 && OFF_KD1 % 1024 == 0, "layout");
+static_assert(OFF_GM + 4 * 128 * 4 <= OFF_GL && OFF_GL + 128 * 4 <= OFF_BAR, "layout");
+static_assert(OFF_QSS + 1024 <= 228000 && OFF_KD % 1024 == 0 && OFF_AQK % 1024 == 0, "layout");
 constexpr int LD = 68;                 // fp32 row stride of the solve matrices (mma fragments
                                        // of 8 rows x 4 columns then touch 32 distinct banks)
 
 // mbarriers (each completes once per chunk, the v tiles once per two chunks)
 enum {
-    B_VFULL = 0, B_QKIN, B_GIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
+    B_VFULL = 0, B_QKIN, B_KQFULL, B_RESTFULL, B_SCORE, B_YDONE, B_VNDONE, B_OHDONE,
     B_DRAIN0, B_DRAIN1, B_GATE, B_STALL, NBAR
 };
 static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC && OFF_MISC + 32 <= OFF_QSS, "mbarriers");
@@ -349,8 +352,9 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 }
                 float kf0[8], kf1[8];  // k 2^(G_m(rq) - G) of the 8 rows
                 {
-                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4], lq0[4], lq1[4];
-                    uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4], kd0[4], kd1[4];
+                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
+                    uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4];
+                    float kd0[8], kd1[8];
 #pragma unroll
                     for (int pr = 0; pr < 4; ++pr) {
                         float ke0[2], ke1[2], qe0[2], qe1[2];
@@ -364,32 +368,40 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                             ke1[u] = kv1 * e1;
                             qe0[u] = scale * bf_0(qrh[i]) * e0;
                             qe1[u] = scale * bf_1(qrh[i]) * e1;
-                            kf0[2 * pr + u] = kv0 * f0;
-                            kf1[2 * pr + u] = kv1 * f1;
+                            kf0[i] = kv0 * f0;
+                            kf1[i] = kv1 * f1;
+                            kd0[i] = kf0[i] * L0;
+                            kd1[i] = kf1[i] * L1;
                         }
                         ak0[pr] = pack_bf16(ke0[0], ke0[1]);
                         ak1[pr] = pack_bf16(ke1[0], ke1[1]);
-                        pack_split(qe0[0], qe0[1], aq0[pr], lq0[pr]);
-                        pack_split(qe1[0], qe1[1], aq1[pr], lq1[pr]);
+                        aq0[pr] = pack_bf16(qe0[0], qe0[1]);
+                        aq1[pr] = pack_bf16(qe1[0], qe1[1]);
                         g_k0[pr] = pack_bf16(ke0[0] * P0, ke0[1] * P0);
                         g_k1[pr] = pack_bf16(ke1[0] * P1, ke1[1] * P1);
                         g_q0[pr] = pack_bf16(qe0[0] * P0, qe0[1] * P0);
                         g_q1[pr] = pack_bf16(qe1[0] * P1, qe1[1] * P1);
-                        kd0[pr] = pack_bf16(kf0[2 * pr] * L0, kf0[2 * pr + 1] * L0);
-                        kd1[pr] = pack_bf16(kf1[2 * pr] * L1, kf1[2 * pr + 1] * L1);
                     }
                     st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
                     st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
                     st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
                     st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
-                    st_s128(sb + OFF_SALQ + r0, lq0[0], lq0[1], lq0[2], lq0[3]);
-                    st_s128(sb + OFF_SALQ + r1, lq1[0], lq1[1], lq1[2], lq1[3]);
                     st_s128(sb + OFF_KG + r0, g_k0[0], g_k0[1], g_k0[2], g_k0[3]);
                     st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
                     st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
                     st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
-                    st_s128(kd_buf + r0, kd0[0], kd0[1], kd0[2], kd0[3]);
-                    st_s128(kd_buf + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
+                    // k 2^(Gl - G) in fp32: the 8 tokens 16 rq + 8 half .. + 7 of a channel are two
+                    // 16-byte chunks of the channel's row in the 32-token half rq / 2
+                    const uint32_t kdh = kd_buf + (uint32_t)(rq >> 1) * 16384u;
+                    const uint32_t kc = (uint32_t)(4 * (rq & 1) + 2 * half);
+                    st_s128(kdh + sw128(ch0, kc), __float_as_uint(kd0[0]), __float_as_uint(kd0[1]),
+                            __float_as_uint(kd0[2]), __float_as_uint(kd0[3]));
+                    st_s128(kdh + sw128(ch0, kc + 1), __float_as_uint(kd0[4]), __float_as_uint(kd0[5]),
+                            __float_as_uint(kd0[6]), __float_as_uint(kd0[7]));
+                    st_s128(kdh + sw128(ch1, kc), __float_as_uint(kd1[0]), __float_as_uint(kd1[1]),
+                            __float_as_uint(kd1[2]), __float_as_uint(kd1[3]));
+                    st_s128(kdh + sw128(ch1, kc + 1), __float_as_uint(kd1[4]), __float_as_uint(kd1[5]),
+                            __float_as_uint(kd1[6]), __float_as_uint(kd1[7]));
                 }
                 // score columns, channel-major [128 ch][n] in groups of 64 columns: sub-block
                 // bi >= rq sees row r as column n = sb_off(bi) + r with anchor m_bi:
@@ -415,20 +427,16 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         tc_fence_before();
         bar_sync(BAR_PREP, NGRP);
 
-        // ---- a2: score MMA against the causal columns: rows hi, then the q rows' lo with the
-        // k rows' hi a second time (the k-row scores come out doubled, exactly; the lo part of
-        // the k rows is below the accuracy the path needs).  k 2^G, s q 2^G, k 2^(Gl - G) and
-        // 2^Glast handed off
+        // ---- a2: score MMA against the causal columns (k rows and q rows in one M = 128 tile).
+        // k 2^G, s q 2^G, k 2^(Gl - G) and 2^Glast handed off
         if (tid == 0 && !sy.aborted()) {
             tc_fence_after();
             const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint64_t b = desc_at(umma_desc(sb + OFF_SB, 16384, 1024), kk * 2048);
-                uint64_t ah = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
-                uint64_t al = desc_at(umma_desc(sb + OFF_SAH, OFF_SALQ - OFF_SAH, 1024), kk * 2048);
-                umma_bf16(tmem + TM_S, ah, b, id_s, kk > 0);
-                umma_bf16(tmem + TM_S, al, b, id_s, 1);
+                uint64_t a = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
+                umma_bf16(tmem + TM_S, a, b, id_s, kk > 0);
             }
             umma_commit(sy.bar(B_SCORE));
             mbar_arrive(sy.bar(B_KQFULL));
@@ -444,8 +452,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 
         // ---- read the scores, all eight warps: warps w and w + 4 share the TMEM lanes of
         // quadrant w & 3 and take alternate 16-column pieces of each row.  Akk rows (lanes
-        // 0-63: beta-scaled, strictly lower) go into the solve matrix, Aqk rows (lanes 64-127:
-        // hi, lo) straight into the hand-off buffers.
+        // 0-63: beta-scaled, strictly lower) go into the solve matrix, Aqk rows (lanes 64-127)
+        // straight into the fp32 hand-off tile.
         {
             const int lq = w & 3, part = w >> 2;
             const int row = 32 * lq + l;  // TMEM lane
@@ -456,7 +464,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             // the piece of both (warp-collective loads), every lane keeps its own
             const int bmin = 2 * (lq & 1);
             const bool own_a = bi == bmin;
-            const float b_i = 0.5f * bcur[i];  // the k-row scores are doubled
+            const float b_i = bcur[i];
             const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16) + TM_S;
 #pragma unroll 1
             for (int tt = 0; tt < 2; ++tt) {
@@ -479,18 +487,18 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         }
                     }
                 } else {
+                    // columns 16 t .. 16 t + 15 of row i: four 16-byte chunks of the row in the
+                    // 32-column half t / 2 of the K-major tile
+                    const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        uint32_t hi[4], lo[4];
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t x[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int j0 = 16 * t + 8 * c2 + 2 * e;
-                            const float x0 = (j0 <= i) ? sv[8 * c2 + 2 * e] : 0.f;
-                            const float x1 = (j0 + 1 <= i) ? sv[8 * c2 + 2 * e + 1] : 0.f;
-                            pack_split(x0, x1, hi[e], lo[e]);
+                            const int j = 16 * t + 4 * c4 + e;
+                            x[e] = __float_as_uint((j <= i) ? sv[4 * c4 + e] : 0.f);
                         }
-                        st_s128(sb + OFF_AQKH + sw128(i, 2 * t + c2), hi[0], hi[1], hi[2], hi[3]);
-                        st_s128(sb + OFF_AQKL + sw128(i, 2 * t + c2), lo[0], lo[1], lo[2], lo[3]);
+                        st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
                     }
                 }
             }
@@ -712,7 +720,8 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     // the totals of the ones before them (one exchange).  Chunk 0 runs before the loop,
     // chunk c + 1 while the chain waits for the prep group to finish chunk c, in a part of
     // the score operand area that the prep group's inverse leaves free.
-    constexpr bool kGateTile = std::is_same<GT, __nv_bfloat16>::value;  // g arrives by TMA
+    constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
+    using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;  // a channel pair
     const GT* gptr = reinterpret_cast<const GT*>(p.g);
     const int gq = ct >> 6, gc0 = 2 * (ct & 63);  // row quarter, first channel of the pair
     const float lbl2 = p.lb * kLog2e;
@@ -741,67 +750,55 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     // TMA loads issued per barrier, counted by their one issuing thread (ct == 0) in shared
     // memory (a register count would stay live across the whole loop)
     volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC) + 2;
-    if (ct == 0) issued[0] = issued[1] = issued[2] = 0u;
-    auto load_gtile = [&](long t) {
-        issued[2] = issued[2] + 1u;
-        mbar_arrive_expect_tx(sy.bar(B_GIN), 16384);
-        for (int cb = 0; cb < 2; ++cb)
-            tma_load_3d(sb + OFF_GT + cb * 8192, tm_g, 64 * cb, h, (int)t, sy.bar(B_GIN));
+    if (ct == 0) issued[0] = issued[1] = 0u;
+    // the g rows of chunk cn towards L2 (bf16 gate: the TMA map; the loads below then hit L2)
+    auto prefetch_g = [&](int cn) {
+        if constexpr (kGateBf16) {
+            const long t = bos + (long)cn * C;
+            for (int cb = 0; cb < 2; ++cb) tma_prefetch_l2_3d(tm_g, 64 * cb, h, (int)t);
+        }
     };
     // score_chunk >= 0: the score MMA of that chunk must have read its operands first
     auto gate_chunk = [&](int cn, int score_chunk) {
         const long tc0 = bos + (long)cn * C;
         const int lenc = (int)min((long)C, eos - tc0);
-        if (w == 8) {
-            if (score_chunk >= 0) sy.wait(B_SCORE, (uint32_t)(score_chunk & 1));
-            if (kGateTile) sy.wait(B_GIN, (uint32_t)(cn & 1));
-        }
-        bar_sync(BAR_CHAIN, NGRP);
-        // compact (rolled) loops: this runs once per chunk next to the prep group's code, and
-        // instruction fetch is a shared limit of the SM
         const int r0 = 16 * gq;
-        const uint32_t base = sb + OFF_GT + (uint32_t)(gc0 >> 6) * 8192u + (uint32_t)(gc0 & 6) * 2u;
-        const uint32_t chunk = (uint32_t)((gc0 & 63) >> 3);
+        // the thread's 16 rows of its channel pair, every load issued before the wait (rows past
+        // the end of the sequence read its last row and are masked below)
+        GW gw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            gw[i] = __ldg(reinterpret_cast<const GW*>(
+                gptr + ((size_t)(tc0 + min(r0 + i, lenc - 1)) * H + h) * KD + gc0));
+        if (ct == 0 && cn + 1 < nt) prefetch_g(cn + 1);
+        if (w == 8 && score_chunk >= 0) sy.wait(B_SCORE, (uint32_t)(score_chunk & 1));
+        bar_sync(BAR_CHAIN, NGRP);
         const float m = (p.mode == 1) ? lbl2 : kLog2e;  // per-token factor into log2 units
         float acc0 = 0.f, acc1 = 0.f;
         float2* grow = reinterpret_cast<float2*>(gs + r0 * KD + gc0);
-#pragma unroll 1
-        for (int i0 = 0; i0 < 16; i0 += 4) {
-            float a0[4], a1[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if constexpr (kGateTile) {
-                    // the pair's word in row r of the token-major [64][128] tile
-                    const uint32_t x = ld_s32(base + sw128((uint32_t)(r0 + i0 + i), chunk));
-                    a0[i] = bf_lo(x);
-                    a1[i] = bf_hi(x);
-                } else {
-                    const float2 v2 = __ldg(reinterpret_cast<const float2*>(
-                        gptr + ((size_t)(tc0 + min(r0 + i0 + i, lenc - 1)) * H + h) * KD + gc0));
-                    a0[i] = v2.x;
-                    a1[i] = v2.y;
-                }
+        for (int i = 0; i < 16; ++i) {
+            float a0, a1;
+            if constexpr (kGateBf16) {
+                a0 = bf_lo(gw[i]);
+                a1 = bf_hi(gw[i]);
+            } else {
+                a0 = gw[i].x;
+                a1 = gw[i].y;
             }
             if (p.mode == 1) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    a0[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0[i], nAd0)));
-                    a1[i] = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1[i], nAd1)));
-                }
+                a0 = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0, nAd0)));
+                a1 = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1, nAd1)));
             }
             // rows past the end add zero (selected, so that NaN padding there does not spread);
             // the partial sums of the quarter are stored now and carried below
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool valid = r0 + i0 + i < lenc;
-                acc0 = fmaf(m, valid ? a0[i] : 0.f, acc0);
-                acc1 = fmaf(m, valid ? a1[i] : 0.f, acc1);
-                grow[(i0 + i) * (KD / 2)] = make_float2(acc0, acc1);
-            }
+            const bool valid = r0 + i < lenc;
+            acc0 = fmaf(m, valid ? a0 : 0.f, acc0);
+            acc1 = fmaf(m, valid ? a1 : 0.f, acc1);
+            grow[i * (KD / 2)] = make_float2(acc0, acc1);
         }
         if (gq < 3) *reinterpret_cast<float2*>(gcarry + gq * KD + gc0) = make_float2(acc0, acc1);
-        bar_sync(BAR_CHAIN, NGRP);  // quarter totals out; every thread has read the tile
-        if (kGateTile && ct == 0 && cn + 1 < nt && !sy.aborted()) load_gtile(tc0 + C);
+        bar_sync(BAR_CHAIN, NGRP);  // quarter totals out
         float cy0 = 0.f, cy1 = 0.f;
         for (int q = 0; q < gq; ++q) {
             const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * KD + gc0);
@@ -856,7 +853,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         }
         tmem_wait_st();
         if (ct == 0) {
-            if (kGateTile) load_gtile(bos);
+            prefetch_g(0);
             load_qk(bos);
             load_v(bos);
         }
@@ -954,38 +951,20 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         sy.group_wait(B_VNDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);  // the v tile is free again
-        // ---- v_new^T -> (hi, lo) bf16 A operands in the Y^T columns
-        {
-            float x[32];
-            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch, x);
-            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch + 16, x + 16);
-            tmem_wait_ld();
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) pack_split(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
-            tmem_st16(tmem + lane_base + TM_Y + 16 * hch, hi);
-            tmem_st16(tmem + lane_base + TM_Y + 32 + 16 * hch, lo);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        bar_sync(BAR_CHAIN, NGRP);
-        // ---- o^T += v_new^T Aqk^T (hi*hi + lo*hi + hi*lo); h^T += v_new^T kd (hi + lo)
+        // ---- o^T += v_new^T Aqk^T; h^T += v_new^T kd: tf32 MMAs whose A operand is the FP32
+        // v_new^T accumulator itself (K = 8 tokens per instruction)
         if (ct == 0 && !sy.aborted()) {
-            tc_fence_after();
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);
-            const uint32_t id_h = idesc_bf16(128, 128, 0, 0);
+            const uint32_t id_o = idesc_tf32(128, 64);
+            const uint32_t id_h = idesc_tf32(128, 128);
             const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t ah = tmem + TM_Y + 8 * kk, al = tmem + TM_Y + 32 + 8 * kk;
-                uint64_t boh = desc_at(umma_desc(sb + OFF_AQKH, 16, 1024), kk * 32);
-                uint64_t bol = desc_at(umma_desc(sb + OFF_AQKL, 16, 1024), kk * 32);
-                uint64_t bk = desc_at(umma_desc(kd_buf, 16, 1024), kk * 32);
-                umma_bf16_ta(tmem + TM_O, ah, boh, id_o, 1);
-                umma_bf16_ta(tmem + TM_O, al, boh, id_o, 1);
-                umma_bf16_ta(tmem + TM_O, ah, bol, id_o, 1);
-                umma_bf16_ta(tmem + TM_H, ah, bk, id_h, 1);
-                umma_bf16_ta(tmem + TM_H, al, bk, id_h, 1);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t a = tmem + TM_VN + 8 * kk;
+                const uint32_t koff = (uint32_t)(kk & 3) * 32u;
+                uint64_t bo = desc_at(umma_desc(sb + OFF_AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024), koff);
+                uint64_t bk = desc_at(umma_desc(kd_buf + (uint32_t)(kk >> 2) * 16384u, 16, 1024), koff);
+                umma_tf32_ta(tmem + TM_O, a, bo, id_o, 1);
+                umma_tf32_ta(tmem + TM_H, a, bk, id_h, 1);
             }
             umma_commit(sy.bar(B_OHDONE));
         }
@@ -1052,9 +1031,9 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     // (bounded) for the last load of each kind (before an abort every load is consumed before
     // the next is issued, after it none is issued, so at most the last one can be in flight).
     if (ct == 0 && sy.aborted()) {
-        for (int b = 0; b < 3; ++b) {
+        for (int b = 0; b < 2; ++b) {
             const uint32_t n = issued[b];
-            if (n > 0) mbar_wait(sy.bar(b == 0 ? B_QKIN : b == 1 ? B_VFULL : B_GIN), (n - 1u) & 1u);
+            if (n > 0) mbar_wait(sy.bar(b == 0 ? B_QKIN : B_VFULL), (n - 1u) & 1u);
         }
     }
 }
