@@ -81,14 +81,13 @@ constexpr uint32_t OFF_SB = 49152;     // score cols [128 ch][160] MN-major, 3 g
 constexpr uint32_t OFF_AS = 16384;     //   after the score MMA: Akk^T fp32 [64][68]
 constexpr uint32_t OFF_TF = 33792;     //   T fp32 [64][68]
 constexpr uint32_t OFF_XS = 51200;     //   block products fp32 [4][16][24]
-constexpr uint32_t OFF_GS = 57344;     //   the next chunk's G fp32 [64 rows][128 ch]
-constexpr uint32_t OFF_KG = 98304;     // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_GS = 98304;     // G fp32 [64 rows][128 ch] of the chunk the prep group reads next
+constexpr uint32_t OFF_KG = 131072;    // hand-off: k 2^G       [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's k tile (TMA)
-constexpr uint32_t OFF_QG = 114688;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
+constexpr uint32_t OFF_QG = 147456;    // hand-off: s q 2^G     [128 ch][64 tok] MN-major B;
                                        //   before that, the next chunk's q tile (TMA)
-constexpr uint32_t OFF_KD = 131072;    // hand-off: k 2^(Gl-G) fp32 [128 ch][64 tok] K-major B in two
-                                       //   32-token halves of 16 KB; even chunks here, odd chunks
-constexpr uint32_t OFF_KD1 = 163840;   //   here
+constexpr uint32_t OFF_KD = 163840;    // hand-off: k 2^(Gl-G) bf16 [128 ch][64 tok] K-major B, even
+constexpr uint32_t OFF_KD1 = 180224;   //   chunks here, odd chunks here
 constexpr uint32_t OFF_TP = 196608;    // hand-off: T diag(beta) bf16 [64][64] K-major B
 constexpr uint32_t OFF_AQK = 204800;   // hand-off: Aqk fp32 [64 i][64 j] K-major B in two
                                        //   32-column halves of 8 KB
@@ -102,10 +101,10 @@ constexpr uint32_t OFF_MISC = 226928;  // tmem base, abort flag, TMA loads issue
 constexpr uint32_t OFF_QSS = 226976;   // hand-off: sums of q^2 per row fp32 [2 chunks][2 halves][64]
 constexpr uint32_t SMEM_BYTES = 228000 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
-static_assert(OFF_SB + 3 * 16384 <= OFF_KG && OFF_XS + 4 * 16 * 24 * 4 <= OFF_GS, "layout");
+static_assert(OFF_SB + 3 * 16384 <= OFF_GS && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB + 3 * 16384, "layout");
 static_assert(OFF_AS + 64 * 68 * 4 <= OFF_TF && OFF_TF + 64 * 68 * 4 <= OFF_XS, "layout");
-static_assert(OFF_GS + 64 * 128 * 4 <= OFF_SB + 3 * 16384, "layout");
-static_assert(OFF_KD + 32768 <= OFF_KD1 && OFF_KD1 + 32768 <= OFF_TP && OFF_TP + 8192 <= OFF_AQK, "layout");
+static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG, "layout");
+static_assert(OFF_KD + 16384 <= OFF_KD1 && OFF_KD1 + 16384 <= OFF_TP && OFF_TP + 8192 <= OFF_AQK, "layout");
 static_assert(OFF_AQK + 16384 <= OFF_GAM && OFF_GAM + 1024 <= OFF_BETA, "layout");
 static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 3 * 128 * 4 <= OFF_GM, "layout");
 static_assert(OFF_GM + 4 * 128 * 4 <= OFF_GL && OFF_GL + 128 * 4 <= OFF_BAR, "layout");
@@ -131,6 +130,10 @@ constexpr uint32_t TM_S = 352;   // scores [128][160]                           
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_S + 160 <= TM_COLS && TM_YA + 32 <= TM_S, "TMEM map");
 constexpr int SB_ROWS = 160;                                                   // causal columns
+// byte offset of the 16-byte chunk q (rows 4 q .. 4 q + 3) of channel ch in the channel-major G
+__host__ __device__ constexpr uint32_t gs_off(int ch, int q) {
+    return (uint32_t)ch * 256u + ((uint32_t)(q ^ (ch & 7)) << 4);
+}
 __host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -243,7 +246,6 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel1)); };
     const float scale = rsqrtf((float)KD);
     const uint32_t sw_d0 = (uint32_t)((d0 & 63) >> 3), sw_b0 = (uint32_t)(d0 & 7) * 2;
-    const float* Gs = reinterpret_cast<const float*>(smem + OFF_GS);
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
 
@@ -285,9 +287,13 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             const uint32_t off = tile_off(16 * rq + i);
             kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
             qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
-            const float2 gv = *reinterpret_cast<const float2*>(Gs + (16 * rq + i) * KD + d0);
-            G0[i] = swap ? gv.y : gv.x;
-            G1[i] = swap ? gv.x : gv.y;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch0, 4 * rq + k));
+            const float4 b = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch1, 4 * rq + k));
+            G0[4 * k] = a.x; G0[4 * k + 1] = a.y; G0[4 * k + 2] = a.z; G0[4 * k + 3] = a.w;
+            G1[4 * k] = b.x; G1[4 * k + 1] = b.y; G1[4 * k + 2] = b.z; G1[4 * k + 3] = b.w;
         }
         bar_sync(BAR_PREP, NGRP);
 
@@ -354,7 +360,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 {
                     uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
                     uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4];
-                    float kd0[8], kd1[8];
+                    uint32_t kd0[4], kd1[4];
 #pragma unroll
                     for (int pr = 0; pr < 4; ++pr) {
                         float ke0[2], ke1[2], qe0[2], qe1[2];
@@ -370,8 +376,6 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                             qe1[u] = scale * bf_1(qrh[i]) * e1;
                             kf0[i] = kv0 * f0;
                             kf1[i] = kv1 * f1;
-                            kd0[i] = kf0[i] * L0;
-                            kd1[i] = kf1[i] * L1;
                         }
                         ak0[pr] = pack_bf16(ke0[0], ke0[1]);
                         ak1[pr] = pack_bf16(ke1[0], ke1[1]);
@@ -381,6 +385,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         g_k1[pr] = pack_bf16(ke1[0] * P1, ke1[1] * P1);
                         g_q0[pr] = pack_bf16(qe0[0] * P0, qe0[1] * P0);
                         g_q1[pr] = pack_bf16(qe1[0] * P1, qe1[1] * P1);
+                        kd0[pr] = pack_bf16(kf0[2 * pr] * L0, kf0[2 * pr + 1] * L0);
+                        kd1[pr] = pack_bf16(kf1[2 * pr] * L1, kf1[2 * pr + 1] * L1);
                     }
                     st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
                     st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
@@ -390,18 +396,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     st_s128(sb + OFF_KG + r1, g_k1[0], g_k1[1], g_k1[2], g_k1[3]);
                     st_s128(sb + OFF_QG + r0, g_q0[0], g_q0[1], g_q0[2], g_q0[3]);
                     st_s128(sb + OFF_QG + r1, g_q1[0], g_q1[1], g_q1[2], g_q1[3]);
-                    // k 2^(Gl - G) in fp32: the 8 tokens 16 rq + 8 half .. + 7 of a channel are two
-                    // 16-byte chunks of the channel's row in the 32-token half rq / 2
-                    const uint32_t kdh = kd_buf + (uint32_t)(rq >> 1) * 16384u;
-                    const uint32_t kc = (uint32_t)(4 * (rq & 1) + 2 * half);
-                    st_s128(kdh + sw128(ch0, kc), __float_as_uint(kd0[0]), __float_as_uint(kd0[1]),
-                            __float_as_uint(kd0[2]), __float_as_uint(kd0[3]));
-                    st_s128(kdh + sw128(ch0, kc + 1), __float_as_uint(kd0[4]), __float_as_uint(kd0[5]),
-                            __float_as_uint(kd0[6]), __float_as_uint(kd0[7]));
-                    st_s128(kdh + sw128(ch1, kc), __float_as_uint(kd1[0]), __float_as_uint(kd1[1]),
-                            __float_as_uint(kd1[2]), __float_as_uint(kd1[3]));
-                    st_s128(kdh + sw128(ch1, kc + 1), __float_as_uint(kd1[4]), __float_as_uint(kd1[5]),
-                            __float_as_uint(kd1[6]), __float_as_uint(kd1[7]));
+                    st_s128(kd_buf + r0, kd0[0], kd0[1], kd0[2], kd0[3]);
+                    st_s128(kd_buf + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
                 }
                 // score columns, channel-major [128 ch][n] in groups of 64 columns: sub-block
                 // bi >= rq sees row r as column n = sb_off(bi) + r with anchor m_bi:
@@ -758,62 +754,71 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             for (int cb = 0; cb < 2; ++cb) tma_prefetch_l2_3d(tm_g, 64 * cb, h, (int)t);
         }
     };
-    // score_chunk >= 0: the score MMA of that chunk must have read its operands first
-    auto gate_chunk = [&](int cn, int score_chunk) {
+    // the thread's 16 rows of its channel pair in chunk cn (rows past the end of the sequence read
+    // its last row and are masked in gate_chunk); issued well before the values are needed
+    auto gate_load = [&](int cn, GW (&gw)[16]) {
         const long tc0 = bos + (long)cn * C;
         const int lenc = (int)min((long)C, eos - tc0);
         const int r0 = 16 * gq;
-        // the thread's 16 rows of its channel pair, every load issued before the wait (rows past
-        // the end of the sequence read its last row and are masked below)
-        GW gw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             gw[i] = __ldg(reinterpret_cast<const GW*>(
                 gptr + ((size_t)(tc0 + min(r0 + i, lenc - 1)) * H + h) * KD + gc0));
         if (ct == 0 && cn + 1 < nt) prefetch_g(cn + 1);
-        if (w == 8 && score_chunk >= 0) sy.wait(B_SCORE, (uint32_t)(score_chunk & 1));
-        bar_sync(BAR_CHAIN, NGRP);
+    };
+    // G of chunk cn into the G buffer (free once the prep group has read the previous chunk's)
+    auto gate_chunk = [&](int cn, const GW (&gw)[16]) {
+        const long tc0 = bos + (long)cn * C;
+        const int lenc = (int)min((long)C, eos - tc0);
+        const int r0 = 16 * gq;
+        bar_sync(BAR_CHAIN, NGRP);  // after the caller's wait: the G buffer is free
         const float m = (p.mode == 1) ? lbl2 : kLog2e;  // per-token factor into log2 units
-        float acc0 = 0.f, acc1 = 0.f;
-        float2* grow = reinterpret_cast<float2*>(gs + r0 * KD + gc0);
+        const float2 nA = make_float2(nA0, nA1), nAd = make_float2(nAd0, nAd1);
+        float2 acc = make_float2(0.f, 0.f);
+        float2 gv[16];  // inclusive sums of the quarter's rows, channel pair (gc0, gc0 + 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            float a0, a1;
+            float2 a;
             if constexpr (kGateBf16) {
-                a0 = bf_lo(gw[i]);
-                a1 = bf_hi(gw[i]);
+                a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
             } else {
-                a0 = gw[i].x;
-                a1 = gw[i].y;
+                a = gw[i];
             }
             if (p.mode == 1) {
-                a0 = rcp_fast(1.0f + ex2_fast(fmaf(nA0, a0, nAd0)));
-                a1 = rcp_fast(1.0f + ex2_fast(fmaf(nA1, a1, nAd1)));
+                float2 z = __ffma2_rn(nA, a, nAd);
+                z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
+                a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
             }
-            // rows past the end add zero (selected, so that NaN padding there does not spread);
-            // the partial sums of the quarter are stored now and carried below
-            const bool valid = r0 + i < lenc;
-            acc0 = fmaf(m, valid ? a0 : 0.f, acc0);
-            acc1 = fmaf(m, valid ? a1 : 0.f, acc1);
-            grow[i * (KD / 2)] = make_float2(acc0, acc1);
+            // rows past the end add zero (they hold the last row's finite values)
+            const float mv = (r0 + i < lenc) ? m : 0.f;
+            acc = __ffma2_rn(make_float2(mv, mv), a, acc);
+            gv[i] = acc;
         }
-        if (gq < 3) *reinterpret_cast<float2*>(gcarry + gq * KD + gc0) = make_float2(acc0, acc1);
+        if (gq < 3) *reinterpret_cast<float2*>(gcarry + gq * KD + gc0) = acc;
         bar_sync(BAR_CHAIN, NGRP);  // quarter totals out
-        float cy0 = 0.f, cy1 = 0.f;
-        for (int q = 0; q < gq; ++q) {
-            const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * KD + gc0);
-            cy0 += t2.x;
-            cy1 += t2.y;
+        float2 cy = make_float2(0.f, 0.f);
+        for (int q = 0; q < gq; ++q) cy = __fadd2_rn(cy, *reinterpret_cast<const float2*>(gcarry + q * KD + gc0));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) gv[i] = __fadd2_rn(gv[i], cy);
+        if (gq == 3) *reinterpret_cast<float2*>(glast + gc0) = gv[15];
+        *reinterpret_cast<float2*>(gmid + gq * KD + gc0) = gv[8];
+        // G channel-major: the thread's 16 rows of a channel are the 16-byte chunks 4 gq .. 4 gq + 3
+        // of the channel's 256-byte row (chunk index XOR channel & 7).  Lanes with bit 2 set store
+        // their second channel first, so the eight lanes of each store phase hit eight bank groups
+        {
+            const int sw = (ct >> 2) & 1;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int ch = gc0 + (u ^ sw);
+                const bool hi = (u ^ sw) != 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = hi ? make_float4(gv[4 * k].y, gv[4 * k + 1].y, gv[4 * k + 2].y, gv[4 * k + 3].y)
+                                        : make_float4(gv[4 * k].x, gv[4 * k + 1].x, gv[4 * k + 2].x, gv[4 * k + 3].x);
+                    *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(gs) + gs_off(ch, 4 * gq + k)) = v;
+                }
+            }
         }
-        // add the carry to the stored partial sums (the thread's own values)
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-            const float2 v = grow[i * (KD / 2)];
-            const float2 g2 = make_float2(v.x + cy0, v.y + cy1);
-            grow[i * (KD / 2)] = g2;
-            if (i == 8) *reinterpret_cast<float2*>(gmid + gq * KD + gc0) = g2;
-        }
-        if (gq == 3) *reinterpret_cast<float2*>(glast + gc0) = make_float2(acc0 + cy0, acc1 + cy1);
         if (ct < C) {
             bsm[(cn & 1) * C + ct] = bet_next;
             bet_next = (cn + 1 < nt) ? beta_of(cn + 1) : 0.f;
@@ -858,7 +863,9 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             load_v(bos);
         }
         tc_fence_before();
-        gate_chunk(0, -1);
+        GW gw0[16];
+        gate_load(0, gw0);
+        gate_chunk(0, gw0);
     }
 
     for (int c = 0; c < nt; ++c) {
@@ -866,6 +873,9 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         const int len = (int)min((long)C, eos - t0);
         const uint32_t vbuf = sb + OFF_V;
 
+        // the next chunk's gate rows, in flight while the chain waits for this chunk's operands
+        GW gw[16];
+        if (c + 1 < nt) gate_load(c + 1, gw);
         // ---- Y^T = h^T kg^T, o^T = h^T qg^T
         if (ct == 0) sy.wait(B_KQFULL, c & 1);
         if (ct == 0 && !sy.aborted()) {
@@ -879,6 +889,12 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
                 umma_bf16_ta(tmem + TM_O, tmem + TM_VN + 8 * kk, bq, id_y, kk > 0);
             }
             umma_commit(sy.bar(B_YDONE));
+        }
+        // ---- a1 of the next chunk while the MMAs run: the prep group has read this chunk's G,
+        // midpoints and last row (KQFULL comes after its operand stage)
+        if (c + 1 < nt) {
+            if (w == 8) sy.wait(B_KQFULL, c & 1);
+            gate_chunk(c + 1, gw);
         }
         sy.group_wait(B_YDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
@@ -910,7 +926,6 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             }
             tmem_wait_st();
         }
-        if (c + 1 < nt) gate_chunk(c + 1, c);
         if (w == 8) {
             sy.wait(B_RESTFULL, c & 1);
             if (len < C) sy.wait(B_VFULL, c & 1);
@@ -951,20 +966,40 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         sy.group_wait(B_VNDONE, c & 1, w == 8, BAR_CHAIN);
         tc_fence_after();
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);  // the v tile is free again
-        // ---- o^T += v_new^T Aqk^T; h^T += v_new^T kd: tf32 MMAs whose A operand is the FP32
-        // v_new^T accumulator itself (K = 8 tokens per instruction)
+        // ---- o^T += v_new^T Aqk^T: tf32 MMAs whose A operand is the FP32 v_new^T accumulator itself
+        // (K = 8 tokens per instruction)
         if (ct == 0 && !sy.aborted()) {
             const uint32_t id_o = idesc_tf32(128, 64);
-            const uint32_t id_h = idesc_tf32(128, 128);
-            const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a = tmem + TM_VN + 8 * kk;
-                const uint32_t koff = (uint32_t)(kk & 3) * 32u;
-                uint64_t bo = desc_at(umma_desc(sb + OFF_AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024), koff);
-                uint64_t bk = desc_at(umma_desc(kd_buf + (uint32_t)(kk >> 2) * 16384u, 16, 1024), koff);
-                umma_tf32_ta(tmem + TM_O, a, bo, id_o, 1);
-                umma_tf32_ta(tmem + TM_H, a, bk, id_h, 1);
+                uint64_t bo = desc_at(umma_desc(sb + OFF_AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
+                                      (uint32_t)(kk & 3) * 32u);
+                umma_tf32_ta(tmem + TM_O, tmem + TM_VN + 8 * kk, bo, id_o, 1);
+            }
+        }
+        // ---- v_new^T -> bf16 A operand (the Y^T bf16 columns are free again), then
+        // h^T += v_new^T kd as a bf16 MMA
+        {
+            float x[32];
+            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch, x);
+            tmem_ld16(tmem + lane_base + TM_VN + 32 * hch + 16, x + 16);
+            tmem_wait_ld();
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+            tmem_st16(tmem + lane_base + TM_YA + 16 * hch, r);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NGRP);
+        if (ct == 0 && !sy.aborted()) {
+            tc_fence_after();
+            const uint32_t id_h = idesc_bf16(128, 128, 0, 0);
+            const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint64_t bk = desc_at(umma_desc(kd_buf, 16, 1024), kk * 32);
+                umma_bf16_ta(tmem + TM_H, tmem + TM_YA + 8 * kk, bk, id_h, 1);
             }
             umma_commit(sy.bar(B_OHDONE));
         }
