@@ -370,6 +370,9 @@ def run_ours(args, world, rank, local):
 
     dec_s, dec_bytes = time_decode(kda, workloads, dev, stream, 512, 64)
     sampler.stop()
+    # the per-configuration lines at one GPU only (a multi-rank run times the headline step)
+    per_config = (None if args.no_per_config or world > 1
+                  else per_config_lines(kda, workloads, dev, peaks, 10))
 
     if rank != 0:
         return
@@ -404,6 +407,8 @@ def run_ours(args, world, rank, local):
                    "workload": "512 one-token sequences, H=32, K=V=128, bf16, states in place"},
         "clocks": sampler.summary(),
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if not args.no_cpu_baseline:
         cores = host_cores()
         tok, dt = oracle_sample(w, 2 * cores, cores, seed=1234)
@@ -412,6 +417,92 @@ def run_ours(args, world, rank, local):
                                           f"({w.T} tokens each), float64, one OpenMP thread "
                                           f"per unit"}
     print(json.dumps(line), flush=True)
+
+
+# every configured chunked workload, timed beside the headline one (the headline workload is
+# the line's own value); decode is reported under "decode"
+PER_CONFIG = (
+    ("config 0", "tiny_fp32_b1_t128_h2_d64"),
+    ("config 1", "dense_bf16_b4_t2048_h16_d128"),
+    ("config 2", "varlen_bf16_n16_cap20480_h32_d128_c32"),
+    ("config 3a", "dense_bf16_b1_t8192_h96_d128"),
+    ("config 3b", "dense_bf16_b4_t4096_h64_d128"),
+    ("config 4b", "dense_bf16_b8_t2048_h32_d256"),
+)
+
+
+def roofline_of(w, seconds, peaks):
+    """Algorithmic bytes and flops of one forward of workload w and the fraction of the GB300
+    roofline it reaches in `seconds`: the slower of the HBM time for the bytes and the bf16
+    tensor time for the flops, over the measured time."""
+    K, V, C = w.K, w.V, w.chunk_size
+    ht = w.head_tokens()
+    state_bytes = 0 if w.initial_state is None else 2 * w.initial_state.numel() * 4
+    nbytes = algorithmic_bytes_per_head_token(K, V, w.q.element_size(), w.g.element_size()) * ht + state_bytes
+    flops = algorithmic_flops_per_head_token(K, V, C) * ht
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_mma = flops / (peaks["bf16_tflops"] * 1e12)
+    return {"bytes": nbytes, "flops": flops, "achieved_gbs": nbytes / seconds / 1e9,
+            "tflops": flops / seconds / 1e12, "bound": "hbm" if t_hbm >= t_mma else "tensor",
+            "frac": max(t_hbm, t_mma) / seconds}
+
+
+def time_chunk_workload(kda, w, dev, steps, warmup, flush=None):
+    """Median CUDA-event time of one kda_chunk_fwd call on workload w (inputs resident); with
+    `flush` (a device buffer larger than L2) L2 is overwritten before every timed call."""
+    import torch
+
+    B, T, H, K, V, C = w.B, w.T, w.H, w.K, w.V, w.chunk_size
+    o = torch.empty((B, T, H, V), device=dev, dtype=w.q.dtype)
+    n_ws = 0 if w.cu_seqlens is None else w.n_seqs
+    ws_bytes = kda.kda_chunk_workspace_bytes(w.q.dtype, B, T, H, K, V, C, n_ws, w.mode)
+    ws = torch.empty(max(ws_bytes, 1), device=dev, dtype=torch.uint8)
+    S_fin = None if w.initial_state is None else torch.empty_like(w.initial_state)
+    n_launch = kda.kda_chunk_fwd_launches(w.q.dtype, B, T, H, K, V, C, n_ws, w.mode, o.dtype)
+
+    def step():
+        kda.kda_chunk_fwd(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, w.mode, w.lower_bound,
+                          w.initial_state, False, w.cu_seqlens, C, o=o, workspace=ws,
+                          final_state=S_fin)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    return statistics.median(times), n_launch
+
+
+def per_config_lines(kda, workloads, dev, peaks, steps):
+    """One entry per configured workload: median time per forward (L2 flushed before each),
+    head-tokens/s, TFLOP/s and the roofline fraction."""
+    import torch
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, device=dev, dtype=torch.float32)
+    out = []
+    for label, name in PER_CONFIG:
+        w = workloads.make(name, device=dev)
+        sec, n_launch = time_chunk_workload(kda, w, dev, steps, 3, flush)
+        r = roofline_of(w, sec, peaks)
+        out.append({"config": label, "workload": name, "ms_per_step": 1e3 * sec,
+                    "head_tokens_per_s": w.head_tokens() / sec, "tflops": r["tflops"],
+                    "achieved_gbs": r["achieved_gbs"], "roofline_bound": r["bound"],
+                    "roofline_frac": r["frac"], "launches_per_call": n_launch,
+                    "path": "fused" if n_launch < 6 else "stage-by-stage",
+                    "dtype": str(w.q.dtype).replace("torch.", "")})
+        del w
+        torch.cuda.empty_cache()
+    del flush
+    return out
 
 
 def time_decode(kda, workloads, dev, stream, n_dec, d_steps):
@@ -473,6 +564,8 @@ def main():
                          "the one the metric is quoted on")
     ap.add_argument("--chunk-only", action="store_true",
                     help="time the chunked forward only (no e2e, decode or CPU leg); for profiling")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration timings that follow the headline step")
     ap.add_argument("--decode-only", action="store_true",
                     help="time the decode step only (kda_recurrent_fwd); for profiling")
     ap.add_argument("--decode-seqs", type=int, default=512,

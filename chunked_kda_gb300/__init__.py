@@ -15,7 +15,7 @@ import threading
 import torch
 
 __all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_bytes_ex",
-           "kda_fused_wait_timeouts", "kda_chunk_fwd_launches",
+           "kda_fused_wait_timeouts", "kda_chunk_fwd_launches", "kda_test_hooks",
            "kda_chunk_fwd", "kda_chunk_fwd_ex",
            "kda_chunk_fwd_noalloc", "kda_recurrent_fwd", "KdaError", "GATE_PRE", "GATE_SAFE",
            "GATE_NONSAFE", "GATE_LOG2", "FLAG_K_L2NORM", "FLAG_BETA_LOGITS", "kda_recurrent_fwd_ex",
@@ -74,8 +74,10 @@ def load_library():
                                       ctypes.c_size_t, vp]
         lib.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
                                          vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
-                                         ctypes.c_size_t, i32, ctypes.c_uint, vp]
+                                         ctypes.c_size_t, i32, ctypes.c_uint, vp, vp]
         lib.kda_chunk_fwd_ex.restype = ctypes.c_int
+        lib.kda_test_hooks.argtypes = [i32, i32, i32]
+        lib.kda_test_hooks.restype = i32
         lib.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
                                              vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
                                              ctypes.c_uint, vp]
@@ -183,6 +185,13 @@ def kda_chunk_fwd_launches(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=GATE
     return int(lib.kda_chunk_fwd_launches(code, ocode, B, T, H, K, V, chunk_size, n_seqs, mode))
 
 
+def kda_test_hooks(wait_timeout_chunk=-1, sm_count=0, one_launch=False) -> None:
+    """The fused path's test hooks (kda_test_hooks in kda.h), process-wide; the defaults turn
+    them off."""
+    _check("kda_test_hooks", load_library().kda_test_hooks(int(wait_timeout_chunk), int(sm_count),
+                                                           1 if one_launch else 0))
+
+
 def kda_fused_wait_timeouts(reset=False) -> int:
     """Fused-kernel mbarrier waits that gave up on the current device (0 after normal runs);
     synchronises with the device."""
@@ -195,7 +204,7 @@ def kda_fused_wait_timeouts(reset=False) -> int:
 def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lower_bound=-5.0,
                   initial_state=None, output_final_state=False, cu_seqlens=None, chunk_size=64,
                   o=None, final_state=None, workspace=None, stream=None, o_dtype=None,
-                  q_l2norm=False):
+                  q_l2norm=False, status=None):
     """Chunked KDA forward; returns (o, final_state or None).
 
     ``o_dtype`` is the dtype of q (default) or torch.float32.
@@ -205,6 +214,10 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
 
     Grouped value heads: q and k may have fewer heads than v (a divisor of them); value
     head h then reads query / key head h / (H / Hk).
+
+    ``status``: an int32 CUDA tensor of one element (kda_chunk_fwd_ex's status word); bit 0
+    is set on the device when a fused-kernel CTA gave up a bounded wait.  The caller zeroes
+    it and reads it after synchronising.
 
     ``final_state`` may be passed (and may be ``initial_state`` itself) to
     write the final state in place; otherwise it is allocated when
@@ -239,9 +252,13 @@ def kda_chunk_fwd(q, k, v, g, beta, A_log=None, dt_bias=None, mode=GATE_SAFE, lo
     args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _dt(g, "g"), _ptr(A_log), _ptr(dt_bias), mode,
             lower_bound, _ptr(beta), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n,
             B, T, H, K, V, chunk_size, _ptr(o), _dt(o, "o"), _ptr(workspace), ws_bytes)
-    if q_l2norm or Hk != H:
+    if status is not None:
+        _cuda(status, "status", torch.int32)
+        if status.numel() < 1:
+            raise ValueError("status needs one int32 element")
+    if q_l2norm or Hk != H or status is not None:
         _check("kda_chunk_fwd_ex", lib.kda_chunk_fwd_ex(
-            *args, Hk, FLAG_Q_L2NORM if q_l2norm else 0, _stream(stream)))
+            *args, Hk, FLAG_Q_L2NORM if q_l2norm else 0, _ptr(status), _stream(stream)))
     else:
         _check("kda_chunk_fwd", lib.kda_chunk_fwd(*args, _stream(stream)))
     return o, final_state

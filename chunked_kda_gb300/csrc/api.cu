@@ -58,6 +58,37 @@ kda_status check_gate(kda_gate_mode mode, const float* A_log, float lower_bound)
 
 namespace kda {
 void record_error(const char* msg) { g_last_error = msg; }
+
+// The host checks of the chunked forward, shared by kda_chunk_fwd_ex and kda_chunk_fwd_noalloc;
+// fills *N (logical sequences)
+kda_status check_chunk_args(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const void* g, kda_dtype g_dtype, const float* A_log,
+                            const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                            const void* beta, const float* initial_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                            int V, int chunk_size, void* o, kda_dtype o_dtype, int n_qk_heads,
+                            unsigned flags, int* N) {
+    if (flags & ~KDA_FLAG_Q_L2NORM) return fail(KDA_ERR_INVALID_ARG, "unknown flag bits");
+    if (n_qk_heads < 0 || (n_qk_heads > 0 && (H <= 0 || H % n_qk_heads != 0)))
+        return fail(KDA_ERR_INVALID_ARG, "n_qk_heads must divide H");
+    kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, N);
+    if (st != KDA_OK) return st;
+    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
+    if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
+    if (o_dtype != qkv_dtype && o_dtype != KDA_F32)
+        return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
+    if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
+    if (chunk_size != 32 && chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 32 or 64");
+    st = check_gate(mode, A_log, lower_bound);
+    if (st != KDA_OK) return st;
+    const bool any_tokens = (long long)B * T > 0 && *N > 0;
+    if (any_tokens && (!q || !k || !v || !g || !beta || !o))
+        return fail(KDA_ERR_INVALID_ARG, "null q, k, v, g, beta or o");
+    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    return KDA_OK;
+}
 }  // namespace kda
 
 extern "C" {
@@ -128,6 +159,12 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
     return 6;
 }
 
+kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch) {
+    g_last_error.clear();
+    kda::set_test_hooks(wait_timeout_chunk, sm_count, one_launch);
+    return KDA_OK;
+}
+
 kda_status kda_fused_wait_timeouts(unsigned int* count, int reset) {
     g_last_error.clear();
     if (!count) return fail(KDA_ERR_INVALID_ARG, "null count");
@@ -143,7 +180,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
                          size_t workspace_bytes, kda_stream_t stream) {
     return kda_chunk_fwd_ex(q, k, v, qkv_dtype, g, g_dtype, A_log, dt_bias, mode, lower_bound, beta,
                             initial_state, final_state, cu_seqlens, n_seqs, B, T, H, K, V,
-                            chunk_size, o, o_dtype, workspace, workspace_bytes, 0, 0u, stream);
+                            chunk_size, o, o_dtype, workspace, workspace_bytes, 0, 0u, nullptr,
+                            stream);
 }
 
 kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -153,28 +191,14 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
                             const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
                             int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                             size_t workspace_bytes, int n_qk_heads, unsigned flags,
-                            kda_stream_t stream) {
+                            int32_t* status, kda_stream_t stream) {
     g_last_error.clear();
-    if (flags & ~KDA_FLAG_Q_L2NORM) return fail(KDA_ERR_INVALID_ARG, "unknown flag bits");
-    if (n_qk_heads < 0 || (n_qk_heads > 0 && (H <= 0 || H % n_qk_heads != 0)))
-        return fail(KDA_ERR_INVALID_ARG, "n_qk_heads must divide H");
     int N = 0;
-    kda_status st = check_layout(cu_seqlens, n_seqs, B, T, H, &N);
+    kda_status st = kda::check_chunk_args(q, k, v, qkv_dtype, g, g_dtype, A_log, dt_bias, mode,
+                                          lower_bound, beta, initial_state, final_state,
+                                          cu_seqlens, n_seqs, B, T, H, K, V, chunk_size, o,
+                                          o_dtype, n_qk_heads, flags, &N);
     if (st != KDA_OK) return st;
-    if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "qkv dtype");
-    if (g_dtype != KDA_F32 && g_dtype != KDA_BF16) return fail(KDA_ERR_UNSUPPORTED, "g dtype");
-    if (o_dtype != qkv_dtype && o_dtype != KDA_F32)
-        return fail(KDA_ERR_UNSUPPORTED, "o dtype must be the qkv dtype or float32");
-    if (!head_dim_ok(K) || !head_dim_ok(V)) return fail(KDA_ERR_UNSUPPORTED, "K and V must be 64, 128 or 256");
-    if (chunk_size != 32 && chunk_size != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk_size must be 32 or 64");
-    st = check_gate(mode, A_log, lower_bound);
-    if (st != KDA_OK) return st;
-    const bool any_tokens = (long long)B * T > 0 && N > 0;
-    if (any_tokens && (!q || !k || !v || !g || !beta || !o))
-        return fail(KDA_ERR_INVALID_ARG, "null q, k, v, g, beta or o");
-    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (N == 0) return KDA_OK;
     size_t need = kda_chunk_workspace_bytes_ex(qkv_dtype, B, T, H, K, V, chunk_size,
                                                cu_seqlens ? n_seqs : 0, mode);
@@ -182,11 +206,13 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
         return fail(KDA_ERR_INVALID_ARG, "workspace smaller than kda_chunk_workspace_bytes_ex()");
     if (workspace && ((uintptr_t)workspace & 255u) != 0)
         return fail(KDA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (status && ((uintptr_t)status & 3u) != 0)
+        return fail(KDA_ERR_INVALID_ARG, "status must be 4-byte aligned");
     kda::FwdArgs a{q, k, v, g, beta, qkv_dtype == KDA_BF16, g_dtype == KDA_BF16, A_log, dt_bias,
                    (int)mode, lower_bound, initial_state, final_state, cu_seqlens, N, B, T, H, K,
                    V, chunk_size, o, o_dtype == KDA_F32, workspace, workspace_bytes,
                    (cudaStream_t)stream, (flags & KDA_FLAG_Q_L2NORM) != 0,
-                   n_qk_heads > 0 ? n_qk_heads : H};
+                   n_qk_heads > 0 ? n_qk_heads : H, reinterpret_cast<int*>(status)};
     if (kda::fused_supported(a)) return cuda_status(kda::launch_chunk_fused(a));
     return cuda_status(kda::launch_chunk_precise(a));
 }

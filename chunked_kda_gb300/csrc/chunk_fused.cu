@@ -51,8 +51,7 @@
 // reads query / key head h / (H / Hk) through the TMA head coordinate).
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
-#include <cstring>
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -189,6 +188,7 @@ struct Params {
     int hr;     // value heads per query / key head: value head h reads q, k head h / hr
     int stall_chunk;  // test hook (>= 0): at this chunk the preparation group waits, with a short
                       // limit, on an mbarrier nothing completes, so the CTA takes its abort path
+    int* status;      // optional caller word (device): bit 0 set when a CTA gives up a wait
     // Dense inputs, split schedule (sp_mode 1, 2; 0 = one CTA per unit on an (N, H) grid).  The
     // units u = n + N h, the order of the plain grid, are laid out on two 1-D launches:
     //   sp_mode 1: CTA i runs tokens [0, sp_cut) of unit i, i < sp_split;
@@ -203,14 +203,18 @@ struct Params {
 struct Sync {
     uint32_t bars;
     volatile uint32_t* abort_flag;
+    int* status;
     __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * i; }
+    // a wait gave up: count it, tell the caller's status word, and stop the CTA's waits
+    __device__ __forceinline__ void give_up() const {
+        atomicAdd(&g_fused_timeouts, 1u);
+        if (status) atomicOr(status, 1);
+        *abort_flag = 1u;
+    }
     // bounded wait; after any timeout the CTA stops waiting
     __device__ __forceinline__ void wait(int i, uint32_t parity) const {
         if (*abort_flag) return;
-        if (!mbar_wait(bar(i), parity)) {
-            atomicAdd(&g_fused_timeouts, 1u);
-            *abort_flag = 1u;
-        }
+        if (!mbar_wait(bar(i), parity)) give_up();
     }
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
     // wait of a whole warp group: one warp polls, the others sleep on the group's barrier
@@ -261,7 +265,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 
         if (c == p.stall_chunk) {  // test hook: a bounded wait that gives up
             if (w == 0 && !sy.aborted() && !mbar_wait(sy.bar(B_STALL), 0, 1u << 10)) {
-                if (l == 0) atomicAdd(&g_fused_timeouts, 1u);
+                if (l == 0) sy.give_up();
                 *sy.abort_flag = 1u;
             }
             bar_sync(BAR_PREP, NGRP);
@@ -1086,7 +1090,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
-    Sync sy{sb + OFF_BAR, misc + 1};
+    Sync sy{sb + OFF_BAR, misc + 1, p.status};
 
     const int tid = threadIdx.x, w = tid >> 5;
 
@@ -1187,20 +1191,24 @@ bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode) {
 
 bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C, a.mode); }
 
-// test hook: KDA_FUSED_SCHEDULE=plain keeps every dense launch at one CTA per unit
-static bool split_allowed_from_env() {
-    const char* v = getenv("KDA_FUSED_SCHEDULE");
-    return !(v && strcmp(v, "plain") == 0);
+// Test hooks, process-wide, set only through kda_test_hooks (off by default): the chunk at which
+// every CTA gives up a wait (-1: none), an SM count to plan the split schedule for (0: the
+// device's), and one launch per call whatever the plan.
+static std::atomic<int> g_hook_stall_chunk{-1};
+static std::atomic<int> g_hook_sm_count{0};
+static std::atomic<int> g_hook_one_launch{0};
+
+void set_test_hooks(int stall_chunk, int sm_count, int one_launch) {
+    g_hook_stall_chunk.store(stall_chunk < 0 ? -1 : stall_chunk);
+    g_hook_sm_count.store(sm_count > 0 ? sm_count : 0);
+    g_hook_one_launch.store(one_launch ? 1 : 0);
 }
 
-// SMs of the current device; test hook: KDA_TEST_SM_COUNT=<n> plans for n SMs instead (the
-// split schedule is correct for any n, only its balance depends on it), which lets the plan be
-// checked without a device
+static bool split_allowed() { return g_hook_one_launch.load(std::memory_order_relaxed) == 0; }
+
+// SMs of the current device (or the test hook's count), cached per device ordinal
 static int sm_count() {
-    if (const char* v = getenv("KDA_TEST_SM_COUNT")) {
-        const int n = atoi(v);
-        if (n > 0) return n;
-    }
+    if (const int n = g_hook_sm_count.load(std::memory_order_relaxed); n > 0) return n;
     static int cached[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
@@ -1244,7 +1252,7 @@ static int split_cut_chunks(int U, int S, int T, int min_tail) {
 
 // chunks of the first piece of the split schedule for these sizes (0: one launch)
 static int split_cut_for(int N, int H, int T, bool packed, bool o_f32) {
-    if (packed || !split_allowed_from_env()) return 0;
+    if (packed || !split_allowed()) return 0;
     // the state (K V words) spans this many of the unit's output rows
     const int stash_rows = fused::KD * fused::VD * 4 / (fused::VD * (o_f32 ? 4 : 2));
     return split_cut_chunks(N * H, sm_count(), T, stash_rows);
@@ -1286,12 +1294,6 @@ static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUten
     return cudaGetLastError();
 }
 
-// test hook: KDA_TEST_WAIT_TIMEOUT_CHUNK=<c> makes every CTA give up a wait at chunk c
-static int stall_chunk_from_env() {
-    const char* v = getenv("KDA_TEST_WAIT_TIMEOUT_CHUNK");
-    return (v && *v) ? atoi(v) : -1;
-}
-
 cudaError_t read_fused_timeouts(unsigned* count, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(count, g_fused_timeouts, sizeof(unsigned));
     if (e == cudaSuccess && reset) {
@@ -1313,7 +1315,8 @@ cudaError_t launch_chunk_fused(const FwdArgs& a) {
     if (!make_map(&mg, a.g_bf16 ? a.g : a.q, tokens, a.H, KD)) return cudaErrorInvalidValue;
     Params p{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta, a.g,
              a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o, a.mode, a.lb, a.T, a.H, a.q_l2norm ? 1 : 0,
-             a.Hk > 0 ? a.H / a.Hk : 1, stall_chunk_from_env(), a.N, 0, 0, 0, 0};
+             a.Hk > 0 ? a.H / a.Hk : 1, g_hook_stall_chunk.load(std::memory_order_relaxed), a.status,
+             a.N, 0, 0, 0, 0};
     if (a.g_bf16)
         return a.o_f32 ? launch_t<__nv_bfloat16, float>(a, mq, mk, mv, mg, p)
                        : launch_t<__nv_bfloat16, __nv_bfloat16>(a, mq, mk, mv, mg, p);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/kda.h"
+
 namespace kda {
 
 struct GateArgs {
@@ -45,6 +47,7 @@ struct FwdArgs {
     cudaStream_t stream;
     bool q_l2norm = false;  // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
     int Hk = 0;             // query / key heads (a divisor of H; value head h reads h / (H / Hk))
+    int* status = nullptr;  // optional device word: bit 0 set when a fused CTA gives up a wait
 };
 constexpr float kQNormEps = 1e-6f;
 
@@ -88,8 +91,21 @@ cudaError_t launch_chunk_fused(const FwdArgs& a);
 int fused_launch_count(int N, int H, int T, bool packed, bool o_f32);
 // fused-kernel mbarrier waits that gave up on the current device (synchronises), optional reset
 cudaError_t read_fused_timeouts(unsigned* count, bool reset);
+// the fused path's test hooks (kda_test_hooks)
+void set_test_hooks(int stall_chunk, int sm_count, int one_launch);
 
 // sets the message kda_last_error() returns on this host thread
 void record_error(const char* msg);
+
+// every host check of the chunked forward (layout and size limits, dtypes, head dims, chunk
+// size, gate mode and bound, null and misaligned pointers), shared by kda_chunk_fwd_ex and
+// kda_chunk_fwd_noalloc; records the error message and fills *N (logical sequences)
+kda_status check_chunk_args(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const void* g, kda_dtype g_dtype, const float* A_log,
+                            const float* dt_bias, kda_gate_mode mode, float lower_bound,
+                            const void* beta, const float* initial_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
+                            int V, int chunk_size, void* o, kda_dtype o_dtype, int n_qk_heads,
+                            unsigned flags, int* N);
 
 }  // namespace kda

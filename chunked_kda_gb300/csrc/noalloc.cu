@@ -8,8 +8,6 @@
 // running while a CUDA graph is being captured through an API that forbids
 // cudaMalloc, or embedded callers with a fixed memory budget.  Such callers
 // cannot call cudaMalloc for the workspace that kda_chunk_fwd needs.
-#include <mutex>
-
 #include "../../include/kda.h"
 #include "kda_internal.h"
 
@@ -19,40 +17,21 @@ namespace {
 // device memory until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_setup_mu;
-constexpr int kMaxDevices = 256;
-void* g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device ordinal
-
-// The address of g_noalloc_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the device address must come
-// from cudaGetSymbolAddress, once per device, with that device current.
+// The device address of g_noalloc_scratch in the current context.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, with the device current.  It is looked up on every call rather
+// than cached: after cudaDeviceReset, or when the primary context is released and created
+// again, the array lives at a new address, and a cached one would point at freed memory.
 kda_status scratch_on_current_device(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        kda::record_error("kda_chunk_fwd_noalloc: cudaGetDevice failed");
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        kda::record_error("kda_chunk_fwd_noalloc: cudaGetSymbolAddress of the scratch failed");
         return KDA_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        kda::record_error("kda_chunk_fwd_noalloc: device ordinal out of range");
-        return KDA_ERR_UNSUPPORTED;
-    }
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            kda::record_error("kda_chunk_fwd_noalloc: cudaGetSymbolAddress of the scratch failed");
-            return KDA_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return KDA_OK;
 }
-
-bool hd_ok(int d) { return d == 64 || d == 128 || d == 256; }
-bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
@@ -63,46 +42,17 @@ extern "C" kda_status kda_chunk_fwd_noalloc(
     const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K, int V, int chunk_size,
     void* o, kda_dtype o_dtype, kda_stream_t stream) {
     kda::record_error("");
-    if (B < 0 || T < 0 || H <= 0 || (cu_seqlens && (B != 1 || n_seqs < 0 || n_seqs > 65535)) ||
-        (!cu_seqlens && B > 65535)) {
-        kda::record_error("kda_chunk_fwd_noalloc: bad B, T, H or n_seqs");
-        return KDA_ERR_INVALID_ARG;
-    }
-    if ((qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) || (g_dtype != KDA_F32 && g_dtype != KDA_BF16) ||
-        (o_dtype != qkv_dtype && o_dtype != KDA_F32) || !hd_ok(K) || !hd_ok(V) ||
-        (chunk_size != 32 && chunk_size != 64)) {
-        kda::record_error("kda_chunk_fwd_noalloc: unsupported dtype, head dim or chunk size");
-        return KDA_ERR_UNSUPPORTED;
-    }
-    if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE) {
-        kda::record_error("kda_chunk_fwd_noalloc: bad gate mode");
-        return KDA_ERR_INVALID_ARG;
-    }
-    if (mode != KDA_GATE_PRE && !A_log) {
-        kda::record_error("kda_chunk_fwd_noalloc: in-kernel gate needs A_log");
-        return KDA_ERR_INVALID_ARG;
-    }
-    if (mode == KDA_GATE_SAFE && !(lower_bound >= -5.0f && lower_bound < 0.0f)) {
-        kda::record_error("kda_chunk_fwd_noalloc: safe gate needs -5 <= lower_bound < 0");
-        return KDA_ERR_INVALID_ARG;
-    }
-    const int N = cu_seqlens ? n_seqs : B;
-    if ((long long)B * T > 0 && N > 0 && (!q || !k || !v || !g || !beta || !o)) {
-        kda::record_error("kda_chunk_fwd_noalloc: null q, k, v, g, beta or o");
-        return KDA_ERR_INVALID_ARG;
-    }
-    const void* ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, A_log, dt_bias};
-    for (const void* p : ptrs)
-        if (p && !al16(p)) {
-            kda::record_error("kda_chunk_fwd_noalloc: pointers must be 16-byte aligned");
-            return KDA_ERR_INVALID_ARG;
-        }
-    if (((uintptr_t)cu_seqlens & 3u) != 0) {
-        kda::record_error("kda_chunk_fwd_noalloc: cu_seqlens misaligned");
-        return KDA_ERR_INVALID_ARG;
-    }
+    // the same host checks as kda_chunk_fwd (sizes, dtypes, head dims, chunk size, gate,
+    // null and misaligned pointers), before anything else
+    int N = 0;
+    kda_status st = kda::check_chunk_args(q, k, v, qkv_dtype, g, g_dtype, A_log, dt_bias, mode,
+                                          lower_bound, beta, initial_state, final_state,
+                                          cu_seqlens, n_seqs, B, T, H, K, V, chunk_size, o,
+                                          o_dtype, 0, 0u, &N);
+    if (st != KDA_OK) return st;
     if (N == 0) return KDA_OK;
-    // the scratch this call needs must fit in the static area; nothing is allocated
+    // the scratch this call needs must fit in the static area; nothing is allocated (the size
+    // is computed in 64-bit arithmetic from sizes the checks above bounded)
     const size_t need = kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, cu_seqlens != nullptr);
     if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) {
         kda::record_error(
@@ -111,7 +61,7 @@ extern "C" kda_status kda_chunk_fwd_noalloc(
         return KDA_ERR_INVALID_ARG;
     }
     void* scratch = nullptr;
-    kda_status st = scratch_on_current_device(&scratch);
+    st = scratch_on_current_device(&scratch);
     if (st != KDA_OK) return st;
     // Every region of the scratch is written before it is read within one call,
     // so nothing needs clearing between calls.

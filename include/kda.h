@@ -142,8 +142,7 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
  * the first S units' remaining chunks, which fill the SMs the last whole units leave free.
  * The FP32 state crosses between the two launches through the unit's own rows of o (before
  * the second launch overwrites them), so the split needs no workspace and the results are
- * bitwise those of one launch.  The environment variable KDA_FUSED_SCHEDULE=plain, read per
- * call, keeps one launch.
+ * bitwise those of one launch.  kda_test_hooks can force one launch (for tests).
  */
 int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T, int H, int K, int V,
                            int chunk_size, int n_seqs, kda_gate_mode mode);
@@ -212,6 +211,16 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype 
  *                      the states have H heads.  0 means H (multi-head); it
  *                      must divide H.
  *
+ *   status             NULL, or a 4-byte aligned device int32 the caller owns:
+ *                      the call ORs KDA_DEVICE_WAIT_GAVE_UP into it when a CTA
+ *                      of the fused kernel gave up one of its bounded waits
+ *                      (the outputs of that call are then not valid; the
+ *                      context stays usable).  The library never clears it:
+ *                      zero it before the call and read it once the caller's
+ *                      stream has synchronised (no host synchronisation in
+ *                      the library).  The stage-by-stage path has no waits
+ *                      that can give up and leaves it untouched.
+ *
  * Every other argument, the layouts and the errors are those of
  * kda_chunk_fwd; unknown flag bits return KDA_ERR_INVALID_ARG.
  */
@@ -222,7 +231,10 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
                             const int32_t* cu_seqlens, int n_seqs, int B, int T, int H, int K,
                             int V, int chunk_size, void* o, kda_dtype o_dtype, void* workspace,
                             size_t workspace_bytes, int n_qk_heads, unsigned flags,
-                            kda_stream_t stream);
+                            int32_t* status, kda_stream_t stream);
+
+/* bit of kda_chunk_fwd_ex's status word: a fused-kernel CTA gave up a bounded wait */
+#define KDA_DEVICE_WAIT_GAVE_UP 1
 
 /*
  * Chunked forward for callers that cannot allocate device memory.
@@ -243,9 +255,13 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
  *   (kda_chunk_workspace_bytes(KDA_F32, ...) of the same sizes, roughly 3.8 KB
  *   per token and head at K = V = 128, C = 64) are rejected with
  *   KDA_ERR_INVALID_ARG before anything is enqueued.
- *   Set-up: the first call on each device looks up the scratch array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.
+ *   Validation: the host checks of kda_chunk_fwd, the same code, run first
+ *   (sizes below 2^31 tokens, dtypes, head dims, chunk size, gate, pointers).
+ *   Set-up: every call looks up the scratch array's device address in the
+ *   current context (cudaGetSymbolAddress, with the device current), so the
+ *   address stays right after cudaDeviceReset or a new primary context.  The
+ *   first call on a device may load the library's device code there; make
+ *   that first call before any stream capture.
  *   Sharing: every call on a device uses the same scratch array and it keeps
  *   the last call's contents (each call writes every byte it reads, so nothing
  *   needs clearing); calls whose kernels overlap on the GPU, e.g. from two
@@ -317,11 +333,22 @@ kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda
  * to *count (0 after normal runs) and zeroes it when reset != 0.  It copies from the device
  * and therefore synchronises with it: a diagnostic call, not for the hot path.  Null count:
  * KDA_ERR_INVALID_ARG; a failing copy: KDA_ERR_CUDA.
- * Test hook: with the environment variable KDA_TEST_WAIT_TIMEOUT_CHUNK=<c> set when
- * kda_chunk_fwd launches the fused kernel, every CTA waits at its chunk c on an mbarrier
- * that nothing completes (with a short limit) and takes that path.
  */
 kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
+
+/*
+ * Test hooks of the fused path, process-wide, all off by default and read by nothing else
+ * (no environment variables).  For tests only; set them back to (-1, 0, 0) afterwards.
+ *   wait_timeout_chunk  >= 0: every CTA of later fused launches waits, at that chunk and
+ *                       with a short limit, on an mbarrier nothing completes, and takes the
+ *                       give-up path (counted by kda_fused_wait_timeouts, flagged in the
+ *                       status word of kda_chunk_fwd_ex); -1: off
+ *   sm_count            > 0: plan the split schedule (kda_chunk_fwd_launches) for this many
+ *                       SMs instead of the device's; 0: the device's
+ *   one_launch          nonzero: never split a fused call into two launches
+ * Always KDA_OK; no device work.
+ */
+kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch);
 
 const char* kda_status_string(kda_status status);
 

@@ -47,7 +47,8 @@ def lib():
     # full prototypes: a call with the wrong arity raises instead of passing stray values
     L.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
                                    i32, i32, i32, i32, i32, i32, vp, i32, vp, ctypes.c_size_t, i32,
-                                   ctypes.c_uint, vp]
+                                   ctypes.c_uint, vp, vp]
+    L.kda_test_hooks.argtypes = [i32, i32, i32]
     L.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
                                        i32, i32, i32, i32, i32, i32, vp, i32, i32, ctypes.c_uint,
                                        vp]
@@ -142,7 +143,7 @@ def test_chunk_ex_flags_host_validation(lib):
         return lib.kda_chunk_fwd_ex(a["q"], P, P, BF16, P, BF16, P, None, 1, ctypes.c_float(a["lb"]),
                                     P, None, None, None, 0, 1, 64, a["H"], 128, 128, a["C"], a["o"],
                                     BF16, None, ctypes.c_size_t(0), ctypes.c_int(a["hk"]),
-                                    ctypes.c_uint(flags), None)
+                                    ctypes.c_uint(flags), a.get("status"), None)
     assert ex(2) == INVALID
     assert b"flag" in lib.kda_last_error()
     assert ex(0, H=3, hk=2) == INVALID  # query / key heads must divide the value heads
@@ -152,6 +153,8 @@ def test_chunk_ex_flags_host_validation(lib):
     assert ex(1, C=48) == UNSUPPORTED
     assert ex(1, q=None) == INVALID
     assert ex(1, lb=0.0) == INVALID
+    assert ex(0, status=ctypes.c_void_p(4098)) == INVALID  # the status word must be 4-byte aligned
+    assert b"status" in lib.kda_last_error()
 
 
 def test_recurrent_and_gate_host_validation(lib):
@@ -237,7 +240,7 @@ def test_workspace_bytes(lib):
     assert ex(F32, B, T, H, K, V, C, 0, 2) == lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0)
 
 
-def test_split_schedule_plan(lib, monkeypatch):
+def test_split_schedule_plan(lib):
     """The two-launch plan for dense fused calls, on a stated SM count (no device needed): it
     splits only when the last wave of (sequence, head) units is at most half full and the second
     pieces hold the FP32 state in their output rows (256 bf16 rows, 128 float32 rows)."""
@@ -245,7 +248,7 @@ def test_split_schedule_plan(lib, monkeypatch):
     SAFE = 1
 
     def launches(B, T, H, o=BF16, S=152):
-        monkeypatch.setenv("KDA_TEST_SM_COUNT", str(S))
+        lib.kda_test_hooks(-1, S, 0)
         return f(BF16, o, B, T, H, 128, 128, 64, 0, SAFE)
 
     assert launches(2, 720, 114) == 2        # 228 units: the last wave half full
@@ -261,8 +264,17 @@ def test_split_schedule_plan(lib, monkeypatch):
     assert launches(1, 4096, 12, S=8) == 2   # any SM count
     assert launches(1, 20480, 32, S=8) == 1  # a whole number of waves
     assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 3, SAFE) == 1  # packed: never split
-    monkeypatch.setenv("KDA_FUSED_SCHEDULE", "plain")
-    assert launches(2, 720, 114) == 1
+    lib.kda_test_hooks(-1, 152, 1)  # one launch whatever the plan
+    assert f(BF16, BF16, 2, 720, 114, 128, 128, 64, 0, SAFE) == 1
+    lib.kda_test_hooks(-1, 0, 0)  # hooks off again
+
+
+def test_no_environment_hooks():
+    """The library reads no environment variables: its test hooks are set only through
+    kda_test_hooks."""
+    for src in os.listdir(os.path.join(ROOT, "chunked_kda_gb300", "csrc")):
+        text = open(os.path.join(ROOT, "chunked_kda_gb300", "csrc", src)).read()
+        assert "getenv" not in text, src
 
 
 def test_layout_and_alignment_validation(lib):
@@ -283,3 +295,39 @@ def test_layout_and_alignment_validation(lib):
     assert lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 128, 64, None, None) == INVALID
     assert b"null g" in lib.kda_last_error()
     assert lib.kda_gate_fwd(P, BF16, P, None, 1, -5.0, None, 0, 1, 4, 2, 0, 64, P, None) == INVALID
+
+
+def _noalloc(lib, **kw):
+    a = dict(q=P, k=P, v=P, dt=F32, g=P, gdt=F32, A_log=P, dt_bias=None, mode=1, lb=-5.0,
+             beta=P, h0=None, hT=None, cu=None, n=0, B=1, T=64, H=2, K=128, V=128, C=64, o=P,
+             odt=None)
+    a.update(kw)
+    if a["odt"] is None:
+        a["odt"] = a["dt"]
+    return lib.kda_chunk_fwd_noalloc(a["q"], a["k"], a["v"], a["dt"], a["g"], a["gdt"], a["A_log"],
+                                     a["dt_bias"], a["mode"], a["lb"], a["beta"], a["h0"], a["hT"],
+                                     a["cu"], a["n"], a["B"], a["T"], a["H"], a["K"], a["V"], a["C"],
+                                     a["o"], a["odt"], None)
+
+
+def test_noalloc_host_validation_is_kda_chunk_fwds(lib):
+    """kda_chunk_fwd_noalloc runs kda_chunk_fwd's host checks, size limits included, before
+    it looks anything up on the device."""
+    assert _noalloc(lib, C=48) == UNSUPPORTED
+    assert _noalloc(lib, K=96) == UNSUPPORTED
+    assert _noalloc(lib, dt=F32, odt=BF16) == UNSUPPORTED
+    assert _noalloc(lib, lb=0.0) == INVALID
+    assert _noalloc(lib, A_log=None) == INVALID
+    assert _noalloc(lib, q=None) == INVALID
+    assert _noalloc(lib, o=ctypes.c_void_p(4098)) == INVALID
+    assert _noalloc(lib, B=2, cu=P, n=1) == INVALID
+    assert _noalloc(lib, cu=ctypes.c_void_p(4098), n=1) == INVALID  # misaligned offsets
+    # B * T must stay below 2^31 (token coordinates are 32-bit), B * T * H at most 2^40
+    assert _noalloc(lib, B=2, T=1 << 30) == INVALID
+    assert b"2^31" in lib.kda_last_error()
+    assert _noalloc(lib, B=1, T=(1 << 31) - 1, H=1 << 10) == INVALID
+    # a size far beyond the fixed scratch is refused before any device work
+    assert _noalloc(lib, B=1, T=1 << 20, H=8) == INVALID
+    assert b"KDA_NOALLOC_SCRATCH_BYTES" in lib.kda_last_error()
+    # no sequences: nothing to do
+    assert _noalloc(lib, B=0) == OK

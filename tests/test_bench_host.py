@@ -34,3 +34,34 @@ def test_code_digest_ignores_comments_only(tmp_path):
 
 def test_traffic_only_for_its_workload():
     assert bench.fused_traffic_bytes("dense_bf16_b4_t2048_h16_d128") is None
+
+
+def test_roofline_of_takes_the_slower_bound():
+    import types
+
+    class T:
+        def __init__(self, n, es):
+            self.n, self.es = n, es
+
+        def numel(self):
+            return self.n
+
+        def element_size(self):
+            return self.es
+
+    w = types.SimpleNamespace(K=128, V=128, chunk_size=64, initial_state=None,
+                              q=T(0, 2), g=T(0, 2), head_tokens=lambda: 1 << 20)
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+    nbytes = 1282 * (1 << 20)
+    flops = bench.algorithmic_flops_per_head_token(128, 128, 64) * (1 << 20)
+    t = 1e-3
+    r = bench.roofline_of(w, t, peaks)
+    assert r["bytes"] == nbytes and r["bound"] == "hbm"
+    assert math.isclose(r["frac"], nbytes / 6800e9 / t)
+    assert math.isclose(r["tflops"], flops / t / 1e12)
+    # with a much lower tensor peak the flops bound the time instead
+    r2 = bench.roofline_of(w, t, {"hbm_gbs": 6800.0, "bf16_tflops": 10.0})
+    assert r2["bound"] == "tensor" and math.isclose(r2["frac"], flops / 10e12 / t)
+    # initial and final states count once each
+    w.initial_state = T(4 * 128 * 128, 4)
+    assert bench.roofline_of(w, t, peaks)["bytes"] == nbytes + 2 * 4 * 128 * 128 * 4

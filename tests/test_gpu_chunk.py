@@ -77,23 +77,31 @@ def test_dense_head_dims(dtype, K, V):
     compare(w, o, st)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+# bf16 inputs with the output in bf16 (checked under the bf16-storage allowance) and in float32
+# (held to the plain max-abs bound), and float32 inputs
+DTYPES_OUT = [(torch.float32, None), (torch.bfloat16, None), (torch.bfloat16, torch.float32)]
+DTYPES_OUT_IDS = ["f32", "bf16", "bf16-f32out"]
+
+
+@pytest.mark.parametrize("dtype,o_dtype", DTYPES_OUT, ids=DTYPES_OUT_IDS)
 @pytest.mark.parametrize("C", [32, 64])
-def test_pre_gated(dtype, C):
+def test_pre_gated(dtype, o_dtype, C):
     w = workloads.make_dense("t", 2, 150, 2, 128, 128, C, dtype, 21, state_std=0.05,
                              mode=workloads.GATE_PRE)
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
+    assert o.dtype == (o_dtype or dtype)
     compare(w, o, st)
 
 
+@pytest.mark.parametrize("o_dtype", [None, torch.float32], ids=["bf16out", "f32out"])
 @pytest.mark.parametrize("lb,g_std", [(-5.0, 10.0), (-0.01, 1.0), (-1e-4, 3.0), (-5.0, 0.01)])
-def test_gate_extremes(lb, g_std):
+def test_gate_extremes(lb, g_std, o_dtype):
     """lb = -5 with large +-(g + dt_bias), lb close to 0, long cumulative decay
     (FLA skill "fla-kda", correctness checklist: gate numerical extremes)."""
     w = workloads.make_dense("t", 1, 300, 2, 128, 128, 64, torch.bfloat16, 31, g_std=g_std,
                              state_std=0.05, lower_bound=lb)
     w.A_log = w.A_log * 3.0  # exp(A_log) up to 4096: saturates the sigmoid
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
     compare(w, o, st)
 
 
@@ -128,16 +136,16 @@ def test_float32_gate_varlen():
 VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dtype,o_dtype", DTYPES_OUT, ids=DTYPES_OUT_IDS)
 @pytest.mark.parametrize("C", [32, 64])
 @pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
-def test_varlen_contract(dtype, C, mode):
+def test_varlen_contract(dtype, o_dtype, C, mode):
     """Packed sequences with empty slots (first, interior, consecutive, last) and a
     NaN-poisoned capacity tail (attention-gym PR #317, Agent note)."""
     cap = sum(VARLEN_LENGTHS) + 23
     w = workloads.make_varlen("t", VARLEN_LENGTHS, cap, 2, 128, 128, C, dtype, 41, mode=mode)
     t = to_device(w)
-    sentinel = torch.full((1, cap, 2, 128), 12345.0, device="cuda", dtype=dtype)
+    sentinel = torch.full((1, cap, 2, 128), 12345.0, device="cuda", dtype=o_dtype or dtype)
     o, st = run_gpu(w, o=sentinel)
     compare(w, o, st)
     end = int(w.cu_seqlens[-1])
@@ -158,9 +166,38 @@ def test_varlen_contract(dtype, C, mode):
                                 w.v[:, sl].contiguous(), w.g[:, sl].contiguous(),
                                 w.beta[:, sl].contiguous(), w.A_log, w.dt_bias,
                                 w.initial_state[n:n + 1].contiguous())
-        od, sd = run_gpu(wd)
+        od, sd = run_gpu(wd, o_dtype=o_dtype)
         assert torch.equal(od[0], o[0, sl]), f"sequence {n}: packed != alone"
         assert torch.equal(sd[0], st[n])
+
+
+# lengths crossing 32-token boundaries (31, 32, 33, 63, 65, 95, 97) and a packed tail
+C32_LENGTHS = [31, 0, 32, 33, 63, 65, 95, 97, 1]
+
+
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+def test_chunk_size_32_on_the_fused_path(mode):
+    """Helion PR #3290: chunk sizes 32 and 64.  The chunked form computes the same function for
+    every chunk size (the chunk size only blocks the recurrence; the oracle pins C = 1, 16, 32,
+    64 against the token recurrence), and the bf16 tensor-core path runs chunk_size = 32 as
+    64-token chunks.  Pinned here: on sequences crossing 32-token boundaries, packed and dense,
+    chunk_size = 32 and 64 give bitwise the same o and final state on that path, both within
+    the tolerance of the oracle."""
+    cap = sum(C32_LENGTHS) + 9
+    w = workloads.make_varlen("t", C32_LENGTHS, cap, 2, 128, 128, 32, torch.bfloat16, 71, mode=mode)
+    assert kda().kda_chunk_fwd_launches(torch.bfloat16, 1, cap, 2, 128, 128, 32, len(C32_LENGTHS),
+                                        mode) == 1
+    o32, s32 = run_gpu(w, o_dtype=torch.float32)
+    o64, s64 = run_gpu(w, o_dtype=torch.float32, chunk_size=64)
+    end = int(w.cu_seqlens[-1])
+    assert torch.equal(o32[:, :end], o64[:, :end]) and torch.equal(s32, s64)
+    compare(w, o32, s32)
+    wd = workloads.make_dense("t", 2, 97, 2, 128, 128, 32, torch.bfloat16, 72, state_std=0.05,
+                              mode=mode)
+    a, sa = run_gpu(wd)
+    b, sb = run_gpu(wd, chunk_size=64)
+    assert torch.equal(a, b) and torch.equal(sa, sb)
+    compare(wd, a, sa)
 
 
 def test_no_initial_state_equals_zeros_and_no_final_state():
@@ -249,16 +286,16 @@ def test_full_size_sampled(name):
         del o, st
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dtype,o_dtype", DTYPES_OUT, ids=DTYPES_OUT_IDS)
 @pytest.mark.parametrize("C", [32, 64])
 @pytest.mark.parametrize("g_std", [1.0, 30.0], ids=["g1", "g30"])
-def test_nonsafe_gate(dtype, C, g_std):
+def test_nonsafe_gate(dtype, o_dtype, C, g_std):
     """The non-safe in-kernel gate -exp(A_log) softplus(g + dt_bias) (FLA skill "fla-kda",
     "Gate modes"): with raw g ~ N(0, 30) single tokens decay by e^-1000 and more; the result
     stays finite and matches the oracle."""
     w = workloads.make_dense("t", 2, 150, 2, 128, 128, C, dtype, 300 + C, state_std=0.05,
                              g_std=g_std, mode=workloads.GATE_NONSAFE)
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
     assert torch.isfinite(o).all() and torch.isfinite(st).all()
     compare(w, o, st)
 
@@ -281,35 +318,37 @@ def grouped(w, hk):
 @pytest.mark.parametrize("dtype,C", [(torch.bfloat16, 64), (torch.bfloat16, 32), (torch.float32, 64)],
                          ids=["fused", "stagewise-c32", "stagewise-f32"])
 @pytest.mark.parametrize("hk", [1, 2])
-def test_grouped_value_heads(dtype, C, hk):
+@pytest.mark.parametrize("o_dtype", [None, torch.float32], ids=["out-in-dtype", "f32out"])
+def test_grouped_value_heads(dtype, C, hk, o_dtype):
     """GVA (FLA skill "fla-kda", "Correctness checklist": HV > H): 4 value heads over 1 or 2
     query / key heads, against the oracle, and equal to the multi-head call on q and k with
     their heads repeated."""
     w = grouped(workloads.make_dense("t", 2, 130, 4, 128, 128, C, dtype, 600 + C + hk,
                                      state_std=0.05), hk)
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
     compare(w, o, st)
     t = to_device(w)
     r = 4 // hk
     q4 = t["q"].repeat_interleave(r, dim=2)
     k4 = t["k"].repeat_interleave(r, dim=2)
     o2, st2 = kda().kda_chunk_fwd(q4, k4, t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
-                                  w.mode, w.lower_bound, t["initial_state"], True, None, C)
+                                  w.mode, w.lower_bound, t["initial_state"], True, None, C,
+                                  o_dtype=o_dtype)
     torch.cuda.synchronize()
     assert torch.equal(o, o2) and torch.equal(st, st2)
 
 
 # ---- degenerate inputs and a long sequence
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
-def test_beta_zero_reads_the_decayed_state(dtype):
+@pytest.mark.parametrize("dtype,o_dtype", DTYPES_OUT, ids=DTYPES_OUT_IDS)
+def test_beta_zero_reads_the_decayed_state(dtype, o_dtype):
     """beta = 0: the state is only decayed, o_t = S_t^T q_t / sqrt(K) with S_t the initial state
     decayed through token t (a closed form; the oracle pins the same case)."""
     w = workloads.make_dense("t", 1, 70, 2, 128, 128, 64, dtype, 801, state_std=0.05,
                              mode=workloads.GATE_PRE)
     w.beta = torch.zeros_like(w.beta)
     w.g = (w.g.float() * 0.02).to(dtype)  # decay mild enough that S_0 is still visible at the end
-    o, st = run_gpu(w)
+    o, st = run_gpu(w, o_dtype=o_dtype)
     a = w.g.double()[0].cumsum(0)                       # [T, H, K] natural-log decay so far
     S0 = w.initial_state.double()[0]                    # [H, K, V]
     q = w.q.double()[0]                                 # [T, H, K]

@@ -47,22 +47,24 @@ def _launches(w, o_dtype=None):
     (workloads.GATE_PRE, None, False),
     (workloads.GATE_SAFE, torch.float32, False),
 ], ids=["safe-bf16o-state", "pre-bf16o", "safe-f32o"])
-def test_split_equals_one_launch(monkeypatch, mode, o_dtype, state):
+def test_split_equals_one_launch(mode, o_dtype, state):
     B, H, S = split_shape()
     w = workloads.make_dense("t", B, T_SPLIT, H, 128, 128, 64, torch.bfloat16, 71 + mode,
                              state_std=0.05 if state else None, mode=mode)
     assert _launches(w, o_dtype) == 2
     o1, s1 = run_gpu(w, o_dtype=o_dtype)
-    monkeypatch.setenv("KDA_FUSED_SCHEDULE", "plain")
-    assert _launches(w, o_dtype) == 1
-    o2, s2 = run_gpu(w, o_dtype=o_dtype)
-    monkeypatch.delenv("KDA_FUSED_SCHEDULE")
+    kda().kda_test_hooks(one_launch=True)
+    try:
+        assert _launches(w, o_dtype) == 1
+        o2, s2 = run_gpu(w, o_dtype=o_dtype)
+    finally:
+        kda().kda_test_hooks()
     assert torch.equal(o1, o2)
     assert torch.equal(s1, s2)
     check_units(w, o1, s1, _units(B, H, S))
 
 
-def test_split_state_in_place_and_q_l2norm(monkeypatch):
+def test_split_state_in_place_and_q_l2norm():
     """final_state aliasing initial_state (each unit's slot is read by its first piece before
     its last piece writes it), with the deferred q l2norm."""
     B, H, S = split_shape()
@@ -79,9 +81,11 @@ def test_split_state_in_place_and_q_l2norm(monkeypatch):
         return o, st
 
     o1, s1 = run()
-    monkeypatch.setenv("KDA_FUSED_SCHEDULE", "plain")
-    o2, s2 = run()
-    monkeypatch.delenv("KDA_FUSED_SCHEDULE")
+    kda().kda_test_hooks(one_launch=True)
+    try:
+        o2, s2 = run()
+    finally:
+        kda().kda_test_hooks()
     assert torch.equal(o1, o2)
     assert torch.equal(s1, s2)
 

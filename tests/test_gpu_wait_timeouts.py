@@ -27,13 +27,22 @@ def test_normal_runs_count_no_timeouts():
 
 
 @pytest.mark.parametrize("chunk", [0, 2])
-def test_wait_gives_up_and_the_context_stays_usable(monkeypatch, chunk):
+def test_wait_gives_up_and_the_context_stays_usable(chunk):
+    """The give-up reaches the caller without a host synchronisation in the library: the
+    status word of kda_chunk_fwd_ex gets bit 0 on the device, read after the caller's own
+    stream sync; the per-device counter agrees."""
     w = workloads.make_dense("t", 1, 260, 2, 128, 128, 64, torch.bfloat16, 62, state_std=0.05)
     kda().kda_fused_wait_timeouts(reset=True)
-    monkeypatch.setenv("KDA_TEST_WAIT_TIMEOUT_CHUNK", str(chunk))
-    run_gpu(w)  # the launch itself succeeds; its outputs are not valid
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda().kda_test_hooks(wait_timeout_chunk=chunk)
+    try:
+        run_gpu(w, status=status)  # the launch itself succeeds; its outputs are not valid
+    finally:
+        kda().kda_test_hooks()
+    assert int(status.item()) & 1 == 1
     assert kda().kda_fused_wait_timeouts(reset=True) >= 2  # both CTAs gave up a wait
-    monkeypatch.delenv("KDA_TEST_WAIT_TIMEOUT_CHUNK")
-    o, st = run_gpu(w)  # the same context: a normal call matches the oracle again
+    status.zero_()
+    o, st = run_gpu(w, status=status)  # the same context: a normal call matches the oracle
+    assert int(status.item()) == 0
     assert kda().kda_fused_wait_timeouts() == 0
     compare(w, o, st)
