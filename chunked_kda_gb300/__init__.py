@@ -76,7 +76,7 @@ def load_library():
                                          vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, vp,
                                          ctypes.c_size_t, i32, ctypes.c_uint, vp, vp]
         lib.kda_chunk_fwd_ex.restype = ctypes.c_int
-        lib.kda_test_hooks.argtypes = [i32, i32, i32]
+        lib.kda_test_hooks.argtypes = [i32, i32, i32, i32]
         lib.kda_test_hooks.restype = i32
         lib.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp,
                                              vp, i32, i32, i32, i32, i32, i32, vp, i32, i32,
@@ -185,11 +185,12 @@ def kda_chunk_fwd_launches(dtype, B, T, H, K, V, chunk_size, n_seqs=0, mode=GATE
     return int(lib.kda_chunk_fwd_launches(code, ocode, B, T, H, K, V, chunk_size, n_seqs, mode))
 
 
-def kda_test_hooks(wait_timeout_chunk=-1, sm_count=0, one_launch=False) -> None:
-    """The fused path's test hooks (kda_test_hooks in kda.h), process-wide; the defaults turn
-    them off."""
+def kda_test_hooks(wait_timeout_chunk=-1, sm_count=0, one_launch=False, two_pass_d128=False) -> None:
+    """The tensor-core paths' test hooks (kda_test_hooks in kda.h), process-wide; the defaults
+    turn them off."""
     _check("kda_test_hooks", load_library().kda_test_hooks(int(wait_timeout_chunk), int(sm_count),
-                                                           1 if one_launch else 0))
+                                                           1 if one_launch else 0,
+                                                           1 if two_pass_d128 else 0))
 
 
 def kda_fused_wait_timeouts(reset=False) -> int:

@@ -137,10 +137,13 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
     if (chunk_size != 32 && chunk_size != 64) return 0;
     if (qkv_dtype != KDA_F32 && qkv_dtype != KDA_BF16) return 0;
     if (mode != KDA_GATE_PRE && mode != KDA_GATE_SAFE && mode != KDA_GATE_NONSAFE) return 0;
-    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode)) return 0;
     bool packed = n_seqs > 0;
     int N = packed ? n_seqs : B;
-    return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
+    switch (kda::select_path(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode, H, false)) {
+        case kda::Path::Fused: return 0;
+        case kda::Path::TwoPass: return kda::twopass_workspace_bytes(T, H, N, packed);
+        default: return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
+    }
 }
 
 int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T, int H, int K, int V,
@@ -154,21 +157,28 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
     if (packed && B != 1) return -1;
     const int N = packed ? n_seqs : B;
     if (N == 0) return 0;
-    if (kda::fused_supported_dims(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode))
-        return kda::fused_launch_count(N, H, T, packed, o_dtype == KDA_F32);
-    return 6;
+    switch (kda::select_path(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode, H, false)) {
+        case kda::Path::Fused: return kda::fused_launch_count(N, H, T, packed, o_dtype == KDA_F32);
+        case kda::Path::TwoPass: return 2;
+        default: return 6;
+    }
 }
 
-kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch) {
+kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch, int two_pass_d128) {
     g_last_error.clear();
-    kda::set_test_hooks(wait_timeout_chunk, sm_count, one_launch);
+    kda::set_test_hooks(wait_timeout_chunk, sm_count, one_launch, two_pass_d128);
     return KDA_OK;
 }
 
 kda_status kda_fused_wait_timeouts(unsigned int* count, int reset) {
     g_last_error.clear();
     if (!count) return fail(KDA_ERR_INVALID_ARG, "null count");
-    return cuda_status(kda::read_fused_timeouts(count, reset != 0));
+    unsigned a = 0, b = 0;
+    kda_status st = cuda_status(kda::read_fused_timeouts(&a, reset != 0));
+    if (st != KDA_OK) return st;
+    st = cuda_status(kda::read_twopass_timeouts(&b, reset != 0));
+    *count = a + b;
+    return st;
 }
 
 kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -213,8 +223,11 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, kda_dty
                    V, chunk_size, o, o_dtype == KDA_F32, workspace, workspace_bytes,
                    (cudaStream_t)stream, (flags & KDA_FLAG_Q_L2NORM) != 0,
                    n_qk_heads > 0 ? n_qk_heads : H, reinterpret_cast<int*>(status)};
-    if (kda::fused_supported(a)) return cuda_status(kda::launch_chunk_fused(a));
-    return cuda_status(kda::launch_chunk_precise(a));
+    switch (kda::select_path(a.qkv_bf16, K, V, chunk_size, (int)mode, H, a.q_l2norm)) {
+        case kda::Path::Fused: return cuda_status(kda::launch_chunk_fused(a));
+        case kda::Path::TwoPass: return cuda_status(kda::launch_chunk_twopass(a));
+        default: return cuda_status(kda::launch_chunk_precise(a));
+    }
 }
 
 kda_status kda_recurrent_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,

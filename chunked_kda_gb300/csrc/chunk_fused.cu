@@ -135,41 +135,6 @@ __host__ __device__ constexpr uint32_t gs_off(int ch, int q) {
 }
 __host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&p);
-}
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-// x = hi + lo: hi = bf16(x), lo = bf16(x - hi), for the pair (a, b)
-__device__ __forceinline__ void pack_split(float a, float b, uint32_t& hi, uint32_t& lo) {
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-    float2 hf = __bfloat1622float2(h2);
-    hi = *reinterpret_cast<uint32_t*>(&h2);
-    lo = pack_bf16(a - hf.x, b - hf.y);
-}
-template <typename OT>
-__device__ __forceinline__ OT to_out(float x);
-template <>
-__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
-template <>
-__device__ __forceinline__ float to_out<float>(float x) { return x; }
-
-__device__ __forceinline__ void st_s32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
-}
-
-
 struct Params {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -1193,16 +1158,20 @@ bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16,
 
 // Test hooks, process-wide, set only through kda_test_hooks (off by default): the chunk at which
 // every CTA gives up a wait (-1: none), an SM count to plan the split schedule for (0: the
-// device's), and one launch per call whatever the plan.
+// device's), one launch per call whatever the plan, and the two-pass kernels for K = V = 128.
 static std::atomic<int> g_hook_stall_chunk{-1};
 static std::atomic<int> g_hook_sm_count{0};
 static std::atomic<int> g_hook_one_launch{0};
+static std::atomic<int> g_hook_two_pass{0};
 
-void set_test_hooks(int stall_chunk, int sm_count, int one_launch) {
+void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_d128) {
     g_hook_stall_chunk.store(stall_chunk < 0 ? -1 : stall_chunk);
     g_hook_sm_count.store(sm_count > 0 ? sm_count : 0);
     g_hook_one_launch.store(one_launch ? 1 : 0);
+    g_hook_two_pass.store(two_pass_d128 ? 1 : 0);
 }
+
+bool hook_two_pass_d128() { return g_hook_two_pass.load(std::memory_order_relaxed) != 0; }
 
 static bool split_allowed() { return g_hook_one_launch.load(std::memory_order_relaxed) == 0; }
 

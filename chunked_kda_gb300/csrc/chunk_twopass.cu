@@ -1,0 +1,1064 @@
+// Two-pass chunked KDA forward for bf16 inputs with K = V in {128, 256} (sm_103a).
+//
+// A K = V = 256 head does not fit the single fused kernel: its FP32 state alone is 256 KB, all
+// of TMEM.  The work is split where the chunked form allows it (FLA skill "fla-kda", "Public
+// code map": the intra / solve stages depend only on the chunk's own inputs, the state scan is
+// the one sequential stage):
+//
+//   pass 1, chunk_prep_kernel: one CTA per (chunk, head), every chunk in parallel.  a1 gate
+//     activation and chunk-local log2 cumsum, a2 the causal scores on 16-token sub-blocks as one
+//     tcgen05 MMA of N = 160 causal columns per 128 key channels (Helion PR #3290, causal columns
+//     only; midpoint anchors and paired offsets, FLA skill "fla-kda", "Safe gate numerical
+//     note"), a3 T = (I + Akk)^-1.  It writes T diag(beta) (bf16) and Aqk (fp32) for the chunk,
+//     as the byte images of the shared-memory operand tiles the second pass multiplies with.
+//   pass 2, chunk_chain_kernel: one CTA per (sequence, head, 128 value channels).  a1 again
+//     (cheaper than storing G), the operands k 2^G, s q 2^G, k 2^(Gl - G), and the state chain
+//     a4-a6 on tcgen05 with the FP32 state h^T [128 v x K] in TMEM:
+//        Y^T  = h^T (k 2^G)^T,  o^T = h^T (s q 2^G)^T
+//        vn^T = v^T (T diag beta)^T - Y^T (T diag beta)^T        (v_new = u - w h)
+//        o^T += vn^T Aqk^T  (tf32, A = the FP32 vn^T accumulator)
+//        h^T <- h^T Diag(2^Gl) + vn^T (k 2^(Gl - G))
+// Rows beyond the end of a sequence are zero in every operand.
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kda_internal.h"
+#include "sm100.cuh"
+
+namespace kda {
+namespace twopass {
+
+using namespace sm100;
+
+constexpr int C = 64;
+constexpr uint32_t IMG_TP = 0;          // T diag(beta) bf16 [64][64] K-major, 128-byte swizzle
+constexpr uint32_t IMG_AQK = 8192;      // Aqk fp32 [64 i][64 j] K-major, two 32-column halves
+constexpr uint32_t IMG_BYTES = 24576;   // per (chunk slot, head) in the workspace
+constexpr int SB_ROWS = 160;            // causal score columns of a 64-token chunk
+__host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
+constexpr int LD = 68;                  // fp32 row stride of the solve matrices
+
+__device__ unsigned int g_twopass_timeouts = 0;  // bounded waits that gave up
+
+// ------------------------------------------------------------------ pass 1
+namespace prep {
+constexpr int NTHR = 256;
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_SAH = 0;         // score rows [128 ch][128 rows] MN-major bf16 (k, q)
+constexpr uint32_t OFF_SB = 32768;      // score cols [128 ch][160] MN-major, 3 x 16 KB
+constexpr uint32_t OFF_AS = 0;          //   after the last score MMA: Akk^T fp32 [64][68]
+constexpr uint32_t OFF_TF = 17408;      //   T fp32 [64][68]
+constexpr uint32_t OFF_XS = 34816;      //   block products fp32 [4][16][24]
+constexpr uint32_t OFF_TP = 40960;      //   T diag(beta) image, 8 KB
+constexpr uint32_t OFF_AQK = 49152;     //   Aqk image, 16 KB
+constexpr uint32_t OFF_GC = 81920;      // gate sums of the row quarters fp32 [3][128]
+constexpr uint32_t OFF_GM = 83456;      // G at the sub-block midpoints fp32 [4][128]
+constexpr uint32_t OFF_BETA = 85504;    // beta fp32 [64]
+constexpr uint32_t OFF_BAR = 85760;     // mbarriers: score MMAs, drain after a give-up
+constexpr uint32_t OFF_MISC = 85776;    // tmem base
+constexpr uint32_t SMEM_END = 85792;
+constexpr uint32_t SMEM_BYTES = SMEM_END + 1024;
+static_assert(OFF_SB + 3 * 16384 <= OFF_GC && OFF_AQK + 16384 <= OFF_SB + 3 * 16384, "layout");
+static_assert(OFF_XS + 4 * 16 * 24 * 4 <= OFF_TP && OFF_TF + 64 * LD * 4 <= OFF_XS, "layout");
+static_assert(OFF_GC + 3 * 128 * 4 <= OFF_GM && OFF_GM + 4 * 128 * 4 <= OFF_BETA, "layout");
+static_assert(OFF_BETA + 256 <= OFF_BAR, "layout");
+
+struct Params {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* beta;
+    const void* g;
+    const float* A_log;
+    const float* dt_bias;
+    int mode;
+    float lb;
+    int H, hr;  // value heads; value heads per query / key head
+    ChunkMap cm;
+    uint8_t* img;  // [slots][H][IMG_BYTES]
+    int* status;   // optional caller word: bit 0 when a wait gives up
+};
+
+template <int K, typename GT>
+__global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int slot = blockIdx.x, h = blockIdx.y, H = p.H;
+    int n, t0, len, bos, eos;
+    if (!p.cm.map(slot, n, t0, len, bos, eos)) return;  // not a chunk: the whole CTA leaves
+    const int Hk = H / p.hr, hq = h / p.hr;
+    constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
+    using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;  // a channel pair
+
+    float* gcarry = reinterpret_cast<float*>(smem + OFF_GC);
+    float* gmid = reinterpret_cast<float*>(smem + OFF_GM);
+    float* bsm = reinterpret_cast<float*>(smem + OFF_BETA);
+    float* As = reinterpret_cast<float*>(smem + OFF_AS);
+    float* Tf = reinterpret_cast<float*>(smem + OFF_TF);
+    float* Xs = reinterpret_cast<float*>(smem + OFF_XS);
+    const uint32_t bar = sb + OFF_BAR;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(bar + 8, 1);
+        fence_mbar_init();
+    }
+    if (w == 0) tmem_alloc(sb + OFF_MISC, 256);
+    if (tid < C) bsm[tid] = (tid < len) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    bool ok = true;  // false (in every thread) once a bounded wait gave up: no further MMA
+
+    // Thread: channel pair (d0, d0 + 1) of the 128-channel half, rows 16 rq .. 16 rq + 15 (one
+    // sub-block); ch0 / ch1 is the pair in swapped order on lanes with bit 2 set, so a warp's
+    // 16-byte stores to a channel-major tile cover all eight bank groups.
+    const int cbp = w & 1, rq = w >> 1;
+    const int d0 = 2 * (32 * cbp + l);
+    const int swap = (l >> 2) & 1;
+    const int ch0 = d0 + swap, ch1 = d0 + 1 - swap;
+    const float scale = rsqrtf((float)K);
+    const GT* gptr = reinterpret_cast<const GT*>(p.g);
+    const float lbl2 = p.lb * kLog2e;
+    const float m = (p.mode == 1) ? lbl2 : kLog2e;
+
+    for (int half = 0; half < K / 128; ++half) {
+        const int cb = 128 * half;
+        // the own rows: k, q pairs and the gate pair, all loads issued first
+        uint32_t kr[16], qr[16];
+        GW gw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * rq + i;
+            const bool valid = r < len;
+            const size_t tok = (size_t)(t0 + (valid ? r : len - 1));
+            kr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.k + (tok * Hk + hq) * K + cb + d0)) : 0u;
+            qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (tok * Hk + hq) * K + cb + d0)) : 0u;
+            gw[i] = __ldg(reinterpret_cast<const GW*>(gptr + (tok * H + h) * K + cb + d0));
+        }
+        // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair)
+        float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
+        if (p.mode == 1) {
+            nA.x = -expf(__ldg(p.A_log + h * K + cb + d0)) * kLog2e;
+            nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1)) * kLog2e;
+            if (p.dt_bias) {
+                nAd.x = nA.x * __ldg(p.dt_bias + h * K + cb + d0);
+                nAd.y = nA.y * __ldg(p.dt_bias + h * K + cb + d0 + 1);
+            }
+        }
+        float2 gv[16], acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float2 a;
+            if constexpr (kGateBf16) {
+                a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
+            } else {
+                a = gw[i];
+            }
+            if (p.mode == 1) {
+                float2 z = __ffma2_rn(nA, a, nAd);
+                z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
+                a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
+            }
+            const float mv = (16 * rq + i < len) ? m : 0.f;  // rows past the end add zero
+            acc = __ffma2_rn(make_float2(mv, mv), a, acc);
+            gv[i] = acc;
+        }
+        if (rq < 3) *reinterpret_cast<float2*>(gcarry + rq * 128 + d0) = acc;
+        __syncthreads();  // carries out; the previous half's readers of gmid are done
+        float2 cy = make_float2(0.f, 0.f);
+        for (int q = 0; q < rq; ++q) cy = __fadd2_rn(cy, *reinterpret_cast<const float2*>(gcarry + q * 128 + d0));
+        float G0[16], G1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 g2 = __fadd2_rn(gv[i], cy);
+            G0[i] = swap ? g2.y : g2.x;
+            G1[i] = swap ? g2.x : g2.y;
+        }
+        gmid[rq * 128 + ch0] = G0[8];
+        gmid[rq * 128 + ch1] = G1[8];
+        // the previous half's score MMA has read the operand tiles (every thread waits; the
+        // verdict is made the same in all of them)
+        const bool w_ok = !(half > 0 && ok) || mbar_wait(bar, (uint32_t)((half - 1) & 1));
+        if (ok && !__syncthreads_and(w_ok)) {  // midpoints out, operand tiles free
+            if (tid == 0) {
+                atomicAdd(&g_twopass_timeouts, 1u);
+                if (p.status) atomicOr(p.status, 1);
+            }
+            ok = false;
+        } else if (!ok) {
+            __syncthreads();
+        }
+
+        // a2 operands, channel-major [128 ch][rows] tiles: rows k 2^(G - G_m(rq)), s q 2^(G - G_m(rq));
+        // columns of sub-block bi >= rq: k 2^(G_m(rq) - G) 2^(G_m(bi) - G_m(rq)) (the second factor
+        // <= 1: paired offsets)
+        {
+            const float gm0 = G0[8], gm1 = G1[8];
+            float R0[4], R1[4];
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {
+                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
+                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+            }
+            const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t chk = 2 * rq + hf;
+                const uint32_t r0 = sw128(ch0, chk), r1 = sw128(ch1, chk);
+                uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
+                float kf0[8], kf1[8];
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                    float ke0[2], ke1[2], qe0[2], qe1[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = 8 * hf + 2 * pr + u;
+                        const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
+                        const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
+                        const float kv0 = __uint_as_float(__byte_perm(kr[i], 0u, sel0));
+                        const float kv1 = __uint_as_float(__byte_perm(kr[i], 0u, sel1));
+                        const float qv0 = __uint_as_float(__byte_perm(qr[i], 0u, sel0));
+                        const float qv1 = __uint_as_float(__byte_perm(qr[i], 0u, sel1));
+                        ke0[u] = kv0 * e0;
+                        ke1[u] = kv1 * e1;
+                        qe0[u] = scale * qv0 * e0;
+                        qe1[u] = scale * qv1 * e1;
+                        kf0[2 * pr + u] = kv0 * f0;
+                        kf1[2 * pr + u] = kv1 * f1;
+                    }
+                    ak0[pr] = pack_bf16(ke0[0], ke0[1]);
+                    ak1[pr] = pack_bf16(ke1[0], ke1[1]);
+                    aq0[pr] = pack_bf16(qe0[0], qe0[1]);
+                    aq1[pr] = pack_bf16(qe1[0], qe1[1]);
+                }
+                st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
+                st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
+                st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
+                st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+                    if (bi < rq) continue;
+                    const uint32_t n0 = (uint32_t)(sb_off(bi) + 16 * rq + 8 * hf);
+                    const uint32_t base = sb + OFF_SB + (n0 >> 6) * 16384u;
+                    const uint32_t cn = (n0 & 63u) >> 3;
+                    uint32_t s0[4], s1[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        s0[pr] = pack_bf16(kf0[2 * pr] * R0[bi], kf0[2 * pr + 1] * R0[bi]);
+                        s1[pr] = pack_bf16(kf1[2 * pr] * R1[bi], kf1[2 * pr + 1] * R1[bi]);
+                    }
+                    st_s128(base + sw128(ch0, cn), s0[0], s0[1], s0[2], s0[3]);
+                    st_s128(base + sw128(ch1, cn), s1[0], s1[1], s1[2], s1[3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint64_t b = desc_at(umma_desc(sb + OFF_SB, 16384, 1024), kk * 2048);
+                uint64_t a = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
+                umma_bf16(tmem, a, b, id_s, (half > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(bar);
+        }
+    }
+    {
+        const bool w_ok = !ok || mbar_wait(bar, (uint32_t)((K / 128 - 1) & 1));
+        if (!__syncthreads_and(w_ok)) {
+            if (tid == 0 && ok) {
+                atomicAdd(&g_twopass_timeouts, 1u);
+                if (p.status) atomicOr(p.status, 1);
+            }
+            ok = false;
+        }
+    }
+    tc_fence_after();
+
+    // the strictly upper 16 x 16 blocks of T diag(beta) are zero
+    for (int idx = tid; idx < 64 * 8; idx += NTHR) {
+        const int i = idx >> 3, c8 = idx & 7;
+        if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
+    }
+    // ---- read the scores: warps w and w + 4 share the TMEM lanes of quadrant w & 3 and take
+    // alternate 16-column pieces.  Akk rows (lanes 0-63, beta-scaled, strictly lower) into the
+    // solve matrix, Aqk rows (lanes 64-127) into the fp32 image.
+    if (ok) {
+        const int lq = w & 3, part = w >> 2;
+        const int row = 32 * lq + l;
+        const int i = row & 63;
+        const bool is_q = row >= 64;
+        const int bi = i >> 4;
+        const int bmin = 2 * (lq & 1);
+        const bool own_a = bi == bmin;
+        const float b_i = bsm[i];
+        const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16);
+#pragma unroll 1
+        for (int tt = 0; tt < 2; ++tt) {
+            const int t = part + 2 * tt;
+            float va[16], vb[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) { va[e] = 0.f; vb[e] = 0.f; }
+            if (t <= bmin) tmem_ld16(tl + sb_off(bmin) + 16 * t, va);
+            if (t <= bmin + 1) tmem_ld16(tl + sb_off(bmin + 1) + 16 * t, vb);
+            if (t <= bmin + 1) tmem_wait_ld();
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
+            if (!is_q) {
+                if (t <= bi) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = 16 * t + e;
+                        As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;
+                    }
+                }
+            } else {
+                const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 16 * t + 4 * c4 + e;
+                        x[e] = __float_as_uint((j <= i) ? sv[4 * c4 + e] : 0.f);
+                    }
+                    st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- a3 on warps 0-3: T = (I + Akk)^-1 into the bf16 T diag(beta) image.  Diagonal 16 x 16
+    // blocks by forward substitution, one thread per column; then the off-diagonal blocks as a
+    // 2 x 2 recursion on 32 x 32 blocks with m16n8k8 tf32 MMAs.
+    if (w < 4 && ok) {
+        if (w < 2) {
+            const int b = 2 * w + (l >> 4), cc = l & 15;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < 15; ++j) {
+                const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
+#pragma unroll
+                for (int mq = (j + 1) / 4; mq < 4; ++mq) {
+                    const float4 c4 = col[mq];
+                    const float av[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * mq + e > j) x[4 * mq + e] = fmaf(-av[e], x[j], x[4 * mq + e]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
+            __syncwarp();
+            const int i = 16 * b + cc;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j0 = 16 * b + 2 * e;
+                pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
+            }
+            st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
+            st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
+        }
+        bar_sync(1, 128);
+        const int gq = l >> 2, tq = l & 3;
+        auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks >= nk) break;
+                const int kc = kc0 + 8 * ks;
+                uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]), to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
+                                 to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
+                                 to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8) {
+                    uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
+                                      to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
+                    mma_tf32_16x8x8(acc[n8], a, bb);
+                }
+            }
+        };
+        auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int kc = k0 + 8 * ks;
+                uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]), to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
+                                 to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
+                                 to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8) {
+                    uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
+                                      to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
+                    mma_tf32_16x8x8(acc[n8], a, bb);
+                }
+            }
+        };
+        auto store_X = [&](float* X, const float (&acc)[2][4]) {
+#pragma unroll
+            for (int n8 = 0; n8 < 2; ++n8) {
+                X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
+                X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
+                X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
+                X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
+            }
+        };
+        auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
+#pragma unroll
+            for (int n8 = 0; n8 < 2; ++n8) {
+                const int j = c0 + 8 * n8 + 2 * tq;
+                if (keep) {
+                    Tf[(r0 + gq) * LD + j] = -acc[n8][0];
+                    Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
+                    Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
+                    Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
+                }
+                const float b0 = -bsm[j], b1 = -bsm[j + 1];
+                const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
+                st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
+                st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
+            }
+        };
+        if (w < 2) {  // T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)
+            const int r0 = 32 * w + 16, c0 = 32 * w;
+            float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            prod_A_T(xa, r0, c0, 2, c0);
+            float* X = Xs + w * (16 * 24);
+            store_X(X, xa);
+            __syncwarp();
+            float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            prod_T_X(ta, r0, r0, X);
+            store_T(r0, c0, ta, true);
+        }
+        bar_sync(1, 128);
+        const int rb = 2 + (w >> 1), cbk = w & 1;
+        {  // X[r][c] = sum_t A[r][t] T[t][c], r = 2, 3; c = 0, 1
+            float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            prod_A_T(xa, 16 * rb, 16 * cbk, 4 - 2 * cbk, 16 * cbk);
+            store_X(Xs + w * (16 * 24), xa);
+        }
+        bar_sync(1, 128);
+        {  // T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]
+            float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+            for (int s = 2; s <= 3; ++s)
+                if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cbk) * (16 * 24));
+            store_T(16 * rb, 16 * cbk, ta, false);
+        }
+    }
+    __syncthreads();
+    // the T diag(beta) and Aqk tile images out, 24 KB contiguous per (slot, head)
+    {
+        uint4* dst = reinterpret_cast<uint4*>(p.img + ((size_t)slot * H + h) * IMG_BYTES);
+        const uint4* tp = reinterpret_cast<const uint4*>(smem + OFF_TP);
+        const uint4* aq = reinterpret_cast<const uint4*>(smem + OFF_AQK);
+        for (int x = tid; x < (int)(IMG_BYTES / 16); x += NTHR)
+            dst[x] = x < 512 ? tp[x] : aq[x - 512];
+    }
+    // a CTA that gave up a wait lets its MMAs in flight finish before it frees TMEM
+    if (!ok && tid == 0) {
+        umma_commit(bar + 8);
+        mbar_wait(bar + 8, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (w == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+}  // namespace prep
+
+// ------------------------------------------------------------------ pass 2
+namespace chain {
+constexpr int NTHR = 512, NGRP = 256;            // operand group (warps 0-7), chain group (8-15)
+constexpr uint32_t BAR_OPS = 1, BAR_CHAIN = 2;   // named barriers of the groups
+
+// shared memory (bytes from a 1024-aligned base); K-dependent sizes
+template <int K>
+struct Smem {
+    static constexpr uint32_t TILE = 64 * K * 2;           // [64 tok][K] bf16, K / 64 boxes of 8 KB
+    static constexpr uint32_t KT = 0;                      // k tile (TMA) -> k 2^G in place
+    static constexpr uint32_t QT = KT + TILE;              // q tile (TMA) -> s q 2^G in place
+    static constexpr uint32_t KD = QT + TILE;              // k 2^(Gl - G), two buffers (parity)
+    static constexpr uint32_t V = KD + 2 * TILE;           // v tile [64 tok][128 v], 16 KB
+    static constexpr uint32_t IMG = V + 16384;             // T diag(beta) + Aqk images, two buffers
+    static constexpr uint32_t YA = IMG + 2 * IMG_BYTES;    // Y^T, then v_new^T, bf16 [128 v][64 tok]
+    static constexpr uint32_t GAM = YA + 16384;            // 2^Glast fp32 [2][K]
+    static constexpr uint32_t GC = GAM + 2 * K * 4;        // gate sums of the row groups fp32 [4][K]
+    static constexpr uint32_t QSS = GC + 4 * K * 4;        // sums of q^2 per row fp32 [2][4][64]
+    static constexpr uint32_t BAR = QSS + 2 * 4 * 64 * 4;  // mbarriers
+    static constexpr uint32_t MISC = BAR + 128;            // tmem base, abort flag, loads issued
+    static constexpr uint32_t END = MISC + 32;
+    static constexpr uint32_t BYTES = END + 1024;
+    static_assert(BYTES <= 232448, "shared memory of one CTA");
+    static_assert(KD % 1024 == 0 && V % 1024 == 0 && IMG % 1024 == 0 && YA % 1024 == 0, "align");
+};
+// TMEM columns: h^T fp32 [128 v][K], its bf16 copy (K / 2 columns), Y^T / v_new^T, o^T
+template <int K>
+struct Tmem {
+    static constexpr uint32_t H = 0, HA = K, Y = K + K / 2, O = Y + 64;
+    static constexpr uint32_t COLS = 512;
+    static_assert(O + 64 <= COLS, "TMEM");
+};
+
+enum { B_TILES = 0, B_OPS, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
+
+struct Params {
+    const __nv_bfloat16* beta;
+    const void* g;
+    const float* A_log;
+    const float* dt_bias;
+    const float* h0;
+    float* hT;
+    const int32_t* cu;
+    void* o;
+    int mode;
+    float lb;
+    int T, H, hr, V;
+    int qnorm;           // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
+    ChunkMap cm;
+    const uint8_t* img;  // pass 1's images [slots][H][IMG_BYTES]
+    int* status;         // optional caller word: bit 0 when a wait gives up
+};
+
+struct Sync {
+    uint32_t bars;
+    volatile uint32_t* abort_flag;
+    int* status;
+    __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * i; }
+    __device__ __forceinline__ void wait(int i, uint32_t parity) const {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar(i), parity)) {
+            atomicAdd(&g_twopass_timeouts, 1u);
+            if (status) atomicOr(status, 1);
+            *abort_flag = 1u;
+        }
+    }
+    __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
+    __device__ __forceinline__ void group_wait(int i, uint32_t parity, bool leader, uint32_t barid) const {
+        if (leader) wait(i, parity);
+        bar_sync(barid, NGRP);
+    }
+};
+
+// k, q tiles of chunk t (K / 64 boxes of 64 channels) into the operand buffers
+__device__ __forceinline__ void load_tiles(uint32_t sb, uint32_t kt, uint32_t qt, const CUtensorMap* tk,
+                                           const CUtensorMap* tq, int nbox, int hq, int t, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, (uint32_t)nbox * 2u * 8192u);
+    for (int cb = 0; cb < nbox; ++cb) {
+        tma_load_3d(sb + kt + cb * 8192, tk, 64 * cb, hq, t, bar);
+        tma_load_3d(sb + qt + cb * 8192, tq, 64 * cb, hq, t, bar);
+    }
+}
+
+template <int K, typename GT, typename OT>
+__global__ void __launch_bounds__(NTHR, 1)
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, Params p) {
+    using S = Smem<K>;
+    using TM = Tmem<K>;
+    constexpr int NBOX = K / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + S::MISC);
+    Sync sy{sb + S::BAR, misc + 1, p.status};
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    const int vb = blockIdx.x, n = blockIdx.y, h = blockIdx.z, H = p.H;
+    const int hq = h / p.hr;
+    long bos, eos;
+    if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
+    else      { bos = (long)n * p.T; eos = bos + p.T; }
+    const int nt = (int)((eos - bos + C - 1) / C);
+    const int slot0 = p.cm.first_slot(n, (int)bos);
+    float* gam = reinterpret_cast<float*>(smem + S::GAM);
+
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
+        fence_mbar_init();
+        misc[1] = 0;
+        misc[2] = misc[3] = misc[4] = 0;  // loads issued: tiles, v, images
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (w == 0) tmem_alloc(sb + S::MISC, TM::COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    volatile uint32_t* issued = misc + 2;
+
+    if (w < 8) {
+        // ================= operand group: a1 and the chain's operands of every chunk.  Thread:
+        // channel pair (d0, d0 + 1) of each 128-channel part, rows 16 rg .. 16 rg + 15
+        const int rg = tid >> 6, r0 = 16 * rg;
+        const GT* gptr = reinterpret_cast<const GT*>(p.g);
+        constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
+        using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;
+        const float m = (p.mode == 1) ? p.lb * kLog2e : kLog2e;
+        const float scale = rsqrtf((float)K);
+        float* gc = reinterpret_cast<float*>(smem + S::GC);
+        for (int c = 0; c < nt; ++c) {
+            const long t0 = bos + (long)c * C;
+            const int len = (int)min((long)C, eos - t0);
+            const uint32_t kdb = sb + S::KD + (uint32_t)(c & 1) * S::TILE;
+#pragma unroll 1
+            for (int part = 0; part < K / 128; ++part) {
+                const int d0 = 128 * part + 2 * (tid & 63);
+                GW gw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    gw[i] = __ldg(reinterpret_cast<const GW*>(
+                        gptr + ((size_t)(t0 + min(r0 + i, len - 1)) * H + h) * K + d0));
+                float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
+                if (p.mode == 1) {
+                    nA.x = -expf(__ldg(p.A_log + h * K + d0)) * kLog2e;
+                    nA.y = -expf(__ldg(p.A_log + h * K + d0 + 1)) * kLog2e;
+                    if (p.dt_bias) {
+                        nAd.x = nA.x * __ldg(p.dt_bias + h * K + d0);
+                        nAd.y = nA.y * __ldg(p.dt_bias + h * K + d0 + 1);
+                    }
+                }
+                // a1: the row group's inclusive sums, then the groups before it
+                float2 gv[16], acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float2 a;
+                    if constexpr (kGateBf16) {
+                        a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
+                    } else {
+                        a = gw[i];
+                    }
+                    if (p.mode == 1) {
+                        float2 z = __ffma2_rn(nA, a, nAd);
+                        z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
+                        a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
+                    }
+                    const float mv = (r0 + i < len) ? m : 0.f;
+                    acc = __ffma2_rn(make_float2(mv, mv), a, acc);
+                    gv[i] = acc;
+                }
+                *reinterpret_cast<float2*>(gc + rg * K + d0) = acc;
+                // this chunk's k / q tiles have landed; the carries are out
+                if (tid == 0 && part == 0) sy.wait(B_TILES, (uint32_t)(c & 1));
+                bar_sync(BAR_OPS, NGRP);
+                float2 cy = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 t2 = *reinterpret_cast<const float2*>(gc + q * K + d0);
+                    if (q < rg) cy = __fadd2_rn(cy, t2);
+                    tot = __fadd2_rn(tot, t2);
+                }
+                // Gl: the chunk's last row (rows past the end add zero, so it is the total)
+                if (rg == 0) {
+                    gam[(c & 1) * K + d0] = ex2_fast(tot.x);
+                    gam[(c & 1) * K + d0 + 1] = ex2_fast(tot.y);
+                }
+                // k 2^G and s q 2^G in place, k 2^(Gl - G) into this chunk's kd buffer; rows past
+                // the end of the sequence are zero.  The pair's word of row r in a token-major tile
+                // of K / 64 boxes [64 tok][64 ch]
+                const uint32_t wbox = (uint32_t)(d0 >> 6) * 8192u, wchunk = (uint32_t)((d0 & 63) >> 3),
+                               wbyte = (uint32_t)(d0 & 7) * 2u;
+                float qsq[16];  // q^2 of the pair, per row (deferred q l2norm)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = r0 + i;
+                    const float2 G = __fadd2_rn(gv[i], cy);
+                    const uint32_t off = wbox + sw128((uint32_t)r, wchunk) + wbyte;
+                    uint32_t kw = 0u, qw = 0u, dw = 0u;
+                    qsq[i] = 0.f;
+                    if (r < len) {
+                        const uint32_t kx = ld_s32(sb + S::KT + off), qx = ld_s32(sb + S::QT + off);
+                        qsq[i] = fmaf(bf_lo(qx), bf_lo(qx), bf_hi(qx) * bf_hi(qx));
+                        const float2 e = make_float2(ex2_fast(G.x), ex2_fast(G.y));
+                        const float2 d = make_float2(ex2_fast(tot.x - G.x), ex2_fast(tot.y - G.y));
+                        const float2 kv = make_float2(bf_lo(kx), bf_hi(kx));
+                        const float2 qv = make_float2(bf_lo(qx), bf_hi(qx));
+                        const float2 ke = __fmul2_rn(kv, e);
+                        const float2 qe = __fmul2_rn(__fmul2_rn(qv, e), make_float2(scale, scale));
+                        const float2 kd = __fmul2_rn(kv, d);
+                        kw = pack_bf16(ke.x, ke.y);
+                        qw = pack_bf16(qe.x, qe.y);
+                        dw = pack_bf16(kd.x, kd.y);
+                    }
+                    st_s32(sb + S::KT + off, kw);
+                    st_s32(sb + S::QT + off, qw);
+                    st_s32(kdb + off, dw);
+                }
+                if (p.qnorm) {
+                    // sum over the warp's 64 channels: butterfly over lane bits 4..1 leaves lane l
+                    // with row (l >> 1) & 15, then the pair (l, l ^ 1) completes it
+                    float v8[8], v4[4], v2[2];
+                    const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v8[i] = (b4 ? qsq[8 + i] : qsq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? qsq[i] : qsq[8 + i], 16);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
+                    float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+                    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+                    // partial j = part * 2 + (which 64 channels of the part)
+                    float* qss = reinterpret_cast<float*>(smem + S::QSS) + (c & 1) * 256;
+                    if ((l & 1) == 0)
+                        qss[(2 * part + ((tid >> 5) & 1)) * 64 + r0 + ((l >> 1) & 15)] = v1;
+                }
+            }
+            fence_proxy_async_smem();
+            bar_sync(BAR_OPS, NGRP);
+            if (tid == 0) mbar_arrive(sy.bar(B_OPS));
+        }
+    } else {
+        // ================= chain group
+        const int ct = tid - NGRP;
+        const int lg = w & 3, hch = (w - 8) >> 2;
+        const int vlane = 32 * lg + l;                  // value channel within the block
+        const int vch = 128 * vb + vlane;               // value channel
+        const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
+        const size_t st_off = ((size_t)n * H + h) * (size_t)K * p.V;
+        const uint32_t yab = sb + S::YA;
+        // state columns of this thread: key channels hch * K / 2 .. + K / 2 - 1, in pieces of 32
+        auto ld_h = [&](int s, float (&hv)[32]) {
+            tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, hv);
+            tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16, hv + 16);
+        };
+        auto st_h = [&](int s, const float (&hv)[32]) {
+            tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, reinterpret_cast<const uint32_t*>(hv));
+            tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16,
+                      reinterpret_cast<const uint32_t*>(hv) + 16);
+        };
+        auto st_hA = [&](int s, const float (&hv)[32]) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hv[2 * e], hv[2 * e + 1]);
+            tmem_st16(tmem + lane_base + TM::HA + (K / 4) * hch + 16 * s, r);
+        };
+        // the thread's 32 tokens (32 hch ..) of a [128 v][64 tok] fp32 accumulator row -> the
+        // bf16 K-major A tile (row = value channel, 128 bytes, 128-byte swizzle)
+        auto acc_to_bf16_tile = [&](uint32_t col) {
+            float x[32];
+            tmem_ld16(tmem + lane_base + col + 32 * hch, x);
+            tmem_ld16(tmem + lane_base + col + 32 * hch + 16, x + 16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_s128(yab + sw128((uint32_t)vlane, (uint32_t)(4 * hch + q)), pack_bf16(x[8 * q], x[8 * q + 1]),
+                        pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                        pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+        };
+        auto load_img = [&](int c) {
+            issued[2] = issued[2] + 1u;
+            const int b = c & 1;
+            mbar_arrive_expect_tx(sy.bar(B_IMG0 + b), IMG_BYTES);
+            bulk_load(sb + S::IMG + (uint32_t)b * IMG_BYTES,
+                      p.img + ((size_t)(slot0 + c) * H + h) * IMG_BYTES, IMG_BYTES, sy.bar(B_IMG0 + b));
+        };
+        auto load_v = [&](long t) {
+            issued[1] = issued[1] + 1u;
+            mbar_arrive_expect_tx(sy.bar(B_VFULL), 16384);
+            for (int cb = 0; cb < 2; ++cb)
+                tma_load_3d(sb + S::V + cb * 8192, &tm_v, 128 * vb + 64 * cb, h, (int)t, sy.bar(B_VFULL));
+        };
+        if (nt > 0) {
+            // the initial state (or zero) into TMEM, fp32 and the bf16 copy
+#pragma unroll 1
+            for (int s = 0; s < K / 64; ++s) {
+                float hv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int kch = (K / 2) * hch + 32 * s + j;
+                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
+                }
+                st_h(s, hv);
+                st_hA(s, hv);
+            }
+            tmem_wait_st();
+            if (ct == 0) {
+                issued[0] = 1u;
+                load_tiles(sb, S::KT, S::QT, &tm_k, &tm_q, NBOX, hq, (int)bos, sy.bar(B_TILES));
+                load_img(0);
+                load_v(bos);
+            }
+        }
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NGRP);
+        for (int c = 0; c < nt; ++c) {
+            const long t0 = bos + (long)c * C;
+            const int len = (int)min((long)C, eos - t0);
+            const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * IMG_BYTES;
+            // ---- Y^T = h^T (k 2^G)^T, o^T = h^T (s q 2^G)^T
+            if (ct == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
+            if (ct == 0 && !sy.aborted()) {
+                tc_fence_after();
+                if (c + 1 < nt) load_img(c + 1);  // its buffer's readers (chunk c - 1) are done
+                const uint32_t id_y = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < K / 16; ++kk) {
+                    const uint32_t boff = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
+                    uint64_t bk = desc_at(umma_desc(sb + S::KT, 16, 1024), boff);
+                    uint64_t bq = desc_at(umma_desc(sb + S::QT, 16, 1024), boff);
+                    umma_bf16_ta(tmem + TM::Y, tmem + TM::HA + 8 * kk, bk, id_y, kk > 0);
+                    umma_bf16_ta(tmem + TM::O, tmem + TM::HA + 8 * kk, bq, id_y, kk > 0);
+                }
+                umma_commit(sy.bar(B_YDONE));
+            }
+            sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
+            tc_fence_after();
+            // the operand tiles are free: the next chunk's k and q
+            if (ct == 0 && c + 1 < nt && !sy.aborted()) {
+                issued[0] = issued[0] + 1u;
+                load_tiles(sb, S::KT, S::QT, &tm_k, &tm_q, NBOX, hq, (int)(t0 + C), sy.bar(B_TILES));
+            }
+            // ---- Y^T -> bf16 A tile; h^T <- h^T Diag(2^Glast)
+            acc_to_bf16_tile(TM::Y);
+            {
+                const float* gm = gam + (c & 1) * K + (K / 2) * hch;
+#pragma unroll 1
+                for (int s = 0; s < K / 64; ++s) {
+                    float hv[32];
+                    ld_h(s, hv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hv[j] *= gm[32 * s + j];
+                    st_h(s, hv);
+                }
+                tmem_wait_st();
+            }
+            if (w == 8) sy.wait(B_VFULL, (uint32_t)(c & 1));
+            bar_sync(BAR_CHAIN, NGRP);
+            if (len < C) {
+                // rows past the end may hold the next sequence's tokens or NaN padding; T diag(beta)
+                // has zero columns there, which would not cancel a NaN
+                for (int idx = ct; idx < (C - len) * 16; idx += NGRP) {
+                    const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
+                    st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(BAR_CHAIN, NGRP);
+            // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns
+            if (ct == 0) {
+                sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
+                if (!sy.aborted()) {
+                    tc_fence_after();
+                    const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
+                    const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
+                        uint64_t b = desc_at(umma_desc(img + IMG_TP, 16, 1024), kk * 32);
+                        umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
+                        uint64_t b = desc_at(umma_desc(img + IMG_TP, 16, 1024), kk * 32);
+                        umma_bf16(tmem + TM::Y, a, b, id_n, 1);
+                    }
+                    umma_commit(sy.bar(B_VNDONE));
+                }
+            }
+            sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
+            tc_fence_after();
+            if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);
+            // ---- o^T += v_new^T Aqk^T (tf32: A = the FP32 v_new^T accumulator)
+            if (ct == 0 && !sy.aborted()) {
+                const uint32_t id_o = idesc_tf32(128, 64);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint64_t bo = desc_at(umma_desc(img + IMG_AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
+                                          (uint32_t)(kk & 3) * 32u);
+                    umma_tf32_ta(tmem + TM::O, tmem + TM::Y + 8 * kk, bo, id_o, 1);
+                }
+            }
+            // ---- v_new^T -> bf16 A tile, then h^T += v_new^T (k 2^(Gl - G))
+            acc_to_bf16_tile(TM::Y);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_sync(BAR_CHAIN, NGRP);
+            if (ct == 0 && !sy.aborted()) {
+                tc_fence_after();
+                const uint32_t id_h = idesc_bf16(128, K, 0, 1);
+                const uint32_t kdb = sb + S::KD + (uint32_t)(c & 1) * S::TILE;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
+                    uint64_t b = desc_at(umma_desc(kdb, 8192, 1024), kk * 2048);
+                    umma_bf16(tmem + TM::H, a, b, id_h, 1);
+                }
+                umma_commit(sy.bar(B_OHDONE));
+            }
+            sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
+            tc_fence_after();
+            // ---- bf16 h^T for the next chunk; o out
+            {
+#pragma unroll 1
+                for (int s = 0; s < K / 64; ++s) {
+                    float hv[32];
+                    ld_h(s, hv);
+                    tmem_wait_ld();
+                    st_hA(s, hv);
+                }
+                float ov[32];
+                tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
+                tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
+                tmem_wait_ld();
+                if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps)
+                    const float* qss = reinterpret_cast<const float*>(smem + S::QSS) + (c & 1) * 256 + 32 * hch;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float ssum = 0.f;
+#pragma unroll
+                        for (int q = 0; q < K / 64; ++q) ssum += qss[q * 64 + j];
+                        ov[j] *= rsqrtf(ssum + kQNormEps);
+                    }
+                }
+                OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * p.V + vch;
+                const size_t ostride = (size_t)H * p.V;
+                const int nvalid = len - 32 * hch;
+#pragma unroll
+                for (int j = 0; j < 32; ++j, op += ostride)
+                    if (j < nvalid) *op = to_out<OT>(ov[j]);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            bar_sync(BAR_CHAIN, NGRP);
+        }
+        if (p.hT && !sy.aborted()) {
+#pragma unroll 1
+            for (int s = 0; s < K / 64; ++s) {
+                float hv[32];
+                if (nt > 0) {
+                    ld_h(s, hv);
+                    tmem_wait_ld();
+                } else {  // an empty sequence passes its state through
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
+            }
+        }
+        // after a give-up: let the last load of each kind land before the CTA leaves
+        if (ct == 0 && sy.aborted()) {
+            if (issued[0] > 0) mbar_wait(sy.bar(B_TILES), (issued[0] - 1u) & 1u);
+            if (issued[1] > 0) mbar_wait(sy.bar(B_VFULL), (issued[1] - 1u) & 1u);
+            const uint32_t ni = issued[2];
+            if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
+        }
+    }
+    // every MMA was waited for, unless a wait gave up: then let the ones in flight finish
+    if (sy.aborted() && tid == NGRP) {
+        umma_commit(sy.bar(B_DRAIN));
+        mbar_wait(sy.bar(B_DRAIN), 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (w == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM::COLS);
+    }
+}
+}  // namespace chain
+}  // namespace twopass
+
+// ------------------------------------------------------------------ host side
+namespace fused {
+bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D);
+}
+
+// bf16, K = V in {128, 256}, a bounded gate (the sub-block anchors rely on it), at most 65535
+// heads (a grid dimension).  Both chunk sizes run as 64-token chunks, as on the fused path.
+bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H) {
+    return qkv_bf16 && K == V && (K == 128 || K == 256) && (mode == 0 || mode == 1) && H <= 65535;
+}
+
+size_t twopass_workspace_bytes(int T, int H, int N, bool packed) {
+    ChunkMap cm{packed ? reinterpret_cast<const int32_t*>(1) : nullptr, N, T, twopass::C};
+    return (size_t)cm.n_slots() * (size_t)H * twopass::IMG_BYTES;
+}
+
+cudaError_t read_twopass_timeouts(unsigned* count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, twopass::g_twopass_timeouts, sizeof(unsigned));
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(twopass::g_twopass_timeouts, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
+namespace {
+template <int K, typename GT, typename OT>
+cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
+    using namespace twopass;
+    const int Hk = a.Hk > 0 ? a.Hk : a.H;
+    const int hr = a.H / Hk;
+    // pass 1: every (chunk, head)
+    {
+        auto kp = prep::chunk_prep_kernel<K, GT>;
+        cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, prep::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        prep::Params pp{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta,
+                        a.g, a.A_log, a.dt_bias, a.mode, a.lb, a.H, hr, cm, (uint8_t*)a.ws, a.status};
+        kp<<<dim3(slots, a.H), prep::NTHR, prep::SMEM_BYTES, a.stream>>>(pp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // pass 2: every (sequence, head, 128 value channels), the value blocks of a head side by
+    // side so that they share their reads of q, k, g and the images in L2
+    CUtensorMap mq, mk, mv;
+    const long tokens = (long)a.B * a.T;
+    if (!fused::make_map(&mq, a.q, tokens, Hk, K) || !fused::make_map(&mk, a.k, tokens, Hk, K) ||
+        !fused::make_map(&mv, a.v, tokens, a.H, a.V))
+        return cudaErrorInvalidValue;
+    auto kc = chain::chunk_chain_kernel<K, GT, OT>;
+    constexpr uint32_t smem = chain::Smem<K>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    chain::Params cp{(const __nv_bfloat16*)a.beta, a.g, a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o,
+                     a.mode, a.lb, a.T, a.H, hr, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
+                     a.status};
+    kc<<<dim3(a.V / 128, a.N, a.H), chain::NTHR, smem, a.stream>>>(mq, mk, mv, cp);
+    return cudaGetLastError();
+}
+template <int K>
+cudaError_t launch_dims(const FwdArgs& a, const ChunkMap& cm, int slots) {
+    if (a.g_bf16)
+        return a.o_f32 ? launch_k<K, __nv_bfloat16, float>(a, cm, slots)
+                       : launch_k<K, __nv_bfloat16, __nv_bfloat16>(a, cm, slots);
+    return a.o_f32 ? launch_k<K, float, float>(a, cm, slots) : launch_k<K, float, __nv_bfloat16>(a, cm, slots);
+}
+}  // namespace
+
+cudaError_t launch_chunk_twopass(const FwdArgs& a) {
+    const ChunkMap cm{a.cu, a.N, a.T, twopass::C};
+    const int slots = cm.n_slots();
+    if (!a.ws || a.ws_bytes < (size_t)slots * (size_t)a.H * twopass::IMG_BYTES) return cudaErrorInvalidValue;
+    return a.K == 256 ? launch_dims<256>(a, cm, slots) : launch_dims<128>(a, cm, slots);
+}
+
+}  // namespace kda

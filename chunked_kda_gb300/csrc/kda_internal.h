@@ -91,8 +91,28 @@ cudaError_t launch_chunk_fused(const FwdArgs& a);
 int fused_launch_count(int N, int H, int T, bool packed, bool o_f32);
 // fused-kernel mbarrier waits that gave up on the current device (synchronises), optional reset
 cudaError_t read_fused_timeouts(unsigned* count, bool reset);
+// bf16 two-pass path (K = V in {128, 256}): a parallel pass per (chunk, head) writes T diag(beta)
+// and Aqk into the workspace, a chain pass per (sequence, head, 128 value channels) runs the state
+// scan; tcgen05 / TMEM / TMA throughout
+bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H);
+size_t twopass_workspace_bytes(int T, int H, int N, bool packed);
+cudaError_t launch_chunk_twopass(const FwdArgs& a);
+cudaError_t read_twopass_timeouts(unsigned* count, bool reset);
 // the fused path's test hooks (kda_test_hooks)
-void set_test_hooks(int stall_chunk, int sm_count, int one_launch);
+void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_d128);
+bool hook_two_pass_d128();
+
+// Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, bounded gate), the
+// two-pass tensor-core kernels (bf16, K = V = 256, bounded gate; K = V = 128 too under the test
+// hook), or the stage-by-stage float32 kernels (everything else)
+enum class Path { Fused, TwoPass, Precise };
+inline Path select_path(bool qkv_bf16, int K, int V, int C, int mode, int H, bool q_l2norm) {
+    (void)q_l2norm;  // every path supports the deferred q l2norm
+    const bool two = twopass_supported_dims(qkv_bf16, K, V, mode, H);
+    if (fused_supported_dims(qkv_bf16, K, V, C, mode) && !(two && hook_two_pass_d128())) return Path::Fused;
+    if (two && (K == 256 || hook_two_pass_d128())) return Path::TwoPass;
+    return Path::Precise;
+}
 
 // sets the message kda_last_error() returns on this host thread
 void record_error(const char* msg);

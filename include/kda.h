@@ -132,7 +132,8 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
 /*
  * Kernel launches one kda_chunk_fwd call with these sizes makes on the current device, for
  * profiling and launch accounting: 0 when there are no sequences, 6 on the stage-by-stage
- * path, 1 on the fused path, 2 when the fused path uses its split schedule.  n_seqs as for
+ * path, 2 on the two-pass path, 1 on the fused path, 2 when the fused path uses its split
+ * schedule.  n_seqs as for
  * kda_chunk_workspace_bytes (0 = dense).  Invalid sizes or enums: -1.  No device work.
  *
  * Split schedule (dense bf16 inputs, K = V = 128): one CTA per SM runs one (sequence, head)
@@ -156,7 +157,11 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  * o = (1/sqrt(K)) (q 2^G) h + Aqk v_new.
  * Paths: bf16 inputs with K = V = 128 and a pre-gated or safe gate run the
  * fused tensor-core kernel (one launch, or two for the split schedule described
- * with kda_chunk_fwd_launches);
+ * with kda_chunk_fwd_launches, no workspace); bf16 inputs with K = V = 256 and a
+ * pre-gated or safe gate run the two-pass tensor-core kernels (two launches: a
+ * parallel pass per chunk and head that writes T diag(beta) and Aqk into the
+ * workspace, 24 KB per 64-token chunk and head, then the state chain per
+ * sequence, head and 128 value channels);
  * everything else runs the stage-by-stage path (six launches, a workspace),
  * which computes in FP32 except that with bf16 inputs the safe-gate scores, the
  * WY terms and the output are tf32 tensor-core products with FP32 accumulation.
@@ -169,10 +174,10 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  *   o          [B, T, H, V], dtype o_dtype (output): the qkv dtype, or KDA_F32
  *              to keep the forward's FP32 result without the final rounding
  *   chunk_size 32 or 64 (Helion PR #3290: the two chunk sizes FLA's KDA accepts).
- *              The bf16 tensor-core path (K = V = 128, pre-gated or safe gate)
- *              runs both as 64-token chunks: the chunked form is exact for any
- *              chunk size, so only the rounding differs; the float32 path uses
- *              the size given.
+ *              The bf16 tensor-core paths (K = V = 128 or 256, pre-gated or safe
+ *              gate) run both as 64-token chunks: the chunked form is exact for
+ *              any chunk size, so only the rounding differs; the float32 path
+ *              uses the size given.
  *   K, V       64, 128 or 256 (K == V on the bf16 tensor-core path; any pair
  *              of these on the float32 path)
  *   workspace  device scratch of at least kda_chunk_workspace_bytes(...) bytes,
@@ -325,20 +330,20 @@ kda_status kda_recurrent_fwd_ex(const void* q, const void* k, const void* v, kda
 
 /* static, NUL-terminated description of a status code */
 /*
- * Diagnostics of the fused path's bounded waits.  Every mbarrier wait of the fused
- * chunked kernel gives up after a fixed number of polls; a CTA whose wait gave up adds to a
- * per-device counter, stops waiting, issuing MMAs and copies, lets the ones in flight finish
- * (bounded), frees its TMEM and returns, so the context stays usable but that launch's
- * outputs are not valid.  kda_fused_wait_timeouts writes the counter of the current device
- * to *count (0 after normal runs) and zeroes it when reset != 0.  It copies from the device
+ * Diagnostics of the tensor-core paths' bounded waits.  Every mbarrier wait of the fused
+ * and two-pass chunked kernels gives up after a fixed number of polls; a CTA whose wait gave
+ * up adds to a per-device counter, stops waiting, issuing MMAs and copies, lets the ones in
+ * flight finish (bounded), frees its TMEM and returns, so the context stays usable but that
+ * launch's outputs are not valid.  kda_fused_wait_timeouts writes the counters of the current
+ * device to *count (their sum, 0 after normal runs) and zeroes them when reset != 0.  It copies from the device
  * and therefore synchronises with it: a diagnostic call, not for the hot path.  Null count:
  * KDA_ERR_INVALID_ARG; a failing copy: KDA_ERR_CUDA.
  */
 kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
 
 /*
- * Test hooks of the fused path, process-wide, all off by default and read by nothing else
- * (no environment variables).  For tests only; set them back to (-1, 0, 0) afterwards.
+ * Test hooks of the tensor-core paths, process-wide, all off by default and read by nothing
+ * else (no environment variables).  For tests only; set them back to (-1, 0, 0, 0) afterwards.
  *   wait_timeout_chunk  >= 0: every CTA of later fused launches waits, at that chunk and
  *                       with a short limit, on an mbarrier nothing completes, and takes the
  *                       give-up path (counted by kda_fused_wait_timeouts, flagged in the
@@ -346,9 +351,11 @@ kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
  *   sm_count            > 0: plan the split schedule (kda_chunk_fwd_launches) for this many
  *                       SMs instead of the device's; 0: the device's
  *   one_launch          nonzero: never split a fused call into two launches
+ *   two_pass_d128       nonzero: bf16 K = V = 128 calls run the two-pass kernels (with their
+ *                       workspace, kda_chunk_workspace_bytes_ex) instead of the fused one
  * Always KDA_OK; no device work.
  */
-kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch);
+kda_status kda_test_hooks(int wait_timeout_chunk, int sm_count, int one_launch, int two_pass_d128);
 
 const char* kda_status_string(kda_status status);
 

@@ -48,7 +48,7 @@ def lib():
     L.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp, i32,
                                    i32, i32, i32, i32, i32, i32, vp, i32, vp, ctypes.c_size_t, i32,
                                    ctypes.c_uint, vp, vp]
-    L.kda_test_hooks.argtypes = [i32, i32, i32]
+    L.kda_test_hooks.argtypes = [i32, i32, i32, i32]
     L.kda_recurrent_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp, vp, vp,
                                        i32, i32, i32, i32, i32, i32, vp, i32, i32, ctypes.c_uint,
                                        vp]
@@ -195,7 +195,9 @@ def test_launch_counts(lib):
     f = lib.kda_chunk_fwd_launches
     SAFE, NONSAFE = 1, 2
     assert f(F32, F32, 1, 128, 2, 64, 64, 64, 0, SAFE) == 6           # stage-by-stage
-    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 6
+    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 2      # two-pass
+    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 6   # unbounded gate: stages
+    assert f(BF16, BF16, 4, 4096, 64, 128, 256, 64, 0, SAFE) == 6      # K != V: stages
     assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 6
     assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, SAFE) == 1   # fused, packed
     assert f(BF16, F32, 4, 4096, 64, 128, 128, 64, 0, SAFE) in (1, 2)  # split: by the SM count
@@ -228,7 +230,19 @@ def test_workspace_bytes(lib):
     # the fused bf16 kernel keeps every intermediate on chip
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) == 0  # fused too
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) > 0
+    # the two-pass path (K = V = 256): 24 KB of T diag(beta) and Aqk per 64-token chunk and head
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) == 4 * 64 * 64 * 24576
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 32, 0) == 4 * 64 * 64 * 24576
+    # packed: floor(T_cap / 64) + N + 1 chunk slots
+    assert lib.kda_chunk_workspace_bytes(BF16, 1, 20480, 32, 256, 256, 64, 16) == (320 + 17) * 32 * 24576
+    # the two-pass test hook moves K = V = 128 onto it
+    lib.kda_test_hooks(-1, 0, 0, 1)
+    try:
+        assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 4 * 64 * 64 * 24576
+        assert lib.kda_chunk_fwd_launches(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 2
+    finally:
+        lib.kda_test_hooks(-1, 0, 0, 0)
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
     # by gate mode: the non-safe gate runs on the stage-by-stage path (scratch for bf16 too)
     ex = lib.kda_chunk_workspace_bytes_ex
     ex.restype = ctypes.c_size_t
@@ -248,7 +262,7 @@ def test_split_schedule_plan(lib):
     SAFE = 1
 
     def launches(B, T, H, o=BF16, S=152):
-        lib.kda_test_hooks(-1, S, 0)
+        lib.kda_test_hooks(-1, S, 0, 0)
         return f(BF16, o, B, T, H, 128, 128, 64, 0, SAFE)
 
     assert launches(2, 720, 114) == 2        # 228 units: the last wave half full
@@ -264,9 +278,9 @@ def test_split_schedule_plan(lib):
     assert launches(1, 4096, 12, S=8) == 2   # any SM count
     assert launches(1, 20480, 32, S=8) == 1  # a whole number of waves
     assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 3, SAFE) == 1  # packed: never split
-    lib.kda_test_hooks(-1, 152, 1)  # one launch whatever the plan
+    lib.kda_test_hooks(-1, 152, 1, 0)  # one launch whatever the plan
     assert f(BF16, BF16, 2, 720, 114, 128, 128, 64, 0, SAFE) == 1
-    lib.kda_test_hooks(-1, 0, 0)  # hooks off again
+    lib.kda_test_hooks(-1, 0, 0, 0)  # hooks off again
 
 
 def test_no_environment_hooks():

@@ -1,0 +1,176 @@
+"""The two-pass tensor-core path of kda_chunk_fwd (bf16, K = V in {128, 256}, bounded gate):
+pass 1 per (chunk, head) writes T diag(beta) and Aqk into the workspace, pass 2 per (sequence,
+head, 128 value channels) runs the state chain.  K = V = 256 takes it by default; K = V = 128
+takes it under the library's test hook (the fused kernel is the default there).  Checked
+against the float64 oracle element by element, with the varlen contract's bitwise parts, on
+small inputs spanning several chunks and ragged tails."""
+import contextlib
+
+import pytest
+import torch
+
+import oracle
+from chunked_kda_gb300 import workloads
+from parity import check_o, check_state, to_device, valid_mask
+from test_gpu_chunk import compare, grouped, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def kda():
+    import chunked_kda_gb300
+
+    return chunked_kda_gb300
+
+
+@contextlib.contextmanager
+def two_pass(D):
+    """K = V = D on the two-pass path (a hook for D = 128, the default for D = 256)."""
+    if D == 128:
+        kda().kda_test_hooks(two_pass_d128=True)
+    try:
+        yield
+    finally:
+        kda().kda_test_hooks()
+
+
+def _launches(w):
+    n = 0 if w.cu_seqlens is None else w.n_seqs
+    return kda().kda_chunk_fwd_launches(w.q.dtype, w.B, w.T, w.H, w.K, w.V, w.chunk_size, n, w.mode)
+
+
+@pytest.mark.parametrize("o_dtype", [None, torch.float32], ids=["bf16out", "f32out"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("T", [1, 17, 64, 65, 130, 200])
+@pytest.mark.parametrize("D", [128, 256])
+def test_two_pass_dense_small(D, T, C, o_dtype):
+    w = workloads.make_dense("t", 2, T, 2, D, D, C, torch.bfloat16, 901 + T + D, state_std=0.05)
+    with two_pass(D):
+        assert _launches(w) == 2
+        o, st = run_gpu(w, o_dtype=o_dtype)
+    compare(w, o, st)
+
+
+VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
+
+
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+@pytest.mark.parametrize("D", [128, 256])
+def test_two_pass_varlen_contract(D, mode):
+    """Packed sequences with empty slots first, interior, consecutive and last, and a
+    NaN-poisoned capacity tail (attention-gym PR #317, Agent note): the tail is not written,
+    empty slots pass their state through and each packed sequence equals the same sequence run
+    alone, bit for bit."""
+    cap = sum(VARLEN_LENGTHS) + 23
+    w = workloads.make_varlen("t", VARLEN_LENGTHS, cap, 2, D, D, 64, torch.bfloat16, 941, mode=mode)
+    t = to_device(w)
+    with two_pass(D):
+        sentinel = torch.full((1, cap, 2, D), 12345.0, device="cuda", dtype=torch.bfloat16)
+        o, st = run_gpu(w, o=sentinel)
+        end = int(w.cu_seqlens[-1])
+        assert torch.equal(o[:, end:], torch.full_like(o[:, end:], 12345.0))
+        for n, L in enumerate(VARLEN_LENGTHS):
+            if L == 0:
+                assert torch.equal(st[n], t["initial_state"][n])
+        cu = w.cu_seqlens.tolist()
+        for n, L in enumerate(VARLEN_LENGTHS):
+            if L == 0:
+                continue
+            sl = slice(cu[n], cu[n + 1])
+            wd = workloads.Workload("d", 1, L, 2, D, D, 64, mode, w.lower_bound,
+                                    w.q[:, sl].contiguous(), w.k[:, sl].contiguous(),
+                                    w.v[:, sl].contiguous(), w.g[:, sl].contiguous(),
+                                    w.beta[:, sl].contiguous(), w.A_log, w.dt_bias,
+                                    w.initial_state[n:n + 1].contiguous())
+            od, sd = run_gpu(wd)
+            assert torch.equal(od[0], o[0, sl]), f"sequence {n}: packed != alone"
+            assert torch.equal(sd[0], st[n])
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("lb,g_std", [(-5.0, 10.0), (-1e-4, 3.0)])
+def test_two_pass_gate_extremes(lb, g_std):
+    """lb = -5 with a saturated sigmoid, and lb close to 0 (FLA skill "fla-kda", correctness
+    checklist: gate numerical extremes), with a float32 o held to the plain bound."""
+    w = workloads.make_dense("t", 1, 300, 2, 256, 256, 64, torch.bfloat16, 951, g_std=g_std,
+                             state_std=0.05, lower_bound=lb)
+    w.A_log = w.A_log * 3.0
+    o, st = run_gpu(w, o_dtype=torch.float32)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("hk", [1, 2])
+def test_two_pass_grouped_value_heads(hk):
+    """GVA: 4 value heads over 1 or 2 query / key heads, against the oracle and bitwise equal to
+    the multi-head call on repeated q and k heads."""
+    w = grouped(workloads.make_dense("t", 2, 130, 4, 256, 256, 64, torch.bfloat16, 960 + hk,
+                                     state_std=0.05), hk)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+    t = to_device(w)
+    r = 4 // hk
+    o2, st2 = kda().kda_chunk_fwd(t["q"].repeat_interleave(r, dim=2), t["k"].repeat_interleave(r, dim=2),
+                                  t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"], w.mode,
+                                  w.lower_bound, t["initial_state"], True, None, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(st, st2)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_two_pass_float32_gate_is_bitwise_the_bf16_gate(D):
+    w = workloads.make_dense("t", 2, 150, 2, D, D, 64, torch.bfloat16, 971, state_std=0.05)
+    with two_pass(D):
+        o16, s16 = run_gpu(w)
+        w.g = w.g.float()
+        o32, s32 = run_gpu(w)
+    assert torch.equal(o16, o32) and torch.equal(s16, s32)
+    compare(w, o32, s32)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_two_pass_q_l2norm(D):
+    """The deferred q l2norm (attention-gym PR #345) on query rows scaled by 10^U(-3, 3) with
+    an all-zero row, against the oracle with the same option."""
+    w = workloads.make_dense("t", 1, 150, 2, D, D, 64, torch.bfloat16, 981, state_std=0.05)
+    g = torch.Generator().manual_seed(982)
+    sc = torch.pow(10.0, torch.rand((1, 150, 2, 1), generator=g) * 6 - 3)
+    sc[:, 70] = 0.0
+    w.q = (w.q.float() * sc).to(w.q.dtype)
+    with two_pass(D):
+        o, st = run_gpu(w, q_l2norm=True, o_dtype=torch.float32)
+    o_ref, s_ref = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.A_log, w.dt_bias, w.mode,
+                                  w.lower_bound, w.initial_state, None, q_l2norm=True)
+    check_o(o, o_ref, torch.bfloat16)
+    check_state(st, s_ref, torch.bfloat16)
+
+
+def test_two_pass_status_word_stays_clear():
+    w = workloads.make_dense("t", 1, 200, 2, 256, 256, 64, torch.bfloat16, 991, state_std=0.05)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda().kda_fused_wait_timeouts(reset=True)
+    o, st = run_gpu(w, status=status)
+    assert int(status.item()) == 0 and kda().kda_fused_wait_timeouts() == 0
+    compare(w, o, st)
+
+
+def test_two_pass_no_initial_state_and_in_place_state():
+    w = workloads.make_dense("t", 2, 100, 2, 256, 256, 64, torch.bfloat16, 992)
+    o1, s1 = run_gpu(w)
+    zeros = torch.zeros((2, 2, 256, 256), device="cuda")
+    o2, s2 = run_gpu(w, initial_state=zeros)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    w2 = workloads.make_dense("t", 2, 100, 2, 256, 256, 64, torch.bfloat16, 993, state_std=0.05)
+    oa, sa = run_gpu(w2)
+    t = to_device(w2)
+    S = t["initial_state"].clone()
+    ob, _ = kda().kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
+                                w2.mode, w2.lower_bound, S, True, None, 64, final_state=S)
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob) and torch.equal(sa, S)
