@@ -33,9 +33,26 @@ namespace twopass {
 using namespace sm100;
 
 constexpr int C = 64;
-constexpr uint32_t IMG_TP = 0;          // T diag(beta) bf16 [64][64] K-major, 128-byte swizzle
-constexpr uint32_t IMG_AQK = 8192;      // Aqk fp32 [64 i][64 j] K-major, two 32-column halves
-constexpr uint32_t IMG_BYTES = 24576;   // per (chunk slot, head) in the workspace
+// Pass 1's output per (chunk slot, head) in the workspace: the byte images of the operand tiles
+// pass 2 multiplies with, in the shared-memory layouts of its MMAs (128-byte swizzle)
+template <int K>
+struct Img {
+    static constexpr uint32_t TP = 0;               // T diag(beta) bf16 [64][64] K-major
+    static constexpr uint32_t AQK = 8192;           // Aqk fp32 [64 i][64 j] K-major, 2 x 32 columns
+    static constexpr uint32_t HANDOFF = 24576;      //   (T diag(beta), Aqk: 24 KB)
+    static constexpr uint32_t TILE = 64 * K * 2;    // [64 tok][K] bf16 in K / 64 boxes [64][64]
+    static constexpr uint32_t KG = HANDOFF;         // k 2^G
+    static constexpr uint32_t QG = KG + TILE;       // s q 2^G
+    static constexpr uint32_t KD = QG + TILE;       // k 2^(Gl - G)
+    static constexpr uint32_t GAM = KD + TILE;      // 2^Glast fp32 [K]
+    static constexpr uint32_t QSS = GAM + K * 4;    // sums of q^2 per row fp32 [64]
+    static constexpr uint32_t BYTES = QSS + 256;
+    static_assert(BYTES % 256 == 0, "image size");
+};
+// the word of channel pair (d, d + 1), token r in a [64 tok][K] image of K / 64 swizzled boxes
+__host__ __device__ __forceinline__ uint32_t pair_off(int r, int d) {
+    return (uint32_t)(d >> 6) * 8192u + sm100::sw128((uint32_t)r, (uint32_t)((d & 63) >> 3)) + (uint32_t)(d & 7) * 2u;
+}
 constexpr int SB_ROWS = 160;            // causal score columns of a 64-token chunk
 __host__ __device__ constexpr int sb_off(int b) { return 8 * b * (b + 1); }  // 0, 16, 48, 96
 constexpr int LD = 68;                  // fp32 row stride of the solve matrices
@@ -53,17 +70,18 @@ constexpr uint32_t OFF_TF = 17408;      //   T fp32 [64][68]
 constexpr uint32_t OFF_XS = 34816;      //   block products fp32 [4][16][24]
 constexpr uint32_t OFF_TP = 40960;      //   T diag(beta) image, 8 KB
 constexpr uint32_t OFF_AQK = 49152;     //   Aqk image, 16 KB
-constexpr uint32_t OFF_GC = 81920;      // gate sums of the row quarters fp32 [3][128]
-constexpr uint32_t OFF_GM = 83456;      // G at the sub-block midpoints fp32 [4][128]
-constexpr uint32_t OFF_BETA = 85504;    // beta fp32 [64]
-constexpr uint32_t OFF_BAR = 85760;     // mbarriers: score MMAs, drain after a give-up
-constexpr uint32_t OFF_MISC = 85776;    // tmem base
-constexpr uint32_t SMEM_END = 85792;
+constexpr uint32_t OFF_GC = 81920;      // gate sums of the row quarters fp32 [4][128]
+constexpr uint32_t OFF_GM = 83968;      // G at the sub-block midpoints fp32 [4][128]
+constexpr uint32_t OFF_BETA = 86016;    // beta fp32 [64]
+constexpr uint32_t OFF_QSS = 86272;     // partial sums of q^2 per row fp32 [4][64]
+constexpr uint32_t OFF_BAR = 87296;     // mbarriers: score MMAs, drain after a give-up
+constexpr uint32_t OFF_MISC = 87312;    // tmem base
+constexpr uint32_t SMEM_END = 87328;
 constexpr uint32_t SMEM_BYTES = SMEM_END + 1024;
 static_assert(OFF_SB + 3 * 16384 <= OFF_GC && OFF_AQK + 16384 <= OFF_SB + 3 * 16384, "layout");
 static_assert(OFF_XS + 4 * 16 * 24 * 4 <= OFF_TP && OFF_TF + 64 * LD * 4 <= OFF_XS, "layout");
-static_assert(OFF_GC + 3 * 128 * 4 <= OFF_GM && OFF_GM + 4 * 128 * 4 <= OFF_BETA, "layout");
-static_assert(OFF_BETA + 256 <= OFF_BAR, "layout");
+static_assert(OFF_GC + 4 * 128 * 4 <= OFF_GM && OFF_GM + 4 * 128 * 4 <= OFF_BETA, "layout");
+static_assert(OFF_BETA + 256 <= OFF_QSS && OFF_QSS + 4 * 64 * 4 <= OFF_BAR, "layout");
 
 struct Params {
     const __nv_bfloat16* q;
@@ -76,8 +94,9 @@ struct Params {
     float lb;
     int H, hr;  // value heads; value heads per query / key head
     ChunkMap cm;
-    uint8_t* img;  // [slots][H][IMG_BYTES]
+    uint8_t* img;  // [slots][H][Img<K>::BYTES]
     int* status;   // optional caller word: bit 0 when a wait gives up
+    int qnorm;     // write the sums of q^2 per row (deferred q l2norm)
 };
 
 template <int K, typename GT>
@@ -170,10 +189,20 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
             acc = __ffma2_rn(make_float2(mv, mv), a, acc);
             gv[i] = acc;
         }
-        if (rq < 3) *reinterpret_cast<float2*>(gcarry + rq * 128 + d0) = acc;
+        *reinterpret_cast<float2*>(gcarry + rq * 128 + d0) = acc;
         __syncthreads();  // carries out; the previous half's readers of gmid are done
-        float2 cy = make_float2(0.f, 0.f);
-        for (int q = 0; q < rq; ++q) cy = __fadd2_rn(cy, *reinterpret_cast<const float2*>(gcarry + q * 128 + d0));
+        float2 cy = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * 128 + d0);
+            if (q < rq) cy = __fadd2_rn(cy, t2);
+            tot = __fadd2_rn(tot, t2);  // G of the chunk's last row (rows past the end add zero)
+        }
+        uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
+        if (rq == 0) {  // 2^Glast of the pair
+            *reinterpret_cast<float2*>(img + Img<K>::GAM + (cb + d0) * 4) =
+                make_float2(ex2_fast(tot.x), ex2_fast(tot.y));
+        }
         float G0[16], G1[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -201,6 +230,12 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
         // <= 1: paired offsets)
         {
             const float gm0 = G0[8], gm1 = G1[8];
+            // chain operands from the anchored products: k 2^G = (k 2^(G - Gm)) 2^Gm,
+            // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gm - G)) 2^(Gl - Gm)
+            const float Pm0 = ex2_fast(gm0), Pm1 = ex2_fast(gm1);
+            const float tl0 = swap ? tot.y : tot.x, tl1 = swap ? tot.x : tot.y;
+            const float Lm0 = ex2_fast(tl0 - gm0), Lm1 = ex2_fast(tl1 - gm1);
+            float qsq[16];
             float R0[4], R1[4];
 #pragma unroll
             for (int bi = 0; bi < 4; ++bi) {
@@ -232,6 +267,18 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                         qe1[u] = scale * qv1 * e1;
                         kf0[2 * pr + u] = kv0 * f0;
                         kf1[2 * pr + u] = kv1 * f1;
+                        qsq[i] = fmaf(qv0, qv0, qv1 * qv1);
+                        // the pair's words in natural channel order (d0 low, d0 + 1 high)
+                        const uint32_t wkg = swap ? pack_bf16(ke1[u] * Pm1, ke0[u] * Pm0)
+                                                  : pack_bf16(ke0[u] * Pm0, ke1[u] * Pm1);
+                        const uint32_t wqg = swap ? pack_bf16(qe1[u] * Pm1, qe0[u] * Pm0)
+                                                  : pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1);
+                        const uint32_t wkd = swap ? pack_bf16(kf1[2 * pr + u] * Lm1, kf0[2 * pr + u] * Lm0)
+                                                  : pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1);
+                        const uint32_t po = pair_off(16 * rq + i, cb + d0);
+                        *reinterpret_cast<uint32_t*>(img + Img<K>::KG + po) = wkg;
+                        *reinterpret_cast<uint32_t*>(img + Img<K>::QG + po) = wqg;
+                        *reinterpret_cast<uint32_t*>(img + Img<K>::KD + po) = wkd;
                     }
                     ak0[pr] = pack_bf16(ke0[0], ke0[1]);
                     ak1[pr] = pack_bf16(ke1[0], ke1[1]);
@@ -257,6 +304,25 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                     st_s128(base + sw128(ch0, cn), s0[0], s0[1], s0[2], s0[3]);
                     st_s128(base + sw128(ch1, cn), s1[0], s1[1], s1[2], s1[3]);
                 }
+            }
+            if (p.qnorm) {
+                // sum over the warp's 64 channels: butterfly over lane bits 4..1 leaves lane l with
+                // row (l >> 1) & 15, then the pair (l, l ^ 1) completes it
+                float v8[8], v4[4], v2[2];
+                const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v8[i] = (b4 ? qsq[8 + i] : qsq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? qsq[i] : qsq[8 + i], 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
+                float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+                v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+                float* qss = reinterpret_cast<float*>(smem + OFF_QSS);
+                if ((l & 1) == 0) qss[(2 * half + cbp) * 64 + 16 * rq + ((l >> 1) & 15)] = v1;
             }
         }
         fence_proxy_async_smem();
@@ -462,13 +528,21 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
         }
     }
     __syncthreads();
-    // the T diag(beta) and Aqk tile images out, 24 KB contiguous per (slot, head)
+    // the T diag(beta) and Aqk tile images out (24 KB), and the sums of q^2 per row
     {
-        uint4* dst = reinterpret_cast<uint4*>(p.img + ((size_t)slot * H + h) * IMG_BYTES);
+        uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
+        uint4* dst = reinterpret_cast<uint4*>(img);
         const uint4* tp = reinterpret_cast<const uint4*>(smem + OFF_TP);
         const uint4* aq = reinterpret_cast<const uint4*>(smem + OFF_AQK);
-        for (int x = tid; x < (int)(IMG_BYTES / 16); x += NTHR)
+        for (int x = tid; x < (int)(Img<K>::HANDOFF / 16); x += NTHR)
             dst[x] = x < 512 ? tp[x] : aq[x - 512];
+        if (p.qnorm && tid < C) {
+            const float* qss = reinterpret_cast<const float*>(smem + OFF_QSS);
+            float ssum = 0.f;
+#pragma unroll
+            for (int j = 0; j < K / 64; ++j) ssum += qss[j * 64 + tid];
+            reinterpret_cast<float*>(img + Img<K>::QSS)[tid] = ssum;
+        }
     }
     // a CTA that gave up a wait lets its MMAs in flight finish before it frees TMEM
     if (!ok && tid == 0) {
@@ -486,28 +560,26 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
 
 // ------------------------------------------------------------------ pass 2
 namespace chain {
-constexpr int NTHR = 512, NGRP = 256;            // operand group (warps 0-7), chain group (8-15)
-constexpr uint32_t BAR_OPS = 1, BAR_CHAIN = 2;   // named barriers of the groups
+constexpr int NTHR = 256;                   // 8 warps, two per TMEM lane quadrant
+constexpr uint32_t BAR_CHAIN = 1;
 
 // shared memory (bytes from a 1024-aligned base); K-dependent sizes
 template <int K>
 struct Smem {
-    static constexpr uint32_t TILE = 64 * K * 2;           // [64 tok][K] bf16, K / 64 boxes of 8 KB
-    static constexpr uint32_t KT = 0;                      // k tile (TMA) -> k 2^G in place
-    static constexpr uint32_t QT = KT + TILE;              // q tile (TMA) -> s q 2^G in place
-    static constexpr uint32_t KD = QT + TILE;              // k 2^(Gl - G), two buffers (parity)
-    static constexpr uint32_t V = KD + 2 * TILE;           // v tile [64 tok][128 v], 16 KB
-    static constexpr uint32_t IMG = V + 16384;             // T diag(beta) + Aqk images, two buffers
-    static constexpr uint32_t YA = IMG + 2 * IMG_BYTES;    // Y^T, then v_new^T, bf16 [128 v][64 tok]
-    static constexpr uint32_t GAM = YA + 16384;            // 2^Glast fp32 [2][K]
-    static constexpr uint32_t GC = GAM + 2 * K * 4;        // gate sums of the row groups fp32 [4][K]
-    static constexpr uint32_t QSS = GC + 4 * K * 4;        // sums of q^2 per row fp32 [2][4][64]
-    static constexpr uint32_t BAR = QSS + 2 * 4 * 64 * 4;  // mbarriers
-    static constexpr uint32_t MISC = BAR + 128;            // tmem base, abort flag, loads issued
+    using I = Img<K>;
+    static constexpr uint32_t KT = 0;                          // k 2^G   (image, bulk copy)
+    static constexpr uint32_t QT = KT + I::TILE;               // s q 2^G (same copy)
+    static constexpr uint32_t KD = QT + I::TILE;               // k 2^(Gl - G), then 2^Glast
+    static constexpr uint32_t GAM = KD + I::TILE;              //   (one copy)
+    static constexpr uint32_t V = (GAM + K * 4 + 1023) / 1024 * 1024;  // v tile [64 tok][128 v]
+    static constexpr uint32_t IMG = V + 16384;                 // T diag(beta), Aqk: two buffers
+    static constexpr uint32_t YA = IMG + 2 * I::HANDOFF;       // Y^T, then v_new^T, bf16 [128 v][64 tok]
+    static constexpr uint32_t BAR = YA + 16384;                // mbarriers
+    static constexpr uint32_t MISC = BAR + 128;                // tmem base, abort flag, loads issued
     static constexpr uint32_t END = MISC + 32;
     static constexpr uint32_t BYTES = END + 1024;
     static_assert(BYTES <= 232448, "shared memory of one CTA");
-    static_assert(KD % 1024 == 0 && V % 1024 == 0 && IMG % 1024 == 0 && YA % 1024 == 0, "align");
+    static_assert(I::QG - I::KG == QT - KT && I::GAM - I::KD == GAM - KD, "copy layout");
 };
 // TMEM columns: h^T fp32 [128 v][K], its bf16 copy (K / 2 columns), Y^T / v_new^T, o^T
 template <int K>
@@ -517,23 +589,17 @@ struct Tmem {
     static_assert(O + 64 <= COLS, "TMEM");
 };
 
-enum { B_TILES = 0, B_OPS, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
+enum { B_OPS = 0, B_KD, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
 
 struct Params {
-    const __nv_bfloat16* beta;
-    const void* g;
-    const float* A_log;
-    const float* dt_bias;
     const float* h0;
     float* hT;
     const int32_t* cu;
     void* o;
-    int mode;
-    float lb;
-    int T, H, hr, V;
+    int T, H, V;
     int qnorm;           // scale each output row by 1 / sqrt(|q row|^2 + kQNormEps)
     ChunkMap cm;
-    const uint8_t* img;  // pass 1's images [slots][H][IMG_BYTES]
+    const uint8_t* img;  // pass 1's images [slots][H][Img<K>::BYTES]
     int* status;         // optional caller word: bit 0 when a wait gives up
 };
 
@@ -551,29 +617,25 @@ struct Sync {
         }
     }
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
-    __device__ __forceinline__ void group_wait(int i, uint32_t parity, bool leader, uint32_t barid) const {
+    __device__ __forceinline__ void group_wait(int i, uint32_t parity, bool leader) const {
         if (leader) wait(i, parity);
-        bar_sync(barid, NGRP);
+        bar_sync(BAR_CHAIN, NTHR);
     }
 };
 
-// k, q tiles of chunk t (K / 64 boxes of 64 channels) into the operand buffers
-__device__ __forceinline__ void load_tiles(uint32_t sb, uint32_t kt, uint32_t qt, const CUtensorMap* tk,
-                                           const CUtensorMap* tq, int nbox, int hq, int t, uint32_t bar) {
-    mbar_arrive_expect_tx(bar, (uint32_t)nbox * 2u * 8192u);
-    for (int cb = 0; cb < nbox; ++cb) {
-        tma_load_3d(sb + kt + cb * 8192, tk, 64 * cb, hq, t, bar);
-        tma_load_3d(sb + qt + cb * 8192, tq, 64 * cb, hq, t, bar);
-    }
+// a bulk copy of `bytes` (a multiple of 16) in pieces of at most 32 KB, completing on `bar`
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const uint8_t* src, uint32_t bytes, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, bytes);
+    for (uint32_t o = 0; o < bytes; o += 32768u)
+        bulk_load(dst + o, src + o, min(32768u, bytes - o), bar);
 }
 
-template <int K, typename GT, typename OT>
+template <int K, typename OT>
 __global__ void __launch_bounds__(NTHR, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, Params p) {
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     using S = Smem<K>;
+    using I = Img<K>;
     using TM = Tmem<K>;
-    constexpr int NBOX = K / 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -582,21 +644,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     Sync sy{sb + S::BAR, misc + 1, p.status};
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int vb = blockIdx.x, n = blockIdx.y, h = blockIdx.z, H = p.H;
-    const int hq = h / p.hr;
     long bos, eos;
     if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
     else      { bos = (long)n * p.T; eos = bos + p.T; }
     const int nt = (int)((eos - bos + C - 1) / C);
     const int slot0 = p.cm.first_slot(n, (int)bos);
-    float* gam = reinterpret_cast<float*>(smem + S::GAM);
+    const float* gam = reinterpret_cast<const float*>(smem + S::GAM);
+    auto image = [&](int c) { return p.img + ((size_t)(slot0 + c) * H + h) * I::BYTES; };
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
         fence_mbar_init();
         misc[1] = 0;
-        misc[2] = misc[3] = misc[4] = 0;  // loads issued: tiles, v, images
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
+        misc[2] = misc[3] = misc[4] = misc[5] = 0;  // copies issued: operands, kd, v, images
         prefetch_tmap(&tm_v);
     }
     if (w == 0) tmem_alloc(sb + S::MISC, TM::COLS);
@@ -606,373 +666,255 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t tmem = misc[0];
     volatile uint32_t* issued = misc + 2;
 
-    if (w < 8) {
-        // ================= operand group: a1 and the chain's operands of every chunk.  Thread:
-        // channel pair (d0, d0 + 1) of each 128-channel part, rows 16 rg .. 16 rg + 15
-        const int rg = tid >> 6, r0 = 16 * rg;
-        const GT* gptr = reinterpret_cast<const GT*>(p.g);
-        constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
-        using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;
-        const float m = (p.mode == 1) ? p.lb * kLog2e : kLog2e;
-        const float scale = rsqrtf((float)K);
-        float* gc = reinterpret_cast<float*>(smem + S::GC);
-        for (int c = 0; c < nt; ++c) {
-            const long t0 = bos + (long)c * C;
-            const int len = (int)min((long)C, eos - t0);
-            const uint32_t kdb = sb + S::KD + (uint32_t)(c & 1) * S::TILE;
+    const int lg = w & 3, hch = w >> 2;
+    const int vlane = 32 * lg + l;                  // value channel within the block
+    const int vch = 128 * vb + vlane;               // value channel
+    const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
+    const size_t st_off = ((size_t)n * H + h) * (size_t)K * p.V;
+    const uint32_t yab = sb + S::YA;
+    // state columns of this thread: key channels hch * K / 2 .. + K / 2 - 1, in pieces of 32
+    auto ld_h = [&](int s, float (&hv)[32]) {
+        tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, hv);
+        tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16, hv + 16);
+    };
+    auto st_h = [&](int s, const float (&hv)[32]) {
+        tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, reinterpret_cast<const uint32_t*>(hv));
+        tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16,
+                  reinterpret_cast<const uint32_t*>(hv) + 16);
+    };
+    auto st_hA = [&](int s, const float (&hv)[32]) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hv[2 * e], hv[2 * e + 1]);
+        tmem_st16(tmem + lane_base + TM::HA + (K / 4) * hch + 16 * s, r);
+    };
+    // the thread's 32 tokens (32 hch ..) of a [128 v][64 tok] fp32 accumulator row -> the bf16
+    // K-major A tile (row = value channel, 128 bytes, 128-byte swizzle)
+    auto acc_to_bf16_tile = [&](uint32_t col) {
+        float x[32];
+        tmem_ld16(tmem + lane_base + col + 32 * hch, x);
+        tmem_ld16(tmem + lane_base + col + 32 * hch + 16, x + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st_s128(yab + sw128((uint32_t)vlane, (uint32_t)(4 * hch + q)), pack_bf16(x[8 * q], x[8 * q + 1]),
+                    pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                    pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+    };
+    // copies of chunk c's image parts (issued by thread 0); the next chunk's parts are prefetched
+    // to L2 along with them
+    auto load_ops = [&](int c) {
+        issued[0] = issued[0] + 1u;
+        bulk_copy(sb + S::KT, image(c) + I::KG, 2 * I::TILE, sy.bar(B_OPS));
+        if (c + 1 < nt) prefetch_l2(image(c + 1) + I::KG, 2 * I::TILE);
+    };
+    auto load_kd = [&](int c) {
+        issued[1] = issued[1] + 1u;
+        bulk_copy(sb + S::KD, image(c) + I::KD, I::TILE + K * 4, sy.bar(B_KD));
+        if (c + 1 < nt) prefetch_l2(image(c + 1) + I::KD, I::TILE + K * 4);
+    };
+    auto load_img = [&](int c) {
+        issued[3] = issued[3] + 1u;
+        const int b = c & 1;
+        bulk_copy(sb + S::IMG + (uint32_t)b * I::HANDOFF, image(c), I::HANDOFF, sy.bar(B_IMG0 + b));
+    };
+    auto load_v = [&](long t) {
+        issued[2] = issued[2] + 1u;
+        mbar_arrive_expect_tx(sy.bar(B_VFULL), 16384);
+        for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sb + S::V + cb * 8192, &tm_v, 128 * vb + 64 * cb, h, (int)t, sy.bar(B_VFULL));
+    };
+    if (nt > 0) {
+        // the initial state (or zero) into TMEM, fp32 and the bf16 copy
 #pragma unroll 1
-            for (int part = 0; part < K / 128; ++part) {
-                const int d0 = 128 * part + 2 * (tid & 63);
-                GW gw[16];
+        for (int s = 0; s < K / 64; ++s) {
+            float hv[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    gw[i] = __ldg(reinterpret_cast<const GW*>(
-                        gptr + ((size_t)(t0 + min(r0 + i, len - 1)) * H + h) * K + d0));
-                float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
-                if (p.mode == 1) {
-                    nA.x = -expf(__ldg(p.A_log + h * K + d0)) * kLog2e;
-                    nA.y = -expf(__ldg(p.A_log + h * K + d0 + 1)) * kLog2e;
-                    if (p.dt_bias) {
-                        nAd.x = nA.x * __ldg(p.dt_bias + h * K + d0);
-                        nAd.y = nA.y * __ldg(p.dt_bias + h * K + d0 + 1);
-                    }
-                }
-                // a1: the row group's inclusive sums, then the groups before it
-                float2 gv[16], acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float2 a;
-                    if constexpr (kGateBf16) {
-                        a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
-                    } else {
-                        a = gw[i];
-                    }
-                    if (p.mode == 1) {
-                        float2 z = __ffma2_rn(nA, a, nAd);
-                        z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
-                        a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
-                    }
-                    const float mv = (r0 + i < len) ? m : 0.f;
-                    acc = __ffma2_rn(make_float2(mv, mv), a, acc);
-                    gv[i] = acc;
-                }
-                *reinterpret_cast<float2*>(gc + rg * K + d0) = acc;
-                // this chunk's k / q tiles have landed; the carries are out
-                if (tid == 0 && part == 0) sy.wait(B_TILES, (uint32_t)(c & 1));
-                bar_sync(BAR_OPS, NGRP);
-                float2 cy = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 t2 = *reinterpret_cast<const float2*>(gc + q * K + d0);
-                    if (q < rg) cy = __fadd2_rn(cy, t2);
-                    tot = __fadd2_rn(tot, t2);
-                }
-                // Gl: the chunk's last row (rows past the end add zero, so it is the total)
-                if (rg == 0) {
-                    gam[(c & 1) * K + d0] = ex2_fast(tot.x);
-                    gam[(c & 1) * K + d0 + 1] = ex2_fast(tot.y);
-                }
-                // k 2^G and s q 2^G in place, k 2^(Gl - G) into this chunk's kd buffer; rows past
-                // the end of the sequence are zero.  The pair's word of row r in a token-major tile
-                // of K / 64 boxes [64 tok][64 ch]
-                const uint32_t wbox = (uint32_t)(d0 >> 6) * 8192u, wchunk = (uint32_t)((d0 & 63) >> 3),
-                               wbyte = (uint32_t)(d0 & 7) * 2u;
-                float qsq[16];  // q^2 of the pair, per row (deferred q l2norm)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = r0 + i;
-                    const float2 G = __fadd2_rn(gv[i], cy);
-                    const uint32_t off = wbox + sw128((uint32_t)r, wchunk) + wbyte;
-                    uint32_t kw = 0u, qw = 0u, dw = 0u;
-                    qsq[i] = 0.f;
-                    if (r < len) {
-                        const uint32_t kx = ld_s32(sb + S::KT + off), qx = ld_s32(sb + S::QT + off);
-                        qsq[i] = fmaf(bf_lo(qx), bf_lo(qx), bf_hi(qx) * bf_hi(qx));
-                        const float2 e = make_float2(ex2_fast(G.x), ex2_fast(G.y));
-                        const float2 d = make_float2(ex2_fast(tot.x - G.x), ex2_fast(tot.y - G.y));
-                        const float2 kv = make_float2(bf_lo(kx), bf_hi(kx));
-                        const float2 qv = make_float2(bf_lo(qx), bf_hi(qx));
-                        const float2 ke = __fmul2_rn(kv, e);
-                        const float2 qe = __fmul2_rn(__fmul2_rn(qv, e), make_float2(scale, scale));
-                        const float2 kd = __fmul2_rn(kv, d);
-                        kw = pack_bf16(ke.x, ke.y);
-                        qw = pack_bf16(qe.x, qe.y);
-                        dw = pack_bf16(kd.x, kd.y);
-                    }
-                    st_s32(sb + S::KT + off, kw);
-                    st_s32(sb + S::QT + off, qw);
-                    st_s32(kdb + off, dw);
-                }
-                if (p.qnorm) {
-                    // sum over the warp's 64 channels: butterfly over lane bits 4..1 leaves lane l
-                    // with row (l >> 1) & 15, then the pair (l, l ^ 1) completes it
-                    float v8[8], v4[4], v2[2];
-                    const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        v8[i] = (b4 ? qsq[8 + i] : qsq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? qsq[i] : qsq[8 + i], 16);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
-                    float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
-                    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-                    // partial j = part * 2 + (which 64 channels of the part)
-                    float* qss = reinterpret_cast<float*>(smem + S::QSS) + (c & 1) * 256;
-                    if ((l & 1) == 0)
-                        qss[(2 * part + ((tid >> 5) & 1)) * 64 + r0 + ((l >> 1) & 15)] = v1;
-                }
+            for (int j = 0; j < 32; ++j) {
+                const int kch = (K / 2) * hch + 32 * s + j;
+                hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
             }
-            fence_proxy_async_smem();
-            bar_sync(BAR_OPS, NGRP);
-            if (tid == 0) mbar_arrive(sy.bar(B_OPS));
+            st_h(s, hv);
+            st_hA(s, hv);
         }
-    } else {
-        // ================= chain group
-        const int ct = tid - NGRP;
-        const int lg = w & 3, hch = (w - 8) >> 2;
-        const int vlane = 32 * lg + l;                  // value channel within the block
-        const int vch = 128 * vb + vlane;               // value channel
-        const uint32_t lane_base = (uint32_t)(32 * lg) << 16;
-        const size_t st_off = ((size_t)n * H + h) * (size_t)K * p.V;
-        const uint32_t yab = sb + S::YA;
-        // state columns of this thread: key channels hch * K / 2 .. + K / 2 - 1, in pieces of 32
-        auto ld_h = [&](int s, float (&hv)[32]) {
-            tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, hv);
-            tmem_ld16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16, hv + 16);
-        };
-        auto st_h = [&](int s, const float (&hv)[32]) {
-            tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s, reinterpret_cast<const uint32_t*>(hv));
-            tmem_st16(tmem + lane_base + TM::H + (K / 2) * hch + 32 * s + 16,
-                      reinterpret_cast<const uint32_t*>(hv) + 16);
-        };
-        auto st_hA = [&](int s, const float (&hv)[32]) {
-            uint32_t r[16];
+        tmem_wait_st();
+        if (tid == 0) {
+            load_ops(0);
+            load_kd(0);
+            load_img(0);
+            load_v(bos);
+        }
+    }
+    tc_fence_before();
+    bar_sync(BAR_CHAIN, NTHR);
+    for (int c = 0; c < nt; ++c) {
+        const long t0 = bos + (long)c * C;
+        const int len = (int)min((long)C, eos - t0);
+        const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * I::HANDOFF;
+        // ---- Y^T = h^T (k 2^G)^T, o^T = h^T (s q 2^G)^T
+        if (tid == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
+        if (tid == 0 && !sy.aborted()) {
+            tc_fence_after();
+            if (c + 1 < nt) load_img(c + 1);  // its buffer's readers (chunk c - 1) are done
+            const uint32_t id_y = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = pack_bf16(hv[2 * e], hv[2 * e + 1]);
-            tmem_st16(tmem + lane_base + TM::HA + (K / 4) * hch + 16 * s, r);
-        };
-        // the thread's 32 tokens (32 hch ..) of a [128 v][64 tok] fp32 accumulator row -> the
-        // bf16 K-major A tile (row = value channel, 128 bytes, 128-byte swizzle)
-        auto acc_to_bf16_tile = [&](uint32_t col) {
-            float x[32];
-            tmem_ld16(tmem + lane_base + col + 32 * hch, x);
-            tmem_ld16(tmem + lane_base + col + 32 * hch + 16, x + 16);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_s128(yab + sw128((uint32_t)vlane, (uint32_t)(4 * hch + q)), pack_bf16(x[8 * q], x[8 * q + 1]),
-                        pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
-                        pack_bf16(x[8 * q + 6], x[8 * q + 7]));
-        };
-        auto load_img = [&](int c) {
-            issued[2] = issued[2] + 1u;
-            const int b = c & 1;
-            mbar_arrive_expect_tx(sy.bar(B_IMG0 + b), IMG_BYTES);
-            bulk_load(sb + S::IMG + (uint32_t)b * IMG_BYTES,
-                      p.img + ((size_t)(slot0 + c) * H + h) * IMG_BYTES, IMG_BYTES, sy.bar(B_IMG0 + b));
-        };
-        auto load_v = [&](long t) {
-            issued[1] = issued[1] + 1u;
-            mbar_arrive_expect_tx(sy.bar(B_VFULL), 16384);
-            for (int cb = 0; cb < 2; ++cb)
-                tma_load_3d(sb + S::V + cb * 8192, &tm_v, 128 * vb + 64 * cb, h, (int)t, sy.bar(B_VFULL));
-        };
-        if (nt > 0) {
-            // the initial state (or zero) into TMEM, fp32 and the bf16 copy
+            for (int kk = 0; kk < K / 16; ++kk) {
+                const uint32_t boff = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
+                uint64_t bk = desc_at(umma_desc(sb + S::KT, 16, 1024), boff);
+                uint64_t bq = desc_at(umma_desc(sb + S::QT, 16, 1024), boff);
+                umma_bf16_ta(tmem + TM::Y, tmem + TM::HA + 8 * kk, bk, id_y, kk > 0);
+                umma_bf16_ta(tmem + TM::O, tmem + TM::HA + 8 * kk, bq, id_y, kk > 0);
+            }
+            umma_commit(sy.bar(B_YDONE));
+        }
+        sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
+        tc_fence_after();
+        // the operand tiles are free: the next chunk's
+        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_ops(c + 1);
+        // ---- Y^T -> bf16 A tile; h^T <- h^T Diag(2^Glast)
+        acc_to_bf16_tile(TM::Y);
+        if (w == 0) sy.wait(B_KD, (uint32_t)(c & 1));
+        bar_sync(BAR_CHAIN, NTHR);
+        {
+            const float* gm = gam + (K / 2) * hch;
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
                 float hv[32];
+                ld_h(s, hv);
+                float gv[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int kch = (K / 2) * hch + 32 * s + j;
-                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4*>(gm + 32 * s + j);
+                    gv[j] = g4.x; gv[j + 1] = g4.y; gv[j + 2] = g4.z; gv[j + 3] = g4.w;
                 }
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hv[j] *= gv[j];
                 st_h(s, hv);
-                st_hA(s, hv);
             }
             tmem_wait_st();
-            if (ct == 0) {
-                issued[0] = 1u;
-                load_tiles(sb, S::KT, S::QT, &tm_k, &tm_q, NBOX, hq, (int)bos, sy.bar(B_TILES));
-                load_img(0);
-                load_v(bos);
+        }
+        if (w == 0) sy.wait(B_VFULL, (uint32_t)(c & 1));
+        bar_sync(BAR_CHAIN, NTHR);
+        if (len < C) {
+            // rows past the end may hold the next sequence's tokens or NaN padding; T diag(beta)
+            // has zero columns there, which would not cancel a NaN
+            for (int idx = tid; idx < (C - len) * 16; idx += NTHR) {
+                const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
+                st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
-        bar_sync(BAR_CHAIN, NGRP);
-        for (int c = 0; c < nt; ++c) {
-            const long t0 = bos + (long)c * C;
-            const int len = (int)min((long)C, eos - t0);
-            const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * IMG_BYTES;
-            // ---- Y^T = h^T (k 2^G)^T, o^T = h^T (s q 2^G)^T
-            if (ct == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
-            if (ct == 0 && !sy.aborted()) {
+        bar_sync(BAR_CHAIN, NTHR);
+        // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns
+        if (tid == 0) {
+            sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
+            if (!sy.aborted()) {
                 tc_fence_after();
-                if (c + 1 < nt) load_img(c + 1);  // its buffer's readers (chunk c - 1) are done
-                const uint32_t id_y = idesc_bf16(128, 64, 0, 0);
+                const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
+                const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
 #pragma unroll
-                for (int kk = 0; kk < K / 16; ++kk) {
-                    const uint32_t boff = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
-                    uint64_t bk = desc_at(umma_desc(sb + S::KT, 16, 1024), boff);
-                    uint64_t bq = desc_at(umma_desc(sb + S::QT, 16, 1024), boff);
-                    umma_bf16_ta(tmem + TM::Y, tmem + TM::HA + 8 * kk, bk, id_y, kk > 0);
-                    umma_bf16_ta(tmem + TM::O, tmem + TM::HA + 8 * kk, bq, id_y, kk > 0);
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
+                    uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
+                    umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
                 }
-                umma_commit(sy.bar(B_YDONE));
-            }
-            sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
-            tc_fence_after();
-            // the operand tiles are free: the next chunk's k and q
-            if (ct == 0 && c + 1 < nt && !sy.aborted()) {
-                issued[0] = issued[0] + 1u;
-                load_tiles(sb, S::KT, S::QT, &tm_k, &tm_q, NBOX, hq, (int)(t0 + C), sy.bar(B_TILES));
-            }
-            // ---- Y^T -> bf16 A tile; h^T <- h^T Diag(2^Glast)
-            acc_to_bf16_tile(TM::Y);
-            {
-                const float* gm = gam + (c & 1) * K + (K / 2) * hch;
-#pragma unroll 1
-                for (int s = 0; s < K / 64; ++s) {
-                    float hv[32];
-                    ld_h(s, hv);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) hv[j] *= gm[32 * s + j];
-                    st_h(s, hv);
-                }
-                tmem_wait_st();
-            }
-            if (w == 8) sy.wait(B_VFULL, (uint32_t)(c & 1));
-            bar_sync(BAR_CHAIN, NGRP);
-            if (len < C) {
-                // rows past the end may hold the next sequence's tokens or NaN padding; T diag(beta)
-                // has zero columns there, which would not cancel a NaN
-                for (int idx = ct; idx < (C - len) * 16; idx += NGRP) {
-                    const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
-                    st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(BAR_CHAIN, NGRP);
-            // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns
-            if (ct == 0) {
-                sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
-                if (!sy.aborted()) {
-                    tc_fence_after();
-                    const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
-                    const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
-                        uint64_t b = desc_at(umma_desc(img + IMG_TP, 16, 1024), kk * 32);
-                        umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
-                        uint64_t b = desc_at(umma_desc(img + IMG_TP, 16, 1024), kk * 32);
-                        umma_bf16(tmem + TM::Y, a, b, id_n, 1);
-                    }
-                    umma_commit(sy.bar(B_VNDONE));
-                }
-            }
-            sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
-            tc_fence_after();
-            if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);
-            // ---- o^T += v_new^T Aqk^T (tf32: A = the FP32 v_new^T accumulator)
-            if (ct == 0 && !sy.aborted()) {
-                const uint32_t id_o = idesc_tf32(128, 64);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    uint64_t bo = desc_at(umma_desc(img + IMG_AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
-                                          (uint32_t)(kk & 3) * 32u);
-                    umma_tf32_ta(tmem + TM::O, tmem + TM::Y + 8 * kk, bo, id_o, 1);
-                }
-            }
-            // ---- v_new^T -> bf16 A tile, then h^T += v_new^T (k 2^(Gl - G))
-            acc_to_bf16_tile(TM::Y);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            bar_sync(BAR_CHAIN, NGRP);
-            if (ct == 0 && !sy.aborted()) {
-                tc_fence_after();
-                const uint32_t id_h = idesc_bf16(128, K, 0, 1);
-                const uint32_t kdb = sb + S::KD + (uint32_t)(c & 1) * S::TILE;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
-                    uint64_t b = desc_at(umma_desc(kdb, 8192, 1024), kk * 2048);
-                    umma_bf16(tmem + TM::H, a, b, id_h, 1);
+                    uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
+                    umma_bf16(tmem + TM::Y, a, b, id_n, 1);
                 }
-                umma_commit(sy.bar(B_OHDONE));
+                umma_commit(sy.bar(B_VNDONE));
             }
-            sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 8, BAR_CHAIN);
-            tc_fence_after();
-            // ---- bf16 h^T for the next chunk; o out
-            {
-#pragma unroll 1
-                for (int s = 0; s < K / 64; ++s) {
-                    float hv[32];
-                    ld_h(s, hv);
-                    tmem_wait_ld();
-                    st_hA(s, hv);
-                }
-                float ov[32];
-                tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
-                tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
-                tmem_wait_ld();
-                if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps)
-                    const float* qss = reinterpret_cast<const float*>(smem + S::QSS) + (c & 1) * 256 + 32 * hch;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        float ssum = 0.f;
-#pragma unroll
-                        for (int q = 0; q < K / 64; ++q) ssum += qss[q * 64 + j];
-                        ov[j] *= rsqrtf(ssum + kQNormEps);
-                    }
-                }
-                OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * p.V + vch;
-                const size_t ostride = (size_t)H * p.V;
-                const int nvalid = len - 32 * hch;
-#pragma unroll
-                for (int j = 0; j < 32; ++j, op += ostride)
-                    if (j < nvalid) *op = to_out<OT>(ov[j]);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            bar_sync(BAR_CHAIN, NGRP);
         }
-        if (p.hT && !sy.aborted()) {
+        sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 0);
+        tc_fence_after();
+        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);
+        // ---- o^T += v_new^T Aqk^T (tf32: A = the FP32 v_new^T accumulator)
+        if (tid == 0 && !sy.aborted()) {
+            const uint32_t id_o = idesc_tf32(128, 64);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint64_t bo = desc_at(umma_desc(img + I::AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
+                                      (uint32_t)(kk & 3) * 32u);
+                umma_tf32_ta(tmem + TM::O, tmem + TM::Y + 8 * kk, bo, id_o, 1);
+            }
+        }
+        // ---- v_new^T -> bf16 A tile, then h^T += v_new^T (k 2^(Gl - G))
+        acc_to_bf16_tile(TM::Y);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NTHR);
+        if (tid == 0 && !sy.aborted()) {
+            tc_fence_after();
+            const uint32_t id_h = idesc_bf16(128, K, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
+                uint64_t b = desc_at(umma_desc(sb + S::KD, 8192, 1024), kk * 2048);
+                umma_bf16(tmem + TM::H, a, b, id_h, 1);
+            }
+            umma_commit(sy.bar(B_OHDONE));
+        }
+        sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
+        tc_fence_after();
+        // the kd tile and 2^Glast are free: the next chunk's
+        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_kd(c + 1);
+        // ---- bf16 h^T for the next chunk; o out
+        {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
                 float hv[32];
-                if (nt > 0) {
-                    ld_h(s, hv);
-                    tmem_wait_ld();
-                } else {  // an empty sequence passes its state through
+                ld_h(s, hv);
+                tmem_wait_ld();
+                st_hA(s, hv);
+            }
+            float ov[32];
+            tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
+            tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
+            tmem_wait_ld();
+            if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps), the sums from pass 1
+                const float* qss = reinterpret_cast<const float*>(image(c) + I::QSS) + 32 * hch;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch) : 0.f;
-                }
+                for (int j = 0; j < 32; ++j) ov[j] *= rsqrtf(__ldg(qss + j) + kQNormEps);
+            }
+            OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * p.V + vch;
+            const size_t ostride = (size_t)H * p.V;
+            const int nvalid = len - 32 * hch;
+#pragma unroll
+            for (int j = 0; j < 32; ++j, op += ostride)
+                if (j < nvalid) *op = to_out<OT>(ov[j]);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        bar_sync(BAR_CHAIN, NTHR);
+    }
+    if (p.hT && !sy.aborted()) {
+#pragma unroll 1
+        for (int s = 0; s < K / 64; ++s) {
+            float hv[32];
+            if (nt > 0) {
+                ld_h(s, hv);
+                tmem_wait_ld();
+            } else {  // an empty sequence passes its state through
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
+                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch) : 0.f;
             }
-        }
-        // after a give-up: let the last load of each kind land before the CTA leaves
-        if (ct == 0 && sy.aborted()) {
-            if (issued[0] > 0) mbar_wait(sy.bar(B_TILES), (issued[0] - 1u) & 1u);
-            if (issued[1] > 0) mbar_wait(sy.bar(B_VFULL), (issued[1] - 1u) & 1u);
-            const uint32_t ni = issued[2];
-            if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
         }
     }
-    // every MMA was waited for, unless a wait gave up: then let the ones in flight finish
-    if (sy.aborted() && tid == NGRP) {
+    // after a give-up: let the last copy of each kind land, and the MMAs in flight finish
+    if (tid == 0 && sy.aborted()) {
+        if (issued[0] > 0) mbar_wait(sy.bar(B_OPS), (issued[0] - 1u) & 1u);
+        if (issued[1] > 0) mbar_wait(sy.bar(B_KD), (issued[1] - 1u) & 1u);
+        if (issued[2] > 0) mbar_wait(sy.bar(B_VFULL), (issued[2] - 1u) & 1u);
+        const uint32_t ni = issued[3];
+        if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
         umma_commit(sy.bar(B_DRAIN));
         mbar_wait(sy.bar(B_DRAIN), 0);
     }
@@ -997,9 +939,10 @@ bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H) {
     return qkv_bf16 && K == V && (K == 128 || K == 256) && (mode == 0 || mode == 1) && H <= 65535;
 }
 
-size_t twopass_workspace_bytes(int T, int H, int N, bool packed) {
+size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed) {
     ChunkMap cm{packed ? reinterpret_cast<const int32_t*>(1) : nullptr, N, T, twopass::C};
-    return (size_t)cm.n_slots() * (size_t)H * twopass::IMG_BYTES;
+    const size_t per = K == 256 ? twopass::Img<256>::BYTES : twopass::Img<128>::BYTES;
+    return (size_t)cm.n_slots() * (size_t)H * per;
 }
 
 cudaError_t read_twopass_timeouts(unsigned* count, bool reset) {
@@ -1023,26 +966,24 @@ cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
         cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, prep::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         prep::Params pp{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta,
-                        a.g, a.A_log, a.dt_bias, a.mode, a.lb, a.H, hr, cm, (uint8_t*)a.ws, a.status};
+                        a.g, a.A_log, a.dt_bias, a.mode, a.lb, a.H, hr, cm, (uint8_t*)a.ws, a.status,
+                        a.q_l2norm ? 1 : 0};
         kp<<<dim3(slots, a.H), prep::NTHR, prep::SMEM_BYTES, a.stream>>>(pp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // pass 2: every (sequence, head, 128 value channels), the value blocks of a head side by
-    // side so that they share their reads of q, k, g and the images in L2
-    CUtensorMap mq, mk, mv;
+    // side so that they share their reads of the images in L2
+    CUtensorMap mv;
     const long tokens = (long)a.B * a.T;
-    if (!fused::make_map(&mq, a.q, tokens, Hk, K) || !fused::make_map(&mk, a.k, tokens, Hk, K) ||
-        !fused::make_map(&mv, a.v, tokens, a.H, a.V))
-        return cudaErrorInvalidValue;
-    auto kc = chain::chunk_chain_kernel<K, GT, OT>;
+    if (!fused::make_map(&mv, a.v, tokens, a.H, a.V)) return cudaErrorInvalidValue;
+    auto kc = chain::chunk_chain_kernel<K, OT>;
     constexpr uint32_t smem = chain::Smem<K>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chain::Params cp{(const __nv_bfloat16*)a.beta, a.g, a.A_log, a.dt_bias, a.h0, a.hT, a.cu, a.o,
-                     a.mode, a.lb, a.T, a.H, hr, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
+    chain::Params cp{a.h0, a.hT, a.cu, a.o, a.T, a.H, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
                      a.status};
-    kc<<<dim3(a.V / 128, a.N, a.H), chain::NTHR, smem, a.stream>>>(mq, mk, mv, cp);
+    kc<<<dim3(a.V / 128, a.N, a.H), chain::NTHR, smem, a.stream>>>(mv, cp);
     return cudaGetLastError();
 }
 template <int K>
@@ -1057,7 +998,8 @@ cudaError_t launch_dims(const FwdArgs& a, const ChunkMap& cm, int slots) {
 cudaError_t launch_chunk_twopass(const FwdArgs& a) {
     const ChunkMap cm{a.cu, a.N, a.T, twopass::C};
     const int slots = cm.n_slots();
-    if (!a.ws || a.ws_bytes < (size_t)slots * (size_t)a.H * twopass::IMG_BYTES) return cudaErrorInvalidValue;
+    if (!a.ws || a.ws_bytes < twopass_workspace_bytes(a.T, a.H, a.K, a.N, a.cu != nullptr))
+        return cudaErrorInvalidValue;
     return a.K == 256 ? launch_dims<256>(a, cm, slots) : launch_dims<128>(a, cm, slots);
 }
 

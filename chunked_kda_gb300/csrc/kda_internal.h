@@ -95,7 +95,7 @@ cudaError_t read_fused_timeouts(unsigned* count, bool reset);
 // and Aqk into the workspace, a chain pass per (sequence, head, 128 value channels) runs the state
 // scan; tcgen05 / TMEM / TMA throughout
 bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H);
-size_t twopass_workspace_bytes(int T, int H, int N, bool packed);
+size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed);
 cudaError_t launch_chunk_twopass(const FwdArgs& a);
 cudaError_t read_twopass_timeouts(unsigned* count, bool reset);
 // the fused path's test hooks (kda_test_hooks)

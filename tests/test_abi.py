@@ -230,15 +230,21 @@ def test_workspace_bytes(lib):
     # the fused bf16 kernel keeps every intermediate on chip
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 32, 0) == 0  # fused too
-    # the two-pass path (K = V = 256): 24 KB of T diag(beta) and Aqk per 64-token chunk and head
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) == 4 * 64 * 64 * 24576
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 32, 0) == 4 * 64 * 64 * 24576
+    # the two-pass path (K = V = 256): per 64-token chunk and head, T diag(beta) bf16 and Aqk fp32
+    # (24 KB), k 2^G, s q 2^G and k 2^(Gl - G) in bf16 (3 x 64 K 2 bytes), 2^Glast (K floats) and
+    # the q^2 row sums (64 floats)
+    def img(K):
+        return 24576 + 3 * 64 * K * 2 + 4 * K + 256
+
+    assert img(256) == 124160 and img(128) == 74496
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) == 4 * 64 * 64 * img(256)
+    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 32, 0) == 4 * 64 * 64 * img(256)
     # packed: floor(T_cap / 64) + N + 1 chunk slots
-    assert lib.kda_chunk_workspace_bytes(BF16, 1, 20480, 32, 256, 256, 64, 16) == (320 + 17) * 32 * 24576
+    assert lib.kda_chunk_workspace_bytes(BF16, 1, 20480, 32, 256, 256, 64, 16) == (320 + 17) * 32 * img(256)
     # the two-pass test hook moves K = V = 128 onto it
     lib.kda_test_hooks(-1, 0, 0, 1)
     try:
-        assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 4 * 64 * 64 * 24576
+        assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 4 * 64 * 64 * img(128)
         assert lib.kda_chunk_fwd_launches(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 2
     finally:
         lib.kda_test_hooks(-1, 0, 0, 0)
