@@ -569,9 +569,10 @@ struct Smem {
     using I = Img<K>;
     static constexpr uint32_t KT = 0;                          // k 2^G   (image, bulk copy)
     static constexpr uint32_t QT = KT + I::TILE;               // s q 2^G (same copy)
-    static constexpr uint32_t KD = QT + I::TILE;               // k 2^(Gl - G), then 2^Glast
-    static constexpr uint32_t GAM = KD + I::TILE;              //   (one copy)
-    static constexpr uint32_t V = (GAM + K * 4 + 1023) / 1024 * 1024;  // v tile [64 tok][128 v]
+    static constexpr uint32_t KDB = (I::TILE + K * 4 + 1023) / 1024 * 1024;  // one kd buffer:
+    static constexpr uint32_t KD = QT + I::TILE;               //   k 2^(Gl - G), then 2^Glast (one
+    static constexpr uint32_t GAM = KD + I::TILE;              //   copy); two buffers (parity)
+    static constexpr uint32_t V = KD + 2 * KDB;                // v tile [64 tok][128 v]
     static constexpr uint32_t IMG = V + 16384;                 // T diag(beta), Aqk: two buffers
     static constexpr uint32_t YA = IMG + 2 * I::HANDOFF;       // Y^T, then v_new^T, bf16 [128 v][64 tok]
     static constexpr uint32_t BAR = YA + 16384;                // mbarriers
@@ -580,6 +581,7 @@ struct Smem {
     static constexpr uint32_t BYTES = END + 1024;
     static_assert(BYTES <= 232448, "shared memory of one CTA");
     static_assert(I::QG - I::KG == QT - KT && I::GAM - I::KD == GAM - KD, "copy layout");
+    static_assert(KDB % 1024 == 0 && V % 1024 == 0, "align");
 };
 // TMEM columns: h^T fp32 [128 v][K], its bf16 copy (K / 2 columns), Y^T / v_new^T, o^T
 template <int K>
@@ -589,7 +591,7 @@ struct Tmem {
     static_assert(O + 64 <= COLS, "TMEM");
 };
 
-enum { B_OPS = 0, B_KD, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
+enum { B_OPS = 0, B_KD0, B_KD1, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
 
 struct Params {
     const float* h0;
@@ -649,7 +651,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     else      { bos = (long)n * p.T; eos = bos + p.T; }
     const int nt = (int)((eos - bos + C - 1) / C);
     const int slot0 = p.cm.first_slot(n, (int)bos);
-    const float* gam = reinterpret_cast<const float*>(smem + S::GAM);
     auto image = [&](int c) { return p.img + ((size_t)(slot0 + c) * H + h) * I::BYTES; };
 
     if (tid == 0) {
@@ -710,7 +711,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     };
     auto load_kd = [&](int c) {
         issued[1] = issued[1] + 1u;
-        bulk_copy(sb + S::KD, image(c) + I::KD, I::TILE + K * 4, sy.bar(B_KD));
+        const int b = c & 1;
+        bulk_copy(sb + S::KD + (uint32_t)b * S::KDB, image(c) + I::KD, I::TILE + K * 4, sy.bar(B_KD0 + b));
         if (c + 1 < nt) prefetch_l2(image(c + 1) + I::KD, I::TILE + K * 4);
     };
     auto load_img = [&](int c) {
@@ -747,6 +749,24 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     }
     tc_fence_before();
     bar_sync(BAR_CHAIN, NTHR);
+    // o of chunk c (the thread's 32 rows of its value channel), stored while chunk c + 1's
+    // MMAs run
+    float ov[32];
+    auto store_o = [&](int c) {
+        const long tc = bos + (long)c * C;
+        const int lc = (int)min((long)C, eos - tc);
+        if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps), the sums from pass 1
+            const float* qss = reinterpret_cast<const float*>(image(c) + I::QSS) + 32 * hch;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] *= rsqrtf(__ldg(qss + j) + kQNormEps);
+        }
+        OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(tc + 32 * hch) * H + h) * p.V + vch;
+        const size_t ostride = (size_t)H * p.V;
+        const int nvalid = lc - 32 * hch;
+#pragma unroll
+        for (int j = 0; j < 32; ++j, op += ostride)
+            if (j < nvalid) *op = to_out<OT>(ov[j]);
+    };
     for (int c = 0; c < nt; ++c) {
         const long t0 = bos + (long)c * C;
         const int len = (int)min((long)C, eos - t0);
@@ -755,7 +775,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         if (tid == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
         if (tid == 0 && !sy.aborted()) {
             tc_fence_after();
-            if (c + 1 < nt) load_img(c + 1);  // its buffer's readers (chunk c - 1) are done
+            if (c + 1 < nt) {  // their buffers' readers (chunk c - 1) are done
+                load_img(c + 1);
+                load_kd(c + 1);
+            }
             const uint32_t id_y = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < K / 16; ++kk) {
@@ -767,16 +790,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             }
             umma_commit(sy.bar(B_YDONE));
         }
-        sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
-        tc_fence_after();
-        // the operand tiles are free: the next chunk's
-        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_ops(c + 1);
-        // ---- Y^T -> bf16 A tile; h^T <- h^T Diag(2^Glast)
-        acc_to_bf16_tile(TM::Y);
-        if (w == 0) sy.wait(B_KD, (uint32_t)(c & 1));
+        // ---- while the MMAs run (they read the bf16 copy of h^T): the previous chunk's o out,
+        // and h^T <- h^T Diag(2^Glast) on the FP32 state
+        if (c > 0) store_o(c - 1);
+        if (w == 0) sy.wait(B_KD0 + (c & 1), (uint32_t)((c >> 1) & 1));
         bar_sync(BAR_CHAIN, NTHR);
+        const uint32_t kdb = S::KD + (uint32_t)(c & 1) * S::KDB;
         {
-            const float* gm = gam + (K / 2) * hch;
+            const float* gm = reinterpret_cast<const float*>(smem + kdb + I::TILE) + (K / 2) * hch;
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
                 float hv[32];
@@ -794,6 +815,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             }
             tmem_wait_st();
         }
+        sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
+        tc_fence_after();
+        // the operand tiles are free: the next chunk's
+        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_ops(c + 1);
+        // ---- Y^T -> bf16 A tile
+        acc_to_bf16_tile(TM::Y);
         if (w == 0) sy.wait(B_VFULL, (uint32_t)(c & 1));
         bar_sync(BAR_CHAIN, NTHR);
         if (len < C) {
@@ -853,16 +880,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
-                uint64_t b = desc_at(umma_desc(sb + S::KD, 8192, 1024), kk * 2048);
+                uint64_t b = desc_at(umma_desc(sb + kdb, 8192, 1024), kk * 2048);
                 umma_bf16(tmem + TM::H, a, b, id_h, 1);
             }
             umma_commit(sy.bar(B_OHDONE));
         }
         sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
         tc_fence_after();
-        // the kd tile and 2^Glast are free: the next chunk's
-        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_kd(c + 1);
-        // ---- bf16 h^T for the next chunk; o out
+        // ---- bf16 h^T for the next chunk; o into registers (stored during the next chunk)
         {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
@@ -871,26 +896,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 tmem_wait_ld();
                 st_hA(s, hv);
             }
-            float ov[32];
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
-            if (p.qnorm) {  // o row / sqrt(|q row|^2 + eps), the sums from pass 1
-                const float* qss = reinterpret_cast<const float*>(image(c) + I::QSS) + 32 * hch;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) ov[j] *= rsqrtf(__ldg(qss + j) + kQNormEps);
-            }
-            OT* op = reinterpret_cast<OT*>(p.o) + ((size_t)(t0 + 32 * hch) * H + h) * p.V + vch;
-            const size_t ostride = (size_t)H * p.V;
-            const int nvalid = len - 32 * hch;
-#pragma unroll
-            for (int j = 0; j < 32; ++j, op += ostride)
-                if (j < nvalid) *op = to_out<OT>(ov[j]);
             tmem_wait_st();
         }
         tc_fence_before();
         bar_sync(BAR_CHAIN, NTHR);
     }
+    if (nt > 0 && !sy.aborted()) store_o(nt - 1);
     if (p.hT && !sy.aborted()) {
 #pragma unroll 1
         for (int s = 0; s < K / 64; ++s) {
@@ -911,7 +925,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     // after a give-up: let the last copy of each kind land, and the MMAs in flight finish
     if (tid == 0 && sy.aborted()) {
         if (issued[0] > 0) mbar_wait(sy.bar(B_OPS), (issued[0] - 1u) & 1u);
-        if (issued[1] > 0) mbar_wait(sy.bar(B_KD), (issued[1] - 1u) & 1u);
+        const uint32_t nk = issued[1];
+        if (nk > 0) mbar_wait(sy.bar(B_KD0 + ((nk - 1u) & 1u)), ((nk - 1u) >> 1) & 1u);
         if (issued[2] > 0) mbar_wait(sy.bar(B_VFULL), (issued[2] - 1u) & 1u);
         const uint32_t ni = issued[3];
         if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
