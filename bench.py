@@ -373,6 +373,7 @@ def run_ours(args, world, rank, local):
     # the per-configuration lines at one GPU only (a multi-rank run times the headline step)
     per_config = (None if args.no_per_config or world > 1
                   else per_config_lines(kda, workloads, dev, peaks, 10))
+    gate = None if args.no_per_config or world > 1 else time_gate(kda, workloads, dev, peaks, 10)
 
     if rank != 0:
         return
@@ -409,6 +410,8 @@ def run_ours(args, world, rank, local):
     }
     if per_config is not None:
         line["per_config"] = per_config
+    if gate is not None:
+        line["gate"] = gate
     if not args.no_cpu_baseline:
         cores = host_cores()
         tok, dt = oracle_sample(w, 2 * cores, cores, seed=1234)
@@ -481,6 +484,20 @@ def time_chunk_workload(kda, w, dev, steps, warmup, flush=None):
     return statistics.median(times), n_launch
 
 
+def path_of(w):
+    """The kernels kda_chunk_fwd runs for workload w (the library's dispatch rule): the fused
+    kernel for bf16 K = V = 128 with a bounded gate, the two-pass kernels for bf16 K = V = 256
+    with a bounded gate, the stage-by-stage kernels otherwise."""
+    import torch
+
+    bounded = w.mode in (0, 1)
+    if w.q.dtype == torch.bfloat16 and bounded and w.K == w.V == 128:
+        return "fused"
+    if w.q.dtype == torch.bfloat16 and bounded and w.K == w.V == 256:
+        return "two-pass"
+    return "stage-by-stage"
+
+
 def per_config_lines(kda, workloads, dev, peaks, steps):
     """One entry per configured workload: median time per forward (L2 flushed before each),
     head-tokens/s, TFLOP/s and the roofline fraction."""
@@ -497,12 +514,47 @@ def per_config_lines(kda, workloads, dev, peaks, steps):
                     "head_tokens_per_s": w.head_tokens() / sec, "tflops": r["tflops"],
                     "achieved_gbs": r["achieved_gbs"], "roofline_bound": r["bound"],
                     "roofline_frac": r["frac"], "launches_per_call": n_launch,
-                    "path": "fused" if n_launch < 6 else "stage-by-stage",
-                    "dtype": str(w.q.dtype).replace("torch.", "")})
+                    "path": path_of(w), "dtype": str(w.q.dtype).replace("torch.", "")})
         del w
         torch.cuda.empty_cache()
     del flush
     return out
+
+
+def time_gate(kda, workloads, dev, peaks, steps):
+    """kda_gate_fwd alone on the headline workload's gate (bf16 g, safe activation, 64-token
+    chunk-local log2 cumsum, float32 out), inputs resident; L2 flushed before each call.
+    Algorithmic bytes: g in (2 B) and the float32 cumsum out (4 B) per element."""
+    import torch
+
+    w = workloads.make(WORKLOAD, device=dev)
+    out = torch.empty(w.g.shape, device=dev, dtype=torch.float32)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, device=dev, dtype=torch.float32)
+
+    def call():
+        kda.kda_gate_fwd(w.g, w.A_log, w.dt_bias, w.mode, w.lower_bound, None, w.chunk_size, out=out)
+
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    sec = statistics.median(times)
+    nbytes = w.g.numel() * (w.g.element_size() + 4)
+    res = {"workload": f"gate of {WORKLOAD} (bf16 g, safe, chunk 64, float32 out)",
+           "ms": 1e3 * sec, "achieved_gbs": nbytes / sec / 1e9,
+           "frac": nbytes / sec / 1e9 / peaks["hbm_gbs"], "bytes_per_element": 6}
+    del w, out, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_decode(kda, workloads, dev, stream, n_dec, d_steps):

@@ -65,3 +65,18 @@ def test_roofline_of_takes_the_slower_bound():
     # initial and final states count once each
     w.initial_state = T(4 * 128 * 128, 4)
     assert bench.roofline_of(w, t, peaks)["bytes"] == nbytes + 2 * 4 * 128 * 128 * 4
+
+
+def test_path_of_follows_the_dispatch_rule():
+    import types
+
+    import torch
+
+    def w(dtype, K, V, mode):
+        return types.SimpleNamespace(q=torch.empty(0, dtype=dtype), K=K, V=V, mode=mode)
+
+    assert bench.path_of(w(torch.bfloat16, 128, 128, 1)) == "fused"
+    assert bench.path_of(w(torch.bfloat16, 256, 256, 0)) == "two-pass"
+    assert bench.path_of(w(torch.bfloat16, 256, 256, 2)) == "stage-by-stage"
+    assert bench.path_of(w(torch.bfloat16, 128, 256, 1)) == "stage-by-stage"
+    assert bench.path_of(w(torch.float32, 128, 128, 1)) == "stage-by-stage"

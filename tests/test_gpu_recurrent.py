@@ -132,6 +132,27 @@ def test_gate_fwd(dtype, C, mode):
         assert (nat <= 0).all() and (nat >= w.lower_bound * (1 + 1e-6)).all()
 
 
+@pytest.mark.parametrize("K", [128, 12])
+def test_gate_fwd_vector_and_scalar_kernels(K):
+    """Rows of H * K channels that are a multiple of 8 with 16-byte aligned g and out take the
+    vectorised kernel; others (K = 12 with H = 3, or an output offset by one element) take the
+    scalar one.  Both match the oracle."""
+    lens = [0, 70, 1, 0, 64, 33]
+    cap = sum(lens) + 11
+    w = workloads.make_varlen("g", lens, cap, 3, K, K, 64, torch.bfloat16, 81, mode=workloads.GATE_SAFE)
+    t = to_device(w)
+    ref = oracle.gate(w.g, w.A_log, w.dt_bias, workloads.GATE_SAFE, w.lower_bound, w.cu_seqlens, 64)
+    end = sum(lens)
+    buf = torch.full((1 + cap * 3 * K,), 4242.0, device="cuda")
+    for off in (0, 1):  # aligned, then one float past it
+        out = buf[off:off + cap * 3 * K].view(1, cap, 3, K)
+        kda().kda_gate_fwd(t["g"], t["A_log"], t["dt_bias"], workloads.GATE_SAFE, w.lower_bound,
+                           t["cu_seqlens"], 64, out=out)
+        torch.cuda.synchronize()
+        got = to_np(out)[0, :end]
+        assert np.allclose(got, ref[0, :end], rtol=1e-5, atol=1e-5), np.abs(got - ref[0, :end]).max()
+
+
 def test_gate_half_point():
     """g + dt_bias = 0 gives sigmoid(0) = 1/2, so the activation is lower_bound / 2."""
     H, K = 2, 128
