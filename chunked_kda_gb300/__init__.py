@@ -23,7 +23,7 @@ __all__ = ["kda_gate_fwd", "kda_chunk_workspace_bytes", "kda_chunk_workspace_byt
 
 GATE_PRE = 0
 GATE_SAFE = 1
-GATE_NONSAFE = 2  # -exp(A_log) * softplus(g + dt_bias); runs on the float32 stage-by-stage path
+GATE_NONSAFE = 2  # -exp(A_log) * softplus(g + dt_bias); fused kernel for bf16 K = V = 128, else stages
 GATE_LOG2 = 3     # the per-token log2 decay (the recurrent entry points' gate)
 NOALLOC_SCRATCH_BYTES = 16 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 FLAG_Q_L2NORM = 1  # KDA_FLAG_Q_L2NORM

@@ -158,7 +158,7 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
     const int N = packed ? n_seqs : B;
     if (N == 0) return 0;
     switch (kda::select_path(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode, H, false)) {
-        case kda::Path::Fused: return kda::fused_launch_count(N, H, T, packed, o_dtype == KDA_F32);
+        case kda::Path::Fused: return kda::fused_launch_count(N, H, T, packed, o_dtype == KDA_F32, (int)mode);
         case kda::Path::TwoPass: return 2;
         default: return 6;
     }

@@ -93,7 +93,7 @@ constexpr uint32_t OFF_AQK = 204800;   // hand-off: Aqk fp32 [64 i][64 j] K-majo
 constexpr uint32_t OFF_GAM = 221184;   // hand-off: 2^Glast fp32 [2][128] (double buffer)
 constexpr uint32_t OFF_BETA = 222208;  // prep: beta fp32 [2 chunks][64]
 constexpr uint32_t OFF_GCARRY = 222720;  // chain: fp32 [3][128] gate sums of row quarters 0-2
-constexpr uint32_t OFF_GM = 224256;    // prep: fp32 [4][128] G at the sub-block midpoints
+constexpr uint32_t OFF_GM = 224256;    // prep: fp32 [4][128] G at the sub-block anchor rows
 constexpr uint32_t OFF_GL = 226304;    // prep: fp32 [128] G at the last row
 constexpr uint32_t OFF_BAR = 226816;   // mbarriers (8 bytes each)
 constexpr uint32_t OFF_MISC = 226928;  // tmem base, abort flag, TMA loads issued (qk, v)
@@ -190,6 +190,7 @@ struct Sync {
 };
 
 // ------------------------------------------------------------------ prep group
+template <bool kNS>
 __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
                                           const Sync& sy, int h, long bos, long eos, int nt) {
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -214,6 +215,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
     auto bf_0 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel0)); };
     auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, sel1)); };
     const float scale = rsqrtf((float)KD);
+    constexpr bool ns = kNS;  // non-safe gate: per-pair factors on the diagonal blocks
     const uint32_t sw_d0 = (uint32_t)((d0 & 63) >> 3), sw_b0 = (uint32_t)(d0 & 7) * 2;
     // own element (row r, channels d0, d0 + 1) in a token-major [64 tok][128 ch] TMA tile
     auto tile_off = [&](int r) { return (uint32_t)cbp * 8192u + sw128((uint32_t)r, sw_d0) + sw_b0; };
@@ -243,27 +245,108 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         // of k 2^G and s q 2^G; k 2^(Gl - G), 2^Glast and the q^2 sums are double buffers.)
         // G of the own rows and channels, from the buffer the gate warps filled (the operand
         // stores below overwrite it as well)
-        uint32_t kr[16], qr[16];
-        float G0[16], G1[16];
         if (w == 0) {
             sy.wait(B_QKIN, c & 1);
             sy.wait(B_GATE, c & 1);
         }
         bar_sync(BAR_PREP, NGRP);
+        // the own rows of k and q and their G
+        auto load_own = [&](uint32_t (&kr)[16], uint32_t (&qr)[16], float (&G0)[16], float (&G1)[16]) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const bool valid = 16 * rq + i < len;
-            const uint32_t off = tile_off(16 * rq + i);
-            kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
-            qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
-        }
+            for (int i = 0; i < 16; ++i) {
+                const bool valid = 16 * rq + i < len;
+                const uint32_t off = tile_off(16 * rq + i);
+                kr[i] = valid ? ld_s32(sb + OFF_KG + off) : 0u;
+                qr[i] = valid ? ld_s32(sb + OFF_QG + off) : 0u;
+            }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch0, 4 * rq + k));
-            const float4 b = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch1, 4 * rq + k));
-            G0[4 * k] = a.x; G0[4 * k + 1] = a.y; G0[4 * k + 2] = a.z; G0[4 * k + 3] = a.w;
-            G1[4 * k] = b.x; G1[4 * k + 1] = b.y; G1[4 * k + 2] = b.z; G1[4 * k + 3] = b.w;
+            for (int k = 0; k < 4; ++k) {
+                const float4 a = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch0, 4 * rq + k));
+                const float4 b = *reinterpret_cast<const float4*>(smem + OFF_GS + gs_off(ch1, 4 * rq + k));
+                G0[4 * k] = a.x; G0[4 * k + 1] = a.y; G0[4 * k + 2] = a.z; G0[4 * k + 3] = a.w;
+                G1[4 * k] = b.x; G1[4 * k + 1] = b.y; G1[4 * k + 2] = b.z; G1[4 * k + 3] = b.w;
+            }
+        };
+
+        // ---- non-safe gate: the diagonal 16 x 16 blocks of Akk and Aqk with a factor
+        // 2^(G_i - G_j) per pair and channel (FLA skill "fla-kda", "Safe vs non-safe intra path":
+        // the token-parallel diagonal blocks), exact for any decay.  Per column j the factor
+        // runs down the rows as a product of the per-token factors 2^(G_i - G_(i-1)) <= 1.
+        // Each thread forms the sums over its two channels; four rounds of 64 entries per
+        // sub-block are summed over the 64 channel pairs through the free score operand area
+        // ([4 sub-blocks][16 entry quads][64 channel pairs] float4, 64 KB), and each thread
+        // keeps one finished entry per round for the store after the readback.  Entry order of
+        // a round q: columns cp = 2q, 15 - 2q, 2q + 1, 14 - 2q; per column j: Aqk(j, j), then
+        // Akk(i, j), Aqk(i, j) for i = j + 1 .. 15 (32 entries per column pair)
+        float dg[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ns) {
+            uint32_t kr[16], qr[16];
+            float2 al[16];
+            {
+                float G0[16], G1[16];
+                load_own(kr, qr, G0, G1);
+#pragma unroll
+                for (int i = 1; i < 16; ++i)
+                    al[i] = make_float2(ex2_fast(G0[i] - G0[i - 1]), ex2_fast(G1[i] - G1[i - 1]));
+            }
+            const int ch64 = 32 * cbp + l;
+            const uint32_t scr = sb + OFF_SAH;
+            // reducer of entry quad qd, part lq of sub-block rb: lanes 8 lq + (qd & 7), so the eight
+            // lanes of each phase of a 16-byte load read eight distinct bank groups
+            const int rb = tid >> 6, qd = (tid & 7) | (((tid >> 5) & 1) << 3), lq = (tid >> 3) & 3;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float buf[4];
+                int slot = 0;
+                auto emit = [&](float v) {
+                    buf[slot & 3] = v;
+                    if ((slot & 3) == 3)
+                        st_s128(scr + ((uint32_t)((rq * 16 + (slot >> 2)) * 64 + ch64) << 4), __float_as_uint(buf[0]),
+                                __float_as_uint(buf[1]), __float_as_uint(buf[2]), __float_as_uint(buf[3]));
+                    ++slot;
+                };
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cp = 2 * q + (u >> 1);
+                    const int j = (u & 1) ? 15 - cp : cp;
+                    float2 kj = make_float2(bf_0(kr[j]), bf_1(kr[j]));
+                    emit(fmaf(bf_0(qr[j]), kj.x, bf_1(qr[j]) * kj.y));
+#pragma unroll
+                    for (int i = j + 1; i < 16; ++i) {
+                        kj = __fmul2_rn(kj, al[i]);
+                        emit(fmaf(bf_0(kr[i]), kj.x, bf_1(kr[i]) * kj.y));
+                        emit(fmaf(bf_0(qr[i]), kj.x, bf_1(qr[i]) * kj.y));
+                    }
+                }
+                bar_sync(BAR_PREP, NGRP);
+                // entry 4 qd + lq of sub-block rb: the 64 channel pairs in four parts of 16 (a
+                // rotated start keeps the warp's loads on distinct bank groups), then the parts
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int ln = 16 * lq + ((k + qd) & 15);
+                    uint32_t x0, x1, x2, x3;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                 : "r"(scr + ((uint32_t)((rb * 16 + qd) * 64 + ln) << 4)));
+                    sum.x += __uint_as_float(x0); sum.y += __uint_as_float(x1);
+                    sum.z += __uint_as_float(x2); sum.w += __uint_as_float(x3);
+                }
+#pragma unroll
+                for (int m = 8; m <= 16; m <<= 1) {
+                    sum.x += __shfl_xor_sync(0xffffffffu, sum.x, m);
+                    sum.y += __shfl_xor_sync(0xffffffffu, sum.y, m);
+                    sum.z += __shfl_xor_sync(0xffffffffu, sum.z, m);
+                    sum.w += __shfl_xor_sync(0xffffffffu, sum.w, m);
+                }
+                dg[q] = (lq == 0) ? sum.x : (lq == 1) ? sum.y : (lq == 2) ? sum.z : sum.w;
+                bar_sync(BAR_PREP, NGRP);  // the next round rewrites the area
+            }
         }
+
+        uint32_t kr[16], qr[16];
+        float G0[16], G1[16];
+        load_own(kr, qr, G0, G1);
         bar_sync(BAR_PREP, NGRP);
 
         // ---- deferred q l2norm (attention-gym PR #345): the sums of q^2 of the own rows over
@@ -295,18 +378,26 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
         }
 
         // ---- operands: channel-major [128 ch][rows] tiles, one 16-byte chunk (8 rows) of
-        // each of the two own channels per store
+        // each of the two own channels per store.  Bounded gates: rows and columns of sub-block
+        // rq anchored at its midpoint m (row factors 2^(G - G_m) within 2^(+-8 tokens of decay)).
+        // Non-safe gate: rows anchored at the sub-block's first row (row factors <= 1), columns
+        // at the next sub-block's first row (the last row for rq = 3; column factors <= 1), so
+        // every factor is <= 1 and one that underflows belongs to a score that underflows too;
+        // the diagonal blocks come from the per-pair pass above (their columns here are zero)
         {
             const uint32_t kd_buf = sb + ((c & 1) ? OFF_KD1 : OFF_KD);
-            const float gm0 = G0[8], gm1 = G1[8];
             const float gl0 = glast[ch0], gl1 = glast[ch1];
-            const float P0 = ex2_fast(gm0), P1 = ex2_fast(gm1);              // 2^G at the midpoint
-            const float L0 = ex2_fast(gl0 - gm0), L1 = ex2_fast(gl1 - gm1);  // 2^(Glast - Gmid) <= 1
-            float R0[4], R1[4];  // paired offsets 2^(G_m(bi) - G_m(rq)) <= 1 for bi > rq
+            const float gm0 = ns ? G0[0] : G0[8], gm1 = ns ? G1[0] : G1[8];  // row anchor
+            const float gc0 = ns ? (rq < 3 ? gmid[(rq + 1) * 128 + ch0] : gl0) : gm0;  // column anchor
+            const float gc1 = ns ? (rq < 3 ? gmid[(rq + 1) * 128 + ch1] : gl1) : gm1;
+            const float P0 = ex2_fast(gm0), P1 = ex2_fast(gm1);              // 2^G at the row anchor
+            const float L0 = ex2_fast(gl0 - gc0), L1 = ex2_fast(gl1 - gc1);  // 2^(Glast - G_anchor) <= 1
+            float R0[4], R1[4];  // paired offsets 2^(G_a(bi) - G_anchor) <= 1 for bi > rq
 #pragma unroll
             for (int bi = 0; bi < 4; ++bi) {
-                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
-                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+                const float d = ns ? 0.f : 1.f;  // the diagonal block's own columns
+                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gc0) : d;
+                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gc1) : d;
             }
             if (rq == 3) {
                 gam[(c & 1) * 128 + ch0] = ex2_fast(G0[15]);
@@ -325,7 +416,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     krh[i] = half ? kr[8 + i] : kr[i];
                     qrh[i] = half ? qr[8 + i] : qr[i];
                 }
-                float kf0[8], kf1[8];  // k 2^(G_m(rq) - G) of the 8 rows
+                float kf0[8], kf1[8];  // k 2^(G_anchor - G) of the 8 rows
                 {
                     uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
                     uint32_t g_k0[4], g_k1[4], g_q0[4], g_q1[4];
@@ -337,7 +428,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         for (int u = 0; u < 2; ++u) {
                             const int i = 2 * pr + u;
                             const float e0 = ex2_fast(Gh0[i] - gm0), e1 = ex2_fast(Gh1[i] - gm1);
-                            const float f0 = ex2_fast(gm0 - Gh0[i]), f1 = ex2_fast(gm1 - Gh1[i]);
+                            const float f0 = ex2_fast(gc0 - Gh0[i]), f1 = ex2_fast(gc1 - Gh1[i]);
                             const float kv0 = bf_0(krh[i]), kv1 = bf_1(krh[i]);
                             ke0[u] = kv0 * e0;
                             ke1[u] = kv1 * e1;
@@ -369,8 +460,8 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                     st_s128(kd_buf + r1, kd1[0], kd1[1], kd1[2], kd1[3]);
                 }
                 // score columns, channel-major [128 ch][n] in groups of 64 columns: sub-block
-                // bi >= rq sees row r as column n = sb_off(bi) + r with anchor m_bi:
-                // k_r 2^(G_m(bi) - G_r) = kf_r R(bi)
+                // bi >= rq sees row r as column n = sb_off(bi) + r with anchor a(bi):
+                // k_r 2^(G_a(bi) - G_r) = kf_r R(bi)
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi) {
                     if (bi < rq) continue;
@@ -444,12 +535,21 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
                 if (!is_q) {
-                    if (t <= bi) {
+                    if (t < bi || (t == bi && !ns)) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int j = 16 * t + e;
                             As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;  // Akk^T
                         }
+                    }
+                } else if (ns && t == bi) {
+                    // the diagonal block (non-safe gate): zeros above the diagonal here, the
+                    // per-pair entries below
+                    const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = 16 * t + e;
+                        if (j > i) st_s32(ab + sw128(i, (uint32_t)(4 * (t & 1) + (e >> 2))) + (uint32_t)(e & 3) * 4u, 0u);
                     }
                 } else {
                     // columns 16 t .. 16 t + 15 of row i: four 16-byte chunks of the row in the
@@ -465,6 +565,23 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                         }
                         st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
                     }
+                }
+            }
+        }
+        if (ns) {  // the per-pair diagonal entries (entry 4 qd + lq of sub-block rb in each round)
+            const int rb = tid >> 6, e = 4 * ((tid & 7) | (((tid >> 5) & 1) << 3)) + ((tid >> 3) & 3);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int cp = 2 * q + (e >> 5), x0 = e & 31, len0 = 31 - 2 * cp;
+                const int j = (x0 < len0) ? cp : 15 - cp;
+                const int x = (x0 < len0) ? x0 : x0 - len0;
+                const int I = 16 * rb + j + ((x + 1) >> 1), J = 16 * rb + j;
+                if (x & 1) {
+                    As[J * LD + I] = bcur[I] * dg[q];  // Akk^T, beta-scaled
+                } else {
+                    st_s32(sb + OFF_AQK + (uint32_t)(J >> 5) * 8192u + sw128(I, (uint32_t)((J & 31) >> 2)) +
+                               (uint32_t)(J & 3) * 4u,
+                           __float_as_uint(scale * dg[q]));
                 }
             }
         }
@@ -633,7 +750,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
 }
 
 // ------------------------------------------------------------------ chain group
-template <typename GT, typename OT, bool kSplit>
+template <typename GT, typename OT, bool kSplit, bool kNS>
 __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t* smem, uint32_t tmem,
                                            const Sync& sy, const CUtensorMap* tm_v,
                                            const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -683,22 +800,26 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
     // half of a double buffer.  Thread ct takes the key channels 2 (ct % 64), 2 (ct % 64)
     // + 1 over the row quarter ct / 64 (all its loads issued at once); the quarters add
     // the totals of the ones before them (one exchange).  Chunk 0 runs before the loop,
-    // chunk c + 1 while the chain waits for the prep group to finish chunk c, in a part of
-    // the score operand area that the prep group's inverse leaves free.
+    // chunk c + 1 while the chain's own MMAs of chunk c run.
     constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
     using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;  // a channel pair
     const GT* gptr = reinterpret_cast<const GT*>(p.g);
     const int gq = ct >> 6, gc0 = 2 * (ct & 63);  // row quarter, first channel of the pair
     const float lbl2 = p.lb * kLog2e;
     // safe gate: lb log2(e) sigmoid(z), z = exp(A_log) (g + dt_bias), as
-    // lbl2 / (1 + 2^(nA g + nAd)) with nA = -exp(A_log) log2(e), nAd = nA dt_bias
+    // lbl2 / (1 + 2^(nA g + nAd)) with nA = -exp(A_log) log2(e), nAd = nA dt_bias.
+    // non-safe gate: -exp(A_log) softplus(g + dt_bias) in log2 units is
+    // nA (max(y, 0) + log2(1 + 2^-|y|)) with y = (g + dt_bias) log2(e), nA = -exp(A_log),
+    // nAd = dt_bias log2(e)
     float nA0 = 0.f, nA1 = 0.f, nAd0 = 0.f, nAd1 = 0.f;
-    if (p.mode == 1) {
-        nA0 = -expf(__ldg(p.A_log + h * KD + gc0)) * kLog2e;
-        nA1 = -expf(__ldg(p.A_log + h * KD + gc0 + 1)) * kLog2e;
+    if (kNS || p.mode == 1) {
+        const float f = kNS ? 1.f : kLog2e;
+        nA0 = -expf(__ldg(p.A_log + h * KD + gc0)) * f;
+        nA1 = -expf(__ldg(p.A_log + h * KD + gc0 + 1)) * f;
         if (p.dt_bias) {
-            nAd0 = nA0 * __ldg(p.dt_bias + h * KD + gc0);
-            nAd1 = nA1 * __ldg(p.dt_bias + h * KD + gc0 + 1);
+            const float d0 = __ldg(p.dt_bias + h * KD + gc0), d1 = __ldg(p.dt_bias + h * KD + gc0 + 1);
+            nAd0 = kNS ? d0 * kLog2e : nA0 * d0;
+            nAd1 = kNS ? d1 * kLog2e : nA1 * d1;
         }
     }
     float* gs = reinterpret_cast<float*>(smem + OFF_GS);
@@ -741,7 +862,8 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         const int lenc = (int)min((long)C, eos - tc0);
         const int r0 = 16 * gq;
         bar_sync(BAR_CHAIN, NGRP);  // after the caller's wait: the G buffer is free
-        const float m = (p.mode == 1) ? lbl2 : kLog2e;  // per-token factor into log2 units
+        // per-token factor into log2 units (the non-safe activation is in log2 units already)
+        const float m = kNS ? 1.f : (p.mode == 1) ? lbl2 : kLog2e;
         const float2 nA = make_float2(nA0, nA1), nAd = make_float2(nAd0, nAd1);
         float2 acc = make_float2(0.f, 0.f);
         float2 gv[16];  // inclusive sums of the quarter's rows, channel pair (gc0, gc0 + 1)
@@ -753,7 +875,12 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             } else {
                 a = gw[i];
             }
-            if (p.mode == 1) {
+            if constexpr (kNS) {
+                const float2 y = __ffma2_rn(a, make_float2(kLog2e, kLog2e), nAd);
+                const float sp0 = fmaxf(y.x, 0.f) + lg2_fast(1.f + ex2_fast(-fabsf(y.x)));
+                const float sp1 = fmaxf(y.y, 0.f) + lg2_fast(1.f + ex2_fast(-fabsf(y.y)));
+                a = make_float2(nA.x * sp0, nA.y * sp1);
+            } else if (p.mode == 1) {
                 float2 z = __ffma2_rn(nA, a, nAd);
                 z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
                 a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
@@ -770,7 +897,8 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 #pragma unroll
         for (int i = 0; i < 16; ++i) gv[i] = __fadd2_rn(gv[i], cy);
         if (gq == 3) *reinterpret_cast<float2*>(glast + gc0) = gv[15];
-        *reinterpret_cast<float2*>(gmid + gq * KD + gc0) = gv[8];
+        // the sub-block anchors: the midpoint row (bounded gates), the first row (non-safe gate)
+        *reinterpret_cast<float2*>(gmid + gq * KD + gc0) = kNS ? gv[0] : gv[8];
         // G channel-major: the thread's 16 rows of a channel are the 16-byte chunks 4 gq .. 4 gq + 3
         // of the channel's 256-byte row (chunk index XOR channel & 7).  Lanes with bit 2 set store
         // their second channel first, so the eight lanes of each store phase hit eight bank groups
@@ -1043,9 +1171,10 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
 }
 
 // kGrid: GRID_DENSE (sequences, heads), GRID_PACKED (heads, sequences), GRID_SPLIT (the
-// split schedule of dense inputs, 1-D)
+// split schedule of dense inputs, 1-D).  kNS: the non-safe gate (its own instance: the per-pair
+// diagonal pass would raise the register pressure of the bounded-gate loop)
 enum { GRID_DENSE = 0, GRID_PACKED = 1, GRID_SPLIT = 2 };
-template <typename GT, typename OT, int kGrid>
+template <typename GT, typename OT, int kGrid, bool kNS>
 __global__ void __launch_bounds__(NTHR, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -1099,8 +1228,8 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (w < 8) prep_loop(p, sb, smem, tmem, sy, h, bos, eos, nt);
-    else       chain_loop<GT, OT, kGrid == GRID_SPLIT>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, &tm_g, n, h, bos, eos, nt);
+    if (w < 8) prep_loop<kNS>(p, sb, smem, tmem, sy, h, bos, eos, nt);
+    else       chain_loop<GT, OT, kGrid == GRID_SPLIT, kNS>(p, sb, smem, tmem, sy, &tm_v, &tm_q, &tm_k, &tm_g, n, h, bos, eos, nt);
 
     // Every MMA was waited for, unless a wait gave up: then let the ones in flight finish.
     if (sy.aborted() && (tid == 0 || tid == NGRP)) {
@@ -1146,12 +1275,11 @@ bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D) {
 
 }  // namespace fused
 
-// bf16, K = V = 128 and a gate whose per-token decay is bounded (pre-gated under the
-// bounded-gate contract, or safe): the sub-block anchors of the score operands rely on it.
-// Both chunk sizes run as 64-token chunks: the chunked form computes the same function for
+// bf16, K = V = 128, every gate mode (the bounded gates with midpoint anchors, the non-safe
+// gate with first-row anchors and per-pair diagonal blocks).  Both chunk sizes run as 64-token chunks: the chunked form computes the same function for
 // any chunk size (only the rounding differs), and chunks restart at every sequence start.
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode) {
-    return qkv_bf16 && K == 128 && V == 128 && (C == 32 || C == 64) && (mode == 0 || mode == 1);
+    return qkv_bf16 && K == 128 && V == 128 && (C == 32 || C == 64) && (mode >= 0 && mode <= 2);
 }
 
 bool fused_supported(const FwdArgs& a) { return fused_supported_dims(a.qkv_bf16, a.K, a.V, a.C, a.mode); }
@@ -1219,16 +1347,17 @@ static int split_cut_chunks(int U, int S, int T, int min_tail) {
     return a;
 }
 
-// chunks of the first piece of the split schedule for these sizes (0: one launch)
-static int split_cut_for(int N, int H, int T, bool packed, bool o_f32) {
-    if (packed || !split_allowed()) return 0;
+// chunks of the first piece of the split schedule for these sizes (0: one launch; always for
+// packed inputs and the non-safe gate)
+static int split_cut_for(int N, int H, int T, bool packed, bool o_f32, int mode) {
+    if (packed || mode == 2 || !split_allowed()) return 0;
     // the state (K V words) spans this many of the unit's output rows
     const int stash_rows = fused::KD * fused::VD * 4 / (fused::VD * (o_f32 ? 4 : 2));
     return split_cut_chunks(N * H, sm_count(), T, stash_rows);
 }
 
-int fused_launch_count(int N, int H, int T, bool packed, bool o_f32) {
-    return split_cut_for(N, H, T, packed, o_f32) > 0 ? 2 : 1;
+int fused_launch_count(int N, int H, int T, bool packed, bool o_f32, int mode) {
+    return split_cut_for(N, H, T, packed, o_f32, mode) > 0 ? 2 : 1;
 }
 
 template <typename GT, typename OT>
@@ -1236,14 +1365,16 @@ static cudaError_t launch_t(const FwdArgs& a, const CUtensorMap& mq, const CUten
                             const CUtensorMap& mv, const CUtensorMap& mg, fused::Params p) {
     using namespace fused;
     const bool packed = a.cu != nullptr;
-    auto kern = packed ? chunk_fused_kernel<GT, OT, GRID_PACKED> : chunk_fused_kernel<GT, OT, GRID_DENSE>;
+    auto kern = (a.mode == 2)
+                    ? (packed ? chunk_fused_kernel<GT, OT, GRID_PACKED, true> : chunk_fused_kernel<GT, OT, GRID_DENSE, true>)
+                    : (packed ? chunk_fused_kernel<GT, OT, GRID_PACKED, false> : chunk_fused_kernel<GT, OT, GRID_DENSE, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     {
-        const int cut = split_cut_for(a.N, a.H, a.T, packed, sizeof(OT) == 4);
+        const int cut = split_cut_for(a.N, a.H, a.T, packed, sizeof(OT) == 4, a.mode);
         const int U = a.N * a.H, S = sm_count();
         if (cut > 0) {
-            auto ks = chunk_fused_kernel<GT, OT, GRID_SPLIT>;
+            auto ks = chunk_fused_kernel<GT, OT, GRID_SPLIT, false>;
             e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
             if (e != cudaSuccess) return e;
             p.sp_split = S;

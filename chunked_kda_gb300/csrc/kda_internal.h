@@ -88,7 +88,7 @@ bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
 // kernel launches of the fused path for these sizes on the current device (1, or 2 for the
 // split schedule of dense inputs)
-int fused_launch_count(int N, int H, int T, bool packed, bool o_f32);
+int fused_launch_count(int N, int H, int T, bool packed, bool o_f32, int mode);
 // fused-kernel mbarrier waits that gave up on the current device (synchronises), optional reset
 cudaError_t read_fused_timeouts(unsigned* count, bool reset);
 // bf16 two-pass path (K = V in {128, 256}): a parallel pass per (chunk, head) writes T diag(beta)
@@ -102,7 +102,7 @@ cudaError_t read_twopass_timeouts(unsigned* count, bool reset);
 void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_d128);
 bool hook_two_pass_d128();
 
-// Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, bounded gate), the
+// Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, every gate mode), the
 // two-pass tensor-core kernels (bf16, K = V = 256, bounded gate; K = V = 128 too under the test
 // hook), or the stage-by-stage float32 kernels (everything else)
 enum class Path { Fused, TwoPass, Precise };

@@ -217,6 +217,12 @@ __device__ __forceinline__ float rcp_fast(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// MUFU log2 approximation (used on arguments in [1, 2])
+__device__ __forceinline__ float lg2_fast(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // warp-level 16x8x8 tf32 MMA (legacy tensor path; used for the 16x16 blocks of
 // the triangular solve, which are too small for tcgen05)
 __device__ __forceinline__ uint32_t to_tf32(float x) {

@@ -124,9 +124,10 @@ def test_chunk_host_validation(lib):
     assert _chunk(lib, H=0) == INVALID
     assert _chunk(lib, B=2, T=1 << 30) == INVALID  # B * T reaches 2^31
     assert b"2^31" in lib.kda_last_error()
-    # non-safe gate: A_log required, lower_bound ignored, scratch needed even for bf16
+    # non-safe gate: A_log required, lower_bound ignored, scratch needed for bf16 with
+    # K = V = 256 (the stage-by-stage path; K = V = 128 runs the fused kernel without one)
     assert _chunk(lib, mode=2, A_log=None) == INVALID
-    assert _chunk(lib, mode=2, lb=0.0) == INVALID
+    assert _chunk(lib, mode=2, lb=0.0, K=256, V=256) == INVALID
     assert b"workspace" in lib.kda_last_error()
     assert _chunk(lib, mode=3) == INVALID
     # nothing to do: zero logical sequences is OK and launches nothing
@@ -196,11 +197,18 @@ def test_launch_counts(lib):
     SAFE, NONSAFE = 1, 2
     assert f(F32, F32, 1, 128, 2, 64, 64, 64, 0, SAFE) == 6           # stage-by-stage
     assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 2      # two-pass
-    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 6   # unbounded gate: stages
+    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 6   # unbounded gate, K = 256: stages
     assert f(BF16, BF16, 4, 4096, 64, 128, 256, 64, 0, SAFE) == 6      # K != V: stages
-    assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 6
+    assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 1   # fused, non-safe instance
+    assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, NONSAFE) == 1
     assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, SAFE) == 1   # fused, packed
     assert f(BF16, F32, 4, 4096, 64, 128, 128, 64, 0, SAFE) in (1, 2)  # split: by the SM count
+    lib.kda_test_hooks(-1, 152, 0, 0)  # plan for 152 SMs: 160 units split in two launches ...
+    try:
+        assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 0, SAFE) == 2
+        assert f(BF16, BF16, 1, 4096, 160, 128, 128, 64, 0, NONSAFE) == 1  # ... never the non-safe gate
+    finally:
+        lib.kda_test_hooks(-1, 0, 0, 0)
     assert f(BF16, BF16, 0, 4096, 64, 128, 128, 64, 0, SAFE) == 0     # no sequences
     assert f(BF16, BF16, 4, 4096, 64, 128, 128, 48, 0, SAFE) == -1    # chunk size
     assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, 7) == -1       # gate mode
@@ -249,13 +257,15 @@ def test_workspace_bytes(lib):
     finally:
         lib.kda_test_hooks(-1, 0, 0, 0)
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
-    # by gate mode: the non-safe gate runs on the stage-by-stage path (scratch for bf16 too)
+    # by gate mode: the fused kernel takes every mode; with K = V = 256 the non-safe gate runs on
+    # the stage-by-stage path (scratch for bf16 too)
     ex = lib.kda_chunk_workspace_bytes_ex
     ex.restype = ctypes.c_size_t
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 0) == 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 0
-    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
-        F32, 4, 4096, 64, 128, 128, 64, 0) > 0
+    assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 2) == 0
+    assert ex(BF16, 4, 2048, 8, 256, 256, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
+        F32, 4, 2048, 8, 256, 256, 64, 0) > 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 3) == 0  # no such mode
     assert ex(F32, B, T, H, K, V, C, 0, 2) == lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0)
 

@@ -76,6 +76,7 @@ def test_path_of_follows_the_dispatch_rule():
         return types.SimpleNamespace(q=torch.empty(0, dtype=dtype), K=K, V=V, mode=mode)
 
     assert bench.path_of(w(torch.bfloat16, 128, 128, 1)) == "fused"
+    assert bench.path_of(w(torch.bfloat16, 128, 128, 2)) == "fused"
     assert bench.path_of(w(torch.bfloat16, 256, 256, 0)) == "two-pass"
     assert bench.path_of(w(torch.bfloat16, 256, 256, 2)) == "stage-by-stage"
     assert bench.path_of(w(torch.bfloat16, 128, 256, 1)) == "stage-by-stage"

@@ -138,7 +138,8 @@ VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
 
 @pytest.mark.parametrize("dtype,o_dtype", DTYPES_OUT, ids=DTYPES_OUT_IDS)
 @pytest.mark.parametrize("C", [32, 64])
-@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE, workloads.GATE_NONSAFE],
+                         ids=["pre", "safe", "nonsafe"])
 def test_varlen_contract(dtype, o_dtype, C, mode):
     """Packed sequences with empty slots (first, interior, consecutive, last) and a
     NaN-poisoned capacity tail (attention-gym PR #317, Agent note)."""
@@ -273,7 +274,8 @@ def _sample_units(w, k=4, seed=0):
                                   "varlen_bf16_n16_cap20480_h32_d128_c32",
                                   "dense_bf16_b1_t8192_h96_d128",
                                   "dense_bf16_b4_t4096_h64_d128",
-                                  "dense_bf16_b8_t2048_h32_d256"])
+                                  "dense_bf16_b8_t2048_h32_d256",
+                                  "dense_bf16_b4_t4096_h64_d128_nonsafe"])
 def test_full_size_sampled(name):
     """The full workloads, in the configuration bench.py times (bf16 o), and with a
     float32 o, checked on sampled (sequence, head) units the oracle computes one by one."""
@@ -292,9 +294,13 @@ def test_full_size_sampled(name):
 def test_nonsafe_gate(dtype, o_dtype, C, g_std):
     """The non-safe in-kernel gate -exp(A_log) softplus(g + dt_bias) (FLA skill "fla-kda",
     "Gate modes"): with raw g ~ N(0, 30) single tokens decay by e^-1000 and more; the result
-    stays finite and matches the oracle."""
+    stays finite and matches the oracle.  bf16 runs the fused kernel (first-row anchors off the
+    diagonal, per-pair factors on the diagonal 16 x 16 blocks), float32 the stage path."""
     w = workloads.make_dense("t", 2, 150, 2, 128, 128, C, dtype, 300 + C, state_std=0.05,
                              g_std=g_std, mode=workloads.GATE_NONSAFE)
+    want = 1 if dtype == torch.bfloat16 else 6
+    assert kda().kda_chunk_fwd_launches(dtype, 2, 150, 2, 128, 128, C, 0, workloads.GATE_NONSAFE,
+                                        o_dtype) == want
     o, st = run_gpu(w, o_dtype=o_dtype)
     assert torch.isfinite(o).all() and torch.isfinite(st).all()
     compare(w, o, st)
