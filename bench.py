@@ -309,7 +309,7 @@ def run_ours(args, world, rank, local):
                   * head_tokens + state_bytes)
             print(json.dumps({"workload": args.workload, "ms_per_step": ms_per_step,
                               "head_tokens_per_s": units_all / t_max,
-                              "path": "fused" if n_launch < 6 else "stage-by-stage",
+                              "path": path_of(w),
                               "launches_per_call": n_launch,
                               "algorithmic_gbs": nb / (ms_per_step / 1e3) / 1e9,
                               "frac_of_hbm": nb / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"]}),

@@ -560,15 +560,21 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
 
 // ------------------------------------------------------------------ pass 2
 namespace chain {
-constexpr int NTHR = 256;                   // 8 warps, two per TMEM lane quadrant
-constexpr uint32_t BAR_CHAIN = 1;
+constexpr int NSIMT = 256;                  // 8 warps, two per TMEM lane quadrant
+constexpr int NTHR = NSIMT + 32;            // and one that issues the MMAs and the copies
+constexpr uint32_t BAR_CHAIN = 1;           // the 8 SIMT warps
+// hand-offs from the SIMT warps (arrive) to the issuing warp (sync), all 9 warps: the bf16 state
+// and the scaled state ready (HR), the bf16 Y^T tile and the v tile (YA), the bf16 v_new^T tile (VN)
+constexpr uint32_t BAR_HR = 2, BAR_YA = 3, BAR_VN = 4;
 
 // shared memory (bytes from a 1024-aligned base); K-dependent sizes
 template <int K>
 struct Smem {
     using I = Img<K>;
-    static constexpr uint32_t KT = 0;                          // k 2^G   (image, bulk copy)
-    static constexpr uint32_t QT = KT + I::TILE;               // s q 2^G (same copy)
+    // k 2^G and s q 2^G (image, bulk copies) interleaved by 64-channel panel: panel p holds the
+    // 64 k rows then the 64 q rows, so one N = 128 MMA forms Y^T and o^T together
+    static constexpr uint32_t KT = 0;                          // 2 TILE bytes
+    static constexpr uint32_t QT = KT + I::TILE;
     static constexpr uint32_t KDB = (I::TILE + K * 4 + 1023) / 1024 * 1024;  // one kd buffer:
     static constexpr uint32_t KD = QT + I::TILE;               //   k 2^(Gl - G), then 2^Glast (one
     static constexpr uint32_t GAM = KD + I::TILE;              //   copy); two buffers (parity)
@@ -580,10 +586,11 @@ struct Smem {
     static constexpr uint32_t END = MISC + 32;
     static constexpr uint32_t BYTES = END + 1024;
     static_assert(BYTES <= 232448, "shared memory of one CTA");
-    static_assert(I::QG - I::KG == QT - KT && I::GAM - I::KD == GAM - KD, "copy layout");
+    static_assert(I::QG - I::KG == I::TILE && I::GAM - I::KD == GAM - KD, "copy layout");
     static_assert(KDB % 1024 == 0 && V % 1024 == 0, "align");
 };
-// TMEM columns: h^T fp32 [128 v][K], its bf16 copy (K / 2 columns), Y^T / v_new^T, o^T
+// TMEM columns: h^T fp32 [128 v][K], its bf16 copy (K / 2 columns), Y^T / v_new^T, o^T (right
+// after Y^T: one N = 128 MMA writes both)
 template <int K>
 struct Tmem {
     static constexpr uint32_t H = 0, HA = K, Y = K + K / 2, O = Y + 64;
@@ -621,7 +628,7 @@ struct Sync {
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
     __device__ __forceinline__ void group_wait(int i, uint32_t parity, bool leader) const {
         if (leader) wait(i, parity);
-        bar_sync(BAR_CHAIN, NTHR);
+        bar_sync(BAR_CHAIN, NSIMT);
     }
 };
 
@@ -706,7 +713,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
     // to L2 along with them
     auto load_ops = [&](int c) {
         issued[0] = issued[0] + 1u;
-        bulk_copy(sb + S::KT, image(c) + I::KG, 2 * I::TILE, sy.bar(B_OPS));
+        mbar_arrive_expect_tx(sy.bar(B_OPS), 2 * I::TILE);
+        for (int pnl = 0; pnl < K / 64; ++pnl)
+            for (int t = 0; t < 2; ++t)
+                bulk_load(sb + S::KT + (uint32_t)pnl * 16384u + (uint32_t)t * 8192u,
+                          image(c) + I::KG + (size_t)t * I::TILE + (size_t)pnl * 8192u, 8192u, sy.bar(B_OPS));
         if (c + 1 < nt) prefetch_l2(image(c + 1) + I::KG, 2 * I::TILE);
     };
     auto load_kd = [&](int c) {
@@ -726,29 +737,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(sb + S::V + cb * 8192, &tm_v, 128 * vb + 64 * cb, h, (int)t, sy.bar(B_VFULL));
     };
-    if (nt > 0) {
-        // the initial state (or zero) into TMEM, fp32 and the bf16 copy
-#pragma unroll 1
-        for (int s = 0; s < K / 64; ++s) {
-            float hv[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int kch = (K / 2) * hch + 32 * s + j;
-                hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
-            }
-            st_h(s, hv);
-            st_hA(s, hv);
-        }
-        tmem_wait_st();
-        if (tid == 0) {
-            load_ops(0);
-            load_kd(0);
-            load_img(0);
-            load_v(bos);
-        }
-    }
-    tc_fence_before();
-    bar_sync(BAR_CHAIN, NTHR);
     // o of chunk c (the thread's 32 rows of its value channel), stored while chunk c + 1's
     // MMAs run
     float ov[32];
@@ -767,171 +755,209 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         for (int j = 0; j < 32; ++j, op += ostride)
             if (j < nvalid) *op = to_out<OT>(ov[j]);
     };
-    for (int c = 0; c < nt; ++c) {
-        const long t0 = bos + (long)c * C;
-        const int len = (int)min((long)C, eos - t0);
-        const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * I::HANDOFF;
-        // ---- Y^T = h^T (k 2^G)^T, o^T = h^T (s q 2^G)^T
-        if (tid == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
-        if (tid == 0 && !sy.aborted()) {
-            tc_fence_after();
-            if (c + 1 < nt) {  // their buffers' readers (chunk c - 1) are done
-                load_img(c + 1);
-                load_kd(c + 1);
-            }
-            const uint32_t id_y = idesc_bf16(128, 64, 0, 0);
+    // the bf16 copy of h^T (the next Y / o MMAs' A operand), then h^T <- h^T Diag(2^Glast) of
+    // chunk cs (the gamma row of that chunk's kd buffer) for its state MMA
+    auto copy_and_scale = [&](int cs) {
+        const float* gm = reinterpret_cast<const float*>(smem + S::KD + (uint32_t)(cs & 1) * S::KDB + I::TILE) +
+                          (K / 2) * hch;
+#pragma unroll 1
+        for (int s = 0; s < K / 64; ++s) {
+            float hv[32];
+            ld_h(s, hv);
+            tmem_wait_ld();
+            st_hA(s, hv);
 #pragma unroll
-            for (int kk = 0; kk < K / 16; ++kk) {
-                const uint32_t boff = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
-                uint64_t bk = desc_at(umma_desc(sb + S::KT, 16, 1024), boff);
-                uint64_t bq = desc_at(umma_desc(sb + S::QT, 16, 1024), boff);
-                umma_bf16_ta(tmem + TM::Y, tmem + TM::HA + 8 * kk, bk, id_y, kk > 0);
-                umma_bf16_ta(tmem + TM::O, tmem + TM::HA + 8 * kk, bq, id_y, kk > 0);
+            for (int j = 0; j < 32; j += 4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gm + 32 * s + j);
+                hv[j] *= g4.x; hv[j + 1] *= g4.y; hv[j + 2] *= g4.z; hv[j + 3] *= g4.w;
             }
-            umma_commit(sy.bar(B_YDONE));
+            st_h(s, hv);
         }
-        // ---- while the MMAs run (they read the bf16 copy of h^T): the previous chunk's o out,
-        // and h^T <- h^T Diag(2^Glast) on the FP32 state
-        if (c > 0) store_o(c - 1);
-        if (w == 0) sy.wait(B_KD0 + (c & 1), (uint32_t)((c >> 1) & 1));
-        bar_sync(BAR_CHAIN, NTHR);
-        const uint32_t kdb = S::KD + (uint32_t)(c & 1) * S::KDB;
-        {
-            const float* gm = reinterpret_cast<const float*>(smem + kdb + I::TILE) + (K / 2) * hch;
+    };
+
+    if (w == 8) {
+        // ---- the issuing warp (lane 0): copies a chunk ahead, and every MMA
+        if (l == 0 && nt > 0) {
+            load_ops(0);
+            load_kd(0);
+            load_img(0);
+            load_v(bos);
+        }
+        for (int c = 0; c < nt; ++c) {
+            const long t0 = bos + (long)c * C;
+            const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * I::HANDOFF;
+            const uint32_t kdb = S::KD + (uint32_t)(c & 1) * S::KDB;
+            if (l == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
+            bar_sync(BAR_HR, NTHR);  // bf16 h^T of the state before chunk c; o^T of chunk c - 1 read
+            // ---- [Y^T | o^T] = h^T [(k 2^G)^T | (s q 2^G)^T] (N = 128)
+            if (l == 0 && !sy.aborted()) {
+                tc_fence_after();
+                if (c + 1 < nt) {  // their buffers' readers (chunk c - 1) are done
+                    load_img(c + 1);
+                    load_kd(c + 1);
+                }
+                const uint32_t id_y = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < K / 16; ++kk) {
+                    const uint32_t boff = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                    uint64_t bkq = desc_at(umma_desc(sb + S::KT, 16, 1024), boff);
+                    umma_bf16_ta(tmem + TM::Y, tmem + TM::HA + 8 * kk, bkq, id_y, kk > 0);
+                }
+                umma_commit(sy.bar(B_YDONE));
+            }
+            if (l == 0) {
+                sy.wait(B_YDONE, (uint32_t)(c & 1));
+                if (c + 1 < nt && !sy.aborted()) load_ops(c + 1);  // the operand tiles are free
+            }
+            bar_sync(BAR_YA, NTHR);  // bf16 Y^T tile, v tile with its tail zeroed
+            // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns, then o^T += v_new^T Aqk^T
+            // (tf32: A = the FP32 v_new^T accumulator)
+            if (l == 0) {
+                sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
+                if (!sy.aborted()) {
+                    tc_fence_after();
+                    const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
+                    const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
+                        uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
+                        umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
+                        uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
+                        umma_bf16(tmem + TM::Y, a, b, id_n, 1);
+                    }
+                    umma_commit(sy.bar(B_VNDONE));
+                }
+                sy.wait(B_VNDONE, (uint32_t)(c & 1));
+                if (c + 1 < nt && !sy.aborted()) load_v(t0 + C);
+                if (!sy.aborted()) {
+                    tc_fence_after();
+                    const uint32_t id_o = idesc_tf32(128, 64);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        uint64_t bo = desc_at(umma_desc(img + I::AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
+                                              (uint32_t)(kk & 3) * 32u);
+                        umma_tf32_ta(tmem + TM::O, tmem + TM::Y + 8 * kk, bo, id_o, 1);
+                    }
+                }
+            }
+            bar_sync(BAR_VN, NTHR);  // bf16 v_new^T tile
+            // ---- h^T += v_new^T (k 2^(Gl - G)) on the scaled state
+            if (l == 0) {
+                sy.wait(B_KD0 + (c & 1), (uint32_t)((c >> 1) & 1));
+                if (!sy.aborted()) {
+                    tc_fence_after();
+                    const uint32_t id_h = idesc_bf16(128, K, 0, 1);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
+                        uint64_t b = desc_at(umma_desc(sb + kdb, 8192, 1024), kk * 2048);
+                        umma_bf16(tmem + TM::H, a, b, id_h, 1);
+                    }
+                    umma_commit(sy.bar(B_OHDONE));
+                }
+                sy.wait(B_OHDONE, (uint32_t)(c & 1));  // the next copies reuse this chunk's buffers
+            }
+            __syncwarp();
+        }
+        // after a give-up: let the last copy of each kind land, and the MMAs in flight finish
+        if (l == 0 && sy.aborted()) {
+            if (issued[0] > 0) mbar_wait(sy.bar(B_OPS), (issued[0] - 1u) & 1u);
+            const uint32_t nk = issued[1];
+            if (nk > 0) mbar_wait(sy.bar(B_KD0 + ((nk - 1u) & 1u)), ((nk - 1u) >> 1) & 1u);
+            if (issued[2] > 0) mbar_wait(sy.bar(B_VFULL), (issued[2] - 1u) & 1u);
+            const uint32_t ni = issued[3];
+            if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
+            umma_commit(sy.bar(B_DRAIN));
+            mbar_wait(sy.bar(B_DRAIN), 0);
+        }
+    } else {
+        // ---- the 8 SIMT warps.  The initial state (or zero) into TMEM: its bf16 copy for the
+        // first Y / o MMAs, and scaled by chunk 0's 2^Glast for the first state MMA
+        if (nt > 0) {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
                 float hv[32];
-                ld_h(s, hv);
-                float gv[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(gm + 32 * s + j);
-                    gv[j] = g4.x; gv[j + 1] = g4.y; gv[j + 2] = g4.z; gv[j + 3] = g4.w;
+                for (int j = 0; j < 32; ++j) {
+                    const int kch = (K / 2) * hch + 32 * s + j;
+                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
                 }
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) hv[j] *= gv[j];
                 st_h(s, hv);
             }
             tmem_wait_st();
+            sy.group_wait(B_KD0, 0u, w == 0);
+            copy_and_scale(0);
+            tmem_wait_st();
+            tc_fence_before();
+            bar_arrive(BAR_HR, NTHR);
         }
-        sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
-        tc_fence_after();
-        // the operand tiles are free: the next chunk's
-        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_ops(c + 1);
-        // ---- Y^T -> bf16 A tile
-        acc_to_bf16_tile(TM::Y);
-        if (w == 0) sy.wait(B_VFULL, (uint32_t)(c & 1));
-        bar_sync(BAR_CHAIN, NTHR);
-        if (len < C) {
-            // rows past the end may hold the next sequence's tokens or NaN padding; T diag(beta)
-            // has zero columns there, which would not cancel a NaN
-            for (int idx = tid; idx < (C - len) * 16; idx += NTHR) {
-                const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
-                st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        bar_sync(BAR_CHAIN, NTHR);
-        // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns
-        if (tid == 0) {
-            sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
-            if (!sy.aborted()) {
-                tc_fence_after();
-                const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
-                const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
-                    uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
-                    umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
-                    uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
-                    umma_bf16(tmem + TM::Y, a, b, id_n, 1);
-                }
-                umma_commit(sy.bar(B_VNDONE));
-            }
-        }
-        sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 0);
-        tc_fence_after();
-        if (tid == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);
-        // ---- o^T += v_new^T Aqk^T (tf32: A = the FP32 v_new^T accumulator)
-        if (tid == 0 && !sy.aborted()) {
-            const uint32_t id_o = idesc_tf32(128, 64);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                uint64_t bo = desc_at(umma_desc(img + I::AQK + (uint32_t)(kk >> 2) * 8192u, 16, 1024),
-                                      (uint32_t)(kk & 3) * 32u);
-                umma_tf32_ta(tmem + TM::O, tmem + TM::Y + 8 * kk, bo, id_o, 1);
-            }
-        }
-        // ---- v_new^T -> bf16 A tile, then h^T += v_new^T (k 2^(Gl - G))
-        acc_to_bf16_tile(TM::Y);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        bar_sync(BAR_CHAIN, NTHR);
-        if (tid == 0 && !sy.aborted()) {
+        for (int c = 0; c < nt; ++c) {
+            const long t0 = bos + (long)c * C;
+            const int len = (int)min((long)C, eos - t0);
+            // the previous chunk's o out while the Y / o MMAs run
+            if (c > 0) store_o(c - 1);
+            sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
             tc_fence_after();
-            const uint32_t id_h = idesc_bf16(128, K, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
-                uint64_t b = desc_at(umma_desc(sb + kdb, 8192, 1024), kk * 2048);
-                umma_bf16(tmem + TM::H, a, b, id_h, 1);
+            // ---- Y^T -> bf16 A tile; the v tile's rows past the end zeroed (they may hold the
+            // next sequence's tokens or NaN padding, which T diag(beta)'s zero columns would not
+            // cancel)
+            acc_to_bf16_tile(TM::Y);
+            sy.group_wait(B_VFULL, (uint32_t)(c & 1), w == 0);
+            if (len < C) {
+                for (int idx = tid; idx < (C - len) * 16; idx += NSIMT) {
+                    const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
+                    st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
+                }
             }
-            umma_commit(sy.bar(B_OHDONE));
-        }
-        sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
-        tc_fence_after();
-        // ---- bf16 h^T for the next chunk; o into registers (stored during the next chunk)
-        {
-#pragma unroll 1
-            for (int s = 0; s < K / 64; ++s) {
-                float hv[32];
-                ld_h(s, hv);
-                tmem_wait_ld();
-                st_hA(s, hv);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_arrive(BAR_YA, NTHR);
+            // ---- v_new^T -> bf16 A tile for the state MMA
+            sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 0);
+            tc_fence_after();
+            acc_to_bf16_tile(TM::Y);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            bar_arrive(BAR_VN, NTHR);
+            // ---- after the state MMA: bf16 h^T for the next chunk and h^T scaled by its
+            // 2^Glast; o into registers (stored during the next chunk)
+            sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
+            tc_fence_after();
+            const bool more = c + 1 < nt;
+            if (more) {
+                sy.group_wait(B_KD0 + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1), w == 0);
+                copy_and_scale(c + 1);
             }
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
             tmem_wait_st();
+            tc_fence_before();
+            if (more) bar_arrive(BAR_HR, NTHR);
         }
-        tc_fence_before();
-        bar_sync(BAR_CHAIN, NTHR);
-    }
-    if (nt > 0 && !sy.aborted()) store_o(nt - 1);
-    if (p.hT && !sy.aborted()) {
+        if (nt > 0 && !sy.aborted()) store_o(nt - 1);
+        if (p.hT && !sy.aborted()) {
 #pragma unroll 1
-        for (int s = 0; s < K / 64; ++s) {
-            float hv[32];
-            if (nt > 0) {
-                ld_h(s, hv);
-                tmem_wait_ld();
-            } else {  // an empty sequence passes its state through
+            for (int s = 0; s < K / 64; ++s) {
+                float hv[32];
+                if (nt > 0) {
+                    ld_h(s, hv);
+                    tmem_wait_ld();
+                } else {  // an empty sequence passes its state through
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch) : 0.f;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch) : 0.f;
+                    p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
         }
-    }
-    // after a give-up: let the last copy of each kind land, and the MMAs in flight finish
-    if (tid == 0 && sy.aborted()) {
-        if (issued[0] > 0) mbar_wait(sy.bar(B_OPS), (issued[0] - 1u) & 1u);
-        const uint32_t nk = issued[1];
-        if (nk > 0) mbar_wait(sy.bar(B_KD0 + ((nk - 1u) & 1u)), ((nk - 1u) >> 1) & 1u);
-        if (issued[2] > 0) mbar_wait(sy.bar(B_VFULL), (issued[2] - 1u) & 1u);
-        const uint32_t ni = issued[3];
-        if (ni > 0) mbar_wait(sy.bar(B_IMG0 + ((ni - 1u) & 1u)), ((ni - 1u) >> 1) & 1u);
-        umma_commit(sy.bar(B_DRAIN));
-        mbar_wait(sy.bar(B_DRAIN), 0);
     }
     tc_fence_before();
     __syncthreads();

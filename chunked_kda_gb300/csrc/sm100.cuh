@@ -206,6 +206,10 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// arrive on a named barrier without waiting (producers of a bar_sync by the consumers)
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // MUFU approximations: 2^x (flushes results below 2^-126 to 0) and 1/x
 __device__ __forceinline__ float ex2_fast(float x) {
     float y;
