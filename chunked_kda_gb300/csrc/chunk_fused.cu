@@ -102,7 +102,7 @@ constexpr uint32_t SMEM_BYTES = 228000 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 static_assert(OFF_SB + 3 * 16384 <= OFF_GS && OFF_XS + 4 * 16 * 24 * 4 <= OFF_SB + 3 * 16384, "layout");
 static_assert(OFF_AS + 64 * 68 * 4 <= OFF_TF && OFF_TF + 64 * 68 * 4 <= OFF_XS, "layout");
-static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG, "layout");
+static_assert(OFF_GS + 64 * 128 * 4 <= OFF_KG && OFF_QG == OFF_KG + 16384, "layout");
 static_assert(OFF_KD + 16384 <= OFF_KD1 && OFF_KD1 + 16384 <= OFF_TP && OFF_TP + 8192 <= OFF_AQK, "layout");
 static_assert(OFF_AQK + 16384 <= OFF_GAM && OFF_GAM + 1024 <= OFF_BETA, "layout");
 static_assert(OFF_BETA + 2 * 64 * 4 <= OFF_GCARRY && OFF_GCARRY + 3 * 128 * 4 <= OFF_GM, "layout");
@@ -122,12 +122,12 @@ static_assert(OFF_BAR + 8 * NBAR <= OFF_MISC && OFF_MISC + 32 <= OFF_QSS, "mbarr
 constexpr uint32_t TM_H = 0;     // the state h^T fp32 [128 lanes = v][128 = k]; the dH MMA
                                  // accumulates into it once it is scaled by 2^Glast  (chain)
 constexpr uint32_t TM_Y = 128;   // Y^T [128][64]; then v_new^T hi (128..159), lo (160..191)
-constexpr uint32_t TM_O = 192;   // o^T [128][64]
+constexpr uint32_t TM_O = 192;   // o^T [128][64] (right after Y^T: one N = 128 MMA writes both)
 constexpr uint32_t TM_VN = 256;  // v_new^T accumulator [128][64]; holds h^T (bf16) between chunks
 constexpr uint32_t TM_YA = 320;  // Y^T bf16 [128][64] packed in 32 columns
 constexpr uint32_t TM_S = 352;   // scores [128][160]                                  (prep)
 constexpr uint32_t TM_COLS = 512;
-static_assert(TM_S + 160 <= TM_COLS && TM_YA + 32 <= TM_S, "TMEM map");
+static_assert(TM_S + 160 <= TM_COLS && TM_YA + 32 <= TM_S && TM_O == TM_Y + 64, "TMEM map");
 constexpr int SB_ROWS = 160;                                                   // causal columns
 // byte offset of the 16-byte chunk q (rows 4 q .. 4 q + 3) of channel ch in the channel-major G
 __host__ __device__ constexpr uint32_t gs_off(int ch, int q) {
@@ -973,17 +973,16 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
         // the next chunk's gate rows, in flight while the chain waits for this chunk's operands
         GW gw[16];
         if (c + 1 < nt) gate_load(c + 1, gw);
-        // ---- Y^T = h^T kg^T, o^T = h^T qg^T
+        // ---- [Y^T | o^T] = h^T [kg^T | qg^T]: one N = 128 MMA chain (the MN-major B operand's
+        // second 64-column atom, 16 KB on, is the s q 2^G tile; o^T's columns follow Y^T's)
         if (ct == 0) sy.wait(B_KQFULL, c & 1);
         if (ct == 0 && !sy.aborted()) {
             tc_fence_after();
-            const uint32_t id_y = idesc_bf16(128, 64, 0, 1);
+            const uint32_t id_y = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint64_t bk = desc_at(umma_desc(sb + OFF_KG, 16384, 1024), kk * 2048);
-                uint64_t bq = desc_at(umma_desc(sb + OFF_QG, 16384, 1024), kk * 2048);
-                umma_bf16_ta(tmem + TM_Y, tmem + TM_VN + 8 * kk, bk, id_y, kk > 0);
-                umma_bf16_ta(tmem + TM_O, tmem + TM_VN + 8 * kk, bq, id_y, kk > 0);
+                uint64_t bkq = desc_at(umma_desc(sb + OFF_KG, 16384, 1024), kk * 2048);
+                umma_bf16_ta(tmem + TM_Y, tmem + TM_VN + 8 * kk, bkq, id_y, kk > 0);
             }
             umma_commit(sy.bar(B_YDONE));
         }
