@@ -161,6 +161,14 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
             qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (tok * Hk + hq) * K + cb + d0)) : 0u;
             gw[i] = __ldg(reinterpret_cast<const GW*>(gptr + (tok * H + h) * K + cb + d0));
         }
+        // the next half's rows of the warp's 64 channels towards L2 (lane i: row 16 rq + i)
+        if (half + 1 < K / 128 && l < 16 && 16 * rq + l < len) {
+            const size_t tok = (size_t)(t0 + 16 * rq + l);
+            const int cn = cb + 128 + 64 * cbp;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k + (tok * Hk + hq) * K + cn));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (tok * Hk + hq) * K + cn));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr + (tok * H + h) * K + cn));
+        }
         // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair)
         float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
         if (p.mode == 1) {
@@ -243,6 +251,7 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
             }
             const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
+            const uint32_t nat = swap ? 0x1032u : 0x3210u;  // (ch0, ch1) word -> (d0, d0 + 1) word
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const uint32_t chk = 2 * rq + hf;
@@ -267,14 +276,11 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                         qe1[u] = scale * qv1 * e1;
                         kf0[2 * pr + u] = kv0 * f0;
                         kf1[2 * pr + u] = kv1 * f1;
-                        qsq[i] = fmaf(qv0, qv0, qv1 * qv1);
+                        if (p.qnorm) qsq[i] = fmaf(qv0, qv0, qv1 * qv1);
                         // the pair's words in natural channel order (d0 low, d0 + 1 high)
-                        const uint32_t wkg = swap ? pack_bf16(ke1[u] * Pm1, ke0[u] * Pm0)
-                                                  : pack_bf16(ke0[u] * Pm0, ke1[u] * Pm1);
-                        const uint32_t wqg = swap ? pack_bf16(qe1[u] * Pm1, qe0[u] * Pm0)
-                                                  : pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1);
-                        const uint32_t wkd = swap ? pack_bf16(kf1[2 * pr + u] * Lm1, kf0[2 * pr + u] * Lm0)
-                                                  : pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1);
+                        const uint32_t wkg = __byte_perm(pack_bf16(ke0[u] * Pm0, ke1[u] * Pm1), 0u, nat);
+                        const uint32_t wqg = __byte_perm(pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1), 0u, nat);
+                        const uint32_t wkd = __byte_perm(pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1), 0u, nat);
                         const uint32_t po = pair_off(16 * rq + i, cb + d0);
                         *reinterpret_cast<uint32_t*>(img + Img<K>::KG + po) = wkg;
                         *reinterpret_cast<uint32_t*>(img + Img<K>::QG + po) = wqg;
@@ -755,22 +761,34 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         for (int j = 0; j < 32; ++j, op += ostride)
             if (j < nvalid) *op = to_out<OT>(ov[j]);
     };
-    // the bf16 copy of h^T (the next Y / o MMAs' A operand), then h^T <- h^T Diag(2^Glast) of
-    // chunk cs (the gamma row of that chunk's kd buffer) for its state MMA
-    auto copy_and_scale = [&](int cs) {
-        const float* gm = reinterpret_cast<const float*>(smem + S::KD + (uint32_t)(cs & 1) * S::KDB + I::TILE) +
-                          (K / 2) * hch;
+    // the bf16 copy of h^T: the next Y / o MMAs' A operand
+    auto copy_hA = [&]() {
 #pragma unroll 1
         for (int s = 0; s < K / 64; ++s) {
             float hv[32];
             ld_h(s, hv);
             tmem_wait_ld();
             st_hA(s, hv);
+        }
+    };
+    // h^T <- h^T Diag(2^Glast) of chunk cs (the gamma row of that chunk's kd buffer) for its
+    // state MMA; runs while that chunk's Y / o MMAs read the bf16 copy
+    auto scale_h = [&](int cs) {
+        const float* gm = reinterpret_cast<const float*>(smem + S::KD + (uint32_t)(cs & 1) * S::KDB + I::TILE) +
+                          (K / 2) * hch;
+#pragma unroll 1
+        for (int s = 0; s < K / 64; ++s) {
+            float hv[32];
+            ld_h(s, hv);
+            float gv[32];
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 g4 = *reinterpret_cast<const float4*>(gm + 32 * s + j);
-                hv[j] *= g4.x; hv[j + 1] *= g4.y; hv[j + 2] *= g4.z; hv[j + 3] *= g4.w;
+                gv[j] = g4.x; gv[j + 1] = g4.y; gv[j + 2] = g4.z; gv[j + 3] = g4.w;
             }
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hv[j] *= gv[j];
             st_h(s, hv);
         }
     };
@@ -876,8 +894,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             mbar_wait(sy.bar(B_DRAIN), 0);
         }
     } else {
-        // ---- the 8 SIMT warps.  The initial state (or zero) into TMEM: its bf16 copy for the
-        // first Y / o MMAs, and scaled by chunk 0's 2^Glast for the first state MMA
+        // ---- the 8 SIMT warps.  The initial state (or zero) into TMEM with its bf16 copy for
+        // the first Y / o MMAs; then scaled by chunk 0's 2^Glast for the first state MMA
         if (nt > 0) {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
@@ -888,13 +906,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                     hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
                 }
                 st_h(s, hv);
+                st_hA(s, hv);
             }
-            tmem_wait_st();
-            sy.group_wait(B_KD0, 0u, w == 0);
-            copy_and_scale(0);
             tmem_wait_st();
             tc_fence_before();
             bar_arrive(BAR_HR, NTHR);
+            sy.group_wait(B_KD0, 0u, w == 0);
+            scale_h(0);
+            tmem_wait_st();
         }
         for (int c = 0; c < nt; ++c) {
             const long t0 = bos + (long)c * C;
@@ -924,21 +943,24 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             fence_proxy_async_smem();
             tc_fence_before();
             bar_arrive(BAR_VN, NTHR);
-            // ---- after the state MMA: bf16 h^T for the next chunk and h^T scaled by its
-            // 2^Glast; o into registers (stored during the next chunk)
+            // ---- after the state MMA: bf16 h^T for the next chunk and o into registers (stored
+            // during the next chunk), then, while the next Y / o MMAs run, h^T scaled by the next
+            // chunk's 2^Glast
             sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
             tc_fence_after();
             const bool more = c + 1 < nt;
-            if (more) {
-                sy.group_wait(B_KD0 + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1), w == 0);
-                copy_and_scale(c + 1);
-            }
+            if (more) copy_hA();
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch, ov);
             tmem_ld16(tmem + lane_base + TM::O + 32 * hch + 16, ov + 16);
             tmem_wait_ld();
             tmem_wait_st();
             tc_fence_before();
-            if (more) bar_arrive(BAR_HR, NTHR);
+            if (more) {
+                bar_arrive(BAR_HR, NTHR);
+                sy.group_wait(B_KD0 + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1), w == 0);
+                scale_h(c + 1);
+                tmem_wait_st();
+            }
         }
         if (nt > 0 && !sy.aborted()) store_o(nt - 1);
         if (p.hT && !sy.aborted()) {
