@@ -106,10 +106,8 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                                                ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    const int slot = blockIdx.x, h = blockIdx.y, H = p.H;
-    int n, t0, len, bos, eos;
-    if (!p.cm.map(slot, n, t0, len, bos, eos)) return;  // not a chunk: the whole CTA leaves
-    const int Hk = H / p.hr, hq = h / p.hr;
+    const int H = p.H, Hk = H / p.hr;
+    const int items = p.cm.n_slots() * H;  // (chunk slot, head) pairs, slot-major
     constexpr bool kGateBf16 = std::is_same<GT, __nv_bfloat16>::value;
     using GW = typename std::conditional<kGateBf16, uint32_t, float2>::type;  // a channel pair
 
@@ -128,12 +126,12 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
         fence_mbar_init();
     }
     if (w == 0) tmem_alloc(sb + OFF_MISC, 256);
-    if (tid < C) bsm[tid] = (tid < len) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
     bool ok = true;  // false (in every thread) once a bounded wait gave up: no further MMA
+    uint32_t ph = 0;  // phases of the score-MMA barrier waited for so far (the same in every thread)
 
     // Thread: channel pair (d0, d0 + 1) of the 128-channel half, rows 16 rq .. 16 rq + 15 (one
     // sub-block); ch0 / ch1 is the pair in swapped order on lanes with bit 2 set, so a warp's
@@ -147,408 +145,438 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
     const float lbl2 = p.lb * kLog2e;
     const float m = (p.mode == 1) ? lbl2 : kLog2e;
 
-    for (int half = 0; half < K / 128; ++half) {
-        const int cb = 128 * half;
-        // the own rows: k, q pairs and the gate pair, all loads issued first
-        uint32_t kr[16], qr[16];
-        GW gw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * rq + i;
-            const bool valid = r < len;
-            const size_t tok = (size_t)(t0 + (valid ? r : len - 1));
-            kr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.k + (tok * Hk + hq) * K + cb + d0)) : 0u;
-            qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (tok * Hk + hq) * K + cb + d0)) : 0u;
-            gw[i] = __ldg(reinterpret_cast<const GW*>(gptr + (tok * H + h) * K + cb + d0));
-        }
-        // the next half's rows of the warp's 64 channels towards L2 (lane i: row 16 rq + i)
-        if (half + 1 < K / 128 && l < 16 && 16 * rq + l < len) {
-            const size_t tok = (size_t)(t0 + 16 * rq + l);
-            const int cn = cb + 128 + 64 * cbp;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k + (tok * Hk + hq) * K + cn));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (tok * Hk + hq) * K + cn));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr + (tok * H + h) * K + cn));
-        }
-        // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair)
-        float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
-        if (p.mode == 1) {
-            nA.x = -expf(__ldg(p.A_log + h * K + cb + d0)) * kLog2e;
-            nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1)) * kLog2e;
-            if (p.dt_bias) {
-                nAd.x = nA.x * __ldg(p.dt_bias + h * K + cb + d0);
-                nAd.y = nA.y * __ldg(p.dt_bias + h * K + cb + d0 + 1);
-            }
-        }
-        float2 gv[16], acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float2 a;
-            if constexpr (kGateBf16) {
-                a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
-            } else {
-                a = gw[i];
-            }
-            if (p.mode == 1) {
-                float2 z = __ffma2_rn(nA, a, nAd);
-                z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
-                a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
-            }
-            const float mv = (16 * rq + i < len) ? m : 0.f;  // rows past the end add zero
-            acc = __ffma2_rn(make_float2(mv, mv), a, acc);
-            gv[i] = acc;
-        }
-        *reinterpret_cast<float2*>(gcarry + rq * 128 + d0) = acc;
-        __syncthreads();  // carries out; the previous half's readers of gmid are done
-        float2 cy = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * 128 + d0);
-            if (q < rq) cy = __fadd2_rn(cy, t2);
-            tot = __fadd2_rn(tot, t2);  // G of the chunk's last row (rows past the end add zero)
-        }
-        uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
-        if (rq == 0) {  // 2^Glast of the pair
-            *reinterpret_cast<float2*>(img + Img<K>::GAM + (cb + d0) * 4) =
-                make_float2(ex2_fast(tot.x), ex2_fast(tot.y));
-        }
-        float G0[16], G1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 g2 = __fadd2_rn(gv[i], cy);
-            G0[i] = swap ? g2.y : g2.x;
-            G1[i] = swap ? g2.x : g2.y;
-        }
-        gmid[rq * 128 + ch0] = G0[8];
-        gmid[rq * 128 + ch1] = G1[8];
-        // the previous half's score MMA has read the operand tiles (every thread waits; the
-        // verdict is made the same in all of them)
-        const bool w_ok = !(half > 0 && ok) || mbar_wait(bar, (uint32_t)((half - 1) & 1));
-        if (ok && !__syncthreads_and(w_ok)) {  // midpoints out, operand tiles free
-            if (tid == 0) {
-                atomicAdd(&g_twopass_timeouts, 1u);
-                if (p.status) atomicOr(p.status, 1);
-            }
-            ok = false;
-        } else if (!ok) {
-            __syncthreads();
-        }
+    // Persistent: the CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...; the warps idle
+    // during an item's inverse send the next item's rows towards L2
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int slot = item / H, h = item - slot * H;
+        int n, t0, len, bos, eos;
+        if (!p.cm.map(slot, n, t0, len, bos, eos)) continue;  // not a chunk (the whole CTA)
+        const int hq = h / p.hr;
+        // beta of the chunk (its previous readers finished with the previous item)
+        if (tid < C) bsm[tid] = (tid < len) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
 
-        // a2 operands, channel-major [128 ch][rows] tiles: rows k 2^(G - G_m(rq)), s q 2^(G - G_m(rq));
-        // columns of sub-block bi >= rq: k 2^(G_m(rq) - G) 2^(G_m(bi) - G_m(rq)) (the second factor
-        // <= 1: paired offsets)
-        {
-            const float gm0 = G0[8], gm1 = G1[8];
-            // chain operands from the anchored products: k 2^G = (k 2^(G - Gm)) 2^Gm,
-            // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gm - G)) 2^(Gl - Gm)
-            const float Pm0 = ex2_fast(gm0), Pm1 = ex2_fast(gm1);
-            const float tl0 = swap ? tot.y : tot.x, tl1 = swap ? tot.x : tot.y;
-            const float Lm0 = ex2_fast(tl0 - gm0), Lm1 = ex2_fast(tl1 - gm1);
-            float qsq[16];
-            float R0[4], R1[4];
+        for (int half = 0; half < K / 128; ++half) {
+            const int cb = 128 * half;
+            // the own rows: k, q pairs and the gate pair, all loads issued first
+            uint32_t kr[16], qr[16];
+            GW gw[16];
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) {
-                R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
-                R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * rq + i;
+                const bool valid = r < len;
+                const size_t tok = (size_t)(t0 + (valid ? r : len - 1));
+                kr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.k + (tok * Hk + hq) * K + cb + d0)) : 0u;
+                qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (tok * Hk + hq) * K + cb + d0)) : 0u;
+                gw[i] = __ldg(reinterpret_cast<const GW*>(gptr + (tok * H + h) * K + cb + d0));
             }
-            const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
-            const uint32_t nat = swap ? 0x1032u : 0x3210u;  // (ch0, ch1) word -> (d0, d0 + 1) word
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t chk = 2 * rq + hf;
-                const uint32_t r0 = sw128(ch0, chk), r1 = sw128(ch1, chk);
-                uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
-                float kf0[8], kf1[8];
-#pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    float ke0[2], ke1[2], qe0[2], qe1[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 8 * hf + 2 * pr + u;
-                        const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
-                        const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
-                        const float kv0 = __uint_as_float(__byte_perm(kr[i], 0u, sel0));
-                        const float kv1 = __uint_as_float(__byte_perm(kr[i], 0u, sel1));
-                        const float qv0 = __uint_as_float(__byte_perm(qr[i], 0u, sel0));
-                        const float qv1 = __uint_as_float(__byte_perm(qr[i], 0u, sel1));
-                        ke0[u] = kv0 * e0;
-                        ke1[u] = kv1 * e1;
-                        qe0[u] = scale * qv0 * e0;
-                        qe1[u] = scale * qv1 * e1;
-                        kf0[2 * pr + u] = kv0 * f0;
-                        kf1[2 * pr + u] = kv1 * f1;
-                        if (p.qnorm) qsq[i] = fmaf(qv0, qv0, qv1 * qv1);
-                        // the pair's words in natural channel order (d0 low, d0 + 1 high)
-                        const uint32_t wkg = __byte_perm(pack_bf16(ke0[u] * Pm0, ke1[u] * Pm1), 0u, nat);
-                        const uint32_t wqg = __byte_perm(pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1), 0u, nat);
-                        const uint32_t wkd = __byte_perm(pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1), 0u, nat);
-                        const uint32_t po = pair_off(16 * rq + i, cb + d0);
-                        *reinterpret_cast<uint32_t*>(img + Img<K>::KG + po) = wkg;
-                        *reinterpret_cast<uint32_t*>(img + Img<K>::QG + po) = wqg;
-                        *reinterpret_cast<uint32_t*>(img + Img<K>::KD + po) = wkd;
-                    }
-                    ak0[pr] = pack_bf16(ke0[0], ke0[1]);
-                    ak1[pr] = pack_bf16(ke1[0], ke1[1]);
-                    aq0[pr] = pack_bf16(qe0[0], qe0[1]);
-                    aq1[pr] = pack_bf16(qe1[0], qe1[1]);
+            // the next half's rows of the warp's 64 channels towards L2 (lane i: row 16 rq + i)
+            if (half + 1 < K / 128 && l < 16 && 16 * rq + l < len) {
+                const size_t tok = (size_t)(t0 + 16 * rq + l);
+                const int cn = cb + 128 + 64 * cbp;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k + (tok * Hk + hq) * K + cn));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (tok * Hk + hq) * K + cn));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr + (tok * H + h) * K + cn));
+            }
+            // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair)
+            float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
+            if (p.mode == 1) {
+                nA.x = -expf(__ldg(p.A_log + h * K + cb + d0)) * kLog2e;
+                nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1)) * kLog2e;
+                if (p.dt_bias) {
+                    nAd.x = nA.x * __ldg(p.dt_bias + h * K + cb + d0);
+                    nAd.y = nA.y * __ldg(p.dt_bias + h * K + cb + d0 + 1);
                 }
-                st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
-                st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
-                st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
-                st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
+            }
+            float2 gv[16], acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float2 a;
+                if constexpr (kGateBf16) {
+                    a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
+                } else {
+                    a = gw[i];
+                }
+                if (p.mode == 1) {
+                    float2 z = __ffma2_rn(nA, a, nAd);
+                    z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
+                    a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
+                }
+                const float mv = (16 * rq + i < len) ? m : 0.f;  // rows past the end add zero
+                acc = __ffma2_rn(make_float2(mv, mv), a, acc);
+                gv[i] = acc;
+            }
+            *reinterpret_cast<float2*>(gcarry + rq * 128 + d0) = acc;
+            __syncthreads();  // carries out; the previous half's readers of gmid are done
+            float2 cy = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 t2 = *reinterpret_cast<const float2*>(gcarry + q * 128 + d0);
+                if (q < rq) cy = __fadd2_rn(cy, t2);
+                tot = __fadd2_rn(tot, t2);  // G of the chunk's last row (rows past the end add zero)
+            }
+            uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
+            if (rq == 0) {  // 2^Glast of the pair
+                *reinterpret_cast<float2*>(img + Img<K>::GAM + (cb + d0) * 4) =
+                    make_float2(ex2_fast(tot.x), ex2_fast(tot.y));
+            }
+            float G0[16], G1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float2 g2 = __fadd2_rn(gv[i], cy);
+                G0[i] = swap ? g2.y : g2.x;
+                G1[i] = swap ? g2.x : g2.y;
+            }
+            gmid[rq * 128 + ch0] = G0[8];
+            gmid[rq * 128 + ch1] = G1[8];
+            // the previous half's score MMA has read the operand tiles (every thread waits; the
+            // verdict is made the same in all of them)
+            const bool w_ok = !(half > 0 && ok) || mbar_wait(bar, ph & 1u);
+            if (ok && !__syncthreads_and(w_ok)) {  // midpoints out, operand tiles free
+                if (tid == 0) {
+                    atomicAdd(&g_twopass_timeouts, 1u);
+                    if (p.status) atomicOr(p.status, 1);
+                }
+                ok = false;
+            } else if (!ok) {
+                __syncthreads();
+            } else if (half > 0) {
+                ++ph;
+            }
+
+            // a2 operands, channel-major [128 ch][rows] tiles: rows k 2^(G - G_m(rq)), s q 2^(G - G_m(rq));
+            // columns of sub-block bi >= rq: k 2^(G_m(rq) - G) 2^(G_m(bi) - G_m(rq)) (the second factor
+            // <= 1: paired offsets)
+            {
+                const float gm0 = G0[8], gm1 = G1[8];
+                // chain operands from the anchored products: k 2^G = (k 2^(G - Gm)) 2^Gm,
+                // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gm - G)) 2^(Gl - Gm)
+                const float Pm0 = ex2_fast(gm0), Pm1 = ex2_fast(gm1);
+                const float tl0 = swap ? tot.y : tot.x, tl1 = swap ? tot.x : tot.y;
+                const float Lm0 = ex2_fast(tl0 - gm0), Lm1 = ex2_fast(tl1 - gm1);
+                float qsq[16];
+                float R0[4], R1[4];
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi) {
-                    if (bi < rq) continue;
-                    const uint32_t n0 = (uint32_t)(sb_off(bi) + 16 * rq + 8 * hf);
-                    const uint32_t base = sb + OFF_SB + (n0 >> 6) * 16384u;
-                    const uint32_t cn = (n0 & 63u) >> 3;
-                    uint32_t s0[4], s1[4];
+                    R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
+                    R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+                }
+                const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
+                const uint32_t nat = swap ? 0x1032u : 0x3210u;  // (ch0, ch1) word -> (d0, d0 + 1) word
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t chk = 2 * rq + hf;
+                    const uint32_t r0 = sw128(ch0, chk), r1 = sw128(ch1, chk);
+                    uint32_t ak0[4], ak1[4], aq0[4], aq1[4];
+                    float kf0[8], kf1[8];
 #pragma unroll
                     for (int pr = 0; pr < 4; ++pr) {
-                        s0[pr] = pack_bf16(kf0[2 * pr] * R0[bi], kf0[2 * pr + 1] * R0[bi]);
-                        s1[pr] = pack_bf16(kf1[2 * pr] * R1[bi], kf1[2 * pr + 1] * R1[bi]);
+                        float ke0[2], ke1[2], qe0[2], qe1[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = 8 * hf + 2 * pr + u;
+                            const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
+                            const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
+                            const float kv0 = __uint_as_float(__byte_perm(kr[i], 0u, sel0));
+                            const float kv1 = __uint_as_float(__byte_perm(kr[i], 0u, sel1));
+                            const float qv0 = __uint_as_float(__byte_perm(qr[i], 0u, sel0));
+                            const float qv1 = __uint_as_float(__byte_perm(qr[i], 0u, sel1));
+                            ke0[u] = kv0 * e0;
+                            ke1[u] = kv1 * e1;
+                            qe0[u] = scale * qv0 * e0;
+                            qe1[u] = scale * qv1 * e1;
+                            kf0[2 * pr + u] = kv0 * f0;
+                            kf1[2 * pr + u] = kv1 * f1;
+                            if (p.qnorm) qsq[i] = fmaf(qv0, qv0, qv1 * qv1);
+                            // the pair's words in natural channel order (d0 low, d0 + 1 high)
+                            const uint32_t wkg = __byte_perm(pack_bf16(ke0[u] * Pm0, ke1[u] * Pm1), 0u, nat);
+                            const uint32_t wqg = __byte_perm(pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1), 0u, nat);
+                            const uint32_t wkd =
+                                __byte_perm(pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1), 0u, nat);
+                            const uint32_t po = pair_off(16 * rq + i, cb + d0);
+                            *reinterpret_cast<uint32_t*>(img + Img<K>::KG + po) = wkg;
+                            *reinterpret_cast<uint32_t*>(img + Img<K>::QG + po) = wqg;
+                            *reinterpret_cast<uint32_t*>(img + Img<K>::KD + po) = wkd;
+                        }
+                        ak0[pr] = pack_bf16(ke0[0], ke0[1]);
+                        ak1[pr] = pack_bf16(ke1[0], ke1[1]);
+                        aq0[pr] = pack_bf16(qe0[0], qe0[1]);
+                        aq1[pr] = pack_bf16(qe1[0], qe1[1]);
                     }
-                    st_s128(base + sw128(ch0, cn), s0[0], s0[1], s0[2], s0[3]);
-                    st_s128(base + sw128(ch1, cn), s1[0], s1[1], s1[2], s1[3]);
+                    st_s128(sb + OFF_SAH + r0, ak0[0], ak0[1], ak0[2], ak0[3]);
+                    st_s128(sb + OFF_SAH + r1, ak1[0], ak1[1], ak1[2], ak1[3]);
+                    st_s128(sb + OFF_SAH + 16384 + r0, aq0[0], aq0[1], aq0[2], aq0[3]);
+                    st_s128(sb + OFF_SAH + 16384 + r1, aq1[0], aq1[1], aq1[2], aq1[3]);
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) {
+                        if (bi < rq) continue;
+                        const uint32_t n0 = (uint32_t)(sb_off(bi) + 16 * rq + 8 * hf);
+                        const uint32_t base = sb + OFF_SB + (n0 >> 6) * 16384u;
+                        const uint32_t cn = (n0 & 63u) >> 3;
+                        uint32_t s0[4], s1[4];
+#pragma unroll
+                        for (int pr = 0; pr < 4; ++pr) {
+                            s0[pr] = pack_bf16(kf0[2 * pr] * R0[bi], kf0[2 * pr + 1] * R0[bi]);
+                            s1[pr] = pack_bf16(kf1[2 * pr] * R1[bi], kf1[2 * pr + 1] * R1[bi]);
+                        }
+                        st_s128(base + sw128(ch0, cn), s0[0], s0[1], s0[2], s0[3]);
+                        st_s128(base + sw128(ch1, cn), s1[0], s1[1], s1[2], s1[3]);
+                    }
+                }
+                if (p.qnorm) {
+                    // sum over the warp's 64 channels: butterfly over lane bits 4..1 leaves lane l with
+                    // row (l >> 1) & 15, then the pair (l, l ^ 1) completes it
+                    float v8[8], v4[4], v2[2];
+                    const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v8[i] = (b4 ? qsq[8 + i] : qsq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? qsq[i] : qsq[8 + i], 16);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
+                    float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+                    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+                    float* qss = reinterpret_cast<float*>(smem + OFF_QSS);
+                    if ((l & 1) == 0) qss[(2 * half + cbp) * 64 + 16 * rq + ((l >> 1) & 15)] = v1;
                 }
             }
-            if (p.qnorm) {
-                // sum over the warp's 64 channels: butterfly over lane bits 4..1 leaves lane l with
-                // row (l >> 1) & 15, then the pair (l, l ^ 1) completes it
-                float v8[8], v4[4], v2[2];
-                const bool b4 = l & 16, b3 = l & 8, b2 = l & 4, b1 = l & 2;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0 && ok) {
+                tc_fence_after();
+                const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v8[i] = (b4 ? qsq[8 + i] : qsq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? qsq[i] : qsq[8 + i], 16);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v4[i] = (b3 ? v8[4 + i] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[4 + i], 8);
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    v2[i] = (b2 ? v4[2 + i] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[2 + i], 4);
-                float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
-                v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-                float* qss = reinterpret_cast<float*>(smem + OFF_QSS);
-                if ((l & 1) == 0) qss[(2 * half + cbp) * 64 + 16 * rq + ((l >> 1) & 15)] = v1;
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint64_t b = desc_at(umma_desc(sb + OFF_SB, 16384, 1024), kk * 2048);
+                    uint64_t a = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
+                    umma_bf16(tmem, a, b, id_s, (half > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(bar);
             }
         }
-        fence_proxy_async_smem();
+        {
+            const bool w_ok = !ok || mbar_wait(bar, ph & 1u);
+            if (!__syncthreads_and(w_ok)) {
+                if (tid == 0 && ok) {
+                    atomicAdd(&g_twopass_timeouts, 1u);
+                    if (p.status) atomicOr(p.status, 1);
+                }
+                ok = false;
+            } else if (ok) {
+                ++ph;
+            }
+        }
+        tc_fence_after();
+
+        // the strictly upper 16 x 16 blocks of T diag(beta) are zero
+        for (int idx = tid; idx < 64 * 8; idx += NTHR) {
+            const int i = idx >> 3, c8 = idx & 7;
+            if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
+        }
+        // ---- read the scores: warps w and w + 4 share the TMEM lanes of quadrant w & 3 and take
+        // alternate 16-column pieces.  Akk rows (lanes 0-63, beta-scaled, strictly lower) into the
+        // solve matrix, Aqk rows (lanes 64-127) into the fp32 image.
+        if (ok) {
+            const int lq = w & 3, part = w >> 2;
+            const int row = 32 * lq + l;
+            const int i = row & 63;
+            const bool is_q = row >= 64;
+            const int bi = i >> 4;
+            const int bmin = 2 * (lq & 1);
+            const bool own_a = bi == bmin;
+            const float b_i = bsm[i];
+            const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16);
+#pragma unroll 1
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = part + 2 * tt;
+                float va[16], vb[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) { va[e] = 0.f; vb[e] = 0.f; }
+                if (t <= bmin) tmem_ld16(tl + sb_off(bmin) + 16 * t, va);
+                if (t <= bmin + 1) tmem_ld16(tl + sb_off(bmin + 1) + 16 * t, vb);
+                if (t <= bmin + 1) tmem_wait_ld();
+                float sv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
+                if (!is_q) {
+                    if (t <= bi) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = 16 * t + e;
+                            As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;
+                        }
+                    }
+                } else {
+                    const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t x[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 16 * t + 4 * c4 + e;
+                            x[e] = __float_as_uint((j <= i) ? sv[4 * c4 + e] : 0.f);
+                        }
+                        st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
+                    }
+                }
+            }
+        }
         tc_fence_before();
         __syncthreads();
-        if (tid == 0 && ok) {
-            tc_fence_after();
-            const uint32_t id_s = idesc_bf16(128, SB_ROWS, 1, 1);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                uint64_t b = desc_at(umma_desc(sb + OFF_SB, 16384, 1024), kk * 2048);
-                uint64_t a = desc_at(umma_desc(sb + OFF_SAH, 16384, 1024), kk * 2048);
-                umma_bf16(tmem, a, b, id_s, (half > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(bar);
-        }
-    }
-    {
-        const bool w_ok = !ok || mbar_wait(bar, (uint32_t)((K / 128 - 1) & 1));
-        if (!__syncthreads_and(w_ok)) {
-            if (tid == 0 && ok) {
-                atomicAdd(&g_twopass_timeouts, 1u);
-                if (p.status) atomicOr(p.status, 1);
-            }
-            ok = false;
-        }
-    }
-    tc_fence_after();
 
-    // the strictly upper 16 x 16 blocks of T diag(beta) are zero
-    for (int idx = tid; idx < 64 * 8; idx += NTHR) {
-        const int i = idx >> 3, c8 = idx & 7;
-        if ((c8 >> 1) > (i >> 4)) st_s128(sb + OFF_TP + sw128(i, c8), 0u, 0u, 0u, 0u);
-    }
-    // ---- read the scores: warps w and w + 4 share the TMEM lanes of quadrant w & 3 and take
-    // alternate 16-column pieces.  Akk rows (lanes 0-63, beta-scaled, strictly lower) into the
-    // solve matrix, Aqk rows (lanes 64-127) into the fp32 image.
-    if (ok) {
-        const int lq = w & 3, part = w >> 2;
-        const int row = 32 * lq + l;
-        const int i = row & 63;
-        const bool is_q = row >= 64;
-        const int bi = i >> 4;
-        const int bmin = 2 * (lq & 1);
-        const bool own_a = bi == bmin;
-        const float b_i = bsm[i];
-        const uint32_t tl = tmem + ((uint32_t)(32 * lq) << 16);
-#pragma unroll 1
-        for (int tt = 0; tt < 2; ++tt) {
-            const int t = part + 2 * tt;
-            float va[16], vb[16];
+        // ---- warps 4-7: the next item's k, q and g rows towards L2 (one row of each per thread)
+        if (w >= 4 && item + (int)gridDim.x < items) {
+            const int nx = item + (int)gridDim.x, sl2 = nx / H, h2 = nx - sl2 * H;
+            int n2, t2, len2, bos2, eos2;
+            const int r = tid - 128;
+            if (p.cm.map(sl2, n2, t2, len2, bos2, eos2) && r < len2) {
+                const size_t tok = (size_t)(t2 + r);
+                const int hq2 = h2 / p.hr;
+                prefetch_l2(p.k + (tok * Hk + hq2) * K, K * 2);
+                prefetch_l2(p.q + (tok * Hk + hq2) * K, K * 2);
+                prefetch_l2(gptr + (tok * H + h2) * K, K * (uint32_t)sizeof(GT));
+            }
+        }
+        // ---- a3 on warps 0-3: T = (I + Akk)^-1 into the bf16 T diag(beta) image.  Diagonal 16 x 16
+        // blocks by forward substitution, one thread per column; then the off-diagonal blocks as a
+        // 2 x 2 recursion on 32 x 32 blocks with m16n8k8 tf32 MMAs.
+        if (w < 4 && ok) {
+            if (w < 2) {
+                const int b = 2 * w + (l >> 4), cc = l & 15;
+                float x[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) { va[e] = 0.f; vb[e] = 0.f; }
-            if (t <= bmin) tmem_ld16(tl + sb_off(bmin) + 16 * t, va);
-            if (t <= bmin + 1) tmem_ld16(tl + sb_off(bmin + 1) + 16 * t, vb);
-            if (t <= bmin + 1) tmem_wait_ld();
-            float sv[16];
+                for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
-            if (!is_q) {
-                if (t <= bi) {
+                for (int j = 0; j < 15; ++j) {
+                    const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = 16 * t + e;
-                        As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;
+                    for (int mq = (j + 1) / 4; mq < 4; ++mq) {
+                        const float4 c4 = col[mq];
+                        const float av[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * mq + e > j) x[4 * mq + e] = fmaf(-av[e], x[j], x[4 * mq + e]);
                     }
                 }
-            } else {
-                const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t x[4];
+                for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
+                __syncwarp();
+                const int i = 16 * b + cc;
+                uint32_t pk[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 16 * t + 4 * c4 + e;
-                        x[e] = __float_as_uint((j <= i) ? sv[4 * c4 + e] : 0.f);
+                for (int e = 0; e < 8; ++e) {
+                    const int j0 = 16 * b + 2 * e;
+                    pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
+                }
+                st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
+                st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
+            }
+            bar_sync(1, 128);
+            const int gq = l >> 2, tq = l & 3;
+            auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks >= nk) break;
+                    const int kc = kc0 + 8 * ks;
+                    uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]), to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
+                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
+                                     to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
+                                          to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
+                        mma_tf32_16x8x8(acc[n8], a, bb);
                     }
-                    st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
                 }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- a3 on warps 0-3: T = (I + Akk)^-1 into the bf16 T diag(beta) image.  Diagonal 16 x 16
-    // blocks by forward substitution, one thread per column; then the off-diagonal blocks as a
-    // 2 x 2 recursion on 32 x 32 blocks with m16n8k8 tf32 MMAs.
-    if (w < 4 && ok) {
-        if (w < 2) {
-            const int b = 2 * w + (l >> 4), cc = l & 15;
-            float x[16];
+            };
+            auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int kc = k0 + 8 * ks;
+                    uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]), to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
+                                     to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
+                                     to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
 #pragma unroll
-            for (int j = 0; j < 15; ++j) {
-                const float4* col = reinterpret_cast<const float4*>(As + (16 * b + j) * LD + 16 * b);
-#pragma unroll
-                for (int mq = (j + 1) / 4; mq < 4; ++mq) {
-                    const float4 c4 = col[mq];
-                    const float av[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (4 * mq + e > j) x[4 * mq + e] = fmaf(-av[e], x[j], x[4 * mq + e]);
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
+                                          to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
+                        mma_tf32_16x8x8(acc[n8], a, bb);
+                    }
                 }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LD + 16 * b + cc] = x[i];
-            __syncwarp();
-            const int i = 16 * b + cc;
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j0 = 16 * b + 2 * e;
-                pk[e] = pack_bf16(Tf[i * LD + j0] * bsm[j0], Tf[i * LD + j0 + 1] * bsm[j0 + 1]);
-            }
-            st_s128(sb + OFF_TP + sw128(i, 2 * b), pk[0], pk[1], pk[2], pk[3]);
-            st_s128(sb + OFF_TP + sw128(i, 2 * b + 1), pk[4], pk[5], pk[6], pk[7]);
-        }
-        bar_sync(1, 128);
-        const int gq = l >> 2, tq = l & 3;
-        auto prod_A_T = [&](float (&acc)[2][4], int r0, int kc0, int nk, int n0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks >= nk) break;
-                const int kc = kc0 + 8 * ks;
-                uint32_t a[4] = {to_tf32(As[(kc + tq) * LD + r0 + gq]), to_tf32(As[(kc + tq) * LD + r0 + gq + 8]),
-                                 to_tf32(As[(kc + tq + 4) * LD + r0 + gq]),
-                                 to_tf32(As[(kc + tq + 4) * LD + r0 + gq + 8])};
+            };
+            auto store_X = [&](float* X, const float (&acc)[2][4]) {
 #pragma unroll
                 for (int n8 = 0; n8 < 2; ++n8) {
-                    uint32_t bb[2] = {to_tf32(Tf[(kc + tq) * LD + n0 + 8 * n8 + gq]),
-                                      to_tf32(Tf[(kc + tq + 4) * LD + n0 + 8 * n8 + gq])};
-                    mma_tf32_16x8x8(acc[n8], a, bb);
+                    X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
+                    X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
+                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
+                    X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
                 }
-            }
-        };
-        auto prod_T_X = [&](float (&acc)[2][4], int r0, int k0, const float* X) {
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int kc = k0 + 8 * ks;
-                uint32_t a[4] = {to_tf32(Tf[(r0 + gq) * LD + kc + tq]), to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq]),
-                                 to_tf32(Tf[(r0 + gq) * LD + kc + tq + 4]),
-                                 to_tf32(Tf[(r0 + gq + 8) * LD + kc + tq + 4])};
+            };
+            auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
 #pragma unroll
                 for (int n8 = 0; n8 < 2; ++n8) {
-                    uint32_t bb[2] = {to_tf32(X[(8 * ks + tq) * 24 + 8 * n8 + gq]),
-                                      to_tf32(X[(8 * ks + tq + 4) * 24 + 8 * n8 + gq])};
-                    mma_tf32_16x8x8(acc[n8], a, bb);
+                    const int j = c0 + 8 * n8 + 2 * tq;
+                    if (keep) {
+                        Tf[(r0 + gq) * LD + j] = -acc[n8][0];
+                        Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
+                        Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
+                        Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
+                    }
+                    const float b0 = -bsm[j], b1 = -bsm[j + 1];
+                    const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
+                    st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
+                    st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
                 }
+            };
+            if (w < 2) {  // T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)
+                const int r0 = 32 * w + 16, c0 = 32 * w;
+                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_A_T(xa, r0, c0, 2, c0);
+                float* X = Xs + w * (16 * 24);
+                store_X(X, xa);
+                __syncwarp();
+                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_T_X(ta, r0, r0, X);
+                store_T(r0, c0, ta, true);
             }
-        };
-        auto store_X = [&](float* X, const float (&acc)[2][4]) {
-#pragma unroll
-            for (int n8 = 0; n8 < 2; ++n8) {
-                X[gq * 24 + 8 * n8 + 2 * tq] = acc[n8][0];
-                X[gq * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][1];
-                X[(gq + 8) * 24 + 8 * n8 + 2 * tq] = acc[n8][2];
-                X[(gq + 8) * 24 + 8 * n8 + 2 * tq + 1] = acc[n8][3];
+            bar_sync(1, 128);
+            const int rb = 2 + (w >> 1), cbk = w & 1;
+            {  // X[r][c] = sum_t A[r][t] T[t][c], r = 2, 3; c = 0, 1
+                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                prod_A_T(xa, 16 * rb, 16 * cbk, 4 - 2 * cbk, 16 * cbk);
+                store_X(Xs + w * (16 * 24), xa);
             }
-        };
-        auto store_T = [&](int r0, int c0, const float (&acc)[2][4], bool keep) {
-#pragma unroll
-            for (int n8 = 0; n8 < 2; ++n8) {
-                const int j = c0 + 8 * n8 + 2 * tq;
-                if (keep) {
-                    Tf[(r0 + gq) * LD + j] = -acc[n8][0];
-                    Tf[(r0 + gq) * LD + j + 1] = -acc[n8][1];
-                    Tf[(r0 + gq + 8) * LD + j] = -acc[n8][2];
-                    Tf[(r0 + gq + 8) * LD + j + 1] = -acc[n8][3];
-                }
-                const float b0 = -bsm[j], b1 = -bsm[j + 1];
-                const uint32_t o = sb + OFF_TP + (uint32_t)(j & 7) * 2;
-                st_s32(o + sw128(r0 + gq, j >> 3), pack_bf16(acc[n8][0] * b0, acc[n8][1] * b1));
-                st_s32(o + sw128(r0 + gq + 8, j >> 3), pack_bf16(acc[n8][2] * b0, acc[n8][3] * b1));
-            }
-        };
-        if (w < 2) {  // T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)
-            const int r0 = 32 * w + 16, c0 = 32 * w;
-            float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            prod_A_T(xa, r0, c0, 2, c0);
-            float* X = Xs + w * (16 * 24);
-            store_X(X, xa);
-            __syncwarp();
-            float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            prod_T_X(ta, r0, r0, X);
-            store_T(r0, c0, ta, true);
-        }
-        bar_sync(1, 128);
-        const int rb = 2 + (w >> 1), cbk = w & 1;
-        {  // X[r][c] = sum_t A[r][t] T[t][c], r = 2, 3; c = 0, 1
-            float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            prod_A_T(xa, 16 * rb, 16 * cbk, 4 - 2 * cbk, 16 * cbk);
-            store_X(Xs + w * (16 * 24), xa);
-        }
-        bar_sync(1, 128);
-        {  // T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]
-            float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            bar_sync(1, 128);
+            {  // T[r][c] = -sum_{s=2..r} T[r][s] X[s][c]
+                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 1
-            for (int s = 2; s <= 3; ++s)
-                if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cbk) * (16 * 24));
-            store_T(16 * rb, 16 * cbk, ta, false);
+                for (int s = 2; s <= 3; ++s)
+                    if (s <= rb) prod_T_X(ta, 16 * rb, 16 * s, Xs + (2 * (s - 2) + cbk) * (16 * 24));
+                store_T(16 * rb, 16 * cbk, ta, false);
+            }
         }
-    }
-    __syncthreads();
-    // the T diag(beta) and Aqk tile images out (24 KB), and the sums of q^2 per row
-    {
-        uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
-        uint4* dst = reinterpret_cast<uint4*>(img);
-        const uint4* tp = reinterpret_cast<const uint4*>(smem + OFF_TP);
-        const uint4* aq = reinterpret_cast<const uint4*>(smem + OFF_AQK);
-        for (int x = tid; x < (int)(Img<K>::HANDOFF / 16); x += NTHR)
-            dst[x] = x < 512 ? tp[x] : aq[x - 512];
-        if (p.qnorm && tid < C) {
-            const float* qss = reinterpret_cast<const float*>(smem + OFF_QSS);
-            float ssum = 0.f;
+        __syncthreads();
+        // the T diag(beta) and Aqk tile images out (24 KB), and the sums of q^2 per row
+        {
+            uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
+            uint4* dst = reinterpret_cast<uint4*>(img);
+            const uint4* tp = reinterpret_cast<const uint4*>(smem + OFF_TP);
+            const uint4* aq = reinterpret_cast<const uint4*>(smem + OFF_AQK);
+            for (int x = tid; x < (int)(Img<K>::HANDOFF / 16); x += NTHR)
+                dst[x] = x < 512 ? tp[x] : aq[x - 512];
+            if (p.qnorm && tid < C) {
+                const float* qss = reinterpret_cast<const float*>(smem + OFF_QSS);
+                float ssum = 0.f;
 #pragma unroll
-            for (int j = 0; j < K / 64; ++j) ssum += qss[j * 64 + tid];
-            reinterpret_cast<float*>(img + Img<K>::QSS)[tid] = ssum;
+                for (int j = 0; j < K / 64; ++j) ssum += qss[j * 64 + tid];
+                reinterpret_cast<float*>(img + Img<K>::QSS)[tid] = ssum;
+            }
         }
+        __syncthreads();  // the item's shared buffers and TMEM columns are free for the next one
     }
     // a CTA that gave up a wait lets its MMAs in flight finish before it frees TMEM
     if (!ok && tid == 0) {
@@ -1018,12 +1046,30 @@ cudaError_t read_twopass_timeouts(unsigned* count, bool reset) {
 }
 
 namespace {
+// SMs of the current device, cached per device ordinal (0 if it cannot be read)
+int device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
 template <int K, typename GT, typename OT>
 cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
     using namespace twopass;
     const int Hk = a.Hk > 0 ? a.Hk : a.H;
     const int hr = a.H / Hk;
-    // pass 1: every (chunk, head)
+    // pass 1: every (chunk, head), two persistent CTAs per SM
     {
         auto kp = prep::chunk_prep_kernel<K, GT>;
         cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, prep::SMEM_BYTES);
@@ -1031,7 +1077,10 @@ cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
         prep::Params pp{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta,
                         a.g, a.A_log, a.dt_bias, a.mode, a.lb, a.H, hr, cm, (uint8_t*)a.ws, a.status,
                         a.q_l2norm ? 1 : 0};
-        kp<<<dim3(slots, a.H), prep::NTHR, prep::SMEM_BYTES, a.stream>>>(pp);
+        const long items = (long)slots * a.H;
+        const int sms = device_sms();
+        const int grid = (int)((sms > 0 && items > 2L * sms) ? 2L * sms : items);
+        kp<<<dim3(grid), prep::NTHR, prep::SMEM_BYTES, a.stream>>>(pp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
