@@ -48,8 +48,8 @@ def algorithmic_flops_per_head_token(K, V, C):
 # 152-head case
 # (311,296 head-tokens) scaled by head-tokens to 1,048,576.  Reported only while the source is
 # unchanged; a changed kernel reports null until it is captured again.
-FUSED_TRAFFIC = {"source_sha256": "a47a858568aa054b", "workload": "dense_bf16_b4_t4096_h64_d128",
-                 "bytes": (319.67e6 + 62.64e6) * 1048576 / 311296}
+FUSED_TRAFFIC = {"source_sha256": "6d2c56c8e2b58fec", "workload": "dense_bf16_b4_t4096_h64_d128",
+                 "bytes": (319.69e6 + 62.76e6) * 1048576 / 311296}
 
 
 def kernel_code_digest(path):
@@ -587,6 +587,20 @@ def time_decode(kda, workloads, dev, stream, n_dec, d_steps):
     return dec_s, dec_bytes
 
 
+def run_gate_only(args, local):
+    """kda_gate_fwd alone (the "gate" object of the full line), for profiling: one JSON line."""
+    import torch
+
+    import chunked_kda_gb300 as kda
+    from chunked_kda_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kda.load_library()
+    peaks, _ = load_peaks()
+    print(json.dumps(time_gate(kda, workloads, dev, peaks, args.steps)), flush=True)
+
+
 def run_decode_only(args, local):
     """The decode step alone (kda_recurrent_fwd), for profiling: one JSON line."""
     import torch
@@ -621,6 +635,8 @@ def main():
                     help="skip the per-configuration timings that follow the headline step")
     ap.add_argument("--decode-only", action="store_true",
                     help="time the decode step only (kda_recurrent_fwd); for profiling")
+    ap.add_argument("--gate-only", action="store_true",
+                    help="time kda_gate_fwd alone on the headline workload's gate; for profiling")
     ap.add_argument("--decode-seqs", type=int, default=512,
                     help="one-token sequences of the decode step (32 heads each)")
     args = ap.parse_args()
@@ -630,6 +646,9 @@ def main():
         return
     if args.decode_only:
         run_decode_only(args, local)
+        return
+    if args.gate_only:
+        run_gate_only(args, local)
         return
     run_ours(args, world, rank, local)
 
