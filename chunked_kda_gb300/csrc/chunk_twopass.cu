@@ -743,6 +743,27 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                     pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
                     pack_bf16(x[8 * q + 6], x[8 * q + 7]));
     };
+    // v - Y^T of the thread's value channel and 32 tokens (the v tile's rows past the end give
+    // zero: they may hold the next sequence's tokens or NaN padding) -> the bf16 A tile of the
+    // v_new MMA
+    auto v_minus_y_tile = [&](int len) {
+        float x[32];
+        tmem_ld16(tmem + lane_base + TM::Y + 32 * hch, x);
+        tmem_ld16(tmem + lane_base + TM::Y + 32 * hch + 16, x + 16);
+        const uint32_t vrow = sb + S::V + (uint32_t)(vlane >> 6) * 8192u + (uint32_t)(vlane & 7) * 2u;
+        const uint32_t vchk = (uint32_t)((vlane & 63) >> 3);
+        float vv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vv[j] = ld_s_bf16(vrow + sw128((uint32_t)(32 * hch + j), vchk));
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (32 * hch + j < len) ? vv[j] - x[j] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st_s128(yab + sw128((uint32_t)vlane, (uint32_t)(4 * hch + q)), pack_bf16(x[8 * q], x[8 * q + 1]),
+                    pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                    pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+    };
     // copies of chunk c's image parts (issued by thread 0); the next chunk's parts are prefetched
     // to L2 along with them
     auto load_ops = [&](int c) {
@@ -800,7 +821,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         }
     };
     // h^T <- h^T Diag(2^Glast) of chunk cs (the gamma row of that chunk's kd buffer) for its
-    // state MMA; runs while that chunk's Y / o MMAs read the bf16 copy
+    // state MMA; runs while that chunk's v_new MMA does
     auto scale_h = [&](int cs) {
         const float* gm = reinterpret_cast<const float*>(smem + S::KD + (uint32_t)(cs & 1) * S::KDB + I::TILE) +
                           (K / 2) * hch;
@@ -855,26 +876,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 sy.wait(B_YDONE, (uint32_t)(c & 1));
                 if (c + 1 < nt && !sy.aborted()) load_ops(c + 1);  // the operand tiles are free
             }
-            bar_sync(BAR_YA, NTHR);  // bf16 Y^T tile, v tile with its tail zeroed
-            // ---- v_new^T = v^T T'^T - Y^T T'^T into the Y^T columns, then o^T += v_new^T Aqk^T
+            bar_sync(BAR_YA, NTHR);  // bf16 (v - Y)^T tile
+            // ---- v_new^T = (v - Y)^T T'^T into the Y^T columns, then o^T += v_new^T Aqk^T
             // (tf32: A = the FP32 v_new^T accumulator)
             if (l == 0) {
                 sy.wait(B_IMG0 + (c & 1), (uint32_t)((c >> 1) & 1));
                 if (!sy.aborted()) {
                     tc_fence_after();
-                    const uint32_t id_v = idesc_bf16(128, 64, 1, 0);
-                    const uint32_t id_n = idesc_bf16(128, 64, 0, 0, 1, 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint64_t a = desc_at(umma_desc(sb + S::V, 8192, 1024), kk * 2048);
-                        uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
-                        umma_bf16(tmem + TM::Y, a, b, id_v, kk > 0);
-                    }
+                    const uint32_t id_n = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         uint64_t a = desc_at(umma_desc(yab, 16, 1024), kk * 32);
                         uint64_t b = desc_at(umma_desc(img + I::TP, 16, 1024), kk * 32);
-                        umma_bf16(tmem + TM::Y, a, b, id_n, 1);
+                        umma_bf16(tmem + TM::Y, a, b, id_n, kk > 0);
                     }
                     umma_commit(sy.bar(B_VNDONE));
                 }
@@ -923,7 +937,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
         }
     } else {
         // ---- the 8 SIMT warps.  The initial state (or zero) into TMEM with its bf16 copy for
-        // the first Y / o MMAs; then scaled by chunk 0's 2^Glast for the first state MMA
+        // the first Y / o MMAs
         if (nt > 0) {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
@@ -939,9 +953,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             tmem_wait_st();
             tc_fence_before();
             bar_arrive(BAR_HR, NTHR);
-            sy.group_wait(B_KD0, 0u, w == 0);
-            scale_h(0);
-            tmem_wait_st();
         }
         for (int c = 0; c < nt; ++c) {
             const long t0 = bos + (long)c * C;
@@ -950,20 +961,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             if (c > 0) store_o(c - 1);
             sy.group_wait(B_YDONE, (uint32_t)(c & 1), w == 0);
             tc_fence_after();
-            // ---- Y^T -> bf16 A tile; the v tile's rows past the end zeroed (they may hold the
-            // next sequence's tokens or NaN padding, which T diag(beta)'s zero columns would not
-            // cancel)
-            acc_to_bf16_tile(TM::Y);
+            // ---- (v - Y)^T -> bf16 A tile
             sy.group_wait(B_VFULL, (uint32_t)(c & 1), w == 0);
-            if (len < C) {
-                for (int idx = tid; idx < (C - len) * 16; idx += NSIMT) {
-                    const int r = len + (idx >> 4), cbk = (idx >> 3) & 1, ch = idx & 7;
-                    st_s128(sb + S::V + cbk * 8192 + sw128(r, ch), 0u, 0u, 0u, 0u);
-                }
-            }
+            v_minus_y_tile(len);
             fence_proxy_async_smem();
             tc_fence_before();
             bar_arrive(BAR_YA, NTHR);
+            // ---- h^T scaled by this chunk's 2^Glast while the v_new MMA runs
+            sy.group_wait(B_KD0 + (c & 1), (uint32_t)((c >> 1) & 1), w == 0);
+            scale_h(c);
+            tmem_wait_st();
             // ---- v_new^T -> bf16 A tile for the state MMA
             sy.group_wait(B_VNDONE, (uint32_t)(c & 1), w == 0);
             tc_fence_after();
@@ -972,8 +979,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             tc_fence_before();
             bar_arrive(BAR_VN, NTHR);
             // ---- after the state MMA: bf16 h^T for the next chunk and o into registers (stored
-            // during the next chunk), then, while the next Y / o MMAs run, h^T scaled by the next
-            // chunk's 2^Glast
+            // during the next chunk)
             sy.group_wait(B_OHDONE, (uint32_t)(c & 1), w == 0);
             tc_fence_after();
             const bool more = c + 1 < nt;
@@ -983,12 +989,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             tmem_wait_ld();
             tmem_wait_st();
             tc_fence_before();
-            if (more) {
-                bar_arrive(BAR_HR, NTHR);
-                sy.group_wait(B_KD0 + ((c + 1) & 1), (uint32_t)(((c + 1) >> 1) & 1), w == 0);
-                scale_h(c + 1);
-                tmem_wait_st();
-            }
+            if (more) bar_arrive(BAR_HR, NTHR);
         }
         if (nt > 0 && !sy.aborted()) store_o(nt - 1);
         if (p.hT && !sy.aborted()) {

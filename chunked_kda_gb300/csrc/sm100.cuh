@@ -274,6 +274,11 @@ __device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint
                  : "memory");
 }
 
+__device__ __forceinline__ float ld_s_bf16(uint32_t a) {  // one bf16 from shared memory, as fp32
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return __uint_as_float((uint32_t)v << 16);
+}
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
