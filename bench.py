@@ -432,6 +432,7 @@ PER_CONFIG = (
     ("config 3b", "dense_bf16_b4_t4096_h64_d128"),
     ("config 4b", "dense_bf16_b8_t2048_h32_d256"),
     ("config 3b, non-safe gate", "dense_bf16_b4_t4096_h64_d128_nonsafe"),
+    ("config 4b, non-safe gate", "dense_bf16_b8_t2048_h32_d256_nonsafe"),
 )
 
 
@@ -487,14 +488,13 @@ def time_chunk_workload(kda, w, dev, steps, warmup, flush=None):
 
 def path_of(w):
     """The kernels kda_chunk_fwd runs for workload w (the library's dispatch rule): the fused
-    kernel for bf16 K = V = 128 (every gate mode), the two-pass kernels for bf16 K = V = 256
-    with a bounded gate, the stage-by-stage kernels otherwise."""
+    kernel for bf16 K = V = 128, the two-pass kernels for bf16 K = V = 256 (every gate mode),
+    the stage-by-stage kernels otherwise."""
     import torch
 
-    bounded = w.mode in (0, 1)
     if w.q.dtype == torch.bfloat16 and w.K == w.V == 128:
         return "fused"
-    if w.q.dtype == torch.bfloat16 and bounded and w.K == w.V == 256:
+    if w.q.dtype == torch.bfloat16 and w.K == w.V == 256:
         return "two-pass"
     return "stage-by-stage"
 

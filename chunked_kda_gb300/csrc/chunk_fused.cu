@@ -56,6 +56,7 @@
 
 #include "common.cuh"
 #include "kda_internal.h"
+#include "nonsafe_diag.cuh"
 #include "sm100.cuh"
 
 namespace kda {
@@ -268,16 +269,9 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
             }
         };
 
-        // ---- non-safe gate: the diagonal 16 x 16 blocks of Akk and Aqk with a factor
-        // 2^(G_i - G_j) per pair and channel (FLA skill "fla-kda", "Safe vs non-safe intra path":
-        // the token-parallel diagonal blocks), exact for any decay.  Per column j the factor
-        // runs down the rows as a product of the per-token factors 2^(G_i - G_(i-1)) <= 1.
-        // Each thread forms the sums over its two channels; four rounds of 64 entries per
-        // sub-block are summed over the 64 channel pairs through the free score operand area
-        // ([4 sub-blocks][16 entry quads][64 channel pairs] float4, 64 KB), and each thread
-        // keeps one finished entry per round for the store after the readback.  Entry order of
-        // a round q: columns cp = 2q, 15 - 2q, 2q + 1, 14 - 2q; per column j: Aqk(j, j), then
-        // Akk(i, j), Aqk(i, j) for i = j + 1 .. 15 (32 entries per column pair)
+        // ---- non-safe gate: the diagonal 16 x 16 blocks of Akk and Aqk with per-pair factors
+        // (nonsafe_diag.cuh), summed through the free score operand area; each thread keeps one
+        // entry per round for the store after the readback
         float dg[4] = {0.f, 0.f, 0.f, 0.f};
         if (ns) {
             uint32_t kr[16], qr[16];
@@ -289,59 +283,7 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 for (int i = 1; i < 16; ++i)
                     al[i] = make_float2(ex2_fast(G0[i] - G0[i - 1]), ex2_fast(G1[i] - G1[i - 1]));
             }
-            const int ch64 = 32 * cbp + l;
-            const uint32_t scr = sb + OFF_SAH;
-            // reducer of entry quad qd, part lq of sub-block rb: lanes 8 lq + (qd & 7), so the eight
-            // lanes of each phase of a 16-byte load read eight distinct bank groups
-            const int rb = tid >> 6, qd = (tid & 7) | (((tid >> 5) & 1) << 3), lq = (tid >> 3) & 3;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float buf[4];
-                int slot = 0;
-                auto emit = [&](float v) {
-                    buf[slot & 3] = v;
-                    if ((slot & 3) == 3)
-                        st_s128(scr + ((uint32_t)((rq * 16 + (slot >> 2)) * 64 + ch64) << 4), __float_as_uint(buf[0]),
-                                __float_as_uint(buf[1]), __float_as_uint(buf[2]), __float_as_uint(buf[3]));
-                    ++slot;
-                };
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int cp = 2 * q + (u >> 1);
-                    const int j = (u & 1) ? 15 - cp : cp;
-                    float2 kj = make_float2(bf_0(kr[j]), bf_1(kr[j]));
-                    emit(fmaf(bf_0(qr[j]), kj.x, bf_1(qr[j]) * kj.y));
-#pragma unroll
-                    for (int i = j + 1; i < 16; ++i) {
-                        kj = __fmul2_rn(kj, al[i]);
-                        emit(fmaf(bf_0(kr[i]), kj.x, bf_1(kr[i]) * kj.y));
-                        emit(fmaf(bf_0(qr[i]), kj.x, bf_1(qr[i]) * kj.y));
-                    }
-                }
-                bar_sync(BAR_PREP, NGRP);
-                // entry 4 qd + lq of sub-block rb: the 64 channel pairs in four parts of 16 (a
-                // rotated start keeps the warp's loads on distinct bank groups), then the parts
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int ln = 16 * lq + ((k + qd) & 15);
-                    uint32_t x0, x1, x2, x3;
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                                 : "r"(scr + ((uint32_t)((rb * 16 + qd) * 64 + ln) << 4)));
-                    sum.x += __uint_as_float(x0); sum.y += __uint_as_float(x1);
-                    sum.z += __uint_as_float(x2); sum.w += __uint_as_float(x3);
-                }
-#pragma unroll
-                for (int m = 8; m <= 16; m <<= 1) {
-                    sum.x += __shfl_xor_sync(0xffffffffu, sum.x, m);
-                    sum.y += __shfl_xor_sync(0xffffffffu, sum.y, m);
-                    sum.z += __shfl_xor_sync(0xffffffffu, sum.z, m);
-                    sum.w += __shfl_xor_sync(0xffffffffu, sum.w, m);
-                }
-                dg[q] = (lq == 0) ? sum.x : (lq == 1) ? sum.y : (lq == 2) ? sum.z : sum.w;
-                bar_sync(BAR_PREP, NGRP);  // the next round rewrites the area
-            }
+            nsdiag::pass(kr, qr, al, bf_0, bf_1, rq, 32 * cbp + l, tid, sb + OFF_SAH, BAR_PREP, dg);
         }
 
         uint32_t kr[16], qr[16];
@@ -568,15 +510,14 @@ __device__ __forceinline__ void prep_loop(const Params& p, uint32_t sb, uint8_t*
                 }
             }
         }
-        if (ns) {  // the per-pair diagonal entries (entry 4 qd + lq of sub-block rb in each round)
-            const int rb = tid >> 6, e = 4 * ((tid & 7) | (((tid >> 5) & 1) << 3)) + ((tid >> 3) & 3);
+        if (ns) {  // the per-pair diagonal entries this thread holds (one per round)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int cp = 2 * q + (e >> 5), x0 = e & 31, len0 = 31 - 2 * cp;
-                const int j = (x0 < len0) ? cp : 15 - cp;
-                const int x = (x0 < len0) ? x0 : x0 - len0;
-                const int I = 16 * rb + j + ((x + 1) >> 1), J = 16 * rb + j;
-                if (x & 1) {
+                int rb, i, j;
+                bool akk;
+                nsdiag::entry(tid, q, rb, i, j, akk);
+                const int I = 16 * rb + i, J = 16 * rb + j;
+                if (akk) {
                     As[J * LD + I] = bcur[I] * dg[q];  // Akk^T, beta-scaled
                 } else {
                     st_s32(sb + OFF_AQK + (uint32_t)(J >> 5) * 8192u + sw128(I, (uint32_t)((J & 31) >> 2)) +

@@ -5,17 +5,20 @@
 // code map": the intra / solve stages depend only on the chunk's own inputs, the state scan is
 // the one sequential stage):
 //
-//   pass 1, chunk_prep_kernel: one CTA per (chunk, head), every chunk in parallel.  a1 gate
+//   pass 1, chunk_prep_kernel: persistent CTAs over the (chunk, head) items, every chunk in
+//     parallel.  a1 gate
 //     activation and chunk-local log2 cumsum, a2 the causal scores on 16-token sub-blocks as one
 //     tcgen05 MMA of N = 160 causal columns per 128 key channels (Helion PR #3290, causal columns
 //     only; midpoint anchors and paired offsets, FLA skill "fla-kda", "Safe gate numerical
 //     note"), a3 T = (I + Akk)^-1.  It writes T diag(beta) (bf16) and Aqk (fp32) for the chunk,
 //     as the byte images of the shared-memory operand tiles the second pass multiplies with.
-//   pass 2, chunk_chain_kernel: one CTA per (sequence, head, 128 value channels).  a1 again
-//     (cheaper than storing G), the operands k 2^G, s q 2^G, k 2^(Gl - G), and the state chain
+//     It also writes the chain's operands k 2^G, s q 2^G, k 2^(Gl - G) and 2^Gl.  With the
+//     non-safe gate the anchors sit at sub-block first rows and the diagonal 16 x 16 blocks take
+//     per-pair factors (nonsafe_diag.cuh).
+//   pass 2, chunk_chain_kernel: one CTA per (sequence, head, 128 value channels), the state chain
 //     a4-a6 on tcgen05 with the FP32 state h^T [128 v x K] in TMEM:
-//        Y^T  = h^T (k 2^G)^T,  o^T = h^T (s q 2^G)^T
-//        vn^T = v^T (T diag beta)^T - Y^T (T diag beta)^T        (v_new = u - w h)
+//        [Y^T | o^T] = h^T [(k 2^G)^T | (s q 2^G)^T]
+//        vn^T = (v - Y)^T (T diag beta)^T                          (v_new = u - w h)
 //        o^T += vn^T Aqk^T  (tf32, A = the FP32 vn^T accumulator)
 //        h^T <- h^T Diag(2^Gl) + vn^T (k 2^(Gl - G))
 // Rows beyond the end of a sequence are zero in every operand.
@@ -25,6 +28,7 @@
 
 #include "common.cuh"
 #include "kda_internal.h"
+#include "nonsafe_diag.cuh"
 #include "sm100.cuh"
 
 namespace kda {
@@ -99,7 +103,8 @@ struct Params {
     int qnorm;     // write the sums of q^2 per row (deferred q l2norm)
 };
 
-template <int K, typename GT>
+// kNS: the non-safe gate (first-row anchors off the diagonal, per-pair diagonal blocks)
+template <int K, typename GT, bool kNS>
 __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -143,7 +148,8 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
     const float scale = rsqrtf((float)K);
     const GT* gptr = reinterpret_cast<const GT*>(p.g);
     const float lbl2 = p.lb * kLog2e;
-    const float m = (p.mode == 1) ? lbl2 : kLog2e;
+    // per-token factor into log2 units (the non-safe activation is in log2 units already)
+    const float m = kNS ? 1.f : (p.mode == 1) ? lbl2 : kLog2e;
 
     // Persistent: the CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...; the warps idle
     // during an item's inverse send the next item's rows towards L2
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
         const int hq = h / p.hr;
         // beta of the chunk (its previous readers finished with the previous item)
         if (tid < C) bsm[tid] = (tid < len) ? __bfloat162float(p.beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+        float dg[4] = {0.f, 0.f, 0.f, 0.f};  // non-safe gate: the diagonal entries this thread holds
 
         for (int half = 0; half < K / 128; ++half) {
             const int cb = 128 * half;
@@ -177,9 +184,18 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (tok * Hk + hq) * K + cn));
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr + (tok * H + h) * K + cn));
             }
-            // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair)
+            // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair).
+            // Non-safe gate: -exp(A_log) softplus(g + dt_bias) in log2 units is
+            // nA (max(y, 0) + log2(1 + 2^-|y|)), y = (g + dt_bias) log2(e), nA = -exp(A_log)
             float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
-            if (p.mode == 1) {
+            if constexpr (kNS) {
+                nA.x = -expf(__ldg(p.A_log + h * K + cb + d0));
+                nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1));
+                if (p.dt_bias) {
+                    nAd.x = __ldg(p.dt_bias + h * K + cb + d0) * kLog2e;
+                    nAd.y = __ldg(p.dt_bias + h * K + cb + d0 + 1) * kLog2e;
+                }
+            } else if (p.mode == 1) {
                 nA.x = -expf(__ldg(p.A_log + h * K + cb + d0)) * kLog2e;
                 nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1)) * kLog2e;
                 if (p.dt_bias) {
@@ -196,7 +212,12 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 } else {
                     a = gw[i];
                 }
-                if (p.mode == 1) {
+                if constexpr (kNS) {
+                    const float2 y = __ffma2_rn(a, make_float2(kLog2e, kLog2e), nAd);
+                    const float sp0 = fmaxf(y.x, 0.f) + lg2_fast(1.f + ex2_fast(-fabsf(y.x)));
+                    const float sp1 = fmaxf(y.y, 0.f) + lg2_fast(1.f + ex2_fast(-fabsf(y.y)));
+                    a = make_float2(nA.x * sp0, nA.y * sp1);
+                } else if (p.mode == 1) {
                     float2 z = __ffma2_rn(nA, a, nAd);
                     z = __fadd2_rn(make_float2(ex2_fast(z.x), ex2_fast(z.y)), make_float2(1.f, 1.f));
                     a = make_float2(rcp_fast(z.x), rcp_fast(z.y));
@@ -226,8 +247,9 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 G0[i] = swap ? g2.y : g2.x;
                 G1[i] = swap ? g2.x : g2.y;
             }
-            gmid[rq * 128 + ch0] = G0[8];
-            gmid[rq * 128 + ch1] = G1[8];
+            // the sub-block anchors: the midpoint row (bounded gates), the first row (non-safe)
+            gmid[rq * 128 + ch0] = kNS ? G0[0] : G0[8];
+            gmid[rq * 128 + ch1] = kNS ? G1[0] : G1[8];
             // the previous half's score MMA has read the operand tiles (every thread waits; the
             // verdict is made the same in all of them)
             const bool w_ok = !(half > 0 && ok) || mbar_wait(bar, ph & 1u);
@@ -242,23 +264,40 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
             } else if (half > 0) {
                 ++ph;
             }
+            // non-safe gate: this half's channel sums of the diagonal blocks (nonsafe_diag.cuh)
+            // through the operand area, free now
+            if constexpr (kNS) {
+                float2 al[16];
+#pragma unroll
+                for (int i = 1; i < 16; ++i)
+                    al[i] = make_float2(ex2_fast(G0[i] - G0[i - 1]), ex2_fast(G1[i] - G1[i - 1]));
+                const uint32_t s0 = swap ? 0x3244u : 0x1044u, s1 = swap ? 0x1044u : 0x3244u;
+                auto bf_0 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, s0)); };
+                auto bf_1 = [&](uint32_t x) { return __uint_as_float(__byte_perm(x, 0u, s1)); };
+                nsdiag::pass(kr, qr, al, bf_0, bf_1, rq, 32 * cbp + l, tid, sb + OFF_SAH, 0u, dg);
+            }
 
             // a2 operands, channel-major [128 ch][rows] tiles: rows k 2^(G - G_m(rq)), s q 2^(G - G_m(rq));
             // columns of sub-block bi >= rq: k 2^(G_m(rq) - G) 2^(G_m(bi) - G_m(rq)) (the second factor
             // <= 1: paired offsets)
+            // (non-safe gate: rows anchored at the sub-block's first row, columns at the next
+            // sub-block's first row, or the last row for rq = 3, so every factor is <= 1; the
+            // diagonal blocks' own columns are zero, their entries come from the pass above)
             {
-                const float gm0 = G0[8], gm1 = G1[8];
+                const float gm0 = kNS ? G0[0] : G0[8], gm1 = kNS ? G1[0] : G1[8];  // row anchor
                 // chain operands from the anchored products: k 2^G = (k 2^(G - Gm)) 2^Gm,
-                // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gm - G)) 2^(Gl - Gm)
+                // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gc - G)) 2^(Gl - Gc)
                 const float Pm0 = ex2_fast(gm0), Pm1 = ex2_fast(gm1);
                 const float tl0 = swap ? tot.y : tot.x, tl1 = swap ? tot.x : tot.y;
-                const float Lm0 = ex2_fast(tl0 - gm0), Lm1 = ex2_fast(tl1 - gm1);
+                const float gc0 = kNS ? (rq < 3 ? gmid[(rq + 1) * 128 + ch0] : tl0) : gm0;  // column anchor
+                const float gc1 = kNS ? (rq < 3 ? gmid[(rq + 1) * 128 + ch1] : tl1) : gm1;
+                const float Lm0 = ex2_fast(tl0 - gc0), Lm1 = ex2_fast(tl1 - gc1);
                 float qsq[16];
                 float R0[4], R1[4];
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi) {
-                    R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gm0) : 1.f;
-                    R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gm1) : 1.f;
+                    R0[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch0] - gc0) : (kNS ? 0.f : 1.f);
+                    R1[bi] = (bi > rq) ? ex2_fast(gmid[bi * 128 + ch1] - gc1) : (kNS ? 0.f : 1.f);
                 }
                 const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
                 const uint32_t nat = swap ? 0x1032u : 0x3210u;  // (ch0, ch1) word -> (d0, d0 + 1) word
@@ -275,7 +314,7 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                         for (int u = 0; u < 2; ++u) {
                             const int i = 8 * hf + 2 * pr + u;
                             const float e0 = ex2_fast(G0[i] - gm0), e1 = ex2_fast(G1[i] - gm1);
-                            const float f0 = ex2_fast(gm0 - G0[i]), f1 = ex2_fast(gm1 - G1[i]);
+                            const float f0 = ex2_fast(gc0 - G0[i]), f1 = ex2_fast(gc1 - G1[i]);
                             const float kv0 = __uint_as_float(__byte_perm(kr[i], 0u, sel0));
                             const float kv1 = __uint_as_float(__byte_perm(kr[i], 0u, sel1));
                             const float qv0 = __uint_as_float(__byte_perm(qr[i], 0u, sel0));
@@ -402,12 +441,22 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sv[e] = own_a ? va[e] : vb[e];
                 if (!is_q) {
-                    if (t <= bi) {
+                    if (t < bi || (t == bi && !kNS)) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int j = 16 * t + e;
                             As[j * LD + i] = (j < i) ? b_i * sv[e] : 0.f;
                         }
+                    }
+                } else if (kNS && t == bi) {
+                    // the diagonal block (non-safe gate): zeros above the diagonal here, the
+                    // per-pair entries below
+                    const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = 16 * t + e;
+                        if (j > i)
+                            st_s32(ab + sw128(i, (uint32_t)(4 * (t & 1) + (e >> 2))) + (uint32_t)(e & 3) * 4u, 0u);
                     }
                 } else {
                     const uint32_t ab = sb + OFF_AQK + (uint32_t)(t >> 1) * 8192u;
@@ -421,6 +470,23 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                         }
                         st_s128(ab + sw128(i, (uint32_t)(4 * (t & 1) + c4)), x[0], x[1], x[2], x[3]);
                     }
+                }
+            }
+        }
+        if constexpr (kNS) {  // the per-pair diagonal entries this thread holds (one per round)
+            const float scale_q = rsqrtf((float)K);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                int rb, i, j;
+                bool akk;
+                nsdiag::entry(tid, q, rb, i, j, akk);
+                const int I = 16 * rb + i, J = 16 * rb + j;
+                if (akk) {
+                    As[J * LD + I] = bsm[I] * dg[q];  // Akk^T, beta-scaled
+                } else {
+                    st_s32(sb + OFF_AQK + (uint32_t)(J >> 5) * 8192u + sw128(I, (uint32_t)((J & 31) >> 2)) +
+                               (uint32_t)(J & 3) * 4u,
+                           __float_as_uint(scale_q * dg[q]));
                 }
             }
         }
@@ -1025,10 +1091,12 @@ namespace fused {
 bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D);
 }
 
-// bf16, K = V in {128, 256}, a bounded gate (the sub-block anchors rely on it), at most 65535
-// heads (a grid dimension).  Both chunk sizes run as 64-token chunks, as on the fused path.
+// bf16, K = V in {128, 256}, at most 65535 heads (a grid dimension); the non-safe gate with
+// K = V = 256 only (K = V = 128 takes the fused kernel for it).  Both chunk sizes run as 64-token
+// chunks, as on the fused path.
 bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H) {
-    return qkv_bf16 && K == V && (K == 128 || K == 256) && (mode == 0 || mode == 1) && H <= 65535;
+    const bool gate_ok = mode == 0 || mode == 1 || (mode == 2 && K == 256);
+    return qkv_bf16 && K == V && (K == 128 || K == 256) && gate_ok && H <= 65535;
 }
 
 size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed) {
@@ -1072,7 +1140,7 @@ cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
     const int hr = a.H / Hk;
     // pass 1: every (chunk, head), two persistent CTAs per SM
     {
-        auto kp = prep::chunk_prep_kernel<K, GT>;
+        auto kp = (a.mode == 2) ? prep::chunk_prep_kernel<K, GT, true> : prep::chunk_prep_kernel<K, GT, false>;
         cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, prep::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         prep::Params pp{(const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.beta,

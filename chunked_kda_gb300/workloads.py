@@ -187,6 +187,9 @@ def make(name, device="cpu"):
     if name == "dense_bf16_b2_t2048_h32_d256":  # a quarter of the D = 256 workload (profiling)
         return make_dense(name, 2, 2048, 32, 256, 256, 64, torch.bfloat16, 1007, device,
                           g_std=2.0)
+    if name == "dense_bf16_b8_t2048_h32_d256_nonsafe":
+        return make_dense(name, 8, 2048, 32, 256, 256, 64, torch.bfloat16, 1004, device,
+                          g_std=2.0, mode=GATE_NONSAFE)
     if name == "dense_bf16_b8_t2048_h32_d256":
         return make_dense(name, 8, 2048, 32, 256, 256, 64, torch.bfloat16, 1004, device,
                           g_std=2.0)

@@ -197,7 +197,7 @@ def test_launch_counts(lib):
     SAFE, NONSAFE = 1, 2
     assert f(F32, F32, 1, 128, 2, 64, 64, 64, 0, SAFE) == 6           # stage-by-stage
     assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 2      # two-pass
-    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 6   # unbounded gate, K = 256: stages
+    assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 2   # two-pass, non-safe instance
     assert f(BF16, BF16, 4, 4096, 64, 128, 256, 64, 0, SAFE) == 6      # K != V: stages
     assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 1   # fused, non-safe instance
     assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, NONSAFE) == 1
@@ -257,14 +257,15 @@ def test_workspace_bytes(lib):
     finally:
         lib.kda_test_hooks(-1, 0, 0, 0)
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
-    # by gate mode: the fused kernel takes every mode; with K = V = 256 the non-safe gate runs on
-    # the stage-by-stage path (scratch for bf16 too)
+    # by gate mode: the fused and two-pass kernels take every mode; float32 inputs and K != V run
+    # on the stage-by-stage path
     ex = lib.kda_chunk_workspace_bytes_ex
     ex.restype = ctypes.c_size_t
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 0) == 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 2) == 0
-    assert ex(BF16, 4, 2048, 8, 256, 256, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
+    assert ex(BF16, 4, 2048, 8, 256, 256, 64, 0, 2) == 4 * 32 * 8 * img(256)
+    assert ex(F32, 4, 2048, 8, 256, 256, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
         F32, 4, 2048, 8, 256, 256, 64, 0) > 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 3) == 0  # no such mode
     assert ex(F32, B, T, H, K, V, C, 0, 2) == lib.kda_chunk_workspace_bytes(F32, B, T, H, K, V, C, 0)

@@ -61,13 +61,16 @@ def test_two_pass_dense_small(D, T, C, o_dtype):
 VARLEN_LENGTHS = [0, 37, 64, 1, 0, 0, 130, 65, 16, 0]
 
 
-@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE], ids=["pre", "safe"])
+@pytest.mark.parametrize("mode", [workloads.GATE_PRE, workloads.GATE_SAFE, workloads.GATE_NONSAFE],
+                         ids=["pre", "safe", "nonsafe"])
 @pytest.mark.parametrize("D", [128, 256])
 def test_two_pass_varlen_contract(D, mode):
     """Packed sequences with empty slots first, interior, consecutive and last, and a
     NaN-poisoned capacity tail (attention-gym PR #317, Agent note): the tail is not written,
     empty slots pass their state through and each packed sequence equals the same sequence run
     alone, bit for bit."""
+    if D == 128 and mode == workloads.GATE_NONSAFE:
+        pytest.skip("K = V = 128 takes the fused kernel for the non-safe gate")
     cap = sum(VARLEN_LENGTHS) + 23
     w = workloads.make_varlen("t", VARLEN_LENGTHS, cap, 2, D, D, 64, torch.bfloat16, 941, mode=mode)
     t = to_device(w)
@@ -92,6 +95,21 @@ def test_two_pass_varlen_contract(D, mode):
             od, sd = run_gpu(wd)
             assert torch.equal(od[0], o[0, sl]), f"sequence {n}: packed != alone"
             assert torch.equal(sd[0], st[n])
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("o_dtype", [None, torch.float32], ids=["bf16out", "f32out"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("g_std", [1.0, 30.0], ids=["g1", "g30"])
+def test_two_pass_nonsafe_gate(g_std, C, o_dtype):
+    """The non-safe gate -exp(A_log) softplus(g + dt_bias) (FLA skill "fla-kda", "Gate modes") on
+    the K = V = 256 two-pass path: first-row anchors off the diagonal, per-pair factors on the
+    diagonal 16 x 16 blocks.  With raw g ~ N(0, 30) single tokens decay by e^-1000 and more."""
+    w = workloads.make_dense("t", 2, 150, 2, 256, 256, C, torch.bfloat16, 1101 + C, state_std=0.05,
+                             g_std=g_std, mode=workloads.GATE_NONSAFE)
+    assert _launches(w) == 2
+    o, st = run_gpu(w, o_dtype=o_dtype)
+    assert torch.isfinite(o).all() and torch.isfinite(st).all()
     compare(w, o, st)
 
 
