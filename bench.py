@@ -488,13 +488,13 @@ def time_chunk_workload(kda, w, dev, steps, warmup, flush=None):
 
 def path_of(w):
     """The kernels kda_chunk_fwd runs for workload w (the library's dispatch rule): the fused
-    kernel for bf16 K = V = 128, the two-pass kernels for bf16 K = V = 256 (every gate mode),
-    the stage-by-stage kernels otherwise."""
+    kernel for bf16 K = V = 128, the two-pass kernels for bf16 K in {128, 256} with V a multiple
+    of 128 otherwise, the stage-by-stage kernels for the rest."""
     import torch
 
     if w.q.dtype == torch.bfloat16 and w.K == w.V == 128:
         return "fused"
-    if w.q.dtype == torch.bfloat16 and w.K == w.V == 256:
+    if w.q.dtype == torch.bfloat16 and w.K in (128, 256) and w.V >= 128 and w.V % 128 == 0:
         return "two-pass"
     return "stage-by-stage"
 

@@ -1091,12 +1091,14 @@ namespace fused {
 bool make_map(CUtensorMap* m, const void* base, long tokens, int H, int D);
 }
 
-// bf16, K = V in {128, 256}, at most 65535 heads (a grid dimension); the non-safe gate with
-// K = V = 256 only (K = V = 128 takes the fused kernel for it).  Both chunk sizes run as 64-token
-// chunks, as on the fused path.
+// bf16, K in {128, 256} and V a multiple of 128 (pass 1 depends on K only, pass 2 takes the
+// value channels in blocks of 128), at most 65535 heads (a grid dimension); every gate mode
+// except the non-safe gate at K = V = 128, which the fused kernel takes.  Both chunk sizes run
+// as 64-token chunks, as on the fused path.
 bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H) {
-    const bool gate_ok = mode == 0 || mode == 1 || (mode == 2 && K == 256);
-    return qkv_bf16 && K == V && (K == 128 || K == 256) && gate_ok && H <= 65535;
+    const bool dims_ok = (K == 128 || K == 256) && V >= 128 && V % 128 == 0;
+    const bool gate_ok = mode == 0 || mode == 1 || (mode == 2 && !(K == 128 && V == 128));
+    return qkv_bf16 && dims_ok && gate_ok && H <= 65535;
 }
 
 size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed) {

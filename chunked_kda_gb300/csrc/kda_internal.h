@@ -103,14 +103,15 @@ void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_
 bool hook_two_pass_d128();
 
 // Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, every gate mode), the
-// two-pass tensor-core kernels (bf16, K = V = 256, bounded gate; K = V = 128 too under the test
-// hook), or the stage-by-stage float32 kernels (everything else)
+// two-pass tensor-core kernels (bf16, K in {128, 256} with V a multiple of 128 other than
+// K = V = 128, every gate mode; K = V = 128 too under the test hook), or the stage-by-stage
+// float32 kernels (everything else)
 enum class Path { Fused, TwoPass, Precise };
 inline Path select_path(bool qkv_bf16, int K, int V, int C, int mode, int H, bool q_l2norm) {
     (void)q_l2norm;  // every path supports the deferred q l2norm
     const bool two = twopass_supported_dims(qkv_bf16, K, V, mode, H);
     if (fused_supported_dims(qkv_bf16, K, V, C, mode) && !(two && hook_two_pass_d128())) return Path::Fused;
-    if (two && (K == 256 || hook_two_pass_d128())) return Path::TwoPass;
+    if (two && (K != 128 || V != 128 || hook_two_pass_d128())) return Path::TwoPass;
     return Path::Precise;
 }
 

@@ -83,10 +83,10 @@ typedef enum {
     KDA_GATE_SAFE = 1,
     /* in-kernel mode without the safe gate: a = -exp(A_log) * softplus(g + dt_bias),
        A_log required, dt_bias optional, lower_bound ignored; the decay is
-       unbounded (same section).  The chunked forward runs it on the float32
-       stage-by-stage path, whose intra-chunk decay ratios 2^(G_i - G_j), j <= i,
-       never exceed 1; that path needs a workspace even for bf16 inputs
-       (kda_chunk_workspace_bytes_ex). */
+       unbounded (same section).  The tensor-core paths anchor the off-diagonal
+       scores at sub-block first rows (every factor <= 1) and compute the
+       diagonal 16 x 16 blocks with per-pair factors 2^(G_i - G_j), j <= i; the
+       float32 stage-by-stage path uses per-pair factors throughout. */
     KDA_GATE_NONSAFE = 2,
     /* the per-token log2 decay itself (S rows scale by 2^g): the gate of the
        recurrent entry points (attention-gym PR #317, Agent note); rejected by
@@ -124,8 +124,9 @@ size_t kda_chunk_workspace_bytes(kda_dtype qkv_dtype, int B, int T, int H, int K
                                  int chunk_size, int n_seqs);
 
 /* The scratch size for a given gate mode: kda_chunk_workspace_bytes is this with
-   KDA_GATE_SAFE (the pre-gated mode needs the same); KDA_GATE_NONSAFE selects
-   the stage-by-stage path, which needs scratch for bf16 inputs as well. */
+   KDA_GATE_SAFE (the pre-gated mode needs the same).  Every mode takes the same
+   path for given dtypes and head sizes, so the sizes agree; the query exists for
+   callers that pass the mode through. */
 size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, int K, int V,
                                     int chunk_size, int n_seqs, kda_gate_mode mode);
 
@@ -155,14 +156,14 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  * lower-triangular solve T = (I + Akk)^-1; WY terms w = T (beta k 2^G),
  * u = T (beta v); the sequential inter-chunk state scan; the output
  * o = (1/sqrt(K)) (q 2^G) h + Aqk v_new.
- * Paths: bf16 inputs with K = V = 128 and a pre-gated or safe gate run the
- * fused tensor-core kernel (one launch, or two for the split schedule described
- * with kda_chunk_fwd_launches, no workspace); bf16 inputs with K = V = 256 and a
- * pre-gated or safe gate run the two-pass tensor-core kernels (two launches: a
- * parallel pass per chunk and head that writes T diag(beta) and Aqk into the
- * workspace, 24 KB per 64-token chunk and head, then the state chain per
- * sequence, head and 128 value channels);
- * everything else runs the stage-by-stage path (six launches, a workspace),
+ * Paths: bf16 inputs with K = V = 128 run the fused tensor-core kernel (one
+ * launch, or two for the split schedule described with kda_chunk_fwd_launches;
+ * no workspace); other bf16 inputs with K in {128, 256} and V a multiple of 128
+ * run the two-pass tensor-core kernels (two launches: a parallel pass per chunk
+ * and head that writes T diag(beta), Aqk and the state chain's operands into
+ * the workspace, 121 KB per 64-token chunk and head at K = 256, then the state
+ * chain per sequence, head and 128 value channels); every gate mode runs on
+ * both.  Everything else runs the stage-by-stage path (six launches, a workspace),
  * which computes in FP32 except that with bf16 inputs the safe-gate scores, the
  * WY terms and the output are tf32 tensor-core products with FP32 accumulation.
  *

@@ -198,7 +198,10 @@ def test_launch_counts(lib):
     assert f(F32, F32, 1, 128, 2, 64, 64, 64, 0, SAFE) == 6           # stage-by-stage
     assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, SAFE) == 2      # two-pass
     assert f(BF16, BF16, 4, 4096, 64, 256, 256, 64, 0, NONSAFE) == 2   # two-pass, non-safe instance
-    assert f(BF16, BF16, 4, 4096, 64, 128, 256, 64, 0, SAFE) == 6      # K != V: stages
+    assert f(BF16, BF16, 4, 4096, 64, 128, 256, 64, 0, SAFE) == 2      # K != V: two-pass
+    assert f(BF16, BF16, 4, 4096, 64, 256, 128, 64, 0, NONSAFE) == 2
+    assert f(BF16, BF16, 4, 4096, 64, 64, 128, 64, 0, SAFE) == 6       # K = 64: stages
+    assert f(BF16, BF16, 4, 4096, 64, 128, 64, 64, 0, SAFE) == 6       # V = 64: stages
     assert f(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, NONSAFE) == 1   # fused, non-safe instance
     assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, NONSAFE) == 1
     assert f(BF16, BF16, 1, 20480, 32, 128, 128, 32, 16, SAFE) == 1   # fused, packed
@@ -257,8 +260,8 @@ def test_workspace_bytes(lib):
     finally:
         lib.kda_test_hooks(-1, 0, 0, 0)
     assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 0
-    # by gate mode: the fused and two-pass kernels take every mode; float32 inputs and K != V run
-    # on the stage-by-stage path
+    # by gate mode: the fused and two-pass kernels take every mode; float32 inputs and head dims
+    # of 64 run on the stage-by-stage path
     ex = lib.kda_chunk_workspace_bytes_ex
     ex.restype = ctypes.c_size_t
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 0) == 0

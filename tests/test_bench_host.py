@@ -79,5 +79,6 @@ def test_path_of_follows_the_dispatch_rule():
     assert bench.path_of(w(torch.bfloat16, 128, 128, 2)) == "fused"
     assert bench.path_of(w(torch.bfloat16, 256, 256, 0)) == "two-pass"
     assert bench.path_of(w(torch.bfloat16, 256, 256, 2)) == "two-pass"
-    assert bench.path_of(w(torch.bfloat16, 128, 256, 1)) == "stage-by-stage"
+    assert bench.path_of(w(torch.bfloat16, 128, 256, 1)) == "two-pass"
+    assert bench.path_of(w(torch.bfloat16, 64, 128, 1)) == "stage-by-stage"
     assert bench.path_of(w(torch.float32, 128, 128, 1)) == "stage-by-stage"

@@ -1,7 +1,8 @@
-"""The two-pass tensor-core path of kda_chunk_fwd (bf16, K = V in {128, 256}, bounded gate):
-pass 1 per (chunk, head) writes T diag(beta) and Aqk into the workspace, pass 2 per (sequence,
-head, 128 value channels) runs the state chain.  K = V = 256 takes it by default; K = V = 128
-takes it under the library's test hook (the fused kernel is the default there).  Checked
+"""The two-pass tensor-core path of kda_chunk_fwd (bf16, K in {128, 256}, V a multiple of 128):
+pass 1 per (chunk, head) writes T diag(beta), Aqk and the chain's operands into the workspace,
+pass 2 per (sequence, head, 128 value channels) runs the state chain.  K = V = 256 and K != V
+take it by default; K = V = 128 takes it under the library's test hook (the fused kernel is the
+default there).  Checked
 against the float64 oracle element by element, with the varlen contract's bitwise parts, on
 small inputs spanning several chunks and ragged tails."""
 import contextlib
@@ -111,6 +112,34 @@ def test_two_pass_nonsafe_gate(g_std, C, o_dtype):
     o, st = run_gpu(w, o_dtype=o_dtype)
     assert torch.isfinite(o).all() and torch.isfinite(st).all()
     compare(w, o, st)
+
+
+@pytest.mark.parametrize("o_dtype", [None, torch.float32], ids=["bf16out", "f32out"])
+@pytest.mark.parametrize("mode,g_std", [(workloads.GATE_SAFE, 1.0), (workloads.GATE_NONSAFE, 30.0)],
+                         ids=["safe", "nonsafe"])
+@pytest.mark.parametrize("K,V", [(128, 256), (256, 128)])
+def test_two_pass_k_not_v(K, V, mode, g_std, o_dtype):
+    """K != V (FLA skill "fla-kda", "Correctness checklist": D != Dv): pass 1 works on the K key
+    channels, pass 2 on V / 128 value blocks with a [128 v][K] state each."""
+    w = workloads.make_dense("t", 2, 150, 2, K, V, 64, torch.bfloat16, 1201 + K + V, state_std=0.05,
+                             g_std=g_std, mode=mode)
+    assert _launches(w) == 2
+    o, st = run_gpu(w, o_dtype=o_dtype)
+    compare(w, o, st)
+
+
+@pytest.mark.parametrize("K,V", [(128, 256), (256, 128)])
+def test_two_pass_k_not_v_varlen(K, V):
+    cap = sum(VARLEN_LENGTHS) + 23
+    w = workloads.make_varlen("t", VARLEN_LENGTHS, cap, 2, K, V, 64, torch.bfloat16, 1211 + K,
+                              mode=workloads.GATE_SAFE)
+    o, st = run_gpu(w)
+    compare(w, o, st)
+    end = int(w.cu_seqlens[-1])
+    t = to_device(w)
+    for n, L in enumerate(VARLEN_LENGTHS):
+        if L == 0:
+            assert torch.equal(st[n], t["initial_state"][n])
 
 
 @pytest.mark.parametrize("lb,g_std", [(-5.0, 10.0), (-1e-4, 3.0)])
