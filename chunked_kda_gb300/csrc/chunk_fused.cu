@@ -180,7 +180,7 @@ struct Sync {
     // bounded wait; after any timeout the CTA stops waiting
     __device__ __forceinline__ void wait(int i, uint32_t parity) const {
         if (*abort_flag) return;
-        if (!mbar_wait(bar(i), parity)) give_up();
+        if (!mbar_wait_unless(bar(i), parity, abort_flag)) give_up();
     }
     __device__ __forceinline__ bool aborted() const { return *abort_flag != 0u; }
     // wait of a whole warp group: one warp polls, the others sleep on the group's barrier
@@ -1240,6 +1240,7 @@ void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_
 }
 
 bool hook_two_pass_d128() { return g_hook_two_pass.load(std::memory_order_relaxed) != 0; }
+int hook_stall_chunk() { return g_hook_stall_chunk.load(std::memory_order_relaxed); }
 
 static bool split_allowed() { return g_hook_one_launch.load(std::memory_order_relaxed) == 0; }
 

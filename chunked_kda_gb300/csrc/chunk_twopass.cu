@@ -698,7 +698,7 @@ struct Tmem {
     static_assert(O + 64 <= COLS, "TMEM");
 };
 
-enum { B_OPS = 0, B_KD0, B_KD1, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, NBAR };
+enum { B_OPS = 0, B_KD0, B_KD1, B_YDONE, B_VFULL, B_IMG0, B_IMG1, B_VNDONE, B_OHDONE, B_DRAIN, B_STALL, NBAR };
 
 struct Params {
     const float* h0;
@@ -710,6 +710,8 @@ struct Params {
     ChunkMap cm;
     const uint8_t* img;  // pass 1's images [slots][H][Img<K>::BYTES]
     int* status;         // optional caller word: bit 0 when a wait gives up
+    int stall_chunk;     // test hook (>= 0): at this chunk the issuing warp waits, with a short
+                         // limit, on an mbarrier nothing arrives on, and gives up
 };
 
 struct Sync {
@@ -719,6 +721,8 @@ struct Sync {
     __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * i; }
     __device__ __forceinline__ void wait(int i, uint32_t parity) const {
         if (*abort_flag) return;
+        // (the plain wait: the abort-aware one measured 2 % slower on this kernel; a give-up
+        // reaches the other waits of the CTA through their own limits)
         if (!mbar_wait(bar(i), parity)) {
             atomicAdd(&g_twopass_timeouts, 1u);
             if (status) atomicOr(status, 1);
@@ -920,6 +924,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             const long t0 = bos + (long)c * C;
             const uint32_t img = sb + S::IMG + (uint32_t)(c & 1) * I::HANDOFF;
             const uint32_t kdb = S::KD + (uint32_t)(c & 1) * S::KDB;
+            if (c == p.stall_chunk && l == 0 && !sy.aborted() && !mbar_wait(sy.bar(B_STALL), 0, 1u << 10)) {
+                atomicAdd(&g_twopass_timeouts, 1u);  // test hook: a bounded wait that gives up
+                if (p.status) atomicOr(p.status, 1);
+                *sy.abort_flag = 1u;
+            }
             if (l == 0) sy.wait(B_OPS, (uint32_t)(c & 1));
             bar_sync(BAR_HR, NTHR);  // bf16 h^T of the state before chunk c; o^T of chunk c - 1 read
             // ---- [Y^T | o^T] = h^T [(k 2^G)^T | (s q 2^G)^T] (N = 128)
@@ -1165,7 +1174,7 @@ cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
     cudaError_t e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     chain::Params cp{a.h0, a.hT, a.cu, a.o, a.T, a.H, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
-                     a.status};
+                     a.status, hook_stall_chunk()};
     kc<<<dim3(a.V / 128, a.N, a.H), chain::NTHR, smem, a.stream>>>(mv, cp);
     return cudaGetLastError();
 }

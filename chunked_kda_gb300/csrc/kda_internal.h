@@ -101,6 +101,7 @@ cudaError_t read_twopass_timeouts(unsigned* count, bool reset);
 // the fused path's test hooks (kda_test_hooks)
 void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_d128);
 bool hook_two_pass_d128();
+int hook_stall_chunk();  // the forced-give-up chunk of both tensor-core paths (-1: none)
 
 // Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, every gate mode), the
 // two-pass tensor-core kernels (bf16, K in {128, 256} with V a multiple of 128 other than

@@ -48,6 +48,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// The same wait, which also stops (returning true) once `*abort` is nonzero: another thread of
+// the CTA gave up a wait, and nothing this one waits for may come any more.  The flag is read
+// every 256 polls only: read in every poll it cost the fused kernel 9 % (the shape of these
+// poll loops shows in the kernels' times; a rolled or nested form measured slower too).
+__device__ __forceinline__ bool mbar_wait_unless(uint32_t bar, uint32_t parity, const volatile uint32_t* abort,
+                                                 uint32_t limit = 1u << 22) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return true;
+    }
+    return false;
+}
 
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -345,10 +345,11 @@ kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
 /*
  * Test hooks of the tensor-core paths, process-wide, all off by default and read by nothing
  * else (no environment variables).  For tests only; set them back to (-1, 0, 0, 0) afterwards.
- *   wait_timeout_chunk  >= 0: every CTA of later fused launches waits, at that chunk and
- *                       with a short limit, on an mbarrier nothing completes, and takes the
- *                       give-up path (counted by kda_fused_wait_timeouts, flagged in the
- *                       status word of kda_chunk_fwd_ex); -1: off
+ *   wait_timeout_chunk  >= 0: every CTA of later fused launches and of the two-pass state
+ *                       chain waits, at that chunk and with a short limit, on an mbarrier
+ *                       nothing completes, and takes the give-up path (counted by
+ *                       kda_fused_wait_timeouts, flagged in the status word of
+ *                       kda_chunk_fwd_ex); -1: off
  *   sm_count            > 0: plan the split schedule (kda_chunk_fwd_launches) for this many
  *                       SMs instead of the device's; 0: the device's
  *   one_launch          nonzero: never split a fused call into two launches

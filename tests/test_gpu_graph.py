@@ -79,9 +79,10 @@ def test_recurrent_graph_replay_mutated_boundaries_and_history():
         check_state(S, s_ref2, torch.bfloat16)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["fused", "stagewise"])
-def test_chunk_graph_replay_mutated_boundaries(dtype):
-    cap, H, K, V, N = 300, 2, 128, 128, 3
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float32, 128), (torch.bfloat16, 256)],
+                         ids=["fused", "stagewise", "two-pass"])
+def test_chunk_graph_replay_mutated_boundaries(dtype, D):
+    cap, H, K, V, N = 300, 2, D, D, 3
     dev = "cuda"
     lens0 = [100, 0, 150]
     w = workloads.make_varlen("g", lens0, cap, H, K, V, 64, dtype, 730, poison_tail=False)
