@@ -415,10 +415,13 @@ def run_ours(args, world, rank, local):
     if not args.no_cpu_baseline:
         cores = host_cores()
         tok, dt = oracle_sample(w, 2 * cores, cores, seed=1234)
+        tok1, dt1 = oracle_sample(w, 1, 1, seed=1235)
         line["cpu_baseline"] = {"value": tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{2 * cores} random (sequence, head) units of {args.workload} "
                                           f"({w.T} tokens each), float64, one OpenMP thread "
-                                          f"per unit"}
+                                          f"per unit",
+                                "single_core": {"value": tok1 / dt1, "unit": UNIT,
+                                                "sample": "one (sequence, head) unit, one thread"}}
     print(json.dumps(line), flush=True)
 
 
