@@ -699,6 +699,17 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
                                            int nt) {
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     const int ct = tid - NGRP;          // 0 .. 255
+    // a wait after which every thread continues on its own data: with the non-safe gate every
+    // warp polls the barrier itself (the chain mostly waits there, 4 % faster); with bounded
+    // gates one warp polls and the group barrier releases the rest (the preparation group is
+    // the busy one and keeps the issue slots: 2.6 % faster)
+    auto chain_wait = [&](int i, uint32_t parity) {
+        if constexpr (kNS) {
+            sy.wait(i, parity);
+        } else {
+            sy.group_wait(i, parity, w == 8, BAR_CHAIN);
+        }
+    };
     const int lg = w & 3;               // TMEM lane group
     const int vlane = 32 * lg + l;      // value channel
     const int hch = (w - 8) >> 2;       // key-channel half of the state / column half
@@ -933,7 +944,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             if (w == 8) sy.wait(B_KQFULL, c & 1);
             gate_chunk(c + 1, gw);
         }
-        sy.group_wait(B_YDONE, c & 1, w == 8, BAR_CHAIN);
+        chain_wait(B_YDONE, c & 1);
         tc_fence_after();
         // the k 2^G / s q 2^G buffers are free: prefetch the next chunk's k and q tiles
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_qk(t0 + C);
@@ -1000,7 +1011,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
                 umma_commit(sy.bar(B_VNDONE));
             }
         }
-        sy.group_wait(B_VNDONE, c & 1, w == 8, BAR_CHAIN);
+        chain_wait(B_VNDONE, c & 1);
         tc_fence_after();
         if (ct == 0 && c + 1 < nt && !sy.aborted()) load_v(t0 + C);  // the v tile is free again
         // ---- o^T += v_new^T Aqk^T: tf32 MMAs whose A operand is the FP32 v_new^T accumulator itself
@@ -1040,7 +1051,7 @@ __device__ __forceinline__ void chain_loop(const Params& p, uint32_t sb, uint8_t
             }
             umma_commit(sy.bar(B_OHDONE));
         }
-        sy.group_wait(B_OHDONE, c & 1, w == 8, BAR_CHAIN);
+        chain_wait(B_OHDONE, c & 1);
         tc_fence_after();
         // ---- bf16 h^T for the next chunk; o out
         {
