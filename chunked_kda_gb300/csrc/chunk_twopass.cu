@@ -167,14 +167,26 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
             // the own rows: k, q pairs and the gate pair, all loads issued first
             uint32_t kr[16], qr[16];
             GW gw[16];
+            {
+                // row pointers of the sub-block's first row, advanced by one token per row (rows
+                // past the end read the last row again: their k, q are zeroed, g adds nothing)
+                const size_t tok0 = (size_t)(t0 + min(16 * rq, len - 1));
+                const __nv_bfloat16* kp = p.k + (tok0 * Hk + hq) * K + cb + d0;
+                const __nv_bfloat16* qp = p.q + (tok0 * Hk + hq) * K + cb + d0;
+                const GT* gp = gptr + (tok0 * H + h) * K + cb + d0;
+                const size_t sqk = (size_t)Hk * K, sg = (size_t)H * K;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = 16 * rq + i;
-                const bool valid = r < len;
-                const size_t tok = (size_t)(t0 + (valid ? r : len - 1));
-                kr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.k + (tok * Hk + hq) * K + cb + d0)) : 0u;
-                qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(p.q + (tok * Hk + hq) * K + cb + d0)) : 0u;
-                gw[i] = __ldg(reinterpret_cast<const GW*>(gptr + (tok * H + h) * K + cb + d0));
+                for (int i = 0; i < 16; ++i) {
+                    const bool valid = 16 * rq + i < len;
+                    kr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(kp)) : 0u;
+                    qr[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qp)) : 0u;
+                    gw[i] = __ldg(reinterpret_cast<const GW*>(gp));
+                    if (16 * rq + i + 1 < len) {
+                        kp += sqk;
+                        qp += sqk;
+                        gp += sg;
+                    }
+                }
             }
             // the next half's rows of the warp's 64 channels towards L2 (lane i: row 16 rq + i)
             if (half + 1 < K / 128 && l < 16 && 16 * rq + l < len) {
@@ -301,6 +313,12 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 }
                 const uint32_t sel0 = swap ? 0x3244u : 0x1044u, sel1 = swap ? 0x1044u : 0x3244u;
                 const uint32_t nat = swap ? 0x1032u : 0x3210u;  // (ch0, ch1) word -> (d0, d0 + 1) word
+                // the image word of row 16 rq + i: pair_off(16 rq + i, cb + d0) =
+                // pbase + 128 i + ((chunk ^ (i & 7)) << 4), the XOR with a constant per row
+                const uint32_t pbase = (uint32_t)((cb + d0) >> 6) * 8192u + (uint32_t)rq * 2048u +
+                                       (uint32_t)((cb + d0) & 7) * 2u;
+                const uint32_t pchunk = (uint32_t)(((cb + d0) & 63) >> 3) << 4;
+                uint8_t* const ikg = img + Img<K>::KG;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const uint32_t chk = 2 * rq + hf;
@@ -331,10 +349,11 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                             const uint32_t wqg = __byte_perm(pack_bf16(qe0[u] * Pm0, qe1[u] * Pm1), 0u, nat);
                             const uint32_t wkd =
                                 __byte_perm(pack_bf16(kf0[2 * pr + u] * Lm0, kf1[2 * pr + u] * Lm1), 0u, nat);
-                            const uint32_t po = pair_off(16 * rq + i, cb + d0);
-                            *reinterpret_cast<uint32_t*>(img + Img<K>::KG + po) = wkg;
-                            *reinterpret_cast<uint32_t*>(img + Img<K>::QG + po) = wqg;
-                            *reinterpret_cast<uint32_t*>(img + Img<K>::KD + po) = wkd;
+                            uint32_t* const wp = reinterpret_cast<uint32_t*>(
+                                ikg + (pbase + (uint32_t)i * 128u + (pchunk ^ ((uint32_t)(i & 7) << 4))));
+                            wp[0] = wkg;                     // k 2^G
+                            wp[Img<K>::TILE / 4] = wqg;      // s q 2^G
+                            wp[2 * Img<K>::TILE / 4] = wkd;  // k 2^(Gl - G)
                         }
                         ak0[pr] = pack_bf16(ke0[0], ke0[1]);
                         ak1[pr] = pack_bf16(ke1[0], ke1[1]);
