@@ -197,32 +197,40 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr + (tok * H + h) * K + cn));
             }
             // a1: activation in log2 units and the sub-block's inclusive sums (f32x2 on the pair).
-            // Non-safe gate: -exp(A_log) softplus(g + dt_bias) in log2 units is
+            // The bounded-gate instances sum in the thread's (ch0, ch1) order, so no row needs a
+            // swap; the non-safe one sums in (d0, d0 + 1) order, which leaves it fewer live
+            // registers.  Non-safe gate: -exp(A_log) softplus(g + dt_bias) in log2 units is
             // nA (max(y, 0) + log2(1 + 2^-|y|)), y = (g + dt_bias) log2(e), nA = -exp(A_log)
+            constexpr bool kPairOrder = !kNS;
+            const int c0 = kPairOrder ? ch0 : d0, c1 = kPairOrder ? ch1 : d0 + 1;
             float2 nA = make_float2(0.f, 0.f), nAd = make_float2(0.f, 0.f);
             if constexpr (kNS) {
-                nA.x = -expf(__ldg(p.A_log + h * K + cb + d0));
-                nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1));
+                nA.x = -expf(__ldg(p.A_log + h * K + cb + c0));
+                nA.y = -expf(__ldg(p.A_log + h * K + cb + c1));
                 if (p.dt_bias) {
-                    nAd.x = __ldg(p.dt_bias + h * K + cb + d0) * kLog2e;
-                    nAd.y = __ldg(p.dt_bias + h * K + cb + d0 + 1) * kLog2e;
+                    nAd.x = __ldg(p.dt_bias + h * K + cb + c0) * kLog2e;
+                    nAd.y = __ldg(p.dt_bias + h * K + cb + c1) * kLog2e;
                 }
             } else if (p.mode == 1) {
-                nA.x = -expf(__ldg(p.A_log + h * K + cb + d0)) * kLog2e;
-                nA.y = -expf(__ldg(p.A_log + h * K + cb + d0 + 1)) * kLog2e;
+                nA.x = -expf(__ldg(p.A_log + h * K + cb + c0)) * kLog2e;
+                nA.y = -expf(__ldg(p.A_log + h * K + cb + c1)) * kLog2e;
                 if (p.dt_bias) {
-                    nAd.x = nA.x * __ldg(p.dt_bias + h * K + cb + d0);
-                    nAd.y = nA.y * __ldg(p.dt_bias + h * K + cb + d0 + 1);
+                    nAd.x = nA.x * __ldg(p.dt_bias + h * K + cb + c0);
+                    nAd.y = nA.y * __ldg(p.dt_bias + h * K + cb + c1);
                 }
             }
             float2 gv[16], acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float2 a;
-                if constexpr (kGateBf16) {
+                if constexpr (kGateBf16 && kPairOrder) {
+                    const uint32_t u0 = swap ? 0x3244u : 0x1044u, u1 = swap ? 0x1044u : 0x3244u;
+                    a = make_float2(__uint_as_float(__byte_perm(gw[i], 0u, u0)),
+                                    __uint_as_float(__byte_perm(gw[i], 0u, u1)));
+                } else if constexpr (kGateBf16) {
                     a = make_float2(bf_lo(gw[i]), bf_hi(gw[i]));
                 } else {
-                    a = gw[i];
+                    a = (kPairOrder && swap) ? make_float2(gw[i].y, gw[i].x) : gw[i];
                 }
                 if constexpr (kNS) {
                     const float2 y = __ffma2_rn(a, make_float2(kLog2e, kLog2e), nAd);
@@ -248,16 +256,17 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 tot = __fadd2_rn(tot, t2);  // G of the chunk's last row (rows past the end add zero)
             }
             uint8_t* img = p.img + ((size_t)slot * H + h) * Img<K>::BYTES;
-            if (rq == 0) {  // 2^Glast of the pair
+            if (rq == 0) {  // 2^Glast of the pair, in channel order
+                const float e0 = ex2_fast(tot.x), e1 = ex2_fast(tot.y);
                 *reinterpret_cast<float2*>(img + Img<K>::GAM + (cb + d0) * 4) =
-                    make_float2(ex2_fast(tot.x), ex2_fast(tot.y));
+                    (kPairOrder && swap) ? make_float2(e1, e0) : make_float2(e0, e1);
             }
-            float G0[16], G1[16];
+            float G0[16], G1[16];  // in (ch0, ch1) order
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float2 g2 = __fadd2_rn(gv[i], cy);
-                G0[i] = swap ? g2.y : g2.x;
-                G1[i] = swap ? g2.x : g2.y;
+                G0[i] = (kPairOrder || !swap) ? g2.x : g2.y;
+                G1[i] = (kPairOrder || !swap) ? g2.y : g2.x;
             }
             // the sub-block anchors: the midpoint row (bounded gates), the first row (non-safe)
             gmid[rq * 128 + ch0] = kNS ? G0[0] : G0[8];
@@ -300,7 +309,8 @@ __global__ void __launch_bounds__(NTHR, 2) chunk_prep_kernel(Params p) {
                 // chain operands from the anchored products: k 2^G = (k 2^(G - Gm)) 2^Gm,
                 // s q 2^G likewise, k 2^(Gl - G) = (k 2^(Gc - G)) 2^(Gl - Gc)
                 const float Pm0 = ex2_fast(gm0), Pm1 = ex2_fast(gm1);
-                const float tl0 = swap ? tot.y : tot.x, tl1 = swap ? tot.x : tot.y;
+                const float tl0 = (kPairOrder || !swap) ? tot.x : tot.y;
+                const float tl1 = (kPairOrder || !swap) ? tot.y : tot.x;
                 const float gc0 = kNS ? (rq < 3 ? gmid[(rq + 1) * 128 + ch0] : tl0) : gm0;  // column anchor
                 const float gc1 = kNS ? (rq < 3 ? gmid[(rq + 1) * 128 + ch1] : tl1) : gm1;
                 const float Lm0 = ex2_fast(tl0 - gc0), Lm1 = ex2_fast(tl1 - gc1);
