@@ -44,12 +44,11 @@ def algorithmic_flops_per_head_token(K, V, C):
 
 
 # DRAM bytes (read + write) per chunk_fused_kernel launch on the default workload, from one ncu
-# capture of the kernel whose code digest (kernel_code_digest) starts with `source_sha256`: the
-# 152-head case
-# (311,296 head-tokens) scaled by head-tokens to 1,048,576.  Reported only while the source is
+# capture (--set full) of that launch on that workload, of the kernel whose code digest
+# (kernel_code_digest) starts with `source_sha256`.  Reported only while the source is
 # unchanged; a changed kernel reports null until it is captured again.
-FUSED_TRAFFIC = {"source_sha256": "6d2c56c8e2b58fec", "workload": "dense_bf16_b4_t4096_h64_d128",
-                 "bytes": (319.69e6 + 62.76e6) * 1048576 / 311296}
+FUSED_TRAFFIC = {"source_sha256": "8bf4f857a5499bbe", "workload": "dense_bf16_b4_t4096_h64_d128",
+                 "bytes": 1078.164e6 + 252.525e6}
 
 
 def kernel_code_digest(path):
