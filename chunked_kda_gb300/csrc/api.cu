@@ -141,7 +141,7 @@ size_t kda_chunk_workspace_bytes_ex(kda_dtype qkv_dtype, int B, int T, int H, in
     int N = packed ? n_seqs : B;
     switch (kda::select_path(qkv_dtype == KDA_BF16, K, V, chunk_size, (int)mode, H, false)) {
         case kda::Path::Fused: return 0;
-        case kda::Path::TwoPass: return kda::twopass_workspace_bytes(T, H, K, N, packed);
+        case kda::Path::TwoPass: return kda::twopass_workspace_bytes(T, H, K, V, N, packed);
         default: return kda::precise_workspace_bytes(B, T, H, K, V, chunk_size, N, packed);
     }
 }

@@ -1254,6 +1254,7 @@ bool hook_two_pass_d128() { return g_hook_two_pass.load(std::memory_order_relaxe
 int hook_stall_chunk() { return g_hook_stall_chunk.load(std::memory_order_relaxed); }
 
 static bool split_allowed() { return g_hook_one_launch.load(std::memory_order_relaxed) == 0; }
+bool hook_one_launch() { return !split_allowed(); }
 
 // SMs of the current device (or the test hook's count), cached per device ordinal
 static int sm_count() {
@@ -1307,6 +1308,8 @@ static int split_cut_for(int N, int H, int T, bool packed, bool o_f32, int mode)
     const int stash_rows = fused::KD * fused::VD * 4 / (fused::VD * (o_f32 ? 4 : 2));
     return split_cut_chunks(N * H, sm_count(), T, stash_rows);
 }
+
+int planned_sm_count() { return sm_count(); }
 
 int fused_launch_count(int N, int H, int T, bool packed, bool o_f32, int mode) {
     return split_cut_for(N, H, T, packed, o_f32, mode) > 0 ? 2 : 1;

@@ -741,6 +741,17 @@ struct Params {
     int* status;         // optional caller word: bit 0 when a wait gives up
     int stall_chunk;     // test hook (>= 0): at this chunk the issuing warp waits, with a short
                          // limit, on an mbarrier nothing arrives on, and gives up
+    // Dense inputs, balanced schedule (chunk_chain_kernel<..., true>, one CTA per SM, all
+    // resident at once): the (sequence, head) units u = n + N h, bal_nt chunks each, laid end to
+    // end; the CTAs form groups of V / 128 (the value blocks of a head side by side), and group
+    // m runs the chunk-times [m bal_cm, (m + 1) bal_cm) of that row.  A unit cut by the boundary
+    // at m bal_cm runs its first chunks at the start of group m and its other chunks at the end
+    // of group m - 1 (bal_cm > bal_nt: the first part ends before the second starts); the FP32
+    // state of value block vb crosses in slot m (V / 128) + vb of bal_state ([K][128] words),
+    // published by the flag of the same index (zero on entry).
+    int N, bal_cm, bal_nt;
+    float* bal_state;
+    unsigned* bal_flag;
 };
 
 struct Sync {
@@ -772,39 +783,27 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const uint8_t* src, uint
         bulk_load(dst + o, src + o, min(32768u, bytes - o), bar);
 }
 
+// One piece of a (sequence, head, value block vb) unit: its chunks [c0, c1).  head_slot >= 0:
+// the piece ends before the unit does, and its final FP32 state goes to that slot of the
+// balanced schedule; cont_slot >= 0: the piece starts after the unit does, and its initial
+// state comes from that slot once its flag is set.
 template <int K, typename OT>
-__global__ void __launch_bounds__(NTHR, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
+__device__ __forceinline__ void chain_piece(const CUtensorMap& tm_v, const Params& p, uint8_t* smem,
+                                            uint32_t sb, uint32_t tmem, const Sync& sy, int vb, int n,
+                                            int h, int c0, int c1, int head_slot, int cont_slot) {
     using S = Smem<K>;
     using I = Img<K>;
     using TM = Tmem<K>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    const uint32_t sb = smem_u32(smem);
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + S::MISC);
-    Sync sy{sb + S::BAR, misc + 1, p.status};
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    const int vb = blockIdx.x, n = blockIdx.y, h = blockIdx.z, H = p.H;
-    long bos, eos;
-    if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
-    else      { bos = (long)n * p.T; eos = bos + p.T; }
-    const int nt = (int)((eos - bos + C - 1) / C);
-    const int slot0 = p.cm.first_slot(n, (int)bos);
+    const int H = p.H;
+    long sbos, seos;  // the sequence
+    if (p.cu) { sbos = __ldg(p.cu + n); seos = __ldg(p.cu + n + 1); }
+    else      { sbos = (long)n * p.T; seos = sbos + p.T; }
+    const long bos = sbos + (long)c0 * C, eos = min(sbos + (long)c1 * C, seos);
+    const int nt = c1 - c0;
+    const int slot0 = p.cm.first_slot(n, (int)sbos) + c0;
     auto image = [&](int c) { return p.img + ((size_t)(slot0 + c) * H + h) * I::BYTES; };
-
-    if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
-        fence_mbar_init();
-        misc[1] = 0;
-        misc[2] = misc[3] = misc[4] = misc[5] = 0;  // copies issued: operands, kd, v, images
-        prefetch_tmap(&tm_v);
-    }
-    if (w == 0) tmem_alloc(sb + S::MISC, TM::COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = misc[0];
     volatile uint32_t* issued = misc + 2;
 
     const int lg = w & 3, hch = w >> 2;
@@ -1040,8 +1039,24 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             mbar_wait(sy.bar(B_DRAIN), 0);
         }
     } else {
-        // ---- the 8 SIMT warps.  The initial state (or zero) into TMEM with its bf16 copy for
-        // the first Y / o MMAs
+        // ---- the 8 SIMT warps.  The initial state (or zero, or the slot a previous piece of the
+        // unit filled) into TMEM with its bf16 copy for the first Y / o MMAs
+        if (cont_slot >= 0) {  // the CTA that ran the unit's first chunks publishes it (bounded)
+            if (tid == 0 && !sy.aborted()) {
+                bool ok = false;
+                for (uint32_t i = 0; i < (1u << 22) && !ok; ++i) {
+                    ok = ld_acquire_gpu(p.bal_flag + cont_slot) != 0u;
+                    if (!ok) __nanosleep(256);
+                }
+                if (!ok) {
+                    atomicAdd(&g_twopass_timeouts, 1u);
+                    if (p.status) atomicOr(p.status, 1);
+                    *sy.abort_flag = 1u;
+                }
+            }
+            bar_sync(BAR_CHAIN, NSIMT);
+            __threadfence();
+        }
         if (nt > 0) {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
@@ -1049,7 +1064,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int kch = (K / 2) * hch + 32 * s + j;
-                    hv[j] = p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
+                    hv[j] = cont_slot >= 0 ? __ldcg(p.bal_state + ((size_t)cont_slot * K + kch) * 128 + vlane)
+                          : p.h0 ? __ldg(p.h0 + st_off + (size_t)kch * p.V + vch) : 0.f;
                 }
                 st_h(s, hv);
                 st_hA(s, hv);
@@ -1096,7 +1112,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
             if (more) bar_arrive(BAR_HR, NTHR);
         }
         if (nt > 0 && !sy.aborted()) store_o(nt - 1);
-        if (p.hT && !sy.aborted()) {
+        if (head_slot >= 0) {  // the unit's first chunks: publish the state
+            if (!sy.aborted()) {
+#pragma unroll 1
+                for (int s = 0; s < K / 64; ++s) {
+                    float hv[32];
+                    ld_h(s, hv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(p.bal_state + ((size_t)head_slot * K + (K / 2) * hch + 32 * s + j) * 128 + vlane, hv[j]);
+                }
+            }
+            __threadfence();
+            bar_sync(BAR_CHAIN, NSIMT);
+            if (tid == 0 && !sy.aborted()) st_release_gpu(p.bal_flag + head_slot, 1u);
+        } else if (p.hT && !sy.aborted()) {
 #pragma unroll 1
             for (int s = 0; s < K / 64; ++s) {
                 float hv[32];
@@ -1112,6 +1143,79 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
                 for (int j = 0; j < 32; ++j)
                     p.hT[st_off + (size_t)((K / 2) * hch + 32 * s + j) * p.V + vch] = hv[j];
             }
+        }
+    }
+}
+
+// kBal: the balanced schedule of dense inputs (a cooperative launch: its CTAs wait on one
+// another); else one CTA per (value block, sequence, head)
+template <int K, typename OT, bool kBal>
+__global__ void __launch_bounds__(NTHR, 1)
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_v, Params p) {
+    using S = Smem<K>;
+    using TM = Tmem<K>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + S::MISC);
+    Sync sy{sb + S::BAR, misc + 1, p.status};
+    const int tid = threadIdx.x, w = tid >> 5;
+    auto init_bars = [&]() {  // fresh barriers and copy counts (operands, kd, v, images)
+        for (int i = 0; i < NBAR; ++i) mbar_init(sy.bar(i), 1);
+        fence_mbar_init();
+        misc[2] = misc[3] = misc[4] = misc[5] = 0;
+    };
+    if (tid == 0) {
+        init_bars();
+        misc[1] = 0;
+        prefetch_tmap(&tm_v);
+    }
+    if (w == 0) tmem_alloc(sb + S::MISC, TM::COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if constexpr (!kBal) {
+        const int n = blockIdx.y;
+        long bos, eos;
+        if (p.cu) { bos = __ldg(p.cu + n); eos = __ldg(p.cu + n + 1); }
+        else      { bos = (long)n * p.T; eos = bos + p.T; }
+        chain_piece<K, OT>(tm_v, p, smem, sb, tmem, sy, blockIdx.x, n, blockIdx.z, 0,
+                           (int)((eos - bos + C - 1) / C), -1, -1);
+    } else {
+        // the group's pieces in order: at most a unit's first chunks, whole units, at most a
+        // unit's last chunks
+        const int nvb = p.V / 128, m = (int)blockIdx.x / nvb, vb = (int)blockIdx.x % nvb;
+        const int ntu = p.bal_nt;
+        const long s0 = (long)m * p.bal_cm, e0 = min(s0 + (long)p.bal_cm, (long)p.N * p.H * ntu);
+        const int u0 = (int)(s0 / ntu);
+        const int npieces = s0 < e0 ? (int)((e0 - 1) / ntu) - u0 + 1 : 0;
+        for (int k = 0; k < npieces; ++k) {
+            const int u = u0 + k;
+            const long ju = (long)u * ntu;
+            const long pos = max(s0, ju), pe = min(e0, ju + ntu);
+            int c0 = 0, c1 = ntu, head_slot = -1, cont_slot = -1;
+            if (pos > ju) {  // cut at the group's start: the unit's first chunks
+                c1 = (int)(pe - pos);
+                head_slot = m * nvb + vb;
+            } else if (pe < ju + ntu) {  // cut at its end: the unit's other chunks
+                c0 = ntu - (int)(pe - pos);
+                cont_slot = (m + 1) * nvb + vb;
+            }
+            if (k > 0) {  // every wait and copy of the previous piece ended
+                if (tid == 0) {
+                    for (int i = 0; i < NBAR; ++i) mbar_inval(sy.bar(i));
+                    init_bars();
+                }
+                __syncthreads();
+                tc_fence_after();
+            }
+            chain_piece<K, OT>(tm_v, p, smem, sb, tmem, sy, vb, u % p.N, u / p.N, c0, c1, head_slot, cont_slot);
+            tc_fence_before();
+            __syncthreads();
+            if (sy.aborted()) break;  // the same verdict in every thread
         }
     }
     tc_fence_before();
@@ -1139,10 +1243,51 @@ bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H) {
     return qkv_bf16 && dims_ok && gate_ok && H <= 65535;
 }
 
-size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed) {
+namespace {
+// Balanced schedule of pass 2 for dense inputs.  One CTA per (value block, sequence, head) puts
+// U = N H units of nt chunks on M = S / (V / 128) groups of SMs: U = f M + r take f + 1
+// unit-lengths, the last wave r / M full.  Laid end to end the U nt chunks fill M groups of
+// cm = ceil(U nt / M) chunk-times each: the wrap-around rule for preemptive scheduling on
+// identical machines (McNaughton, 1959), a unit cut at a group boundary running its first part
+// at the start of the later group, before its second part at the end of the earlier one
+// (cm > nt).  A group runs a few pieces, each paying about a chunk-time to start and end; kept
+// only for a clear gain.  cm = 0: one CTA per unit.
+struct ChainPlan {
+    int cm, nt, groups;
+};
+ChainPlan chain_plan(int T, int H, int V, int N, bool packed) {
+    ChainPlan pl{0, 0, 0};
+    const int nvb = V / 128;
+    if (packed || hook_one_launch() || nvb <= 0) return pl;
+    const int M = planned_sm_count() / nvb, U = N * H;
+    const long nt = (T + twopass::C - 1) / twopass::C;
+    if (M <= 0 || U <= M || U % M == 0 || nt <= 0) return pl;
+    const long cm = ((long)U * nt + M - 1) / M;
+    const long f = U / M;
+    if (20L * (cm + 2) > 19L * (f + 1) * nt) return pl;
+    pl.cm = (int)cm;
+    pl.nt = (int)nt;
+    pl.groups = M;
+    return pl;
+}
+size_t images_bytes(int T, int H, int K, int N, bool packed) {
     ChunkMap cm{packed ? reinterpret_cast<const int32_t*>(1) : nullptr, N, T, twopass::C};
     const size_t per = K == 256 ? twopass::Img<256>::BYTES : twopass::Img<128>::BYTES;
     return (size_t)cm.n_slots() * (size_t)H * per;
+}
+// the balanced schedule's flags (one per slot, rounded to 256 bytes) and FP32 [K][128] slots
+size_t flag_bytes(int slots) { return ((size_t)slots * 4 + 255) / 256 * 256; }
+size_t slot_bytes(int K) { return (size_t)K * 128 * sizeof(float); }
+}  // namespace
+
+size_t twopass_workspace_bytes(int T, int H, int K, int V, int N, bool packed) {
+    size_t bytes = images_bytes(T, H, K, N, packed);
+    const ChainPlan pl = chain_plan(T, H, V, N, packed);
+    if (pl.cm > 0) {
+        const int slots = pl.groups * (V / 128);
+        bytes += flag_bytes(slots) + (size_t)slots * slot_bytes(K);
+    }
+    return bytes;
 }
 
 cudaError_t read_twopass_timeouts(unsigned* count, bool reset) {
@@ -1198,13 +1343,41 @@ cudaError_t launch_k(const FwdArgs& a, const ChunkMap& cm, int slots) {
     CUtensorMap mv;
     const long tokens = (long)a.B * a.T;
     if (!fused::make_map(&mv, a.v, tokens, a.H, a.V)) return cudaErrorInvalidValue;
-    auto kc = chain::chunk_chain_kernel<K, OT>;
     constexpr uint32_t smem = chain::Smem<K>::BYTES;
+    chain::Params cp{a.h0, a.hT, a.cu, a.o, a.T, a.H, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
+                     a.status, hook_stall_chunk(), a.N, 0, 0, nullptr, nullptr};
+    const int nvb = a.V / 128;
+    const ChainPlan pl = chain_plan(a.T, a.H, a.V, a.N, a.cu != nullptr);
+    // (a plan for more SMs than the device has keeps one CTA per unit: the balanced grid must
+    // be resident at once)
+    if (pl.cm > 0 && pl.groups * nvb <= device_sms()) {
+        auto kb = chain::chunk_chain_kernel<K, OT, true>;
+        cudaError_t e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int slots = pl.groups * nvb;
+        uint8_t* extra = reinterpret_cast<uint8_t*>(a.ws) + images_bytes(a.T, a.H, K, a.N, false);
+        cp.bal_cm = pl.cm;
+        cp.bal_nt = pl.nt;
+        cp.bal_flag = reinterpret_cast<unsigned*>(extra);
+        cp.bal_state = reinterpret_cast<float*>(extra + flag_bytes(slots));
+        e = cudaMemsetAsync(extra, 0, flag_bytes(slots), a.stream);
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(slots);
+        cfg.blockDim = dim3(chain::NTHR);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = a.stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kb, mv, cp);
+    }
+    auto kc = chain::chunk_chain_kernel<K, OT, false>;
     cudaError_t e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    chain::Params cp{a.h0, a.hT, a.cu, a.o, a.T, a.H, a.V, a.q_l2norm ? 1 : 0, cm, (const uint8_t*)a.ws,
-                     a.status, hook_stall_chunk()};
-    kc<<<dim3(a.V / 128, a.N, a.H), chain::NTHR, smem, a.stream>>>(mv, cp);
+    kc<<<dim3(nvb, a.N, a.H), chain::NTHR, smem, a.stream>>>(mv, cp);
     return cudaGetLastError();
 }
 template <int K>
@@ -1219,7 +1392,7 @@ cudaError_t launch_dims(const FwdArgs& a, const ChunkMap& cm, int slots) {
 cudaError_t launch_chunk_twopass(const FwdArgs& a) {
     const ChunkMap cm{a.cu, a.N, a.T, twopass::C};
     const int slots = cm.n_slots();
-    if (!a.ws || a.ws_bytes < twopass_workspace_bytes(a.T, a.H, a.K, a.N, a.cu != nullptr))
+    if (!a.ws || a.ws_bytes < twopass_workspace_bytes(a.T, a.H, a.K, a.V, a.N, a.cu != nullptr))
         return cudaErrorInvalidValue;
     return a.K == 256 ? launch_dims<256>(a, cm, slots) : launch_dims<128>(a, cm, slots);
 }

@@ -95,13 +95,16 @@ cudaError_t read_fused_timeouts(unsigned* count, bool reset);
 // and Aqk into the workspace, a chain pass per (sequence, head, 128 value channels) runs the state
 // scan; tcgen05 / TMEM / TMA throughout
 bool twopass_supported_dims(bool qkv_bf16, int K, int V, int mode, int H);
-size_t twopass_workspace_bytes(int T, int H, int K, int N, bool packed);
+// the images of pass 1, and for the balanced schedule of pass 2 its flags and state slots
+size_t twopass_workspace_bytes(int T, int H, int K, int V, int N, bool packed);
 cudaError_t launch_chunk_twopass(const FwdArgs& a);
 cudaError_t read_twopass_timeouts(unsigned* count, bool reset);
 // the fused path's test hooks (kda_test_hooks)
 void set_test_hooks(int stall_chunk, int sm_count, int one_launch, int two_pass_d128);
 bool hook_two_pass_d128();
 int hook_stall_chunk();  // the forced-give-up chunk of both tensor-core paths (-1: none)
+bool hook_one_launch();  // the plain grids whatever the plan (no split or balanced schedule)
+int planned_sm_count();  // the SM count the schedules are planned for (test hook, else device)
 
 // Which kernels run a chunked forward: the fused kernel (bf16, K = V = 128, every gate mode), the
 // two-pass tensor-core kernels (bf16, K in {128, 256} with V a multiple of 128 other than

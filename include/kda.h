@@ -163,7 +163,14 @@ int kda_chunk_fwd_launches(kda_dtype qkv_dtype, kda_dtype o_dtype, int B, int T,
  * and head that writes T diag(beta), Aqk and the state chain's operands into
  * the workspace, 121 KB per 64-token chunk and head at K = 256, then the state
  * chain per sequence, head and 128 value channels); every gate mode runs on
- * both.  Everything else runs the stage-by-stage path (six launches, a workspace),
+ * both.  Dense batches whose (sequence, head) units leave the state chain's last
+ * wave part-empty run the chain as one cooperative launch of one CTA per SM
+ * instead, the value blocks of a head on neighbouring SMs and the units' chunks
+ * shared out evenly; a unit cut between two groups of SMs passes its FP32 state
+ * through the workspace behind a flag (kda_chunk_workspace_bytes includes the
+ * flags and S K x 128 FP32 slots, about 19 MB at K = 256 on 152 SMs; the call
+ * zeroes the flags with cudaMemsetAsync on the stream).  The results are bitwise
+ * those of one CTA per unit.  Everything else runs the stage-by-stage path (six launches, a workspace),
  * which computes in FP32 except that with bf16 inputs the safe-gate scores, the
  * WY terms and the output are tf32 tensor-core products with FP32 accumulation.
  *
@@ -350,9 +357,12 @@ kda_status kda_fused_wait_timeouts(unsigned int* count, int reset);
  *                       nothing completes, and takes the give-up path (counted by
  *                       kda_fused_wait_timeouts, flagged in the status word of
  *                       kda_chunk_fwd_ex); -1: off
- *   sm_count            > 0: plan the split schedule (kda_chunk_fwd_launches) for this many
- *                       SMs instead of the device's; 0: the device's
- *   one_launch          nonzero: never split a fused call into two launches
+ *   sm_count            > 0: plan the fused split schedule (kda_chunk_fwd_launches) and the
+ *                       two-pass state chain's balanced schedule (kda_chunk_fwd) for this
+ *                       many SMs instead of the device's (a chain plan for more SMs than the
+ *                       device has runs one CTA per unit); 0: the device's
+ *   one_launch          nonzero: never split a fused call into two launches, and run the
+ *                       two-pass state chain as one CTA per unit
  *   two_pass_d128       nonzero: bf16 K = V = 128 calls run the two-pass kernels (with their
  *                       workspace, kda_chunk_workspace_bytes_ex) instead of the fused one
  * Always KDA_OK; no device work.

@@ -248,12 +248,16 @@ def test_workspace_bytes(lib):
         return 24576 + 3 * 64 * K * 2 + 4 * K + 256
 
     assert img(256) == 124160 and img(128) == 74496
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) == 4 * 64 * 64 * img(256)
-    assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 32, 0) == 4 * 64 * 64 * img(256)
+    lib.kda_test_hooks(-1, 0, 1, 0)  # one CTA per unit in pass 2 (no balanced schedule)
+    try:
+        assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 64, 0) == 4 * 64 * 64 * img(256)
+        assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 256, 256, 32, 0) == 4 * 64 * 64 * img(256)
+    finally:
+        lib.kda_test_hooks(-1, 0, 0, 0)
     # packed: floor(T_cap / 64) + N + 1 chunk slots
     assert lib.kda_chunk_workspace_bytes(BF16, 1, 20480, 32, 256, 256, 64, 16) == (320 + 17) * 32 * img(256)
     # the two-pass test hook moves K = V = 128 onto it
-    lib.kda_test_hooks(-1, 0, 0, 1)
+    lib.kda_test_hooks(-1, 0, 1, 1)
     try:
         assert lib.kda_chunk_workspace_bytes(BF16, 4, 4096, 64, 128, 128, 64, 0) == 4 * 64 * 64 * img(128)
         assert lib.kda_chunk_fwd_launches(BF16, BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 2
@@ -267,7 +271,7 @@ def test_workspace_bytes(lib):
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 0) == 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 1) == 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 2) == 0
-    assert ex(BF16, 4, 2048, 8, 256, 256, 64, 0, 2) == 4 * 32 * 8 * img(256)
+    assert ex(BF16, 4, 2048, 8, 256, 256, 64, 0, 2) == 4 * 32 * 8 * img(256)  # 32 units: one wave
     assert ex(F32, 4, 2048, 8, 256, 256, 64, 0, 2) == lib.kda_chunk_workspace_bytes(
         F32, 4, 2048, 8, 256, 256, 64, 0) > 0
     assert ex(BF16, 4, 4096, 64, 128, 128, 64, 0, 3) == 0  # no such mode
@@ -301,6 +305,39 @@ def test_split_schedule_plan(lib):
     lib.kda_test_hooks(-1, 152, 1, 0)  # one launch whatever the plan
     assert f(BF16, BF16, 2, 720, 114, 128, 128, 64, 0, SAFE) == 1
     lib.kda_test_hooks(-1, 0, 0, 0)  # hooks off again
+
+
+def test_two_pass_balanced_plan(lib):
+    """Pass 2's balanced schedule, on a stated SM count S (no device needed): dense inputs whose
+    N H units leave the last wave of a one-CTA-per-unit grid part-empty on S / (V / 128) groups
+    of SMs, where ceil(U nt / groups) + 2 chunk-times beat it by 5 % or more.  It adds one flag
+    per CTA (rounded to 256 bytes) and one FP32 K x 128 state slot per CTA to the workspace; the
+    call still makes two launches."""
+    img = 124160  # K = 256 image bytes per chunk and head
+
+    def ws(B, T, H, V=256, S=152, mode=1, n=0):
+        lib.kda_test_hooks(-1, S, 0, 0)
+        assert lib.kda_chunk_fwd_launches(BF16, BF16, B, T, H, 256, V, 64, n, mode) == 2
+        return lib.kda_chunk_workspace_bytes_ex(BF16, B, T, H, 256, V, 64, n, mode)
+
+    def bal(S, V=256):
+        slots = S // (V // 128) * (V // 128)
+        return (slots * 4 + 255) // 256 * 256 + slots * 256 * 128 * 4
+
+    try:
+        base = 8 * 32 * 32 * img
+        assert ws(8, 2048, 32) == base + bal(152)          # 256 units on 76 groups: 108 against 128
+        assert ws(8, 2048, 32, mode=2) == base + bal(152)  # the non-safe gate too
+        assert ws(8, 2048, 32, S=151) == base + bal(151)   # 75 groups of two
+        assert ws(4, 1000, 40) == 4 * 16 * 40 * img + bal(152)
+        assert ws(2, 2048, 38) == 2 * 32 * 38 * img        # 76 units: one whole wave
+        assert ws(1, 2048, 60) == 32 * 60 * img            # fewer units than groups
+        assert ws(4, 2048, 57) == 4 * 32 * 57 * img        # 228 units = 3 waves
+        assert ws(1, 20480, 32, n=3) == (320 + 4) * 32 * img  # packed: never
+        lib.kda_test_hooks(-1, 152, 1, 0)  # one CTA per unit whatever the plan
+        assert lib.kda_chunk_workspace_bytes(BF16, 8, 2048, 32, 256, 256, 64, 0) == base
+    finally:
+        lib.kda_test_hooks(-1, 0, 0, 0)
 
 
 def test_no_environment_hooks():

@@ -221,3 +221,106 @@ def test_two_pass_no_initial_state_and_in_place_state():
                                 w2.mode, w2.lower_bound, S, True, None, 64, final_state=S)
     torch.cuda.synchronize()
     assert torch.equal(oa, ob) and torch.equal(sa, S)
+
+
+# ---- the balanced schedule of pass 2 (dense inputs whose (sequence, head) units leave the last
+# wave of a one-CTA-per-unit grid part-empty): one cooperative launch, the value blocks of a head
+# on a group of CTAs side by side, each group running an equal share of the units' chunks laid
+# end to end; a unit cut at a group boundary runs its first chunks on one group and the rest on
+# the previous one, the FP32 state crossing through the workspace behind a flag.  The chunks are
+# computed from the FP32 state and their images alone, so the two schedules agree bitwise.
+
+def _chain_cuts(N, H, T, groups):
+    """Chunk-times per group and, per cut unit u = n + N h, the chunks of its first part (the
+    library's plan restated: boundaries at multiples of ceil(U nt / groups))."""
+    import math
+
+    nt, U = math.ceil(T / 64), N * H
+    cm = math.ceil(U * nt / groups)
+    cuts = {}
+    for i in range(1, groups):
+        b = i * cm
+        if b < U * nt and b % nt:
+            cuts[b // nt] = (b // nt + 1) * nt - b
+    return cm, cuts
+
+
+def _balanced_shape():
+    """About 2.1 waves of (sequence, head) units of 16 chunks on the device's groups of two SMs
+    (160 units on 76 groups of a 152-SM GB300)."""
+    S = torch.cuda.get_device_properties(0).multi_processor_count
+    return 4, max(1, round(2.1 * (S // 2) / 4)), S // 2
+
+
+def _ws(w):
+    return kda().kda_chunk_workspace_bytes(w.q.dtype, w.B, w.T, w.H, w.K, w.V, w.chunk_size, 0, w.mode)
+
+
+@pytest.mark.parametrize("mode,o_dtype,state", [
+    (workloads.GATE_SAFE, None, True),
+    (workloads.GATE_NONSAFE, None, False),
+    (workloads.GATE_PRE, torch.float32, True),
+], ids=["safe-bf16o-state", "nonsafe-bf16o", "pre-f32o-state"])
+def test_two_pass_balanced_chain_equals_plain_grid(mode, o_dtype, state):
+    from parity import check_units
+
+    B, H, groups = _balanced_shape()
+    T = 1000  # 16 chunks, the last one ragged
+    w = workloads.make_dense("t", B, T, H, 256, 256, 64, torch.bfloat16, 950 + mode,
+                             state_std=0.05 if state else None, mode=mode,
+                             g_std=2.0 if mode == workloads.GATE_NONSAFE else 1.0)
+    cm, cuts = _chain_cuts(B, H, T, groups)
+    assert cuts and min(cuts.values()) >= 1 and max(cuts.values()) < 16
+    ws_bal = _ws(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda().kda_fused_wait_timeouts(reset=True)
+    o1, s1 = run_gpu(w, o_dtype=o_dtype, status=status)
+    assert int(status.item()) == 0 and kda().kda_fused_wait_timeouts() == 0
+    kda().kda_test_hooks(one_launch=True)  # one CTA per (value block, sequence, head)
+    try:
+        assert _ws(w) < ws_bal, "the balanced schedule applies to these sizes"
+        o2, s2 = run_gpu(w, o_dtype=o_dtype)
+    finally:
+        kda().kda_test_hooks()
+    assert torch.equal(o1, o2)
+    assert torch.equal(s1, s2)
+    U = B * H
+    pick = {0, U - 1, min(cuts), min(cuts, key=lambda u: cuts[u]), max(cuts, key=lambda u: cuts[u])}
+    check_units(w, o1, s1, sorted({(u % B, u // B) for u in pick}))
+
+
+def test_two_pass_balanced_chain_in_a_cuda_graph():
+    """The flag reset and the cooperative launch are captured; a replay with new inputs written
+    in place matches an eager call bitwise."""
+    B, H, _ = _balanced_shape()
+    ws = [workloads.make_dense("t", B, 1000, H, 256, 256, 64, torch.bfloat16, 960 + i, state_std=0.05)
+          for i in range(2)]
+    t = to_device(ws[0])
+    S0, S_fin = t["initial_state"].clone(), torch.empty_like(t["initial_state"])
+    o = torch.empty((B, 1000, H, 256), device="cuda", dtype=torch.bfloat16)
+    work = torch.empty(_ws(ws[0]), device="cuda", dtype=torch.uint8)
+
+    def call():
+        kda().kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["A_log"], t["dt_bias"],
+                            ws[0].mode, ws[0].lower_bound, S0, True, None, 64, o=o,
+                            final_state=S_fin, workspace=work)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    for w in ws[::-1]:
+        src = to_device(w)
+        for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias"):
+            t[name].copy_(src[name])
+        S0.copy_(src["initial_state"])
+        graph.replay()
+        torch.cuda.synchronize()
+        o_g, s_g = o.clone(), S_fin.clone()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o) and torch.equal(s_g, S_fin)
