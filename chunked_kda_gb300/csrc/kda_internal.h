@@ -82,7 +82,8 @@ cudaError_t launch_recurrent(const RecArgs& a);
 size_t precise_workspace_bytes(int B, int T, int H, int K, int V, int C, int N, bool packed);
 cudaError_t launch_chunk_precise(const FwdArgs& a);
 
-// bf16 fused single-kernel path (tcgen05 / TMEM / TMA); needs no workspace
+// bf16 fused single-kernel path (tcgen05 / TMEM / TMA); needs no workspace (its split schedule
+// hands the state over in the unit's own output rows)
 bool fused_supported(const FwdArgs& a);
 bool fused_supported_dims(bool qkv_bf16, int K, int V, int C, int mode);
 cudaError_t launch_chunk_fused(const FwdArgs& a);
