@@ -1259,12 +1259,13 @@ ChainPlan chain_plan(int T, int H, int V, int N, bool packed) {
     ChainPlan pl{0, 0, 0};
     const int nvb = V / 128;
     if (packed || hook_one_launch() || nvb <= 0) return pl;
-    const int M = planned_sm_count() / nvb, U = N * H;
+    const int M = planned_sm_count() / nvb;
+    const long U = (long)N * H;  // the kernel indexes units with an int
     const long nt = (T + twopass::C - 1) / twopass::C;
-    if (M <= 0 || U <= M || U % M == 0 || nt <= 0) return pl;
-    const long cm = ((long)U * nt + M - 1) / M;
+    if (M <= 0 || U <= M || U % M == 0 || nt <= 0 || U > 0x7fffffffL) return pl;
+    const long cm = (U * nt + M - 1) / M;
     const long f = U / M;
-    if (20L * (cm + 2) > 19L * (f + 1) * nt) return pl;
+    if (20L * (cm + 2) > 19L * (f + 1) * nt || cm > 0x7fffffffL) return pl;
     pl.cm = (int)cm;
     pl.nt = (int)nt;
     pl.groups = M;
